@@ -1,0 +1,236 @@
+"""fp64 CPU oracle for Kimi Delta Attention -- test infrastructure only.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline arm
+may import this package. It shares no code with the CUDA library: the arithmetic
+is the plain token-by-token loop in ``kda_oracle.c`` (see its header for the
+definition and the passages it follows), loaded here through ctypes.
+
+Inputs are torch CPU tensors in their stored dtype (bf16 or fp32); the C code
+widens them exactly to double. Outputs are float64 numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+from typing import Iterable, Optional
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "kda_oracle.c")
+LIB = os.path.join(HERE, "libkda_oracle.so")
+EPS = 1e-6
+
+
+class Task(C.Structure):
+    _fields_ = [
+        ("T", C.c_int64), ("dk", C.c_int32), ("dv", C.c_int32), ("io_bf16", C.c_int32),
+        ("scale", C.c_double), ("eps", C.c_double),
+        ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p), ("dO", C.c_void_p),
+        ("sq", C.c_int64), ("sk", C.c_int64), ("sv", C.c_int64), ("sdo", C.c_int64),
+        ("beta", C.c_void_p), ("sbeta", C.c_int64),
+        ("g", C.c_void_p), ("sg", C.c_int64),
+        ("h0", C.c_void_p), ("dhT", C.c_void_p),
+        ("accept", C.c_int64),
+        ("so", C.c_int64), ("sb", C.c_int64),
+        ("o", C.c_void_p), ("hT", C.c_void_p),
+        ("dq", C.c_void_p), ("dk_", C.c_void_p), ("dv_", C.c_void_p), ("dg", C.c_void_p),
+        ("dbeta", C.c_void_p), ("dh0", C.c_void_p),
+    ]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP). Returns the library path."""
+    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+        tmp = LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", tmp, SRC, "-lm"])
+        os.replace(tmp, LIB)
+    return LIB
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load the oracle library (default: build and load ``libkda_oracle.so``).
+
+    The mutation tests pass the path of a deliberately broken copy to check
+    that the pins catch it; ``load()`` switches back to the real one.
+    """
+    global _lib
+    if path is None:
+        path = build()
+    handle = C.CDLL(path)
+    for fn in ("kda_oracle_fwd", "kda_oracle_bwd", "kda_oracle_step"):
+        getattr(handle, fn).argtypes = [C.POINTER(Task), C.c_int, C.c_int]
+        getattr(handle, fn).restype = None
+    _lib = handle
+    return handle
+
+
+def lib():
+    return _lib if _lib is not None else load()
+
+
+def default_threads() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def _host(t: Optional[torch.Tensor]):
+    """A contiguous CPU view of an input, keeping bf16 bit patterns as int16."""
+    if t is None:
+        return None, False
+    t = t.detach().to("cpu").contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16), True
+    if t.dtype != torch.float32:
+        t = t.to(torch.float32)
+    return t, False
+
+
+def _ptr(t: Optional[torch.Tensor], offset_elems: int = 0):
+    if t is None:
+        return None
+    return t.data_ptr() + offset_elems * t.element_size()
+
+
+class _Prepared:
+    def __init__(self, q, k, v, beta, g, cu_seqlens, h0, dO, dhT):
+        self.q, bf = _host(q)
+        self.k, _ = _host(k)
+        self.v, _ = _host(v)
+        self.dO, _ = _host(dO)
+        self.bf16 = bf
+        self.beta, _ = _host(beta)
+        self.g, _ = _host(g)
+        self.h0, _ = _host(h0)
+        self.dhT, _ = _host(dhT)
+        self.cu = [int(x) for x in cu_seqlens.to("cpu").tolist()]
+        self.H = self.q.shape[1]
+        self.dk = self.q.shape[2]
+        self.dv = self.v.shape[2]
+
+
+def _task(P: _Prepared, i: int, h: int, scale: float, eps: float) -> Task:
+    t0, t1 = P.cu[i], P.cu[i + 1]
+    H, dk, dv = P.H, P.dk, P.dv
+    st = Task()
+    st.T = t1 - t0
+    st.dk, st.dv, st.io_bf16 = dk, dv, int(P.bf16)
+    st.scale, st.eps = scale, eps
+    st.q = _ptr(P.q, (t0 * H + h) * dk)
+    st.k = _ptr(P.k, (t0 * H + h) * dk)
+    st.v = _ptr(P.v, (t0 * H + h) * dv)
+    st.dO = _ptr(P.dO, (t0 * H + h) * dv) if P.dO is not None else None
+    st.sq = st.sk = H * dk
+    st.sv = st.sdo = H * dv
+    st.beta = _ptr(P.beta, t0 * H + h)
+    st.sbeta = H
+    st.g = _ptr(P.g, (t0 * H + h) * dk)
+    st.sg = H * dk
+    st.h0 = _ptr(P.h0, (i * H + h) * dk * dv) if P.h0 is not None else None
+    st.dhT = _ptr(P.dhT, (i * H + h) * dk * dv) if P.dhT is not None else None
+    return st
+
+
+def _all_tasks(P: _Prepared):
+    return [(i, h) for i in range(len(P.cu) - 1) for h in range(P.H)]
+
+
+def fwd(q, k, v, beta, g, cu_seqlens, h0=None, *, scale: float = 1.0, eps: float = EPS,
+        tasks: Optional[Iterable] = None, n_threads: int = 0):
+    """Forward for the given (sequence, head) tasks (default: all).
+
+    Returns ``{(i, h): (o [T_i, dv], hT [dk, dv])}`` as float64 arrays.
+    """
+    P = _Prepared(q, k, v, beta, g, cu_seqlens, h0, None, None)
+    tasks = list(tasks) if tasks is not None else _all_tasks(P)
+    arr = (Task * max(1, len(tasks)))()
+    out = {}
+    for n, (i, h) in enumerate(tasks):
+        st = _task(P, i, h, scale, eps)
+        o = np.zeros((st.T, P.dv), np.float64)
+        hT = np.zeros((P.dk, P.dv), np.float64)
+        st.o, st.hT, st.so = o.ctypes.data, hT.ctypes.data, P.dv
+        arr[n] = st
+        out[(i, h)] = (o, hT)
+    lib().kda_oracle_fwd(arr, len(tasks), n_threads or default_threads())
+    return out
+
+
+def bwd(q, k, v, beta, g, cu_seqlens, dO, h0=None, dhT=None, *, scale: float = 1.0,
+        eps: float = EPS, tasks: Optional[Iterable] = None, n_threads: int = 0):
+    """Backward for the given tasks. Returns ``{(i, h): dict(dq, dk, dv, dg, dbeta, dh0)}``."""
+    P = _Prepared(q, k, v, beta, g, cu_seqlens, h0, dO, dhT)
+    tasks = list(tasks) if tasks is not None else _all_tasks(P)
+    arr = (Task * max(1, len(tasks)))()
+    out = {}
+    for n, (i, h) in enumerate(tasks):
+        st = _task(P, i, h, scale, eps)
+        r = {"dq": np.zeros((st.T, P.dk)), "dk": np.zeros((st.T, P.dk)),
+             "dv": np.zeros((st.T, P.dv)), "dg": np.zeros((st.T, P.dk)),
+             "dbeta": np.zeros(st.T), "dh0": np.zeros((P.dk, P.dv))}
+        st.so, st.sb = P.dk, 1
+        st.dq, st.dk_, st.dv_ = r["dq"].ctypes.data, r["dk"].ctypes.data, r["dv"].ctypes.data
+        st.dg, st.dbeta, st.dh0 = r["dg"].ctypes.data, r["dbeta"].ctypes.data, r["dh0"].ctypes.data
+        arr[n] = st
+        out[(i, h)] = r
+    lib().kda_oracle_bwd(arr, len(tasks), n_threads or default_threads())
+    return out
+
+
+def step(q, k, v, beta, g, state, accept_len, *, scale: float = 1.0, eps: float = EPS,
+         tasks: Optional[Iterable] = None, n_threads: int = 0):
+    """Decode / draft-verify over L tokens per sequence.
+
+    q, k, v, g: [N, L, H, d]; beta: [N, L, H]; state: [N, H, dk, dv]; accept_len: [N].
+    Returns ``{(i, h): (o [L, dv], committed state [dk, dv])}``.
+    """
+    N, L, H, dk = q.shape
+    flat = lambda t: t.reshape(N * L, *t.shape[2:])
+    cu = torch.arange(0, N * L + 1, L, dtype=torch.int64)
+    P = _Prepared(flat(q), flat(k), flat(v), flat(beta), flat(g), cu, state, None, None)
+    acc = [int(a) for a in accept_len.to("cpu").tolist()]
+    tasks = list(tasks) if tasks is not None else _all_tasks(P)
+    arr = (Task * max(1, len(tasks)))()
+    out = {}
+    for n, (i, h) in enumerate(tasks):
+        st = _task(P, i, h, scale, eps)
+        st.accept = acc[i]
+        o = np.zeros((st.T, P.dv), np.float64)
+        hT = np.zeros((P.dk, P.dv), np.float64)
+        st.o, st.hT, st.so = o.ctypes.data, hT.ctypes.data, P.dv
+        arr[n] = st
+        out[(i, h)] = (o, hT)
+    lib().kda_oracle_step(arr, len(tasks), n_threads or default_threads())
+    return out
+
+
+def assemble_fwd(res: dict, cu_seqlens, H: int, dv: int):
+    """Stack per-task forward results into o [total, H, dv] and hT [N, H, dk, dv]."""
+    cu = [int(x) for x in cu_seqlens.to("cpu").tolist()]
+    N = len(cu) - 1
+    dk = next(iter(res.values()))[1].shape[0]
+    o = np.zeros((cu[-1], H, dv))
+    hT = np.zeros((N, H, dk, dv))
+    for (i, h), (oi, hi) in res.items():
+        o[cu[i]:cu[i + 1], h] = oi
+        hT[i, h] = hi
+    return o, hT
+
+
+def assemble_bwd(res: dict, cu_seqlens, H: int):
+    cu = [int(x) for x in cu_seqlens.to("cpu").tolist()]
+    N = len(cu) - 1
+    any_r = next(iter(res.values()))
+    dk, dv = any_r["dq"].shape[1], any_r["dv"].shape[1]
+    out = {"dq": np.zeros((cu[-1], H, dk)), "dk": np.zeros((cu[-1], H, dk)),
+           "dv": np.zeros((cu[-1], H, dv)), "dg": np.zeros((cu[-1], H, dk)),
+           "dbeta": np.zeros((cu[-1], H)), "dh0": np.zeros((N, H, dk, dv))}
+    for (i, h), r in res.items():
+        for name in ("dq", "dk", "dv", "dg", "dbeta"):
+            out[name][cu[i]:cu[i + 1], h] = r[name]
+        out["dh0"][i, h] = r["dh0"]
+    return out

@@ -1,0 +1,174 @@
+"""GB300-native Kimi Delta Attention (KDA): chunked forward, backward and decode.
+
+Python face of libkda.so (include/kda.h). Every step of the computation runs in
+the library's CUDA kernels; this module only allocates outputs and workspaces
+with PyTorch, passes raw device pointers and the current CUDA stream through
+ctypes, and turns status codes into exceptions.
+
+    o, hT, saved = kda_fwd(q, k, v, beta, g, cu_seqlens, h0, save=True)
+    grads = kda_bwd(q, k, v, beta, g, dO, saved, cu_seqlens, h0, dhT)
+    o = kda_step(q, k, v, beta, g, state, accept_len)     # state updated in place
+
+Shapes: q, k, v, g, dO [total, H, 128]; beta [total, H]; states [N, H, 128, 128]
+(fp32, [key][value]); decode inputs carry an extra step axis: [N, L, H, ...].
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import KdaError
+
+__all__ = ["kda_fwd", "kda_bwd", "kda_step", "fwd_args", "bwd_args", "KdaError", "library"]
+
+
+def library():
+    """The loaded libkda.so handle (raises if it was not built)."""
+    return _lib.load()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _io_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.KDA_BF16
+    if t.dtype == torch.float32:
+        return _lib.KDA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check_inputs(q, k, v, beta, g):
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if beta.dtype != torch.float32 or g.dtype != torch.float32:
+        raise TypeError("beta and g must be float32")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+
+
+def fwd_args(q, k, v, beta, g, cu_seqlens=None, h0=None, o=None, hT=None, saved=None,
+             workspace=None, scale: float = 1.0, n_seqs: Optional[int] = None, dev_status=None) -> _lib.FwdArgs:
+    """Fill the C argument struct for kda_fwd from tensors (no allocation)."""
+    a = _lib.FwdArgs()
+    total, H, dk = q.shape
+    a.n_seqs = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (n_seqs or 1)
+    a.total_tokens, a.heads, a.dk, a.dv, a.chunk = total, H, dk, v.shape[2], 64
+    a.scale, a.io_dtype = scale, _io_dtype(q)
+    a.cu_seqlens = _ptr(cu_seqlens)
+    a.q, a.k, a.v, a.beta, a.g = _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g)
+    a.h0, a.o, a.hT, a.saved = _ptr(h0), _ptr(o), _ptr(hT), _ptr(saved)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    a.dev_status = _ptr(dev_status)
+    return a
+
+
+def bwd_args(fa: _lib.FwdArgs, dO, dq, dk, dv, dbeta, dg, dh0=None, dhT=None, workspace=None) -> _lib.BwdArgs:
+    b = _lib.BwdArgs()
+    b.fwd = fa
+    b.dO, b.dhT = _ptr(dO), _ptr(dhT)
+    b.dq, b.dk, b.dv, b.dbeta, b.dg, b.dh0 = _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg), _ptr(dh0)
+    b.workspace = _ptr(workspace)
+    b.workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return b
+
+
+def _i32(cu_seqlens, device):
+    if cu_seqlens is None:
+        return None
+    return cu_seqlens.to(device=device, dtype=torch.int32).contiguous()
+
+
+def kda_fwd(q, k, v, beta, g, cu_seqlens=None, h0=None, *, scale: float = 1.0, save: bool = False,
+            final_state: bool = True, n_seqs: Optional[int] = None):
+    """Chunked KDA forward. Returns (o, hT or None, saved or None).
+
+    ``saved`` (chunk-start states) is what kda_bwd needs; request it with save=True.
+    Without cu_seqlens the tokens form ``n_seqs`` (default 1) equal sequences.
+    """
+    lib = library()
+    _check_inputs(q, k, v, beta, g)
+    dev = q.device
+    cu = _i32(cu_seqlens, dev)
+    N = (cu.numel() - 1) if cu is not None else (n_seqs or 1)
+    H = q.shape[1]
+    o = torch.empty_like(v)
+    hT = torch.empty((N, H, 128, 128), dtype=torch.float32, device=dev) if final_state else None
+    a = fwd_args(q, k, v, beta, g, cu, h0, o, hT, None, None, scale, n_seqs=N)
+    saved = None
+    if save:
+        saved = torch.empty(lib.kda_saved_size(C.byref(a)), dtype=torch.uint8, device=dev)
+        a.saved = saved.data_ptr()
+    ws_bytes = lib.kda_fwd_workspace_size(C.byref(a))
+    if ws_bytes == 0:
+        _lib.check(lib.kda_fwd(C.byref(a), _stream(dev)))   # reports the argument error
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws_bytes
+    _lib.check(lib.kda_fwd(C.byref(a), _stream(dev)))
+    return o, hT, saved
+
+
+def kda_bwd(q, k, v, beta, g, dO, saved, cu_seqlens=None, h0=None, dhT=None, *, scale: float = 1.0,
+            n_seqs: Optional[int] = None, initial_state_grad: bool = True):
+    """Backward of kda_fwd (``saved`` from kda_fwd(..., save=True) with the same inputs).
+
+    Returns a dict of fp32 gradients: dq, dk, dv, dbeta, dg and dh0 (or None).
+    """
+    lib = library()
+    _check_inputs(q, k, v, beta, g)
+    dev = q.device
+    cu = _i32(cu_seqlens, dev)
+    N = (cu.numel() - 1) if cu is not None else (n_seqs or 1)
+    H = q.shape[1]
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty(q.shape, **f32), torch.empty(k.shape, **f32), torch.empty(v.shape, **f32)
+    dg, dbeta = torch.empty(g.shape, **f32), torch.empty(beta.shape, **f32)
+    dh0 = torch.empty((N, H, 128, 128), **f32) if initial_state_grad else None
+    fa = fwd_args(q, k, v, beta, g, cu, h0, None, None, saved, None, scale, n_seqs=N)
+    b = bwd_args(fa, dO, dq, dk, dv, dbeta, dg, dh0, dhT)
+    ws_bytes = lib.kda_bwd_workspace_size(C.byref(b))
+    if ws_bytes == 0:
+        _lib.check(lib.kda_bwd(C.byref(b), _stream(dev)))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    b.workspace, b.workspace_bytes = ws.data_ptr(), ws_bytes
+    _lib.check(lib.kda_bwd(C.byref(b), _stream(dev)))
+    return {"dq": dq, "dk": dk, "dv": dv, "dbeta": dbeta, "dg": dg, "dh0": dh0}
+
+
+def step_args(q, k, v, beta, g, state, accept_len, o, scale: float = 1.0) -> _lib.StepArgs:
+    a = _lib.StepArgs()
+    N, L, H, dk = q.shape
+    a.n_seqs, a.steps, a.heads, a.dk, a.dv = N, L, H, dk, v.shape[3]
+    a.scale, a.io_dtype = scale, _io_dtype(q)
+    a.q, a.k, a.v, a.beta, a.g = _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g)
+    a.state, a.accept_len, a.o = _ptr(state), _ptr(accept_len), _ptr(o)
+    return a
+
+
+def kda_step(q, k, v, beta, g, state, accept_len=None, *, scale: float = 1.0, out=None):
+    """Decode / draft-verify L tokens per sequence; returns o [N, L, H, 128].
+
+    ``state`` [N, H, 128, 128] fp32 is overwritten with the state after
+    ``accept_len[i]`` tokens (left untouched where accept_len is 0; all L when None).
+    """
+    lib = library()
+    _check_inputs(q, k, v, beta, g)
+    if state.dtype != torch.float32 or not state.is_contiguous():
+        raise TypeError("state must be a contiguous float32 tensor")
+    acc = None if accept_len is None else accept_len.to(device=q.device, dtype=torch.int32).contiguous()
+    o = torch.empty_like(v) if out is None else out
+    a = step_args(q, k, v, beta, g, state, acc, o, scale)
+    _lib.check(lib.kda_step(C.byref(a), _stream(q.device)))
+    return o

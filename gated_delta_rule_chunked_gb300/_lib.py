@@ -1,0 +1,94 @@
+"""ctypes view of the C ABI in include/kda.h (argument marshalling only).
+
+Loading fails loudly when libkda.so has not been built: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkda.so")
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(5)
+KDA_BF16, KDA_F32 = 0, 1
+STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
+                4: "KDA_ERR_TIMEOUT"}
+ABI_VERSION = 1
+
+# every symbol include/kda.h declares
+EXPORTS = ("kda_fwd", "kda_fwd_workspace_size", "kda_saved_size", "kda_bwd", "kda_bwd_workspace_size",
+           "kda_step", "kda_last_error", "kda_abi_version")
+
+
+class FwdArgs(C.Structure):
+    _fields_ = [
+        ("n_seqs", C.c_int32), ("total_tokens", C.c_int64), ("heads", C.c_int32),
+        ("dk", C.c_int32), ("dv", C.c_int32), ("chunk", C.c_int32), ("scale", C.c_float),
+        ("io_dtype", C.c_int32), ("cu_seqlens", C.c_void_p),
+        ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p), ("beta", C.c_void_p), ("g", C.c_void_p),
+        ("h0", C.c_void_p), ("o", C.c_void_p), ("hT", C.c_void_p), ("saved", C.c_void_p),
+        ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("dev_status", C.c_void_p),
+    ]
+
+
+class BwdArgs(C.Structure):
+    _fields_ = [
+        ("fwd", FwdArgs), ("dO", C.c_void_p), ("dhT", C.c_void_p),
+        ("dq", C.c_void_p), ("dk", C.c_void_p), ("dv", C.c_void_p), ("dbeta", C.c_void_p), ("dg", C.c_void_p),
+        ("dh0", C.c_void_p), ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
+    ]
+
+
+class StepArgs(C.Structure):
+    _fields_ = [
+        ("n_seqs", C.c_int32), ("steps", C.c_int32), ("heads", C.c_int32), ("dk", C.c_int32), ("dv", C.c_int32),
+        ("scale", C.c_float), ("io_dtype", C.c_int32),
+        ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p), ("beta", C.c_void_p), ("g", C.c_void_p),
+        ("state", C.c_void_p), ("accept_len", C.c_void_p), ("o", C.c_void_p),
+    ]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libkda.so (once). Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+                          "or `python gated_delta_rule_chunked_gb300/build.py` (no CPU fallback exists)")
+    lib = C.CDLL(path)
+    lib.kda_fwd.argtypes = [C.POINTER(FwdArgs), C.c_void_p]
+    lib.kda_fwd.restype = C.c_int
+    lib.kda_bwd.argtypes = [C.POINTER(BwdArgs), C.c_void_p]
+    lib.kda_bwd.restype = C.c_int
+    lib.kda_step.argtypes = [C.POINTER(StepArgs), C.c_void_p]
+    lib.kda_step.restype = C.c_int
+    lib.kda_fwd_workspace_size.argtypes = [C.POINTER(FwdArgs)]
+    lib.kda_fwd_workspace_size.restype = C.c_size_t
+    lib.kda_saved_size.argtypes = [C.POINTER(FwdArgs)]
+    lib.kda_saved_size.restype = C.c_size_t
+    lib.kda_bwd_workspace_size.argtypes = [C.POINTER(BwdArgs)]
+    lib.kda_bwd_workspace_size.restype = C.c_size_t
+    lib.kda_last_error.argtypes = []
+    lib.kda_last_error.restype = C.c_char_p
+    lib.kda_abi_version.argtypes = []
+    lib.kda_abi_version.restype = C.c_int32
+    if lib.kda_abi_version() != ABI_VERSION:
+        raise ImportError(f"libkda.so ABI {lib.kda_abi_version()} != binding ABI {ABI_VERSION}; rebuild")
+    _lib = lib
+    return lib
+
+
+def check(status: int):
+    if status != KDA_OK:
+        raise KdaError(status, load().kda_last_error().decode())

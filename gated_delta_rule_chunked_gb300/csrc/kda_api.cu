@@ -1,0 +1,258 @@
+// kda_api.cu -- the extern "C" entry points of libkda.so (see include/kda.h).
+//
+// Validates every argument before anything is enqueued, carves the caller's
+// workspace, and launches the kernels on the caller's stream:
+//   kda_fwd:  chunk table -> chunk prep (parallel over chunks x heads)
+//             -> forward state scan (sequences x heads x value slices)
+//   kda_bwd:  chunk table -> chunk prep -> reverse dS scan
+//             -> state-side gradients -> intra-chunk gradients
+//   kda_step: one decode kernel.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kda_status fail(kda_status s, const char *fmt, const char *what = "") {
+  char buf[512];
+  std::snprintf(buf, sizeof buf, fmt, what);
+  g_last_error = buf;
+  return s;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+long long max_chunks(const kda_fwd_args *a) {
+  return a->total_tokens / 64 + (long long)a->n_seqs;
+}
+
+size_t elem_size(int io) { return io == KDA_F32 ? 4 : 2; }
+
+// Workspace carving shared by the forward and the backward.
+struct WsPlan {
+  size_t cu, choff, img, dsaved, grad, bytes;
+};
+
+WsPlan plan(const kda_fwd_args *a, bool bwd) {
+  WsPlan w{};
+  const size_t n1 = (size_t)a->n_seqs + 1;
+  const size_t mc = (size_t)max_chunks(a), H = (size_t)a->heads;
+  const kda::ImgLayout L((int)elem_size(a->io_dtype));
+  w.cu = 0;
+  w.choff = round_up(w.cu + n1 * 4, 256);
+  w.img = round_up(w.choff + n1 * 4, 256);
+  size_t end = w.img + mc * H * L.bytes;
+  if (bwd) {
+    w.dsaved = round_up(end, 256);
+    end = w.dsaved + mc * H * 128 * 128 * elem_size(a->io_dtype);
+    w.grad = round_up(end, 256);
+    end = w.grad + mc * H * kda::GradLayout::bytes;
+  }
+  w.bytes = round_up(end, 256);
+  return w;
+}
+
+kda_status check_fwd(const kda_fwd_args *a, const char *who) {
+  if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", who);
+  if (a->dk != 128 || a->dv != 128 || a->chunk != 64)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: only dk = dv = 128 and chunk = 64 are supported", who);
+  if (a->io_dtype != KDA_BF16 && a->io_dtype != KDA_F32)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: io_dtype must be KDA_BF16 or KDA_F32", who);
+  if (a->n_seqs < 1 || a->heads < 1 || a->total_tokens < 0 || a->total_tokens > 0x7fffffffLL)
+    return fail(KDA_ERR_INVALID_ARG, "%s: need n_seqs >= 1, heads >= 1, 0 <= total_tokens < 2^31", who);
+  if (!a->cu_seqlens && a->total_tokens % a->n_seqs != 0)
+    return fail(KDA_ERR_INVALID_ARG, "%s: without cu_seqlens total_tokens must be a multiple of n_seqs", who);
+  if (a->cu_seqlens && !aligned(a->cu_seqlens, 4))
+    return fail(KDA_ERR_INVALID_ARG, "%s: cu_seqlens must be 4-byte aligned", who);
+  const void *need[] = {a->q, a->k, a->v, a->g, a->o};
+  const char *names[] = {"q", "k", "v", "g", "o"};
+  for (int i = 0; i < 5; ++i) {
+    if (!need[i] && a->total_tokens > 0) return fail(KDA_ERR_INVALID_ARG, "%s: required pointer is NULL", names[i]);
+    if (!aligned(need[i], 16)) return fail(KDA_ERR_INVALID_ARG, "%s: pointer is not 16-byte aligned", names[i]);
+  }
+  if (!a->beta && a->total_tokens > 0) return fail(KDA_ERR_INVALID_ARG, "%s: beta is NULL", who);
+  if (!aligned(a->beta, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: beta is not 4-byte aligned", who);
+  const void *opt[] = {a->h0, a->hT, a->saved, a->workspace};
+  const char *onames[] = {"h0", "hT", "saved", "workspace"};
+  for (int i = 0; i < 4; ++i)
+    if (!aligned(opt[i], 16)) return fail(KDA_ERR_INVALID_ARG, "%s: pointer is not 16-byte aligned", onames[i]);
+  if (a->dev_status && !aligned(a->dev_status, 4))
+    return fail(KDA_ERR_INVALID_ARG, "%s: dev_status is not 4-byte aligned", who);
+  return KDA_OK;
+}
+
+kda::SeqGeom geom(const kda_fwd_args *a, char *ws, const WsPlan &w) {
+  kda::SeqGeom g;
+  g.n_seqs = a->n_seqs;
+  g.total = a->total_tokens;
+  g.heads = a->heads;
+  g.max_chunks = (int)max_chunks(a);
+  g.cu = reinterpret_cast<const int *>(ws + w.cu);
+  g.chunk_off = reinterpret_cast<const int *>(ws + w.choff);
+  return g;
+}
+
+kda_status cuda_fail(cudaError_t e, const char *stage) {
+  char buf[256];
+  std::snprintf(buf, sizeof buf, "%s: %s", stage, cudaGetErrorString(e));
+  g_last_error = buf;
+  return KDA_ERR_CUDA;
+}
+
+int pick_slice(const kda_fwd_args *a) {
+  // value-column slice per scan CTA: enough chains to cover the GPU twice
+  const long long units = (long long)a->n_seqs * a->heads;
+  return units * 2 >= 2LL * sm_count() ? 64 : 32;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kda_abi_version(void) { return 1; }
+
+const char *kda_last_error(void) { return g_last_error.c_str(); }
+
+size_t kda_fwd_workspace_size(const kda_fwd_args *a) {
+  if (check_fwd(a, "kda_fwd_workspace_size") != KDA_OK) return 0;
+  return plan(a, false).bytes;
+}
+
+size_t kda_saved_size(const kda_fwd_args *a) {
+  if (check_fwd(a, "kda_saved_size") != KDA_OK) return 0;
+  return (size_t)max_chunks(a) * a->heads * 128 * 128 * elem_size(a->io_dtype);
+}
+
+size_t kda_bwd_workspace_size(const kda_bwd_args *a) {
+  if (!a || check_fwd(&a->fwd, "kda_bwd_workspace_size") != KDA_OK) return 0;
+  return plan(&a->fwd, true).bytes;
+}
+
+kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
+  kda_status st = check_fwd(a, "kda_fwd");
+  if (st != KDA_OK) return st;
+  const WsPlan w = plan(a, false);
+  if (!a->workspace || a->workspace_bytes < w.bytes)
+    return fail(KDA_ERR_INVALID_ARG, "%s: workspace missing or smaller than kda_fwd_workspace_size()", "kda_fwd");
+  if (a->total_tokens == 0) {
+    if (a->hT) {
+      const size_t n = (size_t)a->n_seqs * a->heads * 128 * 128 * 4;
+      cudaError_t e = a->h0 ? cudaMemcpyAsync(a->hT, a->h0, n, cudaMemcpyDeviceToDevice, stream)
+                            : cudaMemsetAsync(a->hT, 0, n, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "kda_fwd");
+    }
+    g_last_error.clear();
+    return KDA_OK;
+  }
+  char *ws = static_cast<char *>(a->workspace);
+  const bool f32 = a->io_dtype == KDA_F32;
+  kda::SeqGeom geo = geom(a, ws, w);
+  cudaError_t e = kda::launch_chunk_table(a->cu_seqlens, a->n_seqs, a->total_tokens,
+                                          reinterpret_cast<int *>(ws + w.cu), reinterpret_cast<int *>(ws + w.choff),
+                                          stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_fwd chunk table");
+  kda::PrepParams pp{geo, a->q, a->k, a->g, a->beta, a->scale, ws + w.img, a->dev_status};
+  if ((e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
+  kda::FwdScanParams sp{geo, a->v, ws + w.img, a->h0, a->o, a->hT, a->saved, a->dev_status};
+  if ((e = kda::launch_fwd_scan(sp, f32, pick_slice(a), stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd scan");
+  g_last_error.clear();
+  return KDA_OK;
+}
+
+kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
+  if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", "kda_bwd");
+  const kda_fwd_args *f = &a->fwd;
+  kda_fwd_args fcheck = *f;
+  if (!fcheck.o) fcheck.o = a->dq;   // o is not used by the backward
+  kda_status st = check_fwd(&fcheck, "kda_bwd");
+  if (st != KDA_OK) return st;
+  if (f->io_dtype == KDA_F32)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: the backward supports io_dtype KDA_BF16 only", "kda_bwd");
+  const WsPlan w = plan(f, true);
+  if (!a->workspace || a->workspace_bytes < w.bytes)
+    return fail(KDA_ERR_INVALID_ARG, "%s: workspace missing or smaller than kda_bwd_workspace_size()", "kda_bwd");
+  const void *need[] = {a->dO, a->dq, a->dk, a->dv, a->dg, f->saved};
+  const char *names[] = {"dO", "dq", "dk", "dv", "dg", "fwd.saved"};
+  for (int i = 0; i < 6; ++i) {
+    if (!need[i] && f->total_tokens > 0) return fail(KDA_ERR_INVALID_ARG, "kda_bwd: %s is NULL", names[i]);
+    if (!aligned(need[i], 16)) return fail(KDA_ERR_INVALID_ARG, "kda_bwd: %s is not 16-byte aligned", names[i]);
+  }
+  if ((!a->dbeta && f->total_tokens > 0) || !aligned(a->dbeta, 4))
+    return fail(KDA_ERR_INVALID_ARG, "%s: dbeta is NULL or not 4-byte aligned", "kda_bwd");
+  if (!aligned(a->dhT, 16) || !aligned(a->dh0, 16) || !aligned(a->workspace, 16))
+    return fail(KDA_ERR_INVALID_ARG, "%s: dhT, dh0 or workspace is not 16-byte aligned", "kda_bwd");
+  if (f->total_tokens == 0) {
+    if (a->dh0) {
+      const size_t n = (size_t)f->n_seqs * f->heads * 128 * 128 * 4;
+      cudaError_t e = a->dhT ? cudaMemcpyAsync(a->dh0, a->dhT, n, cudaMemcpyDeviceToDevice, stream)
+                             : cudaMemsetAsync(a->dh0, 0, n, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "kda_bwd");
+    }
+    g_last_error.clear();
+    return KDA_OK;
+  }
+  char *ws = static_cast<char *>(a->workspace);
+  kda::SeqGeom geo = geom(f, ws, w);
+  cudaError_t e = kda::launch_chunk_table(f->cu_seqlens, f->n_seqs, f->total_tokens,
+                                          reinterpret_cast<int *>(ws + w.cu), reinterpret_cast<int *>(ws + w.choff),
+                                          stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_bwd chunk table");
+  kda::PrepParams pp{geo, f->q, f->k, f->g, f->beta, f->scale, ws + w.img, f->dev_status};
+  if ((e = kda::launch_prep(pp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd prep");
+  kda::BwdScanParams bp{geo, a->dO, ws + w.img, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
+  if ((e = kda::launch_bwd_scan(bp, false, pick_slice(f), stream)) != cudaSuccess)
+    return cuda_fail(e, "kda_bwd dS scan");
+  kda::BwdStateParams sp{geo, f->v, a->dO, ws + w.img, f->saved, ws + w.dsaved,
+                         reinterpret_cast<float *>(ws + w.grad), f->dev_status};
+  if ((e = kda::launch_bwd_state(sp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd state grads");
+  kda::BwdIntraParams ip{geo, f->q, f->k, f->g, f->beta, f->scale, reinterpret_cast<const float *>(ws + w.grad),
+                         a->dq, a->dk, a->dg, a->dbeta, f->dev_status};
+  if ((e = kda::launch_bwd_intra(ip, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd intra grads");
+  g_last_error.clear();
+  return KDA_OK;
+}
+
+kda_status kda_step(const kda_step_args *a, cudaStream_t stream) {
+  if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", "kda_step");
+  if (a->dk != 128 || a->dv != 128) return fail(KDA_ERR_UNSUPPORTED, "%s: only dk = dv = 128 is supported", "kda_step");
+  if (a->io_dtype != KDA_BF16 && a->io_dtype != KDA_F32)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: io_dtype must be KDA_BF16 or KDA_F32", "kda_step");
+  if (a->n_seqs < 0 || a->heads < 1 || a->steps < 1 || a->steps > 8)
+    return fail(KDA_ERR_INVALID_ARG, "%s: need n_seqs >= 0, heads >= 1, 1 <= steps <= 8", "kda_step");
+  if (a->n_seqs == 0) {
+    g_last_error.clear();
+    return KDA_OK;
+  }
+  const void *need[] = {a->q, a->k, a->v, a->g, a->state, a->o};
+  const char *names[] = {"q", "k", "v", "g", "state", "o"};
+  for (int i = 0; i < 6; ++i) {
+    if (!need[i]) return fail(KDA_ERR_INVALID_ARG, "kda_step: %s is NULL", names[i]);
+    if (!aligned(need[i], 16)) return fail(KDA_ERR_INVALID_ARG, "kda_step: %s is not 16-byte aligned", names[i]);
+  }
+  if (!a->beta || !aligned(a->beta, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: beta is NULL or misaligned", "kda_step");
+  if (!aligned(a->accept_len, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: accept_len is misaligned", "kda_step");
+  kda::StepParams p{a->n_seqs, a->steps, a->heads, a->scale, a->q, a->k, a->v, a->beta, a->g, a->state,
+                    a->accept_len, a->o};
+  cudaError_t e = kda::launch_step(p, a->io_dtype == KDA_F32, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_step");
+  g_last_error.clear();
+  return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,245 @@
+// kda_common.cuh -- shared device helpers of the KDA kernels (sm_103a).
+//
+// * swizzled shared-memory tiles (16-byte chunks XOR-permuted by row so that
+//   8-row ldmatrix accesses hit distinct banks),
+// * warp-level tile GEMMs with one accumulator layout for two element types:
+//   bf16 tiles use ldmatrix + mma.sync m16n8k16 (fp32 accumulate); fp32 tiles
+//   use an FMA loop that fills the same m16n8 fragment positions, which gives
+//   the fp32-I/O path full fp32 products,
+// * mbarrier + cp.async.bulk (TMA bulk copy) helpers with bounded waits.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int D = 128;       // dk = dv
+constexpr int CH = 64;       // chunk length
+constexpr int SUB = 16;      // sub-block of the gated Gram factorisation
+constexpr int NSUB = CH / SUB;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr int ERR_TIMEOUT = 4;   // matches KDA_ERR_TIMEOUT
+
+typedef __nv_bfloat16 bf16;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- tiles
+// Physical 16-byte chunk of logical chunk `ch` in row `row` for rows of CPR chunks.
+template <int CPR>
+__device__ __forceinline__ int swz(int row, int ch) {
+  if constexpr (CPR >= 8) return (ch & ~7) | ((ch ^ row) & 7);
+  else if constexpr (CPR == 4) return ch ^ ((row >> 1) & 3);
+  else if constexpr (CPR == 2) return ch ^ ((row >> 2) & 1);
+  else return ch;
+}
+
+// A row-major tile of element type E whose rows hold LD elements, swizzled.
+template <typename E, int LD>
+struct Tile {
+  static constexpr int EPC = 16 / (int)sizeof(E);   // elements per 16-byte chunk
+  static constexpr int CPR = LD / EPC;              // chunks per row
+  static constexpr int BYTES_PER_ROW = LD * (int)sizeof(E);
+  E *p;
+  __device__ __forceinline__ Tile(E *ptr) : p(ptr) {}
+  __device__ __forceinline__ int off(int r, int c) const {
+    return r * LD + swz<CPR>(r, c / EPC) * EPC + (c % EPC);
+  }
+  __device__ __forceinline__ E *at(int r, int c) const { return p + off(r, c); }
+};
+
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f(float x) { return x; }
+template <typename E> __device__ __forceinline__ E from_f(float x);
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+
+// Store two adjacent elements (c even) of a tile.
+__device__ __forceinline__ void st2(bf16 *p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+}
+__device__ __forceinline__ void st2(float *p, float a, float b) {
+  *reinterpret_cast<float2 *>(p) = make_float2(a, b);
+}
+__device__ __forceinline__ float2 ld2(const bf16 *p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+}
+__device__ __forceinline__ float2 ld2(const float *p) { return *reinterpret_cast<const float2 *>(p); }
+
+// ---------------------------------------------------------------- mma.sync
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t &r0, uint32_t &r1, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t &r0, uint32_t &r1, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Accumulator fragment of an m16n8 tile for lane (g = lane/4, q = lane%4):
+//   c[0] = (g, 2q), c[1] = (g, 2q+1), c[2] = (g+8, 2q), c[3] = (g+8, 2q+1).
+//
+// wgemm: acc[nt] += A[m0:m0+16, k0:k1] * B[k0:k1, n0+8nt : n0+8nt+8] for nt < NT.
+//   AK: A stored [m][k] (true) or [k][m] (false);
+//   BK: B stored [n][k] (true) or [k][n] (false).
+// k0, k1 are multiples of 16.
+template <bool AK, bool BK, int NT, int LDA, int LDB>
+__device__ __forceinline__ void wgemm(float (&acc)[NT][4], Tile<bf16, LDA> A, int m0, Tile<bf16, LDB> B,
+                                      int n0, int k0, int k1) {
+  const int lane = threadIdx.x & 31;
+  const int i = lane >> 3, r8 = lane & 7;
+#pragma unroll 2
+  for (int kk = k0; kk < k1; kk += 16) {
+    uint32_t a[4];
+    if constexpr (AK) {
+      ldsm_x4(a, smem_u32(A.at(m0 + r8 + (i & 1) * 8, kk + (i >> 1) * 8)));
+    } else {
+      ldsm_x4_t(a, smem_u32(A.at(kk + (i >> 1) * 8 + r8, m0 + (i & 1) * 8)));
+    }
+#pragma unroll
+    for (int nt = 0; nt + 1 < NT; nt += 2) {
+      uint32_t b[4];
+      if constexpr (BK) {
+        ldsm_x4(b, smem_u32(B.at(n0 + nt * 8 + (i >> 1) * 8 + r8, kk + (i & 1) * 8)));
+      } else {
+        ldsm_x4_t(b, smem_u32(B.at(kk + (i & 1) * 8 + r8, n0 + nt * 8 + (i >> 1) * 8)));
+      }
+      mma16816(acc[nt], a, b[0], b[1]);
+      mma16816(acc[nt + 1], a, b[2], b[3]);
+    }
+    if constexpr (NT & 1) {
+      constexpr int nt = NT - 1;
+      uint32_t b0, b1;
+      const int j = i & 1;
+      if constexpr (BK) {
+        ldsm_x2(b0, b1, smem_u32(B.at(n0 + nt * 8 + r8, kk + j * 8)));
+      } else {
+        ldsm_x2_t(b0, b1, smem_u32(B.at(kk + j * 8 + r8, n0 + nt * 8)));
+      }
+      mma16816(acc[nt], a, b0, b1);
+    }
+  }
+}
+
+// fp32 tiles: same fragment positions, exact fp32 FMAs.
+template <bool AK, bool BK, int NT, int LDA, int LDB>
+__device__ __forceinline__ void wgemm(float (&acc)[NT][4], Tile<float, LDA> A, int m0, Tile<float, LDB> B,
+                                      int n0, int k0, int k1) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  for (int k = k0; k < k1; ++k) {
+    const float a0 = AK ? *A.at(m0 + g, k) : *A.at(k, m0 + g);
+    const float a1 = AK ? *A.at(m0 + g + 8, k) : *A.at(k, m0 + g + 8);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = n0 + nt * 8 + 2 * q;
+      const float b0 = BK ? *B.at(n, k) : *B.at(k, n);
+      const float b1 = BK ? *B.at(n + 1, k) : *B.at(k, n + 1);
+      acc[nt][0] = fmaf(a0, b0, acc[nt][0]);
+      acc[nt][1] = fmaf(a0, b1, acc[nt][1]);
+      acc[nt][2] = fmaf(a1, b0, acc[nt][2]);
+      acc[nt][3] = fmaf(a1, b1, acc[nt][3]);
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero(float (&acc)[NT][4]) {
+#pragma unroll
+  for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+}
+
+// ---------------------------------------------------------------- TMA bulk copies
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+// Global -> shared bulk copy; bytes and both addresses multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for phase `parity` of `bar`, giving up after ~2 s. Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 2000000000ull) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void report(int *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- chunk table
+// Chunk c of the packed problem: sequence index, first token, valid length.
+struct ChunkRef {
+  int seq;
+  long long t0;
+  int len;
+};
+
+// chunk_off[i] = first global chunk of sequence i (prefix sum of ceil(L_i/64)),
+// chunk_off[N] = number of chunks. Binary search for the owner of chunk c.
+__device__ __forceinline__ bool chunk_lookup(const int *chunk_off, const int *cu, int n_seqs, int c,
+                                             ChunkRef &ref) {
+  if (c >= chunk_off[n_seqs]) return false;
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (chunk_off[mid] <= c) lo = mid; else hi = mid - 1;
+  }
+  const long long s0 = cu[lo], s1 = cu[lo + 1];
+  ref.seq = lo;
+  ref.t0 = s0 + (long long)(c - chunk_off[lo]) * CH;
+  const long long rem = s1 - ref.t0;
+  ref.len = rem < CH ? (int)rem : CH;
+  return true;
+}
+
+}  // namespace kda

@@ -1,0 +1,115 @@
+// kda_internal.h -- host-side launch interfaces between kda_api.cu and the kernels.
+#pragma once
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Per-(chunk, head) record written by the chunk-prep kernel and read by the scans.
+// Tiles are stored exactly as they sit in shared memory (swizzled), so a single
+// bulk copy moves each of them. Element type E = bf16 (2 bytes) or float (4).
+//   [Qt | Kt]  64x128  q^*exp(G), k^*exp(G)           region 1
+//   [Tb]       64x64   T Diag(beta)                    region 2
+//   [Bm]       64x64   masked gated q.k^T              region 3
+//   [Kh | gC]  64x128  k^*exp(G_last-G); 128 fp32 exp(G_last)   region 4
+struct ImgLayout {
+  int esz;
+  size_t qt, kt, tb, bm, kh, gc, bytes;
+  __host__ __device__ explicit ImgLayout(int elem_size) : esz(elem_size) {
+    const size_t t128 = (size_t)64 * 128 * elem_size, t64 = (size_t)64 * 64 * elem_size;
+    qt = 0;
+    kt = qt + t128;
+    tb = kt + t128;
+    bm = tb + t64;
+    kh = bm + t64;
+    gc = kh + t128;
+    bytes = gc + 128 * sizeof(float);
+  }
+};
+
+// Per-(chunk, head) record of state-side gradients written by the backward's
+// state kernel: dQt, dKt, dKh (64x128 fp32 each), dBm, dTb (64x64 fp32), dgC (128).
+struct GradLayout {
+  static constexpr size_t dqt = 0, dkt = 64 * 128 * 4, dkh = 2 * 64 * 128 * 4, dbm = 3 * 64 * 128 * 4,
+                          dtb = dbm + 64 * 64 * 4, dgc = dtb + 64 * 64 * 4, bytes = dgc + 128 * 4;
+};
+
+struct SeqGeom {
+  int n_seqs;
+  long long total;
+  int heads;
+  int max_chunks;          // upper bound of the number of chunks (grid size)
+  const int *cu;           // [N+1] device
+  const int *chunk_off;    // [N+1] device, built by launch_chunk_table
+};
+
+struct PrepParams {
+  SeqGeom geo;
+  const void *q, *k;
+  const float *g, *beta;
+  float scale;
+  void *img;               // [max_chunks][H] ImgLayout records
+  int *status;
+};
+
+struct FwdScanParams {
+  SeqGeom geo;
+  const void *v;
+  const void *img;
+  const float *h0;
+  void *o;
+  float *hT;
+  void *saved;             // [max_chunks][H] 128x128 E tiles (swizzled), or null
+  int *status;
+};
+
+struct BwdScanParams {
+  SeqGeom geo;
+  const void *dO;
+  const void *img;
+  const float *dhT;
+  float *dv;
+  float *dh0;
+  void *dsaved;            // [max_chunks][H] 128x128 E tiles: dS at each chunk end
+  int *status;
+};
+
+struct BwdStateParams {
+  SeqGeom geo;
+  const void *v, *dO;
+  const void *img, *saved, *dsaved;
+  float *grad;             // [max_chunks][H] GradLayout records
+  int *status;
+};
+
+struct BwdIntraParams {
+  SeqGeom geo;
+  const void *q, *k;
+  const float *g, *beta;
+  float scale;
+  const float *grad;
+  float *dq, *dk, *dg, *dbeta;
+  int *status;
+};
+
+struct StepParams {
+  int n_seqs, steps, heads;
+  float scale;
+  const void *q, *k, *v;
+  const float *beta, *g;
+  float *state;
+  const int *accept_len;
+  void *o;
+};
+
+cudaError_t launch_chunk_table(const int *cu_in, int n_seqs, long long total, int *cu_out,
+                               int *chunk_off, cudaStream_t s);
+cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
+cudaError_t launch_bwd_scan(const BwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
+cudaError_t launch_bwd_state(const BwdStateParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_bwd_intra(const BwdIntraParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,392 @@
+// kda_scan.cu -- the sequential inter-chunk state passing (forward) and the
+// reverse dS scan (backward).
+//
+// One CTA per (sequence, head, slice of DVS value columns). Columns of the state
+// evolve independently (the decay and the erase act on key rows), so slicing
+// the value dimension multiplies the number of concurrent chains. The state
+// slice stays in registers (fp32) for the whole sequence; its bf16 copy in
+// shared memory is the tensor-core operand. Per chunk, with the record written
+// by the prep kernel (Qt = q^*exp(G), Kt = k^*exp(G), Kh = k^*exp(G_last - G),
+// Tb = T Diag(beta), Bm = masked gated q.k^T, gC = exp(G_last)):
+//
+//   forward:  V' = V - Kt S;  U = Tb V';  O = Qt S + Bm U;  S <- gC*S + Kh^T U
+//   backward: dU = Bm^T dO + Kh dS;  dV = Tb^T dU;  dS <- gC*dS + Qt^T dO - Kt^T dV
+//
+// (V' is the value minus what the decayed state already predicts; U is the
+// delta-rule update after the intra-chunk WY/UT transform.) The record of the
+// next chunk is fetched with TMA bulk copies into the regions that the current
+// chunk has finished with, tracked by four mbarriers.
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+template <typename E, int DVS>
+struct ScanSmem {
+  static constexpr int T128 = 64 * 128 * (int)sizeof(E), T64 = 64 * 64 * (int)sizeof(E);
+  // record regions (same byte layout as ImgLayout)
+  static constexpr int QT = 0, KT = T128, TB = 2 * T128, BM = TB + T64, KH = BM + T64, GC = KH + T128;
+  static constexpr int REC = GC + 512;
+  static constexpr int R1 = QT, R1B = 2 * T128;     // Qt, Kt
+  static constexpr int R2 = TB, R2B = T64;          // Tb
+  static constexpr int R3 = BM, R3B = T64;          // Bm
+  static constexpr int R4 = KH, R4B = T128 + 512;   // Kh, gC
+  static constexpr int SL = DVS * (int)sizeof(E);   // bytes per slice row
+  static constexpr int X0 = (REC + 127) / 128 * 128;   // [128][DVS] state / dS operand
+  static constexpr int X1 = X0 + 128 * SL;             // [64][DVS]
+  static constexpr int X2 = X1 + 64 * SL;              // [64][DVS]
+  static constexpr int X3 = X2 + 64 * SL;              // [64][DVS]
+  static constexpr int BAR = X3 + 64 * SL;
+  static constexpr int BYTES = BAR + 64;
+};
+
+template <typename E, int DVS>
+__device__ __forceinline__ void issue_region(char *smem, const char *rec, int off, int bytes, uint64_t *bar) {
+  fence_proxy_async();
+  mbar_expect_tx(bar, bytes);
+  bulk_g2s(smem + off, rec + off, bytes, bar);
+}
+
+// Element offset of (row, col) in a swizzled 128x128 E tile (saved-state records).
+template <typename E>
+__device__ __forceinline__ size_t full_off(int r, int c) {
+  constexpr int EPC = 16 / sizeof(E), CPR = 128 / EPC;
+  return (size_t)r * 128 + swz<CPR>(r, c / EPC) * EPC + (c % EPC);
+}
+
+// ------------------------------------------------------------------ forward
+template <typename E, int DVS>
+__global__ void __launch_bounds__(128) kda_fwd_scan_kernel(FwdScanParams p) {
+  constexpr int NZ = 128 / DVS, NT = DVS / 8;
+  using S = ScanSmem<E, DVS>;
+  extern __shared__ __align__(128) char smem[];
+  const int H = p.geo.heads;
+  const int z = blockIdx.x % NZ, h = (blockIdx.x / NZ) % H, seq = blockIdx.x / (NZ * H);
+  const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
+  const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, q4 = lane & 3;
+  const size_t rec_bytes = (size_t)S::REC;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
+  Tile<E, 128> Qt((E *)(smem + S::QT)), Kt((E *)(smem + S::KT)), Kh((E *)(smem + S::KH));
+  Tile<E, 64> Tb((E *)(smem + S::TB)), Bm((E *)(smem + S::BM));
+  const float *gC = (const float *)(smem + S::GC);
+  Tile<E, DVS> sS((E *)(smem + S::X0)), sVp((E *)(smem + S::X1)), sU((E *)(smem + S::X2)), sO((E *)(smem + S::X3));
+  const E *v = (const E *)p.v;
+  E *o = (E *)p.o;
+
+  // state slice: rows c = 32*warp + 16*mt + g8 + 8*hh, columns z*DVS + 8*nt + 2*q4 (+1)
+  float accS[2][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int c = 32 * warp + 16 * mt + g8 + 8 * hh, vv = z * DVS + 8 * nt + 2 * q4;
+        float2 x = make_float2(0.f, 0.f);
+        if (p.h0) x = *reinterpret_cast<const float2 *>(p.h0 + (((size_t)seq * H + h) * 128 + c) * 128 + vv);
+        accS[mt][nt][2 * hh] = x.x;
+        accS[mt][nt][2 * hh + 1] = x.y;
+        st2(sS.at(c, 8 * nt + 2 * q4), x.x, x.y);
+      }
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * rec_bytes; };
+  if (tid == 0 && nch > 0) {
+    const char *r0 = rec_of(0);
+    issue_region<E, DVS>(smem, r0, S::R1, S::R1B, &bar[0]);
+    issue_region<E, DVS>(smem, r0, S::R2, S::R2B, &bar[1]);
+    issue_region<E, DVS>(smem, r0, S::R3, S::R3B, &bar[2]);
+    issue_region<E, DVS>(smem, r0, S::R4, S::R4B, &bar[3]);
+  }
+  bool ok = true;
+  for (int j = 0; j < nch; ++j) {
+    const uint32_t par = j & 1;
+    const long long t0 = s0 + (long long)j * CH;
+    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+    // value fragment of this chunk
+    float2 vf[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * warp + g8 + 8 * hh;
+        vf[nt][hh] = make_float2(0.f, 0.f);
+        if (r < clen) vf[nt][hh] = ld2(v + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + 8 * nt + 2 * q4);
+      }
+    // chunk-start state for the backward
+    if (p.saved) {
+      E *sv = (E *)p.saved + ((size_t)(cbase + j) * H + h) * 128 * 128;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int c = 32 * warp + 16 * mt + g8 + 8 * hh, vv = z * DVS + 8 * nt + 2 * q4;
+            st2(sv + full_off<E>(c, vv), accS[mt][nt][2 * hh], accS[mt][nt][2 * hh + 1]);
+          }
+    }
+    // (a) V' = V - Kt S ;  O = Qt S
+    ok &= mbar_wait(&bar[0], par);
+    float accV[NT][4], accO[NT][4];
+    zero(accV);
+    zero(accO);
+    wgemm<true, false, NT>(accV, Kt, 16 * warp, sS, 0, 0, 128);
+    wgemm<true, false, NT>(accO, Qt, 16 * warp, sS, 0, 0, 128);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        st2(sVp.at(16 * warp + g8 + 8 * hh, 8 * nt + 2 * q4), vf[nt][hh].x - accV[nt][2 * hh],
+            vf[nt][hh].y - accV[nt][2 * hh + 1]);
+    if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
+    if (tid == 0 && j + 1 < nch) issue_region<E, DVS>(smem, rec_of(j + 1), S::R1, S::R1B, &bar[0]);
+    // (b) U = Tb V'   (Tb lower triangular)
+    ok &= mbar_wait(&bar[1], par);
+    float accU[NT][4];
+    zero(accU);
+    wgemm<true, false, NT>(accU, Tb, 16 * warp, sVp, 0, 0, 16 * (warp + 1));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        st2(sU.at(16 * warp + g8 + 8 * hh, 8 * nt + 2 * q4), accU[nt][2 * hh], accU[nt][2 * hh + 1]);
+    if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
+    if (tid == 0 && j + 1 < nch) issue_region<E, DVS>(smem, rec_of(j + 1), S::R2, S::R2B, &bar[1]);
+    // (c) O += Bm U
+    ok &= mbar_wait(&bar[2], par);
+    wgemm<true, false, NT>(accO, Bm, 16 * warp, sU, 0, 0, 16 * (warp + 1));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        st2(sO.at(16 * warp + g8 + 8 * hh, 8 * nt + 2 * q4), accO[nt][2 * hh], accO[nt][2 * hh + 1]);
+    // (d) S <- gC * S + Kh^T U
+    ok &= mbar_wait(&bar[3], par);
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const float d0 = gC[32 * warp + 16 * mt + g8], d1 = gC[32 * warp + 16 * mt + g8 + 8];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        accS[mt][nt][0] *= d0; accS[mt][nt][1] *= d0;
+        accS[mt][nt][2] *= d1; accS[mt][nt][3] *= d1;
+      }
+      wgemm<false, false, NT>(accS[mt], Kh, 32 * warp + 16 * mt, sU, 0, 0, 64);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          st2(sS.at(32 * warp + 16 * mt + g8 + 8 * hh, 8 * nt + 2 * q4), accS[mt][nt][2 * hh],
+              accS[mt][nt][2 * hh + 1]);
+    }
+    if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
+    // output rows, 16-byte coalesced
+    {
+      constexpr int EPC = 16 / sizeof(E), CPR = DVS / EPC;
+      for (int idx = tid; idx < 64 * CPR; idx += 128) {
+        const int r = idx / CPR, ch = idx % CPR;
+        if (r < clen)
+          *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + ch * EPC) =
+              *reinterpret_cast<const uint4 *>(sO.at(r, ch * EPC));
+      }
+    }
+    if (tid == 0 && j + 1 < nch) {
+      issue_region<E, DVS>(smem, rec_of(j + 1), S::R3, S::R3B, &bar[2]);
+      issue_region<E, DVS>(smem, rec_of(j + 1), S::R4, S::R4B, &bar[3]);
+    }
+  }
+  if (p.hT) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int c = 32 * warp + 16 * mt + g8 + 8 * hh, vv = z * DVS + 8 * nt + 2 * q4;
+          *reinterpret_cast<float2 *>(p.hT + (((size_t)seq * H + h) * 128 + c) * 128 + vv) =
+              make_float2(accS[mt][nt][2 * hh], accS[mt][nt][2 * hh + 1]);
+        }
+  }
+}
+
+// ------------------------------------------------------------------ backward
+template <typename E, int DVS>
+__global__ void __launch_bounds__(128) kda_bwd_scan_kernel(BwdScanParams p) {
+  constexpr int NZ = 128 / DVS, NT = DVS / 8;
+  using S = ScanSmem<E, DVS>;
+  extern __shared__ __align__(128) char smem[];
+  const int H = p.geo.heads;
+  const int z = blockIdx.x % NZ, h = (blockIdx.x / NZ) % H, seq = blockIdx.x / (NZ * H);
+  const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
+  const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, q4 = lane & 3;
+  const size_t rec_bytes = (size_t)S::REC;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
+  Tile<E, 128> Qt((E *)(smem + S::QT)), Kt((E *)(smem + S::KT)), Kh((E *)(smem + S::KH));
+  Tile<E, 64> Tb((E *)(smem + S::TB)), Bm((E *)(smem + S::BM));
+  const float *gC = (const float *)(smem + S::GC);
+  Tile<E, DVS> sdS((E *)(smem + S::X0)), sdO((E *)(smem + S::X1)), sdU((E *)(smem + S::X2)), sdV((E *)(smem + S::X3));
+  const E *dO = (const E *)p.dO;
+
+  float accS[2][NT][4];   // dS slice, same fragment layout as the forward state
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int c = 32 * warp + 16 * mt + g8 + 8 * hh, vv = z * DVS + 8 * nt + 2 * q4;
+        float2 x = make_float2(0.f, 0.f);
+        if (p.dhT) x = *reinterpret_cast<const float2 *>(p.dhT + (((size_t)seq * H + h) * 128 + c) * 128 + vv);
+        accS[mt][nt][2 * hh] = x.x;
+        accS[mt][nt][2 * hh + 1] = x.y;
+        st2(sdS.at(c, 8 * nt + 2 * q4), x.x, x.y);
+      }
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * rec_bytes; };
+  if (tid == 0 && nch > 0) {
+    const char *r0 = rec_of(nch - 1);
+    issue_region<E, DVS>(smem, r0, S::R1, S::R1B, &bar[0]);
+    issue_region<E, DVS>(smem, r0, S::R2, S::R2B, &bar[1]);
+    issue_region<E, DVS>(smem, r0, S::R3, S::R3B, &bar[2]);
+    issue_region<E, DVS>(smem, r0, S::R4, S::R4B, &bar[3]);
+  }
+  bool ok = true;
+  for (int it = 0; it < nch; ++it) {
+    const int j = nch - 1 - it;
+    const uint32_t par = it & 1;
+    const long long t0 = s0 + (long long)j * CH;
+    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+    // dO slice rows of this chunk
+    {
+      constexpr int EPC = 16 / sizeof(E), CPR = DVS / EPC;
+      for (int idx = tid; idx < 64 * CPR; idx += 128) {
+        const int r = idx / CPR, ch = idx % CPR;
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (r < clen) x = __ldg(reinterpret_cast<const uint4 *>(dO + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + ch * EPC));
+        *reinterpret_cast<uint4 *>(sdO.at(r, ch * EPC)) = x;
+      }
+    }
+    // dS at the end of this chunk, for the chunk-local gradient kernel
+    {
+      E *sv = (E *)p.dsaved + ((size_t)(cbase + j) * H + h) * 128 * 128;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int c = 32 * warp + 16 * mt + g8 + 8 * hh, vv = z * DVS + 8 * nt + 2 * q4;
+            st2(sv + full_off<E>(c, vv), accS[mt][nt][2 * hh], accS[mt][nt][2 * hh + 1]);
+          }
+    }
+    __syncthreads();
+    // (a) dU = Bm^T dO + Kh dS
+    ok &= mbar_wait(&bar[2], par);
+    ok &= mbar_wait(&bar[3], par);
+    float accU[NT][4];
+    zero(accU);
+    wgemm<false, false, NT>(accU, Bm, 16 * warp, sdO, 0, 16 * warp, 64);
+    wgemm<true, false, NT>(accU, Kh, 16 * warp, sdS, 0, 0, 128);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        st2(sdU.at(16 * warp + g8 + 8 * hh, 8 * nt + 2 * q4), accU[nt][2 * hh], accU[nt][2 * hh + 1]);
+    if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
+    if (tid == 0 && j > 0) issue_region<E, DVS>(smem, rec_of(j - 1), S::R3, S::R3B, &bar[2]);
+    // (b) dV = Tb^T dU  -> dv output; -dV into shared memory
+    ok &= mbar_wait(&bar[1], par);
+    float accV[NT][4];
+    zero(accV);
+    wgemm<false, false, NT>(accV, Tb, 16 * warp, sdU, 0, 16 * warp, 64);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * warp + g8 + 8 * hh;
+        st2(sdV.at(r, 8 * nt + 2 * q4), -accV[nt][2 * hh], -accV[nt][2 * hh + 1]);
+        if (r < clen)
+          *reinterpret_cast<float2 *>(p.dv + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + 8 * nt + 2 * q4) =
+              make_float2(accV[nt][2 * hh], accV[nt][2 * hh + 1]);
+      }
+    if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
+    if (tid == 0 && j > 0) issue_region<E, DVS>(smem, rec_of(j - 1), S::R2, S::R2B, &bar[1]);
+    // (c) dS <- gC * dS + Qt^T dO - Kt^T dV
+    ok &= mbar_wait(&bar[0], par);
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const float d0 = gC[32 * warp + 16 * mt + g8], d1 = gC[32 * warp + 16 * mt + g8 + 8];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        accS[mt][nt][0] *= d0; accS[mt][nt][1] *= d0;
+        accS[mt][nt][2] *= d1; accS[mt][nt][3] *= d1;
+      }
+      wgemm<false, false, NT>(accS[mt], Qt, 32 * warp + 16 * mt, sdO, 0, 0, 64);
+      wgemm<false, false, NT>(accS[mt], Kt, 32 * warp + 16 * mt, sdV, 0, 0, 64);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          st2(sdS.at(32 * warp + 16 * mt + g8 + 8 * hh, 8 * nt + 2 * q4), accS[mt][nt][2 * hh],
+              accS[mt][nt][2 * hh + 1]);
+    }
+    if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
+    if (tid == 0 && j > 0) {
+      issue_region<E, DVS>(smem, rec_of(j - 1), S::R1, S::R1B, &bar[0]);
+      issue_region<E, DVS>(smem, rec_of(j - 1), S::R4, S::R4B, &bar[3]);
+    }
+  }
+  if (p.dh0) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int c = 32 * warp + 16 * mt + g8 + 8 * hh, vv = z * DVS + 8 * nt + 2 * q4;
+          *reinterpret_cast<float2 *>(p.dh0 + (((size_t)seq * H + h) * 128 + c) * 128 + vv) =
+              make_float2(accS[mt][nt][2 * hh], accS[mt][nt][2 * hh + 1]);
+        }
+  }
+}
+
+template <typename K>
+static cudaError_t launch_scan_kernel(K kern, int bytes, unsigned grid, const void *params, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  void *args[] = {const_cast<void *>(params)};
+  return cudaLaunchKernel((const void *)kern, dim3(grid), dim3(128), args, bytes, s);
+}
+
+cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int dvs, cudaStream_t s) {
+  const unsigned grid = (unsigned)((long long)p.geo.n_seqs * p.geo.heads * (128 / dvs));
+  if (grid == 0) return cudaSuccess;
+  if (f32) {
+    if (dvs == 32) return launch_scan_kernel(kda_fwd_scan_kernel<float, 32>, ScanSmem<float, 32>::BYTES, grid, &p, s);
+    return launch_scan_kernel(kda_fwd_scan_kernel<float, 64>, ScanSmem<float, 64>::BYTES, grid, &p, s);
+  }
+  if (dvs == 32) return launch_scan_kernel(kda_fwd_scan_kernel<bf16, 32>, ScanSmem<bf16, 32>::BYTES, grid, &p, s);
+  return launch_scan_kernel(kda_fwd_scan_kernel<bf16, 64>, ScanSmem<bf16, 64>::BYTES, grid, &p, s);
+}
+
+cudaError_t launch_bwd_scan(const BwdScanParams &p, bool f32, int dvs, cudaStream_t s) {
+  const unsigned grid = (unsigned)((long long)p.geo.n_seqs * p.geo.heads * (128 / dvs));
+  if (grid == 0) return cudaSuccess;
+  if (f32) {
+    if (dvs == 32) return launch_scan_kernel(kda_bwd_scan_kernel<float, 32>, ScanSmem<float, 32>::BYTES, grid, &p, s);
+    return launch_scan_kernel(kda_bwd_scan_kernel<float, 64>, ScanSmem<float, 64>::BYTES, grid, &p, s);
+  }
+  if (dvs == 32) return launch_scan_kernel(kda_bwd_scan_kernel<bf16, 32>, ScanSmem<bf16, 32>::BYTES, grid, &p, s);
+  return launch_scan_kernel(kda_bwd_scan_kernel<bf16, 64>, ScanSmem<bf16, 64>::BYTES, grid, &p, s);
+}
+
+}  // namespace kda

@@ -1,0 +1,156 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention library (libkda.so).
+ *
+ * Kimi Delta Attention (KDA) is linear attention whose per-head recurrent state
+ * is updated with channel-wise gating ("Kimi K3 on Fireworks: Fast RL at frontier
+ * scale", training section, KDA paragraph; the first page's section
+ * "KDA：从循环记忆到高效 GPU 执行", whose benchmark caption counts the Q/K
+ * normalisation and the gate scan as part of the KDA core). Per head, with the
+ * state S of shape [dk][dv] (row c = key channel, column j = value channel):
+ *
+ *     q^ = scale * q / sqrt(|q|^2 + 1e-6),     k^ = k / sqrt(|k|^2 + 1e-6)
+ *     S_t = (I - beta_t k^_t k^_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k^_t v_t^T
+ *     o_t = S_t^T q^_t
+ *
+ * g is the per-channel log-decay (g <= 0), beta the per-token write strength.
+ * The model shape of interest is 96 heads x 128 dims with a 128 x 128 state per
+ * head (architecture figure of "Kimi K3 模型结构（10）：RL 与服务中的状态管理").
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or synchronises. Every call only enqueues work on
+ *    `stream` and returns; results are valid once the stream reaches that point.
+ *  - Layouts are dense row-major with the listed shapes. Token-major tensors pack
+ *    all sequences back to back: token t of sequence i is row cu_seqlens[i] + t.
+ *  - Supported sizes: dk = dv = 128, chunk = 64, heads >= 1. Other values return
+ *    KDA_ERR_UNSUPPORTED.
+ *  - Every pointer must be 16-byte aligned; a required pointer that is NULL or
+ *    misaligned, or a workspace smaller than the matching *_workspace_size(),
+ *    returns KDA_ERR_INVALID_ARG. Validation happens before any launch: on an
+ *    error nothing is written.
+ *  - KDA_ERR_CUDA means a launch failed (see kda_last_error()).
+ *  - If dev_status is not NULL it must point to one device int32 that the caller
+ *    zeroes; a kernel that gives up a bounded wait writes KDA_ERR_TIMEOUT there.
+ *  - Results are deterministic: identical inputs give bit-identical outputs
+ *    (no floating-point atomics anywhere).
+ *  - Preconditions that are not checked: inputs are finite; g <= 0; the sum of g
+ *    over any 16 consecutive tokens of one channel inside a 64-token chunk is
+ *    >= -80 (every g >= -5 is enough), which keeps every gating factor in range.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* NULL / misaligned pointer, bad size, small workspace */
+    KDA_ERR_UNSUPPORTED = 2,   /* dk, dv, chunk or dtype outside the supported set       */
+    KDA_ERR_CUDA = 3,          /* a CUDA launch failed                                   */
+    KDA_ERR_TIMEOUT = 4        /* written to *dev_status by a kernel whose wait gave up  */
+} kda_status;
+
+typedef enum {
+    KDA_BF16 = 0,              /* q, k, v, o, dO stored as bfloat16                     */
+    KDA_F32 = 1                /* ... stored as float32                                  */
+} kda_dtype;
+
+/* Chunked training forward. */
+typedef struct {
+    int32_t n_seqs;            /* N >= 1 sequences                                       */
+    int64_t total_tokens;      /* sum of the sequence lengths (0 allowed: no work)      */
+    int32_t heads;             /* H                                                      */
+    int32_t dk, dv;            /* 128, 128                                               */
+    int32_t chunk;             /* 64                                                     */
+    float scale;               /* multiplies q^ (1.0 for plain KDA)                      */
+    int32_t io_dtype;          /* kda_dtype of q, k, v, o                                */
+    const int32_t *cu_seqlens; /* [N+1] sequence offsets, cu[0]=0, cu[N]=total, or NULL:
+                                  N sequences of equal length total/N                   */
+    const void *q;             /* [total, H, dk]                                         */
+    const void *k;             /* [total, H, dk]                                         */
+    const void *v;             /* [total, H, dv]                                         */
+    const float *beta;         /* [total, H]                                             */
+    const float *g;            /* [total, H, dk] log-decay                               */
+    const float *h0;           /* [N, H, dk, dv] initial states, or NULL for zero        */
+    void *o;                   /* out [total, H, dv]                                     */
+    float *hT;                 /* out [N, H, dk, dv] final states, or NULL               */
+    void *saved;               /* out, kda_saved_size() bytes: chunk-start states kept
+                                  for kda_bwd, or NULL when no backward follows          */
+    void *workspace;           /* scratch, kda_fwd_workspace_size() bytes                */
+    size_t workspace_bytes;
+    int32_t *dev_status;       /* optional device int32, see above                       */
+} kda_fwd_args;
+
+/* Backward of kda_fwd: gradients of <dO, o> + <dhT, hT>. */
+typedef struct {
+    kda_fwd_args fwd;          /* the forward's arguments; fwd.o, fwd.hT are ignored and
+                                  fwd.saved must hold what that forward wrote             */
+    const void *dO;            /* [total, H, dv] in io_dtype                             */
+    const float *dhT;          /* [N, H, dk, dv] or NULL for zero                        */
+    float *dq;                 /* out [total, H, dk] fp32                                */
+    float *dk;                 /* out [total, H, dk] fp32                                */
+    float *dv;                 /* out [total, H, dv] fp32                                */
+    float *dbeta;              /* out [total, H] fp32                                    */
+    float *dg;                 /* out [total, H, dk] fp32                                */
+    float *dh0;                /* out [N, H, dk, dv] fp32, or NULL                       */
+    void *workspace;           /* scratch, kda_bwd_workspace_size() bytes                */
+    size_t workspace_bytes;
+} kda_bwd_args;
+
+/* Decode / draft-verify step: L tokens per sequence against a committed state. */
+typedef struct {
+    int32_t n_seqs;            /* N                                                      */
+    int32_t steps;             /* L, 1..8 tokens per sequence in this call               */
+    int32_t heads;             /* H                                                      */
+    int32_t dk, dv;            /* 128, 128                                               */
+    float scale;
+    int32_t io_dtype;          /* kda_dtype of q, k, v, o                                */
+    const void *q;             /* [N, L, H, dk]                                          */
+    const void *k;             /* [N, L, H, dk]                                          */
+    const void *v;             /* [N, L, H, dv]                                          */
+    const float *beta;         /* [N, L, H]                                              */
+    const float *g;            /* [N, L, H, dk]                                          */
+    float *state;              /* in/out [N, H, dk, dv]: read, then overwritten with the
+                                  state after accept_len[i] tokens (untouched if 0)      */
+    const int32_t *accept_len; /* [N] in 0..L, or NULL meaning L for every sequence      */
+    void *o;                   /* out [N, L, H, dv]: outputs of all L tokens             */
+} kda_step_args;
+
+/*
+ * kda_fwd -- chunked forward (chunk 64). Per chunk the intra-chunk work (gated
+ * k.k^T / q.k^T blocks, the WY/UT triangular solve) runs in parallel over all
+ * chunks and heads, and a sequential scan passes the 128x128 state between
+ * chunks (the KDA paragraph: chunk-local work in parallel, little state between).
+ */
+kda_status kda_fwd(const kda_fwd_args *args, cudaStream_t stream);
+size_t kda_fwd_workspace_size(const kda_fwd_args *args);
+/* Bytes of chunk-start states that kda_fwd writes to args->saved for kda_bwd. */
+size_t kda_saved_size(const kda_fwd_args *args);
+
+/* kda_bwd -- gradients for q, k, v, beta, g and the initial state (the pages
+ * report a matching backward kernel next to the forward one). */
+kda_status kda_bwd(const kda_bwd_args *args, cudaStream_t stream);
+size_t kda_bwd_workspace_size(const kda_bwd_args *args);
+
+/* kda_step -- recurrent decode over L <= 8 tokens, returning all L outputs and
+ * committing the state only through the accepted prefix, as ReplaySSM advances
+ * KDA state only through accepted tokens ("Kimi K3 on Fireworks", rollout
+ * section, speculative decoding paragraph). Needs no workspace. */
+kda_status kda_step(const kda_step_args *args, cudaStream_t stream);
+
+/* Message of the last error on the calling host thread ("" if none). */
+const char *kda_last_error(void);
+
+/* Library ABI version (bumped on any change of the structs above). */
+int32_t kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H */

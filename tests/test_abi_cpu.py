@@ -1,0 +1,145 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol,
+the ctypes structs match the C layout, and argument validation rejects bad
+calls before anything touches a GPU."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_chunked_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    from gated_delta_rule_chunked_gb300 import _lib
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", os.path.join(ROOT, "gated_delta_rule_chunked_gb300",
+                                                                     "libkda.so")],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (kda_\w+)", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_abi_version(lib):
+    assert lib.kda_abi_version() == 1
+
+
+def test_struct_layout_matches_c(tmp_path):
+    from gated_delta_rule_chunked_gb300 import _lib
+    probe = tmp_path / "probe.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kda.h"', "int main(void){"]
+    for sname, cls in (("kda_fwd_args", _lib.FwdArgs), ("kda_bwd_args", _lib.BwdArgs),
+                       ("kda_step_args", _lib.StepArgs)):
+        lines.append(f'printf("{sname} %zu\\n", sizeof({sname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'printf("{sname}.{fname} %zu\\n", offsetof({sname}, {fname}));')
+    lines.append("return 0;}")
+    probe.write_text("\n".join(lines))
+    exe = tmp_path / "probe"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include",
+                           str(probe), "-o", str(exe)])
+    got = dict(line.split() for line in subprocess.check_output([str(exe)], text=True).splitlines())
+    for sname, cls in (("kda_fwd_args", _lib.FwdArgs), ("kda_bwd_args", _lib.BwdArgs),
+                       ("kda_step_args", _lib.StepArgs)):
+        assert int(got[sname]) == C.sizeof(cls), sname
+        for fname, _ in cls._fields_:
+            assert int(got[f"{sname}.{fname}"]) == getattr(cls, fname).offset, f"{sname}.{fname}"
+
+
+def _fwd_args(**over):
+    from gated_delta_rule_chunked_gb300 import _lib
+    a = _lib.FwdArgs()
+    a.n_seqs, a.total_tokens, a.heads, a.dk, a.dv, a.chunk = 1, 128, 2, 128, 128, 64
+    a.scale, a.io_dtype = 1.0, _lib.KDA_BF16
+    fake = 1 << 40          # well-aligned, never dereferenced: validation fails first
+    a.q = a.k = a.v = a.g = a.o = a.beta = fake
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("dk", 64, 2), ("chunk", 32, 2), ("io_dtype", 7, 2),
+    ("heads", 0, 1), ("n_seqs", 0, 1), ("total_tokens", -1, 1),
+    ("q", None, 1), ("g", (1 << 40) + 8, 1), ("total_tokens", 127, 1),   # 127 not divisible? n_seqs=1 ok
+])
+def test_fwd_validation_rejects_before_launch(lib, field, value, status):
+    from gated_delta_rule_chunked_gb300 import _lib
+    if field == "total_tokens" and value == 127:
+        a = _fwd_args(n_seqs=2, total_tokens=127)      # equal-length split impossible
+    else:
+        a = _fwd_args(**{field: value})
+    assert lib.kda_fwd(C.byref(a), None) == status
+    assert lib.kda_last_error().decode()
+
+
+def test_fwd_rejects_small_workspace(lib):
+    a = _fwd_args()
+    need = lib.kda_fwd_workspace_size(C.byref(a))
+    assert need > 0
+    a.workspace, a.workspace_bytes = 1 << 40, need - 256
+    assert lib.kda_fwd(C.byref(a), None) == 1
+    assert "workspace" in lib.kda_last_error().decode()
+
+
+def test_workspace_sizes_scale_with_problem(lib):
+    from gated_delta_rule_chunked_gb300 import _lib
+    a = _fwd_args(total_tokens=32768, heads=96)
+    chunks = 32768 // 64 + 1
+    rec = 3 * 64 * 128 * 2 + 2 * 64 * 64 * 2 + 512
+    assert lib.kda_fwd_workspace_size(C.byref(a)) >= chunks * 96 * rec
+    assert lib.kda_saved_size(C.byref(a)) == chunks * 96 * 128 * 128 * 2
+    b = _lib.BwdArgs()
+    b.fwd = a
+    assert lib.kda_bwd_workspace_size(C.byref(b)) > lib.kda_fwd_workspace_size(C.byref(a))
+
+
+def test_bwd_fp32_is_reported_unsupported(lib):
+    from gated_delta_rule_chunked_gb300 import _lib
+    b = _lib.BwdArgs()
+    b.fwd = _fwd_args(io_dtype=_lib.KDA_F32)
+    assert lib.kda_bwd(C.byref(b), None) == 2
+
+
+def test_step_validation(lib):
+    from gated_delta_rule_chunked_gb300 import _lib
+    a = _lib.StepArgs()
+    a.n_seqs, a.steps, a.heads, a.dk, a.dv, a.scale = 4, 9, 2, 128, 128, 1.0
+    fake = 1 << 40
+    a.q = a.k = a.v = a.g = a.beta = a.state = a.o = fake
+    assert lib.kda_step(C.byref(a), None) == 1     # steps > 8
+    a.steps, a.dk = 4, 96
+    assert lib.kda_step(C.byref(a), None) == 2
+    a.dk, a.state = 128, None
+    assert lib.kda_step(C.byref(a), None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from gated_delta_rule_chunked_gb300 import _lib
+    saved = _lib._lib
+    try:
+        _lib._lib = None
+        with pytest.raises(ImportError):
+            _lib.load(str(tmp_path / "missing.so"))
+    finally:
+        _lib._lib = saved

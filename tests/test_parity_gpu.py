@@ -1,0 +1,208 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Metric per output tensor: max|gpu - oracle| / max|oracle|, at most 1e-2 for
+bf16 I/O and 1e-4 for fp32 I/O. The oracle reads exactly the bf16/fp32 values
+the GPU reads. Small cases span several chunks with ragged tails; the full-size
+workloads are compared on sampled (sequence, head) pairs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_chunked_gb300.inputs import make_seq_batch, make_decode_batch, make_workload, WORKLOADS
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 1e-2, "f32": 1e-4}
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import gated_delta_rule_chunked_gb300 as m
+    m.library()
+    return m
+
+
+def rel(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all()
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def to_dev(b, dev="cuda"):
+    out = {}
+    for n in ("q", "k", "v", "beta", "g", "cu_seqlens", "h0", "dO"):
+        t = getattr(b, n)
+        out[n] = None if t is None else t.to(dev)
+    return out
+
+
+def run_fwd(kda, b, save=False, scale=1.0):
+    t = to_dev(b)
+    o, hT, saved = kda.kda_fwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["cu_seqlens"], t["h0"],
+                               save=save, scale=scale)
+    torch.cuda.synchronize()
+    return t, o, hT, saved
+
+
+def check_fwd(kda, b, tol, scale=1.0):
+    _, o, hT, _ = run_fwd(kda, b, scale=scale)
+    res = oracle.fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, scale=scale)
+    o_ref, h_ref = oracle.assemble_fwd(res, b.cu_seqlens, b.heads, 128)
+    e_o, e_h = rel(o.float().cpu(), o_ref), rel(hT.cpu(), h_ref)
+    assert e_o <= tol and e_h <= tol, (e_o, e_h)
+    return e_o, e_h
+
+
+# ---------------------------------------------------------------- forward
+
+@pytest.mark.parametrize("lens", [[1], [63], [64], [65], [129], [200, 1, 64, 130]])
+def test_fwd_bf16_ragged(kda, lens):
+    b = make_seq_batch(lens, heads=3, io_dtype="bf16", seed=sum(lens), h0=True)
+    check_fwd(kda, b, TOL["bf16"])
+
+
+@pytest.mark.parametrize("lens", [[512], [333, 64]])
+def test_fwd_f32(kda, lens):
+    b = make_seq_batch(lens, heads=2, io_dtype="f32", seed=len(lens), h0=(len(lens) > 1))
+    check_fwd(kda, b, TOL["f32"])
+
+
+def test_fwd_workload_f32_T512_H2(kda):
+    check_fwd(kda, make_workload("fwd-f32-T512-H2"), TOL["f32"])
+
+
+def test_fwd_zero_state_and_scale(kda):
+    b = make_seq_batch([300], heads=2, io_dtype="bf16", seed=5, h0=False)
+    check_fwd(kda, b, TOL["bf16"], scale=0.0883883)
+
+
+def test_fwd_many_heads_selects_wide_slices(kda):
+    # n_seqs * heads large enough that the scan uses 64-column value slices
+    b = make_seq_batch([70] * 4, heads=96, io_dtype="bf16", seed=11, h0=True)
+    check_fwd(kda, b, TOL["bf16"])
+
+
+def test_fwd_empty_sequences_keep_state(kda):
+    b = make_seq_batch([0, 100, 0], heads=2, io_dtype="bf16", seed=12, h0=True)
+    _, o, hT, _ = run_fwd(kda, b)
+    np.testing.assert_array_equal(hT[0].cpu().numpy(), b.h0[0].numpy())
+    np.testing.assert_array_equal(hT[2].cpu().numpy(), b.h0[2].numpy())
+    check_fwd(kda, b, TOL["bf16"])
+
+
+def test_fwd_is_deterministic(kda):
+    b = make_seq_batch([400, 77], heads=4, io_dtype="bf16", seed=13, h0=True)
+    _, o1, h1, _ = run_fwd(kda, b)
+    _, o2, h2, _ = run_fwd(kda, b)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_fwd_chaining_matches_single_call(kda):
+    b = make_seq_batch([256], heads=2, io_dtype="bf16", seed=14, h0=True)
+    t = to_dev(b)
+    o, hT, _ = kda.kda_fwd(t["q"], t["k"], t["v"], t["beta"], t["g"], None, t["h0"])
+    o1, h1, _ = kda.kda_fwd(t["q"][:128], t["k"][:128], t["v"][:128], t["beta"][:128], t["g"][:128], None, t["h0"])
+    o2, h2, _ = kda.kda_fwd(t["q"][128:], t["k"][128:], t["v"][128:], t["beta"][128:], t["g"][128:], None, h1)
+    torch.cuda.synchronize()
+    assert rel(torch.cat([o1, o2]).float().cpu(), o.float().cpu()) < 1e-2
+    assert rel(h2.cpu(), hT.cpu()) < 1e-2
+
+
+def test_fwd_workload_T4096_H96_full(kda):
+    check_fwd(kda, make_workload("fwd-bf16-T4096-H96"), TOL["bf16"])
+
+
+# ---------------------------------------------------------------- backward
+
+def check_bwd(kda, b, tol, tasks=None):
+    t, o, hT, saved = run_fwd(kda, b, save=True)
+    gen = torch.Generator().manual_seed(99)
+    dhT = (torch.randn(b.n_seqs, b.heads, 128, 128, generator=gen) * 0.1)
+    gr = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, t["cu_seqlens"], t["h0"],
+                     dhT.to("cuda"))
+    torch.cuda.synchronize()
+    res = oracle.bwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.dO, b.h0, dhT, tasks=tasks)
+    errs = {}
+    cu = [int(x) for x in b.cu_seqlens.tolist()]
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        gots, refs = [], []
+        for (i, h), r in res.items():
+            g = gr[name].cpu()
+            gots.append((g[i, h] if name == "dh0" else g[cu[i]:cu[i + 1], h]).numpy().ravel())
+            refs.append(r[name].ravel())
+        errs[name] = rel(np.concatenate(gots), np.concatenate(refs))
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, errs
+    return errs
+
+
+@pytest.mark.parametrize("lens", [[64], [130], [200, 1, 64, 129]])
+def test_bwd_bf16_ragged(kda, lens):
+    b = make_seq_batch(lens, heads=3, io_dtype="bf16", seed=100 + sum(lens), h0=True, grad=True)
+    check_bwd(kda, b, TOL["bf16"])
+
+
+def test_bwd_many_heads(kda):
+    b = make_seq_batch([150, 90], heads=96, io_dtype="bf16", seed=101, h0=True, grad=True)
+    check_bwd(kda, b, TOL["bf16"], tasks=[(0, 0), (0, 57), (1, 95)])
+
+
+def test_bwd_is_deterministic(kda):
+    b = make_seq_batch([300], heads=2, io_dtype="bf16", seed=102, h0=True, grad=True)
+    t, o, hT, saved = run_fwd(kda, b, save=True)
+    g1 = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, None, t["h0"])
+    g2 = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, None, t["h0"])
+    for name in g1:
+        assert torch.equal(g1[name], g2[name]), name
+
+
+# ---------------------------------------------------------------- decode
+
+def check_step(kda, d, tol):
+    dev = "cuda"
+    st = d.state.to(dev)
+    o = kda.kda_step(d.q.to(dev), d.k.to(dev), d.v.to(dev), d.beta.to(dev), d.g.to(dev), st,
+                     d.accept_len.to(dev))
+    torch.cuda.synchronize()
+    N, L, H, _ = d.q.shape
+    res = oracle.step(d.q, d.k, d.v, d.beta, d.g, d.state, d.accept_len)
+    o_ref = np.stack([np.stack([res[(i, h)][0] for h in range(H)], 1) for i in range(N)])
+    s_ref = np.stack([np.stack([res[(i, h)][1] for h in range(H)], 0) for i in range(N)])
+    e_o, e_s = rel(o.float().cpu(), o_ref), rel(st.cpu(), s_ref)
+    assert e_o <= tol and e_s <= tol, (e_o, e_s)
+
+
+@pytest.mark.parametrize("N,L", [(5, 4), (3, 1), (2, 8)])
+def test_step_bf16(kda, N, L):
+    check_step(kda, make_decode_batch(N, L, 3, "bf16", seed=N * 10 + L), TOL["bf16"])
+
+
+def test_step_f32(kda):
+    check_step(kda, make_decode_batch(4, 4, 2, "f32", seed=3), TOL["f32"])
+
+
+def test_step_accept_zero_leaves_state(kda):
+    d = make_decode_batch(3, 4, 2, "bf16", seed=4)
+    d.accept_len[:] = torch.tensor([0, 4, 0], dtype=torch.int32)
+    st = d.state.clone().cuda()
+    kda.kda_step(d.q.cuda(), d.k.cuda(), d.v.cuda(), d.beta.cuda(), d.g.cuda(), st, d.accept_len.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(st[0].cpu(), d.state[0]) and torch.equal(st[2].cpu(), d.state[2])
+    check_step(kda, d, TOL["bf16"])
+
+
+def test_step_equals_forward(kda):
+    d = make_decode_batch(2, 4, 2, "bf16", seed=5)
+    d.accept_len[:] = 4
+    st = d.state.clone().cuda()
+    o = kda.kda_step(d.q.cuda(), d.k.cuda(), d.v.cuda(), d.beta.cuda(), d.g.cuda(), st)
+    for i in range(2):
+        of, hf, _ = kda.kda_fwd(d.q[i].cuda(), d.k[i].cuda(), d.v[i].cuda(), d.beta[i].cuda(), d.g[i].cuda(),
+                                None, d.state[i:i + 1].cuda())
+        torch.cuda.synchronize()
+        assert rel(o[i].float().cpu(), of.float().cpu()) < 1e-2
+        assert rel(st[i].cpu(), hf[0].cpu()) < 1e-2

@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA hot path on GB300.
+
+One step = one chunked forward (saving chunk-start states) plus the matching
+backward over the fwd+bwd workload B=1, T=32768, H=96, d=128 (bf16 I/O, fp32
+state and gradients, nonzero initial state), through the C ABI with buffers
+resident in HBM. The decode/verify workload (256 sequences x 96 heads, 4 tokens
+per call) is measured in the same run and reported under "decode".
+
+Prints ONE JSON line (rank 0). Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run under torch.distributed.run: every rank runs an independent
+replica on its own GPU (weak scaling; the heads and sequences of KDA are
+independent, so there is no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "fwdbwd-bf16-T32768-H96"
+DECODE = "decode-bf16-N256-L4-H96"
+D = 128
+# algorithmic bytes per token and head (inputs read once, outputs written once)
+FWD_BYTES = 3 * 256 + 512 + 4 + 256          # q,k,v bf16 + g fp32 + beta + o bf16        = 1540
+BWD_BYTES = 3 * 256 + 512 + 4 + 256 + 3 * 512 + 512 + 4   # + dO, dq/dk/dv/dg fp32, dbeta = 3592
+FWD_FLOP = 10 * 64 * D + 6 * D * D           # 180,224
+BWD_FLOP = 24 * 64 * D + 12 * D * D          # 393,216
+DEC_BYTES = 2 * D * D * 4 + 4 * (3 * 256 + 512 + 4 + 256)   # per (sequence, head) per 4-token call
+# per-kernel share of the algorithmic bytes (which kernel reads/writes which tensor)
+KERNEL_BYTES = {
+    "fwd.prep": 256 + 256 + 512 + 4,         # q, k, g, beta
+    "fwd.scan": 256 + 256,                   # v in, o out
+    "bwd.prep": 256 + 256 + 512 + 4,         # q, k, g, beta
+    "bwd.dscan": 256 + 512,                  # dO in, dv out
+    "bwd.state": 256,                        # v
+    "bwd.intra": 3 * 512 + 4,                # dq, dk, dg, dbeta out
+}
+FWD_STAGES = ["fwd.table", "fwd.prep", "fwd.scan"]
+BWD_STAGES = ["bwd.table", "bwd.prep", "bwd.dscan", "bwd.state", "bwd.intra"]
+KERNEL_SRC = {"fwd.prep": "kda_prep.cu", "fwd.scan": "kda_scan.cu", "bwd.prep": "kda_prep.cu",
+              "bwd.dscan": "kda_scan.cu", "bwd.state": "kda_bwd.cu", "bwd.intra": "kda_bwd.cu",
+              "decode": "kda_step.cu"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def src_hash(name):
+    path = os.path.join(ROOT, "gated_delta_rule_chunked_gb300", "csrc", name)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:12]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged.
+
+    Summaries under profiles/ carry lines `traffic <kernel> <bytes_per_launch> <source-sha12> <scale>`.
+    """
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".txt", ".md")):
+            continue
+        for line in open(os.path.join(pdir, fn)):
+            m = re.match(r"^traffic\s+(\S+)\s+([0-9.eE+]+)\s+([0-9a-f]{12})", line.strip())
+            if m and m.group(1) == kernel and m.group(3) == src_hash(KERNEL_SRC[kernel]):
+                return float(m.group(2))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.06)
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        mhz = [float(r[0]) for r in rows if len(r) >= 8 and r[0].strip().replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if len(r) >= 8 and r[1].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows if len(r) >= 8 for i in range(4) if "Active" in r[4 + i]
+                          and "Not" not in r[4 + i]})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- ours
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import gated_delta_rule_chunked_gb300 as kda
+    from gated_delta_rule_chunked_gb300 import _lib
+    from gated_delta_rule_chunked_gb300.inputs import make_workload
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = kda.library()
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    b = make_workload(WORKLOAD, device=dev)
+    T, H, N = b.total, b.heads, b.n_seqs
+    f32 = dict(dtype=torch.float32, device=dev)
+    o = torch.empty_like(b.v)
+    hT = torch.empty((N, H, D, D), **f32)
+    fa = kda.fwd_args(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, o, hT, None, None)
+    saved = torch.empty(lib.kda_saved_size(C.byref(fa)), dtype=torch.uint8, device=dev)
+    fws = torch.empty(lib.kda_fwd_workspace_size(C.byref(fa)), dtype=torch.uint8, device=dev)
+    fa = kda.fwd_args(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, o, hT, saved, fws)
+    grads = {n: torch.empty(s, **f32) for n, s in
+             (("dq", b.q.shape), ("dk", b.k.shape), ("dv", b.v.shape), ("dg", b.g.shape), ("dbeta", b.beta.shape),
+              ("dh0", (N, H, D, D)))}
+    ba = kda.bwd_args(fa, b.dO, grads["dq"], grads["dk"], grads["dv"], grads["dbeta"], grads["dg"], grads["dh0"])
+    bws = torch.empty(lib.kda_bwd_workspace_size(C.byref(ba)), dtype=torch.uint8, device=dev)
+    ba = kda.bwd_args(fa, b.dO, grads["dq"], grads["dk"], grads["dv"], grads["dbeta"], grads["dg"], grads["dh0"],
+                      None, bws)
+
+    # per-kernel events: [start, fwd stages..., bwd stages...] per step
+    nst = 1 + len(FWD_STAGES) + len(BWD_STAGES)
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record(stream)          # materialise the events so their handles exist
+    torch.cuda.synchronize(dev)
+    arrays = [((C.c_void_p * len(FWD_STAGES))(*[e.cuda_event for e in row[1:1 + len(FWD_STAGES)]]),
+               (C.c_void_p * len(BWD_STAGES))(*[e.cuda_event for e in row[1 + len(FWD_STAGES):]])) for row in evs]
+
+    def step(i=None):
+        if i is not None:
+            lib.kda_set_profile_events(C.cast(arrays[i][0], C.c_void_p), len(FWD_STAGES))
+        _lib.check(lib.kda_fwd(C.byref(fa), sptr))
+        if i is not None:
+            lib.kda_set_profile_events(C.cast(arrays[i][1], C.c_void_p), len(BWD_STAGES))
+        _lib.check(lib.kda_bwd(C.byref(ba), sptr))
+        if i is not None:
+            lib.kda_set_profile_events(None, 0)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(K):
+        evs[i][0].record(stream)
+        step(i)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_step_local = t_start.elapsed_time(t_end) / K
+    barrier(world)
+    ck = clocks.stop() if clocks else None
+    ms_step = reduce_max(ms_step_local, world)
+
+    # per-kernel device time (mean over steps)
+    names = ["start"] + FWD_STAGES + BWD_STAGES
+    per = {n: 0.0 for n in names[1:]}
+    for row in evs:
+        for j in range(1, nst):
+            per[names[j]] += row[j - 1].elapsed_time(row[j]) / K
+    fwd_ms = sum(per[n] for n in FWD_STAGES)
+    bwd_ms = sum(per[n] for n in BWD_STAGES)
+
+    peaks = load_peaks()
+    tok = T
+    units = T * H
+    dom = max(KERNEL_BYTES, key=lambda n: per[n])
+    dom_bytes = KERNEL_BYTES[dom] * units
+    achieved = dom_bytes / (per[dom] * 1e-3) / 1e9
+    traffic = recorded_traffic(dom)
+    step_bytes = (FWD_BYTES + BWD_BYTES) * units
+    out = {
+        "metric": "KDA fwd+bwd tokens/s (H=96, d=128, T=32768, bf16 I/O, fp32 state/grads)",
+        "value": world * tok / (ms_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,k,v,dO ~ N(0,1) bf16, beta=sigmoid(N(0,1)), g=logsigmoid(N(3,1)), h0 ~ N(0,0.02))",
+        "config": {"workload": WORKLOAD, "batch": N, "seq_len": T, "heads": H, "head_dim": D, "chunk": 64,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs (4.8 GB) larger than L2; no flush"},
+        "fwd": {"ms": fwd_ms, "tokens_per_s": tok / (fwd_ms * 1e-3),
+                "gbs_algorithmic": FWD_BYTES * units / (fwd_ms * 1e-3) / 1e9,
+                "roofline_frac": FWD_BYTES * units / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "bwd": {"ms": bwd_ms, "tokens_per_s": tok / (bwd_ms * 1e-3),
+                "gbs_algorithmic": BWD_BYTES * units / (bwd_ms * 1e-3) / 1e9,
+                "roofline_frac": BWD_BYTES * units / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "kernels_ms": {k: round(v, 4) for k, v in per.items()},
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom_bytes, "peak_source": peaks["source"]},
+        "roofline_step": {"bound": "hbm", "achieved": step_bytes / (ms_step * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                          "unit": "GB/s", "frac": step_bytes / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                          "flop_frac_of_bf16": (FWD_FLOP + BWD_FLOP) * units / (ms_step * 1e-3) / 1e12
+                          / peaks["bf16_tflops_sustained"]},
+        "gpu_launches": K * (len(FWD_STAGES) + len(BWD_STAGES)),
+        "clocks": ck,
+    }
+    host = None
+    if not args.no_e2e:
+        host = {n: getattr(b, n).to("cpu").pin_memory() for n in ("q", "k", "v", "beta", "g", "h0", "dO")}
+        host["cu_seqlens"] = b.cu_seqlens.to("cpu")
+    del b, grads, saved, fws, bws, o, hT
+    torch.cuda.empty_cache()
+    if not args.no_decode:
+        out["decode"] = bench_decode(args, dev, lib, stream, peaks)
+    if host is not None:
+        out["e2e"] = bench_e2e(args, dev, world, host)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args)
+    return out
+
+
+def bench_decode(args, dev, lib, stream, peaks):
+    import torch
+    import gated_delta_rule_chunked_gb300 as kda
+    from gated_delta_rule_chunked_gb300 import _lib
+    from gated_delta_rule_chunked_gb300.inputs import make_workload
+    d = make_workload(DECODE, device=dev)
+    N, L, H, _ = d.q.shape
+    o = torch.empty_like(d.v)
+    a = kda.step_args(d.q, d.k, d.v, d.beta, d.g, d.state, d.accept_len, o)
+    sptr = stream.cuda_stream
+    K = max(args.steps, 20)
+    for _ in range(max(args.warmup, 3)):
+        _lib.check(lib.kda_step(C.byref(a), sptr))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    s.record(stream)
+    for _ in range(K):
+        _lib.check(lib.kda_step(C.byref(a), sptr))
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e) / K
+    gbs = DEC_BYTES * N * H / (ms * 1e-3) / 1e9
+    return {"workload": DECODE, "ms_per_call": ms, "gbs_algorithmic": gbs, "unit": "GB/s",
+            "roofline": {"kernel": "decode", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("decode")},
+            "tokens_per_s": N * L / (ms * 1e-3), "gpu_launches": K,
+            "state_bytes": N * H * D * D * 4, "l2": "state (1.6 GB) larger than L2; no flush"}
+
+
+def bench_e2e(args, dev, world, host):
+    """Same step through the public Python API with host buffers: pinned H2D of the
+    step's inputs, kda_fwd + kda_bwd, D2H of the gradients, all inside the timed region."""
+    import torch
+    import gated_delta_rule_chunked_gb300 as kda
+    names = ("q", "k", "v", "beta", "g", "h0", "dO")
+    cu = host.pop("cu_seqlens")
+    total = host["q"].shape[0]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    outs_host = None
+    K = max(2, min(args.steps, 5))
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        nonlocal outs_host
+        t = {n: host[n].to(dev, non_blocking=True) for n in names}
+        o, hT, saved = kda.kda_fwd(t["q"], t["k"], t["v"], t["beta"], t["g"], cu, t["h0"], save=True)
+        gr = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, cu, t["h0"])
+        if outs_host is None:
+            outs_host = {n: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for n, v in gr.items()}
+        for n, v in gr.items():
+            outs_host[n].copy_(v, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    d2h = sum(v.numel() * v.element_size() for v in outs_host.values())
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(K):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e) / K
+    ms = reduce_max(ms, world)
+    return {"value": world * total / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K}
+
+
+# ----------------------------------------------------------------------------- oracle
+def cpu_baseline(args, steps=1, sample_tokens=None):
+    """The fp64 oracle as it stands, timed on this host's cores on a bounded sample of
+    the same workload: the first `sample_tokens` tokens of as many heads as cores."""
+    import torch
+    import oracle
+    from gated_delta_rule_chunked_gb300.inputs import make_seq_batch
+    cores = oracle.default_threads()
+    Ts = sample_tokens or args.cpu_sample_tokens
+    heads = cores
+    b = make_seq_batch([Ts], heads=heads, io_dtype="bf16", seed=1002, h0=True, grad=True)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, n_threads=cores)
+        oracle.bwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.dO, b.h0, n_threads=cores)
+    el = (time.perf_counter() - t0) / steps
+    # tokens/s of the full 96-head workload = sampled token-heads per second / 96
+    val = Ts * heads / el / 96
+    return {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fwd+bwd of the first {Ts} tokens of {heads} heads (one head per core) of {WORKLOAD}; "
+                      f"value = sampled token-heads per second / 96 heads", "seconds": el}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    ms = []
+    for _ in range(args.warmup):
+        cpu_baseline(args, sample_tokens=args.ref_sample_tokens)
+    for _ in range(args.steps):
+        r = cpu_baseline(args, sample_tokens=args.ref_sample_tokens)
+        ms.append(r["seconds"] * 1e3)
+    ms_step = statistics.mean(ms)
+    cores = r["cores"]
+    val = args.ref_sample_tokens * cores / (ms_step * 1e-3) / 96
+    return {"impl": "reference", "metric": "KDA fwd+bwd tokens/s (H=96, d=128, T=32768, bf16 I/O, fp32 state/grads)",
+            "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded, same recipe)",
+            "config": {"workload": WORKLOAD, "seq_len": 32768, "heads": 96, "head_dim": D},
+            "cpu_baseline": {"kind": "oracle", "cores": cores, "value": val, "unit": "tokens/s",
+                             "sample": r["sample"]},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------- dist
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=16384)
+    ap.add_argument("--ref-sample-tokens", type=int, default=2048)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "ours":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        if args.warmup < 3:
+            raise SystemExit("--warmup must be >= 3")
+        out = run_ours(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -19,6 +19,12 @@
 namespace {
 
 thread_local std::string g_last_error;
+cudaEvent_t *g_prof_events = nullptr;
+int g_prof_n = 0;
+
+void mark(int i, cudaStream_t s) {
+  if (g_prof_events && i < g_prof_n) cudaEventRecord(g_prof_events[i], s);
+}
 
 kda_status fail(kda_status s, const char *fmt, const char *what = "") {
   char buf[512];
@@ -127,6 +133,11 @@ extern "C" {
 
 int32_t kda_abi_version(void) { return 1; }
 
+void kda_set_profile_events(cudaEvent_t *events, int32_t n_events) {
+  g_prof_events = events;
+  g_prof_n = events ? n_events : 0;
+}
+
 const char *kda_last_error(void) { return g_last_error.c_str(); }
 
 size_t kda_fwd_workspace_size(const kda_fwd_args *a) {
@@ -140,8 +151,11 @@ size_t kda_saved_size(const kda_fwd_args *a) {
 }
 
 size_t kda_bwd_workspace_size(const kda_bwd_args *a) {
-  if (!a || check_fwd(&a->fwd, "kda_bwd_workspace_size") != KDA_OK) return 0;
-  return plan(&a->fwd, true).bytes;
+  if (!a) return 0;
+  kda_fwd_args f = a->fwd;
+  if (!f.o) f.o = a->dq;   // o is not used by the backward
+  if (check_fwd(&f, "kda_bwd_workspace_size") != KDA_OK) return 0;
+  return plan(&f, true).bytes;
 }
 
 kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
@@ -167,10 +181,13 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
                                           reinterpret_cast<int *>(ws + w.cu), reinterpret_cast<int *>(ws + w.choff),
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_fwd chunk table");
+  mark(0, stream);
   kda::PrepParams pp{geo, a->q, a->k, a->g, a->beta, a->scale, ws + w.img, a->dev_status};
   if ((e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
+  mark(1, stream);
   kda::FwdScanParams sp{geo, a->v, ws + w.img, a->h0, a->o, a->hT, a->saved, a->dev_status};
   if ((e = kda::launch_fwd_scan(sp, f32, pick_slice(a), stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd scan");
+  mark(2, stream);
   g_last_error.clear();
   return KDA_OK;
 }
@@ -213,17 +230,22 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
                                           reinterpret_cast<int *>(ws + w.cu), reinterpret_cast<int *>(ws + w.choff),
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_bwd chunk table");
+  mark(0, stream);
   kda::PrepParams pp{geo, f->q, f->k, f->g, f->beta, f->scale, ws + w.img, f->dev_status};
   if ((e = kda::launch_prep(pp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd prep");
+  mark(1, stream);
   kda::BwdScanParams bp{geo, a->dO, ws + w.img, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
   if ((e = kda::launch_bwd_scan(bp, false, pick_slice(f), stream)) != cudaSuccess)
     return cuda_fail(e, "kda_bwd dS scan");
+  mark(2, stream);
   kda::BwdStateParams sp{geo, f->v, a->dO, ws + w.img, f->saved, ws + w.dsaved,
                          reinterpret_cast<float *>(ws + w.grad), f->dev_status};
   if ((e = kda::launch_bwd_state(sp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd state grads");
+  mark(3, stream);
   kda::BwdIntraParams ip{geo, f->q, f->k, f->g, f->beta, f->scale, reinterpret_cast<const float *>(ws + w.grad),
                          a->dq, a->dk, a->dg, a->dbeta, f->dev_status};
   if ((e = kda::launch_bwd_intra(ip, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd intra grads");
+  mark(4, stream);
   g_last_error.clear();
   return KDA_OK;
 }
@@ -251,6 +273,7 @@ kda_status kda_step(const kda_step_args *a, cudaStream_t stream) {
                     a->accept_len, a->o};
   cudaError_t e = kda::launch_step(p, a->io_dtype == KDA_F32, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_step");
+  mark(0, stream);
   g_last_error.clear();
   return KDA_OK;
 }

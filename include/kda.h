@@ -144,6 +144,17 @@ size_t kda_bwd_workspace_size(const kda_bwd_args *args);
  * section, speculative decoding paragraph). Needs no workspace. */
 kda_status kda_step(const kda_step_args *args, cudaStream_t stream);
 
+/* Per-kernel timing hook for benchmarks. When `events` is not NULL, every later
+ * kda_fwd / kda_bwd / kda_step call records events[i] on its stream right after
+ * enqueueing its i-th kernel (i < n_events): kda_fwd has 3 kernels (chunk table,
+ * chunk prep, state scan), kda_bwd 5 (chunk table, chunk prep, reverse dS scan,
+ * state-side gradients, intra-chunk gradients), kda_step 1. Elapsed times
+ * between consecutive events (and one the caller records before the call) give
+ * each kernel's device time. The caller owns the events and the array, which
+ * must stay valid until the hook is cleared with kda_set_profile_events(NULL, 0).
+ * Process-wide, not thread-safe; meant for single-threaded benchmarking. */
+void kda_set_profile_events(cudaEvent_t *events, int32_t n_events);
+
 /* Message of the last error on the calling host thread ("" if none). */
 const char *kda_last_error(void);
 

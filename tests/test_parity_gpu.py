@@ -206,3 +206,61 @@ def test_step_equals_forward(kda):
         torch.cuda.synchronize()
         assert rel(o[i].float().cpu(), of.float().cpu()) < 1e-2
         assert rel(st[i].cpu(), hf[0].cpu()) < 1e-2
+
+
+# ---------------------------------------------------------------- full-size workloads (sampled)
+
+def _sampled(b, heads):
+    """CPU copies of the inputs restricted to the sampled heads (all tokens)."""
+    from gated_delta_rule_chunked_gb300.inputs import SeqBatch
+    pick = lambda t: None if t is None else t[:, heads].cpu()
+    return SeqBatch(pick(b.q), pick(b.k), pick(b.v), pick(b.beta), pick(b.g), b.cu_seqlens.cpu(),
+                    None if b.h0 is None else b.h0[:, heads].cpu(), pick(b.dO))
+
+
+@pytest.mark.parametrize("name,tasks", [
+    ("fwdbwd-bf16-T32768-H96", [(0, 0), (0, 95)]),
+    ("fwdbwd-bf16-varlen8-T131072-H96", [(0, 1), (7, 94)]),
+])
+def test_fullsize_fwd_bwd_sampled(kda, name, tasks):
+    dev = torch.device("cuda")
+    b = make_workload(name, device=dev)
+    heads = sorted({h for _, h in tasks})
+    o, hT, saved = kda.kda_fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, save=True)
+    gr = kda.kda_bwd(b.q, b.k, b.v, b.beta, b.g, b.dO, saved, b.cu_seqlens, b.h0)
+    torch.cuda.synchronize()
+    s = _sampled(b, heads)
+    cu = [int(x) for x in b.cu_seqlens.tolist()]
+    otasks = [(i, heads.index(h)) for i, h in tasks]
+    fres = oracle.fwd(s.q, s.k, s.v, s.beta, s.g, s.cu_seqlens, s.h0, tasks=otasks)
+    bres = oracle.bwd(s.q, s.k, s.v, s.beta, s.g, s.cu_seqlens, s.dO, s.h0, tasks=otasks)
+    errs = {}
+    for (i, h), (i2, hh) in zip(tasks, otasks):
+        sl = slice(cu[i], cu[i + 1])
+        pairs = {"o": (o[sl, h].float().cpu(), fres[(i2, hh)][0]), "hT": (hT[i, h].cpu(), fres[(i2, hh)][1])}
+        for n in ("dq", "dk", "dv", "dg", "dbeta"):
+            pairs[n] = (gr[n][sl, h].cpu(), bres[(i2, hh)][n])
+        pairs["dh0"] = (gr["dh0"][i, h].cpu(), bres[(i2, hh)]["dh0"])
+        for n, (g_, r_) in pairs.items():
+            errs[f"{n}[{i},{h}]"] = rel(g_, r_)
+    bad = {k: v for k, v in errs.items() if not v <= TOL["bf16"]}
+    print(name, {k: f"{v:.2e}" for k, v in errs.items()})
+    assert not bad, errs
+
+
+def test_fullsize_decode_sampled(kda):
+    dev = torch.device("cuda")
+    d = make_workload("decode-bf16-N256-L4-H96", device=dev)
+    st = d.state.clone()
+    o = kda.kda_step(d.q, d.k, d.v, d.beta, d.g, st, d.accept_len)
+    torch.cuda.synchronize()
+    seqs = [0, 17, 128, 255]
+    heads = [0, 33, 95]
+    sub = lambda t: t[seqs][:, :, heads].cpu() if t.dim() >= 3 else t[seqs].cpu()
+    res = oracle.step(sub(d.q), sub(d.k), sub(d.v), sub(d.beta), sub(d.g), d.state[seqs][:, heads].cpu(),
+                      d.accept_len[seqs].cpu())
+    go = np.stack([[o[i, :, h].float().cpu().numpy() for h in heads] for i in seqs])
+    ro = np.stack([[res[(a, b_)][0] for b_ in range(len(heads))] for a in range(len(seqs))])
+    gs = np.stack([[st[i, h].cpu().numpy() for h in heads] for i in seqs])
+    rs = np.stack([[res[(a, b_)][1] for b_ in range(len(heads))] for a in range(len(seqs))])
+    assert rel(go, ro) <= TOL["bf16"] and rel(gs, rs) <= TOL["bf16"], (rel(go, ro), rel(gs, rs))

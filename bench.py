@@ -133,7 +133,7 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
 
-    b = make_workload(WORKLOAD, device=dev)
+    b = make_workload(WORKLOAD, device=dev, **({"seq_lens": (args.seq_len,)} if args.seq_len else {}))
     T, H, N = b.total, b.heads, b.n_seqs
     f32 = dict(dtype=torch.float32, device=dev)
     o = torch.empty_like(b.v)
@@ -234,6 +234,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": K * (len(FWD_STAGES) + len(BWD_STAGES)),
         "clocks": ck,
     }
+    if args.seq_len:
+        out["config"]["workload"] += f" (T overridden to {T})"
     host = None
     if not args.no_e2e:
         host = {n: getattr(b, n).to("cpu").pin_memory() for n in ("q", "k", "v", "beta", "g", "h0", "dO")}
@@ -389,6 +391,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16384)
     ap.add_argument("--ref-sample-tokens", type=int, default=2048)
+    ap.add_argument("--seq-len", type=int, default=0, help="override T (profiling runs only)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

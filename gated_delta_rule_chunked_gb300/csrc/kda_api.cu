@@ -182,7 +182,7 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_fwd chunk table");
   mark(0, stream);
-  kda::PrepParams pp{geo, a->q, a->k, a->g, a->beta, a->scale, ws + w.img, a->dev_status};
+  kda::PrepParams pp{geo, a->q, a->k, a->g, a->beta, a->scale, ws + w.img, nullptr, a->dev_status};
   if ((e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
   kda::FwdScanParams sp{geo, a->v, ws + w.img, a->h0, a->o, a->hT, a->saved, a->dev_status};
@@ -231,7 +231,7 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_bwd chunk table");
   mark(0, stream);
-  kda::PrepParams pp{geo, f->q, f->k, f->g, f->beta, f->scale, ws + w.img, f->dev_status};
+  kda::PrepParams pp{geo, f->q, f->k, f->g, f->beta, f->scale, ws + w.img, nullptr, f->dev_status};
   if ((e = kda::launch_prep(pp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd prep");
   mark(1, stream);
   kda::BwdScanParams bp{geo, a->dO, ws + w.img, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};

@@ -50,6 +50,7 @@ struct PrepParams {
   const float *g, *beta;
   float scale;
   void *img;               // [max_chunks][H] ImgLayout records
+  float *aux;              // optional [max_chunks][H] x {A (strict lower), T} fp32 64x64 each
   int *status;
 };
 

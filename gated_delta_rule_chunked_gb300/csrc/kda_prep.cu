@@ -6,13 +6,24 @@
 //   2. the gate scan G_r = sum_{i<=r} g_i per key channel, restarted per chunk
 //      (kept in log2 units);
 //   3. the gated Gram blocks A_rj = sum_c k^_rc k^_jc exp(G_rc-G_jc) (j<r) and
-//      B_rj = sum_c q^_rc k^_jc exp(G_rc-G_jc) (j<=r) on tensor cores;
-//   4. the WY/UT transform T = (I + Diag(beta) A)^-1 (fp32 block substitution);
+//      B_rj = sum_c q^_rc k^_jc exp(G_rc-G_jc) (j<=r) on TF32 tensor cores
+//      (these dot products cancel heavily, so bf16 operands are not enough);
+//   4. the WY/UT transform T = (I + Diag(beta) A)^-1 (16x16 diagonal blocks by
+//      forward substitution, off-diagonal blocks by TF32 block products);
 //   5. the operands the sequential state scan needs, written as one record.
 //
-// The gating factorisation used by the Gram products is described in kda_intra.cuh.
+// Gating factorisation. exp(G_r - G_j) is split into two bounded factors so the
+// Gram products run as plain matrix multiplies. With 16-token sub-blocks and
+// E_a = G at the last row of sub-block a (E_-1 = 0), for r in sub-block a and j
+// in sub-block b <= a:
+//   exp(G_r - G_j) = exp(G_r - E_{a-1}) * exp(E_b - G_j) * exp(E_{a-1} - E_b)
+// The first two factors are <= 1 (one per row, stored once), the third is a
+// per-channel vector per sub-block pair: <= 1 for b < a and, for b = a,
+// exp(-(sum of g over the sub-block)), which the library's precondition
+// (16-token gate sums >= -80) keeps finite. Within a sub-block the local running
+// sum of g gives G_r - E_{a-1} directly, so no large G is ever subtracted.
+// This is this library's kernel design, not taken from the pages.
 #include "kda_common.cuh"
-#include "kda_intra.cuh"
 #include "kda_internal.h"
 
 namespace kda {
@@ -61,109 +72,346 @@ cudaError_t launch_chunk_table(const int *cu_in, int n_seqs, long long total, in
 }
 
 // ------------------------------------------------------------ the prep kernel
+constexpr int PREP_THREADS = 256;
+constexpr int LDF = 132;   // padded fp32 row of the 64x128 factor tiles (conflict-free fragments)
+constexpr int LDS64 = 68;  // padded fp32 row of 64x64 tiles
+constexpr int LDP = 24;    // padded fp32 row of the 16x16 solver scratch
+
 template <typename E>
-__global__ void __launch_bounds__(128) kda_prep_kernel(PrepParams p) {
-  using S = PrepSmem<E>;
+struct PrepSmem2 {
+  static constexpr int TILE = 64 * LDF * 4;
+  static constexpr int KL = 0, QL = TILE, R = 2 * TILE;     // fp32 [64][LDF] each
+  static constexpr int DV = 3 * TILE;                        // fp32 [10][128] pair factors
+  static constexpr int TOT = DV + 10 * 512;                  // fp32 [4][128] sub-block gate sums
+  static constexpr int RQ = TOT + 4 * 512, RK = RQ + 256, BETA = RK + 256;
+  static constexpr int BYTES = BETA + 256;
+  // after the Gram products (KL, QL, R are dead)
+  static constexpr int LM = 0;                               // fp32 [64][LDS64]  Diag(beta) A
+  static constexpr int TT = LM + 64 * LDS64 * 4;             // fp32 [64][LDS64]  T
+  static constexpr int SCR = TT + 64 * LDS64 * 4;            // fp32 4 x [16][LDP]
+  static constexpr int BM = R;                               // E record tile [64][64]
+  static constexpr int TB = R + 64 * 64 * (int)sizeof(E);    // E record tile [64][64]
+  static_assert(SCR + 4 * 16 * LDP * 4 <= R, "solver tiles overlap the staging tiles");
+  static_assert(TB + 64 * 64 * (int)sizeof(E) <= DV, "staging tiles overlap the vectors");
+};
+
+__device__ __forceinline__ void pair_of(int p, int &a, int &b) {
+  a = p >= 6 ? 3 : (p >= 3 ? 2 : (p >= 1 ? 1 : 0));
+  b = p - a * (a + 1) / 2;
+}
+
+// acc[nt] (16 rows x 16 cols) += X[16 rows][0:128] * (R[16 rows][0:128] * dvec)^T
+template <bool PRECISE>
+__device__ __forceinline__ void gram16(float (&acc)[2][4], const float *X, const float *Rr, const float *dvec) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  if constexpr (PRECISE) {
+    for (int c = 0; c < 128; ++c) {
+      const float x0 = X[g * LDF + c], x1 = X[(g + 8) * LDF + c], d = dvec[c];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float r0 = Rr[(8 * nt + 2 * q) * LDF + c] * d, r1 = Rr[(8 * nt + 2 * q + 1) * LDF + c] * d;
+        acc[nt][0] = fmaf(x0, r0, acc[nt][0]);
+        acc[nt][1] = fmaf(x0, r1, acc[nt][1]);
+        acc[nt][2] = fmaf(x1, r0, acc[nt][2]);
+        acc[nt][3] = fmaf(x1, r1, acc[nt][3]);
+      }
+    }
+  } else {
+#pragma unroll 4
+    for (int kk = 0; kk < 128; kk += 8) {
+      uint32_t a[4];
+      a[0] = tf32(X[g * LDF + kk + q]);
+      a[1] = tf32(X[(g + 8) * LDF + kk + q]);
+      a[2] = tf32(X[g * LDF + kk + q + 4]);
+      a[3] = tf32(X[(g + 8) * LDF + kk + q + 4]);
+      const float d0 = dvec[kk + q], d1 = dvec[kk + q + 4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float *rr = Rr + (8 * nt + g) * LDF + kk;
+        mma1688(acc[nt], a, tf32(rr[q] * d0), tf32(rr[q + 4] * d1));
+      }
+    }
+  }
+}
+
+// acc (16x16) += A[16][16] * B[16][16], row-major fp32 with leading dims lda, ldb.
+template <bool PRECISE>
+__device__ __forceinline__ void mm16(float (&acc)[2][4], const float *A, int lda, const float *B, int ldb) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  if constexpr (PRECISE) {
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k) {
+      const float a0 = A[g * lda + k], a1 = A[(g + 8) * lda + k];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float b0 = B[k * ldb + 8 * nt + 2 * q], b1 = B[k * ldb + 8 * nt + 2 * q + 1];
+        acc[nt][0] = fmaf(a0, b0, acc[nt][0]);
+        acc[nt][1] = fmaf(a0, b1, acc[nt][1]);
+        acc[nt][2] = fmaf(a1, b0, acc[nt][2]);
+        acc[nt][3] = fmaf(a1, b1, acc[nt][3]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < 16; kk += 8) {
+      uint32_t a[4];
+      a[0] = tf32(A[g * lda + kk + q]);
+      a[1] = tf32(A[(g + 8) * lda + kk + q]);
+      a[2] = tf32(A[g * lda + kk + q + 4]);
+      a[3] = tf32(A[(g + 8) * lda + kk + q + 4]);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+        mma1688(acc[nt], a, tf32(B[(kk + q) * ldb + 8 * nt + g]), tf32(B[(kk + q + 4) * ldb + 8 * nt + g]));
+    }
+  }
+}
+
+template <typename E>
+__global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p) {
+  using S = PrepSmem2<E>;
+  constexpr bool PRECISE = sizeof(E) == 4;   // fp32 I/O: exact fp32 products
   extern __shared__ __align__(128) char smem[];
   const int chunk = blockIdx.x, h = blockIdx.y, H = p.geo.heads;
   ChunkRef ref;
   if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) return;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g8 = lane >> 2, q4 = lane & 3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+  const E *qg = (const E *)p.q, *kg = (const E *)p.k;
+  float *rq = (float *)(smem + S::RQ), *rk = (float *)(smem + S::RK), *sb = (float *)(smem + S::BETA);
+  float *KL = (float *)(smem + S::KL), *QL = (float *)(smem + S::QL), *RR = (float *)(smem + S::R);
+  float(*dv)[128] = (float(*)[128])(smem + S::DV);
+  float(*tot)[128] = (float(*)[128])(smem + S::TOT);
+  const ImgLayout L(sizeof(E));
+  char *rec = (char *)p.img + ((size_t)chunk * H + h) * L.bytes;
 
-  load_chunk_qkg<E>(smem, (const E *)p.q, (const E *)p.k, p.g, p.beta, ref.t0, ref.len, h, H, 128);
-  __syncthreads();
-  row_norms<E>(smem, p.scale);
-  gate_scan<E>(smem);
-  __syncthreads();
-  factor_pass<E>(smem);
-  __syncthreads();
-
-  float accA[NSUB][2][4], accB[NSUB][2][4];
-  gram<E>(smem, warp, accA, accB);
-  __syncthreads();   // G and RD rows < 96 are free from here on
-
-  // epilogue: Lm = Diag(beta) A (strict lower, fp32), Bm = B (lower incl. diagonal)
+  // 1. row norms: 4 threads per row, 32 channels each
   {
-    Tile<float, 64> Lm((float *)(smem + S::A));
-    Tile<E, 64> Bm((E *)(smem + S::BM));
-    const float *sb = (const float *)(smem + S::BETA);
-    const int ap = warp;
+    const int r = tid >> 2, part = tid & 3;
+    float sq = 0.f, sk = 0.f;
+    if (r < ref.len) {
+      const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + part * 32;
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        const float2 a = ld2(qg + off + c), b = ld2(kg + off + c);
+        sq = fmaf(a.x, a.x, fmaf(a.y, a.y, sq));
+        sk = fmaf(b.x, b.x, fmaf(b.y, b.y, sk));
+      }
+    }
+    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+    sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+    if (part == 0) {
+      rq[r] = p.scale * rsqrtf(sq + 1e-6f);
+      rk[r] = rsqrtf(sk + 1e-6f);
+    }
+    if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
+  }
+  // 2. gate scan and factors: thread = (channel pair cp, sub-block a)
+  const int cp = tid & 63, a = tid >> 6, c0 = 2 * cp;
+  float2 cs[SUB];
+  {
+#pragma unroll
+    for (int i = 0; i < SUB; ++i) {
+      const int r = a * SUB + i;
+      cs[i] = make_float2(0.f, 0.f);
+      if (r < ref.len) cs[i] = *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + r) * H + h) * D + c0);
+    }
+    float2 run = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < SUB; ++i) {
+      run.x = fmaf(cs[i].x, LOG2E, run.x);
+      run.y = fmaf(cs[i].y, LOG2E, run.y);
+      cs[i] = run;                          // G_r - E_{a-1}, log2 units
+    }
+    tot[a][c0] = run.x;
+    tot[a][c0 + 1] = run.y;
+  }
+  __syncthreads();
+  {
+    // E_{a-1}, E_a, E_3 per channel (running sums of the sub-block totals)
+    float em[2] = {0.f, 0.f}, ea[2], e3[2] = {0.f, 0.f}, eb[2] = {0.f, 0.f};
 #pragma unroll
     for (int b = 0; b < NSUB; ++b) {
+      const float t0 = tot[b][c0], t1 = tot[b][c0 + 1];
+      if (b < a) { em[0] += t0; em[1] += t1; }
+      e3[0] += t0;
+      e3[1] += t1;
+    }
+    ea[0] = em[0] + tot[a][c0];
+    ea[1] = em[1] + tot[a][c0 + 1];
+    // pair factors D_{a,b} = 2^(E_{a-1} - E_b), b <= a
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+    for (int b = 0; b < NSUB; ++b) {
+      eb[0] += tot[b][c0];
+      eb[1] += tot[b][c0 + 1];
+      if (b <= a) {
+        const int pr = a * (a + 1) / 2 + b;
+        dv[pr][c0] = exp2f(em[0] - eb[0]);
+        dv[pr][c0 + 1] = exp2f(em[1] - eb[1]);
+      }
+    }
+    const float pa0 = exp2f(em[0]), pa1 = exp2f(em[1]);                       // exp(E_{a-1})
+    const float fa0 = exp2f(e3[0] - ea[0]), fa1 = exp2f(e3[1] - ea[1]);       // exp(E_3 - E_a)
+    const float ta0 = tot[a][c0], ta1 = tot[a][c0 + 1];   // E_a - E_{a-1}
+    Tile<E, 128> tqt((E *)(rec + L.qt)), tkt((E *)(rec + L.kt)), tkh((E *)(rec + L.kh));
+#pragma unroll
+    for (int i = 0; i < SUB; ++i) {
+      const int r = a * SUB + i;
+      float2 qv = make_float2(0.f, 0.f), kv = qv;
+      if (r < ref.len) {
+        const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + c0;
+        qv = ld2(qg + off);
+        kv = ld2(kg + off);
+      }
+      const float x0 = exp2f(cs[i].x), x1 = exp2f(cs[i].y);
+      const float y0 = exp2f(ta0 - cs[i].x), y1 = exp2f(ta1 - cs[i].y);
+      const float qh0 = qv.x * rq[r], qh1 = qv.y * rq[r], kh0 = kv.x * rk[r], kh1 = kv.y * rk[r];
+      const float kl0 = kh0 * x0, kl1 = kh1 * x1, ql0 = qh0 * x0, ql1 = qh1 * x1;
+      const float rr0 = kh0 * y0, rr1 = kh1 * y1;
+      *reinterpret_cast<float2 *>(KL + r * LDF + c0) = make_float2(kl0, kl1);
+      *reinterpret_cast<float2 *>(QL + r * LDF + c0) = make_float2(ql0, ql1);
+      *reinterpret_cast<float2 *>(RR + r * LDF + c0) = make_float2(rr0, rr1);
+      st2(tqt.at(r, c0), ql0 * pa0, ql1 * pa1);   // Qt = q^ exp(G_r)
+      st2(tkt.at(r, c0), kl0 * pa0, kl1 * pa1);   // Kt = k^ exp(G_r)
+      st2(tkh.at(r, c0), rr0 * fa0, rr1 * fa1);   // Kh = k^ exp(G_last - G_r)
+    }
+    if (a == 0)
+      *reinterpret_cast<float2 *>(rec + L.gc + c0 * 4) = make_float2(exp2f(e3[0]), exp2f(e3[1]));
+  }
+  __syncthreads();
+  // 3. Gram products: 20 tasks (pair, A|B), warp w takes tasks w, w+8, w+16
+  float acc[3][2][4];
+#pragma unroll
+  for (int u = 0; u < 3; ++u) {
+    zero(acc[u]);
+    const int task = warp + 8 * u;
+    if (task < 20) {
+      int pa, pb;
+      pair_of(task >> 1, pa, pb);
+      const float *X = (task & 1) ? QL : KL;
+      gram16<PRECISE>(acc[u], X + pa * SUB * LDF, RR + pb * SUB * LDF, dv[task >> 1]);
+    }
+  }
+  __syncthreads();   // KL, QL, R are free from here on
+  {
+    float *Lm = (float *)(smem + S::LM);
+    Tile<E, 64> bm((E *)(smem + S::BM));
+    float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) : nullptr;
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      const int task = warp + 8 * u;
+      if (task >= 20) continue;
+      int pa, pb;
+      pair_of(task >> 1, pa, pb);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int r = ap * SUB + g8 + 8 * hh, j = b * SUB + nt * 8 + 2 * q4;
-          const float a0 = (j < r) ? accA[b][nt][2 * hh] : 0.f, a1 = (j + 1 < r) ? accA[b][nt][2 * hh + 1] : 0.f;
-          const float b0 = (j <= r) ? accB[b][nt][2 * hh] : 0.f, b1 = (j + 1 <= r) ? accB[b][nt][2 * hh + 1] : 0.f;
-          st2(Lm.at(r, j), sb[r] * a0, sb[r] * a1);
-          st2(Bm.at(r, j), b0, b1);
+          const int r = pa * SUB + g + 8 * hh, j = pb * SUB + 8 * nt + 2 * q;
+          const float v0 = acc[u][nt][2 * hh], v1 = acc[u][nt][2 * hh + 1];
+          if (task & 1) {
+            st2(bm.at(r, j), j <= r ? v0 : 0.f, j + 1 <= r ? v1 : 0.f);
+          } else {
+            const float a0 = j < r ? v0 : 0.f, a1 = j + 1 < r ? v1 : 0.f;
+            *reinterpret_cast<float2 *>(Lm + r * LDS64 + j) = make_float2(sb[r] * a0, sb[r] * a1);
+            if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(a0, a1);
+          }
         }
-      }
+    }
+    // zero the upper sub-blocks of the Bm record tile
+    for (int idx = tid; idx < 64 * 64; idx += PREP_THREADS) {
+      const int r = idx >> 6, j = idx & 63;
+      if ((j >> 4) > (r >> 4)) *bm.at(r, j) = from_f<E>(0.f);
     }
   }
   __syncthreads();
-  ut_solve((float *)(smem + S::A), (float *)(smem + S::T), (float *)(smem + S::SCR));
-
-  // Tb = T Diag(beta)
+  // 4. T = (I + Lm)^-1: diagonal sub-blocks by forward substitution (warps 0..3)
   {
-    Tile<float, 64> T((float *)(smem + S::T));
-    Tile<E, 64> Tb((E *)(smem + S::TB));
-    const float *sb = (const float *)(smem + S::BETA);
-    for (int idx = tid; idx < 64 * 32; idx += 128) {
-      const int r = idx / 32, j = (idx % 32) * 2;
-      const float2 t = ld2(T.at(r, j));
-      st2(Tb.at(r, j), t.x * sb[j], t.y * sb[j + 1]);
-    }
-  }
-  // Qt = QL * 2^E_{a-1}, Kt = KL * 2^E_{a-1}, Kh = RD(3, .) * 2^(E_3 - E_2), gC = 2^E_3
-  {
-    constexpr int EPC = 16 / sizeof(E);
-    Tile<E, 128> tq((E *)(smem + S::Q)), tk((E *)(smem + S::K));
-    Tile<E, 128> kh((E *)(smem + S::RD) + pair_idx(3, 0) * SUB * 128);
-    const float(*pv)[128] = (const float(*)[128])(smem + S::PV);
-    const float *fv = (const float *)(smem + S::FV);
-    for (int idx = tid; idx < 64 * (128 / EPC); idx += 128) {
-      const int r = idx / (128 / EPC), c0 = (idx % (128 / EPC)) * EPC, a = r >> 4;
+    const float *Lm = (const float *)(smem + S::LM);
+    float *T = (float *)(smem + S::TT);
+    if (warp < NSUB) {
+      const int ab = warp, j = lane & 15;
+      float x[SUB];
 #pragma unroll
-      for (int e = 0; e < EPC; ++e) {
-        const int c = c0 + e;
-        const float pa = pv[a][c], f = fv[c];
-        *tq.at(r, c) = from_f<E>(to_f(*tq.at(r, c)) * pa);
-        *tk.at(r, c) = from_f<E>(to_f(*tk.at(r, c)) * pa);
-        *kh.at(r, c) = from_f<E>(to_f(*kh.at(r, c)) * f);
+      for (int i = 0; i < SUB; ++i) x[i] = (i == j) ? 1.f : 0.f;
+#pragma unroll
+      for (int i = 1; i < SUB; ++i) {
+        float s = 0.f;
+#pragma unroll
+        for (int m = 0; m < i; ++m) s = fmaf(Lm[(ab * SUB + i) * LDS64 + ab * SUB + m], x[m], s);
+        if (i > j) x[i] = -s;
       }
+      if (lane < SUB) {
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) T[(ab * SUB + i) * LDS64 + ab * SUB + j] = x[i];
+      }
+    } else {
+      // warps 4..7 zero the blocks above the diagonal
+      for (int idx = tid - 128; idx < 64 * 64; idx += 128) {
+        const int r = idx >> 6, j = idx & 63;
+        if ((j >> 4) > (r >> 4)) T[r * LDS64 + j] = 0.f;
+      }
+    }
+    __syncthreads();
+    // off-diagonal sub-blocks by levels: T_ab = -T_aa * sum_{m=b}^{a-1} Lm_am T_mb
+    float *P = (float *)(smem + S::SCR) + warp * 16 * LDP;
+    for (int d = 1; d < NSUB; ++d) {
+      const int b = warp, ab = warp + d;
+      if (warp < NSUB && ab < NSUB) {
+        float pacc[2][4];
+        zero(pacc);
+        for (int m = b; m < ab; ++m)
+          mm16<PRECISE>(pacc, Lm + ab * SUB * LDS64 + m * SUB, LDS64, T + m * SUB * LDS64 + b * SUB, LDS64);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          *reinterpret_cast<float2 *>(P + g * LDP + 8 * nt + 2 * q) = make_float2(pacc[nt][0], pacc[nt][1]);
+          *reinterpret_cast<float2 *>(P + (g + 8) * LDP + 8 * nt + 2 * q) = make_float2(pacc[nt][2], pacc[nt][3]);
+        }
+        __syncwarp();
+        float tacc[2][4];
+        zero(tacc);
+        mm16<PRECISE>(tacc, T + ab * SUB * LDS64 + ab * SUB, LDS64, P, LDP);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          float *dst = T + (ab * SUB + g) * LDS64 + b * SUB + 8 * nt + 2 * q;
+          *reinterpret_cast<float2 *>(dst) = make_float2(-tacc[nt][0], -tacc[nt][1]);
+          *reinterpret_cast<float2 *>(dst + 8 * LDS64) = make_float2(-tacc[nt][2], -tacc[nt][3]);
+        }
+        __syncwarp();
+      }
+      __syncthreads();
+    }
+  }
+  // 5. Tb = T Diag(beta) into the record tile; copy the staged tiles out
+  {
+    const float *T = (const float *)(smem + S::TT);
+    Tile<E, 64> tb((E *)(smem + S::TB));
+    float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) + 64 * 64 : nullptr;
+    for (int idx = tid; idx < 64 * 32; idx += PREP_THREADS) {
+      const int r = idx >> 5, j = (idx & 31) * 2;
+      const float t0 = T[r * LDS64 + j], t1 = T[r * LDS64 + j + 1];
+      st2(tb.at(r, j), t0 * sb[j], t1 * sb[j + 1]);
+      if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(t0, t1);
     }
   }
   __syncthreads();
-  // write the record with plain 16-byte stores (tiles keep their swizzled layout)
   {
-    const ImgLayout L(sizeof(E));
-    char *rec = (char *)p.img + ((size_t)chunk * H + h) * L.bytes;
-    const int T128 = S::T128, T64 = 64 * 64 * (int)sizeof(E);
-    auto copy = [&](size_t dst, int src, int bytes) {
-      for (int o = tid * 16; o < bytes; o += 128 * 16)
-        *reinterpret_cast<uint4 *>(rec + dst + o) = *reinterpret_cast<const uint4 *>(smem + src + o);
-    };
-    copy(L.qt, S::Q, T128);
-    copy(L.kt, S::K, T128);
-    copy(L.tb, S::TB, T64);
-    copy(L.bm, S::BM, T64);
-    copy(L.kh, S::RD + pair_idx(3, 0) * SUB * 128 * (int)sizeof(E), T128);
-    copy(L.gc, S::GC, 512);
+    const int T64 = 64 * 64 * (int)sizeof(E);
+    for (int o = tid * 16; o < T64; o += PREP_THREADS * 16) {
+      *reinterpret_cast<uint4 *>(rec + L.tb + o) = *reinterpret_cast<const uint4 *>(smem + S::TB + o);
+      *reinterpret_cast<uint4 *>(rec + L.bm + o) = *reinterpret_cast<const uint4 *>(smem + S::BM + o);
+    }
   }
 }
 
 template <typename E>
 static cudaError_t launch_prep_t(const PrepParams &p, cudaStream_t s) {
-  using S = PrepSmem<E>;
+  using S = PrepSmem2<E>;
   auto kern = kda_prep_kernel<E>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(p.geo.max_chunks, p.geo.heads);
-  kern<<<grid, 128, S::BYTES, s>>>(p);
+  kern<<<grid, PREP_THREADS, S::BYTES, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -18,7 +18,8 @@ ABI_VERSION = 1
 
 # every symbol include/kda.h declares
 EXPORTS = ("kda_fwd", "kda_fwd_workspace_size", "kda_saved_size", "kda_bwd", "kda_bwd_workspace_size",
-           "kda_step", "kda_set_profile_events", "kda_last_error", "kda_abi_version")
+           "kda_step", "kda_fwd_no_alloc", "kda_set_profile_events", "kda_last_error", "kda_abi_version")
+NO_ALLOC_SCRATCH_BYTES = 256 * 1024 * 1024
 
 
 class FwdArgs(C.Structure):
@@ -81,6 +82,8 @@ def load(path: str = LIB_PATH):
     lib.kda_bwd_workspace_size.restype = C.c_size_t
     lib.kda_last_error.argtypes = []
     lib.kda_last_error.restype = C.c_char_p
+    lib.kda_fwd_no_alloc.argtypes = [C.POINTER(FwdArgs), C.c_void_p]
+    lib.kda_fwd_no_alloc.restype = C.c_int
     lib.kda_set_profile_events.argtypes = [C.c_void_p, C.c_int32]
     lib.kda_set_profile_events.restype = None
     lib.kda_abi_version.argtypes = []

@@ -129,6 +129,8 @@ int pick_slice(const kda_fwd_args *a) {
 
 }  // namespace
 
+void kda::set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
+
 extern "C" {
 
 int32_t kda_abi_version(void) { return 1; }

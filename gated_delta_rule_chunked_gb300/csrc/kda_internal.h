@@ -113,4 +113,7 @@ cudaError_t launch_bwd_state(const BwdStateParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_bwd_intra(const BwdIntraParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s);
 
+// Sets the message that kda_last_error() returns on this host thread.
+void set_last_error(const char *msg);
+
 }  // namespace kda

@@ -144,6 +144,32 @@ size_t kda_bwd_workspace_size(const kda_bwd_args *args);
  * section, speculative decoding paragraph). Needs no workspace. */
 kda_status kda_step(const kda_step_args *args, cudaStream_t stream);
 
+/*
+ * kda_fwd_no_alloc -- kda_fwd for callers that cannot allocate device memory.
+ * (This entry point has no counterpart in the pages; it is a deployment aid.)
+ *
+ * Some callers cannot call cudaMalloc, or any allocator, when they run the
+ * forward: for example a plugin or callback executing inside another engine
+ * that owns all device memory and passes it only the inputs and outputs, or a
+ * latency-critical path that cannot afford cudaMalloc's implicit device
+ * synchronisation. This call takes the same arguments as kda_fwd, ignores
+ * args->workspace and args->workspace_bytes, and uses instead one file-scope
+ * device array of KDA_NO_ALLOC_SCRATCH_BYTES bytes; it calls no allocator.
+ *  - A problem whose kda_fwd_workspace_size() exceeds KDA_NO_ALLOC_SCRATCH_BYTES
+ *    is rejected with KDA_ERR_INVALID_ARG before anything is enqueued.
+ *  - Every GPU on which the array is loaded keeps it until the process exits.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current (cudaGetSymbolAddress) and caches it; make that first call
+ *    before any stream capture. A failed lookup returns KDA_ERR_CUDA.
+ *  - All calls share the one array: calls whose work overlaps on the GPU (other
+ *    streams or host threads) race. The array keeps the last call's contents;
+ *    the forward writes every scratch byte before reading it, so nothing needs
+ *    clearing between calls.
+ * Outputs (o, hT, saved) are identical to kda_fwd's on the same inputs.
+ */
+#define KDA_NO_ALLOC_SCRATCH_BYTES (256u * 1024u * 1024u)
+kda_status kda_fwd_no_alloc(const kda_fwd_args *args, cudaStream_t stream);
+
 /* Per-kernel timing hook for benchmarks. When `events` is not NULL, every later
  * kda_fwd / kda_bwd / kda_step call records events[i] on its stream right after
  * enqueueing its i-th kernel (i < n_events): kda_fwd has 3 kernels (chunk table,

@@ -52,7 +52,7 @@ size_t elem_size(int io) { return io == KDA_F32 ? 4 : 2; }
 
 // Workspace carving shared by the forward and the backward.
 struct WsPlan {
-  size_t cu, choff, img, dsaved, grad, bytes;
+  size_t cu, choff, img, dsaved, grad, aux, bytes;
 };
 
 WsPlan plan(const kda_fwd_args *a, bool bwd) {
@@ -69,6 +69,8 @@ WsPlan plan(const kda_fwd_args *a, bool bwd) {
     end = w.dsaved + mc * H * 128 * 128 * elem_size(a->io_dtype);
     w.grad = round_up(end, 256);
     end = w.grad + mc * H * kda::GradLayout::bytes;
+    w.aux = round_up(end, 256);
+    end = w.aux + mc * H * 2 * 64 * 64 * sizeof(float);
   }
   w.bytes = round_up(end, 256);
   return w;
@@ -233,7 +235,7 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_bwd chunk table");
   mark(0, stream);
-  kda::PrepParams pp{geo, f->q, f->k, f->g, f->beta, f->scale, ws + w.img, nullptr, f->dev_status};
+  kda::PrepParams pp{geo, f->q, f->k, f->g, f->beta, f->scale, ws + w.img, reinterpret_cast<float *>(ws + w.aux), f->dev_status};
   if ((e = kda::launch_prep(pp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd prep");
   mark(1, stream);
   kda::BwdScanParams bp{geo, a->dO, ws + w.img, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
@@ -245,7 +247,7 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
   if ((e = kda::launch_bwd_state(sp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd state grads");
   mark(3, stream);
   kda::BwdIntraParams ip{geo, f->q, f->k, f->g, f->beta, f->scale, reinterpret_cast<const float *>(ws + w.grad),
-                         a->dq, a->dk, a->dg, a->dbeta, f->dev_status};
+                         reinterpret_cast<const float *>(ws + w.aux), a->dq, a->dk, a->dg, a->dbeta, f->dev_status};
   if ((e = kda::launch_bwd_intra(ip, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd intra grads");
   mark(4, stream);
   g_last_error.clear();

@@ -12,11 +12,10 @@
 //  intra kernel (per chunk, head): back through the intra-chunk graph
 //     Tb = T Diag(beta),  T = (I + Diag(beta) A)^-1:
 //        dT = dTb Diag(beta),  dL = -T^T dT T^T,  dA = Diag(beta) dL (strict lower)
-//     A, Bm through the bounded gating factors (see kda_intra.cuh),
+//     A, Bm through the bounded gating factors (the factorisation of kda_prep.cu),
 //     Qt, Kt, Kh, gC through exp(G), then dg = reverse cumulative sum of dG
 //     inside the chunk, and the L2-norm backward for q and k.
 #include "kda_common.cuh"
-#include "kda_intra.cuh"
 #include "kda_internal.h"
 
 namespace kda {
@@ -178,248 +177,327 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
 }
 
 // ------------------------------------------------------------ intra kernel
-template <typename E>
+// Per (chunk, head), 16 warps. Inputs: q, k, g, beta; the forward's A (strict
+// lower) and T from the prep run; the state-side gradients. The gating enters
+// through three factor tiles (r in sub-block a, x_r = e^{G_r-E_{a-1}},
+// y_r = e^{E_a-G_r}):  QL = q^ x,  KL = k^ x,  R = k^ y, and the record tiles
+// Qt = QL P_a, Kt = KL P_a, Kh = R F_a (P_a = e^{E_{a-1}}, F_a = e^{E_3-E_a}).
+// Gradients w.r.t. the factor tiles are gathered first, then
+//   dq^ = dQL x,  dk^ = dKL x + dR y,  dG = dQL QL + dKL KL - dR R,
+// dg = reverse cumulative sum of dG inside the chunk (plus the e^{G_last} terms
+// on the last row), and the L2-norm backward gives dq, dk.
+constexpr int INTRA_THREADS = 512;
+constexpr int LDI = 132;   // padded fp32 row, 128-wide tiles
+constexpr int LDJ = 68;    // padded fp32 row, 64-wide tiles
+
 struct IntraSmem {
-  using P = PrepSmem<E>;
-  static constexpr int W0 = (P::BYTES + 127) / 128 * 128;   // A (fp32 64x64) ; later dG (with W1)
-  static constexpr int W1 = W0 + 16384;                     // Lm -> X
-  static constexpr int W2 = W1 + 16384;                     // T
-  static constexpr int W3 = W2 + 16384;                     // dTb -> dT
-  static constexpr int DA = W3 + 16384;                     // dA (E 64x64)
-  static constexpr int DB = DA + 64 * 64 * (int)sizeof(E);  // dBm (E 64x64)
-  static constexpr int SCR = DB + 64 * 64 * (int)sizeof(E); // 4 KB
-  static constexpr int DB1 = SCR + 4096, DB2 = DB1 + 256;   // dbeta parts [64]
-  static constexpr int ROWQ = DB2 + 256, ROWK = ROWQ + 512; // [2][64]
-  static constexpr int PART = ROWK + 512;                   // [4][128]
-  static constexpr int DGC = PART + 2048;                   // [128]
+  static constexpr int T128 = 64 * LDI * 4, T64 = 64 * LDJ * 4;
+  static constexpr int KL = 0, QL = T128, R = 2 * T128, CS = 3 * T128;   // CS: local gate sums -> dG
+  static constexpr int TT = 4 * T128, DT = TT + T64, X = DT + T64, DB = X + T64;   // DT: dTb -> dT -> dA
+  static constexpr int DV = DB + T64;                    // [10][128] pair factors
+  static constexpr int TOT = DV + 10 * 512;              // [4][128]
+  static constexpr int PV = TOT + 4 * 512, FV = PV + 4 * 512;   // [4][128] each
+  static constexpr int RQ = FV + 4 * 512, RQ0 = RQ + 256, RK = RQ0 + 256, BETA = RK + 256;
+  static constexpr int DB1 = BETA + 256, DB2 = DB1 + 256;       // dbeta parts: [64], [4][64]
+  static constexpr int ROWQ = DB2 + 1024, ROWK = ROWQ + 1024;  // [4][64]
+  static constexpr int PART = ROWK + 1024;               // [4][128]
+  static constexpr int DGC = PART + 2048;                // [128]
   static constexpr int BYTES = DGC + 512;
 };
 
-template <typename E>
-__global__ void __launch_bounds__(256) kda_bwd_intra_kernel(BwdIntraParams p) {
-  using P = PrepSmem<E>;
-  using S = IntraSmem<E>;
+// acc[nt] (16 x 8*NT) += A * B over k in [k0, k1) (multiples of 8), TF32 tensor cores.
+// A(m, k) = a_ptr[m * a_rs + k * a_cs], B(k, n) = b_ptr[k * b_rs + n * b_cs] * (bscale ? bscale[n] : 1).
+template <int NT>
+__device__ __forceinline__ void mma_tf32_block(float (&acc)[NT][4], const float *a_ptr, int a_rs, int a_cs,
+                                               const float *b_ptr, int b_rs, int b_cs, int k0, int k1,
+                                               const float *bscale = nullptr) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  for (int kk = k0; kk < k1; kk += 8) {
+    uint32_t a[4];
+    a[0] = tf32(a_ptr[g * a_rs + (kk + q) * a_cs]);
+    a[1] = tf32(a_ptr[(g + 8) * a_rs + (kk + q) * a_cs]);
+    a[2] = tf32(a_ptr[g * a_rs + (kk + q + 4) * a_cs]);
+    a[3] = tf32(a_ptr[(g + 8) * a_rs + (kk + q + 4) * a_cs]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = 8 * nt + g;
+      float b0 = b_ptr[(kk + q) * b_rs + n * b_cs], b1 = b_ptr[(kk + q + 4) * b_rs + n * b_cs];
+      if (bscale) { b0 *= bscale[n]; b1 *= bscale[n]; }
+      mma1688(acc[nt], a, tf32(b0), tf32(b1));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntraParams p) {
+  using S = IntraSmem;
   extern __shared__ __align__(128) char smem[];
   const int chunk = blockIdx.x, h = blockIdx.y, H = p.geo.heads;
   ChunkRef ref;
   if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) return;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, q4 = lane & 3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
   const size_t rid = (size_t)chunk * H + h;
   const float *rec = p.grad + rid * (GradLayout::bytes / 4);
-  Tile<float, 64> tA((float *)(smem + S::W0)), tLm((float *)(smem + S::W1)), tT((float *)(smem + S::W2)),
-      tdT((float *)(smem + S::W3)), tX((float *)(smem + S::W1));
-  Tile<E, 64> tdA((E *)(smem + S::DA)), tdB((E *)(smem + S::DB));
-  const float *sb = (const float *)(smem + P::BETA);
+  const float *auxA = p.aux + rid * (2 * 64 * 64), *auxT = auxA + 64 * 64;
+  const bf16 *qg = (const bf16 *)p.q, *kg = (const bf16 *)p.k;
+  float *KL = (float *)(smem + S::KL), *QL = (float *)(smem + S::QL), *RR = (float *)(smem + S::R),
+        *CS = (float *)(smem + S::CS);
+  float *TT = (float *)(smem + S::TT), *DT = (float *)(smem + S::DT), *XX = (float *)(smem + S::X),
+        *DBm = (float *)(smem + S::DB);
+  float(*dv)[128] = (float(*)[128])(smem + S::DV);
+  float(*tot)[128] = (float(*)[128])(smem + S::TOT);
+  float(*pv)[128] = (float(*)[128])(smem + S::PV);
+  float(*fv)[128] = (float(*)[128])(smem + S::FV);
+  float *rq = (float *)(smem + S::RQ), *rq0 = (float *)(smem + S::RQ0), *rk = (float *)(smem + S::RK),
+        *sb = (float *)(smem + S::BETA);
 
-  load_chunk_qkg<E>(smem, (const E *)p.q, (const E *)p.k, p.g, p.beta, ref.t0, ref.len, h, H, 256);
-  for (int idx = tid; idx < 64 * 32; idx += 256) {
-    const int r = idx / 32, j = (idx % 32) * 2;
-    const float2 a = *reinterpret_cast<const float2 *>(rec + GradLayout::dtb / 4 + r * 64 + j);
-    const float2 b = *reinterpret_cast<const float2 *>(rec + GradLayout::dbm / 4 + r * 64 + j);
-    st2(tdT.at(r, j), a.x, a.y);
-    st2(tdB.at(r, j), b.x, b.y);
+  // P1: row norms (8 threads per row), beta, and the 64x64 inputs
+  {
+    const int r = tid >> 3, part = tid & 7;
+    float sq = 0.f, sk = 0.f;
+    if (r < ref.len) {
+      const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + part * 16;
+#pragma unroll
+      for (int c = 0; c < 16; c += 2) {
+        const float2 a = ld2(qg + off + c), b = ld2(kg + off + c);
+        sq = fmaf(a.x, a.x, fmaf(a.y, a.y, sq));
+        sk = fmaf(b.x, b.x, fmaf(b.y, b.y, sk));
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    }
+    if (part == 0) {
+      const float r0 = rsqrtf(sq + 1e-6f);
+      rq0[r] = r0;
+      rq[r] = p.scale * r0;
+      rk[r] = rsqrtf(sk + 1e-6f);
+    }
+    if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
+    if (tid < 128) ((float *)(smem + S::DGC))[tid] = rec[GradLayout::dgc / 4 + tid];
+    for (int idx = tid; idx < 64 * 16; idx += INTRA_THREADS) {
+      const int rr = idx >> 4, c4 = (idx & 15) * 4;
+      *reinterpret_cast<float4 *>(TT + rr * LDJ + c4) = *reinterpret_cast<const float4 *>(auxT + rr * 64 + c4);
+      *reinterpret_cast<float4 *>(DT + rr * LDJ + c4) =
+          *reinterpret_cast<const float4 *>(rec + GradLayout::dtb / 4 + rr * 64 + c4);
+      *reinterpret_cast<float4 *>(DBm + rr * LDJ + c4) =
+          *reinterpret_cast<const float4 *>(rec + GradLayout::dbm / 4 + rr * 64 + c4);
+    }
   }
-  if (tid < 128) ((float *)(smem + S::DGC))[tid] = rec[GradLayout::dgc / 4 + tid];
+  // P2a: gate scan (threads 0..255: channel pair x sub-block)
+  const int cp = tid & 63, a = (tid >> 6) & 3, c0 = 2 * cp;
+  float2 cs[SUB];
+  if (tid < 256) {
+#pragma unroll
+    for (int i = 0; i < SUB; ++i) {
+      const int r = a * SUB + i;
+      cs[i] = make_float2(0.f, 0.f);
+      if (r < ref.len) cs[i] = *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + r) * H + h) * D + c0);
+    }
+    float2 run = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < SUB; ++i) {
+      run.x = fmaf(cs[i].x, LOG2E, run.x);
+      run.y = fmaf(cs[i].y, LOG2E, run.y);
+      cs[i] = run;
+    }
+    tot[a][c0] = run.x;
+    tot[a][c0 + 1] = run.y;
+  }
   __syncthreads();
-  row_norms<E>(smem, p.scale);
-  gate_scan<E>(smem);
-  __syncthreads();
-  factor_pass<E>(smem);
-  __syncthreads();
-  // A (strict lower): warps 0..3 own row sub-block a' = warp
-  if (warp < NSUB) {
-    const int ap = warp;
-    Tile<E, 128> tk((E *)(smem + P::K));
+  if (tid < 256) {
+    // P2b: factor tiles and per-channel factors
+    float em[2] = {0.f, 0.f}, e3[2] = {0.f, 0.f}, eb[2] = {0.f, 0.f};
 #pragma unroll
     for (int b = 0; b < NSUB; ++b) {
-      float accA[2][4];
-      zero(accA);
-      if (b <= ap) {
-        Tile<E, 128> rd((E *)(smem + P::RD) + pair_idx(ap, b) * SUB * 128);
-        wgemm<true, true, 2>(accA, tk, ap * SUB, rd, 0, 0, 128);
+      const float t0 = tot[b][c0], t1 = tot[b][c0 + 1];
+      if (b < a) { em[0] += t0; em[1] += t1; }
+      e3[0] += t0;
+      e3[1] += t1;
+    }
+#pragma unroll
+    for (int b = 0; b < NSUB; ++b) {
+      eb[0] += tot[b][c0];
+      eb[1] += tot[b][c0 + 1];
+      if (b <= a) {
+        const int pr = a * (a + 1) / 2 + b;
+        dv[pr][c0] = exp2f(em[0] - eb[0]);
+        dv[pr][c0 + 1] = exp2f(em[1] - eb[1]);
+      }
+    }
+    const float ta0 = tot[a][c0], ta1 = tot[a][c0 + 1];
+    pv[a][c0] = exp2f(em[0]);
+    pv[a][c0 + 1] = exp2f(em[1]);
+    fv[a][c0] = exp2f(e3[0] - em[0] - ta0);
+    fv[a][c0 + 1] = exp2f(e3[1] - em[1] - ta1);
+#pragma unroll
+    for (int i = 0; i < SUB; ++i) {
+      const int r = a * SUB + i;
+      float2 qv = make_float2(0.f, 0.f), kv = qv;
+      if (r < ref.len) {
+        const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + c0;
+        qv = ld2(qg + off);
+        kv = ld2(kg + off);
+      }
+      const float x0 = exp2f(cs[i].x), x1 = exp2f(cs[i].y);
+      const float y0 = exp2f(ta0 - cs[i].x), y1 = exp2f(ta1 - cs[i].y);
+      const float kh0 = kv.x * rk[r], kh1 = kv.y * rk[r];
+      *reinterpret_cast<float2 *>(KL + r * LDI + c0) = make_float2(kh0 * x0, kh1 * x1);
+      *reinterpret_cast<float2 *>(QL + r * LDI + c0) = make_float2(qv.x * rq[r] * x0, qv.y * rq[r] * x1);
+      *reinterpret_cast<float2 *>(RR + r * LDI + c0) = make_float2(kh0 * y0, kh1 * y1);
+      *reinterpret_cast<float2 *>(CS + r * LDI + c0) = cs[i];
+    }
+    if (a == 0) ((float *)(smem + S::PART))[c0] = 0.f;   // keeps PART defined for masked lanes
+  } else if (tid < 320) {
+    // dbeta_j through Tb = T Diag(beta), and dT = dTb Diag(beta)
+    const int j = tid - 256;
+    float sacc = 0.f;
+    for (int r = j; r < 64; ++r) {
+      const float d = DT[r * LDJ + j];
+      sacc = fmaf(d, TT[r * LDJ + j], sacc);
+      DT[r * LDJ + j] = d * sb[j];
+    }
+    ((float *)(smem + S::DB1))[j] = sacc;
+  }
+  __syncthreads();
+  // P3: X = dT T^T (dT, T lower triangular)
+  {
+    const int mt = warp & 3, np = warp >> 2;     // rows 16mt.., columns 16np..16np+15
+    float acc[2][4];
+    zero(acc);
+    mma_tf32_block<2>(acc, DT + 16 * mt * LDJ, LDJ, 1, TT + 16 * np * LDJ, 1, LDJ, 0, 16 * (mt + 1));
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      float *dst = XX + (16 * mt + g) * LDJ + 16 * np + 8 * nt + 2 * q;
+      *reinterpret_cast<float2 *>(dst) = make_float2(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<float2 *>(dst + 8 * LDJ) = make_float2(acc[nt][2], acc[nt][3]);
+    }
+  }
+  __syncthreads();
+  // P4: dL = -T^T X (strict lower part);  dA = Diag(beta) dL;  dbeta_r += sum_j dL_rj A_rj
+  {
+    const int mt = warp & 3, np = warp >> 2;
+    float acc[2][4];
+    zero(acc);
+    mma_tf32_block<2>(acc, TT + 16 * mt, 1, LDJ, XX + 16 * np, LDJ, 1, 16 * mt, 64);
+    float part[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * mt + g + 8 * hh, j = 16 * np + 8 * nt + 2 * q;
+        const float d0 = j < r ? -acc[nt][2 * hh] : 0.f, d1 = j + 1 < r ? -acc[nt][2 * hh + 1] : 0.f;
+        const float2 av = *reinterpret_cast<const float2 *>(auxA + r * 64 + j);
+        part[hh] = fmaf(d0, j < r ? av.x : 0.f, fmaf(d1, j + 1 < r ? av.y : 0.f, part[hh]));
+        *reinterpret_cast<float2 *>(DT + r * LDJ + j) = make_float2(sb[r] * d0, sb[r] * d1);
       }
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+    for (int hh = 0; hh < 2; ++hh) {
+      part[hh] += __shfl_xor_sync(0xffffffffu, part[hh], 1);
+      part[hh] += __shfl_xor_sync(0xffffffffu, part[hh], 2);
+      if (q == 0) ((float *)(smem + S::DB2))[np * 64 + 16 * mt + g + 8 * hh] = part[hh];
+    }
+  }
+  __syncthreads();
+  // P5: gradients w.r.t. the factor tiles; warp -> (row sub-block t, channel quarter cq)
+  const int t = warp & 3, cq = warp >> 2, cbase = 32 * cq;
+  float tQ[4][4], tK[4][4], tW[4][4];
+  zero(tQ);
+  zero(tK);
+  zero(tW);
+  for (int b = 0; b <= t; ++b) {
+    const float *dsc = dv[t * (t + 1) / 2 + b] + cbase;
+    mma_tf32_block<4>(tQ, DBm + 16 * t * LDJ + 16 * b, LDJ, 1, RR + 16 * b * LDI + cbase, LDI, 1, 0, 16, dsc);
+    mma_tf32_block<4>(tK, DT + 16 * t * LDJ + 16 * b, LDJ, 1, RR + 16 * b * LDI + cbase, LDI, 1, 0, 16, dsc);
+  }
+  for (int aa = t; aa < NSUB; ++aa) {
+    float tR[4][4];
+    zero(tR);
+    mma_tf32_block<4>(tR, DBm + 16 * aa * LDJ + 16 * t, 1, LDJ, QL + 16 * aa * LDI + cbase, LDI, 1, 0, 16);
+    mma_tf32_block<4>(tR, DT + 16 * aa * LDJ + 16 * t, 1, LDJ, KL + 16 * aa * LDI + cbase, LDI, 1, 0, 16);
+    const float *dsc = dv[aa * (aa + 1) / 2 + t] + cbase;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = ap * SUB + g8 + 8 * hh, j = b * SUB + nt * 8 + 2 * q4;
-          const float a0 = (j < r) ? accA[nt][2 * hh] : 0.f, a1 = (j + 1 < r) ? accA[nt][2 * hh + 1] : 0.f;
-          st2(tA.at(r, j), a0, a1);
-          st2(tLm.at(r, j), sb[r] * a0, sb[r] * a1);
-        }
-    }
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tW[nt][e] = fmaf(tR[nt][e], dsc[8 * nt + 2 * q + (e & 1)], tW[nt][e]);
   }
-  __syncthreads();
-  ut_solve((float *)(smem + S::W1), (float *)(smem + S::W2), (float *)(smem + S::SCR));
-  // dbeta_j (through Tb = T Diag(beta)) and dT = dTb Diag(beta)
-  if (tid < 64) {
-    const int j = tid;
-    float s = 0.f;
-    for (int r = j; r < 64; ++r) {
-      const float d = *tdT.at(r, j);
-      s = fmaf(d, *tT.at(r, j), s);
-      *tdT.at(r, j) = d * sb[j];
-    }
-    ((float *)(smem + S::DB1))[j] = s;
-  }
-  __syncthreads();
-  // X = dT T^T
+  __syncthreads();   // every warp is done reading the factor tiles of other rows
+  float dqh[4][4], dkh[4][4];
   {
-    const int r = tid >> 2, m0 = (tid & 3) * 16;
-    float x[16];
+    float rowq[2] = {0.f, 0.f}, rowk[2] = {0.f, 0.f}, colsum[4][2];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = 0.f;
-    for (int j = 0; j <= r; ++j) {
-      const float d = *tdT.at(r, j);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = fmaf(d, *tT.at(m0 + i, j), x[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < 16; i += 2) st2(tX.at(r, m0 + i), x[i], x[i + 1]);
-  }
-  __syncthreads();
-  // dL = -T^T X (strict lower);  dA = Diag(beta) dL ;  dbeta_r += sum_j dL_rj A_rj
-  {
-    const int r = tid >> 2, j0 = (tid & 3) * 16;
-    float dl[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) dl[i] = 0.f;
-    for (int m = r; m < 64; ++m) {
-      const float t = *tT.at(m, r);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) dl[i] = fmaf(t, *tX.at(m, j0 + i), dl[i]);
-    }
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const int j = j0 + i;
-      const float d0 = (j < r) ? -dl[i] : 0.f, d1 = (j + 1 < r) ? -dl[i + 1] : 0.f;
-      s = fmaf(d0, *tA.at(r, j), fmaf(d1, *tA.at(r, j + 1), s));
-      st2(tdA.at(r, j), sb[r] * d0, sb[r] * d1);
-    }
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    if ((tid & 3) == 0) ((float *)(smem + S::DB2))[r] = s;
-  }
-  __syncthreads();
-
-  // Gram backward and gate combine: warp -> row sub-block t, channel half hf
-  const int t = warp & 3, hf = warp >> 2;
-  Tile<E, 128> QL((E *)(smem + P::Q)), KL((E *)(smem + P::K));
-  Tile<float, 128> tG((float *)(smem + P::G)), tdG((float *)(smem + S::W0));
-  const float(*ev)[128] = (const float(*)[128])(smem + P::EV);
-  const float(*pv)[128] = (const float(*)[128])(smem + P::PV);
-  const float *fv = (const float *)(smem + P::FV);
-  float dqh[8][4], dkh[8][4];
-  float colsum[8][2];
-  float rowq[2] = {0.f, 0.f}, rowk[2] = {0.f, 0.f};
-  {
-    float tQ[8][4], tK[8][4], tW[8][4], dG[8][4];
-    zero(tQ);
-    zero(tK);
-    zero(tW);
-    zero(dG);
-    for (int b = 0; b <= t; ++b) {
-      Tile<E, 128> rdb((E *)(smem + P::RD) + (pair_idx(t, b) - b) * SUB * 128);
-      wgemm<true, false, 8>(tQ, tdB, 16 * t, rdb, 64 * hf, 16 * b, 16 * b + 16);
-      wgemm<true, false, 8>(tK, tdA, 16 * t, rdb, 64 * hf, 16 * b, 16 * b + 16);
-    }
-    for (int a = t; a < NSUB; ++a) {
-      float tR[8][4];
-      zero(tR);
-      wgemm<false, false, 8>(tR, tdB, 16 * t, QL, 64 * hf, 16 * a, 16 * a + 16);
-      wgemm<false, false, 8>(tR, tdA, 16 * t, KL, 64 * hf, 16 * a, 16 * a + 16);
-      Tile<E, 128> rdat((E *)(smem + P::RD) + pair_idx(a, t) * SUB * 128);
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int jl = g8 + 8 * (e >> 1), c = 64 * hf + 8 * nt + 2 * q4 + (e & 1);
-          const float dat = exp2f(ev[a][c] - ev[t + 1][c]);
-          tW[nt][e] = fmaf(tR[nt][e], dat, tW[nt][e]);
-          dG[nt][e] = fmaf(-tR[nt][e], to_f(*rdat.at(jl, c)), dG[nt][e]);
-        }
-    }
-    Tile<E, 128> rd3((E *)(smem + P::RD) + pair_idx(3, 0) * SUB * 128);
-    const E *qg = (const E *)p.q, *kg = (const E *)p.k;
-    const float *rq0 = (const float *)(smem + P::RQ0), *rk = (const float *)(smem + P::RK);
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < 4; ++nt) {
       colsum[nt][0] = colsum[nt][1] = 0.f;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * t + g8 + 8 * hh, c = 64 * hf + 8 * nt + 2 * q4;
+        const int r = 16 * t + g + 8 * hh, c = cbase + 8 * nt + 2 * q;
         const float2 dqt = *reinterpret_cast<const float2 *>(rec + GradLayout::dqt / 4 + r * 128 + c);
         const float2 dkt = *reinterpret_cast<const float2 *>(rec + GradLayout::dkt / 4 + r * 128 + c);
-        const float2 dkhs = *reinterpret_cast<const float2 *>(rec + GradLayout::dkh / 4 + r * 128 + c);
+        const float2 dkk = *reinterpret_cast<const float2 *>(rec + GradLayout::dkh / 4 + r * 128 + c);
         float2 qr = make_float2(0.f, 0.f), kr = qr;
         if (r < ref.len) {
-          const size_t off = ((size_t)(ref.t0 + r) * H + h) * 128 + c;
+          const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + c;
           qr = ld2(qg + off);
           kr = ld2(kg + off);
         }
-        const float dqv[2] = {dqt.x, dqt.y}, dktv[2] = {dkt.x, dkt.y}, dkhv[2] = {dkhs.x, dkhs.y};
+        const float dqtv[2] = {dqt.x, dqt.y}, dktv[2] = {dkt.x, dkt.y}, dkkv[2] = {dkk.x, dkk.y};
         const float qrv[2] = {qr.x, qr.y}, krv[2] = {kr.x, kr.y};
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int cc = c + e2, e = 2 * hh + e2;
-          const float Gr = *tG.at(r, cc);
-          const float x = exp2f(Gr - ev[t][cc]), y = exp2f(ev[t + 1][cc] - Gr);
-          const float px = pv[t][cc], ft = exp2f(ev[4][cc] - ev[t + 1][cc]);
-          const float ql = to_f(*QL.at(r, cc)), kl = to_f(*KL.at(r, cc));
-          const float khv = to_f(*rd3.at(r, cc)) * fv[cc];
-          const float xq = x * px;
-          const float dq_ = tQ[nt][e] * x + dqv[e2] * xq;
-          const float dk_ = tK[nt][e] * x + tW[nt][e] * y + dktv[e2] * xq + dkhv[e2] * (y * ft);
-          const float dg_ = dG[nt][e] + tQ[nt][e] * ql + tK[nt][e] * kl + (dqv[e2] * ql + dktv[e2] * kl) * px -
-                            dkhv[e2] * khv;
-          colsum[nt][e2] = fmaf(dkhv[e2], khv, colsum[nt][e2]);
+          const float pa = pv[t][cc], fa = fv[t][cc];
+          const float csv = CS[r * LDI + cc];
+          const float x = exp2f(csv), y = exp2f(tot[t][cc] - csv);
+          const float ql = QL[r * LDI + cc], kl = KL[r * LDI + cc], rr = RR[r * LDI + cc];
+          const float dQL = tQ[nt][e] + dqtv[e2] * pa, dKL = tK[nt][e] + dktv[e2] * pa;
+          const float dR = tW[nt][e] + dkkv[e2] * fa;
+          const float dq_ = dQL * x, dk_ = dKL * x + dR * y;
+          CS[r * LDI + cc] = dQL * ql + dKL * kl - dR * rr;   // dG (natural-log units)
+          colsum[nt][e2] = fmaf(dkkv[e2], rr * fa, colsum[nt][e2]);
           dqh[nt][e] = dq_;
           dkh[nt][e] = dk_;
-          *tdG.at(r, cc) = dg_;
           rowq[hh] = fmaf(qrv[e2] * rq0[r], dq_, rowq[hh]);
           rowk[hh] = fmaf(krv[e2] * rk[r], dk_, rowk[hh]);
         }
       }
     }
-  }
-  // row dot products for the norm backward; column sums of dKh*Kh for dG_last
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    rowq[hh] += __shfl_xor_sync(0xffffffffu, rowq[hh], 1);
-    rowq[hh] += __shfl_xor_sync(0xffffffffu, rowq[hh], 2);
-    rowk[hh] += __shfl_xor_sync(0xffffffffu, rowk[hh], 1);
-    rowk[hh] += __shfl_xor_sync(0xffffffffu, rowk[hh], 2);
-    if (q4 == 0) {
-      ((float *)(smem + S::ROWQ))[hf * 64 + 16 * t + g8 + 8 * hh] = rowq[hh];
-      ((float *)(smem + S::ROWK))[hf * 64 + 16 * t + g8 + 8 * hh] = rowk[hh];
+    for (int hh = 0; hh < 2; ++hh) {
+      rowq[hh] += __shfl_xor_sync(0xffffffffu, rowq[hh], 1);
+      rowq[hh] += __shfl_xor_sync(0xffffffffu, rowq[hh], 2);
+      rowk[hh] += __shfl_xor_sync(0xffffffffu, rowk[hh], 1);
+      rowk[hh] += __shfl_xor_sync(0xffffffffu, rowk[hh], 2);
+      if (q == 0) {
+        ((float *)(smem + S::ROWQ))[cq * 64 + 16 * t + g + 8 * hh] = rowq[hh];
+        ((float *)(smem + S::ROWK))[cq * 64 + 16 * t + g + 8 * hh] = rowk[hh];
+      }
     }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        float sum = colsum[nt][e2];
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+        if (g == 0) ((float *)(smem + S::PART))[t * 128 + cbase + 8 * nt + 2 * q + e2] = sum;
+      }
   }
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-    for (int e2 = 0; e2 < 2; ++e2) {
-      float s = colsum[nt][e2];
-      s += __shfl_xor_sync(0xffffffffu, s, 4);
-      s += __shfl_xor_sync(0xffffffffu, s, 8);
-      s += __shfl_xor_sync(0xffffffffu, s, 16);
-      if (g8 == 0) ((float *)(smem + S::PART))[t * 128 + 64 * hf + 8 * nt + 2 * q4 + e2] = s;
-    }
   __syncthreads();
-  // dq, dk: L2-norm backward
+  // P6: L2-norm backward, dg (reverse cumulative sum), dbeta
   {
     const float *rowQ = (const float *)(smem + S::ROWQ), *rowK = (const float *)(smem + S::ROWK);
-    const float *rq0 = (const float *)(smem + P::RQ0), *rk = (const float *)(smem + P::RK);
-    const E *qg = (const E *)p.q, *kg = (const E *)p.k;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * t + g8 + 8 * hh, c = 64 * hf + 8 * nt + 2 * q4;
+        const int r = 16 * t + g + 8 * hh, c = cbase + 8 * nt + 2 * q;
         if (r < ref.len) {
-          const size_t off = ((size_t)(ref.t0 + r) * H + h) * 128 + c;
+          const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + c;
           const float2 qr = ld2(qg + off), kr = ld2(kg + off);
-          const float dq_dot = rowQ[r] + rowQ[64 + r], dk_dot = rowK[r] + rowK[64 + r];
+          const float dq_dot = rowQ[r] + rowQ[64 + r] + rowQ[128 + r] + rowQ[192 + r];
+          const float dk_dot = rowK[r] + rowK[64 + r] + rowK[128 + r] + rowK[192 + r];
           const float sq = p.scale * rq0[r], rkr = rk[r];
           *reinterpret_cast<float2 *>(p.dq + off) =
               make_float2(sq * (dqh[nt][2 * hh] - qr.x * rq0[r] * dq_dot),
@@ -429,21 +507,23 @@ __global__ void __launch_bounds__(256) kda_bwd_intra_kernel(BwdIntraParams p) {
                           rkr * (dkh[nt][2 * hh + 1] - kr.y * rkr * dk_dot));
         }
       }
-  }
-  // dg = reverse cumulative sum of dG inside the chunk; dbeta
-  if (tid < 128) {
-    const int c = tid;
-    const float *part = (const float *)(smem + S::PART);
-    const float gcv = ((const float *)(smem + P::GC))[c];
-    float run = part[c] + part[128 + c] + part[256 + c] + part[384 + c] + ((const float *)(smem + S::DGC))[c] * gcv;
-    for (int r = 63; r >= 0; --r) {
-      run += *tdG.at(r, c);
-      if (r < ref.len) p.dg[((size_t)(ref.t0 + r) * H + h) * 128 + c] = run;
+    if (tid < 128) {
+      const int c = tid;
+      const float *part = (const float *)(smem + S::PART);
+      float e3 = tot[0][c] + tot[1][c] + tot[2][c] + tot[3][c];
+      float run = part[c] + part[128 + c] + part[256 + c] + part[384 + c] +
+                  ((const float *)(smem + S::DGC))[c] * exp2f(e3);
+      for (int r = 63; r >= 0; --r) {
+        run += CS[r * LDI + c];
+        if (r < ref.len) p.dg[((size_t)(ref.t0 + r) * H + h) * 128 + c] = run;
+      }
+    } else if (tid < 192) {
+      const int r = tid - 128;
+      const float *d2 = (const float *)(smem + S::DB2);
+      if (r < ref.len)
+        p.dbeta[(size_t)(ref.t0 + r) * H + h] =
+            ((const float *)(smem + S::DB1))[r] + d2[r] + d2[64 + r] + d2[128 + r] + d2[192 + r];
     }
-  } else if (tid < 192) {
-    const int r = tid - 128;
-    if (r < ref.len)
-      p.dbeta[(size_t)(ref.t0 + r) * H + h] = ((const float *)(smem + S::DB1))[r] + ((const float *)(smem + S::DB2))[r];
   }
 }
 
@@ -466,8 +546,8 @@ cudaError_t launch_bwd_state(const BwdStateParams &p, bool f32, cudaStream_t s) 
 cudaError_t launch_bwd_intra(const BwdIntraParams &p, bool f32, cudaStream_t s) {
   if (p.geo.max_chunks == 0) return cudaSuccess;
   if (f32) return cudaErrorNotSupported;
-  return launch_chunk_kernel(kda_bwd_intra_kernel<bf16>, IntraSmem<bf16>::BYTES,
-                             dim3(p.geo.max_chunks, p.geo.heads), 256, &p, s);
+  return launch_chunk_kernel(kda_bwd_intra_kernel, IntraSmem::BYTES, dim3(p.geo.max_chunks, p.geo.heads),
+                             INTRA_THREADS, &p, s);
 }
 
 }  // namespace kda

@@ -90,6 +90,7 @@ struct BwdIntraParams {
   const float *g, *beta;
   float scale;
   const float *grad;
+  const float *aux;        // [max_chunks][H] x {A, T} written by the prep kernel
   float *dq, *dk, *dg, *dbeta;
   int *status;
 };

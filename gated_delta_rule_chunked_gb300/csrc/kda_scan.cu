@@ -1,11 +1,14 @@
 // kda_scan.cu -- the sequential inter-chunk state passing (forward) and the
 // reverse dS scan (backward).
 //
-// One CTA per (sequence, head, slice of DVS value columns). Columns of the state
-// evolve independently (the decay and the erase act on key rows), so slicing
-// the value dimension multiplies the number of concurrent chains. The state
+// Columns of the state evolve independently (the decay and the erase act on key
+// rows), so the value dimension is cut into slices of DVS columns, each an
+// independent chain run by one group of 4 warps. A CTA holds NG such groups
+// (NG = 4 for bf16: one CTA per (sequence, head) covering all 128 columns), so
+// the per-chunk record is fetched once and shared by all slices. The state
 // slice stays in registers (fp32) for the whole sequence; its bf16 copy in
-// shared memory is the tensor-core operand. Per chunk, with the record written
+// shared memory is the tensor-core operand. The next chunk's values (forward)
+// or output gradients (backward) are loaded one chunk ahead into registers. Per chunk, with the record written
 // by the prep kernel (Qt = q^*exp(G), Kt = k^*exp(G), Kh = k^*exp(G_last - G),
 // Tb = T Diag(beta), Bm = masked gated q.k^T, gC = exp(G_last)):
 //
@@ -21,7 +24,7 @@
 
 namespace kda {
 
-template <typename E, int DVS>
+template <typename E, int DVS, int NG>
 struct ScanSmem {
   static constexpr int T128 = 64 * 128 * (int)sizeof(E), T64 = 64 * 64 * (int)sizeof(E);
   // record regions (same byte layout as ImgLayout)
@@ -32,15 +35,14 @@ struct ScanSmem {
   static constexpr int R3 = BM, R3B = T64;          // Bm
   static constexpr int R4 = KH, R4B = T128 + 512;   // Kh, gC
   static constexpr int SL = DVS * (int)sizeof(E);   // bytes per slice row
-  static constexpr int X0 = (REC + 127) / 128 * 128;   // [128][DVS] state / dS operand
-  static constexpr int X1 = X0 + 128 * SL;             // [64][DVS]
-  static constexpr int X2 = X1 + 64 * SL;              // [64][DVS]
-  static constexpr int X3 = X2 + 64 * SL;              // [64][DVS]
-  static constexpr int BAR = X3 + 64 * SL;
+  static constexpr int GRP = 128 * SL + 3 * 64 * SL;   // per-group tiles
+  static constexpr int G0 = (REC + 127) / 128 * 128;
+  // per group g at G0 + g*GRP: [128][DVS] state / dS operand, then three [64][DVS] tiles
+  static constexpr int X0 = 0, X1 = 128 * SL, X2 = X1 + 64 * SL, X3 = X2 + 64 * SL;
+  static constexpr int BAR = G0 + NG * GRP;
   static constexpr int BYTES = BAR + 64;
 };
 
-template <typename E, int DVS>
 __device__ __forceinline__ void issue_region(char *smem, const char *rec, int off, int bytes, uint64_t *bar) {
   fence_proxy_async();
   mbar_expect_tx(bar, bytes);
@@ -55,24 +57,39 @@ __device__ __forceinline__ size_t full_off(int r, int c) {
 }
 
 // ------------------------------------------------------------------ forward
-template <typename E, int DVS>
-__global__ void __launch_bounds__(128) kda_fwd_scan_kernel(FwdScanParams p) {
-  constexpr int NZ = 128 / DVS, NT = DVS / 8;
-  using S = ScanSmem<E, DVS>;
+template <typename E, int DVS, int NG>
+__global__ void __launch_bounds__(128 * NG, 1) kda_fwd_scan_kernel(FwdScanParams p) {
+  constexpr int NZ = 128 / DVS, NT = DVS / 8, NB = NZ / NG;
+  using S = ScanSmem<E, DVS, NG>;
   extern __shared__ __align__(128) char smem[];
   const int H = p.geo.heads;
-  const int z = blockIdx.x % NZ, h = (blockIdx.x / NZ) % H, seq = blockIdx.x / (NZ * H);
+  const int tid = threadIdx.x, lane = tid & 31, g8 = lane >> 2, q4 = lane & 3;
+  const int grp = tid >> 7, warp = (tid >> 5) & 3;   // value-slice group, warp within the group
+  const int z = (blockIdx.x % NB) * NG + grp, h = (blockIdx.x / NB) % H, seq = blockIdx.x / (NB * H);
   const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
   const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, q4 = lane & 3;
+  char *gsm = smem + S::G0 + grp * S::GRP;
   const size_t rec_bytes = (size_t)S::REC;
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
   Tile<E, 128> Qt((E *)(smem + S::QT)), Kt((E *)(smem + S::KT)), Kh((E *)(smem + S::KH));
   Tile<E, 64> Tb((E *)(smem + S::TB)), Bm((E *)(smem + S::BM));
   const float *gC = (const float *)(smem + S::GC);
-  Tile<E, DVS> sS((E *)(smem + S::X0)), sVp((E *)(smem + S::X1)), sU((E *)(smem + S::X2)), sO((E *)(smem + S::X3));
+  Tile<E, DVS> sS((E *)(gsm + S::X0)), sVp((E *)(gsm + S::X1)), sU((E *)(gsm + S::X2)), sO((E *)(gsm + S::X3));
   const E *v = (const E *)p.v;
   E *o = (E *)p.o;
+  // value fragment loader (rows 16*warp + g8 + 8*hh, columns z*DVS + 8*nt + 2*q4)
+  auto load_v = [&](int j, float2 (&vf)[NT][2]) {
+    const long long t0 = s0 + (long long)j * CH;
+    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * warp + g8 + 8 * hh;
+        vf[nt][hh] = make_float2(0.f, 0.f);
+        if (r < clen) vf[nt][hh] = ld2(v + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + 8 * nt + 2 * q4);
+      }
+  };
 
   // state slice: rows c = 32*warp + 16*mt + g8 + 8*hh, columns z*DVS + 8*nt + 2*q4 (+1)
   float accS[2][NT][4];
@@ -97,26 +114,22 @@ __global__ void __launch_bounds__(128) kda_fwd_scan_kernel(FwdScanParams p) {
   auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * rec_bytes; };
   if (tid == 0 && nch > 0) {
     const char *r0 = rec_of(0);
-    issue_region<E, DVS>(smem, r0, S::R1, S::R1B, &bar[0]);
-    issue_region<E, DVS>(smem, r0, S::R2, S::R2B, &bar[1]);
-    issue_region<E, DVS>(smem, r0, S::R3, S::R3B, &bar[2]);
-    issue_region<E, DVS>(smem, r0, S::R4, S::R4B, &bar[3]);
+    issue_region(smem, r0, S::R1, S::R1B, &bar[0]);
+    issue_region(smem, r0, S::R2, S::R2B, &bar[1]);
+    issue_region(smem, r0, S::R3, S::R3B, &bar[2]);
+    issue_region(smem, r0, S::R4, S::R4B, &bar[3]);
   }
   bool ok = true;
+  float2 vnext[NT][2];
+  if (nch > 0) load_v(0, vnext);
   for (int j = 0; j < nch; ++j) {
     const uint32_t par = j & 1;
     const long long t0 = s0 + (long long)j * CH;
     const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-    // value fragment of this chunk
     float2 vf[NT][2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * warp + g8 + 8 * hh;
-        vf[nt][hh] = make_float2(0.f, 0.f);
-        if (r < clen) vf[nt][hh] = ld2(v + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + 8 * nt + 2 * q4);
-      }
+    for (int nt = 0; nt < NT; ++nt) { vf[nt][0] = vnext[nt][0]; vf[nt][1] = vnext[nt][1]; }
+    if (j + 1 < nch) load_v(j + 1, vnext);   // one chunk ahead
     // chunk-start state for the backward
     if (p.saved) {
       E *sv = (E *)p.saved + ((size_t)(cbase + j) * H + h) * 128 * 128;
@@ -144,7 +157,7 @@ __global__ void __launch_bounds__(128) kda_fwd_scan_kernel(FwdScanParams p) {
         st2(sVp.at(16 * warp + g8 + 8 * hh, 8 * nt + 2 * q4), vf[nt][hh].x - accV[nt][2 * hh],
             vf[nt][hh].y - accV[nt][2 * hh + 1]);
     if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
-    if (tid == 0 && j + 1 < nch) issue_region<E, DVS>(smem, rec_of(j + 1), S::R1, S::R1B, &bar[0]);
+    if (tid == 0 && j + 1 < nch) issue_region(smem, rec_of(j + 1), S::R1, S::R1B, &bar[0]);
     // (b) U = Tb V'   (Tb lower triangular)
     ok &= mbar_wait(&bar[1], par);
     float accU[NT][4];
@@ -156,7 +169,7 @@ __global__ void __launch_bounds__(128) kda_fwd_scan_kernel(FwdScanParams p) {
       for (int hh = 0; hh < 2; ++hh)
         st2(sU.at(16 * warp + g8 + 8 * hh, 8 * nt + 2 * q4), accU[nt][2 * hh], accU[nt][2 * hh + 1]);
     if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
-    if (tid == 0 && j + 1 < nch) issue_region<E, DVS>(smem, rec_of(j + 1), S::R2, S::R2B, &bar[1]);
+    if (tid == 0 && j + 1 < nch) issue_region(smem, rec_of(j + 1), S::R2, S::R2B, &bar[1]);
     // (c) O += Bm U
     ok &= mbar_wait(&bar[2], par);
     wgemm<true, false, NT>(accO, Bm, 16 * warp, sU, 0, 0, 16 * (warp + 1));
@@ -187,7 +200,7 @@ __global__ void __launch_bounds__(128) kda_fwd_scan_kernel(FwdScanParams p) {
     // output rows, 16-byte coalesced
     {
       constexpr int EPC = 16 / sizeof(E), CPR = DVS / EPC;
-      for (int idx = tid; idx < 64 * CPR; idx += 128) {
+      for (int idx = tid & 127; idx < 64 * CPR; idx += 128) {
         const int r = idx / CPR, ch = idx % CPR;
         if (r < clen)
           *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + ch * EPC) =
@@ -195,8 +208,8 @@ __global__ void __launch_bounds__(128) kda_fwd_scan_kernel(FwdScanParams p) {
       }
     }
     if (tid == 0 && j + 1 < nch) {
-      issue_region<E, DVS>(smem, rec_of(j + 1), S::R3, S::R3B, &bar[2]);
-      issue_region<E, DVS>(smem, rec_of(j + 1), S::R4, S::R4B, &bar[3]);
+      issue_region(smem, rec_of(j + 1), S::R3, S::R3B, &bar[2]);
+      issue_region(smem, rec_of(j + 1), S::R4, S::R4B, &bar[3]);
     }
   }
   if (p.hT) {
@@ -214,23 +227,37 @@ __global__ void __launch_bounds__(128) kda_fwd_scan_kernel(FwdScanParams p) {
 }
 
 // ------------------------------------------------------------------ backward
-template <typename E, int DVS>
-__global__ void __launch_bounds__(128) kda_bwd_scan_kernel(BwdScanParams p) {
-  constexpr int NZ = 128 / DVS, NT = DVS / 8;
-  using S = ScanSmem<E, DVS>;
+template <typename E, int DVS, int NG>
+__global__ void __launch_bounds__(128 * NG, 1) kda_bwd_scan_kernel(BwdScanParams p) {
+  constexpr int NZ = 128 / DVS, NT = DVS / 8, NB = NZ / NG;
+  using S = ScanSmem<E, DVS, NG>;
   extern __shared__ __align__(128) char smem[];
   const int H = p.geo.heads;
-  const int z = blockIdx.x % NZ, h = (blockIdx.x / NZ) % H, seq = blockIdx.x / (NZ * H);
+  const int tid = threadIdx.x, lane = tid & 31, g8 = lane >> 2, q4 = lane & 3;
+  const int grp = tid >> 7, warp = (tid >> 5) & 3, gtid = tid & 127;
+  const int z = (blockIdx.x % NB) * NG + grp, h = (blockIdx.x / NB) % H, seq = blockIdx.x / (NB * H);
   const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
   const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, q4 = lane & 3;
+  char *gsm = smem + S::G0 + grp * S::GRP;
   const size_t rec_bytes = (size_t)S::REC;
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
   Tile<E, 128> Qt((E *)(smem + S::QT)), Kt((E *)(smem + S::KT)), Kh((E *)(smem + S::KH));
   Tile<E, 64> Tb((E *)(smem + S::TB)), Bm((E *)(smem + S::BM));
   const float *gC = (const float *)(smem + S::GC);
-  Tile<E, DVS> sdS((E *)(smem + S::X0)), sdO((E *)(smem + S::X1)), sdU((E *)(smem + S::X2)), sdV((E *)(smem + S::X3));
+  Tile<E, DVS> sdS((E *)(gsm + S::X0)), sdO((E *)(gsm + S::X1)), sdU((E *)(gsm + S::X2)), sdV((E *)(gsm + S::X3));
   const E *dO = (const E *)p.dO;
+  // dO slice rows of chunk j, 16-byte pieces owned by this thread of the group
+  constexpr int EPC = 16 / sizeof(E), CPR = DVS / EPC, PER = 64 * CPR / 128;
+  auto load_do = [&](int j, uint4 (&x)[PER]) {
+    const long long t0 = s0 + (long long)j * CH;
+    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int idx = gtid + 128 * u, r = idx / CPR, ch = idx % CPR;
+      x[u] = make_uint4(0, 0, 0, 0);
+      if (r < clen) x[u] = __ldg(reinterpret_cast<const uint4 *>(dO + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + ch * EPC));
+    }
+  };
 
   float accS[2][NT][4];   // dS slice, same fragment layout as the forward state
 #pragma unroll
@@ -254,27 +281,26 @@ __global__ void __launch_bounds__(128) kda_bwd_scan_kernel(BwdScanParams p) {
   auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * rec_bytes; };
   if (tid == 0 && nch > 0) {
     const char *r0 = rec_of(nch - 1);
-    issue_region<E, DVS>(smem, r0, S::R1, S::R1B, &bar[0]);
-    issue_region<E, DVS>(smem, r0, S::R2, S::R2B, &bar[1]);
-    issue_region<E, DVS>(smem, r0, S::R3, S::R3B, &bar[2]);
-    issue_region<E, DVS>(smem, r0, S::R4, S::R4B, &bar[3]);
+    issue_region(smem, r0, S::R1, S::R1B, &bar[0]);
+    issue_region(smem, r0, S::R2, S::R2B, &bar[1]);
+    issue_region(smem, r0, S::R3, S::R3B, &bar[2]);
+    issue_region(smem, r0, S::R4, S::R4B, &bar[3]);
   }
   bool ok = true;
+  uint4 donext[PER];
+  if (nch > 0) load_do(nch - 1, donext);
   for (int it = 0; it < nch; ++it) {
     const int j = nch - 1 - it;
     const uint32_t par = it & 1;
     const long long t0 = s0 + (long long)j * CH;
     const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-    // dO slice rows of this chunk
-    {
-      constexpr int EPC = 16 / sizeof(E), CPR = DVS / EPC;
-      for (int idx = tid; idx < 64 * CPR; idx += 128) {
-        const int r = idx / CPR, ch = idx % CPR;
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if (r < clen) x = __ldg(reinterpret_cast<const uint4 *>(dO + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + ch * EPC));
-        *reinterpret_cast<uint4 *>(sdO.at(r, ch * EPC)) = x;
-      }
+    // dO slice rows of this chunk (loaded one chunk ahead)
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int idx = gtid + 128 * u, r = idx / CPR, ch = idx % CPR;
+      *reinterpret_cast<uint4 *>(sdO.at(r, ch * EPC)) = donext[u];
     }
+    if (j > 0) load_do(j - 1, donext);
     // dS at the end of this chunk, for the chunk-local gradient kernel
     {
       E *sv = (E *)p.dsaved + ((size_t)(cbase + j) * H + h) * 128 * 128;
@@ -302,7 +328,7 @@ __global__ void __launch_bounds__(128) kda_bwd_scan_kernel(BwdScanParams p) {
       for (int hh = 0; hh < 2; ++hh)
         st2(sdU.at(16 * warp + g8 + 8 * hh, 8 * nt + 2 * q4), accU[nt][2 * hh], accU[nt][2 * hh + 1]);
     if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
-    if (tid == 0 && j > 0) issue_region<E, DVS>(smem, rec_of(j - 1), S::R3, S::R3B, &bar[2]);
+    if (tid == 0 && j > 0) issue_region(smem, rec_of(j - 1), S::R3, S::R3B, &bar[2]);
     // (b) dV = Tb^T dU  -> dv output; -dV into shared memory
     ok &= mbar_wait(&bar[1], par);
     float accV[NT][4];
@@ -319,7 +345,7 @@ __global__ void __launch_bounds__(128) kda_bwd_scan_kernel(BwdScanParams p) {
               make_float2(accV[nt][2 * hh], accV[nt][2 * hh + 1]);
       }
     if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
-    if (tid == 0 && j > 0) issue_region<E, DVS>(smem, rec_of(j - 1), S::R2, S::R2B, &bar[1]);
+    if (tid == 0 && j > 0) issue_region(smem, rec_of(j - 1), S::R2, S::R2B, &bar[1]);
     // (c) dS <- gC * dS + Qt^T dO - Kt^T dV
     ok &= mbar_wait(&bar[0], par);
 #pragma unroll
@@ -341,8 +367,8 @@ __global__ void __launch_bounds__(128) kda_bwd_scan_kernel(BwdScanParams p) {
     }
     if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
     if (tid == 0 && j > 0) {
-      issue_region<E, DVS>(smem, rec_of(j - 1), S::R1, S::R1B, &bar[0]);
-      issue_region<E, DVS>(smem, rec_of(j - 1), S::R4, S::R4B, &bar[3]);
+      issue_region(smem, rec_of(j - 1), S::R1, S::R1B, &bar[0]);
+      issue_region(smem, rec_of(j - 1), S::R4, S::R4B, &bar[3]);
     }
   }
   if (p.dh0) {
@@ -360,33 +386,33 @@ __global__ void __launch_bounds__(128) kda_bwd_scan_kernel(BwdScanParams p) {
 }
 
 template <typename K>
-static cudaError_t launch_scan_kernel(K kern, int bytes, unsigned grid, const void *params, cudaStream_t s) {
+static cudaError_t launch_scan_kernel(K kern, int bytes, unsigned grid, int threads, const void *params,
+                                      cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   void *args[] = {const_cast<void *>(params)};
-  return cudaLaunchKernel((const void *)kern, dim3(grid), dim3(128), args, bytes, s);
+  return cudaLaunchKernel((const void *)kern, dim3(grid), dim3(threads), args, bytes, s);
 }
 
-cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int dvs, cudaStream_t s) {
-  const unsigned grid = (unsigned)((long long)p.geo.n_seqs * p.geo.heads * (128 / dvs));
-  if (grid == 0) return cudaSuccess;
-  if (f32) {
-    if (dvs == 32) return launch_scan_kernel(kda_fwd_scan_kernel<float, 32>, ScanSmem<float, 32>::BYTES, grid, &p, s);
-    return launch_scan_kernel(kda_fwd_scan_kernel<float, 64>, ScanSmem<float, 64>::BYTES, grid, &p, s);
-  }
-  if (dvs == 32) return launch_scan_kernel(kda_fwd_scan_kernel<bf16, 32>, ScanSmem<bf16, 32>::BYTES, grid, &p, s);
-  return launch_scan_kernel(kda_fwd_scan_kernel<bf16, 64>, ScanSmem<bf16, 64>::BYTES, grid, &p, s);
+// bf16: one CTA of 4 slice groups (16 warps) per (sequence, head); fp32: one 4-warp CTA per slice.
+cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int, cudaStream_t s) {
+  const long long units = (long long)p.geo.n_seqs * p.geo.heads;
+  if (units == 0) return cudaSuccess;
+  if (f32)
+    return launch_scan_kernel(kda_fwd_scan_kernel<float, 32, 1>, ScanSmem<float, 32, 1>::BYTES,
+                              (unsigned)(units * 4), 128, &p, s);
+  return launch_scan_kernel(kda_fwd_scan_kernel<bf16, 32, 4>, ScanSmem<bf16, 32, 4>::BYTES, (unsigned)units,
+                            512, &p, s);
 }
 
-cudaError_t launch_bwd_scan(const BwdScanParams &p, bool f32, int dvs, cudaStream_t s) {
-  const unsigned grid = (unsigned)((long long)p.geo.n_seqs * p.geo.heads * (128 / dvs));
-  if (grid == 0) return cudaSuccess;
-  if (f32) {
-    if (dvs == 32) return launch_scan_kernel(kda_bwd_scan_kernel<float, 32>, ScanSmem<float, 32>::BYTES, grid, &p, s);
-    return launch_scan_kernel(kda_bwd_scan_kernel<float, 64>, ScanSmem<float, 64>::BYTES, grid, &p, s);
-  }
-  if (dvs == 32) return launch_scan_kernel(kda_bwd_scan_kernel<bf16, 32>, ScanSmem<bf16, 32>::BYTES, grid, &p, s);
-  return launch_scan_kernel(kda_bwd_scan_kernel<bf16, 64>, ScanSmem<bf16, 64>::BYTES, grid, &p, s);
+cudaError_t launch_bwd_scan(const BwdScanParams &p, bool f32, int, cudaStream_t s) {
+  const long long units = (long long)p.geo.n_seqs * p.geo.heads;
+  if (units == 0) return cudaSuccess;
+  if (f32)
+    return launch_scan_kernel(kda_bwd_scan_kernel<float, 32, 1>, ScanSmem<float, 32, 1>::BYTES,
+                              (unsigned)(units * 4), 128, &p, s);
+  return launch_scan_kernel(kda_bwd_scan_kernel<bf16, 32, 4>, ScanSmem<bf16, 32, 4>::BYTES, (unsigned)units,
+                            512, &p, s);
 }
 
 }  // namespace kda

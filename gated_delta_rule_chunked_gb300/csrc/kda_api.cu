@@ -186,11 +186,12 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_fwd chunk table");
   mark(0, stream);
-  kda::PrepParams pp{geo, a->q, a->k, a->g, a->beta, a->scale, ws + w.img, nullptr, a->dev_status};
+  kda::PrepParams pp{geo, a->q, a->k, a->g, a->beta, a->scale, ws + w.img, nullptr, f32 ? 0 : 1, a->dev_status};
   if ((e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
   kda::FwdScanParams sp{geo, a->v, ws + w.img, a->h0, a->o, a->hT, a->saved, a->dev_status};
-  if ((e = kda::launch_fwd_scan(sp, f32, pick_slice(a), stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd scan");
+  e = f32 ? kda::launch_fwd_scan(sp, true, pick_slice(a), stream) : kda::launch_fwd_scan_tc(sp, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_fwd scan");
   mark(2, stream);
   g_last_error.clear();
   return KDA_OK;
@@ -235,7 +236,7 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_bwd chunk table");
   mark(0, stream);
-  kda::PrepParams pp{geo, f->q, f->k, f->g, f->beta, f->scale, ws + w.img, reinterpret_cast<float *>(ws + w.aux), f->dev_status};
+  kda::PrepParams pp{geo, f->q, f->k, f->g, f->beta, f->scale, ws + w.img, reinterpret_cast<float *>(ws + w.aux), 0, f->dev_status};
   if ((e = kda::launch_prep(pp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd prep");
   mark(1, stream);
   kda::BwdScanParams bp{geo, a->dO, ws + w.img, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};

@@ -28,6 +28,17 @@ struct ImgLayout {
   }
 };
 
+// Per-(chunk, head) record for the tcgen05 forward scan (bf16). Every tile is a
+// K-major, 128-byte-swizzled operand image, so one bulk copy lands it ready for
+// the tensor cores:
+//   B1 [128 rows][K = 128 dk]: rows 0..63 Qt[tok], rows 64..127 -W[tok],  W = Tb Kt
+//   B2 [192 rows][K = 64 tok]: rows 0..127 Kh^T[dk], rows 128..191 Bm[r]
+//   TB [64 rows][K = 64]     : Tb[r][j]
+//   GC 128 fp32              : exp(G_last)
+struct TcRec {
+  static constexpr int B1 = 0, B2 = 32768, TB = B2 + 24576, GC = TB + 8192, BYTES = GC + 512;
+};
+
 // Per-(chunk, head) record of state-side gradients written by the backward's
 // state kernel: dQt, dKt, dKh (64x128 fp32 each), dBm, dTb (64x64 fp32), dgC (128).
 struct GradLayout {
@@ -49,8 +60,9 @@ struct PrepParams {
   const void *q, *k;
   const float *g, *beta;
   float scale;
-  void *img;               // [max_chunks][H] ImgLayout records
+  void *img;               // [max_chunks][H] records (ImgLayout, or TcRec when tc_layout)
   float *aux;              // optional [max_chunks][H] x {A (strict lower), T} fp32 64x64 each
+  int tc_layout;           // bf16 only: write the tcgen05 forward record
   int *status;
 };
 
@@ -61,7 +73,8 @@ struct FwdScanParams {
   const float *h0;
   void *o;
   float *hT;
-  void *saved;             // [max_chunks][H] 128x128 E tiles (swizzled), or null
+  void *saved;             // [max_chunks][H] chunk-start states S^T[v][k] as 128x128 E tiles
+                           // (swizzled), or null
   int *status;
 };
 
@@ -109,6 +122,7 @@ cudaError_t launch_chunk_table(const int *cu_in, int n_seqs, long long total, in
                                int *chunk_off, cudaStream_t s);
 cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
+cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_scan(const BwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
 cudaError_t launch_bwd_state(const BwdStateParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_bwd_intra(const BwdIntraParams &p, bool f32, cudaStream_t s);

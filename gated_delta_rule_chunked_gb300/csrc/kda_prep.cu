@@ -25,6 +25,7 @@
 // This is this library's kernel design, not taken from the pages.
 #include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_tc05.cuh"
 
 namespace kda {
 
@@ -77,22 +78,19 @@ constexpr int LDF = 132;   // padded fp32 row of the 64x128 factor tiles (confli
 constexpr int LDS64 = 68;  // padded fp32 row of 64x64 tiles
 constexpr int LDP = 24;    // padded fp32 row of the 16x16 solver scratch
 
-template <typename E>
 struct PrepSmem2 {
   static constexpr int TILE = 64 * LDF * 4;
   static constexpr int KL = 0, QL = TILE, R = 2 * TILE;     // fp32 [64][LDF] each
   static constexpr int DV = 3 * TILE;                        // fp32 [10][128] pair factors
   static constexpr int TOT = DV + 10 * 512;                  // fp32 [4][128] sub-block gate sums
-  static constexpr int RQ = TOT + 4 * 512, RK = RQ + 256, BETA = RK + 256;
+  static constexpr int PV = TOT + 4 * 512;                   // fp32 [4][128] exp(E_{a-1})
+  static constexpr int RQ = PV + 4 * 512, RK = RQ + 256, BETA = RK + 256;
   static constexpr int BYTES = BETA + 256;
-  // after the Gram products (KL, QL, R are dead)
-  static constexpr int LM = 0;                               // fp32 [64][LDS64]  Diag(beta) A
-  static constexpr int TT = LM + 64 * LDS64 * 4;             // fp32 [64][LDS64]  T
+  // after the Gram products QL and R are dead; KL lives on (it becomes Kt)
+  static constexpr int LM = QL;                              // fp32 [64][LDS64]  Diag(beta) A
+  static constexpr int TT = LM + 64 * LDS64 * 4;             // fp32 [64][LDS64]  T, then T Diag(beta)
   static constexpr int SCR = TT + 64 * LDS64 * 4;            // fp32 4 x [16][LDP]
-  static constexpr int BM = R;                               // E record tile [64][64]
-  static constexpr int TB = R + 64 * 64 * (int)sizeof(E);    // E record tile [64][64]
-  static_assert(SCR + 4 * 16 * LDP * 4 <= R, "solver tiles overlap the staging tiles");
-  static_assert(TB + 64 * 64 * (int)sizeof(E) <= DV, "staging tiles overlap the vectors");
+  static_assert(SCR + 4 * 16 * LDP * 4 <= DV, "solver tiles overlap the vectors");
 };
 
 __device__ __forceinline__ void pair_of(int p, int &a, int &b) {
@@ -168,20 +166,24 @@ __device__ __forceinline__ void mm16(float (&acc)[2][4], const float *A, int lda
 
 template <typename E>
 __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p) {
-  using S = PrepSmem2<E>;
+  using S = PrepSmem2;
   constexpr bool PRECISE = sizeof(E) == 4;   // fp32 I/O: exact fp32 products
   extern __shared__ __align__(128) char smem[];
   const int chunk = blockIdx.x, h = blockIdx.y, H = p.geo.heads;
   ChunkRef ref;
   if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+  // tcgen05 record (bf16 forward) or the tile record (fp32 forward, backward)
+  const bool tcrec = !PRECISE && p.tc_layout;
   const E *qg = (const E *)p.q, *kg = (const E *)p.k;
   float *rq = (float *)(smem + S::RQ), *rk = (float *)(smem + S::RK), *sb = (float *)(smem + S::BETA);
   float *KL = (float *)(smem + S::KL), *QL = (float *)(smem + S::QL), *RR = (float *)(smem + S::R);
   float(*dv)[128] = (float(*)[128])(smem + S::DV);
   float(*tot)[128] = (float(*)[128])(smem + S::TOT);
+  float(*pvv)[128] = (float(*)[128])(smem + S::PV);
   const ImgLayout L(sizeof(E));
-  char *rec = (char *)p.img + ((size_t)chunk * H + h) * L.bytes;
+  const size_t rec_bytes = tcrec ? (size_t)TcRec::BYTES : L.bytes;
+  char *rec = (char *)p.img + ((size_t)chunk * H + h) * rec_bytes;
 
   // 1. row norms: 4 threads per row, 32 channels each
   {
@@ -252,8 +254,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
     }
     const float pa0 = exp2f(em[0]), pa1 = exp2f(em[1]);                       // exp(E_{a-1})
     const float fa0 = exp2f(e3[0] - ea[0]), fa1 = exp2f(e3[1] - ea[1]);       // exp(E_3 - E_a)
-    const float ta0 = tot[a][c0], ta1 = tot[a][c0 + 1];   // E_a - E_{a-1}
+    const float ta0 = tot[a][c0], ta1 = tot[a][c0 + 1];                       // E_a - E_{a-1}
+    pvv[a][c0] = pa0;
+    pvv[a][c0 + 1] = pa1;
     Tile<E, 128> tqt((E *)(rec + L.qt)), tkt((E *)(rec + L.kt)), tkh((E *)(rec + L.kh));
+    float kh0v[SUB], kh1v[SUB];
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
@@ -271,12 +276,33 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       *reinterpret_cast<float2 *>(KL + r * LDF + c0) = make_float2(kl0, kl1);
       *reinterpret_cast<float2 *>(QL + r * LDF + c0) = make_float2(ql0, ql1);
       *reinterpret_cast<float2 *>(RR + r * LDF + c0) = make_float2(rr0, rr1);
-      st2(tqt.at(r, c0), ql0 * pa0, ql1 * pa1);   // Qt = q^ exp(G_r)
-      st2(tkt.at(r, c0), kl0 * pa0, kl1 * pa1);   // Kt = k^ exp(G_r)
-      st2(tkh.at(r, c0), rr0 * fa0, rr1 * fa1);   // Kh = k^ exp(G_last - G_r)
+      kh0v[i] = rr0 * fa0;                        // Kh = k^ exp(G_last - G_r)
+      kh1v[i] = rr1 * fa1;
+      if (tcrec) {
+        // B1 rows 0..63: Qt[tok][dk] = q^ exp(G_r)
+        st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, r, c0)), ql0 * pa0, ql1 * pa1);
+      } else {
+        st2(tqt.at(r, c0), ql0 * pa0, ql1 * pa1);   // Qt = q^ exp(G_r)
+        st2(tkt.at(r, c0), kl0 * pa0, kl1 * pa1);   // Kt = k^ exp(G_r)
+        st2(tkh.at(r, c0), kh0v[i], kh1v[i]);
+      }
     }
-    if (a == 0)
-      *reinterpret_cast<float2 *>(rec + L.gc + c0 * 4) = make_float2(exp2f(e3[0]), exp2f(e3[1]));
+    if (tcrec) {
+      // B2 rows 0..127: Kh^T[dk][tok]; this thread holds 16 tokens of channels c0, c0 + 1
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int k0 = a * SUB + 8 * half;
+        float t0[8], t1[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { t0[i] = kh0v[8 * half + i]; t1[i] = kh1v[8 * half + i]; }
+        *reinterpret_cast<uint4 *>(rec + TcRec::B2 + tc::sw128_off(192, c0, k0)) = tc::pack8(t0);
+        *reinterpret_cast<uint4 *>(rec + TcRec::B2 + tc::sw128_off(192, c0 + 1, k0)) = tc::pack8(t1);
+      }
+    }
+    if (a == 0) {
+      char *gcp = rec + (tcrec ? TcRec::GC : L.gc);
+      *reinterpret_cast<float2 *>(gcp + c0 * 4) = make_float2(exp2f(e3[0]), exp2f(e3[1]));
+    }
   }
   __syncthreads();
   // 3. Gram products: 20 tasks (pair, A|B), warp w takes tasks w, w+8, w+16
@@ -292,10 +318,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       gram16<PRECISE>(acc[u], X + pa * SUB * LDF, RR + pb * SUB * LDF, dv[task >> 1]);
     }
   }
-  __syncthreads();   // KL, QL, R are free from here on
+  __syncthreads();   // QL and R are free from here on
   {
     float *Lm = (float *)(smem + S::LM);
-    Tile<E, 64> bm((E *)(smem + S::BM));
+    Tile<E, 64> bm((E *)(rec + L.bm));
     float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) : nullptr;
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
@@ -310,7 +336,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
           const int r = pa * SUB + g + 8 * hh, j = pb * SUB + 8 * nt + 2 * q;
           const float v0 = acc[u][nt][2 * hh], v1 = acc[u][nt][2 * hh + 1];
           if (task & 1) {
-            st2(bm.at(r, j), j <= r ? v0 : 0.f, j + 1 <= r ? v1 : 0.f);
+            const float b0 = j <= r ? v0 : 0.f, b1 = j + 1 <= r ? v1 : 0.f;
+            if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), b0, b1);
+            else st2(bm.at(r, j), b0, b1);
           } else {
             const float a0 = j < r ? v0 : 0.f, a1 = j + 1 < r ? v1 : 0.f;
             *reinterpret_cast<float2 *>(Lm + r * LDS64 + j) = make_float2(sb[r] * a0, sb[r] * a1);
@@ -318,10 +346,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
           }
         }
     }
-    // zero the upper sub-blocks of the Bm record tile
-    for (int idx = tid; idx < 64 * 64; idx += PREP_THREADS) {
-      const int r = idx >> 6, j = idx & 63;
-      if ((j >> 4) > (r >> 4)) *bm.at(r, j) = from_f<E>(0.f);
+    // zero the sub-blocks of Bm above the diagonal
+    for (int idx = tid; idx < 64 * 32; idx += PREP_THREADS) {
+      const int r = idx >> 5, j = (idx & 31) * 2;
+      if ((j >> 4) > (r >> 4)) {
+        if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), 0.f, 0.f);
+        else st2(bm.at(r, j), 0.f, 0.f);
+      }
     }
   }
   __syncthreads();
@@ -336,20 +367,28 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       for (int i = 0; i < SUB; ++i) x[i] = (i == j) ? 1.f : 0.f;
 #pragma unroll
       for (int i = 1; i < SUB; ++i) {
-        float s = 0.f;
+        float s_ = 0.f;
 #pragma unroll
-        for (int m = 0; m < i; ++m) s = fmaf(Lm[(ab * SUB + i) * LDS64 + ab * SUB + m], x[m], s);
-        if (i > j) x[i] = -s;
+        for (int m = 0; m < i; ++m) s_ = fmaf(Lm[(ab * SUB + i) * LDS64 + ab * SUB + m], x[m], s_);
+        if (i > j) x[i] = -s_;
       }
       if (lane < SUB) {
 #pragma unroll
         for (int i = 0; i < SUB; ++i) T[(ab * SUB + i) * LDS64 + ab * SUB + j] = x[i];
       }
     } else {
-      // warps 4..7 zero the blocks above the diagonal
+      // warps 4..7 zero the blocks above the diagonal and turn KL into Kt = KL exp(E_{a-1})
       for (int idx = tid - 128; idx < 64 * 64; idx += 128) {
         const int r = idx >> 6, j = idx & 63;
         if ((j >> 4) > (r >> 4)) T[r * LDS64 + j] = 0.f;
+      }
+      if (tcrec) {
+        for (int idx = tid - 128; idx < 64 * 64; idx += 128) {
+          const int r = idx >> 6, c = (idx & 63) * 2;
+          float2 *kp = reinterpret_cast<float2 *>(KL + r * LDF + c);
+          const float2 kv = *kp;
+          *kp = make_float2(kv.x * pvv[r >> 4][c], kv.y * pvv[r >> 4][c + 1]);
+        }
       }
     }
     __syncthreads();
@@ -382,31 +421,58 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       __syncthreads();
     }
   }
-  // 5. Tb = T Diag(beta) into the record tile; copy the staged tiles out
+  // 5. Tb = T Diag(beta) (fp32 in place, and into the record); T for the backward
   {
-    const float *T = (const float *)(smem + S::TT);
-    Tile<E, 64> tb((E *)(smem + S::TB));
+    float *T = (float *)(smem + S::TT);
+    Tile<E, 64> tb((E *)(rec + L.tb));
     float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) + 64 * 64 : nullptr;
     for (int idx = tid; idx < 64 * 32; idx += PREP_THREADS) {
       const int r = idx >> 5, j = (idx & 31) * 2;
       const float t0 = T[r * LDS64 + j], t1 = T[r * LDS64 + j + 1];
-      st2(tb.at(r, j), t0 * sb[j], t1 * sb[j + 1]);
+      const float b0 = t0 * sb[j], b1 = t1 * sb[j + 1];
+      if (tcrec) {
+        st2((E *)(rec + TcRec::TB + tc::sw128_off(64, r, j)), b0, b1);
+        *reinterpret_cast<float2 *>(T + r * LDS64 + j) = make_float2(b0, b1);
+      } else {
+        st2(tb.at(r, j), b0, b1);
+      }
       if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(t0, t1);
     }
   }
-  __syncthreads();
-  {
-    const int T64 = 64 * 64 * (int)sizeof(E);
-    for (int o = tid * 16; o < T64; o += PREP_THREADS * 16) {
-      *reinterpret_cast<uint4 *>(rec + L.tb + o) = *reinterpret_cast<const uint4 *>(smem + S::TB + o);
-      *reinterpret_cast<uint4 *>(rec + L.bm + o) = *reinterpret_cast<const uint4 *>(smem + S::BM + o);
+  if (tcrec) {
+    __syncthreads();
+    // 6. W = Tb Kt (64 x 128): B1 rows 64..127 hold -W[tok][dk]. Warp: rows 16*(w&3), columns 64*(w>>2).
+    const float *Tb = (const float *)(smem + S::TT);
+    const int mt = warp & 3, nh = warp >> 2;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float wacc[4][4];
+      zero(wacc);
+      const int n0 = 64 * nh + 32 * half;
+      for (int kk = 0; kk < 16 * (mt + 1); kk += 8) {
+        uint32_t af[4];
+        af[0] = tf32(Tb[(16 * mt + g) * LDS64 + kk + q]);
+        af[1] = tf32(Tb[(16 * mt + g + 8) * LDS64 + kk + q]);
+        af[2] = tf32(Tb[(16 * mt + g) * LDS64 + kk + q + 4]);
+        af[3] = tf32(Tb[(16 * mt + g + 8) * LDS64 + kk + q + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+          mma1688(wacc[nt], af, tf32(KL[(kk + q) * LDF + n0 + 8 * nt + g]), tf32(KL[(kk + q + 4) * LDF + n0 + 8 * nt + g]));
+      }
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * mt + g + 8 * hh, c = n0 + 8 * nt + 2 * q;
+          st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, 64 + r, c)), -wacc[nt][2 * hh], -wacc[nt][2 * hh + 1]);
+        }
     }
   }
 }
 
 template <typename E>
 static cudaError_t launch_prep_t(const PrepParams &p, cudaStream_t s) {
-  using S = PrepSmem2<E>;
+  using S = PrepSmem2;
   auto kern = kda_prep_kernel<E>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
   if (e != cudaSuccess) return e;

@@ -1,0 +1,267 @@
+// kda_scan_tc.cu -- the forward inter-chunk state passing on 5th-generation tensor cores.
+//
+// One CTA (4 warps) per (sequence, head). The 128x128 fp32 state lives in tensor
+// memory for the whole sequence, transposed: TMEM lane m = value channel m,
+// column n = key channel n (S^T). Thread t of warp w owns lane 32w + t, so every
+// elementwise pass is a row pass. TMEM columns: [0,128) S^T, [128,192) O^T,
+// [192,256) U^T. Per 64-token chunk, with the record of the prep kernel
+// (B1 = [Qt; -W], B2 = [Kh^T; Bm], Tb, gC; W = Tb Kt folds the intra-chunk
+// WY/UT transform into one operand):
+//
+//   pass A : S^T -> bf16 operand tile (and the saved chunk-start state);
+//            S^T <- S^T Diag(gC) in TMEM; values V^T -> operand tile
+//   phase 1: [O^T | U^T]  = S^T [Qt; -W]^T          (M=128, N=128, K=128)
+//            U^T         += V^T Tb^T                 (M=128, N=64,  K=64)
+//   pass B : U^T -> bf16 operand tile
+//   phase 2: [S^T | O^T] += U^T [Kh^T; Bm]^T         (M=128, N=192, K=64)
+//
+// i.e. U = Tb (V - Kt S), O = Qt S + Bm U, S <- gC*S + Kh^T U. One thread issues
+// the MMAs; completion is signalled through mbarriers (tcgen05.commit). The next
+// chunk's record arrives by TMA bulk copy into the second of two buffers, and
+// the next chunk's values are loaded into registers one chunk ahead. Every wait
+// is bounded; on a timeout the kernel reports KDA_ERR_TIMEOUT, frees its tensor
+// memory and returns.
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "kda_tc05.cuh"
+
+namespace kda {
+
+struct TcScanSmem {
+  static constexpr int RECS = (TcRec::BYTES + 1023) / 1024 * 1024;
+  static constexpr int REC0 = 0, REC1 = RECS;
+  static constexpr int AS = 2 * RECS;        // S^T bf16 [128][K=128]: two 16 KB blocks
+  static constexpr int AU = AS + 32768;      // U^T bf16 [128][K=64]
+  static constexpr int AV = AU + 16384;      // V^T bf16 [128][K=64]
+  static constexpr int OST = AV + 16384;     // output staging [64 tok][128] bf16, plain rows
+  static constexpr int BAR = OST + 16384;    // record buffers 0/1, phase 1, phase 2
+  static constexpr int TSLOT = BAR + 32;
+  static constexpr int BYTES = TSLOT + 32 + 1024;   // + alignment slack
+};
+
+__device__ __forceinline__ void tc_issue_record(char *dst, const char *src, uint64_t *bar) {
+  fence_proxy_async();
+  mbar_expect_tx(bar, TcRec::BYTES);
+  bulk_g2s(dst, src, TcRec::BYTES, bar);
+}
+
+__global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p) {
+  using S = TcScanSmem;
+  extern __shared__ __align__(1024) char smem_raw[];
+  // operand tiles need 1024-byte alignment in the shared window
+  char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int H = p.geo.heads, h = blockIdx.x % H, seq = blockIdx.x / H;
+  const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
+  const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
+  const int tid = threadIdx.x, warp = tid >> 5, row = tid;   // row = TMEM lane = value channel
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + S::TSLOT);
+  const bf16 *v = (const bf16 *)p.v;
+  bf16 *o = (bf16 *)p.o;
+  const size_t sh = (size_t)seq * H + h;
+
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tc::alloc(tslot, 256);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's lane quarter
+
+  auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * TcRec::BYTES; };
+  // values of chunk j: 16-byte coalesced loads (row r = idx / 16, chunk idx % 16) held in registers
+  auto load_v = [&](int j, uint4 (&vr)[8]) {
+    const long long t0 = s0 + (long long)j * CH;
+    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = tid + 128 * i, r = idx >> 4, ch = idx & 15;
+      vr[i] = make_uint4(0, 0, 0, 0);
+      if (r < clen) vr[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
+    }
+  };
+  auto store_o = [&](int j) {   // staging -> o rows of chunk j
+    const long long t0 = s0 + (long long)j * CH;
+    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+    for (int idx = tid; idx < 64 * 16; idx += 128) {
+      const int r = idx >> 4, ch = idx & 15;
+      if (r < clen)
+        *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + r) * H + h) * 128 + ch * 8) =
+            *reinterpret_cast<const uint4 *>(smem + S::OST + r * 256 + ch * 16);
+    }
+  };
+  auto stage_o = [&]() {        // O^T (TMEM) -> staging [tok][value channel]
+    uint32_t r[64];
+    tc::ld64(tl + 128, r);
+    tc::wait_ld();
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      *reinterpret_cast<bf16 *>(smem + S::OST + i * 256 + row * 2) = __float2bfloat16_rn(__uint_as_float(r[i]));
+  };
+
+  // initial state: S^T[dv][dk] = h0[dk][dv]
+  {
+    float buf[16];
+#pragma unroll
+    for (int cb = 0; cb < 8; ++cb) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        buf[i] = p.h0 ? p.h0[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f;
+      tc::st16(tl + 16 * cb, buf);
+    }
+    tc::wait_st();
+  }
+  if (tid == 0 && nch > 0) {
+    tc_issue_record(smem + S::REC0, rec_of(0), &bar[0]);
+    if (nch > 1) tc_issue_record(smem + S::REC1, rec_of(1), &bar[1]);
+  }
+  uint4 vr[8];
+  if (nch > 0) load_v(0, vr);
+  bool ok = true;
+  int done = 0;   // chunks whose phase 2 was issued
+  for (int j = 0; j < nch; ++j) {
+    const int b = j & 1;
+    char *rb = smem + (b ? S::REC1 : S::REC0);
+    ok &= mbar_wait(&bar[b], (j >> 1) & 1);
+    if (j > 0) ok &= mbar_wait(&bar[3], (j - 1) & 1);
+    tc::fence_after();
+    if (!__syncthreads_and(ok)) break;
+    // pass A: state -> operand tile (+ saved state), scaled state back to TMEM;
+    // this chunk's values -> plain [tok][128] rows in the U tile (free until pass B)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = tid + 128 * i;
+      *reinterpret_cast<uint4 *>(smem + S::AU + (idx >> 4) * 256 + (idx & 15) * 16) = vr[i];
+    }
+    {
+      const float *gC = reinterpret_cast<const float *>(rb + TcRec::GC);
+      bf16 *sv = p.saved ? (bf16 *)p.saved + ((size_t)(cbase + j) * H + h) * 128 * 128 : nullptr;
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {   // 64 key channels at a time, one TMEM round trip each
+        uint32_t r[64];
+        tc::ld64(tl + 64 * hb, r);
+        tc::wait_ld();
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+          float buf[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) buf[i] = __uint_as_float(r[16 * cb + i]);
+          const int k0 = 64 * hb + 16 * cb;
+          const uint4 lo = tc::pack8(buf), hi = tc::pack8(buf + 8);
+          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0)) = lo;
+          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = hi;
+          if (sv) {   // chunk-start state S^T[dv][dk] in the swizzled 128x128 tile layout
+            Tile<bf16, 128> t(sv);
+            *reinterpret_cast<uint4 *>(t.at(row, k0)) = lo;
+            *reinterpret_cast<uint4 *>(t.at(row, k0 + 8)) = hi;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) buf[i] *= gC[k0 + i];
+          tc::st16(tl + k0, buf);
+        }
+      }
+      if (j > 0) stage_o();
+      tc::wait_st();
+    }
+    __syncthreads();
+    // V^T operand: row = value channel, 64 tokens
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t lo = *reinterpret_cast<const unsigned short *>(smem + S::AU + (8 * c + 2 * e) * 256 + row * 2);
+        const uint32_t hi = *reinterpret_cast<const unsigned short *>(smem + S::AU + (8 * c + 2 * e + 1) * 256 + row * 2);
+        w[e] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint4 *>(smem + S::AV + tc::sw128_off(128, row, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    fence_proxy_async();
+    tc::fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t as = smem_u32(smem + S::AS), b1 = smem_u32(rb + TcRec::B1);
+      const uint32_t av = smem_u32(smem + S::AV), tb = smem_u32(rb + TcRec::TB);
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem + 128, tc::desc_sw128(as + kb * 16384 + 32 * ks), tc::desc_sw128(b1 + kb * 16384 + 32 * ks),
+                       tc::idesc_bf16(128, 128), (kb | ks) != 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc::mma_bf16(tmem + 192, tc::desc_sw128(av + 32 * ks), tc::desc_sw128(tb + 32 * ks), tc::idesc_bf16(128, 64), 1);
+      tc::commit(&bar[2]);
+      if (j >= 1 && j + 1 < nch) tc_issue_record(smem + ((j + 1) & 1 ? S::REC1 : S::REC0), rec_of(j + 1), &bar[(j + 1) & 1]);
+    }
+    if (j > 0) store_o(j - 1);
+    if (j + 1 < nch) load_v(j + 1, vr);
+    ok &= mbar_wait(&bar[2], j & 1);
+    tc::fence_after();
+    // pass B: U^T -> operand tile
+    {
+      uint32_t r[64];
+      tc::ld64(tl + 192, r);
+      tc::wait_ld();
+#pragma unroll
+      for (int cb = 0; cb < 8; ++cb) {
+        float buf[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) buf[i] = __uint_as_float(r[8 * cb + i]);
+        *reinterpret_cast<uint4 *>(smem + S::AU + tc::sw128_off(128, row, 8 * cb)) = tc::pack8(buf);
+      }
+    }
+    fence_proxy_async();
+    tc::fence_before();
+    if (!__syncthreads_and(ok)) break;
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t au = smem_u32(smem + S::AU), b2 = smem_u32(rb + TcRec::B2);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc::mma_bf16(tmem, tc::desc_sw128(au + 32 * ks), tc::desc_sw128(b2 + 32 * ks), tc::idesc_bf16(128, 192), 1);
+      tc::commit(&bar[3]);
+    }
+    done = j + 1;
+  }
+  if (ok && done > 0) ok = mbar_wait(&bar[3], (done - 1) & 1);
+  tc::fence_after();
+  if (__syncthreads_and(ok)) {
+    if (done > 0) {
+      stage_o();
+      __syncthreads();
+      store_o(done - 1);
+    }
+    if (p.hT) {   // hT[dk][dv] = S^T[dv][dk]
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t r[64];
+        tc::ld64(tl + 64 * hb, r);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 64; ++i) p.hT[(sh * 128 + 64 * hb + i) * 128 + row] = __uint_as_float(r[i]);
+      }
+    }
+  } else {
+    report(p.status, ERR_TIMEOUT);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, 256);
+}
+
+cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
+  const long long units = (long long)p.geo.n_seqs * p.geo.heads;
+  if (units == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kda_fwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TcScanSmem::BYTES);
+  if (e != cudaSuccess) return e;
+  kda_fwd_scan_tc_kernel<<<(unsigned)units, 128, TcScanSmem::BYTES, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -52,7 +52,7 @@ size_t elem_size(int io) { return io == KDA_F32 ? 4 : 2; }
 
 // Workspace carving shared by the forward and the backward.
 struct WsPlan {
-  size_t cu, choff, img, dsaved, grad, aux, bytes;
+  size_t cu, choff, img, dsaved, grad, aux, img2, bytes;
 };
 
 WsPlan plan(const kda_fwd_args *a, bool bwd) {
@@ -71,6 +71,8 @@ WsPlan plan(const kda_fwd_args *a, bool bwd) {
     end = w.grad + mc * H * kda::GradLayout::bytes;
     w.aux = round_up(end, 256);
     end = w.aux + mc * H * 2 * 64 * 64 * sizeof(float);
+    w.img2 = round_up(end, 256);
+    end = w.img2 + mc * H * kda::TcRecB::BYTES;
   }
   w.bytes = round_up(end, 256);
   return w;
@@ -186,7 +188,7 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_fwd chunk table");
   mark(0, stream);
-  kda::PrepParams pp{geo, a->q, a->k, a->g, a->beta, a->scale, ws + w.img, nullptr, f32 ? 0 : 1, a->dev_status};
+  kda::PrepParams pp{geo, a->q, a->k, a->g, a->beta, a->scale, ws + w.img, nullptr, f32 ? 0 : 1, nullptr, a->dev_status};
   if ((e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
   kda::FwdScanParams sp{geo, a->v, ws + w.img, a->h0, a->o, a->hT, a->saved, a->dev_status};
@@ -236,12 +238,12 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_bwd chunk table");
   mark(0, stream);
-  kda::PrepParams pp{geo, f->q, f->k, f->g, f->beta, f->scale, ws + w.img, reinterpret_cast<float *>(ws + w.aux), 0, f->dev_status};
+  kda::PrepParams pp{geo,       f->q, f->k, f->g, f->beta, f->scale, ws + w.img, reinterpret_cast<float *>(ws + w.aux),
+                     2,         ws + w.img2, f->dev_status};
   if ((e = kda::launch_prep(pp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd prep");
   mark(1, stream);
-  kda::BwdScanParams bp{geo, a->dO, ws + w.img, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
-  if ((e = kda::launch_bwd_scan(bp, false, pick_slice(f), stream)) != cudaSuccess)
-    return cuda_fail(e, "kda_bwd dS scan");
+  kda::BwdScanParams bp{geo, a->dO, ws + w.img2, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
+  if ((e = kda::launch_bwd_scan_tc(bp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd dS scan");
   mark(2, stream);
   kda::BwdStateParams sp{geo, f->v, a->dO, ws + w.img, f->saved, ws + w.dsaved,
                          reinterpret_cast<float *>(ws + w.grad), f->dev_status};

@@ -4,8 +4,8 @@
 // gradient dS at the chunk end and the value gradient. Two chunk-parallel
 // kernels then finish the chunk-local gradients:
 //
-//  state kernel (per chunk, head), with the forward's chunk-start state S (kept
-//  transposed, S^T[v][k], as the forward scan produces it):
+//  state kernel (per chunk, head), with the forward's chunk-start state S and the
+//  chunk-end state gradient dS (both kept transposed, [v][k], as the scans produce them):
 //     V' = V - Kt S,  U = Tb V',  dU = Bm^T dO + Kh dS,  dV' = Tb^T dU
 //     dQt = dO S^T,   dKt = -dV' S^T,  dKh = U dS^T,
 //     dBm = dO U^T (j <= r),  dTb = dU V'^T (j <= r),  dgC_c = sum_v S_cv dS_cv
@@ -28,7 +28,7 @@ struct StateSmem {
   static constexpr int QT = 0, KT = T128, TB = 2 * T128, BM = TB + T64, KH = BM + T64, GC = KH + T128;
   static constexpr int REC = GC + 512;
   static constexpr int SS = (REC + 127) / 128 * 128;      // S^T [128][128]
-  static constexpr int SDS = SS + 2 * T128;               // dS [128][128]
+  static constexpr int SDS = SS + 2 * T128;               // dS^T [128][128]
   static constexpr int SV = SDS + 2 * T128;               // V -> V' [64][128]
   static constexpr int SDO = SV + T128;
   static constexpr int SU = SDO + T128;
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
       st2(sU.at(r0 + 8 * hh, 64 * nh + 8 * nt + 2 * q4), acc[nt][2 * hh], acc[nt][2 * hh + 1]);
   zero(acc);
   wgemm<false, false, 8>(acc, Bm, 16 * mt, sdO, 64 * nh, 16 * mt, 64);
-  wgemm<true, false, 8>(acc, Kh, 16 * mt, sdS, 64 * nh, 0, 128);
+  wgemm<true, true, 8>(acc, Kh, 16 * mt, sdS, 64 * nh, 0, 128);   // B(k=c, n=v) = dS^T[v][c]
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -162,17 +162,14 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
   wgemm<true, false, 8>(acc, sdO, 16 * mt, sS, 64 * nh, 0, 128);   // B(k=v, n=c) = S^T[v][c]
   store128(rec + GradLayout::dqt / 4, acc);
   zero(acc);
-  wgemm<true, true, 8>(acc, sU, 16 * mt, sdS, 64 * nh, 0, 128);
+  wgemm<true, false, 8>(acc, sU, 16 * mt, sdS, 64 * nh, 0, 128);  // B(k=v, n=c) = dS^T[v][c]
   store128(rec + GradLayout::dkh / 4, acc);
   zero(acc);
   wgemm<true, false, 8>(acc, sdV, 16 * mt, sS, 64 * nh, 0, 128);
   store128(rec + GradLayout::dkt / 4, acc);
-  if (tid < 128) {   // dgC_c = sum_v S[c][v] dS[c][v] = sum_v S^T[v][c] dS[c][v]
+  if (tid < 128) {   // dgC_c = sum_v S[c][v] dS[c][v] = sum_v S^T[v][c] dS^T[v][c]
     float s = 0.f;
-    for (int vv = 0; vv < 128; vv += 2) {
-      const float2 b = ld2(sdS.at(tid, vv));
-      s = fmaf(to_f(*sS.at(vv, tid)), b.x, fmaf(to_f(*sS.at(vv + 1, tid)), b.y, s));
-    }
+    for (int vv = 0; vv < 128; ++vv) s = fmaf(to_f(*sS.at(vv, tid)), to_f(*sdS.at(vv, tid)), s);
     rec[GradLayout::dgc / 4 + tid] = s;
   }
 }

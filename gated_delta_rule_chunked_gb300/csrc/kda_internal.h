@@ -39,6 +39,16 @@ struct TcRec {
   static constexpr int B1 = 0, B2 = 32768, TB = B2 + 24576, GC = TB + 8192, BYTES = GC + 512;
 };
 
+// Per-(chunk, head) record for the tcgen05 backward dS scan (bf16), same format:
+//   BMT [64 rows r][K = 64 j] : Bm^T (Bm[j][r])
+//   KH  [64 rows tok][K = 128]: Kh[tok][dk]
+//   QWT [128 rows dk][K = 128]: K < 64: Qt^T[dk][tok], K >= 64: -W^T[dk][tok]
+//   TBT [64 rows r][K = 64 j] : Tb^T (Tb[j][r])
+//   GC  128 fp32              : exp(G_last)
+struct TcRecB {
+  static constexpr int BMT = 0, KH = 8192, QWT = KH + 16384, TBT = QWT + 32768, GC = TBT + 8192, BYTES = GC + 512;
+};
+
 // Per-(chunk, head) record of state-side gradients written by the backward's
 // state kernel: dQt, dKt, dKh (64x128 fp32 each), dBm, dTb (64x64 fp32), dgC (128).
 struct GradLayout {
@@ -62,7 +72,9 @@ struct PrepParams {
   float scale;
   void *img;               // [max_chunks][H] records (ImgLayout, or TcRec when tc_layout)
   float *aux;              // optional [max_chunks][H] x {A (strict lower), T} fp32 64x64 each
-  int tc_layout;           // bf16 only: write the tcgen05 forward record
+  int tc_layout;           // bf16 only: 1 = write the tcgen05 forward record (to img);
+                           // 2 = also write the tcgen05 backward record (to img2)
+  void *img2;              // [max_chunks][H] TcRecB records (tc_layout == 2)
   int *status;
 };
 
@@ -81,11 +93,11 @@ struct FwdScanParams {
 struct BwdScanParams {
   SeqGeom geo;
   const void *dO;
-  const void *img;
+  const void *img;         // TcRecB records for the tcgen05 scan, ImgLayout records otherwise
   const float *dhT;
   float *dv;
   float *dh0;
-  void *dsaved;            // [max_chunks][H] 128x128 E tiles: dS at each chunk end
+  void *dsaved;            // [max_chunks][H] 128x128 E tiles (swizzled): dS^T[v][k] at each chunk end
   int *status;
 };
 
@@ -124,6 +136,7 @@ cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
 cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_scan(const BwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
+cudaError_t launch_bwd_scan_tc(const BwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_state(const BwdStateParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_bwd_intra(const BwdIntraParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s);

@@ -90,7 +90,8 @@ struct PrepSmem2 {
   static constexpr int LM = QL;                              // fp32 [64][LDS64]  Diag(beta) A
   static constexpr int TT = LM + 64 * LDS64 * 4;             // fp32 [64][LDS64]  T, then T Diag(beta)
   static constexpr int SCR = TT + 64 * LDS64 * 4;            // fp32 4 x [16][LDP]
-  static_assert(SCR + 4 * 16 * LDP * 4 <= DV, "solver tiles overlap the vectors");
+  static constexpr int BMS = SCR + 4 * 16 * LDP * 4;         // bf16 [64][64] Bm staging (backward record)
+  static_assert(BMS + 64 * 64 * 2 <= DV, "solver tiles overlap the vectors");
 };
 
 __device__ __forceinline__ void pair_of(int p, int &a, int &b) {
@@ -174,7 +175,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
   // tcgen05 record (bf16 forward) or the tile record (fp32 forward, backward)
-  const bool tcrec = !PRECISE && p.tc_layout;
+  const bool tcrec = !PRECISE && p.tc_layout == 1;   // forward tcgen05 record instead of the tiles
+  const bool bwdrec = !PRECISE && p.tc_layout == 2;  // tiles plus the backward tcgen05 record
   const E *qg = (const E *)p.q, *kg = (const E *)p.k;
   float *rq = (float *)(smem + S::RQ), *rk = (float *)(smem + S::RK), *sb = (float *)(smem + S::BETA);
   float *KL = (float *)(smem + S::KL), *QL = (float *)(smem + S::QL), *RR = (float *)(smem + S::R);
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   const ImgLayout L(sizeof(E));
   const size_t rec_bytes = tcrec ? (size_t)TcRec::BYTES : L.bytes;
   char *rec = (char *)p.img + ((size_t)chunk * H + h) * rec_bytes;
+  char *recb = bwdrec ? (char *)p.img2 + ((size_t)chunk * H + h) * TcRecB::BYTES : nullptr;
 
   // 1. row norms: 4 threads per row, 32 channels each
   {
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
     pvv[a][c0] = pa0;
     pvv[a][c0 + 1] = pa1;
     Tile<E, 128> tqt((E *)(rec + L.qt)), tkt((E *)(rec + L.kt)), tkh((E *)(rec + L.kh));
-    float kh0v[SUB], kh1v[SUB];
+    float kh0v[SUB], kh1v[SUB], qt0v[SUB], qt1v[SUB];
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
@@ -282,9 +285,24 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
         // B1 rows 0..63: Qt[tok][dk] = q^ exp(G_r)
         st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, r, c0)), ql0 * pa0, ql1 * pa1);
       } else {
-        st2(tqt.at(r, c0), ql0 * pa0, ql1 * pa1);   // Qt = q^ exp(G_r)
-        st2(tkt.at(r, c0), kl0 * pa0, kl1 * pa1);   // Kt = k^ exp(G_r)
+        if (!bwdrec) st2(tqt.at(r, c0), ql0 * pa0, ql1 * pa1);   // Qt = q^ exp(G_r) (unused by the backward)
+        st2(tkt.at(r, c0), kl0 * pa0, kl1 * pa1);                 // Kt = k^ exp(G_r)
         st2(tkh.at(r, c0), kh0v[i], kh1v[i]);
+        if (bwdrec) st2((E *)(recb + TcRecB::KH + tc::sw128_off(64, r, c0)), kh0v[i], kh1v[i]);
+      }
+      qt0v[i] = ql0 * pa0;
+      qt1v[i] = ql1 * pa1;
+    }
+    if (bwdrec) {
+      // QWT rows dk, K-block 0: Qt^T[dk][tok] for this thread's 16 tokens
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int k0 = a * SUB + 8 * half;
+        float t0[8], t1[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { t0[i] = qt0v[8 * half + i]; t1[i] = qt1v[8 * half + i]; }
+        *reinterpret_cast<uint4 *>(recb + TcRecB::QWT + tc::sw128_off(128, c0, k0)) = tc::pack8(t0);
+        *reinterpret_cast<uint4 *>(recb + TcRecB::QWT + tc::sw128_off(128, c0 + 1, k0)) = tc::pack8(t1);
       }
     }
     if (tcrec) {
@@ -302,6 +320,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
     if (a == 0) {
       char *gcp = rec + (tcrec ? TcRec::GC : L.gc);
       *reinterpret_cast<float2 *>(gcp + c0 * 4) = make_float2(exp2f(e3[0]), exp2f(e3[1]));
+      if (bwdrec) *reinterpret_cast<float2 *>(recb + TcRecB::GC + c0 * 4) = make_float2(exp2f(e3[0]), exp2f(e3[1]));
     }
   }
   __syncthreads();
@@ -339,6 +358,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
             const float b0 = j <= r ? v0 : 0.f, b1 = j + 1 <= r ? v1 : 0.f;
             if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), b0, b1);
             else st2(bm.at(r, j), b0, b1);
+            if (bwdrec) st2((E *)(smem + S::BMS) + r * 64 + j, b0, b1);   // staged, transposed below
           } else {
             const float a0 = j < r ? v0 : 0.f, a1 = j + 1 < r ? v1 : 0.f;
             *reinterpret_cast<float2 *>(Lm + r * LDS64 + j) = make_float2(sb[r] * a0, sb[r] * a1);
@@ -352,6 +372,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       if ((j >> 4) > (r >> 4)) {
         if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), 0.f, 0.f);
         else st2(bm.at(r, j), 0.f, 0.f);
+        if (bwdrec) st2((E *)(smem + S::BMS) + r * 64 + j, 0.f, 0.f);
       }
     }
   }
@@ -382,7 +403,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
         const int r = idx >> 6, j = idx & 63;
         if ((j >> 4) > (r >> 4)) T[r * LDS64 + j] = 0.f;
       }
-      if (tcrec) {
+      if (tcrec || bwdrec) {
         for (int idx = tid - 128; idx < 64 * 64; idx += 128) {
           const int r = idx >> 6, c = (idx & 63) * 2;
           float2 *kp = reinterpret_cast<float2 *>(KL + r * LDF + c);
@@ -432,16 +453,17 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       const float b0 = t0 * sb[j], b1 = t1 * sb[j + 1];
       if (tcrec) {
         st2((E *)(rec + TcRec::TB + tc::sw128_off(64, r, j)), b0, b1);
-        *reinterpret_cast<float2 *>(T + r * LDS64 + j) = make_float2(b0, b1);
       } else {
         st2(tb.at(r, j), b0, b1);
       }
+      if (tcrec || bwdrec) *reinterpret_cast<float2 *>(T + r * LDS64 + j) = make_float2(b0, b1);
       if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(t0, t1);
     }
   }
   if (tcrec) {
     __syncthreads();
-    // 6. W = Tb Kt (64 x 128): B1 rows 64..127 hold -W[tok][dk]. Warp: rows 16*(w&3), columns 64*(w>>2).
+    // 6. W = Tb Kt (64 x 128): forward B1 rows 64..127 hold -W[tok][dk].
+    //    Warp: rows 16*(w&3), columns 64*(w>>2).
     const float *Tb = (const float *)(smem + S::TT);
     const int mt = warp & 3, nh = warp >> 2;
 #pragma unroll
@@ -466,6 +488,44 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
           const int r = 16 * mt + g + 8 * hh, c = n0 + 8 * nt + 2 * q;
           st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, 64 + r, c)), -wacc[nt][2 * hh], -wacc[nt][2 * hh + 1]);
         }
+    }
+  }
+  if (bwdrec) {
+    __syncthreads();
+    // 6'. backward record: -W^T = -(Kt^T Tb^T) (128 x 64) into QWT K-block 1 (warp w: rows dk 16w..16w+15);
+    //     Bm^T and Tb^T as 16-byte chunks from shared memory.
+    const float *Tb = (const float *)(smem + S::TT);
+    float wacc[8][4];
+    zero(wacc);
+    for (int kk = 0; kk < 64; kk += 8) {
+      uint32_t af[4];   // A(m = dk, k = j) = Kt[j][dk]
+      af[0] = tf32(KL[(kk + q) * LDF + 16 * warp + g]);
+      af[1] = tf32(KL[(kk + q) * LDF + 16 * warp + g + 8]);
+      af[2] = tf32(KL[(kk + q + 4) * LDF + 16 * warp + g]);
+      af[3] = tf32(KL[(kk + q + 4) * LDF + 16 * warp + g + 8]);
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)   // B(k = j, n = r) = Tb[r][j]
+        if (kk <= 8 * nt + 7)
+          mma1688(wacc[nt], af, tf32(Tb[(8 * nt + g) * LDS64 + kk + q]), tf32(Tb[(8 * nt + g) * LDS64 + kk + q + 4]));
+    }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int c = 16 * warp + g + 8 * hh, r = 8 * nt + 2 * q;
+        st2((E *)(recb + TcRecB::QWT + tc::sw128_off(128, c, 64 + r)), -wacc[nt][2 * hh], -wacc[nt][2 * hh + 1]);
+      }
+    // Bm^T and Tb^T: one 16-byte chunk (row n, columns 8c..8c+7) per thread and tile
+    for (int idx = tid; idx < 64 * 8; idx += PREP_THREADS) {
+      const int n = idx & 63, c = idx >> 6;
+      float bv[8], tv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        bv[e] = to_f(*((const E *)(smem + S::BMS) + (8 * c + e) * 64 + n));   // Bm[k][n]
+        tv[e] = Tb[(8 * c + e) * LDS64 + n];                                   // Tb[k][n]
+      }
+      *reinterpret_cast<uint4 *>(recb + TcRecB::BMT + tc::sw128_off(64, n, 8 * c)) = tc::pack8(bv);
+      *reinterpret_cast<uint4 *>(recb + TcRecB::TBT + tc::sw128_off(64, n, 8 * c)) = tc::pack8(tv);
     }
   }
 }

@@ -264,4 +264,239 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ----------------------------------------------------------------- backward
+// Reverse dS scan, same arrangement: dS^T in TMEM columns [0,128), dU^T in
+// [128,192), dV^T in [192,256). Per chunk (last to first), with the backward
+// record (Bm^T, Kh, [Qt^T | -W^T], Tb^T, gC):
+//   pass A : dS^T -> bf16 operand tile (and saved as the chunk-end dS);
+//            dS^T <- dS^T Diag(gC); dO^T -> operand tile (K-block 0 of A2)
+//   phase 1: dU^T  = dO^T Bm + dS^T Kh^T           (M=128, N=64, K=64 + 128)
+//   pass B : dU^T -> operand tile (K-block 1 of A2)
+//   phase 2: dS^T += [dO^T | dU^T] [Qt^T | -W^T]^T  (M=128, N=128, K=128)
+//            dV^T  = dU^T Tb                        (M=128, N=64,  K=64)
+// i.e. dU = Bm^T dO + Kh dS, dS <- gC*dS + Qt^T dO - W^T dU, dv = Tb^T dU.
+struct TcBwdSmem {
+  static constexpr int RECS = (TcRecB::BYTES + 1023) / 1024 * 1024;
+  static constexpr int REC0 = 0, REC1 = RECS;
+  static constexpr int AS = 2 * RECS;        // dS^T bf16 [128][K=128]
+  static constexpr int A2 = AS + 32768;      // [dO^T | dU^T] bf16 [128][K=128]
+  static constexpr int DST = A2 + 32768;     // dO staging [64 tok][128] bf16, plain rows
+  static constexpr int BAR = DST + 16384;
+  static constexpr int TSLOT = BAR + 32;
+  static constexpr int BYTES = TSLOT + 32 + 1024;
+};
+
+__global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p) {
+  using S = TcBwdSmem;
+  extern __shared__ __align__(1024) char smem_raw[];
+  char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int H = p.geo.heads, h = blockIdx.x % H, seq = blockIdx.x / H;
+  const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
+  const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
+  const int tid = threadIdx.x, warp = tid >> 5, row = tid;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + S::TSLOT);
+  const bf16 *dO = (const bf16 *)p.dO;
+  const size_t sh = (size_t)seq * H + h;
+
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tc::alloc(tslot, 256);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+
+  auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * TcRecB::BYTES; };
+  auto issue = [&](char *dst, const char *src, uint64_t *b) {
+    fence_proxy_async();
+    mbar_expect_tx(b, TcRecB::BYTES);
+    bulk_g2s(dst, src, TcRecB::BYTES, b);
+  };
+  auto load_do = [&](int j, uint4 (&x)[8]) {
+    const long long t0 = s0 + (long long)j * CH;
+    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = tid + 128 * i, r = idx >> 4, ch = idx & 15;
+      x[i] = make_uint4(0, 0, 0, 0);
+      if (r < clen) x[i] = __ldg(reinterpret_cast<const uint4 *>(dO + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
+    }
+  };
+  auto store_dv = [&](int j) {   // dV^T (TMEM) -> dv rows of chunk j (fp32)
+    const long long t0 = s0 + (long long)j * CH;
+    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+    uint32_t r[64];
+    tc::ld64(tl + 192, r);
+    tc::wait_ld();
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (i < clen) p.dv[((size_t)(t0 + i) * H + h) * 128 + row] = __uint_as_float(r[i]);
+  };
+
+  // initial dS^T[dv][dk] = dhT[dk][dv]
+  {
+    float buf[16];
+#pragma unroll
+    for (int cb = 0; cb < 8; ++cb) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) buf[i] = p.dhT ? p.dhT[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f;
+      tc::st16(tl + 16 * cb, buf);
+    }
+    tc::wait_st();
+  }
+  if (tid == 0 && nch > 0) {
+    issue(smem + S::REC0, rec_of(nch - 1), &bar[0]);
+    if (nch > 1) issue(smem + S::REC1, rec_of(nch - 2), &bar[1]);
+  }
+  uint4 dr[8];
+  if (nch > 0) load_do(nch - 1, dr);
+  bool ok = true;
+  int done = 0, last_j = -1;
+  for (int it = 0; it < nch; ++it) {
+    const int j = nch - 1 - it, b = it & 1;
+    char *rb = smem + (b ? S::REC1 : S::REC0);
+    ok &= mbar_wait(&bar[b], (it >> 1) & 1);
+    if (it > 0) ok &= mbar_wait(&bar[3], (it - 1) & 1);
+    tc::fence_after();
+    if (!__syncthreads_and(ok)) break;
+    // pass A
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = tid + 128 * i;
+      *reinterpret_cast<uint4 *>(smem + S::DST + (idx >> 4) * 256 + (idx & 15) * 16) = dr[i];
+    }
+    if (it > 0) store_dv(j + 1);
+    {
+      const float *gC = reinterpret_cast<const float *>(rb + TcRecB::GC);
+      bf16 *sv = (bf16 *)p.dsaved + ((size_t)(cbase + j) * H + h) * 128 * 128;
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t r[64];
+        tc::ld64(tl + 64 * hb, r);
+        tc::wait_ld();
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+          float buf[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) buf[i] = __uint_as_float(r[16 * cb + i]);
+          const int k0 = 64 * hb + 16 * cb;
+          const uint4 lo = tc::pack8(buf), hi = tc::pack8(buf + 8);
+          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0)) = lo;
+          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = hi;
+          Tile<bf16, 128> t(sv);
+          *reinterpret_cast<uint4 *>(t.at(row, k0)) = lo;
+          *reinterpret_cast<uint4 *>(t.at(row, k0 + 8)) = hi;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) buf[i] *= gC[k0 + i];
+          tc::st16(tl + k0, buf);
+        }
+      }
+      tc::wait_st();
+    }
+    __syncthreads();
+    // dO^T operand (K-block 0 of A2): row = value channel, 64 tokens
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t lo = *reinterpret_cast<const unsigned short *>(smem + S::DST + (8 * c + 2 * e) * 256 + row * 2);
+        const uint32_t hi = *reinterpret_cast<const unsigned short *>(smem + S::DST + (8 * c + 2 * e + 1) * 256 + row * 2);
+        w[e] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint4 *>(smem + S::A2 + tc::sw128_off(128, row, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    fence_proxy_async();
+    tc::fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t a2 = smem_u32(smem + S::A2), as = smem_u32(smem + S::AS);
+      const uint32_t bmt = smem_u32(rb + TcRecB::BMT), kh = smem_u32(rb + TcRecB::KH);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc::mma_bf16(tmem + 128, tc::desc_sw128(a2 + 32 * ks), tc::desc_sw128(bmt + 32 * ks), tc::idesc_bf16(128, 64), ks > 0);
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem + 128, tc::desc_sw128(as + kb * 16384 + 32 * ks), tc::desc_sw128(kh + kb * 8192 + 32 * ks),
+                       tc::idesc_bf16(128, 64), 1);
+      tc::commit(&bar[2]);
+      if (it >= 1 && it + 1 < nch)
+        issue(smem + ((it + 1) & 1 ? S::REC1 : S::REC0), rec_of(j - 1), &bar[(it + 1) & 1]);
+    }
+    if (it + 1 < nch) load_do(j - 1, dr);
+    ok &= mbar_wait(&bar[2], it & 1);
+    tc::fence_after();
+    // pass B: dU^T -> K-block 1 of A2
+    {
+      uint32_t r[64];
+      tc::ld64(tl + 128, r);
+      tc::wait_ld();
+#pragma unroll
+      for (int cb = 0; cb < 8; ++cb) {
+        float buf[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) buf[i] = __uint_as_float(r[8 * cb + i]);
+        *reinterpret_cast<uint4 *>(smem + S::A2 + tc::sw128_off(128, row, 64 + 8 * cb)) = tc::pack8(buf);
+      }
+    }
+    fence_proxy_async();
+    tc::fence_before();
+    if (!__syncthreads_and(ok)) break;
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t a2 = smem_u32(smem + S::A2), qwt = smem_u32(rb + TcRecB::QWT), tbt = smem_u32(rb + TcRecB::TBT);
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem, tc::desc_sw128(a2 + kb * 16384 + 32 * ks), tc::desc_sw128(qwt + kb * 16384 + 32 * ks),
+                       tc::idesc_bf16(128, 128), 1);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc::mma_bf16(tmem + 192, tc::desc_sw128(a2 + 16384 + 32 * ks), tc::desc_sw128(tbt + 32 * ks),
+                     tc::idesc_bf16(128, 64), ks > 0);
+      tc::commit(&bar[3]);
+    }
+    done = it + 1;
+    last_j = j;
+  }
+  if (ok && done > 0) ok = mbar_wait(&bar[3], (done - 1) & 1);
+  tc::fence_after();
+  if (__syncthreads_and(ok)) {
+    if (done > 0) store_dv(last_j);
+    if (p.dh0) {   // dh0[dk][dv] = dS^T[dv][dk]
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t r[64];
+        tc::ld64(tl + 64 * hb, r);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 64; ++i) p.dh0[(sh * 128 + 64 * hb + i) * 128 + row] = __uint_as_float(r[i]);
+      }
+    }
+  } else {
+    report(p.status, ERR_TIMEOUT);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, 256);
+}
+
+cudaError_t launch_bwd_scan_tc(const BwdScanParams &p, cudaStream_t s) {
+  const long long units = (long long)p.geo.n_seqs * p.geo.heads;
+  if (units == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TcBwdSmem::BYTES);
+  if (e != cudaSuccess) return e;
+  kda_bwd_scan_tc_kernel<<<(unsigned)units, 128, TcBwdSmem::BYTES, s>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace kda

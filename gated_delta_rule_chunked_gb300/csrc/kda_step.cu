@@ -1,16 +1,25 @@
 // kda_step.cu -- recurrent decode / draft-verify step (memory-bound).
 //
-// One CTA per (sequence, head). The 128x128 fp32 state (64 KiB) is read once
-// into registers (8 warps x 16 rows, each lane 4 consecutive value columns, so
-// every row is one coalesced 512-byte float4 access), advanced through the L
-// tokens of the call, and written back once -- after accept_len tokens, the
-// accepted prefix (ReplaySSM advances KDA state only through accepted tokens:
-// "Kimi K3 on Fireworks", rollout section, speculative decoding paragraph).
+// One CTA per (sequence, head). The 128x128 fp32 state S0 (64 KiB) is read
+// once into registers (8 warps x 16 key rows, each lane 4 consecutive value
+// columns, so every row is one coalesced 512-byte float4 access) and written
+// back once, after accept_len tokens -- the accepted prefix (ReplaySSM advances
+// KDA state only through accepted tokens: "Kimi K3 on Fireworks", rollout
+// section, speculative decoding paragraph).
 //
-// Per token (gated delta rule, channel-wise decay on the key rows):
-//   S' = Diag(exp g) S;  w = S'^T k^;  p = S'^T q^;  u = beta (v - w)
-//   S  = S' + k^ u^T;    o = S^T q^ = p + u (k^ . q^)
-// The two column reductions w and p share one pass over the state.
+// The L tokens of a call are evaluated against S0 together instead of one at a
+// time (the KDA recurrence unrolled over the call). With G_l = g_1 + .. + g_l
+// (per key channel), gamma_l = exp(G_l) and the token recurrence
+//   S_l = Diag(exp g_l) S_{l-1} + k^_l u_l^T,  u_l = beta_l (v_l - (Diag(exp g_l) S_{l-1})^T k^_l),
+//   o_l = S_l^T q^_l,
+// every quantity is S0 seen through a decayed vector plus a small coupling
+// between the call's own tokens:
+//   w_l = S0^T (gamma_l o k^_l) + sum_{m<l} a_lm u_m,   a_lm = sum_c k^_m k^_l exp(G_l - G_m)
+//   o_l = S0^T (gamma_l o q^_l) + sum_{m<l} b_lm u_m + (k^_l . q^_l) u_l,
+//                                                     b_lm = sum_c k^_m q^_l exp(G_l - G_m)
+//   S_A = Diag(gamma_A) S0 + sum_{m<=A} (exp(G_A - G_m) o k^_m) u_m^T   (A = accept_len).
+// So the state is swept twice per call (2L column sums, then one rank-A
+// update), with one cross-warp reduction, instead of twice per token.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -22,135 +31,250 @@ constexpr int STEP_MAX_L = 8;
 template <typename IO>
 __device__ __forceinline__ float ld_io(const IO *p) { return to_f(*p); }
 
-template <typename IO>
-__device__ __forceinline__ void st_io4(IO *p, float a, float b, float c, float d);
-template <>
-__device__ __forceinline__ void st_io4<bf16>(bf16 *p, float a, float b, float c, float d) {
-  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
-  uint2 u;
-  u.x = *reinterpret_cast<uint32_t *>(&lo);
-  u.y = *reinterpret_cast<uint32_t *>(&hi);
-  *reinterpret_cast<uint2 *>(p) = u;
-}
-template <>
-__device__ __forceinline__ void st_io4<float>(float *p, float a, float b, float c, float d) {
-  *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
-}
+__device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
+
+// Shared memory of one CTA (static part; the column-sum partials are dynamic).
+struct StepSmem {
+  float q[STEP_MAX_L][D];    // q^ (times scale)
+  float k[STEP_MAX_L][D];    // k^
+  float v[STEP_MAX_L][D];
+  float G[STEP_MAX_L][D];    // raw g, then the running sums G_l
+  float kt[STEP_MAX_L][D];   // gamma_l o k^_l
+  float qt[STEP_MAX_L][D];   // gamma_l o q^_l
+  float kc[STEP_MAX_L][D];   // exp(G_A - G_m) o k^_m
+  float U[STEP_MAX_L][D];    // u_m
+  float gA[D];               // gamma_A
+  float a[STEP_MAX_L][STEP_MAX_L], b[STEP_MAX_L][STEP_MAX_L];
+  float beta[STEP_MAX_L];
+};
 
 template <typename IO>
 __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p) {
-  __shared__ float s_q[STEP_MAX_L][D], s_k[STEP_MAX_L][D], s_v[STEP_MAX_L][D], s_dec[STEP_MAX_L][D];
-  __shared__ float s_beta[STEP_MAX_L], s_kq[STEP_MAX_L];
-  __shared__ __align__(16) float s_red[2][8][2][D];
+  __shared__ __align__(16) StepSmem sm;
+  // partials [8 row groups][2L vectors][D], then the reduced sums [2L][D]
+  extern __shared__ __align__(16) float step_red[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seq = blockIdx.x / p.heads, h = blockIdx.x % p.heads;
-  const int L = p.steps, H = p.heads;
-  int acc = p.accept_len ? p.accept_len[seq] : L;
-  acc = acc < 0 ? 0 : (acc > L ? L : acc);
+  const int L = p.steps, H = p.heads, NV = 2 * L;
+  int A = p.accept_len ? p.accept_len[seq] : L;
+  A = A < 0 ? 0 : (A > L ? L : A);
+  float *red = step_red, *W = step_red + 8 * NV * D;
 
-  // state rows [16*warp, 16*warp+16), columns [4*lane, 4*lane+4)
+  // state rows [16 warp, +16), columns [4 lane, +4) as two column pairs
   float *st = p.state + ((size_t)seq * H + h) * D * D;
-  float4 S[16];
+  float2 S[16][2];
 #pragma unroll
-  for (int r = 0; r < 16; ++r)
-    S[r] = __ldcs(reinterpret_cast<const float4 *>(st + (size_t)(16 * warp + r) * D + 4 * lane));
+  for (int r = 0; r < 16; ++r) {
+    const float4 t = __ldcs(reinterpret_cast<const float4 *>(st + (size_t)(16 * warp + r) * D + 4 * lane));
+    S[r][0] = make_float2(t.x, t.y);
+    S[r][1] = make_float2(t.z, t.w);
+  }
 
-  // the call's L tokens: raw q, k, v and exp(g) into shared memory
+  // the call's tokens into shared memory
   const IO *q = static_cast<const IO *>(p.q), *k = static_cast<const IO *>(p.k),
            *v = static_cast<const IO *>(p.v);
   for (int idx = tid; idx < L * D; idx += STEP_THREADS) {
     const int l = idx / D, c = idx % D;
     const size_t off = (((size_t)seq * L + l) * H + h) * D + c;
-    s_q[l][c] = ld_io(q + off);
-    s_k[l][c] = ld_io(k + off);
-    s_v[l][c] = ld_io(v + off);
-    s_dec[l][c] = __expf(p.g[off]);
+    sm.q[l][c] = ld_io(q + off);
+    sm.k[l][c] = ld_io(k + off);
+    sm.v[l][c] = ld_io(v + off);
+    sm.G[l][c] = p.g[off];
   }
-  if (tid < L) s_beta[tid] = p.beta[((size_t)seq * L + tid) * H + h];
+  if (tid < L) sm.beta[tid] = p.beta[((size_t)seq * L + tid) * H + h];
   __syncthreads();
-  // L2 normalisation, one warp per token
+
+  // L2 normalisation (one warp per token) and the running gate sums (one thread per channel)
   if (warp < L) {
     float sq = 0.f, sk = 0.f, qk = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float a = s_q[warp][lane + 32 * j], b = s_k[warp][lane + 32 * j];
-      sq = fmaf(a, a, sq);
-      sk = fmaf(b, b, sk);
-      qk = fmaf(a, b, qk);
+      const float x = sm.q[warp][lane + 32 * j], y = sm.k[warp][lane + 32 * j];
+      sq = fmaf(x, x, sq);
+      sk = fmaf(y, y, sk);
+      qk = fmaf(x, y, qk);
     }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
-      qk += __shfl_xor_sync(0xffffffffu, qk, o);
+    for (int m = 16; m; m >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, m);
+      sk += __shfl_xor_sync(0xffffffffu, sk, m);
+      qk += __shfl_xor_sync(0xffffffffu, qk, m);
     }
     const float rq = p.scale * rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      s_q[warp][lane + 32 * j] *= rq;
-      s_k[warp][lane + 32 * j] *= rk;
+      sm.q[warp][lane + 32 * j] *= rq;
+      sm.k[warp][lane + 32 * j] *= rk;
     }
-    if (lane == 0) s_kq[warp] = qk * rq * rk;
+    if (lane == 0) sm.b[warp][warp] = qk * rq * rk;
+  }
+  if (tid < D) {
+    float run = 0.f;
+    for (int l = 0; l < L; ++l) {
+      run += sm.G[l][tid];
+      sm.G[l][tid] = run;
+    }
   }
   __syncthreads();
 
-  IO *o = static_cast<IO *>(p.o);
-  for (int l = 0; l < L; ++l) {
-    float pw[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const int c = 16 * warp + r;
-      const float d = s_dec[l][c], kc = s_k[l][c], qc = s_q[l][c];
-      S[r].x *= d; S[r].y *= d; S[r].z *= d; S[r].w *= d;
-      pw[0] = fmaf(S[r].x, kc, pw[0]); pw[1] = fmaf(S[r].y, kc, pw[1]);
-      pw[2] = fmaf(S[r].z, kc, pw[2]); pw[3] = fmaf(S[r].w, kc, pw[3]);
-      pq[0] = fmaf(S[r].x, qc, pq[0]); pq[1] = fmaf(S[r].y, qc, pq[1]);
-      pq[2] = fmaf(S[r].z, qc, pq[2]); pq[3] = fmaf(S[r].w, qc, pq[3]);
+  // decayed vectors, and the token-token couplings a_lm, b_lm (m < l)
+  for (int idx = tid; idx < L * D; idx += STEP_THREADS) {
+    const int l = idx / D, c = idx % D;
+    const float Gl = sm.G[l][c], kk = sm.k[l][c], gam = __expf(Gl);
+    sm.kt[l][c] = gam * kk;
+    sm.qt[l][c] = gam * sm.q[l][c];
+    sm.kc[l][c] = A > 0 ? __expf(sm.G[A - 1][c] - Gl) * kk : 0.f;
+  }
+  if (tid < D) sm.gA[tid] = A > 0 ? __expf(sm.G[A - 1][tid]) : 1.f;
+  for (int pr = warp; pr < L * (L - 1) / 2; pr += STEP_THREADS / 32) {
+    int l = 1, m = pr;   // pair index -> (l, m) with m < l
+    while (m >= l) {
+      m -= l;
+      ++l;
     }
-    float(*red)[2][D] = s_red[l & 1];
-    *reinterpret_cast<float4 *>(&red[warp][0][4 * lane]) = make_float4(pw[0], pw[1], pw[2], pw[3]);
-    *reinterpret_cast<float4 *>(&red[warp][1][4 * lane]) = make_float4(pq[0], pq[1], pq[2], pq[3]);
-    __syncthreads();
-    float w4[4] = {0.f, 0.f, 0.f, 0.f}, q4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ww = 0; ww < 8; ++ww) {   // fixed order: deterministic
-      const float4 a = *reinterpret_cast<const float4 *>(&red[ww][0][4 * lane]);
-      const float4 b = *reinterpret_cast<const float4 *>(&red[ww][1][4 * lane]);
-      w4[0] += a.x; w4[1] += a.y; w4[2] += a.z; w4[3] += a.w;
-      q4[0] += b.x; q4[1] += b.y; q4[2] += b.z; q4[3] += b.w;
-    }
-    const float beta = s_beta[l], kq = s_kq[l];
-    float u[4], out[4];
+    float sa = 0.f, sb = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      u[j] = beta * (s_v[l][4 * lane + j] - w4[j]);
-      out[j] = fmaf(u[j], kq, q4[j]);
+      const int c = lane + 32 * j;
+      const float e = __expf(sm.G[l][c] - sm.G[m][c]) * sm.k[m][c];
+      sa = fmaf(e, sm.k[l][c], sa);
+      sb = fmaf(e, sm.q[l][c], sb);
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const float kc = s_k[l][16 * warp + r];
-      S[r].x = fmaf(kc, u[0], S[r].x); S[r].y = fmaf(kc, u[1], S[r].y);
-      S[r].z = fmaf(kc, u[2], S[r].z); S[r].w = fmaf(kc, u[3], S[r].w);
+    for (int s = 16; s; s >>= 1) {
+      sa += __shfl_xor_sync(0xffffffffu, sa, s);
+      sb += __shfl_xor_sync(0xffffffffu, sb, s);
     }
-    if (warp == 0)
-      st_io4<IO>(o + (((size_t)seq * L + l) * H + h) * D + 4 * lane, out[0], out[1], out[2], out[3]);
-    if (l + 1 == acc) {
-#pragma unroll
-      for (int r = 0; r < 16; ++r)
-        __stcs(reinterpret_cast<float4 *>(st + (size_t)(16 * warp + r) * D + 4 * lane), S[r]);
+    if (lane == 0) {
+      sm.a[l][m] = sa;
+      sm.b[l][m] = sb;
     }
   }
+  __syncthreads();
+
+  // sweep 1: partial column sums of S0^T kt_l and S0^T qt_l over this warp's rows, two tokens at a time
+  for (int l0 = 0; l0 < L; l0 += 2) {
+    const bool two = l0 + 1 < L;
+    const int l1 = two ? l0 + 1 : l0;
+    float2 acc[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int r4 = 0; r4 < 16; r4 += 4) {
+      const int c = 16 * warp + r4;
+      const float4 k0 = *reinterpret_cast<const float4 *>(&sm.kt[l0][c]);
+      const float4 q0 = *reinterpret_cast<const float4 *>(&sm.qt[l0][c]);
+      const float4 k1 = *reinterpret_cast<const float4 *>(&sm.kt[l1][c]);
+      const float4 q1 = *reinterpret_cast<const float4 *>(&sm.qt[l1][c]);
+      const float kv0[4] = {k0.x, k0.y, k0.z, k0.w}, qv0[4] = {q0.x, q0.y, q0.z, q0.w};
+      const float kv1[4] = {k1.x, k1.y, k1.z, k1.w}, qv1[4] = {q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          acc[0][j] = __ffma2_rn(S[r4 + i][j], dup2(kv0[i]), acc[0][j]);
+          acc[1][j] = __ffma2_rn(S[r4 + i][j], dup2(qv0[i]), acc[1][j]);
+          acc[2][j] = __ffma2_rn(S[r4 + i][j], dup2(kv1[i]), acc[2][j]);
+          acc[3][j] = __ffma2_rn(S[r4 + i][j], dup2(qv1[i]), acc[3][j]);
+        }
+      }
+    }
+    const int nv = two ? 4 : 2;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (i < nv)
+        *reinterpret_cast<float4 *>(&red[((size_t)warp * NV + 2 * l0 + i) * D + 4 * lane]) =
+            make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
+  }
+  __syncthreads();
+
+  // reduce the 8 row-group partials: one (vector, column quad) per task, fixed order
+  for (int t = tid; t < NV * (D / 4); t += STEP_THREADS) {
+    const int vec = t / (D / 4), c4 = 4 * (t % (D / 4));
+    float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+      const float4 x = *reinterpret_cast<const float4 *>(&red[((size_t)g8 * NV + vec) * D + c4]);
+      s0 = __fadd2_rn(s0, make_float2(x.x, x.y));
+      s1 = __fadd2_rn(s1, make_float2(x.z, x.w));
+    }
+    *reinterpret_cast<float4 *>(&W[vec * D + c4]) = make_float4(s0.x, s0.y, s1.x, s1.y);
+  }
+  __syncthreads();
+
+  // the token-token solve, one value column per thread; outputs of all L tokens
+  if (tid < D) {
+    IO *o = static_cast<IO *>(p.o);
+    float u[STEP_MAX_L];
+#pragma unroll
+    for (int l = 0; l < STEP_MAX_L; ++l) {
+      if (l < L) {
+        float w = W[(2 * l) * D + tid], ol = W[(2 * l + 1) * D + tid];
+#pragma unroll
+        for (int m = 0; m < l; ++m) {
+          w = fmaf(sm.a[l][m], u[m], w);
+          ol = fmaf(sm.b[l][m], u[m], ol);
+        }
+        u[l] = sm.beta[l] * (sm.v[l][tid] - w);
+        ol = fmaf(sm.b[l][l], u[l], ol);
+        sm.U[l][tid] = u[l];
+        o[(((size_t)seq * L + l) * H + h) * D + tid] = from_f<IO>(ol);
+      }
+    }
+  }
+  __syncthreads();
+
+  // sweep 2: S_A = Diag(gamma_A) S0 + sum_{m<A} kc_m u_m^T, then the one write-back
+  if (A > 0) {
+#pragma unroll
+    for (int r4 = 0; r4 < 16; r4 += 4) {
+      const float4 g4 = *reinterpret_cast<const float4 *>(&sm.gA[16 * warp + r4]);
+      const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        S[r4 + i][0] = __fmul2_rn(S[r4 + i][0], dup2(gv[i]));
+        S[r4 + i][1] = __fmul2_rn(S[r4 + i][1], dup2(gv[i]));
+      }
+    }
+    for (int m = 0; m < A; ++m) {
+      const float4 u4 = *reinterpret_cast<const float4 *>(&sm.U[m][4 * lane]);
+      const float2 u0 = make_float2(u4.x, u4.y), u1 = make_float2(u4.z, u4.w);
+#pragma unroll
+      for (int r4 = 0; r4 < 16; r4 += 4) {
+        const float4 c4 = *reinterpret_cast<const float4 *>(&sm.kc[m][16 * warp + r4]);
+        const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          S[r4 + i][0] = __ffma2_rn(dup2(cv[i]), u0, S[r4 + i][0]);
+          S[r4 + i][1] = __ffma2_rn(dup2(cv[i]), u1, S[r4 + i][1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      __stcs(reinterpret_cast<float4 *>(st + (size_t)(16 * warp + r) * D + 4 * lane),
+             make_float4(S[r][0].x, S[r][0].y, S[r][1].x, S[r][1].y));
+  }
+}
+
+template <typename IO>
+static cudaError_t launch_step_t(const StepParams &p, unsigned grid, cudaStream_t s) {
+  // Dynamic shared memory: 8 row-group partials plus the reduced sums, 2L vectors each.
+  constexpr int max_smem = (8 + 1) * 2 * STEP_MAX_L * D * (int)sizeof(float);
+  const int smem = (8 + 1) * 2 * p.steps * D * (int)sizeof(float);
+  // static + dynamic exceeds the 48 KiB default: opt in (per device, idempotent)
+  const cudaError_t e =
+      cudaFuncSetAttribute(kda_step_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e != cudaSuccess) return e;
+  kda_step_kernel<IO><<<grid, STEP_THREADS, smem, s>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s) {
   const unsigned grid = (unsigned)((long long)p.n_seqs * p.heads);
   if (grid == 0) return cudaSuccess;
-  if (f32)
-    kda_step_kernel<float><<<grid, STEP_THREADS, 0, s>>>(p);
-  else
-    kda_step_kernel<bf16><<<grid, STEP_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
+  return f32 ? launch_step_t<float>(p, grid, s) : launch_step_t<bf16>(p, grid, s);
 }
 
 }  // namespace kda

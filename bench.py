@@ -50,8 +50,8 @@ KERNEL_BYTES = {
 }
 FWD_STAGES = ["fwd.table", "fwd.prep", "fwd.scan"]
 BWD_STAGES = ["bwd.table", "bwd.prep", "bwd.dscan", "bwd.state", "bwd.intra"]
-KERNEL_SRC = {"fwd.prep": "kda_prep.cu", "fwd.scan": "kda_scan.cu", "bwd.prep": "kda_prep.cu",
-              "bwd.dscan": "kda_scan.cu", "bwd.state": "kda_bwd.cu", "bwd.intra": "kda_bwd.cu",
+KERNEL_SRC = {"fwd.prep": "kda_prep.cu", "fwd.scan": "kda_scan_tc.cu", "bwd.prep": "kda_prep.cu",
+              "bwd.dscan": "kda_scan_tc.cu", "bwd.state": "kda_bwd.cu", "bwd.intra": "kda_bwd.cu",
               "decode": "kda_step.cu"}
 
 

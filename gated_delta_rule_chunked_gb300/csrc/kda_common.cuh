@@ -181,6 +181,15 @@ __device__ __forceinline__ void zero(float (&acc)[NT][4]) {
   for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 }
 
+// ---------------------------------------------------------------- cp.async (LDGSTS)
+// 16-byte global -> shared copy through the load/store units; `valid` bytes are
+// read (0 or 16), the rest of the 16 is zero-filled. Completes at cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int valid = 16) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(valid)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA bulk copies
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));

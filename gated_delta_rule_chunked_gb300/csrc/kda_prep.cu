@@ -165,6 +165,19 @@ __device__ __forceinline__ void mm16(float (&acc)[2][4], const float *A, int lda
   }
 }
 
+// Two consecutive channels of one staged row, held in registers in the io type.
+template <typename E> struct Pair;
+template <> struct Pair<bf16> {
+  typedef __nv_bfloat162 T;
+  static __device__ __forceinline__ T load(const bf16 *p) { return *reinterpret_cast<const T *>(p); }
+  static __device__ __forceinline__ float2 get(T v) { return __bfloat1622float2(v); }
+};
+template <> struct Pair<float> {
+  typedef float2 T;
+  static __device__ __forceinline__ T load(const float *p) { return *reinterpret_cast<const T *>(p); }
+  static __device__ __forceinline__ float2 get(T v) { return v; }
+};
+
 template <typename E>
 __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p) {
   using S = PrepSmem2;
@@ -188,18 +201,40 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   char *rec = (char *)p.img + ((size_t)chunk * H + h) * rec_bytes;
   char *recb = bwdrec ? (char *)p.img2 + ((size_t)chunk * H + h) * TcRecB::BYTES : nullptr;
 
+  // 0. stage the chunk's q, k (io type) and g (fp32) in shared memory with one batch of
+  //    asynchronous copies: q in the KL tile, k in the R tile, g in the QL tile (row
+  //    stride LDF); rows past the sequence end are zero-filled. All three tiles are
+  //    rewritten only after their contents have been consumed.
+  constexpr int QROW = D * (int)sizeof(E);            // bytes of one staged q / k row
+  const E *sq_ = (const E *)KL, *sk_ = (const E *)RR;
+  {
+    constexpr int QCH = QROW / 16;
+    for (int idx = tid; idx < CH * QCH; idx += PREP_THREADS) {
+      const int r = idx / QCH, ch = idx % QCH;
+      const bool ok = r < ref.len;
+      const size_t off = ok ? ((size_t)(ref.t0 + r) * H + h) * D * sizeof(E) + 16 * ch : 0;
+      cp_async16((char *)KL + r * QROW + 16 * ch, (const char *)qg + off, ok ? 16 : 0);
+      cp_async16((char *)RR + r * QROW + 16 * ch, (const char *)kg + off, ok ? 16 : 0);
+    }
+    for (int idx = tid; idx < CH * (D / 4); idx += PREP_THREADS) {
+      const int r = idx / (D / 4), ch = idx % (D / 4);
+      const bool ok = r < ref.len;
+      const float *src = ok ? p.g + ((size_t)(ref.t0 + r) * H + h) * D + 4 * ch : p.g;
+      cp_async16(QL + r * LDF + 4 * ch, src, ok ? 16 : 0);
+    }
+    if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
+    cp_async_wait_all();
+  }
+  __syncthreads();
   // 1. row norms: 4 threads per row, 32 channels each
   {
     const int r = tid >> 2, part = tid & 3;
     float sq = 0.f, sk = 0.f;
-    if (r < ref.len) {
-      const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + part * 32;
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        const float2 a = ld2(qg + off + c), b = ld2(kg + off + c);
-        sq = fmaf(a.x, a.x, fmaf(a.y, a.y, sq));
-        sk = fmaf(b.x, b.x, fmaf(b.y, b.y, sk));
-      }
+    for (int c = 0; c < 32; c += 2) {
+      const float2 a = ld2(sq_ + r * D + part * 32 + c), b = ld2(sk_ + r * D + part * 32 + c);
+      sq = fmaf(a.x, a.x, fmaf(a.y, a.y, sq));
+      sk = fmaf(b.x, b.x, fmaf(b.y, b.y, sk));
     }
     sq += __shfl_xor_sync(0xffffffffu, sq, 1);
     sq += __shfl_xor_sync(0xffffffffu, sq, 2);
@@ -209,17 +244,18 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       rq[r] = p.scale * rsqrtf(sq + 1e-6f);
       rk[r] = rsqrtf(sk + 1e-6f);
     }
-    if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
   }
   // 2. gate scan and factors: thread = (channel pair cp, sub-block a)
   const int cp = tid & 63, a = tid >> 6, c0 = 2 * cp;
   float2 cs[SUB];
+  typename Pair<E>::T qpair[SUB], kpair[SUB];   // this thread's raw q, k (rows a*SUB.., channels c0, c0+1)
   {
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
-      cs[i] = make_float2(0.f, 0.f);
-      if (r < ref.len) cs[i] = *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + r) * H + h) * D + c0);
+      cs[i] = *reinterpret_cast<const float2 *>(QL + r * LDF + c0);
+      qpair[i] = Pair<E>::load(sq_ + r * D + c0);
+      kpair[i] = Pair<E>::load(sk_ + r * D + c0);
     }
     float2 run = make_float2(0.f, 0.f);
 #pragma unroll
@@ -265,12 +301,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
-      float2 qv = make_float2(0.f, 0.f), kv = qv;
-      if (r < ref.len) {
-        const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + c0;
-        qv = ld2(qg + off);
-        kv = ld2(kg + off);
-      }
+      const float2 qv = Pair<E>::get(qpair[i]), kv = Pair<E>::get(kpair[i]);
       const float x0 = exp2f(cs[i].x), x1 = exp2f(cs[i].y);
       const float y0 = exp2f(ta0 - cs[i].x), y1 = exp2f(ta1 - cs[i].y);
       const float qh0 = qv.x * rq[r], qh1 = qv.y * rq[r], kh0 = kv.x * rk[r], kh1 = kv.y * rk[r];

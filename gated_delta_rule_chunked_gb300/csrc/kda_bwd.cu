@@ -248,18 +248,41 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
   float *rq = (float *)(smem + S::RQ), *rq0 = (float *)(smem + S::RQ0), *rk = (float *)(smem + S::RK),
         *sb = (float *)(smem + S::BETA);
 
-  // P1: row norms (8 threads per row), beta, and the 64x64 inputs
+  // P0: stage the chunk's inputs with one batch of asynchronous copies: q (bf16) in
+  //     the X tile, k in the KL tile, g (fp32, row stride LDI) in the QL tile, T, dTb
+  //     and dBm in their 64x64 tiles, dgC. Rows past the sequence end read as zero.
+  const bf16 *sq_ = (const bf16 *)XX, *sk_ = (const bf16 *)KL;
+  {
+    for (int idx = tid; idx < 64 * 16; idx += INTRA_THREADS) {
+      const int r = idx >> 4, ch = idx & 15;
+      const bool ok = r < ref.len;
+      const size_t off = ok ? ((size_t)(ref.t0 + r) * H + h) * D + 8 * ch : 0;
+      cp_async16((bf16 *)XX + r * D + 8 * ch, qg + off, ok ? 16 : 0);
+      cp_async16((bf16 *)KL + r * D + 8 * ch, kg + off, ok ? 16 : 0);
+      cp_async16(TT + r * LDJ + 4 * ch, auxT + r * 64 + 4 * ch);
+      cp_async16(DT + r * LDJ + 4 * ch, rec + GradLayout::dtb / 4 + r * 64 + 4 * ch);
+      cp_async16(DBm + r * LDJ + 4 * ch, rec + GradLayout::dbm / 4 + r * 64 + 4 * ch);
+    }
+    for (int idx = tid; idx < 64 * 32; idx += INTRA_THREADS) {
+      const int r = idx >> 5, ch = idx & 31;
+      const bool ok = r < ref.len;
+      const float *src = ok ? p.g + ((size_t)(ref.t0 + r) * H + h) * D + 4 * ch : p.g;
+      cp_async16(QL + r * LDI + 4 * ch, src, ok ? 16 : 0);
+    }
+    if (tid < 32) cp_async16((float *)(smem + S::DGC) + 4 * tid, rec + GradLayout::dgc / 4 + 4 * tid);
+    if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
+    cp_async_wait_all();
+  }
+  __syncthreads();
+  // P1: row norms (8 threads per row)
   {
     const int r = tid >> 3, part = tid & 7;
     float sq = 0.f, sk = 0.f;
-    if (r < ref.len) {
-      const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + part * 16;
 #pragma unroll
-      for (int c = 0; c < 16; c += 2) {
-        const float2 a = ld2(qg + off + c), b = ld2(kg + off + c);
-        sq = fmaf(a.x, a.x, fmaf(a.y, a.y, sq));
-        sk = fmaf(b.x, b.x, fmaf(b.y, b.y, sk));
-      }
+    for (int c = 0; c < 16; c += 2) {
+      const float2 a = ld2(sq_ + r * D + part * 16 + c), b = ld2(sk_ + r * D + part * 16 + c);
+      sq = fmaf(a.x, a.x, fmaf(a.y, a.y, sq));
+      sk = fmaf(b.x, b.x, fmaf(b.y, b.y, sk));
     }
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) {
@@ -272,26 +295,18 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
       rq[r] = p.scale * r0;
       rk[r] = rsqrtf(sk + 1e-6f);
     }
-    if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
-    if (tid < 128) ((float *)(smem + S::DGC))[tid] = rec[GradLayout::dgc / 4 + tid];
-    for (int idx = tid; idx < 64 * 16; idx += INTRA_THREADS) {
-      const int rr = idx >> 4, c4 = (idx & 15) * 4;
-      *reinterpret_cast<float4 *>(TT + rr * LDJ + c4) = *reinterpret_cast<const float4 *>(auxT + rr * 64 + c4);
-      *reinterpret_cast<float4 *>(DT + rr * LDJ + c4) =
-          *reinterpret_cast<const float4 *>(rec + GradLayout::dtb / 4 + rr * 64 + c4);
-      *reinterpret_cast<float4 *>(DBm + rr * LDJ + c4) =
-          *reinterpret_cast<const float4 *>(rec + GradLayout::dbm / 4 + rr * 64 + c4);
-    }
   }
-  // P2a: gate scan (threads 0..255: channel pair x sub-block)
+  // P2a: gate scan (threads 0..255: channel pair x sub-block); this thread's raw q, k pairs
   const int cp = tid & 63, a = (tid >> 6) & 3, c0 = 2 * cp;
   float2 cs[SUB];
+  __nv_bfloat162 qpair[SUB], kpair[SUB];
   if (tid < 256) {
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
-      cs[i] = make_float2(0.f, 0.f);
-      if (r < ref.len) cs[i] = *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + r) * H + h) * D + c0);
+      cs[i] = *reinterpret_cast<const float2 *>(QL + r * LDI + c0);
+      qpair[i] = *reinterpret_cast<const __nv_bfloat162 *>(sq_ + r * D + c0);
+      kpair[i] = *reinterpret_cast<const __nv_bfloat162 *>(sk_ + r * D + c0);
     }
     float2 run = make_float2(0.f, 0.f);
 #pragma unroll
@@ -332,12 +347,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
-      float2 qv = make_float2(0.f, 0.f), kv = qv;
-      if (r < ref.len) {
-        const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + c0;
-        qv = ld2(qg + off);
-        kv = ld2(kg + off);
-      }
+      const float2 qv = __bfloat1622float2(qpair[i]), kv = __bfloat1622float2(kpair[i]);
       const float x0 = exp2f(cs[i].x), x1 = exp2f(cs[i].y);
       const float y0 = exp2f(ta0 - cs[i].x), y1 = exp2f(ta1 - cs[i].y);
       const float kh0 = kv.x * rk[r], kh1 = kv.y * rk[r];
@@ -346,7 +356,6 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
       *reinterpret_cast<float2 *>(RR + r * LDI + c0) = make_float2(kh0 * y0, kh1 * y1);
       *reinterpret_cast<float2 *>(CS + r * LDI + c0) = cs[i];
     }
-    if (a == 0) ((float *)(smem + S::PART))[c0] = 0.f;   // keeps PART defined for masked lanes
   } else if (tid < 320) {
     // dbeta_j through Tb = T Diag(beta), and dT = dTb Diag(beta)
     const int j = tid - 256;
@@ -398,6 +407,16 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
     }
   }
   __syncthreads();
+  // The 64x64 tiles T and X are dead from here on: stage q and k again (for the
+  // epilogue and the L2-norm backward) while the factor-tile products run.
+  const bf16 *eq_ = (const bf16 *)XX, *ek_ = (const bf16 *)TT;
+  for (int idx = tid; idx < 64 * 16; idx += INTRA_THREADS) {
+    const int r = idx >> 4, ch = idx & 15;
+    const bool ok = r < ref.len;
+    const size_t off = ok ? ((size_t)(ref.t0 + r) * H + h) * D + 8 * ch : 0;
+    cp_async16((bf16 *)XX + r * D + 8 * ch, qg + off, ok ? 16 : 0);
+    cp_async16((bf16 *)TT + r * D + 8 * ch, kg + off, ok ? 16 : 0);
+  }
   // P5: gradients w.r.t. the factor tiles; warp -> (row sub-block t, channel quarter cq)
   const int t = warp & 3, cq = warp >> 2, cbase = 32 * cq;
   float tQ[4][4], tK[4][4], tW[4][4];
@@ -420,7 +439,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
 #pragma unroll
       for (int e = 0; e < 4; ++e) tW[nt][e] = fmaf(tR[nt][e], dsc[8 * nt + 2 * q + (e & 1)], tW[nt][e]);
   }
-  __syncthreads();   // every warp is done reading the factor tiles of other rows
+  cp_async_wait_all();
+  __syncthreads();   // every warp is done reading the factor tiles of other rows; q, k staged
   float dqh[4][4], dkh[4][4];
   {
     float rowq[2] = {0.f, 0.f}, rowk[2] = {0.f, 0.f}, colsum[4][2];
@@ -433,12 +453,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
         const float2 dqt = *reinterpret_cast<const float2 *>(rec + GradLayout::dqt / 4 + r * 128 + c);
         const float2 dkt = *reinterpret_cast<const float2 *>(rec + GradLayout::dkt / 4 + r * 128 + c);
         const float2 dkk = *reinterpret_cast<const float2 *>(rec + GradLayout::dkh / 4 + r * 128 + c);
-        float2 qr = make_float2(0.f, 0.f), kr = qr;
-        if (r < ref.len) {
-          const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + c;
-          qr = ld2(qg + off);
-          kr = ld2(kg + off);
-        }
+        const float2 qr = ld2(eq_ + r * D + c), kr = ld2(ek_ + r * D + c);
         const float dqtv[2] = {dqt.x, dqt.y}, dktv[2] = {dkt.x, dkt.y}, dkkv[2] = {dkk.x, dkk.y};
         const float qrv[2] = {qr.x, qr.y}, krv[2] = {kr.x, kr.y};
 #pragma unroll
@@ -493,7 +508,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
         const int r = 16 * t + g + 8 * hh, c = cbase + 8 * nt + 2 * q;
         if (r < ref.len) {
           const size_t off = ((size_t)(ref.t0 + r) * H + h) * D + c;
-          const float2 qr = ld2(qg + off), kr = ld2(kg + off);
+          const float2 qr = ld2(eq_ + r * D + c), kr = ld2(ek_ + r * D + c);
           const float dq_dot = rowQ[r] + rowQ[64 + r] + rowQ[128 + r] + rowQ[192 + r];
           const float dk_dot = rowK[r] + rowK[64 + r] + rowK[128 + r] + rowK[192 + r];
           const float sq = p.scale * rq0[r], rkr = rk[r];

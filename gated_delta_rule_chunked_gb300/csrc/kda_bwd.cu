@@ -150,23 +150,24 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
   }
   __syncthreads();
   // dQt = dO S^T ; dKh = U dS^T ; dKt = -dV' S^T
-  auto store128 = [&](float *dst, float(&a)[8][4]) {
+  auto store128 = [&](size_t off, float(&a)[8][4]) {   // bf16 [64][128] at byte offset off
+    bf16 *dst = reinterpret_cast<bf16 *>(reinterpret_cast<char *>(rec) + off);
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh)
-        *reinterpret_cast<float2 *>(dst + (r0 + 8 * hh) * 128 + 64 * nh + 8 * nt + 2 * q4) =
-            make_float2(a[nt][2 * hh], a[nt][2 * hh + 1]);
+        *reinterpret_cast<__nv_bfloat162 *>(dst + (r0 + 8 * hh) * 128 + 64 * nh + 8 * nt + 2 * q4) =
+            __floats2bfloat162_rn(a[nt][2 * hh], a[nt][2 * hh + 1]);
   };
   zero(acc);
   wgemm<true, false, 8>(acc, sdO, 16 * mt, sS, 64 * nh, 0, 128);   // B(k=v, n=c) = S^T[v][c]
-  store128(rec + GradLayout::dqt / 4, acc);
+  store128(GradLayout::dqt, acc);
   zero(acc);
   wgemm<true, false, 8>(acc, sU, 16 * mt, sdS, 64 * nh, 0, 128);  // B(k=v, n=c) = dS^T[v][c]
-  store128(rec + GradLayout::dkh / 4, acc);
+  store128(GradLayout::dkh, acc);
   zero(acc);
   wgemm<true, false, 8>(acc, sdV, 16 * mt, sS, 64 * nh, 0, 128);
-  store128(rec + GradLayout::dkt / 4, acc);
+  store128(GradLayout::dkt, acc);
   if (tid < 128) {   // dgC_c = sum_v S[c][v] dS[c][v] = sum_v S^T[v][c] dS^T[v][c]
     float s = 0.f;
     for (int vv = 0; vv < 128; ++vv) s = fmaf(to_f(*sS.at(vv, tid)), to_f(*sdS.at(vv, tid)), s);
@@ -419,6 +420,23 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
   }
   // P5: gradients w.r.t. the factor tiles; warp -> (row sub-block t, channel quarter cq)
   const int t = warp & 3, cq = warp >> 2, cbase = 32 * cq;
+  // this thread's elements of the state-side gradients dQt, dKt, dKh, loaded now so the
+  // loads are in flight during the products
+  __nv_bfloat162 gq[4][2], gk[4][2], gh[4][2];
+  {
+    const bf16 *gqt = reinterpret_cast<const bf16 *>(reinterpret_cast<const char *>(rec) + GradLayout::dqt);
+    const bf16 *gkt = reinterpret_cast<const bf16 *>(reinterpret_cast<const char *>(rec) + GradLayout::dkt);
+    const bf16 *gkh = reinterpret_cast<const bf16 *>(reinterpret_cast<const char *>(rec) + GradLayout::dkh);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = 16 * t + g + 8 * hh, c = cbase + 8 * nt + 2 * q;
+        gq[nt][hh] = *reinterpret_cast<const __nv_bfloat162 *>(gqt + r * 128 + c);
+        gk[nt][hh] = *reinterpret_cast<const __nv_bfloat162 *>(gkt + r * 128 + c);
+        gh[nt][hh] = *reinterpret_cast<const __nv_bfloat162 *>(gkh + r * 128 + c);
+      }
+  }
   float tQ[4][4], tK[4][4], tW[4][4];
   zero(tQ);
   zero(tK);
@@ -450,9 +468,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int r = 16 * t + g + 8 * hh, c = cbase + 8 * nt + 2 * q;
-        const float2 dqt = *reinterpret_cast<const float2 *>(rec + GradLayout::dqt / 4 + r * 128 + c);
-        const float2 dkt = *reinterpret_cast<const float2 *>(rec + GradLayout::dkt / 4 + r * 128 + c);
-        const float2 dkk = *reinterpret_cast<const float2 *>(rec + GradLayout::dkh / 4 + r * 128 + c);
+        const float2 dqt = __bfloat1622float2(gq[nt][hh]), dkt = __bfloat1622float2(gk[nt][hh]),
+                     dkk = __bfloat1622float2(gh[nt][hh]);
         const float2 qr = ld2(eq_ + r * D + c), kr = ld2(ek_ + r * D + c);
         const float dqtv[2] = {dqt.x, dqt.y}, dktv[2] = {dkt.x, dkt.y}, dkkv[2] = {dkk.x, dkk.y};
         const float qrv[2] = {qr.x, qr.y}, krv[2] = {kr.x, kr.y};

@@ -319,15 +319,16 @@ def bench_e2e(args, dev, world, host):
 
 
 # ----------------------------------------------------------------------------- oracle
-def cpu_baseline(args, steps=1, sample_tokens=None):
+def cpu_baseline(args, steps=1, sample_tokens=None, heads_per_core=4):
     """The fp64 oracle as it stands, timed on this host's cores on a bounded sample of
-    the same workload: the first `sample_tokens` tokens of as many heads as cores."""
+    the workload: `sample_tokens` tokens of `heads_per_core` x cores heads (at most 96),
+    drawn with the workload's recipe and seed."""
     import torch
     import oracle
     from gated_delta_rule_chunked_gb300.inputs import make_seq_batch
     cores = oracle.default_threads()
     Ts = sample_tokens or args.cpu_sample_tokens
-    heads = cores
+    heads = min(96, heads_per_core * cores)
     b = make_seq_batch([Ts], heads=heads, io_dtype="bf16", seed=1002, h0=True, grad=True)
     t0 = time.perf_counter()
     for _ in range(steps):
@@ -337,7 +338,8 @@ def cpu_baseline(args, steps=1, sample_tokens=None):
     # tokens/s of the full 96-head workload = sampled token-heads per second / 96
     val = Ts * heads / el / 96
     return {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"fwd+bwd of the first {Ts} tokens of {heads} heads (one head per core) of {WORKLOAD}; "
+            "sample": f"fwd+bwd of one {Ts}-token sequence x {heads} heads drawn with the recipe and seed of "
+                      f"{WORKLOAD} ({cores} threads, one (sequence, head) task per thread at a time); "
                       f"value = sampled token-heads per second / 96 heads", "seconds": el}
 
 
@@ -346,13 +348,13 @@ def run_reference(args, rank, world):
         return None
     ms = []
     for _ in range(args.warmup):
-        cpu_baseline(args, sample_tokens=args.ref_sample_tokens)
+        cpu_baseline(args, sample_tokens=args.ref_sample_tokens, heads_per_core=1)
     for _ in range(args.steps):
-        r = cpu_baseline(args, sample_tokens=args.ref_sample_tokens)
+        r = cpu_baseline(args, sample_tokens=args.ref_sample_tokens, heads_per_core=1)
         ms.append(r["seconds"] * 1e3)
     ms_step = statistics.mean(ms)
     cores = r["cores"]
-    val = args.ref_sample_tokens * cores / (ms_step * 1e-3) / 96
+    val = args.ref_sample_tokens * min(96, cores) / (ms_step * 1e-3) / 96
     return {"impl": "reference", "metric": "KDA fwd+bwd tokens/s (H=96, d=128, T=32768, bf16 I/O, fp32 state/grads)",
             "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

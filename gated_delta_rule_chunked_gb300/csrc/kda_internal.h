@@ -138,7 +138,6 @@ cudaError_t launch_chunk_table(const int *cu_in, int n_seqs, long long total, in
 cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
 cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s);
-cudaError_t launch_bwd_scan(const BwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
 cudaError_t launch_bwd_scan_tc(const BwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_state(const BwdStateParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_bwd_intra(const BwdIntraParams &p, bool f32, cudaStream_t s);

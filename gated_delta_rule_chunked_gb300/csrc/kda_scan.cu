@@ -1,19 +1,17 @@
-// kda_scan.cu -- the sequential inter-chunk state passing (forward) and the
-// reverse dS scan (backward).
+// kda_scan.cu -- the sequential inter-chunk state passing for fp32 I/O (the
+// bf16 forward and the backward dS scan run on tcgen05, kda_scan_tc.cu).
 //
 // Columns of the state evolve independently (the decay and the erase act on key
 // rows), so the value dimension is cut into slices of DVS columns, each an
-// independent chain run by one group of 4 warps. A CTA holds NG such groups
-// (NG = 4 for bf16: one CTA per (sequence, head) covering all 128 columns), so
-// the per-chunk record is fetched once and shared by all slices. The state
-// slice stays in registers (fp32) for the whole sequence; its bf16 copy in
-// shared memory is the tensor-core operand. The next chunk's values (forward)
-// or output gradients (backward) are loaded one chunk ahead into registers. Per chunk, with the record written
+// independent chain run by one group of 4 warps (NG groups per CTA share one
+// fetched record; the fp32 path launches NG = 1). The state slice stays in
+// registers for the whole sequence; its copy in shared memory is the operand of
+// the fp32 products. The next chunk's values are loaded one chunk ahead into
+// registers. Per chunk, with the record written
 // by the prep kernel (Qt = q^*exp(G), Kt = k^*exp(G), Kh = k^*exp(G_last - G),
 // Tb = T Diag(beta), Bm = masked gated q.k^T, gC = exp(G_last)):
 //
-//   forward:  V' = V - Kt S;  U = Tb V';  O = Qt S + Bm U;  S <- gC*S + Kh^T U
-//   backward: dU = Bm^T dO + Kh dS;  dV = Tb^T dU;  dS <- gC*dS + Qt^T dO - Kt^T dV
+//   V' = V - Kt S;  U = Tb V';  O = Qt S + Bm U;  S <- gC*S + Kh^T U
 //
 // (V' is the value minus what the decayed state already predicts; U is the
 // delta-rule update after the intra-chunk WY/UT transform.) The record of the
@@ -226,165 +224,6 @@ __global__ void __launch_bounds__(128 * NG, 1) kda_fwd_scan_kernel(FwdScanParams
   }
 }
 
-// ------------------------------------------------------------------ backward
-template <typename E, int DVS, int NG>
-__global__ void __launch_bounds__(128 * NG, 1) kda_bwd_scan_kernel(BwdScanParams p) {
-  constexpr int NZ = 128 / DVS, NT = DVS / 8, NB = NZ / NG;
-  using S = ScanSmem<E, DVS, NG>;
-  extern __shared__ __align__(128) char smem[];
-  const int H = p.geo.heads;
-  const int tid = threadIdx.x, lane = tid & 31, g8 = lane >> 2, q4 = lane & 3;
-  const int grp = tid >> 7, warp = (tid >> 5) & 3, gtid = tid & 127;
-  const int z = (blockIdx.x % NB) * NG + grp, h = (blockIdx.x / NB) % H, seq = blockIdx.x / (NB * H);
-  const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
-  const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
-  char *gsm = smem + S::G0 + grp * S::GRP;
-  const size_t rec_bytes = (size_t)S::REC;
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
-  Tile<E, 128> Qt((E *)(smem + S::QT)), Kt((E *)(smem + S::KT)), Kh((E *)(smem + S::KH));
-  Tile<E, 64> Tb((E *)(smem + S::TB)), Bm((E *)(smem + S::BM));
-  const float *gC = (const float *)(smem + S::GC);
-  Tile<E, DVS> sdS((E *)(gsm + S::X0)), sdO((E *)(gsm + S::X1)), sdU((E *)(gsm + S::X2)), sdV((E *)(gsm + S::X3));
-  const E *dO = (const E *)p.dO;
-  // dO slice rows of chunk j, 16-byte pieces owned by this thread of the group
-  constexpr int EPC = 16 / sizeof(E), CPR = DVS / EPC, PER = 64 * CPR / 128;
-  auto load_do = [&](int j, uint4 (&x)[PER]) {
-    const long long t0 = s0 + (long long)j * CH;
-    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int idx = gtid + 128 * u, r = idx / CPR, ch = idx % CPR;
-      x[u] = make_uint4(0, 0, 0, 0);
-      if (r < clen) x[u] = __ldg(reinterpret_cast<const uint4 *>(dO + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + ch * EPC));
-    }
-  };
-
-  float accS[2][NT][4];   // dS slice, same fragment layout as the forward state
-#pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int c = 32 * warp + 16 * mt + g8 + 8 * hh, vv = z * DVS + 8 * nt + 2 * q4;
-        float2 x = make_float2(0.f, 0.f);
-        if (p.dhT) x = *reinterpret_cast<const float2 *>(p.dhT + (((size_t)seq * H + h) * 128 + c) * 128 + vv);
-        accS[mt][nt][2 * hh] = x.x;
-        accS[mt][nt][2 * hh + 1] = x.y;
-        st2(sdS.at(c, 8 * nt + 2 * q4), x.x, x.y);
-      }
-  if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * rec_bytes; };
-  if (tid == 0 && nch > 0) {
-    const char *r0 = rec_of(nch - 1);
-    issue_region(smem, r0, S::R1, S::R1B, &bar[0]);
-    issue_region(smem, r0, S::R2, S::R2B, &bar[1]);
-    issue_region(smem, r0, S::R3, S::R3B, &bar[2]);
-    issue_region(smem, r0, S::R4, S::R4B, &bar[3]);
-  }
-  bool ok = true;
-  uint4 donext[PER];
-  if (nch > 0) load_do(nch - 1, donext);
-  for (int it = 0; it < nch; ++it) {
-    const int j = nch - 1 - it;
-    const uint32_t par = it & 1;
-    const long long t0 = s0 + (long long)j * CH;
-    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-    // dO slice rows of this chunk (loaded one chunk ahead)
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int idx = gtid + 128 * u, r = idx / CPR, ch = idx % CPR;
-      *reinterpret_cast<uint4 *>(sdO.at(r, ch * EPC)) = donext[u];
-    }
-    if (j > 0) load_do(j - 1, donext);
-    // dS at the end of this chunk, for the chunk-local gradient kernel
-    {
-      E *sv = (E *)p.dsaved + ((size_t)(cbase + j) * H + h) * 128 * 128;
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int c = 32 * warp + 16 * mt + g8 + 8 * hh, vv = z * DVS + 8 * nt + 2 * q4;
-            st2(sv + full_off<E>(c, vv), accS[mt][nt][2 * hh], accS[mt][nt][2 * hh + 1]);
-          }
-    }
-    __syncthreads();
-    // (a) dU = Bm^T dO + Kh dS
-    ok &= mbar_wait(&bar[2], par);
-    ok &= mbar_wait(&bar[3], par);
-    float accU[NT][4];
-    zero(accU);
-    wgemm<false, false, NT>(accU, Bm, 16 * warp, sdO, 0, 16 * warp, 64);
-    wgemm<true, false, NT>(accU, Kh, 16 * warp, sdS, 0, 0, 128);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-        st2(sdU.at(16 * warp + g8 + 8 * hh, 8 * nt + 2 * q4), accU[nt][2 * hh], accU[nt][2 * hh + 1]);
-    if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
-    if (tid == 0 && j > 0) issue_region(smem, rec_of(j - 1), S::R3, S::R3B, &bar[2]);
-    // (b) dV = Tb^T dU  -> dv output; -dV into shared memory
-    ok &= mbar_wait(&bar[1], par);
-    float accV[NT][4];
-    zero(accV);
-    wgemm<false, false, NT>(accV, Tb, 16 * warp, sdU, 0, 16 * warp, 64);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = 16 * warp + g8 + 8 * hh;
-        st2(sdV.at(r, 8 * nt + 2 * q4), -accV[nt][2 * hh], -accV[nt][2 * hh + 1]);
-        if (r < clen)
-          *reinterpret_cast<float2 *>(p.dv + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + 8 * nt + 2 * q4) =
-              make_float2(accV[nt][2 * hh], accV[nt][2 * hh + 1]);
-      }
-    if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
-    if (tid == 0 && j > 0) issue_region(smem, rec_of(j - 1), S::R2, S::R2B, &bar[1]);
-    // (c) dS <- gC * dS + Qt^T dO - Kt^T dV
-    ok &= mbar_wait(&bar[0], par);
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const float d0 = gC[32 * warp + 16 * mt + g8], d1 = gC[32 * warp + 16 * mt + g8 + 8];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        accS[mt][nt][0] *= d0; accS[mt][nt][1] *= d0;
-        accS[mt][nt][2] *= d1; accS[mt][nt][3] *= d1;
-      }
-      wgemm<false, false, NT>(accS[mt], Qt, 32 * warp + 16 * mt, sdO, 0, 0, 64);
-      wgemm<false, false, NT>(accS[mt], Kt, 32 * warp + 16 * mt, sdV, 0, 0, 64);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-          st2(sdS.at(32 * warp + 16 * mt + g8 + 8 * hh, 8 * nt + 2 * q4), accS[mt][nt][2 * hh],
-              accS[mt][nt][2 * hh + 1]);
-    }
-    if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
-    if (tid == 0 && j > 0) {
-      issue_region(smem, rec_of(j - 1), S::R1, S::R1B, &bar[0]);
-      issue_region(smem, rec_of(j - 1), S::R4, S::R4B, &bar[3]);
-    }
-  }
-  if (p.dh0) {
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int c = 32 * warp + 16 * mt + g8 + 8 * hh, vv = z * DVS + 8 * nt + 2 * q4;
-          *reinterpret_cast<float2 *>(p.dh0 + (((size_t)seq * H + h) * 128 + c) * 128 + vv) =
-              make_float2(accS[mt][nt][2 * hh], accS[mt][nt][2 * hh + 1]);
-        }
-  }
-}
-
 template <typename K>
 static cudaError_t launch_scan_kernel(K kern, int bytes, unsigned grid, int threads, const void *params,
                                       cudaStream_t s) {
@@ -394,25 +233,14 @@ static cudaError_t launch_scan_kernel(K kern, int bytes, unsigned grid, int thre
   return cudaLaunchKernel((const void *)kern, dim3(grid), dim3(threads), args, bytes, s);
 }
 
-// bf16: one CTA of 4 slice groups (16 warps) per (sequence, head); fp32: one 4-warp CTA per slice.
+// fp32 I/O: one 4-warp CTA per 32-column slice of each (sequence, head). The bf16
+// forward runs on the tcgen05 scan (kda_scan_tc.cu).
 cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int, cudaStream_t s) {
   const long long units = (long long)p.geo.n_seqs * p.geo.heads;
   if (units == 0) return cudaSuccess;
-  if (f32)
-    return launch_scan_kernel(kda_fwd_scan_kernel<float, 32, 1>, ScanSmem<float, 32, 1>::BYTES,
-                              (unsigned)(units * 4), 128, &p, s);
-  return launch_scan_kernel(kda_fwd_scan_kernel<bf16, 32, 4>, ScanSmem<bf16, 32, 4>::BYTES, (unsigned)units,
-                            512, &p, s);
-}
-
-cudaError_t launch_bwd_scan(const BwdScanParams &p, bool f32, int, cudaStream_t s) {
-  const long long units = (long long)p.geo.n_seqs * p.geo.heads;
-  if (units == 0) return cudaSuccess;
-  if (f32)
-    return launch_scan_kernel(kda_bwd_scan_kernel<float, 32, 1>, ScanSmem<float, 32, 1>::BYTES,
-                              (unsigned)(units * 4), 128, &p, s);
-  return launch_scan_kernel(kda_bwd_scan_kernel<bf16, 32, 4>, ScanSmem<bf16, 32, 4>::BYTES, (unsigned)units,
-                            512, &p, s);
+  if (!f32) return cudaErrorNotSupported;
+  return launch_scan_kernel(kda_fwd_scan_kernel<float, 32, 1>, ScanSmem<float, 32, 1>::BYTES,
+                            (unsigned)(units * 4), 128, &p, s);
 }
 
 }  // namespace kda

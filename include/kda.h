@@ -24,10 +24,12 @@
  *    all sequences back to back: token t of sequence i is row cu_seqlens[i] + t.
  *  - Supported sizes: dk = dv = 128, chunk = 64, heads >= 1. Other values return
  *    KDA_ERR_UNSUPPORTED.
- *  - Every pointer must be 16-byte aligned; a required pointer that is NULL or
- *    misaligned, or a workspace smaller than the matching *_workspace_size(),
- *    returns KDA_ERR_INVALID_ARG. Validation happens before any launch: on an
- *    error nothing is written.
+ *  - Tensor, state and workspace pointers must be 16-byte aligned; the int32 and
+ *    per-token scalar arrays (cu_seqlens, beta, dbeta, accept_len, dev_status)
+ *    need 4-byte alignment. A required pointer that is NULL or misaligned, or a
+ *    workspace smaller than the matching *_workspace_size(), returns
+ *    KDA_ERR_INVALID_ARG. Validation happens before any launch: on an error
+ *    nothing is written.
  *  - KDA_ERR_CUDA means a launch failed (see kda_last_error()).
  *  - If dev_status is not NULL it must point to one device int32 that the caller
  *    zeroes; a kernel that gives up a bounded wait writes KDA_ERR_TIMEOUT there.

@@ -63,8 +63,10 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
   }
   Tile<E, 128> Kt((E *)(smem + S::KT)), Kh((E *)(smem + S::KH));
   Tile<E, 64> Tb((E *)(smem + S::TB)), Bm((E *)(smem + S::BM));
-  Tile<E, 128> sS((E *)(smem + S::SS)), sdS((E *)(smem + S::SDS)), sV((E *)(smem + S::SV)),
-      sdO((E *)(smem + S::SDO)), sU((E *)(smem + S::SU)), sdU((E *)(smem + S::SDU)), sdV((E *)(smem + S::SDV));
+  // saved S^T and dS^T [v][k] arrive in the scans' operand-tile layout
+  TileSW<128> sS((bf16 *)(smem + S::SS)), sdS((bf16 *)(smem + S::SDS));
+  Tile<E, 128> sV((E *)(smem + S::SV)), sdO((E *)(smem + S::SDO)), sU((E *)(smem + S::SU)), sdU((E *)(smem + S::SDU)),
+      sdV((E *)(smem + S::SDV));
   {
     constexpr int EPC = 16 / sizeof(E), CPR = 128 / EPC;
     const E *v = (const E *)p.v, *dO = (const E *)p.dO;

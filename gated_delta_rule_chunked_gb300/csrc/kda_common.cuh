@@ -50,6 +50,20 @@ struct Tile {
   __device__ __forceinline__ E *at(int r, int c) const { return p + off(r, c); }
 };
 
+// A bf16 tile of R rows x 128 columns in the tcgen05 K-major 128-byte-swizzle
+// layout: two 64-column blocks of R rows x 128 bytes; inside a row, 16-byte chunk
+// c sits at c ^ (row % 8). This is the layout of the scans' operand tiles and of
+// the chunk states they save, so a saved state is one contiguous bulk copy.
+template <int R>
+struct TileSW {
+  bf16 *p;
+  __device__ __forceinline__ TileSW(bf16 *ptr) : p(ptr) {}
+  __device__ __forceinline__ int off(int r, int c) const {
+    return (c >> 6) * R * 64 + r * 64 + ((((c & 63) >> 3) ^ (r & 7)) << 3) + (c & 7);
+  }
+  __device__ __forceinline__ bf16 *at(int r, int c) const { return p + off(r, c); }
+};
+
 __device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_f(float x) { return x; }
 template <typename E> __device__ __forceinline__ E from_f(float x);
@@ -114,10 +128,10 @@ __device__ __forceinline__ void mma1688(float (&c)[4], const uint32_t (&a)[4], u
 // wgemm: acc[nt] += A[m0:m0+16, k0:k1] * B[k0:k1, n0+8nt : n0+8nt+8] for nt < NT.
 //   AK: A stored [m][k] (true) or [k][m] (false);
 //   BK: B stored [n][k] (true) or [k][n] (false).
-// k0, k1 are multiples of 16.
-template <bool AK, bool BK, int NT, int LDA, int LDB>
-__device__ __forceinline__ void wgemm(float (&acc)[NT][4], Tile<bf16, LDA> A, int m0, Tile<bf16, LDB> B,
-                                      int n0, int k0, int k1) {
+// k0, k1 are multiples of 16. A and B are bf16 tiles (Tile<bf16, LD> or TileSW<R>:
+// any tile whose 8 consecutive columns from a multiple of 8 are 16 contiguous bytes).
+template <bool AK, bool BK, int NT, class TA, class TB>
+__device__ __forceinline__ void wgemm(float (&acc)[NT][4], TA A, int m0, TB B, int n0, int k0, int k1) {
   const int lane = threadIdx.x & 31;
   const int i = lane >> 3, r8 = lane & 7;
 #pragma unroll 2
@@ -212,6 +226,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Shared -> global bulk copy (one thread); bytes and both addresses multiples of 16.
+// Tracked per thread by bulk groups: bulk_commit() closes a group, bulk_wait_read()
+// returns once every committed group has finished reading shared memory.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(smem_u32(src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -3,17 +3,18 @@
 // One CTA (4 warps) per (sequence, head). The 128x128 fp32 state lives in tensor
 // memory for the whole sequence, transposed: TMEM lane m = value channel m,
 // column n = key channel n (S^T). Thread t of warp w owns lane 32w + t, so every
-// elementwise pass is a row pass. TMEM columns: [0,128) S^T, [128,192) O^T,
-// [192,256) U^T. Per 64-token chunk, with the record of the prep kernel
+// elementwise pass is a row pass. TMEM columns: [0,128) S^T, then O^T and U^T
+// (64 columns each) in two alternating sets at 128 and 256. Per 64-token chunk, with the record of the prep kernel
 // (B1 = [Qt; -W], B2 = [Kh^T; Bm], Tb, gC; W = Tb Kt folds the intra-chunk
 // WY/UT transform into one operand):
 //
-//   pass A : S^T -> bf16 operand tile (and the saved chunk-start state);
-//            S^T <- S^T Diag(gC) in TMEM; values V^T -> operand tile
+//   pass A : S^T -> bf16 operand tile (the saved chunk-start state is a bulk
+//            copy of it); S^T <- S^T Diag(gC) in TMEM; values V^T -> operand tile
 //   phase 1: [O^T | U^T]  = S^T [Qt; -W]^T          (M=128, N=128, K=128)
 //            U^T         += V^T Tb^T                 (M=128, N=64,  K=64)
 //   pass B : U^T -> bf16 operand tile
-//   phase 2: [S^T | O^T] += U^T [Kh^T; Bm]^T         (M=128, N=192, K=64)
+//   phase 2: S^T += U^T Kh, O^T += U^T Bm^T          (M=128, N=128 + 64, K=64)
+// and the previous chunk's O^T is written out while phase 1 runs.
 //
 // i.e. U = Tb (V - Kt S), O = Qt S + Bm U, S <- gC*S + Kh^T U. One thread issues
 // the MMAs; completion is signalled through mbarriers (tcgen05.commit). The next
@@ -30,10 +31,10 @@ namespace kda {
 struct TcScanSmem {
   static constexpr int RECS = (TcRec::BYTES + 1023) / 1024 * 1024;
   static constexpr int REC0 = 0, REC1 = RECS;
-  static constexpr int AS = 2 * RECS;        // S^T bf16 [128][K=128]: two 16 KB blocks
-  static constexpr int AU = AS + 32768;      // U^T bf16 [128][K=64]
+  static constexpr int AS = 2 * RECS;        // S^T bf16 [128][K=128]: two 16 KB blocks (also the saved state)
+  static constexpr int AU = AS + 32768;      // U^T bf16 [128][K=64]; raw value rows before pass B
   static constexpr int AV = AU + 16384;      // V^T bf16 [128][K=64]
-  static constexpr int OST = AV + 16384;     // output staging [64 tok][128] bf16, plain rows
+  static constexpr int OST = AV + 16384;     // output staging [64 tok][128] bf16; warp w owns columns 32w..32w+31
   static constexpr int BAR = OST + 16384;    // record buffers 0/1, phase 1, phase 2
   static constexpr int TSLOT = BAR + 32;
   static constexpr int BYTES = TSLOT + 32 + 1024;   // + alignment slack
@@ -64,12 +65,15 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
     for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
   }
-  if (warp == 0) tc::alloc(tslot, 256);
+  if (warp == 0) tc::alloc(tslot, 512);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's lane quarter
+  // [O^T | U^T] of chunk j: columns [colO, colO + 128), alternating between two sets so
+  // chunk j's output can be read out while chunk j + 1's first products run
+  auto colO = [](int j) -> uint32_t { return 128u + 128u * (uint32_t)(j & 1); };
 
   auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * TcRec::BYTES; };
   // values of chunk j: 16-byte coalesced loads (row r = idx / 16, chunk idx % 16) held in registers
@@ -83,23 +87,27 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
       if (r < clen) vr[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
     }
   };
-  auto store_o = [&](int j) {   // staging -> o rows of chunk j
+  // O^T of chunk j (TMEM) -> o. Each warp transposes its 32 value channels through its
+  // own columns of the staging tile, then writes 64-byte row pieces with 16-byte stores.
+  auto store_o = [&](int j) {
     const long long t0 = s0 + (long long)j * CH;
     const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-    for (int idx = tid; idx < 64 * 16; idx += 128) {
-      const int r = idx >> 4, ch = idx & 15;
-      if (r < clen)
-        *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + r) * H + h) * 128 + ch * 8) =
-            *reinterpret_cast<const uint4 *>(smem + S::OST + r * 256 + ch * 16);
-    }
-  };
-  auto stage_o = [&]() {        // O^T (TMEM) -> staging [tok][value channel]
     uint32_t r[64];
-    tc::ld64(tl + 128, r);
+    tc::ld64(tl + colO(j), r);
     tc::wait_ld();
 #pragma unroll
     for (int i = 0; i < 64; ++i)
       *reinterpret_cast<bf16 *>(smem + S::OST + i * 256 + row * 2) = __float2bfloat16_rn(__uint_as_float(r[i]));
+    __syncwarp();
+    const int lane = tid & 31;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int tok = 8 * k + (lane >> 2), ch = 4 * warp + (lane & 3);   // 16-byte chunk ch of row tok
+      if (tok < clen)
+        *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + tok) * H + h) * 128 + ch * 8) =
+            *reinterpret_cast<const uint4 *>(smem + S::OST + tok * 256 + ch * 16);
+    }
+    __syncwarp();
   };
 
   // initial state: S^T[dv][dk] = h0[dk][dv]
@@ -127,10 +135,11 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
     char *rb = smem + (b ? S::REC1 : S::REC0);
     ok &= mbar_wait(&bar[b], (j >> 1) & 1);
     if (j > 0) ok &= mbar_wait(&bar[3], (j - 1) & 1);
+    if (tid == 32 && p.saved) bulk_wait_read();   // the previous saved-state copy has read the S^T tile
     tc::fence_after();
     if (!__syncthreads_and(ok)) break;
-    // pass A: state -> operand tile (+ saved state), scaled state back to TMEM;
-    // this chunk's values -> plain [tok][128] rows in the U tile (free until pass B)
+    // pass A: this chunk's values -> plain [tok][128] rows in the U tile (free until pass B);
+    // state -> operand tile, scaled state back to TMEM
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int idx = tid + 128 * i;
@@ -138,7 +147,6 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
     }
     {
       const float *gC = reinterpret_cast<const float *>(rb + TcRec::GC);
-      bf16 *sv = p.saved ? (bf16 *)p.saved + ((size_t)(cbase + j) * H + h) * 128 * 128 : nullptr;
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {   // 64 key channels at a time, one TMEM round trip each
         uint32_t r[64];
@@ -150,20 +158,13 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
 #pragma unroll
           for (int i = 0; i < 16; ++i) buf[i] = __uint_as_float(r[16 * cb + i]);
           const int k0 = 64 * hb + 16 * cb;
-          const uint4 lo = tc::pack8(buf), hi = tc::pack8(buf + 8);
-          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0)) = lo;
-          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = hi;
-          if (sv) {   // chunk-start state S^T[dv][dk] in the swizzled 128x128 tile layout
-            Tile<bf16, 128> t(sv);
-            *reinterpret_cast<uint4 *>(t.at(row, k0)) = lo;
-            *reinterpret_cast<uint4 *>(t.at(row, k0 + 8)) = hi;
-          }
+          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0)) = tc::pack8(buf);
+          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = tc::pack8(buf + 8);
 #pragma unroll
           for (int i = 0; i < 16; ++i) buf[i] *= gC[k0 + i];
           tc::st16(tl + k0, buf);
         }
       }
-      if (j > 0) stage_o();
       tc::wait_st();
     }
     __syncthreads();
@@ -190,12 +191,19 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
       for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + 128, tc::desc_sw128(as + kb * 16384 + 32 * ks), tc::desc_sw128(b1 + kb * 16384 + 32 * ks),
-                       tc::idesc_bf16(128, 128), (kb | ks) != 0);
+          tc::mma_bf16(tmem + colO(j), tc::desc_sw128(as + kb * 16384 + 32 * ks),
+                       tc::desc_sw128(b1 + kb * 16384 + 32 * ks), tc::idesc_bf16(128, 128), (kb | ks) != 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        tc::mma_bf16(tmem + 192, tc::desc_sw128(av + 32 * ks), tc::desc_sw128(tb + 32 * ks), tc::idesc_bf16(128, 64), 1);
+        tc::mma_bf16(tmem + colO(j) + 64, tc::desc_sw128(av + 32 * ks), tc::desc_sw128(tb + 32 * ks),
+                     tc::idesc_bf16(128, 64), 1);
       tc::commit(&bar[2]);
+    } else if (tid == 32) {
+      // the chunk-start state leaves as one bulk copy of the operand tile; the next record comes in
+      if (p.saved) {
+        bulk_s2g((bf16 *)p.saved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
+        bulk_commit();
+      }
       if (j >= 1 && j + 1 < nch) tc_issue_record(smem + ((j + 1) & 1 ? S::REC1 : S::REC0), rec_of(j + 1), &bar[(j + 1) & 1]);
     }
     if (j > 0) store_o(j - 1);
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
     // pass B: U^T -> operand tile
     {
       uint32_t r[64];
-      tc::ld64(tl + 192, r);
+      tc::ld64(tl + colO(j) + 64, r);
       tc::wait_ld();
 #pragma unroll
       for (int cb = 0; cb < 8; ++cb) {
@@ -220,10 +228,15 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
     if (!__syncthreads_and(ok)) break;
     if (tid == 0) {
       tc::fence_after();
+      // S^T += U^T Kh (B2 rows 0..127);  O^T += U^T Bm^T (B2 rows 128..191)
       const uint32_t au = smem_u32(smem + S::AU), b2 = smem_u32(rb + TcRec::B2);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        tc::mma_bf16(tmem, tc::desc_sw128(au + 32 * ks), tc::desc_sw128(b2 + 32 * ks), tc::idesc_bf16(128, 192), 1);
+        tc::mma_bf16(tmem, tc::desc_sw128(au + 32 * ks), tc::desc_sw128(b2 + 32 * ks), tc::idesc_bf16(128, 128), 1);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc::mma_bf16(tmem + colO(j), tc::desc_sw128(au + 32 * ks), tc::desc_sw128(b2 + 16384 + 32 * ks),
+                     tc::idesc_bf16(128, 64), 1);
       tc::commit(&bar[3]);
     }
     done = j + 1;
@@ -231,11 +244,7 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
   if (ok && done > 0) ok = mbar_wait(&bar[3], (done - 1) & 1);
   tc::fence_after();
   if (__syncthreads_and(ok)) {
-    if (done > 0) {
-      stage_o();
-      __syncthreads();
-      store_o(done - 1);
-    }
+    if (done > 0) store_o(done - 1);
     if (p.hT) {   // hT[dk][dv] = S^T[dv][dk]
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
@@ -249,9 +258,10 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
   } else {
     report(p.status, ERR_TIMEOUT);
   }
+  if (tid == 32 && p.saved) bulk_wait_all();   // saved states complete before the CTA leaves
   tc::fence_before();
   __syncthreads();
-  if (warp == 0) tc::dealloc(tmem, 256);
+  if (warp == 0) tc::dealloc(tmem, 512);
 }
 
 cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
@@ -268,7 +278,7 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
 // Reverse dS scan, same arrangement: dS^T in TMEM columns [0,128), dU^T in
 // [128,192), dV^T in [192,256). Per chunk (last to first), with the backward
 // record (Bm^T, Kh, [Qt^T | -W^T], Tb^T, gC):
-//   pass A : dS^T -> bf16 operand tile (and saved as the chunk-end dS);
+//   pass A : dS^T -> bf16 operand tile (saved as the chunk-end dS by one bulk copy);
 //            dS^T <- dS^T Diag(gC); dO^T -> operand tile (K-block 0 of A2)
 //   phase 1: dU^T  = dO^T Bm + dS^T Kh^T           (M=128, N=64, K=64 + 128)
 //   pass B : dU^T -> operand tile (K-block 1 of A2)
@@ -361,6 +371,7 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
     char *rb = smem + (b ? S::REC1 : S::REC0);
     ok &= mbar_wait(&bar[b], (it >> 1) & 1);
     if (it > 0) ok &= mbar_wait(&bar[3], (it - 1) & 1);
+    if (tid == 32) bulk_wait_read();   // the previous saved dS copy has read the dS^T tile
     tc::fence_after();
     if (!__syncthreads_and(ok)) break;
     // pass A
@@ -369,10 +380,8 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
       const int idx = tid + 128 * i;
       *reinterpret_cast<uint4 *>(smem + S::DST + (idx >> 4) * 256 + (idx & 15) * 16) = dr[i];
     }
-    if (it > 0) store_dv(j + 1);
     {
       const float *gC = reinterpret_cast<const float *>(rb + TcRecB::GC);
-      bf16 *sv = (bf16 *)p.dsaved + ((size_t)(cbase + j) * H + h) * 128 * 128;
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
         uint32_t r[64];
@@ -384,12 +393,8 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
 #pragma unroll
           for (int i = 0; i < 16; ++i) buf[i] = __uint_as_float(r[16 * cb + i]);
           const int k0 = 64 * hb + 16 * cb;
-          const uint4 lo = tc::pack8(buf), hi = tc::pack8(buf + 8);
-          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0)) = lo;
-          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = hi;
-          Tile<bf16, 128> t(sv);
-          *reinterpret_cast<uint4 *>(t.at(row, k0)) = lo;
-          *reinterpret_cast<uint4 *>(t.at(row, k0 + 8)) = hi;
+          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0)) = tc::pack8(buf);
+          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = tc::pack8(buf + 8);
 #pragma unroll
           for (int i = 0; i < 16; ++i) buf[i] *= gC[k0 + i];
           tc::st16(tl + k0, buf);
@@ -427,9 +432,14 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
           tc::mma_bf16(tmem + 128, tc::desc_sw128(as + kb * 16384 + 32 * ks), tc::desc_sw128(kh + kb * 8192 + 32 * ks),
                        tc::idesc_bf16(128, 64), 1);
       tc::commit(&bar[2]);
+    } else if (tid == 32) {
+      // the chunk-end dS leaves as one bulk copy of the operand tile; the next record comes in
+      bulk_s2g((bf16 *)p.dsaved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
+      bulk_commit();
       if (it >= 1 && it + 1 < nch)
         issue(smem + ((it + 1) & 1 ? S::REC1 : S::REC0), rec_of(j - 1), &bar[(it + 1) & 1]);
     }
+    if (it > 0) store_dv(j + 1);   // dV^T of the previous chunk; phase 1 leaves its columns alone
     if (it + 1 < nch) load_do(j - 1, dr);
     ok &= mbar_wait(&bar[2], it & 1);
     tc::fence_after();
@@ -484,6 +494,7 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
   } else {
     report(p.status, ERR_TIMEOUT);
   }
+  if (tid == 32) bulk_wait_all();   // saved dS complete before the CTA leaves
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, 256);

@@ -56,8 +56,8 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
   __syncthreads();
   if (tid == 0) {
     fence_proxy_async();
-    mbar_expect_tx(bar, S::REC + 4 * S::T128);
-    bulk_g2s(smem, (const char *)p.img + rid * S::REC, S::REC, bar);
+    mbar_expect_tx(bar, S::REC - S::KT + 4 * S::T128);   // the record's Qt slot is not needed here
+    bulk_g2s(smem + S::KT, (const char *)p.img + rid * S::REC + S::KT, S::REC - S::KT, bar);
     bulk_g2s(smem + S::SS, (const char *)p.saved + rid * 2 * S::T128, 2 * S::T128, bar);
     bulk_g2s(smem + S::SDS, (const char *)p.dsaved + rid * 2 * S::T128, 2 * S::T128, bar);
   }
@@ -170,10 +170,18 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
   zero(acc);
   wgemm<true, false, 8>(acc, sdV, 16 * mt, sS, 64 * nh, 0, 128);
   store128(GradLayout::dkt, acc);
-  if (tid < 128) {   // dgC_c = sum_v S[c][v] dS[c][v] = sum_v S^T[v][c] dS^T[v][c]
-    float s = 0.f;
-    for (int vv = 0; vv < 128; ++vv) s = fmaf(to_f(*sS.at(vv, tid)), to_f(*sdS.at(vv, tid)), s);
-    rec[GradLayout::dgc / 4 + tid] = s;
+  {   // dgC_c = sum_v S[c][v] dS[c][v] = sum_v S^T[v][c] dS^T[v][c]: two threads per channel,
+      // four independent partial sums each, halves combined through shared memory (the V tile is free)
+    const int c = tid & 127, half = tid >> 7;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int vv = 64 * half; vv < 64 * half + 64; vv += 4)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) s4[u] = fmaf(to_f(*sS.at(vv + u, c)), to_f(*sdS.at(vv + u, c)), s4[u]);
+    float *xch = reinterpret_cast<float *>(smem + S::SV);
+    if (half) xch[c] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    __syncthreads();
+    if (!half) rec[GradLayout::dgc / 4 + c] = (s4[0] + s4[1]) + (s4[2] + s4[3]) + xch[c];
   }
 }
 

@@ -3,8 +3,7 @@
 // One CTA (4 warps) per (sequence, head). The 128x128 fp32 state lives in tensor
 // memory for the whole sequence, transposed: TMEM lane m = value channel m,
 // column n = key channel n (S^T). Thread t of warp w owns lane 32w + t, so every
-// elementwise pass is a row pass. TMEM columns: [0,128) S^T, then O^T and U^T
-// (64 columns each) in two alternating sets at 128 and 256. Per 64-token chunk, with the record of the prep kernel
+// elementwise pass is a row pass. TMEM: two sets of 256 columns, [S^T | O^T | U^T]. Per 64-token chunk, with the record of the prep kernel
 // (B1 = [Qt; -W], B2 = [Kh^T; Bm], Tb, gC; W = Tb Kt folds the intra-chunk
 // WY/UT transform into one operand):
 //
@@ -13,8 +12,9 @@
 //   phase 1: [O^T | U^T]  = S^T [Qt; -W]^T          (M=128, N=128, K=128)
 //            U^T         += V^T Tb^T                 (M=128, N=64,  K=64)
 //   pass B : U^T -> bf16 operand tile
-//   phase 2: S^T += U^T Kh, O^T += U^T Bm^T          (M=128, N=128 + 64, K=64)
-// and the previous chunk's O^T is written out while phase 1 runs.
+//   phase 2: [S^T | O^T] += U^T [Kh^T; Bm]^T         (M=128, N=192, K=64)
+// TMEM holds two sets of [S^T | O^T | U^T], alternating per chunk, so the previous
+// chunk's O^T is written out while this chunk's phase 1 runs.
 //
 // i.e. U = Tb (V - Kt S), O = Qt S + Bm U, S <- gC*S + Kh^T U. One thread issues
 // the MMAs; completion is signalled through mbarriers (tcgen05.commit). The next
@@ -71,9 +71,12 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
   tc::fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's lane quarter
-  // [O^T | U^T] of chunk j: columns [colO, colO + 128), alternating between two sets so
-  // chunk j's output can be read out while chunk j + 1's first products run
-  auto colO = [](int j) -> uint32_t { return 128u + 128u * (uint32_t)(j & 1); };
+  // Two TMEM sets of [S^T | O^T | U^T] (128 + 64 + 64 columns) at 0 and 256; chunk j
+  // works in set j & 1: pass A reads its start state from the other set and writes the
+  // decayed state here, phase 2 accumulates [S^T | O^T] here in one N = 192 product, and
+  // O^T of chunk j survives while chunk j + 1 runs in the other set.
+  auto set_of = [](int j) -> uint32_t { return 256u * (uint32_t)(j & 1); };
+  auto colO = [&](int j) -> uint32_t { return set_of(j) + 128u; };
 
   auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * TcRec::BYTES; };
   // values of chunk j: 16-byte coalesced loads (row r = idx / 16, chunk idx % 16) held in registers
@@ -110,7 +113,7 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
     __syncwarp();
   };
 
-  // initial state: S^T[dv][dk] = h0[dk][dv]
+  // initial state S^T[dv][dk] = h0[dk][dv], in the set chunk 0 reads from
   {
     float buf[16];
 #pragma unroll
@@ -118,10 +121,14 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         buf[i] = p.h0 ? p.h0[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f;
-      tc::st16(tl + 16 * cb, buf);
+      tc::st16(tl + set_of(1) + 16 * cb, buf);
     }
     tc::wait_st();
   }
+  // shared-memory descriptors: the start-address field takes byte offsets >> 4 directly
+  const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS)), d_au = tc::desc_sw128(smem_u32(smem + S::AU)),
+                 d_av = tc::desc_sw128(smem_u32(smem + S::AV));
+  const uint64_t d_rec0 = tc::desc_sw128(smem_u32(smem + S::REC0)), d_rec1 = tc::desc_sw128(smem_u32(smem + S::REC1));
   if (tid == 0 && nch > 0) {
     tc_issue_record(smem + S::REC0, rec_of(0), &bar[0]);
     if (nch > 1) tc_issue_record(smem + S::REC1, rec_of(1), &bar[1]);
@@ -150,7 +157,7 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {   // 64 key channels at a time, one TMEM round trip each
         uint32_t r[64];
-        tc::ld64(tl + 64 * hb, r);
+        tc::ld64(tl + set_of(j + 1) + 64 * hb, r);
         tc::wait_ld();
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
           *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = tc::pack8(buf + 8);
 #pragma unroll
           for (int i = 0; i < 16; ++i) buf[i] *= gC[k0 + i];
-          tc::st16(tl + k0, buf);
+          tc::st16(tl + set_of(j) + k0, buf);
         }
       }
       tc::wait_st();
@@ -185,18 +192,17 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
     __syncthreads();
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t as = smem_u32(smem + S::AS), b1 = smem_u32(rb + TcRec::B1);
-      const uint32_t av = smem_u32(smem + S::AV), tb = smem_u32(rb + TcRec::TB);
+      const uint64_t d_rb = b ? d_rec1 : d_rec0, d_b1 = d_rb + (TcRec::B1 >> 4), d_tb = d_rb + (TcRec::TB >> 4);
+      const uint32_t dO = tmem + colO(j);
 #pragma unroll
       for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + colO(j), tc::desc_sw128(as + kb * 16384 + 32 * ks),
-                       tc::desc_sw128(b1 + kb * 16384 + 32 * ks), tc::idesc_bf16(128, 128), (kb | ks) != 0);
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t off = (kb * 16384 + 32 * ks) >> 4;
+          tc::mma_bf16(dO, d_as + off, d_b1 + off, tc::idesc_bf16(128, 128), (kb | ks) != 0);
+        }
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc::mma_bf16(tmem + colO(j) + 64, tc::desc_sw128(av + 32 * ks), tc::desc_sw128(tb + 32 * ks),
-                     tc::idesc_bf16(128, 64), 1);
+      for (int ks = 0; ks < 4; ++ks) tc::mma_bf16(dO + 64, d_av + 2 * ks, d_tb + 2 * ks, tc::idesc_bf16(128, 64), 1);
       tc::commit(&bar[2]);
     } else if (tid == 32) {
       // the chunk-start state leaves as one bulk copy of the operand tile; the next record comes in
@@ -228,15 +234,11 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
     if (!__syncthreads_and(ok)) break;
     if (tid == 0) {
       tc::fence_after();
-      // S^T += U^T Kh (B2 rows 0..127);  O^T += U^T Bm^T (B2 rows 128..191)
-      const uint32_t au = smem_u32(smem + S::AU), b2 = smem_u32(rb + TcRec::B2);
+      // [S^T | O^T] += U^T [Kh^T; Bm]^T in this chunk's set
+      const uint64_t d_b2 = (b ? d_rec1 : d_rec0) + (TcRec::B2 >> 4);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        tc::mma_bf16(tmem, tc::desc_sw128(au + 32 * ks), tc::desc_sw128(b2 + 32 * ks), tc::idesc_bf16(128, 128), 1);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc::mma_bf16(tmem + colO(j), tc::desc_sw128(au + 32 * ks), tc::desc_sw128(b2 + 16384 + 32 * ks),
-                     tc::idesc_bf16(128, 64), 1);
+        tc::mma_bf16(tmem + set_of(j), d_au + 2 * ks, d_b2 + 2 * ks, tc::idesc_bf16(128, 192), 1);
       tc::commit(&bar[3]);
     }
     done = j + 1;
@@ -245,11 +247,11 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
   tc::fence_after();
   if (__syncthreads_and(ok)) {
     if (done > 0) store_o(done - 1);
-    if (p.hT) {   // hT[dk][dv] = S^T[dv][dk]
+    if (p.hT) {   // hT[dk][dv] = S^T[dv][dk], in the set of the last chunk
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
         uint32_t r[64];
-        tc::ld64(tl + 64 * hb, r);
+        tc::ld64(tl + set_of(done + 1) + 64 * hb, r);
         tc::wait_ld();
 #pragma unroll
         for (int i = 0; i < 64; ++i) p.hT[(sh * 128 + 64 * hb + i) * 128 + row] = __uint_as_float(r[i]);
@@ -358,6 +360,8 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
     }
     tc::wait_st();
   }
+  const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS)), d_a2 = tc::desc_sw128(smem_u32(smem + S::A2));
+  const uint64_t d_rec0 = tc::desc_sw128(smem_u32(smem + S::REC0)), d_rec1 = tc::desc_sw128(smem_u32(smem + S::REC1));
   if (tid == 0 && nch > 0) {
     issue(smem + S::REC0, rec_of(nch - 1), &bar[0]);
     if (nch > 1) issue(smem + S::REC1, rec_of(nch - 2), &bar[1]);
@@ -420,16 +424,14 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
     __syncthreads();
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t a2 = smem_u32(smem + S::A2), as = smem_u32(smem + S::AS);
-      const uint32_t bmt = smem_u32(rb + TcRecB::BMT), kh = smem_u32(rb + TcRecB::KH);
+      const uint64_t d_rb = b ? d_rec1 : d_rec0, d_bmt = d_rb + (TcRecB::BMT >> 4), d_kh = d_rb + (TcRecB::KH >> 4);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc::mma_bf16(tmem + 128, tc::desc_sw128(a2 + 32 * ks), tc::desc_sw128(bmt + 32 * ks), tc::idesc_bf16(128, 64), ks > 0);
+      for (int ks = 0; ks < 4; ++ks) tc::mma_bf16(tmem + 128, d_a2 + 2 * ks, d_bmt + 2 * ks, tc::idesc_bf16(128, 64), ks > 0);
 #pragma unroll
       for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + 128, tc::desc_sw128(as + kb * 16384 + 32 * ks), tc::desc_sw128(kh + kb * 8192 + 32 * ks),
+          tc::mma_bf16(tmem + 128, d_as + ((kb * 16384 + 32 * ks) >> 4), d_kh + ((kb * 8192 + 32 * ks) >> 4),
                        tc::idesc_bf16(128, 64), 1);
       tc::commit(&bar[2]);
     } else if (tid == 32) {
@@ -461,17 +463,17 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
     if (!__syncthreads_and(ok)) break;
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t a2 = smem_u32(smem + S::A2), qwt = smem_u32(rb + TcRecB::QWT), tbt = smem_u32(rb + TcRecB::TBT);
+      const uint64_t d_rb = b ? d_rec1 : d_rec0, d_qwt = d_rb + (TcRecB::QWT >> 4), d_tbt = d_rb + (TcRecB::TBT >> 4);
 #pragma unroll
       for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem, tc::desc_sw128(a2 + kb * 16384 + 32 * ks), tc::desc_sw128(qwt + kb * 16384 + 32 * ks),
-                       tc::idesc_bf16(128, 128), 1);
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t off = (kb * 16384 + 32 * ks) >> 4;
+          tc::mma_bf16(tmem, d_a2 + off, d_qwt + off, tc::idesc_bf16(128, 128), 1);
+        }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        tc::mma_bf16(tmem + 192, tc::desc_sw128(a2 + 16384 + 32 * ks), tc::desc_sw128(tbt + 32 * ks),
-                     tc::idesc_bf16(128, 64), ks > 0);
+        tc::mma_bf16(tmem + 192, d_a2 + (16384 >> 4) + 2 * ks, d_tbt + 2 * ks, tc::idesc_bf16(128, 64), ks > 0);
       tc::commit(&bar[3]);
     }
     done = it + 1;

@@ -129,14 +129,13 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
     float a4[4][4];
     zero(a4);
     wgemm<true, true, 4>(a4, sdO, 16 * mt, sU, 32 * nh, 0, 128);
-    float *dbm = rec + GradLayout::dbm / 4;
+    bf16 *dbm = reinterpret_cast<bf16 *>(reinterpret_cast<char *>(rec) + GradLayout::dbm);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int r = r0 + 8 * hh, j = 32 * nh + 8 * nt + 2 * q4;
-        *reinterpret_cast<float2 *>(dbm + r * 64 + j) =
-            make_float2(j <= r ? a4[nt][2 * hh] : 0.f, j + 1 <= r ? a4[nt][2 * hh + 1] : 0.f);
+        st2(dbm + r * 64 + j, j <= r ? a4[nt][2 * hh] : 0.f, j + 1 <= r ? a4[nt][2 * hh + 1] : 0.f);
       }
     zero(a4);
     wgemm<true, true, 4>(a4, sdU, 16 * mt, sV, 32 * nh, 0, 128);
@@ -194,23 +193,27 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
 // Gradients w.r.t. the factor tiles are gathered first, then
 //   dq^ = dQL x,  dk^ = dKL x + dR y,  dG = dQL QL + dKL KL - dR R,
 // dg = reverse cumulative sum of dG inside the chunk (plus the e^{G_last} terms
-// on the last row), and the L2-norm backward gives dq, dk.
+// on the last row), and the L2-norm backward gives dq, dk. The products through T
+// (64x64) run on TF32 tensor cores; the factor tiles, dA and dBm are bf16 operands
+// of the bf16 tensor cores (fp32 accumulation).
 constexpr int INTRA_THREADS = 512;
 constexpr int LDI = 132;   // padded fp32 row, 128-wide tiles
 constexpr int LDJ = 68;    // padded fp32 row, 64-wide tiles
 
 struct IntraSmem {
-  static constexpr int T128 = 64 * LDI * 4, T64 = 64 * LDJ * 4;
-  static constexpr int KL = 0, QL = T128, R = 2 * T128, CS = 3 * T128;   // CS: local gate sums -> dG
-  static constexpr int TT = 4 * T128, DT = TT + T64, X = DT + T64, DB = X + T64;   // DT: dTb -> dT -> dA
-  static constexpr int DV = DB + T64;                    // [10][128] pair factors
-  static constexpr int TOT = DV + 10 * 512;              // [4][128]
-  static constexpr int PV = TOT + 4 * 512, FV = PV + 4 * 512;   // [4][128] each
+  static constexpr int T128 = 64 * LDI * 4, T64 = 64 * LDJ * 4, B128 = 64 * 128 * 2, B64 = 64 * 64 * 2;
+  static constexpr int KL = 0, QL = B128, R = 2 * B128;        // bf16 factor tiles, Tile<bf16, 128>
+  static constexpr int CS = 3 * B128;                          // fp32 [64][LDI]: g, local gate sums, then dG
+  static constexpr int TT = CS + T128, DT = TT + T64, X = DT + T64;   // fp32 [64][LDJ]: T, dTb -> dT, X
+  static constexpr int DAB = X + T64, DBB = DAB + B64;         // bf16 Tile<bf16, 64>: dA, dBm
+  static constexpr int DV = DBB + B64;                         // [10][128] pair factors
+  static constexpr int TOT = DV + 10 * 512;                    // [4][128]
+  static constexpr int PV = TOT + 4 * 512, FV = PV + 4 * 512;  // [4][128] each
   static constexpr int RQ = FV + 4 * 512, RQ0 = RQ + 256, RK = RQ0 + 256, BETA = RK + 256;
-  static constexpr int DB1 = BETA + 256, DB2 = DB1 + 256;       // dbeta parts: [64], [4][64]
+  static constexpr int DB1 = BETA + 256, DB2 = DB1 + 256;      // dbeta parts: [64], [4][64]
   static constexpr int ROWQ = DB2 + 1024, ROWK = ROWQ + 1024;  // [4][64]
-  static constexpr int PART = ROWK + 1024;               // [4][128]
-  static constexpr int DGC = PART + 2048;                // [128]
+  static constexpr int PART = ROWK + 1024;                     // [4][128]
+  static constexpr int DGC = PART + 2048;                      // [128]
   static constexpr int BYTES = DGC + 512;
 };
 
@@ -248,10 +251,10 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
   const float *rec = p.grad + rid * (GradLayout::bytes / 4);
   const float *auxA = p.aux + rid * (2 * 64 * 64), *auxT = auxA + 64 * 64;
   const bf16 *qg = (const bf16 *)p.q, *kg = (const bf16 *)p.k;
-  float *KL = (float *)(smem + S::KL), *QL = (float *)(smem + S::QL), *RR = (float *)(smem + S::R),
-        *CS = (float *)(smem + S::CS);
-  float *TT = (float *)(smem + S::TT), *DT = (float *)(smem + S::DT), *XX = (float *)(smem + S::X),
-        *DBm = (float *)(smem + S::DB);
+  const Tile<bf16, 128> KLt((bf16 *)(smem + S::KL)), QLt((bf16 *)(smem + S::QL)), Rt((bf16 *)(smem + S::R));
+  const Tile<bf16, 64> DAt((bf16 *)(smem + S::DAB)), DBt((bf16 *)(smem + S::DBB));
+  float *CS = (float *)(smem + S::CS);
+  float *TT = (float *)(smem + S::TT), *DT = (float *)(smem + S::DT), *XX = (float *)(smem + S::X);
   float(*dv)[128] = (float(*)[128])(smem + S::DV);
   float(*tot)[128] = (float(*)[128])(smem + S::TOT);
   float(*pv)[128] = (float(*)[128])(smem + S::PV);
@@ -260,25 +263,27 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
         *sb = (float *)(smem + S::BETA);
 
   // P0: stage the chunk's inputs with one batch of asynchronous copies: q (bf16) in
-  //     the X tile, k in the KL tile, g (fp32, row stride LDI) in the QL tile, T, dTb
-  //     and dBm in their 64x64 tiles, dgC. Rows past the sequence end read as zero.
-  const bf16 *sq_ = (const bf16 *)XX, *sk_ = (const bf16 *)KL;
+  //     the X tile, k in the KL tile, g (fp32, row stride LDI) in the CS tile, T and
+  //     dTb in their fp32 64x64 tiles, dBm (bf16) in its tile, dgC. Rows past the
+  //     sequence end read as zero.
+  const bf16 *sq_ = (const bf16 *)XX, *sk_ = (const bf16 *)(smem + S::KL);
   {
+    const char *grec = reinterpret_cast<const char *>(rec);
     for (int idx = tid; idx < 64 * 16; idx += INTRA_THREADS) {
       const int r = idx >> 4, ch = idx & 15;
       const bool ok = r < ref.len;
       const size_t off = ok ? ((size_t)(ref.t0 + r) * H + h) * D + 8 * ch : 0;
       cp_async16((bf16 *)XX + r * D + 8 * ch, qg + off, ok ? 16 : 0);
-      cp_async16((bf16 *)KL + r * D + 8 * ch, kg + off, ok ? 16 : 0);
+      cp_async16((bf16 *)(smem + S::KL) + r * D + 8 * ch, kg + off, ok ? 16 : 0);
       cp_async16(TT + r * LDJ + 4 * ch, auxT + r * 64 + 4 * ch);
       cp_async16(DT + r * LDJ + 4 * ch, rec + GradLayout::dtb / 4 + r * 64 + 4 * ch);
-      cp_async16(DBm + r * LDJ + 4 * ch, rec + GradLayout::dbm / 4 + r * 64 + 4 * ch);
+      if (ch < 8) cp_async16(DBt.at(r, 8 * ch), grec + GradLayout::dbm + r * 128 + 16 * ch);
     }
     for (int idx = tid; idx < 64 * 32; idx += INTRA_THREADS) {
       const int r = idx >> 5, ch = idx & 31;
       const bool ok = r < ref.len;
       const float *src = ok ? p.g + ((size_t)(ref.t0 + r) * H + h) * D + 4 * ch : p.g;
-      cp_async16(QL + r * LDI + 4 * ch, src, ok ? 16 : 0);
+      cp_async16(CS + r * LDI + 4 * ch, src, ok ? 16 : 0);
     }
     if (tid < 32) cp_async16((float *)(smem + S::DGC) + 4 * tid, rec + GradLayout::dgc / 4 + 4 * tid);
     if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
-      cs[i] = *reinterpret_cast<const float2 *>(QL + r * LDI + c0);
+      cs[i] = *reinterpret_cast<const float2 *>(CS + r * LDI + c0);
       qpair[i] = *reinterpret_cast<const __nv_bfloat162 *>(sq_ + r * D + c0);
       kpair[i] = *reinterpret_cast<const __nv_bfloat162 *>(sk_ + r * D + c0);
     }
@@ -362,9 +367,9 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
       const float x0 = exp2f(cs[i].x), x1 = exp2f(cs[i].y);
       const float y0 = exp2f(ta0 - cs[i].x), y1 = exp2f(ta1 - cs[i].y);
       const float kh0 = kv.x * rk[r], kh1 = kv.y * rk[r];
-      *reinterpret_cast<float2 *>(KL + r * LDI + c0) = make_float2(kh0 * x0, kh1 * x1);
-      *reinterpret_cast<float2 *>(QL + r * LDI + c0) = make_float2(qv.x * rq[r] * x0, qv.y * rq[r] * x1);
-      *reinterpret_cast<float2 *>(RR + r * LDI + c0) = make_float2(kh0 * y0, kh1 * y1);
+      st2(KLt.at(r, c0), kh0 * x0, kh1 * x1);
+      st2(QLt.at(r, c0), qv.x * rq[r] * x0, qv.y * rq[r] * x1);
+      st2(Rt.at(r, c0), kh0 * y0, kh1 * y1);
       *reinterpret_cast<float2 *>(CS + r * LDI + c0) = cs[i];
     }
   } else if (tid < 320) {
@@ -408,7 +413,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
         const float d0 = j < r ? -acc[nt][2 * hh] : 0.f, d1 = j + 1 < r ? -acc[nt][2 * hh + 1] : 0.f;
         const float2 av = *reinterpret_cast<const float2 *>(auxA + r * 64 + j);
         part[hh] = fmaf(d0, j < r ? av.x : 0.f, fmaf(d1, j + 1 < r ? av.y : 0.f, part[hh]));
-        *reinterpret_cast<float2 *>(DT + r * LDJ + j) = make_float2(sb[r] * d0, sb[r] * d1);
+        st2(DAt.at(r, j), sb[r] * d0, sb[r] * d1);
       }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -451,16 +456,30 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
   zero(tQ);
   zero(tK);
   zero(tW);
+  // tQ, tK: sum over sub-blocks b <= t of (dBm | dA)[t, b] (R_b o D_tb); the per-channel pair
+  // factor D_tb scales result columns, so each block product is scaled as it is added
   for (int b = 0; b <= t; ++b) {
     const float *dsc = dv[t * (t + 1) / 2 + b] + cbase;
-    mma_tf32_block<4>(tQ, DBm + 16 * t * LDJ + 16 * b, LDJ, 1, RR + 16 * b * LDI + cbase, LDI, 1, 0, 16, dsc);
-    mma_tf32_block<4>(tK, DT + 16 * t * LDJ + 16 * b, LDJ, 1, RR + 16 * b * LDI + cbase, LDI, 1, 0, 16, dsc);
+    float pq[4][4], pk[4][4];
+    zero(pq);
+    zero(pk);
+    wgemm<true, false, 4>(pq, DBt, 16 * t, Rt, cbase, 16 * b, 16 * b + 16);
+    wgemm<true, false, 4>(pk, DAt, 16 * t, Rt, cbase, 16 * b, 16 * b + 16);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float d = dsc[8 * nt + 2 * q + (e & 1)];
+        tQ[nt][e] = fmaf(pq[nt][e], d, tQ[nt][e]);
+        tK[nt][e] = fmaf(pk[nt][e], d, tK[nt][e]);
+      }
   }
+  // tW: sum over sub-blocks aa >= t of D_{aa,t} o ((dBm^T QL + dA^T KL)[aa rows -> t])
   for (int aa = t; aa < NSUB; ++aa) {
     float tR[4][4];
     zero(tR);
-    mma_tf32_block<4>(tR, DBm + 16 * aa * LDJ + 16 * t, 1, LDJ, QL + 16 * aa * LDI + cbase, LDI, 1, 0, 16);
-    mma_tf32_block<4>(tR, DT + 16 * aa * LDJ + 16 * t, 1, LDJ, KL + 16 * aa * LDI + cbase, LDI, 1, 0, 16);
+    wgemm<false, false, 4>(tR, DBt, 16 * t, QLt, cbase, 16 * aa, 16 * aa + 16);
+    wgemm<false, false, 4>(tR, DAt, 16 * t, KLt, cbase, 16 * aa, 16 * aa + 16);
     const float *dsc = dv[aa * (aa + 1) / 2 + t] + cbase;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
@@ -489,7 +508,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) kda_bwd_intra_kernel(BwdIntr
           const float pa = pv[t][cc], fa = fv[t][cc];
           const float csv = CS[r * LDI + cc];
           const float x = exp2f(csv), y = exp2f(tot[t][cc] - csv);
-          const float ql = QL[r * LDI + cc], kl = KL[r * LDI + cc], rr = RR[r * LDI + cc];
+          const float ql = to_f(*QLt.at(r, cc)), kl = to_f(*KLt.at(r, cc)), rr = to_f(*Rt.at(r, cc));
           const float dQL = tQ[nt][e] + dqtv[e2] * pa, dKL = tK[nt][e] + dktv[e2] * pa;
           const float dR = tW[nt][e] + dkkv[e2] * fa;
           const float dq_ = dQL * x, dk_ = dKL * x + dR * y;

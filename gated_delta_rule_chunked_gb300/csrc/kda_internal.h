@@ -52,11 +52,11 @@ struct TcRecB {
 // Per-(chunk, head) record of state-side gradients written by the backward's
 // state kernel: dQt, dKt, dKh (64x128 fp32 each), dBm, dTb (64x64 fp32), dgC (128).
 // State-side gradients of one (chunk, head), written by the state kernel for the
-// intra kernel: dQt, dKt, dKh as bf16 [64][128] (fp32 accumulation, rounded once),
-// dBm, dTb fp32 [64][64], dgC fp32 [128]. Byte offsets.
+// intra kernel: dQt, dKt, dKh bf16 [64][128] and dBm bf16 [64][64] (fp32
+// accumulation, rounded once), dTb fp32 [64][64], dgC fp32 [128]. Byte offsets.
 struct GradLayout {
   static constexpr size_t dqt = 0, dkt = 64 * 128 * 2, dkh = 2 * 64 * 128 * 2, dbm = 3 * 64 * 128 * 2,
-                          dtb = dbm + 64 * 64 * 4, dgc = dtb + 64 * 64 * 4, bytes = dgc + 128 * 4;
+                          dtb = dbm + 64 * 64 * 2, dgc = dtb + 64 * 64 * 4, bytes = dgc + 128 * 4;
 };
 
 struct SeqGeom {

@@ -53,6 +53,7 @@ def check_fwd(kda, b, tol, scale=1.0):
     res = oracle.fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, scale=scale)
     o_ref, h_ref = oracle.assemble_fwd(res, b.cu_seqlens, b.heads, 128)
     e_o, e_h = rel(o.float().cpu(), o_ref), rel(hT.cpu(), h_ref)
+    print("fwd", f"o {e_o:.2e} hT {e_h:.2e}")
     assert e_o <= tol and e_h <= tol, (e_o, e_h)
     return e_o, e_h
 
@@ -136,6 +137,7 @@ def check_bwd(kda, b, tol, tasks=None):
             refs.append(r[name].ravel())
         errs[name] = rel(np.concatenate(gots), np.concatenate(refs))
     bad = {k: v for k, v in errs.items() if not v <= tol}
+    print("bwd", {k: f"{v:.2e}" for k, v in errs.items()})
     assert not bad, errs
     return errs
 

@@ -22,6 +22,8 @@
 namespace kda {
 
 // ------------------------------------------------------------ state kernel
+constexpr int STATE_THREADS = 512;   // 16 warps: 4 row blocks x 4 column quarters of every product
+
 template <typename E>
 struct StateSmem {
   static constexpr int T128 = 64 * 128 * (int)sizeof(E), T64 = 64 * 64 * (int)sizeof(E);
@@ -39,14 +41,14 @@ struct StateSmem {
 };
 
 template <typename E>
-__global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
+__global__ void __launch_bounds__(STATE_THREADS) kda_bwd_state_kernel(BwdStateParams p) {
   using S = StateSmem<E>;
   extern __shared__ __align__(128) char smem[];
   const int chunk = blockIdx.x, h = blockIdx.y, H = p.geo.heads;
   ChunkRef ref;
   if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g8 = lane >> 2, q4 = lane & 3;
-  const int mt = warp & 3, nh = warp >> 2;
+  const int mt = warp & 3, nq = warp >> 2;   // 16-row block, 32-column quarter
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
   const size_t rid = (size_t)chunk * H + h;
   if (tid == 0) {
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
   {
     constexpr int EPC = 16 / sizeof(E), CPR = 128 / EPC;
     const E *v = (const E *)p.v, *dO = (const E *)p.dO;
-    for (int idx = tid; idx < 64 * CPR; idx += 256) {
+    for (int idx = tid; idx < 64 * CPR; idx += STATE_THREADS) {
       const int r = idx / CPR, ch = idx % CPR;
       uint4 a = make_uint4(0, 0, 0, 0), b = a;
       if (r < ref.len) {
@@ -85,103 +87,104 @@ __global__ void __launch_bounds__(256) kda_bwd_state_kernel(BwdStateParams p) {
   const bool ok = mbar_wait(bar, 0);
   if (!__syncthreads_and(ok)) { report(p.status, ERR_TIMEOUT); return; }
 
-  float acc[8][4];
+  float acc[4][4];
   const int r0 = 16 * mt + g8;
   // V' = V - Kt S (in place); B(k, n) = S[k][n] = S^T[n][k]
   zero(acc);
-  wgemm<true, true, 8>(acc, Kt, 16 * mt, sS, 64 * nh, 0, 128);
+  wgemm<true, true, 4>(acc, Kt, 16 * mt, sS, 32 * nq, 0, 128);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      E *e = sV.at(r0 + 8 * hh, 64 * nh + 8 * nt + 2 * q4);
+      E *e = sV.at(r0 + 8 * hh, 32 * nq + 8 * nt + 2 * q4);
       const float2 x = ld2(e);
       st2(e, x.x - acc[nt][2 * hh], x.y - acc[nt][2 * hh + 1]);
     }
   __syncthreads();
   // U = Tb V' ;  dU = Bm^T dO + Kh dS
   zero(acc);
-  wgemm<true, false, 8>(acc, Tb, 16 * mt, sV, 64 * nh, 0, 16 * (mt + 1));
+  wgemm<true, false, 4>(acc, Tb, 16 * mt, sV, 32 * nq, 0, 16 * (mt + 1));
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
-      st2(sU.at(r0 + 8 * hh, 64 * nh + 8 * nt + 2 * q4), acc[nt][2 * hh], acc[nt][2 * hh + 1]);
+      st2(sU.at(r0 + 8 * hh, 32 * nq + 8 * nt + 2 * q4), acc[nt][2 * hh], acc[nt][2 * hh + 1]);
   zero(acc);
-  wgemm<false, false, 8>(acc, Bm, 16 * mt, sdO, 64 * nh, 16 * mt, 64);
-  wgemm<true, true, 8>(acc, Kh, 16 * mt, sdS, 64 * nh, 0, 128);   // B(k=c, n=v) = dS^T[v][c]
+  wgemm<false, false, 4>(acc, Bm, 16 * mt, sdO, 32 * nq, 16 * mt, 64);
+  wgemm<true, true, 4>(acc, Kh, 16 * mt, sdS, 32 * nq, 0, 128);   // B(k=c, n=v) = dS^T[v][c]
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
-      st2(sdU.at(r0 + 8 * hh, 64 * nh + 8 * nt + 2 * q4), acc[nt][2 * hh], acc[nt][2 * hh + 1]);
+      st2(sdU.at(r0 + 8 * hh, 32 * nq + 8 * nt + 2 * q4), acc[nt][2 * hh], acc[nt][2 * hh + 1]);
   __syncthreads();
   float *rec = p.grad + rid * (GradLayout::bytes / 4);
   // -dV' = -Tb^T dU ;  dBm = dO U^T ;  dTb = dU V'^T
   zero(acc);
-  wgemm<false, false, 8>(acc, Tb, 16 * mt, sdU, 64 * nh, 16 * mt, 64);
+  wgemm<false, false, 4>(acc, Tb, 16 * mt, sdU, 32 * nq, 16 * mt, 64);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
-      st2(sdV.at(r0 + 8 * hh, 64 * nh + 8 * nt + 2 * q4), -acc[nt][2 * hh], -acc[nt][2 * hh + 1]);
+      st2(sdV.at(r0 + 8 * hh, 32 * nq + 8 * nt + 2 * q4), -acc[nt][2 * hh], -acc[nt][2 * hh + 1]);
   {
-    float a4[4][4];
+    float a4[2][4];
     zero(a4);
-    wgemm<true, true, 4>(a4, sdO, 16 * mt, sU, 32 * nh, 0, 128);
+    wgemm<true, true, 2>(a4, sdO, 16 * mt, sU, 16 * nq, 0, 128);
     bf16 *dbm = reinterpret_cast<bf16 *>(reinterpret_cast<char *>(rec) + GradLayout::dbm);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int r = r0 + 8 * hh, j = 32 * nh + 8 * nt + 2 * q4;
+        const int r = r0 + 8 * hh, j = 16 * nq + 8 * nt + 2 * q4;
         st2(dbm + r * 64 + j, j <= r ? a4[nt][2 * hh] : 0.f, j + 1 <= r ? a4[nt][2 * hh + 1] : 0.f);
       }
     zero(a4);
-    wgemm<true, true, 4>(a4, sdU, 16 * mt, sV, 32 * nh, 0, 128);
+    wgemm<true, true, 2>(a4, sdU, 16 * mt, sV, 16 * nq, 0, 128);
     float *dtb = rec + GradLayout::dtb / 4;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int r = r0 + 8 * hh, j = 32 * nh + 8 * nt + 2 * q4;
+        const int r = r0 + 8 * hh, j = 16 * nq + 8 * nt + 2 * q4;
         *reinterpret_cast<float2 *>(dtb + r * 64 + j) =
             make_float2(j <= r ? a4[nt][2 * hh] : 0.f, j + 1 <= r ? a4[nt][2 * hh + 1] : 0.f);
       }
   }
   __syncthreads();
   // dQt = dO S^T ; dKh = U dS^T ; dKt = -dV' S^T
-  auto store128 = [&](size_t off, float(&a)[8][4]) {   // bf16 [64][128] at byte offset off
+  auto store128 = [&](size_t off, float(&a)[4][4]) {   // bf16 [64][128] at byte offset off
     bf16 *dst = reinterpret_cast<bf16 *>(reinterpret_cast<char *>(rec) + off);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh)
-        *reinterpret_cast<__nv_bfloat162 *>(dst + (r0 + 8 * hh) * 128 + 64 * nh + 8 * nt + 2 * q4) =
+        *reinterpret_cast<__nv_bfloat162 *>(dst + (r0 + 8 * hh) * 128 + 32 * nq + 8 * nt + 2 * q4) =
             __floats2bfloat162_rn(a[nt][2 * hh], a[nt][2 * hh + 1]);
   };
   zero(acc);
-  wgemm<true, false, 8>(acc, sdO, 16 * mt, sS, 64 * nh, 0, 128);   // B(k=v, n=c) = S^T[v][c]
+  wgemm<true, false, 4>(acc, sdO, 16 * mt, sS, 32 * nq, 0, 128);   // B(k=v, n=c) = S^T[v][c]
   store128(GradLayout::dqt, acc);
   zero(acc);
-  wgemm<true, false, 8>(acc, sU, 16 * mt, sdS, 64 * nh, 0, 128);  // B(k=v, n=c) = dS^T[v][c]
+  wgemm<true, false, 4>(acc, sU, 16 * mt, sdS, 32 * nq, 0, 128);  // B(k=v, n=c) = dS^T[v][c]
   store128(GradLayout::dkh, acc);
   zero(acc);
-  wgemm<true, false, 8>(acc, sdV, 16 * mt, sS, 64 * nh, 0, 128);
+  wgemm<true, false, 4>(acc, sdV, 16 * mt, sS, 32 * nq, 0, 128);
   store128(GradLayout::dkt, acc);
-  {   // dgC_c = sum_v S[c][v] dS[c][v] = sum_v S^T[v][c] dS^T[v][c]: two threads per channel,
-      // four independent partial sums each, halves combined through shared memory (the V tile is free)
-    const int c = tid & 127, half = tid >> 7;
+  {   // dgC_c = sum_v S[c][v] dS[c][v] = sum_v S^T[v][c] dS^T[v][c]: four threads per channel,
+      // four independent partial sums each, quarters combined through shared memory (the V tile is free)
+    const int c = tid & 127, qv = tid >> 7;
     float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int vv = 64 * half; vv < 64 * half + 64; vv += 4)
+#pragma unroll
+    for (int vv = 32 * qv; vv < 32 * qv + 32; vv += 4)
 #pragma unroll
       for (int u = 0; u < 4; ++u) s4[u] = fmaf(to_f(*sS.at(vv + u, c)), to_f(*sdS.at(vv + u, c)), s4[u]);
     float *xch = reinterpret_cast<float *>(smem + S::SV);
-    if (half) xch[c] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    xch[qv * 128 + c] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     __syncthreads();
-    if (!half) rec[GradLayout::dgc / 4 + c] = (s4[0] + s4[1]) + (s4[2] + s4[3]) + xch[c];
+    if (qv == 0) rec[GradLayout::dgc / 4 + c] = (xch[c] + xch[128 + c]) + (xch[256 + c] + xch[384 + c]);
   }
+
 }
 
 // ------------------------------------------------------------ intra kernel
@@ -599,7 +602,7 @@ cudaError_t launch_bwd_state(const BwdStateParams &p, bool f32, cudaStream_t s) 
   if (p.geo.max_chunks == 0) return cudaSuccess;
   if (f32) return cudaErrorNotSupported;
   return launch_chunk_kernel(kda_bwd_state_kernel<bf16>, StateSmem<bf16>::BYTES,
-                             dim3(p.geo.max_chunks, p.geo.heads), 256, &p, s);
+                             dim3(p.geo.max_chunks, p.geo.heads), STATE_THREADS, &p, s);
 }
 
 cudaError_t launch_bwd_intra(const BwdIntraParams &p, bool f32, cudaStream_t s) {

@@ -145,6 +145,10 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
     if (tid == 32 && p.saved) bulk_wait_read();   // the previous saved-state copy has read the S^T tile
     tc::fence_after();
     if (!__syncthreads_and(ok)) break;
+    // the other record buffer's last reader (phase 2 of the previous chunk) has finished:
+    // fetch the next chunk's record now, a whole chunk step ahead
+    if (tid == 32 && j >= 1 && j + 1 < nch)
+      tc_issue_record(smem + ((j + 1) & 1 ? S::REC1 : S::REC0), rec_of(j + 1), &bar[(j + 1) & 1]);
     // pass A: this chunk's values -> plain [tok][128] rows in the U tile (free until pass B);
     // state -> operand tile, scaled state back to TMEM
 #pragma unroll
@@ -205,12 +209,11 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
       for (int ks = 0; ks < 4; ++ks) tc::mma_bf16(dO + 64, d_av + 2 * ks, d_tb + 2 * ks, tc::idesc_bf16(128, 64), 1);
       tc::commit(&bar[2]);
     } else if (tid == 32) {
-      // the chunk-start state leaves as one bulk copy of the operand tile; the next record comes in
+      // the chunk-start state leaves as one bulk copy of the operand tile
       if (p.saved) {
         bulk_s2g((bf16 *)p.saved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
         bulk_commit();
       }
-      if (j >= 1 && j + 1 < nch) tc_issue_record(smem + ((j + 1) & 1 ? S::REC1 : S::REC0), rec_of(j + 1), &bar[(j + 1) & 1]);
     }
     if (j > 0) store_o(j - 1);
     if (j + 1 < nch) load_v(j + 1, vr);
@@ -378,6 +381,8 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
     if (tid == 32) bulk_wait_read();   // the previous saved dS copy has read the dS^T tile
     tc::fence_after();
     if (!__syncthreads_and(ok)) break;
+    if (tid == 32 && it >= 1 && it + 1 < nch)   // next record, a whole chunk step ahead
+      issue(smem + ((it + 1) & 1 ? S::REC1 : S::REC0), rec_of(j - 1), &bar[(it + 1) & 1]);
     // pass A
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -435,11 +440,9 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
                        tc::idesc_bf16(128, 64), 1);
       tc::commit(&bar[2]);
     } else if (tid == 32) {
-      // the chunk-end dS leaves as one bulk copy of the operand tile; the next record comes in
+      // the chunk-end dS leaves as one bulk copy of the operand tile
       bulk_s2g((bf16 *)p.dsaved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
       bulk_commit();
-      if (it >= 1 && it + 1 < nch)
-        issue(smem + ((it + 1) & 1 ? S::REC1 : S::REC0), rec_of(j - 1), &bar[(it + 1) & 1]);
     }
     if (it > 0) store_dv(j + 1);   // dV^T of the previous chunk; phase 1 leaves its columns alone
     if (it + 1 < nch) load_do(j - 1, dr);

@@ -341,15 +341,31 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
       if (r < clen) x[i] = __ldg(reinterpret_cast<const uint4 *>(dO + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
     }
   };
-  auto store_dv = [&](int j) {   // dV^T (TMEM) -> dv rows of chunk j (fp32)
+  // dV^T (TMEM) -> dv rows of chunk j (fp32). Each warp transposes its 32 value channels
+  // through its own 4 KB of the dO staging tile (free between the dO^T transpose and the
+  // next pass A), 32 tokens at a time, and writes 128-byte row pieces with 16-byte stores.
+  auto store_dv = [&](int j) {
     const long long t0 = s0 + (long long)j * CH;
     const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
     uint32_t r[64];
     tc::ld64(tl + 192, r);
     tc::wait_ld();
+    float *wst = reinterpret_cast<float *>(smem + S::DST + warp * 4096);   // [32 tok][32 channels]
+    const int lane = tid & 31;
 #pragma unroll
-    for (int i = 0; i < 64; ++i)
-      if (i < clen) p.dv[((size_t)(t0 + i) * H + h) * 128 + row] = __uint_as_float(r[i]);
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) wst[i * 32 + lane] = __uint_as_float(r[32 * half + i]);
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int tok = 4 * k + (lane >> 3), ch = lane & 7, gt = 32 * half + tok;
+        if (gt < clen)
+          *reinterpret_cast<float4 *>(p.dv + ((size_t)(t0 + gt) * H + h) * 128 + 32 * warp + 4 * ch) =
+              *reinterpret_cast<const float4 *>(wst + tok * 32 + 4 * ch);
+      }
+      __syncwarp();
+    }
   };
 
   // initial dS^T[dv][dk] = dhT[dk][dv]

@@ -1,6 +1,7 @@
 // kda_scan_tc.cu -- the forward inter-chunk state passing on 5th-generation tensor cores.
 //
-// One CTA (4 warps) per (sequence, head). The 128x128 fp32 state lives in tensor
+// One CTA per (sequence, head): 4 state warps run the chain below, 4 io warps load
+// and transpose the next chunk's values and write the outputs. The 128x128 fp32 state lives in tensor
 // memory for the whole sequence, transposed: TMEM lane m = value channel m,
 // column n = key channel n (S^T). Thread t of warp w owns lane 32w + t, so every
 // elementwise pass is a row pass. TMEM: two sets of 256 columns, [S^T | O^T | U^T]. Per 64-token chunk, with the record of the prep kernel
@@ -34,9 +35,9 @@ struct TcScanSmem {
   static constexpr int AS = 2 * RECS;        // S^T bf16 [128][K=128]: two 16 KB blocks (also the saved state)
   static constexpr int AU = AS + 32768;      // U^T bf16 [128][K=64]; raw value rows before pass B
   static constexpr int AV = AU + 16384;      // V^T bf16 [128][K=64]
-  static constexpr int OST = AV + 16384;     // output staging [64 tok][128] bf16; warp w owns columns 32w..32w+31
-  static constexpr int BAR = OST + 16384;    // record buffers 0/1, phase 1, phase 2
-  static constexpr int TSLOT = BAR + 32;
+  static constexpr int OST = AV + 16384;     // staging [64 tok][128] bf16: raw values in, outputs out (io warps)
+  static constexpr int BAR = OST + 16384;    // 6 mbarriers (see the kernel)
+  static constexpr int TSLOT = BAR + 64;
   static constexpr int BYTES = TSLOT + 32 + 1024;   // + alignment slack
 };
 
@@ -46,7 +47,7 @@ __device__ __forceinline__ void tc_issue_record(char *dst, const char *src, uint
   bulk_g2s(dst, src, TcRec::BYTES, bar);
 }
 
-__global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p) {
+__global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p) {
   using S = TcScanSmem;
   extern __shared__ __align__(1024) char smem_raw[];
   // operand tiles need 1024-byte alignment in the shared window
@@ -54,15 +55,21 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
   const int H = p.geo.heads, h = blockIdx.x % H, seq = blockIdx.x / H;
   const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
   const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
-  const int tid = threadIdx.x, warp = tid >> 5, row = tid;   // row = TMEM lane = value channel
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool io = warp >= 4;                  // warps 4..7: values in, outputs out
+  const int row = tid & 127, qw = warp & 3;   // row = TMEM lane = value channel
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + S::TSLOT);
   const bf16 *v = (const bf16 *)p.v;
   bf16 *o = (bf16 *)p.o;
   const size_t sh = (size_t)seq * H + h;
 
+  // bar[0..1]: record buffers; bar[2]: phase 1 done; bar[3]: phase 2 done (MMA commits);
+  // bar[4]: V^T of the next chunk staged (128 io arrivals); bar[5]: O^T of a chunk read out
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    mbar_init(&bar[4], 128);
+    mbar_init(&bar[5], 128);
     fence_mbar_init();
   }
   if (warp == 0) tc::alloc(tslot, 512);
@@ -70,200 +77,225 @@ __global__ void __launch_bounds__(128, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's lane quarter
+  const uint32_t tl = tmem + ((uint32_t)(32 * qw) << 16);   // this warp's lane quarter
   // Two TMEM sets of [S^T | O^T | U^T] (128 + 64 + 64 columns) at 0 and 256; chunk j
   // works in set j & 1: pass A reads its start state from the other set and writes the
   // decayed state here, phase 2 accumulates [S^T | O^T] here in one N = 192 product, and
   // O^T of chunk j survives while chunk j + 1 runs in the other set.
   auto set_of = [](int j) -> uint32_t { return 256u * (uint32_t)(j & 1); };
   auto colO = [&](int j) -> uint32_t { return set_of(j) + 128u; };
-
   auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * TcRec::BYTES; };
-  // values of chunk j: 16-byte coalesced loads (row r = idx / 16, chunk idx % 16) held in registers
-  auto load_v = [&](int j, uint4 (&vr)[8]) {
-    const long long t0 = s0 + (long long)j * CH;
-    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int idx = tid + 128 * i, r = idx >> 4, ch = idx & 15;
-      vr[i] = make_uint4(0, 0, 0, 0);
-      if (r < clen) vr[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
-    }
-  };
-  // O^T of chunk j (TMEM) -> o. Each warp transposes its 32 value channels through its
-  // own columns of the staging tile, then writes 64-byte row pieces with 16-byte stores.
-  auto store_o = [&](int j) {
-    const long long t0 = s0 + (long long)j * CH;
-    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-    uint32_t r[64];
-    tc::ld64(tl + colO(j), r);
-    tc::wait_ld();
-#pragma unroll
-    for (int i = 0; i < 64; ++i)
-      *reinterpret_cast<bf16 *>(smem + S::OST + i * 256 + row * 2) = __float2bfloat16_rn(__uint_as_float(r[i]));
-    __syncwarp();
-    const int lane = tid & 31;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int tok = 8 * k + (lane >> 2), ch = 4 * warp + (lane & 3);   // 16-byte chunk ch of row tok
-      if (tok < clen)
-        *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + tok) * H + h) * 128 + ch * 8) =
-            *reinterpret_cast<const uint4 *>(smem + S::OST + tok * 256 + ch * 16);
-    }
-    __syncwarp();
-  };
 
-  // initial state S^T[dv][dk] = h0[dk][dv], in the set chunk 0 reads from
-  {
-    float buf[16];
-#pragma unroll
-    for (int cb = 0; cb < 8; ++cb) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        buf[i] = p.h0 ? p.h0[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f;
-      tc::st16(tl + set_of(1) + 16 * cb, buf);
-    }
-    tc::wait_st();
-  }
-  // shared-memory descriptors: the start-address field takes byte offsets >> 4 directly
-  const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS)), d_au = tc::desc_sw128(smem_u32(smem + S::AU)),
-                 d_av = tc::desc_sw128(smem_u32(smem + S::AV));
-  const uint64_t d_rec0 = tc::desc_sw128(smem_u32(smem + S::REC0)), d_rec1 = tc::desc_sw128(smem_u32(smem + S::REC1));
-  if (tid == 0 && nch > 0) {
-    tc_issue_record(smem + S::REC0, rec_of(0), &bar[0]);
-    if (nch > 1) tc_issue_record(smem + S::REC1, rec_of(1), &bar[1]);
-  }
-  uint4 vr[8];
-  if (nch > 0) load_v(0, vr);
   bool ok = true;
-  int done = 0;   // chunks whose phase 2 was issued
-  for (int j = 0; j < nch; ++j) {
-    const int b = j & 1;
-    char *rb = smem + (b ? S::REC1 : S::REC0);
-    ok &= mbar_wait(&bar[b], (j >> 1) & 1);
-    if (j > 0) ok &= mbar_wait(&bar[3], (j - 1) & 1);
-    if (tid == 32 && p.saved) bulk_wait_read();   // the previous saved-state copy has read the S^T tile
-    tc::fence_after();
-    if (!__syncthreads_and(ok)) break;
-    // the other record buffer's last reader (phase 2 of the previous chunk) has finished:
-    // fetch the next chunk's record now, a whole chunk step ahead
-    if (tid == 32 && j >= 1 && j + 1 < nch)
-      tc_issue_record(smem + ((j + 1) & 1 ? S::REC1 : S::REC0), rec_of(j + 1), &bar[(j + 1) & 1]);
-    // pass A: this chunk's values -> plain [tok][128] rows in the U tile (free until pass B);
-    // state -> operand tile, scaled state back to TMEM
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int idx = tid + 128 * i;
-      *reinterpret_cast<uint4 *>(smem + S::AU + (idx >> 4) * 256 + (idx & 15) * 16) = vr[i];
-    }
+  if (!io) {
+    // ------------------------------------------------------------ state warps
+    // initial state S^T[dv][dk] = h0[dk][dv], in the set chunk 0 reads from
     {
-      const float *gC = reinterpret_cast<const float *>(rb + TcRec::GC);
+      float buf[16];
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {   // 64 key channels at a time, one TMEM round trip each
-        uint32_t r[64];
-        tc::ld64(tl + set_of(j + 1) + 64 * hb, r);
-        tc::wait_ld();
+      for (int cb = 0; cb < 8; ++cb) {
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          float buf[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) buf[i] = __uint_as_float(r[16 * cb + i]);
-          const int k0 = 64 * hb + 16 * cb;
-          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0)) = tc::pack8(buf);
-          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = tc::pack8(buf + 8);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) buf[i] *= gC[k0 + i];
-          tc::st16(tl + set_of(j) + k0, buf);
-        }
+        for (int i = 0; i < 16; ++i)
+          buf[i] = p.h0 ? p.h0[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f;
+        tc::st16(tl + set_of(1) + 16 * cb, buf);
       }
       tc::wait_st();
     }
-    __syncthreads();
-    // V^T operand: row = value channel, 64 tokens
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t lo = *reinterpret_cast<const unsigned short *>(smem + S::AU + (8 * c + 2 * e) * 256 + row * 2);
-        const uint32_t hi = *reinterpret_cast<const unsigned short *>(smem + S::AU + (8 * c + 2 * e + 1) * 256 + row * 2);
-        w[e] = lo | (hi << 16);
-      }
-      *reinterpret_cast<uint4 *>(smem + S::AV + tc::sw128_off(128, row, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+    // shared-memory descriptors: the start-address field takes byte offsets >> 4 directly
+    const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS)), d_au = tc::desc_sw128(smem_u32(smem + S::AU)),
+                   d_av = tc::desc_sw128(smem_u32(smem + S::AV));
+    const uint64_t d_rec0 = tc::desc_sw128(smem_u32(smem + S::REC0)), d_rec1 = tc::desc_sw128(smem_u32(smem + S::REC1));
+    if (tid == 0 && nch > 0) {
+      tc_issue_record(smem + S::REC0, rec_of(0), &bar[0]);
+      if (nch > 1) tc_issue_record(smem + S::REC1, rec_of(1), &bar[1]);
     }
-    fence_proxy_async();
-    tc::fence_before();
-    __syncthreads();
-    if (tid == 0) {
+    int done = 0;   // chunks whose phase 2 was issued
+    for (int j = 0; j < nch; ++j) {
+      const int b = j & 1;
+      char *rb = smem + (b ? S::REC1 : S::REC0);
+      ok &= mbar_wait(&bar[b], (j >> 1) & 1);
+      if (j > 0) ok &= mbar_wait(&bar[3], (j - 1) & 1);
+      if (tid == 32 && p.saved) bulk_wait_read();   // the previous saved-state copy has read the S^T tile
       tc::fence_after();
-      const uint64_t d_rb = b ? d_rec1 : d_rec0, d_b1 = d_rb + (TcRec::B1 >> 4), d_tb = d_rb + (TcRec::TB >> 4);
-      const uint32_t dO = tmem + colO(j);
+      if (!named_sync_and(1, 128, ok)) break;
+      // the other record buffer's last reader (phase 2 of the previous chunk) has finished:
+      // fetch the next chunk's record now, a whole chunk step ahead
+      if (tid == 32 && j >= 1 && j + 1 < nch)
+        tc_issue_record(smem + ((j + 1) & 1 ? S::REC1 : S::REC0), rec_of(j + 1), &bar[(j + 1) & 1]);
+      // pass A: state -> operand tile, decayed state into this chunk's set
+      {
+        const float *gC = reinterpret_cast<const float *>(rb + TcRec::GC);
 #pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
+        for (int hb = 0; hb < 2; ++hb) {   // 64 key channels at a time, one TMEM round trip each
+          uint32_t r[64];
+          tc::ld64(tl + set_of(j + 1) + 64 * hb, r);
+          tc::wait_ld();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t off = (kb * 16384 + 32 * ks) >> 4;
-          tc::mma_bf16(dO, d_as + off, d_b1 + off, tc::idesc_bf16(128, 128), (kb | ks) != 0);
+          for (int cb = 0; cb < 4; ++cb) {
+            float buf[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) buf[i] = __uint_as_float(r[16 * cb + i]);
+            const int k0 = 64 * hb + 16 * cb;
+            *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0)) = tc::pack8(buf);
+            *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = tc::pack8(buf + 8);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) buf[i] *= gC[k0 + i];
+            tc::st16(tl + set_of(j) + k0, buf);
+          }
         }
+        tc::wait_st();
+      }
+      fence_proxy_async();
+      tc::fence_before();
+      named_sync(1, 128);
+      if (tid == 0) {
+        bool ready = mbar_wait(&bar[4], j & 1);                // V^T of chunk j staged
+        if (j >= 2) ready &= mbar_wait(&bar[5], j & 1);        // O^T of chunk j - 2 (same set) read out
+        tc::fence_after();
+        ok &= ready;
+        if (ready) {
+          const uint64_t d_rb = b ? d_rec1 : d_rec0, d_b1 = d_rb + (TcRec::B1 >> 4), d_tb = d_rb + (TcRec::TB >> 4);
+          const uint32_t dO = tmem + colO(j);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) tc::mma_bf16(dO + 64, d_av + 2 * ks, d_tb + 2 * ks, tc::idesc_bf16(128, 64), 1);
-      tc::commit(&bar[2]);
-    } else if (tid == 32) {
-      // the chunk-start state leaves as one bulk copy of the operand tile
-      if (p.saved) {
+          for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t off = (kb * 16384 + 32 * ks) >> 4;
+              tc::mma_bf16(dO, d_as + off, d_b1 + off, tc::idesc_bf16(128, 128), (kb | ks) != 0);
+            }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) tc::mma_bf16(dO + 64, d_av + 2 * ks, d_tb + 2 * ks, tc::idesc_bf16(128, 64), 1);
+          tc::commit(&bar[2]);
+        }
+      } else if (tid == 32 && p.saved) {
+        // the chunk-start state leaves as one bulk copy of the operand tile
         bulk_s2g((bf16 *)p.saved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
         bulk_commit();
       }
-    }
-    if (j > 0) store_o(j - 1);
-    if (j + 1 < nch) load_v(j + 1, vr);
-    ok &= mbar_wait(&bar[2], j & 1);
-    tc::fence_after();
-    // pass B: U^T -> operand tile
-    {
-      uint32_t r[64];
-      tc::ld64(tl + colO(j) + 64, r);
-      tc::wait_ld();
-#pragma unroll
-      for (int cb = 0; cb < 8; ++cb) {
-        float buf[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) buf[i] = __uint_as_float(r[8 * cb + i]);
-        *reinterpret_cast<uint4 *>(smem + S::AU + tc::sw128_off(128, row, 8 * cb)) = tc::pack8(buf);
-      }
-    }
-    fence_proxy_async();
-    tc::fence_before();
-    if (!__syncthreads_and(ok)) break;
-    if (tid == 0) {
+      ok &= mbar_wait(&bar[2], j & 1);
       tc::fence_after();
-      // [S^T | O^T] += U^T [Kh^T; Bm]^T in this chunk's set
-      const uint64_t d_b2 = (b ? d_rec1 : d_rec0) + (TcRec::B2 >> 4);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc::mma_bf16(tmem + set_of(j), d_au + 2 * ks, d_b2 + 2 * ks, tc::idesc_bf16(128, 192), 1);
-      tc::commit(&bar[3]);
-    }
-    done = j + 1;
-  }
-  if (ok && done > 0) ok = mbar_wait(&bar[3], (done - 1) & 1);
-  tc::fence_after();
-  if (__syncthreads_and(ok)) {
-    if (done > 0) store_o(done - 1);
-    if (p.hT) {   // hT[dk][dv] = S^T[dv][dk], in the set of the last chunk
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
+      // pass B: U^T -> operand tile
+      {
         uint32_t r[64];
-        tc::ld64(tl + set_of(done + 1) + 64 * hb, r);
+        tc::ld64(tl + colO(j) + 64, r);
         tc::wait_ld();
 #pragma unroll
-        for (int i = 0; i < 64; ++i) p.hT[(sh * 128 + 64 * hb + i) * 128 + row] = __uint_as_float(r[i]);
+        for (int cb = 0; cb < 8; ++cb) {
+          float buf[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) buf[i] = __uint_as_float(r[8 * cb + i]);
+          *reinterpret_cast<uint4 *>(smem + S::AU + tc::sw128_off(128, row, 8 * cb)) = tc::pack8(buf);
+        }
       }
+      fence_proxy_async();
+      tc::fence_before();
+      if (!named_sync_and(1, 128, ok)) break;
+      if (tid == 0) {
+        tc::fence_after();
+        // [S^T | O^T] += U^T [Kh^T; Bm]^T in this chunk's set
+        const uint64_t d_b2 = (b ? d_rec1 : d_rec0) + (TcRec::B2 >> 4);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_bf16(tmem + set_of(j), d_au + 2 * ks, d_b2 + 2 * ks, tc::idesc_bf16(128, 192), 1);
+        tc::commit(&bar[3]);
+      }
+      done = j + 1;
     }
+    if (ok && done > 0) ok = mbar_wait(&bar[3], (done - 1) & 1);
+    tc::fence_after();
+    if (named_sync_and(1, 128, ok)) {
+      if (p.hT) {   // hT[dk][dv] = S^T[dv][dk], in the set of the last chunk
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t r[64];
+          tc::ld64(tl + set_of(done + 1) + 64 * hb, r);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 64; ++i) p.hT[(sh * 128 + 64 * hb + i) * 128 + row] = __uint_as_float(r[i]);
+        }
+      }
+    } else {
+      report(p.status, ERR_TIMEOUT);
+    }
+    if (tid == 32 && p.saved) bulk_wait_all();   // saved states complete before the CTA leaves
   } else {
-    report(p.status, ERR_TIMEOUT);
+    // ------------------------------------------------------------ io warps
+    // values of chunk j: 16-byte coalesced loads (row r = idx / 16, chunk idx % 16) held in registers
+    auto load_v = [&](int j, uint4 (&vr)[8]) {
+      const long long t0 = s0 + (long long)j * CH;
+      const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int idx = row + 128 * i, r = idx >> 4, ch = idx & 15;
+        vr[i] = make_uint4(0, 0, 0, 0);
+        if (r < clen) vr[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
+      }
+    };
+    // raw rows -> staging tile -> V^T operand (row = value channel, 64 tokens); then signal
+    auto stage_v = [&](const uint4 (&vr)[8]) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int idx = row + 128 * i;
+        *reinterpret_cast<uint4 *>(smem + S::OST + (idx >> 4) * 256 + (idx & 15) * 16) = vr[i];
+      }
+      named_sync(2, 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t lo = *reinterpret_cast<const unsigned short *>(smem + S::OST + (8 * c + 2 * e) * 256 + row * 2);
+          const uint32_t hi = *reinterpret_cast<const unsigned short *>(smem + S::OST + (8 * c + 2 * e + 1) * 256 + row * 2);
+          w[e] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4 *>(smem + S::AV + tc::sw128_off(128, row, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async();
+      named_sync(2, 128);   // the staging tile is free again
+      mbar_arrive(&bar[4]);
+    };
+    // O^T of chunk j (TMEM) -> o. Each warp transposes its 32 value channels through its
+    // own columns of the staging tile, then writes 64-byte row pieces with 16-byte stores.
+    auto store_o = [&](int j) {
+      const long long t0 = s0 + (long long)j * CH;
+      const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+      uint32_t r[64];
+      tc::ld64(tl + colO(j), r);
+      tc::wait_ld();
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        *reinterpret_cast<bf16 *>(smem + S::OST + i * 256 + row * 2) = __float2bfloat16_rn(__uint_as_float(r[i]));
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int tok = 8 * k + (lane >> 2), ch = 4 * qw + (lane & 3);   // 16-byte chunk ch of row tok
+        if (tok < clen)
+          *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + tok) * H + h) * 128 + ch * 8) =
+              *reinterpret_cast<const uint4 *>(smem + S::OST + tok * 256 + ch * 16);
+      }
+      __syncwarp();
+    };
+    uint4 vr[8];
+    if (nch > 0) {
+      load_v(0, vr);
+      stage_v(vr);
+    }
+    for (int j = 0; j < nch; ++j) {
+      if (j + 1 < nch) {
+        load_v(j + 1, vr);
+        ok &= mbar_wait(&bar[2], j & 1);   // phase 1 of chunk j has read the V^T tile
+        if (!named_sync_and(2, 128, ok)) break;
+        stage_v(vr);
+      }
+      ok &= mbar_wait(&bar[3], j & 1);     // phase 2 of chunk j has completed O^T
+      tc::fence_after();
+      if (!named_sync_and(2, 128, ok)) break;
+      store_o(j);
+      named_sync(2, 128);                  // every warp is done with the staging tile
+      tc::fence_before();
+      mbar_arrive(&bar[5]);
+    }
   }
-  if (tid == 32 && p.saved) bulk_wait_all();   // saved states complete before the CTA leaves
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, 512);
@@ -275,7 +307,7 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kda_fwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        TcScanSmem::BYTES);
   if (e != cudaSuccess) return e;
-  kda_fwd_scan_tc_kernel<<<(unsigned)units, 128, TcScanSmem::BYTES, s>>>(p);
+  kda_fwd_scan_tc_kernel<<<(unsigned)units, 256, TcScanSmem::BYTES, s>>>(p);
   return cudaGetLastError();
 }
 

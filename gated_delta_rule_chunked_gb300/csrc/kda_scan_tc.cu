@@ -149,8 +149,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
       tc::fence_before();
       named_sync(1, 128);
       if (tid == 0) {
-        bool ready = mbar_wait(&bar[4], j & 1);                // V^T of chunk j staged
-        if (j >= 2) ready &= mbar_wait(&bar[5], j & 1);        // O^T of chunk j - 2 (same set) read out
+        const bool ready = mbar_wait(&bar[4], j & 1);          // V^T of chunk j staged
         tc::fence_after();
         ok &= ready;
         if (ready) {
@@ -191,13 +190,21 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
       tc::fence_before();
       if (!named_sync_and(1, 128, ok)) break;
       if (tid == 0) {
+        // O^T of the previous chunk has been read out by the io warps. This keeps the io
+        // warps at most one phase behind on every barrier they wait on (a parity wait
+        // cannot tell two completed phases apart), and frees that set's O^T before the
+        // next chunk's phase 1 overwrites it.
+        const bool freed = j == 0 || mbar_wait(&bar[5], (j - 1) & 1);
         tc::fence_after();
-        // [S^T | O^T] += U^T [Kh^T; Bm]^T in this chunk's set
-        const uint64_t d_b2 = (b ? d_rec1 : d_rec0) + (TcRec::B2 >> 4);
+        ok &= freed;
+        if (freed) {
+          // [S^T | O^T] += U^T [Kh^T; Bm]^T in this chunk's set
+          const uint64_t d_b2 = (b ? d_rec1 : d_rec0) + (TcRec::B2 >> 4);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + set_of(j), d_au + 2 * ks, d_b2 + 2 * ks, tc::idesc_bf16(128, 192), 1);
-        tc::commit(&bar[3]);
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16(tmem + set_of(j), d_au + 2 * ks, d_b2 + 2 * ks, tc::idesc_bf16(128, 192), 1);
+          tc::commit(&bar[3]);
+        }
       }
       done = j + 1;
     }
@@ -280,12 +287,13 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
       load_v(0, vr);
       stage_v(vr);
     }
+    if (nch > 1) load_v(1, vr);
     for (int j = 0; j < nch; ++j) {
       if (j + 1 < nch) {
-        load_v(j + 1, vr);
         ok &= mbar_wait(&bar[2], j & 1);   // phase 1 of chunk j has read the V^T tile
         if (!named_sync_and(2, 128, ok)) break;
-        stage_v(vr);
+        stage_v(vr);                       // chunk j + 1, loaded a whole step earlier
+        if (j + 2 < nch) load_v(j + 2, vr);
       }
       ok &= mbar_wait(&bar[3], j & 1);     // phase 2 of chunk j has completed O^T
       tc::fence_after();

@@ -141,7 +141,8 @@ def run_ours(args, rank, world, local_rank):
     fa = kda.fwd_args(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, o, hT, None, None)
     saved = torch.empty(lib.kda_saved_size(C.byref(fa)), dtype=torch.uint8, device=dev)
     fws = torch.empty(lib.kda_fwd_workspace_size(C.byref(fa)), dtype=torch.uint8, device=dev)
-    fa = kda.fwd_args(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, o, hT, saved, fws)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)   # a kernel that gives up a bounded wait writes here
+    fa = kda.fwd_args(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, o, hT, saved, fws, dev_status=status)
     grads = {n: torch.empty(s, **f32) for n, s in
              (("dq", b.q.shape), ("dk", b.k.shape), ("dv", b.v.shape), ("dg", b.g.shape), ("dbeta", b.beta.shape),
               ("dh0", (N, H, D, D)))}
@@ -186,6 +187,8 @@ def run_ours(args, rank, world, local_rank):
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     ms_step_local = t_start.elapsed_time(t_end) / K
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())}: a kernel gave up a bounded wait; no number reported")
     barrier(world)
     ck = clocks.stop() if clocks else None
     ms_step = reduce_max(ms_step_local, world)

@@ -92,11 +92,13 @@ def _i32(cu_seqlens, device):
 
 
 def kda_fwd(q, k, v, beta, g, cu_seqlens=None, h0=None, *, scale: float = 1.0, save: bool = False,
-            final_state: bool = True, n_seqs: Optional[int] = None):
+            final_state: bool = True, n_seqs: Optional[int] = None, dev_status=None):
     """Chunked KDA forward. Returns (o, hT or None, saved or None).
 
     ``saved`` (chunk-start states) is what kda_bwd needs; request it with save=True.
     Without cu_seqlens the tokens form ``n_seqs`` (default 1) equal sequences.
+    ``dev_status`` (optional int32 device tensor, zeroed by the caller) receives
+    KDA_ERR_TIMEOUT if a kernel gives up a bounded wait.
     """
     lib = library()
     _check_inputs(q, k, v, beta, g)
@@ -106,7 +108,7 @@ def kda_fwd(q, k, v, beta, g, cu_seqlens=None, h0=None, *, scale: float = 1.0, s
     H = q.shape[1]
     o = torch.empty_like(v)
     hT = torch.empty((N, H, 128, 128), dtype=torch.float32, device=dev) if final_state else None
-    a = fwd_args(q, k, v, beta, g, cu, h0, o, hT, None, None, scale, n_seqs=N)
+    a = fwd_args(q, k, v, beta, g, cu, h0, o, hT, None, None, scale, n_seqs=N, dev_status=dev_status)
     saved = None
     if save:
         saved = torch.empty(lib.kda_saved_size(C.byref(a)), dtype=torch.uint8, device=dev)
@@ -121,7 +123,7 @@ def kda_fwd(q, k, v, beta, g, cu_seqlens=None, h0=None, *, scale: float = 1.0, s
 
 
 def kda_bwd(q, k, v, beta, g, dO, saved, cu_seqlens=None, h0=None, dhT=None, *, scale: float = 1.0,
-            n_seqs: Optional[int] = None, initial_state_grad: bool = True):
+            n_seqs: Optional[int] = None, initial_state_grad: bool = True, dev_status=None):
     """Backward of kda_fwd (``saved`` from kda_fwd(..., save=True) with the same inputs).
 
     Returns a dict of fp32 gradients: dq, dk, dv, dbeta, dg and dh0 (or None).
@@ -136,7 +138,7 @@ def kda_bwd(q, k, v, beta, g, dO, saved, cu_seqlens=None, h0=None, dhT=None, *, 
     dq, dk, dv = torch.empty(q.shape, **f32), torch.empty(k.shape, **f32), torch.empty(v.shape, **f32)
     dg, dbeta = torch.empty(g.shape, **f32), torch.empty(beta.shape, **f32)
     dh0 = torch.empty((N, H, 128, 128), **f32) if initial_state_grad else None
-    fa = fwd_args(q, k, v, beta, g, cu, h0, None, None, saved, None, scale, n_seqs=N)
+    fa = fwd_args(q, k, v, beta, g, cu, h0, None, None, saved, None, scale, n_seqs=N, dev_status=dev_status)
     b = bwd_args(fa, dO, dq, dk, dv, dbeta, dg, dh0, dhT)
     ws_bytes = lib.kda_bwd_workspace_size(C.byref(b))
     if ws_bytes == 0:

@@ -40,11 +40,22 @@ def to_dev(b, dev="cuda"):
     return out
 
 
+def new_status():
+    """A zeroed device status word; kernels write KDA_ERR_TIMEOUT there if a bounded wait gives up."""
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def assert_no_timeout(st):
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())} (a bounded wait gave up)"
+
+
 def run_fwd(kda, b, save=False, scale=1.0):
     t = to_dev(b)
+    st = new_status()
     o, hT, saved = kda.kda_fwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["cu_seqlens"], t["h0"],
-                               save=save, scale=scale)
-    torch.cuda.synchronize()
+                               save=save, scale=scale, dev_status=st)
+    assert_no_timeout(st)
     return t, o, hT, saved
 
 
@@ -123,9 +134,10 @@ def check_bwd(kda, b, tol, tasks=None):
     t, o, hT, saved = run_fwd(kda, b, save=True)
     gen = torch.Generator().manual_seed(99)
     dhT = (torch.randn(b.n_seqs, b.heads, 128, 128, generator=gen) * 0.1)
+    st = new_status()
     gr = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, t["cu_seqlens"], t["h0"],
-                     dhT.to("cuda"))
-    torch.cuda.synchronize()
+                     dhT.to("cuda"), dev_status=st)
+    assert_no_timeout(st)
     res = oracle.bwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.dO, b.h0, dhT, tasks=tasks)
     errs = {}
     cu = [int(x) for x in b.cu_seqlens.tolist()]
@@ -228,9 +240,10 @@ def test_fullsize_fwd_bwd_sampled(kda, name, tasks):
     dev = torch.device("cuda")
     b = make_workload(name, device=dev)
     heads = sorted({h for _, h in tasks})
-    o, hT, saved = kda.kda_fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, save=True)
-    gr = kda.kda_bwd(b.q, b.k, b.v, b.beta, b.g, b.dO, saved, b.cu_seqlens, b.h0)
-    torch.cuda.synchronize()
+    st = new_status()
+    o, hT, saved = kda.kda_fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, save=True, dev_status=st)
+    gr = kda.kda_bwd(b.q, b.k, b.v, b.beta, b.g, b.dO, saved, b.cu_seqlens, b.h0, dev_status=st)
+    assert_no_timeout(st)
     s = _sampled(b, heads)
     cu = [int(x) for x in b.cu_seqlens.tolist()]
     otasks = [(i, heads.index(h)) for i, h in tasks]

@@ -320,7 +320,8 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
 }
 
 // ----------------------------------------------------------------- backward
-// Reverse dS scan, same arrangement: dS^T in TMEM columns [0,128), dU^T in
+// Reverse dS scan, same arrangement (4 state warps, 4 io warps staging dO^T and
+// writing dv): dS^T in TMEM columns [0,128), dU^T in
 // [128,192), dV^T in [192,256). Per chunk (last to first), with the backward
 // record (Bm^T, Kh, [Qt^T | -W^T], Tb^T, gC):
 //   pass A : dS^T -> bf16 operand tile (saved as the chunk-end dS by one bulk copy);
@@ -335,27 +336,33 @@ struct TcBwdSmem {
   static constexpr int REC0 = 0, REC1 = RECS;
   static constexpr int AS = 2 * RECS;        // dS^T bf16 [128][K=128]
   static constexpr int A2 = AS + 32768;      // [dO^T | dU^T] bf16 [128][K=128]
-  static constexpr int DST = A2 + 32768;     // dO staging [64 tok][128] bf16, plain rows
+  static constexpr int DST = A2 + 32768;     // staging: raw dO rows in, dv rows out (io warps)
   static constexpr int BAR = DST + 16384;
-  static constexpr int TSLOT = BAR + 32;
+  static constexpr int TSLOT = BAR + 64;   // 6 mbarriers (see the kernel)
   static constexpr int BYTES = TSLOT + 32 + 1024;
 };
 
-__global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p) {
+__global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p) {
   using S = TcBwdSmem;
   extern __shared__ __align__(1024) char smem_raw[];
   char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int H = p.geo.heads, h = blockIdx.x % H, seq = blockIdx.x / H;
   const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
   const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
-  const int tid = threadIdx.x, warp = tid >> 5, row = tid;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool io = warp >= 4;                  // warps 4..7: dO in, dv out
+  const int row = tid & 127, qw = warp & 3;   // row = TMEM lane = value channel
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + S::TSLOT);
   const bf16 *dO = (const bf16 *)p.dO;
   const size_t sh = (size_t)seq * H + h;
 
+  // bar[0..1]: record buffers; bar[2]: phase 1 done; bar[3]: phase 2 done (MMA commits);
+  // bar[4]: dO^T of the next chunk staged (128 io arrivals); bar[5]: dV^T of a chunk read out
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    mbar_init(&bar[4], 128);
+    mbar_init(&bar[5], 128);
     fence_mbar_init();
   }
   if (warp == 0) tc::alloc(tslot, 256);
@@ -363,199 +370,232 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
-
+  const uint32_t tl = tmem + ((uint32_t)(32 * qw) << 16);
   auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * TcRecB::BYTES; };
-  auto issue = [&](char *dst, const char *src, uint64_t *b) {
-    fence_proxy_async();
-    mbar_expect_tx(b, TcRecB::BYTES);
-    bulk_g2s(dst, src, TcRecB::BYTES, b);
-  };
-  auto load_do = [&](int j, uint4 (&x)[8]) {
-    const long long t0 = s0 + (long long)j * CH;
-    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int idx = tid + 128 * i, r = idx >> 4, ch = idx & 15;
-      x[i] = make_uint4(0, 0, 0, 0);
-      if (r < clen) x[i] = __ldg(reinterpret_cast<const uint4 *>(dO + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
-    }
-  };
-  // dV^T (TMEM) -> dv rows of chunk j (fp32). Each warp transposes its 32 value channels
-  // through its own 4 KB of the dO staging tile (free between the dO^T transpose and the
-  // next pass A), 32 tokens at a time, and writes 128-byte row pieces with 16-byte stores.
-  auto store_dv = [&](int j) {
-    const long long t0 = s0 + (long long)j * CH;
-    const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-    uint32_t r[64];
-    tc::ld64(tl + 192, r);
-    tc::wait_ld();
-    float *wst = reinterpret_cast<float *>(smem + S::DST + warp * 4096);   // [32 tok][32 channels]
-    const int lane = tid & 31;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) wst[i * 32 + lane] = __uint_as_float(r[32 * half + i]);
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int tok = 4 * k + (lane >> 3), ch = lane & 7, gt = 32 * half + tok;
-        if (gt < clen)
-          *reinterpret_cast<float4 *>(p.dv + ((size_t)(t0 + gt) * H + h) * 128 + 32 * warp + 4 * ch) =
-              *reinterpret_cast<const float4 *>(wst + tok * 32 + 4 * ch);
-      }
-      __syncwarp();
-    }
-  };
 
-  // initial dS^T[dv][dk] = dhT[dk][dv]
-  {
-    float buf[16];
-#pragma unroll
-    for (int cb = 0; cb < 8; ++cb) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) buf[i] = p.dhT ? p.dhT[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f;
-      tc::st16(tl + 16 * cb, buf);
-    }
-    tc::wait_st();
-  }
-  const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS)), d_a2 = tc::desc_sw128(smem_u32(smem + S::A2));
-  const uint64_t d_rec0 = tc::desc_sw128(smem_u32(smem + S::REC0)), d_rec1 = tc::desc_sw128(smem_u32(smem + S::REC1));
-  if (tid == 0 && nch > 0) {
-    issue(smem + S::REC0, rec_of(nch - 1), &bar[0]);
-    if (nch > 1) issue(smem + S::REC1, rec_of(nch - 2), &bar[1]);
-  }
-  uint4 dr[8];
-  if (nch > 0) load_do(nch - 1, dr);
   bool ok = true;
-  int done = 0, last_j = -1;
-  for (int it = 0; it < nch; ++it) {
-    const int j = nch - 1 - it, b = it & 1;
-    char *rb = smem + (b ? S::REC1 : S::REC0);
-    ok &= mbar_wait(&bar[b], (it >> 1) & 1);
-    if (it > 0) ok &= mbar_wait(&bar[3], (it - 1) & 1);
-    if (tid == 32) bulk_wait_read();   // the previous saved dS copy has read the dS^T tile
-    tc::fence_after();
-    if (!__syncthreads_and(ok)) break;
-    if (tid == 32 && it >= 1 && it + 1 < nch)   // next record, a whole chunk step ahead
-      issue(smem + ((it + 1) & 1 ? S::REC1 : S::REC0), rec_of(j - 1), &bar[(it + 1) & 1]);
-    // pass A
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int idx = tid + 128 * i;
-      *reinterpret_cast<uint4 *>(smem + S::DST + (idx >> 4) * 256 + (idx & 15) * 16) = dr[i];
-    }
+  if (!io) {
+    // ------------------------------------------------------------ state warps
+    auto issue = [&](char *dst, const char *src, uint64_t *b) {
+      fence_proxy_async();
+      mbar_expect_tx(b, TcRecB::BYTES);
+      bulk_g2s(dst, src, TcRecB::BYTES, b);
+    };
+    // initial dS^T[dv][dk] = dhT[dk][dv]
     {
-      const float *gC = reinterpret_cast<const float *>(rb + TcRecB::GC);
+      float buf[16];
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        uint32_t r[64];
-        tc::ld64(tl + 64 * hb, r);
-        tc::wait_ld();
+      for (int cb = 0; cb < 8; ++cb) {
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          float buf[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) buf[i] = __uint_as_float(r[16 * cb + i]);
-          const int k0 = 64 * hb + 16 * cb;
-          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0)) = tc::pack8(buf);
-          *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = tc::pack8(buf + 8);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) buf[i] *= gC[k0 + i];
-          tc::st16(tl + k0, buf);
-        }
+        for (int i = 0; i < 16; ++i) buf[i] = p.dhT ? p.dhT[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f;
+        tc::st16(tl + 16 * cb, buf);
       }
       tc::wait_st();
     }
-    __syncthreads();
-    // dO^T operand (K-block 0 of A2): row = value channel, 64 tokens
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t lo = *reinterpret_cast<const unsigned short *>(smem + S::DST + (8 * c + 2 * e) * 256 + row * 2);
-        const uint32_t hi = *reinterpret_cast<const unsigned short *>(smem + S::DST + (8 * c + 2 * e + 1) * 256 + row * 2);
-        w[e] = lo | (hi << 16);
-      }
-      *reinterpret_cast<uint4 *>(smem + S::A2 + tc::sw128_off(128, row, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+    const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS)), d_a2 = tc::desc_sw128(smem_u32(smem + S::A2));
+    const uint64_t d_rec0 = tc::desc_sw128(smem_u32(smem + S::REC0)), d_rec1 = tc::desc_sw128(smem_u32(smem + S::REC1));
+    if (tid == 0 && nch > 0) {
+      issue(smem + S::REC0, rec_of(nch - 1), &bar[0]);
+      if (nch > 1) issue(smem + S::REC1, rec_of(nch - 2), &bar[1]);
     }
-    fence_proxy_async();
-    tc::fence_before();
-    __syncthreads();
-    if (tid == 0) {
+    int done = 0;
+    for (int it = 0; it < nch; ++it) {
+      const int j = nch - 1 - it, b = it & 1;
+      char *rb = smem + (b ? S::REC1 : S::REC0);
+      ok &= mbar_wait(&bar[b], (it >> 1) & 1);
+      if (it > 0) ok &= mbar_wait(&bar[3], (it - 1) & 1);
+      if (tid == 32) bulk_wait_read();   // the previous saved dS copy has read the dS^T tile
       tc::fence_after();
-      const uint64_t d_rb = b ? d_rec1 : d_rec0, d_bmt = d_rb + (TcRecB::BMT >> 4), d_kh = d_rb + (TcRecB::KH >> 4);
+      if (!named_sync_and(1, 128, ok)) break;
+      if (tid == 32 && it >= 1 && it + 1 < nch)   // next record, a whole chunk step ahead
+        issue(smem + ((it + 1) & 1 ? S::REC1 : S::REC0), rec_of(j - 1), &bar[(it + 1) & 1]);
+      // pass A: dS^T -> operand tile, decayed dS^T back to TMEM
+      {
+        const float *gC = reinterpret_cast<const float *>(rb + TcRecB::GC);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) tc::mma_bf16(tmem + 128, d_a2 + 2 * ks, d_bmt + 2 * ks, tc::idesc_bf16(128, 64), ks > 0);
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t r[64];
+          tc::ld64(tl + 64 * hb, r);
+          tc::wait_ld();
 #pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
+          for (int cb = 0; cb < 4; ++cb) {
+            float buf[16];
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_bf16(tmem + 128, d_as + ((kb * 16384 + 32 * ks) >> 4), d_kh + ((kb * 8192 + 32 * ks) >> 4),
-                       tc::idesc_bf16(128, 64), 1);
-      tc::commit(&bar[2]);
-    } else if (tid == 32) {
-      // the chunk-end dS leaves as one bulk copy of the operand tile
-      bulk_s2g((bf16 *)p.dsaved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
-      bulk_commit();
-    }
-    if (it > 0) store_dv(j + 1);   // dV^T of the previous chunk; phase 1 leaves its columns alone
-    if (it + 1 < nch) load_do(j - 1, dr);
-    ok &= mbar_wait(&bar[2], it & 1);
-    tc::fence_after();
-    // pass B: dU^T -> K-block 1 of A2
-    {
-      uint32_t r[64];
-      tc::ld64(tl + 128, r);
-      tc::wait_ld();
+            for (int i = 0; i < 16; ++i) buf[i] = __uint_as_float(r[16 * cb + i]);
+            const int k0 = 64 * hb + 16 * cb;
+            *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0)) = tc::pack8(buf);
+            *reinterpret_cast<uint4 *>(smem + S::AS + tc::sw128_off(128, row, k0 + 8)) = tc::pack8(buf + 8);
 #pragma unroll
-      for (int cb = 0; cb < 8; ++cb) {
-        float buf[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) buf[i] = __uint_as_float(r[8 * cb + i]);
-        *reinterpret_cast<uint4 *>(smem + S::A2 + tc::sw128_off(128, row, 64 + 8 * cb)) = tc::pack8(buf);
-      }
-    }
-    fence_proxy_async();
-    tc::fence_before();
-    if (!__syncthreads_and(ok)) break;
-    if (tid == 0) {
-      tc::fence_after();
-      const uint64_t d_rb = b ? d_rec1 : d_rec0, d_qwt = d_rb + (TcRecB::QWT >> 4), d_tbt = d_rb + (TcRecB::TBT >> 4);
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t off = (kb * 16384 + 32 * ks) >> 4;
-          tc::mma_bf16(tmem, d_a2 + off, d_qwt + off, tc::idesc_bf16(128, 128), 1);
+            for (int i = 0; i < 16; ++i) buf[i] *= gC[k0 + i];
+            tc::st16(tl + k0, buf);
+          }
         }
+        tc::wait_st();
+      }
+      fence_proxy_async();
+      tc::fence_before();
+      named_sync(1, 128);
+      if (tid == 0) {
+        const bool ready = mbar_wait(&bar[4], it & 1);   // dO^T of this chunk staged in K-block 0 of A2
+        tc::fence_after();
+        ok &= ready;
+        if (ready) {
+          const uint64_t d_rb = b ? d_rec1 : d_rec0, d_bmt = d_rb + (TcRecB::BMT >> 4), d_kh = d_rb + (TcRecB::KH >> 4);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc::mma_bf16(tmem + 192, d_a2 + (16384 >> 4) + 2 * ks, d_tbt + 2 * ks, tc::idesc_bf16(128, 64), ks > 0);
-      tc::commit(&bar[3]);
-    }
-    done = it + 1;
-    last_j = j;
-  }
-  if (ok && done > 0) ok = mbar_wait(&bar[3], (done - 1) & 1);
-  tc::fence_after();
-  if (__syncthreads_and(ok)) {
-    if (done > 0) store_dv(last_j);
-    if (p.dh0) {   // dh0[dk][dv] = dS^T[dv][dk]
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16(tmem + 128, d_a2 + 2 * ks, d_bmt + 2 * ks, tc::idesc_bf16(128, 64), ks > 0);
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
+          for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_bf16(tmem + 128, d_as + ((kb * 16384 + 32 * ks) >> 4), d_kh + ((kb * 8192 + 32 * ks) >> 4),
+                           tc::idesc_bf16(128, 64), 1);
+          tc::commit(&bar[2]);
+        }
+      } else if (tid == 32) {
+        // the chunk-end dS leaves as one bulk copy of the operand tile
+        bulk_s2g((bf16 *)p.dsaved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
+        bulk_commit();
+      }
+      ok &= mbar_wait(&bar[2], it & 1);
+      tc::fence_after();
+      // pass B: dU^T -> K-block 1 of A2
+      {
         uint32_t r[64];
-        tc::ld64(tl + 64 * hb, r);
+        tc::ld64(tl + 128, r);
         tc::wait_ld();
 #pragma unroll
-        for (int i = 0; i < 64; ++i) p.dh0[(sh * 128 + 64 * hb + i) * 128 + row] = __uint_as_float(r[i]);
+        for (int cb = 0; cb < 8; ++cb) {
+          float buf[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) buf[i] = __uint_as_float(r[8 * cb + i]);
+          *reinterpret_cast<uint4 *>(smem + S::A2 + tc::sw128_off(128, row, 64 + 8 * cb)) = tc::pack8(buf);
+        }
       }
+      fence_proxy_async();
+      tc::fence_before();
+      if (!named_sync_and(1, 128, ok)) break;
+      if (tid == 0) {
+        // dV^T of the previous chunk has been read out by the io warps (frees its columns and
+        // keeps the io warps at most one phase behind on every barrier they wait on)
+        const bool freed = it == 0 || mbar_wait(&bar[5], (it - 1) & 1);
+        tc::fence_after();
+        ok &= freed;
+        if (freed) {
+          const uint64_t d_rb = b ? d_rec1 : d_rec0, d_qwt = d_rb + (TcRecB::QWT >> 4), d_tbt = d_rb + (TcRecB::TBT >> 4);
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t off = (kb * 16384 + 32 * ks) >> 4;
+              tc::mma_bf16(tmem, d_a2 + off, d_qwt + off, tc::idesc_bf16(128, 128), 1);
+            }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16(tmem + 192, d_a2 + (16384 >> 4) + 2 * ks, d_tbt + 2 * ks, tc::idesc_bf16(128, 64), ks > 0);
+          tc::commit(&bar[3]);
+        }
+      }
+      done = it + 1;
     }
+    if (ok && done > 0) ok = mbar_wait(&bar[3], (done - 1) & 1);
+    tc::fence_after();
+    if (named_sync_and(1, 128, ok)) {
+      if (p.dh0) {   // dh0[dk][dv] = dS^T[dv][dk]
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t r[64];
+          tc::ld64(tl + 64 * hb, r);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 64; ++i) p.dh0[(sh * 128 + 64 * hb + i) * 128 + row] = __uint_as_float(r[i]);
+        }
+      }
+    } else {
+      report(p.status, ERR_TIMEOUT);
+    }
+    if (tid == 32) bulk_wait_all();   // saved dS complete before the CTA leaves
   } else {
-    report(p.status, ERR_TIMEOUT);
+    // ------------------------------------------------------------ io warps
+    auto load_do = [&](int j, uint4 (&x)[8]) {
+      const long long t0 = s0 + (long long)j * CH;
+      const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int idx = row + 128 * i, r = idx >> 4, ch = idx & 15;
+        x[i] = make_uint4(0, 0, 0, 0);
+        if (r < clen) x[i] = __ldg(reinterpret_cast<const uint4 *>(dO + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
+      }
+    };
+    // raw dO rows -> staging tile -> dO^T operand (K-block 0 of A2: row = value channel); then signal
+    auto stage_do = [&](const uint4 (&x)[8]) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int idx = row + 128 * i;
+        *reinterpret_cast<uint4 *>(smem + S::DST + (idx >> 4) * 256 + (idx & 15) * 16) = x[i];
+      }
+      named_sync(2, 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t lo = *reinterpret_cast<const unsigned short *>(smem + S::DST + (8 * c + 2 * e) * 256 + row * 2);
+          const uint32_t hi = *reinterpret_cast<const unsigned short *>(smem + S::DST + (8 * c + 2 * e + 1) * 256 + row * 2);
+          w[e] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4 *>(smem + S::A2 + tc::sw128_off(128, row, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async();
+      named_sync(2, 128);   // the staging tile is free again
+      mbar_arrive(&bar[4]);
+    };
+    // dV^T (TMEM) -> dv rows of chunk j (fp32). Each warp transposes its 32 value channels
+    // through its own 4 KB of the staging tile, 32 tokens at a time, and writes 128-byte
+    // row pieces with 16-byte stores.
+    auto store_dv = [&](int j) {
+      const long long t0 = s0 + (long long)j * CH;
+      const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+      uint32_t r[64];
+      tc::ld64(tl + 192, r);
+      tc::wait_ld();
+      float *wst = reinterpret_cast<float *>(smem + S::DST + qw * 4096);   // [32 tok][32 channels]
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) wst[i * 32 + lane] = __uint_as_float(r[32 * half + i]);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int tok = 4 * k + (lane >> 3), ch = lane & 7, gt = 32 * half + tok;
+          if (gt < clen)
+            *reinterpret_cast<float4 *>(p.dv + ((size_t)(t0 + gt) * H + h) * 128 + 32 * qw + 4 * ch) =
+                *reinterpret_cast<const float4 *>(wst + tok * 32 + 4 * ch);
+        }
+        __syncwarp();
+      }
+    };
+    uint4 dr[8];
+    if (nch > 0) {
+      load_do(nch - 1, dr);
+      stage_do(dr);
+    }
+    if (nch > 1) load_do(nch - 2, dr);
+    for (int it = 0; it < nch; ++it) {
+      const int j = nch - 1 - it;
+      ok &= mbar_wait(&bar[3], it & 1);   // phase 2 of this chunk: A2 and dV^T are final
+      tc::fence_after();
+      if (!named_sync_and(2, 128, ok)) break;
+      if (it + 1 < nch) {
+        stage_do(dr);                      // the next chunk's dO, loaded a whole step earlier
+        if (it + 2 < nch) load_do(j - 2, dr);
+      }
+      store_dv(j);
+      named_sync(2, 128);                  // every warp is done with the staging tile
+      tc::fence_before();
+      mbar_arrive(&bar[5]);
+    }
   }
-  if (tid == 32) bulk_wait_all();   // saved dS complete before the CTA leaves
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, 256);
@@ -567,7 +607,7 @@ cudaError_t launch_bwd_scan_tc(const BwdScanParams &p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kda_bwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        TcBwdSmem::BYTES);
   if (e != cudaSuccess) return e;
-  kda_bwd_scan_tc_kernel<<<(unsigned)units, 128, TcBwdSmem::BYTES, s>>>(p);
+  kda_bwd_scan_tc_kernel<<<(unsigned)units, 256, TcBwdSmem::BYTES, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -43,14 +43,13 @@ DEC_BYTES = 2 * D * D * 4 + 4 * (3 * 256 + 512 + 4 + 256)   # per (sequence, hea
 KERNEL_BYTES = {
     "fwd.prep": 256 + 256 + 512 + 4,         # q, k, g, beta
     "fwd.scan": 256 + 256,                   # v in, o out
-    "bwd.prep": 256 + 256 + 512 + 4,         # q, k, g, beta
     "bwd.dscan": 256 + 512,                  # dO in, dv out
     "bwd.state": 256,                        # v
-    "bwd.intra": 3 * 512 + 4,                # dq, dk, dg, dbeta out
+    "bwd.intra": 256 + 256 + 512 + 4 + 3 * 512 + 4,   # q, k, g, beta in; dq, dk, dg, dbeta out
 }
 FWD_STAGES = ["fwd.table", "fwd.prep", "fwd.scan"]
-BWD_STAGES = ["bwd.table", "bwd.prep", "bwd.dscan", "bwd.state", "bwd.intra"]
-KERNEL_SRC = {"fwd.prep": "kda_prep.cu", "fwd.scan": "kda_scan_tc.cu", "bwd.prep": "kda_prep.cu",
+BWD_STAGES = ["bwd.table", "bwd.dscan", "bwd.state", "bwd.intra"]
+KERNEL_SRC = {"fwd.prep": "kda_prep.cu", "fwd.scan": "kda_scan_tc.cu",
               "bwd.dscan": "kda_scan_tc.cu", "bwd.state": "kda_bwd.cu", "bwd.intra": "kda_bwd.cu",
               "decode": "kda_step.cu"}
 

@@ -52,7 +52,7 @@ size_t elem_size(int io) { return io == KDA_F32 ? 4 : 2; }
 
 // Workspace carving shared by the forward and the backward.
 struct WsPlan {
-  size_t cu, choff, img, dsaved, grad, aux, img2, bytes;
+  size_t cu, choff, img, dsaved, grad, bytes;
 };
 
 WsPlan plan(const kda_fwd_args *a, bool bwd) {
@@ -62,20 +62,44 @@ WsPlan plan(const kda_fwd_args *a, bool bwd) {
   const kda::ImgLayout L((int)elem_size(a->io_dtype));
   w.cu = 0;
   w.choff = round_up(w.cu + n1 * 4, 256);
-  w.img = round_up(w.choff + n1 * 4, 256);
-  size_t end = w.img + mc * H * L.bytes;
-  if (bwd) {
+  size_t end = w.choff + n1 * 4;
+  if (!bwd) {   // the forward record (the backward's records come with `saved`)
+    w.img = round_up(end, 256);
+    end = w.img + mc * H * (a->io_dtype == KDA_F32 ? L.bytes : (size_t)kda::TcRec::BYTES);
+  } else {
     w.dsaved = round_up(end, 256);
     end = w.dsaved + mc * H * 128 * 128 * elem_size(a->io_dtype);
     w.grad = round_up(end, 256);
     end = w.grad + mc * H * kda::GradLayout::bytes;
-    w.aux = round_up(end, 256);
-    end = w.aux + mc * H * 2 * 64 * 64 * sizeof(float);
-    w.img2 = round_up(end, 256);
-    end = w.img2 + mc * H * kda::TcRecB::BYTES;
   }
   w.bytes = round_up(end, 256);
   return w;
+}
+
+// What kda_fwd writes to `saved` for kda_bwd, per (chunk, head), as consecutive arrays:
+// the chunk-start states (io type, S^T in the scans' operand-tile layout) and, for bf16,
+// the backward's chunk records computed once by the forward's prep: the tile record
+// (Kt, Kh, Tb, Bm, e^{G_last}), the fp32 A and T, and the dS-scan record (TcRecB).
+struct SavedPlan {
+  size_t states, tiles, aux, img2, bytes;
+};
+
+SavedPlan saved_plan(const kda_fwd_args *a) {
+  SavedPlan sp{};
+  const size_t n = (size_t)max_chunks(a) * a->heads;
+  sp.states = 0;
+  size_t end = n * 128 * 128 * elem_size(a->io_dtype);
+  if (a->io_dtype != KDA_F32) {
+    const kda::ImgLayout L(2);
+    sp.tiles = round_up(end, 256);
+    end = sp.tiles + n * L.bytes;
+    sp.aux = round_up(end, 256);
+    end = sp.aux + n * 2 * 64 * 64 * sizeof(float);
+    sp.img2 = round_up(end, 256);
+    end = sp.img2 + n * kda::TcRecB::BYTES;
+  }
+  sp.bytes = round_up(end, 256);
+  return sp;
 }
 
 kda_status check_fwd(const kda_fwd_args *a, const char *who) {
@@ -153,7 +177,7 @@ size_t kda_fwd_workspace_size(const kda_fwd_args *a) {
 
 size_t kda_saved_size(const kda_fwd_args *a) {
   if (check_fwd(a, "kda_saved_size") != KDA_OK) return 0;
-  return (size_t)max_chunks(a) * a->heads * 128 * 128 * elem_size(a->io_dtype);
+  return saved_plan(a).bytes;
 }
 
 size_t kda_bwd_workspace_size(const kda_bwd_args *a) {
@@ -188,7 +212,22 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_fwd chunk table");
   mark(0, stream);
-  kda::PrepParams pp{geo, a->q, a->k, a->g, a->beta, a->scale, ws + w.img, nullptr, f32 ? 0 : 1, nullptr, a->dev_status};
+  // with `saved` (a training forward) the prep also writes the backward's chunk records there
+  const SavedPlan sv = saved_plan(a);
+  char *sd = static_cast<char *>(a->saved);
+  const bool bwd_recs = !f32 && sd;
+  kda::PrepParams pp{geo,
+                     a->q,
+                     a->k,
+                     a->g,
+                     a->beta,
+                     a->scale,
+                     ws + w.img,
+                     bwd_recs ? reinterpret_cast<float *>(sd + sv.aux) : nullptr,
+                     f32 ? 0 : (bwd_recs ? 3 : 1),
+                     bwd_recs ? sd + sv.img2 : nullptr,
+                     bwd_recs ? sd + sv.tiles : nullptr,
+                     a->dev_status};
   if ((e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
   kda::FwdScanParams sp{geo, a->v, ws + w.img, a->h0, a->o, a->hT, a->saved, a->dev_status};
@@ -238,21 +277,20 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_bwd chunk table");
   mark(0, stream);
-  kda::PrepParams pp{geo,       f->q, f->k, f->g, f->beta, f->scale, ws + w.img, reinterpret_cast<float *>(ws + w.aux),
-                     2,         ws + w.img2, f->dev_status};
-  if ((e = kda::launch_prep(pp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd prep");
-  mark(1, stream);
-  kda::BwdScanParams bp{geo, a->dO, ws + w.img2, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
+  // the chunk records were written by the forward's prep into `saved`
+  const SavedPlan sv = saved_plan(f);
+  char *sd = static_cast<char *>(f->saved);
+  kda::BwdScanParams bp{geo, a->dO, sd + sv.img2, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
   if ((e = kda::launch_bwd_scan_tc(bp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd dS scan");
-  mark(2, stream);
-  kda::BwdStateParams sp{geo, f->v, a->dO, ws + w.img, f->saved, ws + w.dsaved,
+  mark(1, stream);
+  kda::BwdStateParams sp{geo, f->v, a->dO, sd + sv.tiles, sd + sv.states, ws + w.dsaved,
                          reinterpret_cast<float *>(ws + w.grad), f->dev_status};
   if ((e = kda::launch_bwd_state(sp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd state grads");
-  mark(3, stream);
+  mark(2, stream);
   kda::BwdIntraParams ip{geo, f->q, f->k, f->g, f->beta, f->scale, reinterpret_cast<const float *>(ws + w.grad),
-                         reinterpret_cast<const float *>(ws + w.aux), a->dq, a->dk, a->dg, a->dbeta, f->dev_status};
+                         reinterpret_cast<const float *>(sd + sv.aux), a->dq, a->dk, a->dg, a->dbeta, f->dev_status};
   if ((e = kda::launch_bwd_intra(ip, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd intra grads");
-  mark(4, stream);
+  mark(3, stream);
   g_last_error.clear();
   return KDA_OK;
 }

@@ -73,11 +73,12 @@ struct PrepParams {
   const void *q, *k;
   const float *g, *beta;
   float scale;
-  void *img;               // [max_chunks][H] records (ImgLayout, or TcRec when tc_layout)
-  float *aux;              // optional [max_chunks][H] x {A (strict lower), T} fp32 64x64 each
-  int tc_layout;           // bf16 only: 1 = write the tcgen05 forward record (to img);
-                           // 2 = also write the tcgen05 backward record (to img2)
-  void *img2;              // [max_chunks][H] TcRecB records (tc_layout == 2)
+  void *img;               // [max_chunks][H] forward records: TcRec (bf16) or the tile record (fp32)
+  float *aux;              // [max_chunks][H] x {A (strict lower), T} fp32 64x64 each, or NULL
+  int tc_layout;           // bf16: bit 0 = write the tcgen05 forward record to img;
+                           //       bit 1 = write the backward records: tiles, TcRecB, aux
+  void *img2;              // [max_chunks][H] TcRecB records (bit 1)
+  void *tiles;             // [max_chunks][H] tile records ImgLayout (bit 1)
   int *status;
 };
 

@@ -188,8 +188,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
   // tcgen05 record (bf16 forward) or the tile record (fp32 forward, backward)
-  const bool tcrec = !PRECISE && p.tc_layout == 1;   // forward tcgen05 record instead of the tiles
-  const bool bwdrec = !PRECISE && p.tc_layout == 2;  // tiles plus the backward tcgen05 record
+  const bool tcrec = !PRECISE && (p.tc_layout & 1);   // forward tcgen05 record
+  const bool bwdrec = !PRECISE && (p.tc_layout & 2);  // backward records: tiles, TcRecB, A and T
   const E *qg = (const E *)p.q, *kg = (const E *)p.k;
   float *rq = (float *)(smem + S::RQ), *rk = (float *)(smem + S::RK), *sb = (float *)(smem + S::BETA);
   float *KL = (float *)(smem + S::KL), *QL = (float *)(smem + S::QL), *RR = (float *)(smem + S::R);
@@ -197,9 +197,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   float(*tot)[128] = (float(*)[128])(smem + S::TOT);
   float(*pvv)[128] = (float(*)[128])(smem + S::PV);
   const ImgLayout L(sizeof(E));
-  const size_t rec_bytes = tcrec ? (size_t)TcRec::BYTES : L.bytes;
-  char *rec = (char *)p.img + ((size_t)chunk * H + h) * rec_bytes;
-  char *recb = bwdrec ? (char *)p.img2 + ((size_t)chunk * H + h) * TcRecB::BYTES : nullptr;
+  const size_t rid = (size_t)chunk * H + h;
+  char *rec = tcrec ? (char *)p.img + rid * TcRec::BYTES : nullptr;                       // forward tcgen05 record
+  char *trec = bwdrec ? (char *)p.tiles + rid * L.bytes : (PRECISE ? (char *)p.img + rid * L.bytes : nullptr);
+  char *recb = bwdrec ? (char *)p.img2 + rid * TcRecB::BYTES : nullptr;
 
   // 0. stage the chunk's q, k (io type) and g (fp32) in shared memory with one batch of
   //    asynchronous copies: q in the KL tile, k in the R tile, g in the QL tile (row
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
     const float ta0 = tot[a][c0], ta1 = tot[a][c0 + 1];                       // E_a - E_{a-1}
     pvv[a][c0] = pa0;
     pvv[a][c0 + 1] = pa1;
-    Tile<E, 128> tqt((E *)(rec + L.qt)), tkt((E *)(rec + L.kt)), tkh((E *)(rec + L.kh));
+    Tile<E, 128> tqt((E *)(trec + L.qt)), tkt((E *)(trec + L.kt)), tkh((E *)(trec + L.kh));
     float kh0v[SUB], kh1v[SUB], qt0v[SUB], qt1v[SUB];
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
@@ -312,15 +313,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       *reinterpret_cast<float2 *>(RR + r * LDF + c0) = make_float2(rr0, rr1);
       kh0v[i] = rr0 * fa0;                        // Kh = k^ exp(G_last - G_r)
       kh1v[i] = rr1 * fa1;
-      if (tcrec) {
-        // B1 rows 0..63: Qt[tok][dk] = q^ exp(G_r)
+      if (tcrec)   // B1 rows 0..63: Qt[tok][dk] = q^ exp(G_r)
         st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, r, c0)), ql0 * pa0, ql1 * pa1);
-      } else {
+      if (trec) {
         if (!bwdrec) st2(tqt.at(r, c0), ql0 * pa0, ql1 * pa1);   // Qt = q^ exp(G_r) (unused by the backward)
         st2(tkt.at(r, c0), kl0 * pa0, kl1 * pa1);                 // Kt = k^ exp(G_r)
         st2(tkh.at(r, c0), kh0v[i], kh1v[i]);
-        if (bwdrec) st2((E *)(recb + TcRecB::KH + tc::sw128_off(64, r, c0)), kh0v[i], kh1v[i]);
       }
+      if (bwdrec) st2((E *)(recb + TcRecB::KH + tc::sw128_off(64, r, c0)), kh0v[i], kh1v[i]);
       qt0v[i] = ql0 * pa0;
       qt1v[i] = ql1 * pa1;
     }
@@ -349,9 +349,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       }
     }
     if (a == 0) {
-      char *gcp = rec + (tcrec ? TcRec::GC : L.gc);
-      *reinterpret_cast<float2 *>(gcp + c0 * 4) = make_float2(exp2f(e3[0]), exp2f(e3[1]));
-      if (bwdrec) *reinterpret_cast<float2 *>(recb + TcRecB::GC + c0 * 4) = make_float2(exp2f(e3[0]), exp2f(e3[1]));
+      const float2 gc = make_float2(exp2f(e3[0]), exp2f(e3[1]));
+      if (tcrec) *reinterpret_cast<float2 *>(rec + TcRec::GC + c0 * 4) = gc;
+      if (trec) *reinterpret_cast<float2 *>(trec + L.gc + c0 * 4) = gc;
+      if (bwdrec) *reinterpret_cast<float2 *>(recb + TcRecB::GC + c0 * 4) = gc;
     }
   }
   __syncthreads();
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   __syncthreads();   // QL and R are free from here on
   {
     float *Lm = (float *)(smem + S::LM);
-    Tile<E, 64> bm((E *)(rec + L.bm));
+    Tile<E, 64> bm((E *)(trec + L.bm));
     float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) : nullptr;
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
           if (task & 1) {
             const float b0 = j <= r ? v0 : 0.f, b1 = j + 1 <= r ? v1 : 0.f;
             if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), b0, b1);
-            else st2(bm.at(r, j), b0, b1);
+            if (trec) st2(bm.at(r, j), b0, b1);
             if (bwdrec) st2((E *)(smem + S::BMS) + r * 64 + j, b0, b1);   // staged, transposed below
           } else {
             const float a0 = j < r ? v0 : 0.f, a1 = j + 1 < r ? v1 : 0.f;
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       const int r = idx >> 5, j = (idx & 31) * 2;
       if ((j >> 4) > (r >> 4)) {
         if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), 0.f, 0.f);
-        else st2(bm.at(r, j), 0.f, 0.f);
+        if (trec) st2(bm.at(r, j), 0.f, 0.f);
         if (bwdrec) st2((E *)(smem + S::BMS) + r * 64 + j, 0.f, 0.f);
       }
     }
@@ -476,17 +477,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   // 5. Tb = T Diag(beta) (fp32 in place, and into the record); T for the backward
   {
     float *T = (float *)(smem + S::TT);
-    Tile<E, 64> tb((E *)(rec + L.tb));
+    Tile<E, 64> tb((E *)(trec + L.tb));
     float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) + 64 * 64 : nullptr;
     for (int idx = tid; idx < 64 * 32; idx += PREP_THREADS) {
       const int r = idx >> 5, j = (idx & 31) * 2;
       const float t0 = T[r * LDS64 + j], t1 = T[r * LDS64 + j + 1];
       const float b0 = t0 * sb[j], b1 = t1 * sb[j + 1];
-      if (tcrec) {
-        st2((E *)(rec + TcRec::TB + tc::sw128_off(64, r, j)), b0, b1);
-      } else {
-        st2(tb.at(r, j), b0, b1);
-      }
+      if (tcrec) st2((E *)(rec + TcRec::TB + tc::sw128_off(64, r, j)), b0, b1);
+      if (trec) st2(tb.at(r, j), b0, b1);
       if (tcrec || bwdrec) *reinterpret_cast<float2 *>(T + r * LDS64 + j) = make_float2(b0, b1);
       if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(t0, t1);
     }

@@ -82,8 +82,10 @@ typedef struct {
     const float *h0;           /* [N, H, dk, dv] initial states, or NULL for zero        */
     void *o;                   /* out [total, H, dv]                                     */
     float *hT;                 /* out [N, H, dk, dv] final states, or NULL               */
-    void *saved;               /* out, kda_saved_size() bytes: chunk-start states kept
-                                  for kda_bwd, or NULL when no backward follows          */
+    void *saved;               /* out, kda_saved_size() bytes: what kda_bwd needs from this
+                                  forward (chunk-start states; for bf16 also the chunk
+                                  records of the backward, computed in the same pass), or
+                                  NULL when no backward follows                           */
     void *workspace;           /* scratch, kda_fwd_workspace_size() bytes                */
     size_t workspace_bytes;
     int32_t *dev_status;       /* optional device int32, see above                       */
@@ -132,7 +134,9 @@ typedef struct {
  */
 kda_status kda_fwd(const kda_fwd_args *args, cudaStream_t stream);
 size_t kda_fwd_workspace_size(const kda_fwd_args *args);
-/* Bytes of chunk-start states that kda_fwd writes to args->saved for kda_bwd. */
+/* Bytes that kda_fwd writes to args->saved for kda_bwd: per (chunk, head) the
+ * chunk-start state (io type) and, for bf16 I/O, the backward's chunk records
+ * (about 164 KB more per chunk and head). */
 size_t kda_saved_size(const kda_fwd_args *args);
 
 /* kda_bwd -- gradients for q, k, v, beta, g and the initial state (the pages

@@ -78,10 +78,10 @@ WsPlan plan(const kda_fwd_args *a, bool bwd) {
 
 // What kda_fwd writes to `saved` for kda_bwd, per (chunk, head), as consecutive arrays:
 // the chunk-start states (io type, S^T in the scans' operand-tile layout) and, for bf16,
-// the backward's chunk records computed once by the forward's prep: the tile record
-// (Kt, Kh, Tb, Bm, e^{G_last}), the fp32 A and T, and the dS-scan record (TcRecB).
+// the backward's chunk records computed once by the forward's prep: the fp32 A and T,
+// and the backward record (TcRecB: the dS scan's operands plus Kt).
 struct SavedPlan {
-  size_t states, tiles, aux, img2, bytes;
+  size_t states, aux, img2, bytes;
 };
 
 SavedPlan saved_plan(const kda_fwd_args *a) {
@@ -90,9 +90,6 @@ SavedPlan saved_plan(const kda_fwd_args *a) {
   sp.states = 0;
   size_t end = n * 128 * 128 * elem_size(a->io_dtype);
   if (a->io_dtype != KDA_F32) {
-    const kda::ImgLayout L(2);
-    sp.tiles = round_up(end, 256);
-    end = sp.tiles + n * L.bytes;
     sp.aux = round_up(end, 256);
     end = sp.aux + n * 2 * 64 * 64 * sizeof(float);
     sp.img2 = round_up(end, 256);
@@ -226,7 +223,6 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
                      bwd_recs ? reinterpret_cast<float *>(sd + sv.aux) : nullptr,
                      f32 ? 0 : (bwd_recs ? 3 : 1),
                      bwd_recs ? sd + sv.img2 : nullptr,
-                     bwd_recs ? sd + sv.tiles : nullptr,
                      a->dev_status};
   if ((e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
@@ -283,7 +279,7 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
   kda::BwdScanParams bp{geo, a->dO, sd + sv.img2, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
   if ((e = kda::launch_bwd_scan_tc(bp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd dS scan");
   mark(1, stream);
-  kda::BwdStateParams sp{geo, f->v, a->dO, sd + sv.tiles, sd + sv.states, ws + w.dsaved,
+  kda::BwdStateParams sp{geo, f->v, a->dO, sd + sv.img2, sd + sv.states, ws + w.dsaved,
                          reinterpret_cast<float *>(ws + w.grad), f->dev_status};
   if ((e = kda::launch_bwd_state(sp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd state grads");
   mark(2, stream);

@@ -27,8 +27,9 @@ constexpr int STATE_THREADS = 512;   // 16 warps: 4 row blocks x 4 column quarte
 template <typename E>
 struct StateSmem {
   static constexpr int T128 = 64 * 128 * (int)sizeof(E), T64 = 64 * 64 * (int)sizeof(E);
-  static constexpr int QT = 0, KT = T128, TB = 2 * T128, BM = TB + T64, KH = BM + T64, GC = KH + T128;
-  static constexpr int REC = GC + 512;
+  // the backward record's BMT, KH (contiguous), TBT, GC (contiguous) and KT, packed
+  static constexpr int BMT = 0, KH = BMT + T64, TBT = KH + T128, GC = TBT + T64, KT = GC + 1024;
+  static constexpr int REC = KT + T128;
   static constexpr int SS = (REC + 127) / 128 * 128;      // S^T [128][128]
   static constexpr int SDS = SS + 2 * T128;               // dS^T [128][128]
   static constexpr int SV = SDS + 2 * T128;               // V -> V' [64][128]
@@ -58,13 +59,17 @@ __global__ void __launch_bounds__(STATE_THREADS) kda_bwd_state_kernel(BwdStatePa
   __syncthreads();
   if (tid == 0) {
     fence_proxy_async();
-    mbar_expect_tx(bar, S::REC - S::KT + 4 * S::T128);   // the record's Qt slot is not needed here
-    bulk_g2s(smem + S::KT, (const char *)p.img + rid * S::REC + S::KT, S::REC - S::KT, bar);
+    const char *rb = (const char *)p.img + rid * TcRecB::BYTES;
+    mbar_expect_tx(bar, (TcRecB::QWT - TcRecB::BMT) + (TcRecB::SCAN - TcRecB::TBT) + S::T128 + 4 * S::T128);
+    bulk_g2s(smem + S::BMT, rb + TcRecB::BMT, TcRecB::QWT - TcRecB::BMT, bar);     // Bm^T, Kh
+    bulk_g2s(smem + S::TBT, rb + TcRecB::TBT, TcRecB::SCAN - TcRecB::TBT, bar);    // Tb^T, e^{G_last}
+    bulk_g2s(smem + S::KT, rb + TcRecB::KT, S::T128, bar);                          // Kt
     bulk_g2s(smem + S::SS, (const char *)p.saved + rid * 2 * S::T128, 2 * S::T128, bar);
     bulk_g2s(smem + S::SDS, (const char *)p.dsaved + rid * 2 * S::T128, 2 * S::T128, bar);
   }
-  Tile<E, 128> Kt((E *)(smem + S::KT)), Kh((E *)(smem + S::KH));
-  Tile<E, 64> Tb((E *)(smem + S::TB)), Bm((E *)(smem + S::BM));
+  // operand tiles in the tcgen05 swizzled layout the prep wrote them in
+  TileSW<64> Kt((bf16 *)(smem + S::KT)), Kh((bf16 *)(smem + S::KH)), TbT((bf16 *)(smem + S::TBT)),
+      BmT((bf16 *)(smem + S::BMT));
   // saved S^T and dS^T [v][k] arrive in the scans' operand-tile layout
   TileSW<128> sS((bf16 *)(smem + S::SS)), sdS((bf16 *)(smem + S::SDS));
   Tile<E, 128> sV((E *)(smem + S::SV)), sdO((E *)(smem + S::SDO)), sU((E *)(smem + S::SU)), sdU((E *)(smem + S::SDU)),
@@ -103,14 +108,14 @@ __global__ void __launch_bounds__(STATE_THREADS) kda_bwd_state_kernel(BwdStatePa
   __syncthreads();
   // U = Tb V' ;  dU = Bm^T dO + Kh dS
   zero(acc);
-  wgemm<true, false, 4>(acc, Tb, 16 * mt, sV, 32 * nq, 0, 16 * (mt + 1));
+  wgemm<false, false, 4>(acc, TbT, 16 * mt, sV, 32 * nq, 0, 16 * (mt + 1));   // A(r, j) = Tb[r][j] = TbT[j][r]
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
       st2(sU.at(r0 + 8 * hh, 32 * nq + 8 * nt + 2 * q4), acc[nt][2 * hh], acc[nt][2 * hh + 1]);
   zero(acc);
-  wgemm<false, false, 4>(acc, Bm, 16 * mt, sdO, 32 * nq, 16 * mt, 64);
+  wgemm<true, false, 4>(acc, BmT, 16 * mt, sdO, 32 * nq, 16 * mt, 64);     // A(r, j) = Bm[j][r] = BmT[r][j]
   wgemm<true, true, 4>(acc, Kh, 16 * mt, sdS, 32 * nq, 0, 128);   // B(k=c, n=v) = dS^T[v][c]
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
@@ -121,7 +126,7 @@ __global__ void __launch_bounds__(STATE_THREADS) kda_bwd_state_kernel(BwdStatePa
   float *rec = p.grad + rid * (GradLayout::bytes / 4);
   // -dV' = -Tb^T dU ;  dBm = dO U^T ;  dTb = dU V'^T
   zero(acc);
-  wgemm<false, false, 4>(acc, Tb, 16 * mt, sdU, 32 * nq, 16 * mt, 64);
+  wgemm<true, false, 4>(acc, TbT, 16 * mt, sdU, 32 * nq, 16 * mt, 64);     // A(r, j) = Tb[j][r] = TbT[r][j]
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
 #pragma unroll

@@ -39,18 +39,19 @@ struct TcRec {
   static constexpr int B1 = 0, B2 = 32768, TB = B2 + 24576, GC = TB + 8192, BYTES = GC + 512;
 };
 
-// Per-(chunk, head) record for the tcgen05 backward dS scan (bf16), same format:
+// Per-(chunk, head) backward record (bf16), same format; the dS scan copies the
+// first SCAN bytes, the state kernel BMT, KH, TBT, GC and KT:
 //   BMT [64 rows r][K = 64 j] : Bm^T (Bm[j][r])
 //   KH  [64 rows tok][K = 128]: Kh[tok][dk]
 //   QWT [128 rows dk][K = 128]: K < 64: Qt^T[dk][tok], K >= 64: -W^T[dk][tok]
 //   TBT [64 rows r][K = 64 j] : Tb^T (Tb[j][r])
 //   GC  128 fp32              : exp(G_last)
+//   KT  [64 rows tok][K = 128]: Kt[tok][dk]
 struct TcRecB {
-  static constexpr int BMT = 0, KH = 8192, QWT = KH + 16384, TBT = QWT + 32768, GC = TBT + 8192, BYTES = GC + 512;
+  static constexpr int BMT = 0, KH = 8192, QWT = KH + 16384, TBT = QWT + 32768, GC = TBT + 8192, SCAN = GC + 512;
+  static constexpr int KT = (SCAN + 1023) / 1024 * 1024, BYTES = KT + 16384;
 };
 
-// Per-(chunk, head) record of state-side gradients written by the backward's
-// state kernel: dQt, dKt, dKh (64x128 fp32 each), dBm, dTb (64x64 fp32), dgC (128).
 // State-side gradients of one (chunk, head), written by the state kernel for the
 // intra kernel: dQt, dKt, dKh bf16 [64][128] and dBm bf16 [64][64] (fp32
 // accumulation, rounded once), dTb fp32 [64][64], dgC fp32 [128]. Byte offsets.
@@ -76,9 +77,8 @@ struct PrepParams {
   void *img;               // [max_chunks][H] forward records: TcRec (bf16) or the tile record (fp32)
   float *aux;              // [max_chunks][H] x {A (strict lower), T} fp32 64x64 each, or NULL
   int tc_layout;           // bf16: bit 0 = write the tcgen05 forward record to img;
-                           //       bit 1 = write the backward records: tiles, TcRecB, aux
+                           //       bit 1 = write the backward records: TcRecB and aux
   void *img2;              // [max_chunks][H] TcRecB records (bit 1)
-  void *tiles;             // [max_chunks][H] tile records ImgLayout (bit 1)
   int *status;
 };
 
@@ -108,7 +108,7 @@ struct BwdScanParams {
 struct BwdStateParams {
   SeqGeom geo;
   const void *v, *dO;
-  const void *img, *saved, *dsaved;
+  const void *img, *saved, *dsaved;   // img: TcRecB records
   float *grad;             // [max_chunks][H] GradLayout records
   int *status;
 };

@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
   // tcgen05 record (bf16 forward) or the tile record (fp32 forward, backward)
   const bool tcrec = !PRECISE && (p.tc_layout & 1);   // forward tcgen05 record
-  const bool bwdrec = !PRECISE && (p.tc_layout & 2);  // backward records: tiles, TcRecB, A and T
+  const bool bwdrec = !PRECISE && (p.tc_layout & 2);  // backward records: TcRecB, A and T
   const E *qg = (const E *)p.q, *kg = (const E *)p.k;
   float *rq = (float *)(smem + S::RQ), *rk = (float *)(smem + S::RK), *sb = (float *)(smem + S::BETA);
   float *KL = (float *)(smem + S::KL), *QL = (float *)(smem + S::QL), *RR = (float *)(smem + S::R);
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   const ImgLayout L(sizeof(E));
   const size_t rid = (size_t)chunk * H + h;
   char *rec = tcrec ? (char *)p.img + rid * TcRec::BYTES : nullptr;                       // forward tcgen05 record
-  char *trec = bwdrec ? (char *)p.tiles + rid * L.bytes : (PRECISE ? (char *)p.img + rid * L.bytes : nullptr);
+  char *trec = PRECISE ? (char *)p.img + rid * L.bytes : nullptr;                         // fp32 tile record
   char *recb = bwdrec ? (char *)p.img2 + rid * TcRecB::BYTES : nullptr;
 
   // 0. stage the chunk's q, k (io type) and g (fp32) in shared memory with one batch of
@@ -320,7 +320,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
         st2(tkt.at(r, c0), kl0 * pa0, kl1 * pa1);                 // Kt = k^ exp(G_r)
         st2(tkh.at(r, c0), kh0v[i], kh1v[i]);
       }
-      if (bwdrec) st2((E *)(recb + TcRecB::KH + tc::sw128_off(64, r, c0)), kh0v[i], kh1v[i]);
+      if (bwdrec) {
+        st2((E *)(recb + TcRecB::KH + tc::sw128_off(64, r, c0)), kh0v[i], kh1v[i]);
+        st2((E *)(recb + TcRecB::KT + tc::sw128_off(64, r, c0)), kl0 * pa0, kl1 * pa1);
+      }
       qt0v[i] = ql0 * pa0;
       qt1v[i] = ql1 * pa1;
     }

@@ -332,7 +332,7 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
 //            dV^T  = dU^T Tb                        (M=128, N=64,  K=64)
 // i.e. dU = Bm^T dO + Kh dS, dS <- gC*dS + Qt^T dO - W^T dU, dv = Tb^T dU.
 struct TcBwdSmem {
-  static constexpr int RECS = (TcRecB::BYTES + 1023) / 1024 * 1024;
+  static constexpr int RECS = (TcRecB::SCAN + 1023) / 1024 * 1024;
   static constexpr int REC0 = 0, REC1 = RECS;
   static constexpr int AS = 2 * RECS;        // dS^T bf16 [128][K=128]
   static constexpr int A2 = AS + 32768;      // [dO^T | dU^T] bf16 [128][K=128]
@@ -378,8 +378,8 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
     // ------------------------------------------------------------ state warps
     auto issue = [&](char *dst, const char *src, uint64_t *b) {
       fence_proxy_async();
-      mbar_expect_tx(b, TcRecB::BYTES);
-      bulk_g2s(dst, src, TcRecB::BYTES, b);
+      mbar_expect_tx(b, TcRecB::SCAN);
+      bulk_g2s(dst, src, TcRecB::SCAN, b);
     };
     // initial dS^T[dv][dk] = dhT[dk][dv]
     {

@@ -136,7 +136,7 @@ kda_status kda_fwd(const kda_fwd_args *args, cudaStream_t stream);
 size_t kda_fwd_workspace_size(const kda_fwd_args *args);
 /* Bytes that kda_fwd writes to args->saved for kda_bwd: per (chunk, head) the
  * chunk-start state (io type) and, for bf16 I/O, the backward's chunk records
- * (about 164 KB more per chunk and head). */
+ * (about 113 KB more per chunk and head). */
 size_t kda_saved_size(const kda_fwd_args *args);
 
 /* kda_bwd -- gradients for q, k, v, beta, g and the initial state (the pages

@@ -109,8 +109,8 @@ def test_workspace_sizes_scale_with_problem(lib):
     rec = 3 * 64 * 128 * 2 + 2 * 64 * 64 * 2 + 512
     assert lib.kda_fwd_workspace_size(C.byref(a)) >= chunks * 96 * rec
     # saved (bf16): chunk-start states, plus the backward's chunk records written by the
-    # forward's prep: tile record (= rec), fp32 A and T, and the dS-scan record (66048 B)
-    per = 128 * 128 * 2 + rec + 2 * 64 * 64 * 4 + 66048
+    # forward's prep: fp32 A and T, and the backward record (82944 B: dS-scan operands + Kt)
+    per = 128 * 128 * 2 + 2 * 64 * 64 * 4 + 82944
     assert chunks * 96 * per <= lib.kda_saved_size(C.byref(a)) <= chunks * 96 * per + 4 * 256
     b = _lib.BwdArgs()
     b.fwd = a

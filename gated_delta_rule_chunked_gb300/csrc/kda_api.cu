@@ -281,7 +281,7 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
   mark(1, stream);
   kda::BwdStateParams sp{geo, f->v, a->dO, sd + sv.img2, sd + sv.states, ws + w.dsaved,
                          reinterpret_cast<float *>(ws + w.grad), f->dev_status};
-  if ((e = kda::launch_bwd_state(sp, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd state grads");
+  if ((e = kda::launch_bwd_state_tc(sp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd state grads");
   mark(2, stream);
   kda::BwdIntraParams ip{geo, f->q, f->k, f->g, f->beta, f->scale, reinterpret_cast<const float *>(ws + w.grad),
                          reinterpret_cast<const float *>(sd + sv.aux), a->dq, a->dk, a->dg, a->dbeta, f->dev_status};

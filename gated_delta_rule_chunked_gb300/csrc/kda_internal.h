@@ -141,6 +141,7 @@ cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int dv_slice, cuda
 cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_scan_tc(const BwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_state(const BwdStateParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_bwd_state_tc(const BwdStateParams &p, cudaStream_t s);
 cudaError_t launch_bwd_intra(const BwdIntraParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s);
 

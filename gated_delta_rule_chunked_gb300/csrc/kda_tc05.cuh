@@ -30,9 +30,27 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major SW128 operand: 128-byte rows hold 64
+// consecutive M (or N) elements of one K index, 8 K rows form a 1024-byte atom
+// (chunk c of row r at c ^ (r % 8)); `lbo` is the byte stride between 64-element
+// M/N atoms, the K atoms are 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t smem_addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor: D fp32, A and B bf16, both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Same with A and/or B MN-major. For M = 64, row m of D is TMEM lane 32 (m / 16) + m % 16.
+__host__ __device__ constexpr uint32_t idesc_bf16_mn(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_bf16(M, N) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T over one K = 16 step. Issued by one thread.

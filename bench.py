@@ -44,13 +44,12 @@ KERNEL_BYTES = {
     "fwd.prep": 256 + 256 + 512 + 4,         # q, k, g, beta
     "fwd.scan": 256 + 256,                   # v in, o out
     "bwd.dscan": 256 + 512,                  # dO in, dv out
-    "bwd.state": 256,                        # v
-    "bwd.intra": 256 + 256 + 512 + 4 + 3 * 512 + 4,   # q, k, g, beta in; dq, dk, dg, dbeta out
+    "bwd.chunk": 256 + 256 + 256 + 512 + 4 + 3 * 512 + 4,   # v, q, k, g, beta in; dq, dk, dg, dbeta out
 }
 FWD_STAGES = ["fwd.table", "fwd.prep", "fwd.scan"]
-BWD_STAGES = ["bwd.table", "bwd.dscan", "bwd.state", "bwd.intra"]
+BWD_STAGES = ["bwd.table", "bwd.dscan", "bwd.chunk"]
 KERNEL_SRC = {"fwd.prep": "kda_prep.cu", "fwd.scan": "kda_scan_tc.cu",
-              "bwd.dscan": "kda_scan_tc.cu", "bwd.state": "kda_bwd.cu", "bwd.intra": "kda_bwd.cu",
+              "bwd.dscan": "kda_scan_tc.cu", "bwd.chunk": "kda_bwd_tc.cu",
               "decode": "kda_step.cu"}
 
 

@@ -4,8 +4,8 @@
 // workspace, and launches the kernels on the caller's stream:
 //   kda_fwd:  chunk table -> chunk prep (parallel over chunks x heads)
 //             -> forward state scan (sequences x heads x value slices)
-//   kda_bwd:  chunk table -> chunk prep -> reverse dS scan
-//             -> state-side gradients -> intra-chunk gradients
+//   kda_bwd:  chunk table -> reverse dS scan -> chunk gradients (one tcgen05 kernel
+//             per chunk and head; the chunk records come from the forward's prep)
 //   kda_step: one decode kernel.
 #include <cuda_runtime.h>
 
@@ -52,7 +52,7 @@ size_t elem_size(int io) { return io == KDA_F32 ? 4 : 2; }
 
 // Workspace carving shared by the forward and the backward.
 struct WsPlan {
-  size_t cu, choff, img, dsaved, grad, bytes;
+  size_t cu, choff, img, dsaved, bytes;
 };
 
 WsPlan plan(const kda_fwd_args *a, bool bwd) {
@@ -69,8 +69,6 @@ WsPlan plan(const kda_fwd_args *a, bool bwd) {
   } else {
     w.dsaved = round_up(end, 256);
     end = w.dsaved + mc * H * 128 * 128 * elem_size(a->io_dtype);
-    w.grad = round_up(end, 256);
-    end = w.grad + mc * H * kda::GradLayout::bytes;
   }
   w.bytes = round_up(end, 256);
   return w;
@@ -279,14 +277,11 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
   kda::BwdScanParams bp{geo, a->dO, sd + sv.img2, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
   if ((e = kda::launch_bwd_scan_tc(bp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd dS scan");
   mark(1, stream);
-  kda::BwdStateParams sp{geo, f->v, a->dO, sd + sv.img2, sd + sv.states, ws + w.dsaved,
-                         reinterpret_cast<float *>(ws + w.grad), f->dev_status};
-  if ((e = kda::launch_bwd_state_tc(sp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd state grads");
+  kda::BwdChunkParams cp{geo, f->q, f->k, f->v, a->dO, f->g, f->beta, f->scale, sd + sv.img2, sd + sv.states,
+                         ws + w.dsaved, reinterpret_cast<const float *>(sd + sv.aux), a->dq, a->dk, a->dg, a->dbeta,
+                         f->dev_status};
+  if ((e = kda::launch_bwd_chunk_tc(cp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd chunk grads");
   mark(2, stream);
-  kda::BwdIntraParams ip{geo, f->q, f->k, f->g, f->beta, f->scale, reinterpret_cast<const float *>(ws + w.grad),
-                         reinterpret_cast<const float *>(sd + sv.aux), a->dq, a->dk, a->dg, a->dbeta, f->dev_status};
-  if ((e = kda::launch_bwd_intra(ip, false, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd intra grads");
-  mark(3, stream);
   g_last_error.clear();
   return KDA_OK;
 }

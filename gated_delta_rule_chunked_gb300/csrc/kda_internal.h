@@ -52,14 +52,6 @@ struct TcRecB {
   static constexpr int KT = (SCAN + 1023) / 1024 * 1024, BYTES = KT + 16384;
 };
 
-// State-side gradients of one (chunk, head), written by the state kernel for the
-// intra kernel: dQt, dKt, dKh bf16 [64][128] and dBm bf16 [64][64] (fp32
-// accumulation, rounded once), dTb fp32 [64][64], dgC fp32 [128]. Byte offsets.
-struct GradLayout {
-  static constexpr size_t dqt = 0, dkt = 64 * 128 * 2, dkh = 2 * 64 * 128 * 2, dbm = 3 * 64 * 128 * 2,
-                          dtb = dbm + 64 * 64 * 2, dgc = dtb + 64 * 64 * 4, bytes = dgc + 128 * 4;
-};
-
 struct SeqGeom {
   int n_seqs;
   long long total;
@@ -105,21 +97,14 @@ struct BwdScanParams {
   int *status;
 };
 
-struct BwdStateParams {
+struct BwdChunkParams {
   SeqGeom geo;
-  const void *v, *dO;
-  const void *img, *saved, *dsaved;   // img: TcRecB records
-  float *grad;             // [max_chunks][H] GradLayout records
-  int *status;
-};
-
-struct BwdIntraParams {
-  SeqGeom geo;
-  const void *q, *k;
+  const void *q, *k, *v, *dO;   // io type (bf16)
   const float *g, *beta;
   float scale;
-  const float *grad;
-  const float *aux;        // [max_chunks][H] x {A, T} written by the prep kernel
+  const void *img;              // [max_chunks][H] TcRecB records
+  const void *saved, *dsaved;   // [max_chunks][H] chunk-start states S^T, chunk-end dS^T (bf16 tiles)
+  const float *aux;             // [max_chunks][H] x {A (strict lower), T} written by the prep kernel
   float *dq, *dk, *dg, *dbeta;
   int *status;
 };
@@ -140,9 +125,7 @@ cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
 cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_scan_tc(const BwdScanParams &p, cudaStream_t s);
-cudaError_t launch_bwd_state(const BwdStateParams &p, bool f32, cudaStream_t s);
-cudaError_t launch_bwd_state_tc(const BwdStateParams &p, cudaStream_t s);
-cudaError_t launch_bwd_intra(const BwdIntraParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_bwd_chunk_tc(const BwdChunkParams &p, cudaStream_t s);
 cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s);
 
 // Sets the message that kda_last_error() returns on this host thread.

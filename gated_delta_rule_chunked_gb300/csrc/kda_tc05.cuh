@@ -53,6 +53,27 @@ __host__ __device__ constexpr uint32_t idesc_bf16_mn(int M, int N, bool a_mn, bo
   return idesc_bf16(M, N) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
 }
 
+// Instruction descriptor of kind::tf32: D fp32, A and B tf32 (format 2), both K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Byte offset of fp32 element (row, k) inside a K-major SW128 tile with `rows` rows:
+// 32 elements per 128-byte row, K-blocks of 32 columns.
+__host__ __device__ __forceinline__ uint32_t sw128_off32(int rows, int row, int k) {
+  return (uint32_t)((k >> 5) * rows * 128 + row * 128 + ((((k & 31) >> 2) ^ (row & 7)) << 4) + (k & 3) * 4);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T over one K = 8 step of tf32 operands (fp32 in
+// shared memory, read at tf32 precision). Issued by one thread.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T over one K = 16 step. Issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {

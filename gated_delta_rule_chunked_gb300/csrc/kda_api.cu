@@ -76,10 +76,10 @@ WsPlan plan(const kda_fwd_args *a, bool bwd) {
 
 // What kda_fwd writes to `saved` for kda_bwd, per (chunk, head), as consecutive arrays:
 // the chunk-start states (io type, S^T in the scans' operand-tile layout) and, for bf16,
-// the backward's chunk records computed once by the forward's prep: the fp32 A and T,
-// and the backward record (TcRecB: the dS scan's operands plus Kt).
+// the forward's chunk record itself (TcRec: the dS scan and the chunk-gradient kernel read
+// it MN-major where they need the transposed tiles), the fp32 A and T of the prep, and Kt.
 struct SavedPlan {
-  size_t states, aux, img2, bytes;
+  size_t states, aux, rec, kt, bytes;
 };
 
 SavedPlan saved_plan(const kda_fwd_args *a) {
@@ -90,8 +90,10 @@ SavedPlan saved_plan(const kda_fwd_args *a) {
   if (a->io_dtype != KDA_F32) {
     sp.aux = round_up(end, 256);
     end = sp.aux + n * 2 * 64 * 64 * sizeof(float);
-    sp.img2 = round_up(end, 256);
-    end = sp.img2 + n * kda::TcRecB::BYTES;
+    sp.rec = round_up(end, 256);
+    end = sp.rec + n * kda::TcRec::BYTES;
+    sp.kt = round_up(end, 256);
+    end = sp.kt + n * kda::KtRec::BYTES;
   }
   sp.bytes = round_up(end, 256);
   return sp;
@@ -207,24 +209,26 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_fwd chunk table");
   mark(0, stream);
-  // with `saved` (a training forward) the prep also writes the backward's chunk records there
+  // with `saved` (a training forward) the chunk record goes there, with the backward's
+  // extras (A, T, Kt); otherwise it lives in the workspace
   const SavedPlan sv = saved_plan(a);
   char *sd = static_cast<char *>(a->saved);
   const bool bwd_recs = !f32 && sd;
+  char *rec = bwd_recs ? sd + sv.rec : ws + w.img;
   kda::PrepParams pp{geo,
                      a->q,
                      a->k,
                      a->g,
                      a->beta,
                      a->scale,
-                     ws + w.img,
+                     rec,
                      bwd_recs ? reinterpret_cast<float *>(sd + sv.aux) : nullptr,
                      f32 ? 0 : (bwd_recs ? 3 : 1),
-                     bwd_recs ? sd + sv.img2 : nullptr,
+                     bwd_recs ? sd + sv.kt : nullptr,
                      a->dev_status};
   if ((e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
-  kda::FwdScanParams sp{geo, a->v, ws + w.img, a->h0, a->o, a->hT, a->saved, a->dev_status};
+  kda::FwdScanParams sp{geo, a->v, rec, a->h0, a->o, a->hT, a->saved, a->dev_status};
   e = f32 ? kda::launch_fwd_scan(sp, true, pick_slice(a), stream) : kda::launch_fwd_scan_tc(sp, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_fwd scan");
   mark(2, stream);
@@ -274,12 +278,12 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
   // the chunk records were written by the forward's prep into `saved`
   const SavedPlan sv = saved_plan(f);
   char *sd = static_cast<char *>(f->saved);
-  kda::BwdScanParams bp{geo, a->dO, sd + sv.img2, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
+  kda::BwdScanParams bp{geo, a->dO, sd + sv.rec, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
   if ((e = kda::launch_bwd_scan_tc(bp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd dS scan");
   mark(1, stream);
-  kda::BwdChunkParams cp{geo, f->q, f->k, f->v, a->dO, f->g, f->beta, f->scale, sd + sv.img2, sd + sv.states,
-                         ws + w.dsaved, reinterpret_cast<const float *>(sd + sv.aux), a->dq, a->dk, a->dg, a->dbeta,
-                         f->dev_status};
+  kda::BwdChunkParams cp{geo, f->q, f->k, f->v, a->dO, f->g, f->beta, f->scale, sd + sv.rec, sd + sv.kt,
+                         sd + sv.states, ws + w.dsaved, reinterpret_cast<const float *>(sd + sv.aux), a->dq, a->dk,
+                         a->dg, a->dbeta, f->dev_status};
   if ((e = kda::launch_bwd_chunk_tc(cp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd chunk grads");
   mark(2, stream);
   g_last_error.clear();

@@ -45,8 +45,8 @@ constexpr int BC_THREADS = 256;
 struct BcSmem {
   static constexpr int SS = 0, SDS = 32768;            // S^T, dS^T [v][k] bf16, K-major over k (2 blocks of 16 KB)
   static constexpr int KT = 65536;                     // Kt [tok][k] bf16 (2 blocks of 8 KB)
-  static constexpr int BMT = 81920, KH = BMT + 8192;   // Bm^T [r][j] and Kh [tok][k]: one copy from the record
-  static constexpr int TBT = 106496;                   // Tb^T [r][j] (+ e^{G_last}, unused here)
+  static constexpr int KHT = 81920, BM = KHT + 16384;  // the record's B2 tile: Kh^T [k][tok] and Bm [r][j]
+  static constexpr int TB = 106496;                    // the record's Tb [r][j] (+ e^{G_last}, unused here)
   static constexpr int V = 115712, DO = 132096;        // [tok][v] bf16, K-major over v (2 blocks of 8 KB)
   static constexpr int BAR = 148480, TSLOT = BAR + 128;
   static constexpr int TK = 149504;                    // T [m][j], then T^T [r][m]: fp32 K-major (2 blocks of 8 KB)
@@ -66,11 +66,11 @@ struct BcSmem {
   // regions reused once their first contents are consumed
   static constexpr int VPT = KT, UT = KT;              // V'^T, then U^T [v][tok] (groups A, B)
   static constexpr int DUT = V, DVT = V;               // dU^T, then dV'^T [v][tok]
-  static constexpr int DT0 = TBT, DT1 = BMT;           // dT [r][j] fp32 K-major: the two 8 KB K-blocks (group C)
+  static constexpr int DT0 = TB, DT1 = BM;             // dT [r][j] fp32 K-major: the two 8 KB K-blocks (group C)
   static constexpr int XT = SS;                        // X^T [j][m] fp32 K-major (group D)
   static constexpr int AS = DO;                        // A fp32 [64][64], 16-byte chunks XOR-swizzled by row (group D)
-  static constexpr int CSA = SS + 16384, CSB = KH;     // local gate sums (log2) of rows 0..31, 32..63: [32][128] fp32
-  static constexpr int DBM = BMT, DBMT = TBT;          // dBm [r][j], dBm^T [j][r] bf16 (rounds)
+  static constexpr int CSA = SS + 16384, CSB = KHT;    // local gate sums (log2) of rows 0..31, 32..63: [32][128] fp32
+  static constexpr int DBM = BM, DBMT = TB;            // dBm [r][j], dBm^T [j][r] bf16 (rounds)
   static constexpr int DA = V, DAT = V + 8192;         // dA [r][j], dA^T [j][r] bf16 (rounds)
   static constexpr int QLF = SDS, KLF = SDS + 16384, RF = KT;   // factor tiles [r][c] bf16 (rounds)
 };
@@ -294,14 +294,14 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
 
   // ---------------------------------------------------------------- loads
   if (tid == 0) {
-    const char *rb = (const char *)p.img + rid * TcRecB::BYTES;
+    const char *rb = (const char *)p.img + rid * TcRec::BYTES;
     fence_proxy_async();
-    mbar_expect_tx(&bar[0], 2 * 32768 + (TcRecB::QWT - TcRecB::BMT) + (TcRecB::SCAN - TcRecB::TBT) + 16384);
+    mbar_expect_tx(&bar[0], 2 * 32768 + (TcRec::TB - TcRec::B2) + (TcRec::BYTES - TcRec::TB) + KtRec::BYTES);
     bulk_g2s(smem + S::SS, (const char *)p.saved + rid * 32768, 32768, &bar[0]);
     bulk_g2s(smem + S::SDS, (const char *)p.dsaved + rid * 32768, 32768, &bar[0]);
-    bulk_g2s(smem + S::BMT, rb + TcRecB::BMT, TcRecB::QWT - TcRecB::BMT, &bar[0]);   // Bm^T, Kh
-    bulk_g2s(smem + S::TBT, rb + TcRecB::TBT, TcRecB::SCAN - TcRecB::TBT, &bar[0]);  // Tb^T, e^{G_last}
-    bulk_g2s(smem + S::KT, rb + TcRecB::KT, 16384, &bar[0]);                          // Kt
+    bulk_g2s(smem + S::KHT, rb + TcRec::B2, TcRec::TB - TcRec::B2, &bar[0]);        // Kh^T, Bm
+    bulk_g2s(smem + S::TB, rb + TcRec::TB, TcRec::BYTES - TcRec::TB, &bar[0]);      // Tb, e^{G_last}
+    bulk_g2s(smem + S::KT, (const char *)p.kt + rid * KtRec::BYTES, KtRec::BYTES, &bar[0]);   // Kt
   }
   {
     // V, dO rows into [tok][v] tiles (K-major over v, 128-byte swizzle); rows past the end are zero
@@ -354,20 +354,20 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
   tc::fence_after();
 
   const uint32_t s_ss = smem_u32(smem + S::SS), s_sds = smem_u32(smem + S::SDS), s_kt = smem_u32(smem + S::KT),
-                 s_bmt = smem_u32(smem + S::BMT), s_kh = smem_u32(smem + S::KH), s_tbt = smem_u32(smem + S::TBT),
-                 s_v = smem_u32(smem + S::V), s_do = smem_u32(smem + S::DO);
-  (void)s_v;
+                 s_bm = smem_u32(smem + S::BM), s_kht = smem_u32(smem + S::KHT), s_tb = smem_u32(smem + S::TB),
+                 s_do = smem_u32(smem + S::DO);
 
   // ---------------------------------------------------------------- group A
   if (tid == 0) {
     // (Kt S)^T [v][j] = S^T Kt^T; V'^T = V^T - (Kt S)^T in the epilogue
     for (int ks = 0; ks < 8; ++ks)
       tc::mma_bf16(tmem + T_VP, kmaj(s_ss, ks, 16384), kmaj(s_kt, ks, 8192), tc::idesc_bf16(128, 64), ks > 0);
-    // dU^T [v][r] = dO^T Bm + dS^T Kh^T
+    // dU^T [v][j] = dO^T Bm + dS^T Kh^T: B(n = j, k = r) = Bm[r][j] and B(n = j, k = dk) = Kh^T[dk][j],
+    // both rows k of the record's tiles -> MN-major
     for (int ks = 0; ks < 4; ++ks)
-      tc::mma_bf16(tmem + T_DU, mnmaj(s_do, ks, 8192), kmaj(s_bmt, ks, 0), tc::idesc_bf16_mn(128, 64, true, false), ks > 0);
+      tc::mma_bf16(tmem + T_DU, mnmaj(s_do, ks, 8192), mnmaj(s_bm, ks, 8192), tc::idesc_bf16_mn(128, 64, true, true), ks > 0);
     for (int ks = 0; ks < 8; ++ks)
-      tc::mma_bf16(tmem + T_DU, kmaj(s_sds, ks, 16384), kmaj(s_kh, ks, 8192), tc::idesc_bf16(128, 64), 1);
+      tc::mma_bf16(tmem + T_DU, kmaj(s_sds, ks, 16384), mnmaj(s_kht, ks, 8192), tc::idesc_bf16_mn(128, 64, false, true), 1);
     // dQt^T [k][r] = S dO^T: A = S (k rows) MN-major over S^T, B = dO [r][v] K-major
     for (int ks = 0; ks < 8; ++ks)
       tc::mma_bf16(tmem + T_DQ, mnmaj(s_ss, ks, 16384), kmaj(s_do, ks, 8192), tc::idesc_bf16_mn(128, 64, true, false), ks > 0);
@@ -478,12 +478,12 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
   // ---------------------------------------------------------------- group B
   const uint32_t s_vpt = smem_u32(smem + S::VPT), s_dut = smem_u32(smem + S::DUT);
   if (tid == 0) {
-    // U^T [v][r] = V'^T Tb^T: B(n = r, k = j) = Tb[r][j] = Tb^T tile[j][r] -> MN-major
+    // U^T [v][r] = V'^T Tb^T: B(n = r, k = j) = Tb[r][j] -> K-major
     for (int ks = 0; ks < 4; ++ks)
-      tc::mma_bf16(tmem + T_U, kmaj(s_vpt, ks, 0), mnmaj(s_tbt, ks, 8192), tc::idesc_bf16_mn(128, 64, false, true), ks > 0);
-    // dV'^T [v][j] = dU^T Tb: B(n = j, k = r) = Tb[r][j] = Tb^T tile[j][r] -> K-major
+      tc::mma_bf16(tmem + T_U, kmaj(s_vpt, ks, 0), kmaj(s_tb, ks, 0), tc::idesc_bf16(128, 64), ks > 0);
+    // dV'^T [v][j] = dU^T Tb: B(n = j, k = r) = Tb[r][j] -> MN-major
     for (int ks = 0; ks < 4; ++ks)
-      tc::mma_bf16(tmem + T_DV, kmaj(s_dut, ks, 0), kmaj(s_tbt, ks, 0), tc::idesc_bf16(128, 64), ks > 0);
+      tc::mma_bf16(tmem + T_DV, kmaj(s_dut, ks, 0), mnmaj(s_tb, ks, 8192), tc::idesc_bf16_mn(128, 64, false, true), ks > 0);
     // dTb [r][j] = dU V'^T (M = 64): A(m = r, k = v) = dU^T tile[v][r], B(n = j, k = v) = V'^T tile[v][j]
     for (int ks = 0; ks < 8; ++ks)
       tc::mma_bf16(tmem + T_DTB, mnmaj(s_dut, ks, 8192), mnmaj(s_vpt, ks, 8192), tc::idesc_bf16_mn(64, 64, true, true), ks > 0);
@@ -607,13 +607,21 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
               __float2bfloat16_rn(x8[e]);
       }
     }
-    // sum_r dKh_rc Kh_rc (the e^{G_last} term of dg through Kh), over this warp's 32 rows
+    // sum_r dKh_rc Kh_rc (the e^{G_last} term of dg through Kh), over this warp's 32 rows:
+    // row c of the Kh^T tile, 16-byte chunks
     ld32(tl + T_DKH + 32 * hf, v);
     tc::wait_ld();
     float cs = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      cs = fmaf(v[i], to_f(*reinterpret_cast<const bf16 *>(smem + S::KH + tc::sw128_off(64, 32 * hf + i, row))), cs);
+    for (int cb = 0; cb < 4; ++cb) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(smem + S::KHT + tc::sw128_off(128, row, 32 * hf + 8 * cb));
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv[e]));
+        cs = fmaf(v[8 * cb + 2 * e], kk.x, fmaf(v[8 * cb + 2 * e + 1], kk.y, cs));
+      }
+    }
     reinterpret_cast<float *>(smem + S::CSUM)[hf * 128 + row] = cs;
     // X -> X^T [j][m] (fp32 K-major over m) over the dead S^T tile
     ld32(tl + T_X + 32 * hf, v);

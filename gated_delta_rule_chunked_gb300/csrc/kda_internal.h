@@ -39,17 +39,12 @@ struct TcRec {
   static constexpr int B1 = 0, B2 = 32768, TB = B2 + 24576, GC = TB + 8192, BYTES = GC + 512;
 };
 
-// Per-(chunk, head) backward record (bf16), same format; the dS scan copies the
-// first SCAN bytes, the state kernel BMT, KH, TBT, GC and KT:
-//   BMT [64 rows r][K = 64 j] : Bm^T (Bm[j][r])
-//   KH  [64 rows tok][K = 128]: Kh[tok][dk]
-//   QWT [128 rows dk][K = 128]: K < 64: Qt^T[dk][tok], K >= 64: -W^T[dk][tok]
-//   TBT [64 rows r][K = 64 j] : Tb^T (Tb[j][r])
-//   GC  128 fp32              : exp(G_last)
-//   KT  [64 rows tok][K = 128]: Kt[tok][dk]
-struct TcRecB {
-  static constexpr int BMT = 0, KH = 8192, QWT = KH + 16384, TBT = QWT + 32768, GC = TBT + 8192, SCAN = GC + 512;
-  static constexpr int KT = (SCAN + 1023) / 1024 * 1024, BYTES = KT + 16384;
+// Per-(chunk, head) Kt tile for the backward (bf16, training forward only): Kt[tok][dk]
+// in the same K-major 128-byte-swizzle layout (two 8 KB blocks). Everything else the
+// backward reads per chunk is in the forward record (TcRec), read MN-major where a
+// product needs the other orientation.
+struct KtRec {
+  static constexpr int BYTES = 64 * 128 * 2;
 };
 
 struct SeqGeom {
@@ -69,8 +64,8 @@ struct PrepParams {
   void *img;               // [max_chunks][H] forward records: TcRec (bf16) or the tile record (fp32)
   float *aux;              // [max_chunks][H] x {A (strict lower), T} fp32 64x64 each, or NULL
   int tc_layout;           // bf16: bit 0 = write the tcgen05 forward record to img;
-                           //       bit 1 = write the backward records: TcRecB and aux
-  void *img2;              // [max_chunks][H] TcRecB records (bit 1)
+                           //       bit 1 = write the backward extras: Kt (img2) and aux
+  void *img2;              // [max_chunks][H] KtRec tiles (bit 1)
   int *status;
 };
 
@@ -89,7 +84,7 @@ struct FwdScanParams {
 struct BwdScanParams {
   SeqGeom geo;
   const void *dO;
-  const void *img;         // TcRecB records for the tcgen05 scan, ImgLayout records otherwise
+  const void *img;         // TcRec records (the forward's)
   const float *dhT;
   float *dv;
   float *dh0;
@@ -102,7 +97,8 @@ struct BwdChunkParams {
   const void *q, *k, *v, *dO;   // io type (bf16)
   const float *g, *beta;
   float scale;
-  const void *img;              // [max_chunks][H] TcRecB records
+  const void *img;              // [max_chunks][H] TcRec records (the forward's)
+  const void *kt;               // [max_chunks][H] KtRec tiles
   const void *saved, *dsaved;   // [max_chunks][H] chunk-start states S^T, chunk-end dS^T (bf16 tiles)
   const float *aux;             // [max_chunks][H] x {A (strict lower), T} written by the prep kernel
   float *dq, *dk, *dg, *dbeta;

@@ -90,8 +90,7 @@ struct PrepSmem2 {
   static constexpr int LM = QL;                              // fp32 [64][LDS64]  Diag(beta) A
   static constexpr int TT = LM + 64 * LDS64 * 4;             // fp32 [64][LDS64]  T, then T Diag(beta)
   static constexpr int SCR = TT + 64 * LDS64 * 4;            // fp32 4 x [16][LDP]
-  static constexpr int BMS = SCR + 4 * 16 * LDP * 4;         // bf16 [64][64] Bm staging (backward record)
-  static_assert(BMS + 64 * 64 * 2 <= DV, "solver tiles overlap the vectors");
+  static_assert(SCR + 4 * 16 * LDP * 4 <= DV, "solver tiles overlap the vectors");
 };
 
 __device__ __forceinline__ void pair_of(int p, int &a, int &b) {
@@ -189,7 +188,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
   // tcgen05 record (bf16 forward) or the tile record (fp32 forward, backward)
   const bool tcrec = !PRECISE && (p.tc_layout & 1);   // forward tcgen05 record
-  const bool bwdrec = !PRECISE && (p.tc_layout & 2);  // backward records: TcRecB, A and T
+  const bool bwdrec = !PRECISE && (p.tc_layout & 2);  // backward extras: Kt, A and T
   const E *qg = (const E *)p.q, *kg = (const E *)p.k;
   float *rq = (float *)(smem + S::RQ), *rk = (float *)(smem + S::RK), *sb = (float *)(smem + S::BETA);
   float *KL = (float *)(smem + S::KL), *QL = (float *)(smem + S::QL), *RR = (float *)(smem + S::R);
@@ -200,7 +199,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   const size_t rid = (size_t)chunk * H + h;
   char *rec = tcrec ? (char *)p.img + rid * TcRec::BYTES : nullptr;                       // forward tcgen05 record
   char *trec = PRECISE ? (char *)p.img + rid * L.bytes : nullptr;                         // fp32 tile record
-  char *recb = bwdrec ? (char *)p.img2 + rid * TcRecB::BYTES : nullptr;
+  char *recb = bwdrec ? (char *)p.img2 + rid * KtRec::BYTES : nullptr;
 
   // 0. stage the chunk's q, k (io type) and g (fp32) in shared memory with one batch of
   //    asynchronous copies: q in the KL tile, k in the R tile, g in the QL tile (row
@@ -298,7 +297,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
     pvv[a][c0] = pa0;
     pvv[a][c0 + 1] = pa1;
     Tile<E, 128> tqt((E *)(trec + L.qt)), tkt((E *)(trec + L.kt)), tkh((E *)(trec + L.kh));
-    float kh0v[SUB], kh1v[SUB], qt0v[SUB], qt1v[SUB];
+    float kh0v[SUB], kh1v[SUB];
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
@@ -316,28 +315,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       if (tcrec)   // B1 rows 0..63: Qt[tok][dk] = q^ exp(G_r)
         st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, r, c0)), ql0 * pa0, ql1 * pa1);
       if (trec) {
-        if (!bwdrec) st2(tqt.at(r, c0), ql0 * pa0, ql1 * pa1);   // Qt = q^ exp(G_r) (unused by the backward)
+        st2(tqt.at(r, c0), ql0 * pa0, ql1 * pa1);                 // Qt = q^ exp(G_r)
         st2(tkt.at(r, c0), kl0 * pa0, kl1 * pa1);                 // Kt = k^ exp(G_r)
         st2(tkh.at(r, c0), kh0v[i], kh1v[i]);
       }
-      if (bwdrec) {
-        st2((E *)(recb + TcRecB::KH + tc::sw128_off(64, r, c0)), kh0v[i], kh1v[i]);
-        st2((E *)(recb + TcRecB::KT + tc::sw128_off(64, r, c0)), kl0 * pa0, kl1 * pa1);
-      }
-      qt0v[i] = ql0 * pa0;
-      qt1v[i] = ql1 * pa1;
-    }
-    if (bwdrec) {
-      // QWT rows dk, K-block 0: Qt^T[dk][tok] for this thread's 16 tokens
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int k0 = a * SUB + 8 * half;
-        float t0[8], t1[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { t0[i] = qt0v[8 * half + i]; t1[i] = qt1v[8 * half + i]; }
-        *reinterpret_cast<uint4 *>(recb + TcRecB::QWT + tc::sw128_off(128, c0, k0)) = tc::pack8(t0);
-        *reinterpret_cast<uint4 *>(recb + TcRecB::QWT + tc::sw128_off(128, c0 + 1, k0)) = tc::pack8(t1);
-      }
+      if (bwdrec) st2((E *)(recb + tc::sw128_off(64, r, c0)), kl0 * pa0, kl1 * pa1);   // Kt[tok][dk]
     }
     if (tcrec) {
       // B2 rows 0..127: Kh^T[dk][tok]; this thread holds 16 tokens of channels c0, c0 + 1
@@ -355,7 +337,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       const float2 gc = make_float2(exp2f(e3[0]), exp2f(e3[1]));
       if (tcrec) *reinterpret_cast<float2 *>(rec + TcRec::GC + c0 * 4) = gc;
       if (trec) *reinterpret_cast<float2 *>(trec + L.gc + c0 * 4) = gc;
-      if (bwdrec) *reinterpret_cast<float2 *>(recb + TcRecB::GC + c0 * 4) = gc;
     }
   }
   __syncthreads();
@@ -393,7 +374,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
             const float b0 = j <= r ? v0 : 0.f, b1 = j + 1 <= r ? v1 : 0.f;
             if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), b0, b1);
             if (trec) st2(bm.at(r, j), b0, b1);
-            if (bwdrec) st2((E *)(smem + S::BMS) + r * 64 + j, b0, b1);   // staged, transposed below
           } else {
             const float a0 = j < r ? v0 : 0.f, a1 = j + 1 < r ? v1 : 0.f;
             *reinterpret_cast<float2 *>(Lm + r * LDS64 + j) = make_float2(sb[r] * a0, sb[r] * a1);
@@ -407,7 +387,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       if ((j >> 4) > (r >> 4)) {
         if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), 0.f, 0.f);
         if (trec) st2(bm.at(r, j), 0.f, 0.f);
-        if (bwdrec) st2((E *)(smem + S::BMS) + r * 64 + j, 0.f, 0.f);
       }
     }
   }
@@ -438,7 +417,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
         const int r = idx >> 6, j = idx & 63;
         if ((j >> 4) > (r >> 4)) T[r * LDS64 + j] = 0.f;
       }
-      if (tcrec || bwdrec) {
+      if (tcrec) {
         for (int idx = tid - 128; idx < 64 * 64; idx += 128) {
           const int r = idx >> 6, c = (idx & 63) * 2;
           float2 *kp = reinterpret_cast<float2 *>(KL + r * LDF + c);
@@ -488,7 +467,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
       const float b0 = t0 * sb[j], b1 = t1 * sb[j + 1];
       if (tcrec) st2((E *)(rec + TcRec::TB + tc::sw128_off(64, r, j)), b0, b1);
       if (trec) st2(tb.at(r, j), b0, b1);
-      if (tcrec || bwdrec) *reinterpret_cast<float2 *>(T + r * LDS64 + j) = make_float2(b0, b1);
+      if (tcrec) *reinterpret_cast<float2 *>(T + r * LDS64 + j) = make_float2(b0, b1);
       if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(t0, t1);
     }
   }
@@ -520,44 +499,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
           const int r = 16 * mt + g + 8 * hh, c = n0 + 8 * nt + 2 * q;
           st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, 64 + r, c)), -wacc[nt][2 * hh], -wacc[nt][2 * hh + 1]);
         }
-    }
-  }
-  if (bwdrec) {
-    __syncthreads();
-    // 6'. backward record: -W^T = -(Kt^T Tb^T) (128 x 64) into QWT K-block 1 (warp w: rows dk 16w..16w+15);
-    //     Bm^T and Tb^T as 16-byte chunks from shared memory.
-    const float *Tb = (const float *)(smem + S::TT);
-    float wacc[8][4];
-    zero(wacc);
-    for (int kk = 0; kk < 64; kk += 8) {
-      uint32_t af[4];   // A(m = dk, k = j) = Kt[j][dk]
-      af[0] = tf32(KL[(kk + q) * LDF + 16 * warp + g]);
-      af[1] = tf32(KL[(kk + q) * LDF + 16 * warp + g + 8]);
-      af[2] = tf32(KL[(kk + q + 4) * LDF + 16 * warp + g]);
-      af[3] = tf32(KL[(kk + q + 4) * LDF + 16 * warp + g + 8]);
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt)   // B(k = j, n = r) = Tb[r][j]
-        if (kk <= 8 * nt + 7)
-          mma1688(wacc[nt], af, tf32(Tb[(8 * nt + g) * LDS64 + kk + q]), tf32(Tb[(8 * nt + g) * LDS64 + kk + q + 4]));
-    }
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int c = 16 * warp + g + 8 * hh, r = 8 * nt + 2 * q;
-        st2((E *)(recb + TcRecB::QWT + tc::sw128_off(128, c, 64 + r)), -wacc[nt][2 * hh], -wacc[nt][2 * hh + 1]);
-      }
-    // Bm^T and Tb^T: one 16-byte chunk (row n, columns 8c..8c+7) per thread and tile
-    for (int idx = tid; idx < 64 * 8; idx += PREP_THREADS) {
-      const int n = idx & 63, c = idx >> 6;
-      float bv[8], tv[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        bv[e] = to_f(*((const E *)(smem + S::BMS) + (8 * c + e) * 64 + n));   // Bm[k][n]
-        tv[e] = Tb[(8 * c + e) * LDS64 + n];                                   // Tb[k][n]
-      }
-      *reinterpret_cast<uint4 *>(recb + TcRecB::BMT + tc::sw128_off(64, n, 8 * c)) = tc::pack8(bv);
-      *reinterpret_cast<uint4 *>(recb + TcRecB::TBT + tc::sw128_off(64, n, 8 * c)) = tc::pack8(tv);
     }
   }
 }

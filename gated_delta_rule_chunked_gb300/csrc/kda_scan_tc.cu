@@ -322,8 +322,9 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
 // ----------------------------------------------------------------- backward
 // Reverse dS scan, same arrangement (4 state warps, 4 io warps staging dO^T and
 // writing dv): dS^T in TMEM columns [0,128), dU^T in
-// [128,192), dV^T in [192,256). Per chunk (last to first), with the backward
-// record (Bm^T, Kh, [Qt^T | -W^T], Tb^T, gC):
+// [128,192), dV^T in [192,256). Per chunk (last to first), with the forward's record
+// read MN-major (its [Qt; -W], [Kh^T; Bm] and Tb tiles are the transposes of what the
+// products here take K-major):
 //   pass A : dS^T -> bf16 operand tile (saved as the chunk-end dS by one bulk copy);
 //            dS^T <- dS^T Diag(gC); dO^T -> operand tile (K-block 0 of A2)
 //   phase 1: dU^T  = dO^T Bm + dS^T Kh^T           (M=128, N=64, K=64 + 128)
@@ -332,7 +333,7 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
 //            dV^T  = dU^T Tb                        (M=128, N=64,  K=64)
 // i.e. dU = Bm^T dO + Kh dS, dS <- gC*dS + Qt^T dO - W^T dU, dv = Tb^T dU.
 struct TcBwdSmem {
-  static constexpr int RECS = (TcRecB::SCAN + 1023) / 1024 * 1024;
+  static constexpr int RECS = (TcRec::BYTES + 1023) / 1024 * 1024;
   static constexpr int REC0 = 0, REC1 = RECS;
   static constexpr int AS = 2 * RECS;        // dS^T bf16 [128][K=128]
   static constexpr int A2 = AS + 32768;      // [dO^T | dU^T] bf16 [128][K=128]
@@ -371,15 +372,15 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
   tc::fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t tl = tmem + ((uint32_t)(32 * qw) << 16);
-  auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * TcRecB::BYTES; };
+  auto rec_of = [&](int j) { return (const char *)p.img + ((size_t)(cbase + j) * H + h) * TcRec::BYTES; };
 
   bool ok = true;
   if (!io) {
     // ------------------------------------------------------------ state warps
     auto issue = [&](char *dst, const char *src, uint64_t *b) {
       fence_proxy_async();
-      mbar_expect_tx(b, TcRecB::SCAN);
-      bulk_g2s(dst, src, TcRecB::SCAN, b);
+      mbar_expect_tx(b, TcRec::BYTES);
+      bulk_g2s(dst, src, TcRec::BYTES, b);
     };
     // initial dS^T[dv][dk] = dhT[dk][dv]
     {
@@ -393,7 +394,6 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
       tc::wait_st();
     }
     const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS)), d_a2 = tc::desc_sw128(smem_u32(smem + S::A2));
-    const uint64_t d_rec0 = tc::desc_sw128(smem_u32(smem + S::REC0)), d_rec1 = tc::desc_sw128(smem_u32(smem + S::REC1));
     if (tid == 0 && nch > 0) {
       issue(smem + S::REC0, rec_of(nch - 1), &bar[0]);
       if (nch > 1) issue(smem + S::REC1, rec_of(nch - 2), &bar[1]);
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
         issue(smem + ((it + 1) & 1 ? S::REC1 : S::REC0), rec_of(j - 1), &bar[(it + 1) & 1]);
       // pass A: dS^T -> operand tile, decayed dS^T back to TMEM
       {
-        const float *gC = reinterpret_cast<const float *>(rb + TcRecB::GC);
+        const float *gC = reinterpret_cast<const float *>(rb + TcRec::GC);
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
           uint32_t r[64];
@@ -440,16 +440,19 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
         tc::fence_after();
         ok &= ready;
         if (ready) {
-          const uint64_t d_rb = b ? d_rec1 : d_rec0, d_bmt = d_rb + (TcRecB::BMT >> 4), d_kh = d_rb + (TcRecB::KH >> 4);
+          // B(n = j, k = r) = Bm[r][j]: rows r of the record's Bm tile -> MN-major
+          const uint32_t s_b2 = smem_u32(rb) + TcRec::B2;
+          constexpr uint32_t idn = tc::idesc_bf16_mn(128, 64, false, true);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + 128, d_a2 + 2 * ks, d_bmt + 2 * ks, tc::idesc_bf16(128, 64), ks > 0);
+            tc::mma_bf16(tmem + 128, d_a2 + 2 * ks, tc::desc_sw128_mn(s_b2 + 16384 + 2048 * ks, 8192), idn, ks > 0);
+          // B(n = j, k = dk) = Kh[j][dk] = Kh^T rows dk -> MN-major
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              tc::mma_bf16(tmem + 128, d_as + ((kb * 16384 + 32 * ks) >> 4), d_kh + ((kb * 8192 + 32 * ks) >> 4),
-                           tc::idesc_bf16(128, 64), 1);
+              tc::mma_bf16(tmem + 128, d_as + ((kb * 16384 + 32 * ks) >> 4),
+                           tc::desc_sw128_mn(s_b2 + 8192 * kb + 2048 * ks, 8192), idn, 1);
           tc::commit(&bar[2]);
         }
       } else if (tid == 32) {
@@ -482,17 +485,21 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
         tc::fence_after();
         ok &= freed;
         if (freed) {
-          const uint64_t d_rb = b ? d_rec1 : d_rec0, d_qwt = d_rb + (TcRecB::QWT >> 4), d_tbt = d_rb + (TcRecB::TBT >> 4);
+          // B(n = dk, k = tok) = [Qt; -W][tok][dk]: rows tok of the record's B1 tile -> MN-major,
+          // two 64-channel atoms 16 KB apart
+          const uint32_t s_rb = smem_u32(rb);
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint32_t off = (kb * 16384 + 32 * ks) >> 4;
-              tc::mma_bf16(tmem, d_a2 + off, d_qwt + off, tc::idesc_bf16(128, 128), 1);
-            }
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_bf16(tmem, d_a2 + ((kb * 16384 + 32 * ks) >> 4),
+                           tc::desc_sw128_mn(s_rb + TcRec::B1 + 8192 * kb + 2048 * ks, 16384),
+                           tc::idesc_bf16_mn(128, 128, false, true), 1);
+          // B(n = j, k = r) = Tb[r][j]: rows r of the record's Tb tile -> MN-major
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + 192, d_a2 + (16384 >> 4) + 2 * ks, d_tbt + 2 * ks, tc::idesc_bf16(128, 64), ks > 0);
+            tc::mma_bf16(tmem + 192, d_a2 + (16384 >> 4) + 2 * ks, tc::desc_sw128_mn(s_rb + TcRec::TB + 2048 * ks, 8192),
+                         tc::idesc_bf16_mn(128, 64, false, true), ks > 0);
           tc::commit(&bar[3]);
         }
       }

@@ -83,9 +83,9 @@ typedef struct {
     void *o;                   /* out [total, H, dv]                                     */
     float *hT;                 /* out [N, H, dk, dv] final states, or NULL               */
     void *saved;               /* out, kda_saved_size() bytes: what kda_bwd needs from this
-                                  forward (chunk-start states; for bf16 also the chunk
-                                  records of the backward, computed in the same pass), or
-                                  NULL when no backward follows                           */
+                                  forward (chunk-start states; for bf16 also the forward's
+                                  chunk records and the prep's A, T and Kt tiles, computed
+                                  in the same pass), or NULL when no backward follows     */
     void *workspace;           /* scratch, kda_fwd_workspace_size() bytes                */
     size_t workspace_bytes;
     int32_t *dev_status;       /* optional device int32, see above                       */
@@ -135,8 +135,8 @@ typedef struct {
 kda_status kda_fwd(const kda_fwd_args *args, cudaStream_t stream);
 size_t kda_fwd_workspace_size(const kda_fwd_args *args);
 /* Bytes that kda_fwd writes to args->saved for kda_bwd: per (chunk, head) the
- * chunk-start state (io type) and, for bf16 I/O, the backward's chunk records
- * (about 113 KB more per chunk and head). */
+ * chunk-start state (io type) and, for bf16 I/O, the forward's chunk record with the
+ * prep's A, T and Kt tiles (about 113 KB more per chunk and head). */
 size_t kda_saved_size(const kda_fwd_args *args);
 
 /* kda_bwd -- gradients for q, k, v, beta, g and the initial state (the pages

@@ -7,6 +7,7 @@
 //   kda_bwd:  chunk table -> reverse dS scan -> chunk gradients (one tcgen05 kernel
 //             per chunk and head; the chunk records come from the forward's prep)
 //   kda_step: one decode kernel.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -72,6 +73,51 @@ WsPlan plan(const kda_fwd_args *a, bool bwd) {
   }
   w.bytes = round_up(end, 256);
   return w;
+}
+
+// TMA tensor maps (the driver's cuTensorMapEncodeTiled, reached through the runtime).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;   // a racing second lookup stores the same pointer
+  if (!fn) {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// Token-major [total][H][128] tensor as a 3D map (channel, head, token) with a box of
+// box_c channels x 1 head x 64 tokens; 128-byte swizzle when `swz`.
+bool map_tokens(CUtensorMap *m, const void *base, bool f32, long long total, int H, int box_c, bool swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t esz = f32 ? 4 : 2;
+  const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)total};
+  const cuuint64_t strides[2] = {128 * esz, (cuuint64_t)H * 128 * esz};
+  const cuuint32_t box[3] = {(cuuint32_t)box_c, 1, 64}, estr[3] = {1, 1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The prep's fp32 {A, T} array ([items][2][64][64]) as [items * 128 rows][64], box 32 x 64 with the
+// 128-byte swizzle: one box is one K-block of a K-major tf32 operand tile.
+bool map_aux(CUtensorMap *m, const void *base, size_t items) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {64, (cuuint64_t)items * 128};
+  const cuuint64_t strides[1] = {64 * 4};
+  const cuuint32_t box[2] = {32, 64}, estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // What kda_fwd writes to `saved` for kda_bwd, per (chunk, head), as consecutive arrays:
@@ -269,21 +315,44 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
     return KDA_OK;
   }
   char *ws = static_cast<char *>(a->workspace);
+  // the chunk records were written by the forward's prep into `saved`
+  const SavedPlan sv = saved_plan(f);
+  char *sd = static_cast<char *>(f->saved);
+  kda::BwdChunkParams cp{};
+  const long long T = f->total_tokens;
+  if (!map_tokens(&cp.tm_q, f->q, false, T, f->heads, 128, false) ||
+      !map_tokens(&cp.tm_k, f->k, false, T, f->heads, 128, false) ||
+      !map_tokens(&cp.tm_v, f->v, false, T, f->heads, 128, false) ||
+      !map_tokens(&cp.tm_do, a->dO, false, T, f->heads, 64, true) ||
+      !map_aux(&cp.tm_aux, sd + sv.aux, (size_t)max_chunks(f) * f->heads))
+    return fail(KDA_ERR_CUDA, "%s: could not encode the TMA tensor maps", "kda_bwd");
   kda::SeqGeom geo = geom(f, ws, w);
   cudaError_t e = kda::launch_chunk_table(f->cu_seqlens, f->n_seqs, f->total_tokens,
                                           reinterpret_cast<int *>(ws + w.cu), reinterpret_cast<int *>(ws + w.choff),
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_bwd chunk table");
   mark(0, stream);
-  // the chunk records were written by the forward's prep into `saved`
-  const SavedPlan sv = saved_plan(f);
-  char *sd = static_cast<char *>(f->saved);
   kda::BwdScanParams bp{geo, a->dO, sd + sv.rec, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
   if ((e = kda::launch_bwd_scan_tc(bp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd dS scan");
   mark(1, stream);
-  kda::BwdChunkParams cp{geo, f->q, f->k, f->v, a->dO, f->g, f->beta, f->scale, sd + sv.rec, sd + sv.kt,
-                         sd + sv.states, ws + w.dsaved, reinterpret_cast<const float *>(sd + sv.aux), a->dq, a->dk,
-                         a->dg, a->dbeta, f->dev_status};
+  cp.geo = geo;
+  cp.q = f->q;
+  cp.k = f->k;
+  cp.v = f->v;
+  cp.dO = a->dO;
+  cp.g = f->g;
+  cp.beta = f->beta;
+  cp.scale = f->scale;
+  cp.img = sd + sv.rec;
+  cp.kt = sd + sv.kt;
+  cp.saved = sd + sv.states;
+  cp.dsaved = ws + w.dsaved;
+  cp.aux = reinterpret_cast<const float *>(sd + sv.aux);
+  cp.dq = a->dq;
+  cp.dk = a->dk;
+  cp.dg = a->dg;
+  cp.dbeta = a->dbeta;
+  cp.status = f->dev_status;
   if ((e = kda::launch_bwd_chunk_tc(cp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd chunk grads");
   mark(2, stream);
   g_last_error.clear();

@@ -47,7 +47,8 @@ struct BcSmem {
   static constexpr int KT = 65536;                     // Kt [tok][k] bf16 (2 blocks of 8 KB)
   static constexpr int KHT = 81920, BM = KHT + 16384;  // the record's B2 tile: Kh^T [k][tok] and Bm [r][j]
   static constexpr int TB = 106496;                    // the record's Tb [r][j] (+ e^{G_last}, unused here)
-  static constexpr int V = 115712, DO = 132096;        // [tok][v] bf16, K-major over v (2 blocks of 8 KB)
+  static constexpr int V = 115712;                     // V [tok][v] bf16, plain 256-byte rows
+  static constexpr int DO = 132096;                    // dO [tok][v] bf16, K-major over v (2 blocks of 8 KB)
   static constexpr int BAR = 148480, TSLOT = BAR + 128;
   static constexpr int TK = 149504;                    // T [m][j], then T^T [r][m]: fp32 K-major (2 blocks of 8 KB)
   static constexpr int QR = TK + 16384, KR = QR + 16384;   // raw q, k [64][128] bf16 rows
@@ -68,7 +69,7 @@ struct BcSmem {
   static constexpr int DUT = V, DVT = V;               // dU^T, then dV'^T [v][tok]
   static constexpr int DT0 = TB, DT1 = BM;             // dT [r][j] fp32 K-major: the two 8 KB K-blocks (group C)
   static constexpr int XT = SS;                        // X^T [j][m] fp32 K-major (group D)
-  static constexpr int AS = DO;                        // A fp32 [64][64], 16-byte chunks XOR-swizzled by row (group D)
+  static constexpr int AS = DO;                        // A fp32 [64][64] in the layout of T (group D)
   static constexpr int CSA = SS + 16384, CSB = KHT;    // local gate sums (log2) of rows 0..31, 32..63: [32][128] fp32
   static constexpr int DBM = BM, DBMT = TB;            // dBm [r][j], dBm^T [j][r] bf16 (rounds)
   static constexpr int DA = V, DAT = V + 8192;         // dA [r][j], dA^T [j][r] bf16 (rounds)
@@ -110,9 +111,6 @@ __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int ks, uint32_t lbo) {
   return tc::desc_sw128_mn(base + 2048u * (uint32_t)ks, lbo);
 }
 
-// fp32 element (r, j) of the A tile: row r, 16-byte chunk j/4 at chunk (j/4) ^ (r % 16)
-__device__ __forceinline__ int as_off(int r, int j) { return r * 64 + 4 * (((j >> 2) ^ r) & 15) + (j & 3); }
-
 struct RoundCtx {
   const BwdChunkParams *p;
   const ChunkRef *ref;
@@ -146,35 +144,43 @@ __device__ __forceinline__ void round_epilogue(RoundCtx &x, const int t, uint32_
   const float(*dvp)[128] = (const float(*)[128])(x.smem + S::DV);
   const float *rq0 = (const float *)(x.smem + S::RQ0), *rk = (const float *)(x.smem + S::RK);
   const float pa = pv[t][c], fa = fv[t][c], tt = tot[t][c];
-  // tensor memory: pair products, scaled by the pair factors as they are summed
-  float tq[8], tk[8], tw[8], gq[8], gk[8], gh[8];
+  // tensor memory: the round's pair products (t + 6 blocks of 8 columns for this thread) and
+  // dQt^T, dKt^T, dKh^T, issued together (warp-uniform predicates) with one wait
+  float pp[NSUB][8], pq[NSUB][8], pw[NSUB][8], gq[8], gk[8], gh[8];
   ld8(x.tl + T_DQ + 16 * t + 8 * hf, gq);
   ld8(x.tl + T_DKT + 16 * t + 8 * hf, gk);   // holds -dKt^T
   ld8(x.tl + T_DKH + 16 * t + 8 * hf, gh);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) tq[i] = tk[i] = tw[i] = 0.f;
-#pragma unroll 1
-  for (int b = 0; b <= t; ++b) {
-    float pp[8], pq[8];
-    ld8(x.tl + base + 16 * b + 8 * hf, pp);
-    ld8(x.tl + base + 16 * (t + 1) + 16 * b + 8 * hf, pq);
-    tc::wait_ld();
-    const float d = dvp[t * (t + 1) / 2 + b][c];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      tq[i] = fmaf(d, pp[i], tq[i]);
-      tk[i] = fmaf(d, pq[i], tk[i]);
+  for (int b = 0; b < NSUB; ++b)
+    if (b <= t) {
+      ld8(x.tl + base + 16 * b + 8 * hf, pp[b]);
+      ld8(x.tl + base + 16 * (t + 1) + 16 * b + 8 * hf, pq[b]);
     }
-  }
-#pragma unroll 1
-  for (int aa = t; aa < NSUB; ++aa) {
-    float pw[8];
-    ld8(x.tl + base + 32 * (t + 1) + 16 * (aa - t) + 8 * hf, pw);
-    tc::wait_ld();
-    const float d = dvp[aa * (aa + 1) / 2 + t][c];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) tw[i] = fmaf(d, pw[i], tw[i]);
-  }
+  for (int aa = 0; aa < NSUB; ++aa)
+    if (aa >= t) ld8(x.tl + base + 32 * (t + 1) + 16 * (aa - t) + 8 * hf, pw[aa]);
+  tc::wait_ld();
+  // pair products scaled by the pair factors as they are summed
+  float tq[8], tk[8], tw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tq[i] = tk[i] = tw[i] = 0.f;
+#pragma unroll
+  for (int b = 0; b < NSUB; ++b)
+    if (b <= t) {
+      const float d = dvp[t * (t + 1) / 2 + b][c];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        tq[i] = fmaf(d, pp[b][i], tq[i]);
+        tk[i] = fmaf(d, pq[b][i], tk[i]);
+      }
+    }
+#pragma unroll
+  for (int aa = 0; aa < NSUB; ++aa)
+    if (aa >= t) {
+      const float d = dvp[aa * (aa + 1) / 2 + t][c];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) tw[i] = fmaf(d, pw[aa][i], tw[i]);
+    }
   // per row: factor values in fp32, factor-tile gradients, dq^, dk^, dG
   const int len = x.ref->len;
   const long long t0 = x.ref->t0;
@@ -229,11 +235,24 @@ __device__ __forceinline__ void round_epilogue(RoundCtx &x, const int t, uint32_
   named_sync(1 + hf, 128);
   float *xs = (float *)(x.smem + S::XS);
   float sdg = 0.f;
+  float dq4[8], dk4[8];   // the 4 warps' partial row dots, 16-byte reads
+#pragma unroll
+  for (int hlf = 0; hlf < 2; ++hlf) {
+    float4 sq4 = make_float4(0.f, 0.f, 0.f, 0.f), sk4 = sq4;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float4 a4 = *reinterpret_cast<const float4 *>(rd + 16 * w + 4 * hlf);
+      const float4 b4 = *reinterpret_cast<const float4 *>(rd + 16 * w + 8 + 4 * hlf);
+      sq4.x += a4.x; sq4.y += a4.y; sq4.z += a4.z; sq4.w += a4.w;
+      sk4.x += b4.x; sk4.y += b4.y; sk4.z += b4.z; sk4.w += b4.w;
+    }
+    dq4[4 * hlf] = sq4.x; dq4[4 * hlf + 1] = sq4.y; dq4[4 * hlf + 2] = sq4.z; dq4[4 * hlf + 3] = sq4.w;
+    dk4[4 * hlf] = sk4.x; dk4[4 * hlf + 1] = sk4.y; dk4[4 * hlf + 2] = sk4.z; dk4[4 * hlf + 3] = sk4.w;
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = 16 * t + 8 * hf + i;
-    const float dotq = (rd[i] + rd[16 + i]) + (rd[32 + i] + rd[48 + i]);
-    const float dotk = (rd[8 + i] + rd[24 + i]) + (rd[40 + i] + rd[56 + i]);
+    const float dotq = dq4[i], dotk = dk4[i];
     if (r < len) {
       const size_t off = ((size_t)(t0 + r) * H + x.h) * D + c;
       const float r0 = rq0[r], rkr = rk[r];
@@ -256,7 +275,7 @@ __device__ __forceinline__ void round_epilogue(RoundCtx &x, const int t, uint32_
 }
 }  // namespace
 
-__global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChunkParams p) {
+__global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const __grid_constant__ BwdChunkParams p) {
   using S = BcSmem;
   extern __shared__ __align__(1024) char smem_raw[];
   char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -267,7 +286,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
   const int qw = warp & 3, hf = warp >> 2;          // lane quarter, column half
   const int row = 32 * qw + lane;                   // TMEM lane of this thread
   const int r64 = 16 * qw + (lane & 15);            // row of this lane in an M = 64 accumulator (lanes < 16)
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);   // [0] loads, [1..4] groups A-D, [5..8] rounds
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);   // [0] loads, [1..4] groups A-D, [5..8] rounds, [9] A
   uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + S::TSLOT);
   const size_t rid = (size_t)chunk * H + h;
   float *sb = reinterpret_cast<float *>(smem + S::SB);
@@ -278,7 +297,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
   float(*dvp)[128] = (float(*)[128])(smem + S::DV);
 
   if (tid == 0) {
-    for (int i = 0; i < 9; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < 10; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
   }
   if (warp == 0) tc::alloc(tslot, 512);
@@ -293,62 +312,62 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
   };
 
   // ---------------------------------------------------------------- loads
+  // bulk copies of the saved tiles and the record; TMA boxes of this chunk's V, dO, q, k rows
+  // (rows past the tensor read as zero) and of T
+  const int t0i = (int)ref.t0, arow = (int)rid * 128;
   if (tid == 0) {
     const char *rb = (const char *)p.img + rid * TcRec::BYTES;
     fence_proxy_async();
-    mbar_expect_tx(&bar[0], 2 * 32768 + (TcRec::TB - TcRec::B2) + (TcRec::BYTES - TcRec::TB) + KtRec::BYTES);
+    mbar_expect_tx(&bar[0], 2 * 32768 + (TcRec::TB - TcRec::B2) + (TcRec::BYTES - TcRec::TB) + KtRec::BYTES +
+                                5 * 16384);
     bulk_g2s(smem + S::SS, (const char *)p.saved + rid * 32768, 32768, &bar[0]);
     bulk_g2s(smem + S::SDS, (const char *)p.dsaved + rid * 32768, 32768, &bar[0]);
     bulk_g2s(smem + S::KHT, rb + TcRec::B2, TcRec::TB - TcRec::B2, &bar[0]);        // Kh^T, Bm
     bulk_g2s(smem + S::TB, rb + TcRec::TB, TcRec::BYTES - TcRec::TB, &bar[0]);      // Tb, e^{G_last}
     bulk_g2s(smem + S::KT, (const char *)p.kt + rid * KtRec::BYTES, KtRec::BYTES, &bar[0]);   // Kt
+    tc::tma_load_3d(smem + S::V, &p.tm_v, 0, h, t0i, &bar[0]);
+    tc::tma_load_3d(smem + S::DO, &p.tm_do, 0, h, t0i, &bar[0]);
+    tc::tma_load_3d(smem + S::DO + 8192, &p.tm_do, 64, h, t0i, &bar[0]);
+    tc::tma_load_3d(smem + S::QR, &p.tm_q, 0, h, t0i, &bar[0]);
+    tc::tma_load_3d(smem + S::KR, &p.tm_k, 0, h, t0i, &bar[0]);
+    tc::tma_load_2d(smem + S::TK, &p.tm_aux, 0, arow + 64, &bar[0]);
+    tc::tma_load_2d(smem + S::TK + 8192, &p.tm_aux, 32, arow + 64, &bar[0]);
   }
-  {
-    // V, dO rows into [tok][v] tiles (K-major over v, 128-byte swizzle); rows past the end are zero
-    const bf16 *vg = (const bf16 *)p.v, *dog = (const bf16 *)p.dO;
-    for (int idx = tid; idx < 64 * 16; idx += BC_THREADS) {
-      const int r = idx >> 4, ch = idx & 15;
-      const bool ok = r < ref.len;
-      const size_t off = ok ? ((size_t)(ref.t0 + r) * H + h) * 128 + 8 * ch : 0;
-      const uint32_t dst = tc::sw128_off(64, r, 8 * ch);
-      cp_async16(smem + S::V + dst, vg + off, ok ? 16 : 0);
-      cp_async16(smem + S::DO + dst, dog + off, ok ? 16 : 0);
-    }
-    // T (K-major fp32 tile) of the prep; raw q, k rows
-    const float *auxT = p.aux + rid * (2 * 64 * 64) + 64 * 64;
-    const bf16 *qg = (const bf16 *)p.q, *kg = (const bf16 *)p.k;
-    for (int idx = tid; idx < 64 * 16; idx += BC_THREADS) {
-      const int r = idx >> 4, ch = idx & 15;
-      cp_async16(smem + S::TK + tc::sw128_off32(64, r, 4 * ch), auxT + r * 64 + 4 * ch);
-      const bool ok = r < ref.len;
-      const size_t off = ok ? ((size_t)(ref.t0 + r) * H + h) * D + 8 * ch : 0;
-      cp_async16((bf16 *)(smem + S::QR) + r * D + 8 * ch, qg + off, ok ? 16 : 0);
-      cp_async16((bf16 *)(smem + S::KR) + r * D + 8 * ch, kg + off, ok ? 16 : 0);
-    }
-    if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
-  }
-  // while the copies land: the gate scan (thread = channel pair x sub-block), from global memory
+  if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
+  // while the copies land: the gate scan (thread = channel pair x sub-block), from global memory;
+  // the local sums G_r - E_{a-1} (log2) stay in registers for the factor tiles
   const int cp = tid & 63, a = tid >> 6, c0 = 2 * cp;
+  float2 csr[SUB];
   {
-    float2 gg[SUB];
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int rr = a * SUB + i;
-      gg[i] = rr < ref.len ? *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + rr) * H + h) * D + c0)
-                           : make_float2(0.f, 0.f);
+      csr[i] = rr < ref.len ? *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + rr) * H + h) * D + c0)
+                            : make_float2(0.f, 0.f);
     }
     float2 run = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
-      run.x = fmaf(gg[i].x, LOG2E, run.x);
-      run.y = fmaf(gg[i].y, LOG2E, run.y);
+      run.x = fmaf(csr[i].x, LOG2E, run.x);
+      run.y = fmaf(csr[i].y, LOG2E, run.y);
+      csr[i] = run;
     }
     tot[a][c0] = run.x;
     tot[a][c0 + 1] = run.y;
   }
-  cp_async_wait_all();
-  fence_proxy_async();
   bool ok = mbar_wait(&bar[0], 0);
+  if (ref.len < CH && ok) {
+    // a sequence's last chunk: rows past its end read as zero (the boxes hold the next sequence's rows)
+    for (int idx = tid; idx < (CH - ref.len) * 16; idx += BC_THREADS) {
+      const int r = ref.len + (idx >> 4), ch = idx & 15;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4 *>(smem + S::V + r * 256 + 16 * ch) = z;
+      *reinterpret_cast<uint4 *>(smem + S::QR + r * 256 + 16 * ch) = z;
+      *reinterpret_cast<uint4 *>(smem + S::KR + r * 256 + 16 * ch) = z;
+      *reinterpret_cast<uint4 *>(smem + S::DO + (ch >> 3) * 8192 + r * 128 + 16 * (ch & 7)) = z;
+    }
+    fence_proxy_async();
+  }
   tc::fence_before();
   if (!__syncthreads_and(ok)) return fail_out();
   tc::fence_after();
@@ -461,7 +480,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int j = 32 * hf + 8 * cb + i;
-        x8[i] = to_f(*reinterpret_cast<const bf16 *>(smem + S::V + tc::sw128_off(64, j, row))) - v[8 * cb + i];
+        x8[i] = to_f(*reinterpret_cast<const bf16 *>(smem + S::V + j * 256 + 2 * row)) - v[8 * cb + i];
       }
       *reinterpret_cast<uint4 *>(smem + S::VPT + tc::sw128_off(128, row, 32 * hf + 8 * cb)) = tc::pack8(x8);
     }
@@ -580,10 +599,10 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
   float tcol[16];   // T[m0 + e][r] for the in-place transpose of T (thread: r = tid % 64, m0 = 16 (tid / 64))
   if (ok) {
     // A of the prep into the dead dO tile, for the dbeta term of epilogue D
-    const float *auxA = p.aux + rid * (2 * 64 * 64);
-    for (int idx = tid; idx < 64 * 16; idx += BC_THREADS) {
-      const int r = idx >> 4, ch = idx & 15;
-      cp_async16((float *)(smem + S::AS) + as_off(r, 4 * ch), auxA + r * 64 + 4 * ch);
+    if (tid == 0) {
+      mbar_expect_tx(&bar[9], 16384);
+      tc::tma_load_2d(smem + S::AS, &p.tm_aux, 0, arow, &bar[9]);
+      tc::tma_load_2d(smem + S::AS + 8192, &p.tm_aux, 32, arow, &bar[9]);
     }
     {
       const int r = tid & 63, m0 = 16 * (tid >> 6);
@@ -656,21 +675,12 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
   // factor tiles QL, KL, R [r][c] (bf16, K-major over c) over the dead dS^T and U^T tiles, and the
   // local gate sums for the rounds: thread = channel pair x sub-block, as in the prep
   {
-    float2 gg[SUB];
-#pragma unroll
-    for (int i = 0; i < SUB; ++i) {
-      const int r = a * SUB + i;
-      gg[i] = r < ref.len ? *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + r) * H + h) * D + c0)
-                          : make_float2(0.f, 0.f);
-    }
-    float2 run = make_float2(0.f, 0.f);
     const float ta0 = tot[a][c0], ta1 = tot[a][c0 + 1];
     const bf16 *sq_ = (const bf16 *)(smem + S::QR), *sk_ = (const bf16 *)(smem + S::KR);
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
-      run.x = fmaf(gg[i].x, LOG2E, run.x);
-      run.y = fmaf(gg[i].y, LOG2E, run.y);
+      const float2 run = csr[i];
       *reinterpret_cast<float2 *>(smem + (r < 32 ? S::CSA + r * 512 : S::CSB + (r - 32) * 512) + c0 * 4) = run;
       const float2 qf = ld2(sq_ + r * D + c0), kf = ld2(sk_ + r * D + c0);
       const float x0 = exp2f(run.x), x1 = exp2f(run.y), y0 = exp2f(ta0 - run.x), y1 = exp2f(ta1 - run.y);
@@ -681,9 +691,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
       st2((bf16 *)(smem + S::RF + o), kf.x * ks_ * y0, kf.y * ks_ * y1);
     }
   }
-  cp_async_wait_all();   // A
-  __syncthreads();
-  ok = __all_sync(0xffffffffu, mbar_wait(&bar[4], 0));
+  ok = __all_sync(0xffffffffu, mbar_wait(&bar[4], 0) && mbar_wait(&bar[9], 0));
   tc::fence_after();
   float *db2 = reinterpret_cast<float *>(smem + S::DB2P);
   if (ok) {
@@ -694,13 +702,12 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(BwdChun
     tc::wait_ld();
     if (lane < 16) {
       const float br = sb[r64];
-      const float *as = reinterpret_cast<const float *>(smem + S::AS);
       float part = 0.f;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         const int j0 = 32 * hf + 8 * cb;
-        const float4 a0 = *reinterpret_cast<const float4 *>(as + as_off(r64, j0));
-        const float4 a1 = *reinterpret_cast<const float4 *>(as + as_off(r64, j0 + 4));
+        const float4 a0 = *reinterpret_cast<const float4 *>(smem + S::AS + tc::sw128_off32(64, r64, j0));
+        const float4 a1 = *reinterpret_cast<const float4 *>(smem + S::AS + tc::sw128_off32(64, r64, j0 + 4));
         const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         float x8[8];
 #pragma unroll

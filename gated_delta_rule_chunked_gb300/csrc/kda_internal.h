@@ -1,5 +1,6 @@
 // kda_internal.h -- host-side launch interfaces between kda_api.cu and the kernels.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime_api.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -93,6 +94,9 @@ struct BwdScanParams {
 };
 
 struct BwdChunkParams {
+  // TMA maps: q, k, v (box 128 x 1 head x 64 tokens, plain rows), dO (box 64 x 1 x 64, 128-byte
+  // swizzle), and the prep's A/T array as [items * 128 rows][64] fp32 (box 32 x 64, 128-byte swizzle)
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_aux;
   SeqGeom geo;
   const void *q, *k, *v, *dO;   // io type (bf16)
   const float *g, *beta;

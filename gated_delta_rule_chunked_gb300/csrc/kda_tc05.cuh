@@ -7,6 +7,7 @@
 // Accumulators live in tensor memory (TMEM): for M = 128, row m of D is TMEM
 // lane m and column n is TMEM column base + n (fp32).
 #pragma once
+#include <cuda.h>
 #include <stdint.h>
 
 #include "kda_common.cuh"
@@ -135,6 +136,25 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float (&v)[16]) {
       : "memory");
 }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+// TMA tensor loads: one box of the tensor described by `map` (a kernel parameter declared
+// __grid_constant__, so its address is valid here) into shared memory, completing on `bar`
+// with the box's bytes. The innermost coordinate times the element size must be a multiple
+// of 16 bytes; boxes reaching past the tensor are zero-filled.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
 
 // Pack 8 floats into one 16-byte chunk of bf16.
 __device__ __forceinline__ uint4 pack8(const float *x) {

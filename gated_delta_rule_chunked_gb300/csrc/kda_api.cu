@@ -249,6 +249,11 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
   }
   char *ws = static_cast<char *>(a->workspace);
   const bool f32 = a->io_dtype == KDA_F32;
+  CUtensorMap tm_q, tm_k, tm_g;
+  if (!map_tokens(&tm_q, a->q, f32, a->total_tokens, a->heads, 128, false) ||
+      !map_tokens(&tm_k, a->k, f32, a->total_tokens, a->heads, 128, false) ||
+      !map_tokens(&tm_g, a->g, true, a->total_tokens, a->heads, 128, false))
+    return fail(KDA_ERR_CUDA, "%s: could not encode the TMA tensor maps", "kda_fwd");
   kda::SeqGeom geo = geom(a, ws, w);
   cudaError_t e = kda::launch_chunk_table(a->cu_seqlens, a->n_seqs, a->total_tokens,
                                           reinterpret_cast<int *>(ws + w.cu), reinterpret_cast<int *>(ws + w.choff),
@@ -261,17 +266,21 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
   char *sd = static_cast<char *>(a->saved);
   const bool bwd_recs = !f32 && sd;
   char *rec = bwd_recs ? sd + sv.rec : ws + w.img;
-  kda::PrepParams pp{geo,
-                     a->q,
-                     a->k,
-                     a->g,
-                     a->beta,
-                     a->scale,
-                     rec,
-                     bwd_recs ? reinterpret_cast<float *>(sd + sv.aux) : nullptr,
-                     f32 ? 0 : (bwd_recs ? 3 : 1),
-                     bwd_recs ? sd + sv.kt : nullptr,
-                     a->dev_status};
+  kda::PrepParams pp{};
+  pp.geo = geo;
+  pp.q = a->q;
+  pp.k = a->k;
+  pp.g = a->g;
+  pp.beta = a->beta;
+  pp.scale = a->scale;
+  pp.img = rec;
+  pp.aux = bwd_recs ? reinterpret_cast<float *>(sd + sv.aux) : nullptr;
+  pp.tc_layout = f32 ? 0 : (bwd_recs ? 3 : 1);
+  pp.img2 = bwd_recs ? sd + sv.kt : nullptr;
+  pp.status = a->dev_status;
+  pp.tm_q = tm_q;
+  pp.tm_k = tm_k;
+  pp.tm_g = tm_g;
   if ((e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
   kda::FwdScanParams sp{geo, a->v, rec, a->h0, a->o, a->hT, a->saved, a->dev_status};

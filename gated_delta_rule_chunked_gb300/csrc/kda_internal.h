@@ -58,6 +58,8 @@ struct SeqGeom {
 };
 
 struct PrepParams {
+  // TMA maps of q, k (io type) and g (fp32): box 128 channels x 1 head x 64 tokens, plain rows
+  CUtensorMap tm_q, tm_k, tm_g;
   SeqGeom geo;
   const void *q, *k;
   const float *g, *beta;

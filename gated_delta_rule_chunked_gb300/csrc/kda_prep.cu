@@ -85,7 +85,8 @@ struct PrepSmem2 {
   static constexpr int TOT = DV + 10 * 512;                  // fp32 [4][128] sub-block gate sums
   static constexpr int PV = TOT + 4 * 512;                   // fp32 [4][128] exp(E_{a-1})
   static constexpr int RQ = PV + 4 * 512, RK = RQ + 256, BETA = RK + 256;
-  static constexpr int BYTES = BETA + 256;
+  static constexpr int BAR = BETA + 256;                     // mbarrier of the staging copies
+  static constexpr int BYTES = BAR + 16;
   // after the Gram products QL and R are dead; KL lives on (it becomes Kt)
   static constexpr int LM = QL;                              // fp32 [64][LDS64]  Diag(beta) A
   static constexpr int TT = LM + 64 * LDS64 * 4;             // fp32 [64][LDS64]  T, then T Diag(beta)
@@ -178,7 +179,7 @@ template <> struct Pair<float> {
 };
 
 template <typename E>
-__global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p) {
+__global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_constant__ PrepParams p) {
   using S = PrepSmem2;
   constexpr bool PRECISE = sizeof(E) == 4;   // fp32 I/O: exact fp32 products
   extern __shared__ __align__(128) char smem[];
@@ -189,7 +190,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   // tcgen05 record (bf16 forward) or the tile record (fp32 forward, backward)
   const bool tcrec = !PRECISE && (p.tc_layout & 1);   // forward tcgen05 record
   const bool bwdrec = !PRECISE && (p.tc_layout & 2);  // backward extras: Kt, A and T
-  const E *qg = (const E *)p.q, *kg = (const E *)p.k;
   float *rq = (float *)(smem + S::RQ), *rk = (float *)(smem + S::RK), *sb = (float *)(smem + S::BETA);
   float *KL = (float *)(smem + S::KL), *QL = (float *)(smem + S::QL), *RR = (float *)(smem + S::R);
   float(*dv)[128] = (float(*)[128])(smem + S::DV);
@@ -201,31 +201,44 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
   char *trec = PRECISE ? (char *)p.img + rid * L.bytes : nullptr;                         // fp32 tile record
   char *recb = bwdrec ? (char *)p.img2 + rid * KtRec::BYTES : nullptr;
 
-  // 0. stage the chunk's q, k (io type) and g (fp32) in shared memory with one batch of
-  //    asynchronous copies: q in the KL tile, k in the R tile, g in the QL tile (row
-  //    stride LDF); rows past the sequence end are zero-filled. All three tiles are
-  //    rewritten only after their contents have been consumed.
+  // 0. stage the chunk's q, k (io type) and g (fp32) in shared memory with three TMA boxes:
+  //    q in the KL tile, k in the R tile (plain rows), g in the QL tile (dense 128-float rows);
+  //    rows past the sequence end are zeroed. All three tiles are rewritten only after their
+  //    contents have been consumed.
   constexpr int QROW = D * (int)sizeof(E);            // bytes of one staged q / k row
   const E *sq_ = (const E *)KL, *sk_ = (const E *)RR;
   {
-    constexpr int QCH = QROW / 16;
-    for (int idx = tid; idx < CH * QCH; idx += PREP_THREADS) {
-      const int r = idx / QCH, ch = idx % QCH;
-      const bool ok = r < ref.len;
-      const size_t off = ok ? ((size_t)(ref.t0 + r) * H + h) * D * sizeof(E) + 16 * ch : 0;
-      cp_async16((char *)KL + r * QROW + 16 * ch, (const char *)qg + off, ok ? 16 : 0);
-      cp_async16((char *)RR + r * QROW + 16 * ch, (const char *)kg + off, ok ? 16 : 0);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
+    if (tid == 0) {
+      mbar_init(bar, 1);
+      fence_mbar_init();
     }
-    for (int idx = tid; idx < CH * (D / 4); idx += PREP_THREADS) {
-      const int r = idx / (D / 4), ch = idx % (D / 4);
-      const bool ok = r < ref.len;
-      const float *src = ok ? p.g + ((size_t)(ref.t0 + r) * H + h) * D + 4 * ch : p.g;
-      cp_async16(QL + r * LDF + 4 * ch, src, ok ? 16 : 0);
+    __syncthreads();
+    if (tid == 0) {
+      const int t0i = (int)ref.t0;
+      mbar_expect_tx(bar, 2 * CH * QROW + CH * D * 4);
+      tc::tma_load_3d(KL, &p.tm_q, 0, h, t0i, bar);
+      tc::tma_load_3d(RR, &p.tm_k, 0, h, t0i, bar);
+      tc::tma_load_3d(QL, &p.tm_g, 0, h, t0i, bar);
     }
     if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
-    cp_async_wait_all();
+    const bool ok = mbar_wait(bar, 0);
+    if (ok && ref.len < CH) {   // the boxes hold the next sequence's rows there
+      for (int idx = tid; idx < (CH - ref.len) * (QROW / 16); idx += PREP_THREADS) {
+        const int r = ref.len + idx / (QROW / 16), ch = idx % (QROW / 16);
+        *reinterpret_cast<uint4 *>((char *)KL + r * QROW + 16 * ch) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>((char *)RR + r * QROW + 16 * ch) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int idx = tid; idx < (CH - ref.len) * (D / 4); idx += PREP_THREADS) {
+        const int r = ref.len + idx / (D / 4), ch = idx % (D / 4);
+        *reinterpret_cast<float4 *>(QL + r * D + 4 * ch) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    if (!__syncthreads_and(ok)) {
+      report(p.status, ERR_TIMEOUT);
+      return;
+    }
   }
-  __syncthreads();
   // 1. row norms: 4 threads per row, 32 channels each
   {
     const int r = tid >> 2, part = tid & 3;
@@ -253,7 +266,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(PrepParams p)
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
-      cs[i] = *reinterpret_cast<const float2 *>(QL + r * LDF + c0);
+      cs[i] = *reinterpret_cast<const float2 *>(QL + r * D + c0);
       qpair[i] = Pair<E>::load(sq_ + r * D + c0);
       kpair[i] = Pair<E>::load(sk_ + r * D + c0);
     }

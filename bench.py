@@ -290,8 +290,8 @@ def bench_e2e(args, dev, world, host):
     output buffers."""
     import torch
     import gated_delta_rule_chunked_gb300 as kda
-    names = ("q", "k", "v", "beta", "g", "h0", "dO")
-    cu = host.pop("cu_seqlens")
+    names = ("q", "k", "v", "beta", "g", "h0", "dO", "cu_seqlens")
+    host["cu_seqlens"] = host["cu_seqlens"].to(torch.int32).pin_memory()
     total = host["q"].shape[0]
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     K = max(2, min(args.steps, 8))
@@ -314,6 +314,7 @@ def bench_e2e(args, dev, world, host):
             ev_in[slot].record(s_in)
         with torch.cuda.stream(s_c):
             s_c.wait_event(ev_in[slot])
+            cu = d["cu_seqlens"]
             o, hT, saved = kda.kda_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], cu, d["h0"], save=True)
             gr = kda.kda_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["dO"], saved, cu, d["h0"])
             ev_c[slot].record(s_c)

@@ -88,6 +88,10 @@ def bwd_args(fa: _lib.FwdArgs, dO, dq, dk, dv, dbeta, dg, dh0=None, dhT=None, wo
 def _i32(cu_seqlens, device):
     if cu_seqlens is None:
         return None
+    if cu_seqlens.device.type == "cpu":
+        # through pinned memory, so the copy is enqueued on the current stream instead of
+        # blocking the host until the stream reaches it
+        return cu_seqlens.to(dtype=torch.int32).contiguous().pin_memory().to(device, non_blocking=True)
     return cu_seqlens.to(device=device, dtype=torch.int32).contiguous()
 
 

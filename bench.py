@@ -274,11 +274,56 @@ def bench_decode(args, dev, lib, stream, peaks):
     torch.cuda.synchronize(dev)
     ms = s.elapsed_time(e) / K
     gbs = DEC_BYTES * N * H / (ms * 1e-3) / 1e9
-    return {"workload": DECODE, "ms_per_call": ms, "gbs_algorithmic": gbs, "unit": "GB/s",
+    out = {"workload": DECODE, "ms_per_call": ms, "gbs_algorithmic": gbs, "unit": "GB/s",
+           "roofline": {"kernel": "decode", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("decode")},
+           "tokens_per_s": N * L / (ms * 1e-3), "gpu_launches": K,
+           "state_bytes": N * H * D * D * 4, "l2": "state (1.6 GB) larger than L2; no flush"}
+    del d, o, a
+    out["replay_verify"] = bench_replay_verify(args, dev, lib, stream, peaks, N, L, H)
+    return out
+
+
+def bench_replay_verify(args, dev, lib, stream, peaks, N, L, H, P=512):
+    """Two-phase draft/verify over a paged state pool: each call replays the a_i accepted
+    tokens of the previous L-token draft (right-aligned after padding) and verifies the next
+    L-token draft, committing after the replay; states sit in random distinct slots of a pool
+    of P. Algorithmic bytes: the state read and written once, and every real token slot's
+    inputs and output."""
+    import torch
+    from gated_delta_rule_chunked_gb300 import _lib
+    from gated_delta_rule_chunked_gb300.inputs import make_decode_batch
+    import gated_delta_rule_chunked_gb300 as kda
+    d = make_decode_batch(N, 2 * L, H, "bf16", seed=4242, device=dev)
+    gen = torch.Generator().manual_seed(4243)
+    pool = (torch.randn(P, H, D, D, generator=gen) * 0.02).to(dev)
+    idx = torch.randperm(P, generator=gen)[:N].to(torch.int32).to(dev)
+    acc_prev = torch.randint(1, L + 1, (N,), generator=gen, dtype=torch.int32)
+    first = (L - acc_prev).to(torch.int32).to(dev)
+    commit = torch.full((N,), L, dtype=torch.int32, device=dev)
+    o = torch.empty_like(d.v)
+    a = kda.step_args(d.q, d.k, d.v, d.beta, d.g, pool, commit, o, 1.0, idx, first)
+    sptr = stream.cuda_stream
+    K = max(args.steps, 20)
+    for _ in range(max(args.warmup, 3)):
+        _lib.check(lib.kda_step(C.byref(a), sptr))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    s.record(stream)
+    for _ in range(K):
+        _lib.check(lib.kda_step(C.byref(a), sptr))
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e) / K
+    real = int(acc_prev.sum()) + N * L                     # real token slots per head
+    byts = H * (N * 2 * D * D * 4 + real * (3 * 256 + 512 + 4 + 256))
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"workload": f"decode-replay-verify-bf16-N{N}-P{P}-L{L}+{L}-H{H}", "ms_per_call": ms,
+            "gbs_algorithmic": gbs, "unit": "GB/s",
             "roofline": {"kernel": "decode", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("decode")},
-            "tokens_per_s": N * L / (ms * 1e-3), "gpu_launches": K,
-            "state_bytes": N * H * D * D * 4, "l2": "state (1.6 GB) larger than L2; no flush"}
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]},
+            "draft_tokens_per_s": N * L / (ms * 1e-3), "replayed_tokens_per_call": int(acc_prev.sum()),
+            "gpu_launches": K, "pool_bytes": P * H * D * D * 4}
 
 
 def bench_e2e(args, dev, world, host):

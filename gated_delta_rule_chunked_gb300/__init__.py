@@ -153,28 +153,41 @@ def kda_bwd(q, k, v, beta, g, dO, saved, cu_seqlens=None, h0=None, dhT=None, *, 
     return {"dq": dq, "dk": dk, "dv": dv, "dbeta": dbeta, "dg": dg, "dh0": dh0}
 
 
-def step_args(q, k, v, beta, g, state, accept_len, o, scale: float = 1.0) -> _lib.StepArgs:
+def step_args(q, k, v, beta, g, state, accept_len, o, scale: float = 1.0, state_indices=None,
+              first_slot=None, dev_status=None) -> _lib.StepArgs:
     a = _lib.StepArgs()
     N, L, H, dk = q.shape
     a.n_seqs, a.steps, a.heads, a.dk, a.dv = N, L, H, dk, v.shape[3]
     a.scale, a.io_dtype = scale, _io_dtype(q)
     a.q, a.k, a.v, a.beta, a.g = _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g)
     a.state, a.accept_len, a.o = _ptr(state), _ptr(accept_len), _ptr(o)
+    a.state_indices, a.first_slot, a.dev_status = _ptr(state_indices), _ptr(first_slot), _ptr(dev_status)
+    a.n_slots = state.shape[0]
     return a
 
 
-def kda_step(q, k, v, beta, g, state, accept_len=None, *, scale: float = 1.0, out=None):
+def kda_step(q, k, v, beta, g, state, accept_len=None, *, scale: float = 1.0, out=None, state_indices=None,
+             first_slot=None, dev_status=None):
     """Decode / draft-verify L tokens per sequence; returns o [N, L, H, 128].
 
-    ``state`` [N, H, 128, 128] fp32 is overwritten with the state after
-    ``accept_len[i]`` tokens (left untouched where accept_len is 0; all L when None).
+    ``state`` [N, H, 128, 128] fp32 (or a pool [P, H, 128, 128] addressed by
+    ``state_indices`` [N]) is overwritten with the state after ``accept_len[i]`` token
+    slots (left untouched where accept_len is 0; all L when None). Slots before
+    ``first_slot[i]`` are padding: no state change, output not written. See
+    include/kda.h for the verify-then-replay use of the two.
     """
     lib = library()
     _check_inputs(q, k, v, beta, g)
     if state.dtype != torch.float32 or not state.is_contiguous():
         raise TypeError("state must be a contiguous float32 tensor")
-    acc = None if accept_len is None else accept_len.to(device=q.device, dtype=torch.int32).contiguous()
+    i32 = lambda t: None if t is None else t.to(device=q.device, dtype=torch.int32).contiguous()
+    acc, idx, first = i32(accept_len), i32(state_indices), i32(first_slot)
+    N = q.shape[0]
+    if (idx is None and state.shape[0] != N) or (idx is not None and idx.numel() != N):
+        raise ValueError("state has one slot per sequence unless state_indices [N] addresses a pool")
+    if first is not None and first.numel() != N:
+        raise ValueError("first_slot must have one entry per sequence")
     o = torch.empty_like(v) if out is None else out
-    a = step_args(q, k, v, beta, g, state, acc, o, scale)
+    a = step_args(q, k, v, beta, g, state, acc, o, scale, idx, first, dev_status)
     _lib.check(lib.kda_step(C.byref(a), _stream(q.device)))
     return o

@@ -14,7 +14,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT 
 KDA_BF16, KDA_F32 = 0, 1
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
                 4: "KDA_ERR_TIMEOUT"}
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 # every symbol include/kda.h declares
 EXPORTS = ("kda_fwd", "kda_fwd_workspace_size", "kda_saved_size", "kda_bwd", "kda_bwd_workspace_size",
@@ -47,6 +47,8 @@ class StepArgs(C.Structure):
         ("scale", C.c_float), ("io_dtype", C.c_int32),
         ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p), ("beta", C.c_void_p), ("g", C.c_void_p),
         ("state", C.c_void_p), ("accept_len", C.c_void_p), ("o", C.c_void_p),
+        ("state_indices", C.c_void_p), ("n_slots", C.c_int32), ("first_slot", C.c_void_p),
+        ("dev_status", C.c_void_p),
     ]
 
 

@@ -204,7 +204,7 @@ void kda::set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
 
 extern "C" {
 
-int32_t kda_abi_version(void) { return 1; }
+int32_t kda_abi_version(void) { return 2; }
 
 void kda_set_profile_events(cudaEvent_t *events, int32_t n_events) {
   g_prof_events = events;
@@ -386,9 +386,14 @@ kda_status kda_step(const kda_step_args *a, cudaStream_t stream) {
     if (!aligned(need[i], 16)) return fail(KDA_ERR_INVALID_ARG, "kda_step: %s is not 16-byte aligned", names[i]);
   }
   if (!a->beta || !aligned(a->beta, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: beta is NULL or misaligned", "kda_step");
-  if (!aligned(a->accept_len, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: accept_len is misaligned", "kda_step");
+  if (!aligned(a->accept_len, 4) || !aligned(a->state_indices, 4) || !aligned(a->first_slot, 4) ||
+      !aligned(a->dev_status, 4))
+    return fail(KDA_ERR_INVALID_ARG, "%s: accept_len, state_indices, first_slot or dev_status is misaligned",
+                "kda_step");
+  if (a->state_indices && a->n_slots < 1)
+    return fail(KDA_ERR_INVALID_ARG, "%s: state_indices needs n_slots >= 1", "kda_step");
   kda::StepParams p{a->n_seqs, a->steps, a->heads, a->scale, a->q, a->k, a->v, a->beta, a->g, a->state,
-                    a->accept_len, a->o};
+                    a->accept_len, a->o, a->state_indices, a->n_slots, a->first_slot, a->dev_status};
   cudaError_t e = kda::launch_step(p, a->io_dtype == KDA_F32, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_step");
   mark(0, stream);

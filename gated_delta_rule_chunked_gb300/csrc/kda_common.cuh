@@ -19,6 +19,7 @@ constexpr int SUB = 16;      // sub-block of the gated Gram factorisation
 constexpr int NSUB = CH / SUB;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int ERR_TIMEOUT = 4;   // matches KDA_ERR_TIMEOUT
+constexpr int KDA_ERR_INVALID_ARG_CODE = 1;   // matches KDA_ERR_INVALID_ARG
 
 typedef __nv_bfloat16 bf16;
 

@@ -119,6 +119,10 @@ struct StepParams {
   float *state;
   const int *accept_len;
   void *o;
+  const int *state_indices;   // [N] pool slot per sequence, or null (slot = sequence)
+  int n_slots;                // pool size with state_indices
+  const int *first_slot;      // [N] leading padding slots, or null (0)
+  int *status;
 };
 
 cudaError_t launch_chunk_table(const int *cu_in, int n_seqs, long long total, int *cu_out,

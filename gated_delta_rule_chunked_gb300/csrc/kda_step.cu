@@ -20,6 +20,13 @@
 //   S_A = Diag(gamma_A) S0 + sum_{m<=A} (exp(G_A - G_m) o k^_m) u_m^T   (A = accept_len).
 // So the state is swept twice per call (2L column sums, then one rank-A
 // update), with one cross-warp reduction, instead of twice per token.
+//
+// Two-phase draft/verify: the state of a sequence may sit in any slot of a pool
+// (state_indices), and a call's leading slots may be padding (first_slot): a
+// padded slot has zero inputs, beta = 0 and g = 0, so it leaves S and every other
+// token's quantities exactly as they were, and its output is not written. A call
+// can thus replay a sequence's accepted draft tokens (right-aligned before the new
+// draft) and commit after them while verifying the next draft in the same pass.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -59,10 +66,18 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
   const int L = p.steps, H = p.heads, NV = 2 * L;
   int A = p.accept_len ? p.accept_len[seq] : L;
   A = A < 0 ? 0 : (A > L ? L : A);
+  // slots before F are padding: zero inputs, beta = 0 and g = 0 make them exact identities
+  int F = p.first_slot ? p.first_slot[seq] : 0;
+  F = F < 0 ? 0 : (F > L ? L : F);
+  const int slot = p.state_indices ? p.state_indices[seq] : seq;
+  if (p.state_indices && (slot < 0 || slot >= p.n_slots)) {   // block-uniform
+    if (tid == 0) report(p.status, KDA_ERR_INVALID_ARG_CODE);
+    return;
+  }
   float *red = step_red, *W = step_red + 8 * NV * D;
 
   // state rows [16 warp, +16), columns [4 lane, +4) as two column pairs
-  float *st = p.state + ((size_t)seq * H + h) * D * D;
+  float *st = p.state + ((size_t)slot * H + h) * D * D;
   float2 S[16][2];
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
@@ -77,12 +92,13 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
   for (int idx = tid; idx < L * D; idx += STEP_THREADS) {
     const int l = idx / D, c = idx % D;
     const size_t off = (((size_t)seq * L + l) * H + h) * D + c;
-    sm.q[l][c] = ld_io(q + off);
-    sm.k[l][c] = ld_io(k + off);
-    sm.v[l][c] = ld_io(v + off);
-    sm.G[l][c] = p.g[off];
+    const bool pad = l < F;
+    sm.q[l][c] = pad ? 0.f : ld_io(q + off);
+    sm.k[l][c] = pad ? 0.f : ld_io(k + off);
+    sm.v[l][c] = pad ? 0.f : ld_io(v + off);
+    sm.G[l][c] = pad ? 0.f : p.g[off];
   }
-  if (tid < L) sm.beta[tid] = p.beta[((size_t)seq * L + tid) * H + h];
+  if (tid < L) sm.beta[tid] = tid < F ? 0.f : p.beta[((size_t)seq * L + tid) * H + h];
   __syncthreads();
 
   // L2 normalisation (one warp per token) and the running gate sums (one thread per channel)
@@ -219,7 +235,7 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
         u[l] = sm.beta[l] * (sm.v[l][tid] - w);
         ol = fmaf(sm.b[l][l], u[l], ol);
         sm.U[l][tid] = u[l];
-        o[(((size_t)seq * L + l) * H + h) * D + tid] = from_f<IO>(ol);
+        if (l >= F) o[(((size_t)seq * L + l) * H + h) * D + tid] = from_f<IO>(ol);
       }
     }
   }

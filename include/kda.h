@@ -120,10 +120,23 @@ typedef struct {
     const void *v;             /* [N, L, H, dv]                                          */
     const float *beta;         /* [N, L, H]                                              */
     const float *g;            /* [N, L, H, dk]                                          */
-    float *state;              /* in/out [N, H, dk, dv]: read, then overwritten with the
-                                  state after accept_len[i] tokens (untouched if 0)      */
+    float *state;              /* in/out [N, H, dk, dv] (or [P, H, dk, dv] with state_indices):
+                                  read, then overwritten with the state after accept_len[i]
+                                  token slots (untouched if 0)                            */
     const int32_t *accept_len; /* [N] in 0..L, or NULL meaning L for every sequence      */
-    void *o;                   /* out [N, L, H, dv]: outputs of all L tokens             */
+    void *o;                   /* out [N, L, H, dv]: outputs of the L token slots (slots
+                                  before first_slot[i] are not written)                   */
+    /* ABI version 2: */
+    const int32_t *state_indices; /* [N] slot of sequence i in a pool of n_slots states, or
+                                     NULL (slot i); distinct slots for sequences that
+                                     commit. A slot outside 0..n_slots-1 leaves that
+                                     sequence untouched and writes KDA_ERR_INVALID_ARG to
+                                     *dev_status                                          */
+    int32_t n_slots;              /* P, the pool size (used with state_indices)           */
+    const int32_t *first_slot;    /* [N] in 0..L: slots before first_slot[i] are padding,
+                                     exact identities (no state change, no output), or
+                                     NULL (0)                                             */
+    int32_t *dev_status;          /* optional device int32, as in kda_fwd_args            */
 } kda_step_args;
 
 /*
@@ -147,7 +160,16 @@ size_t kda_bwd_workspace_size(const kda_bwd_args *args);
 /* kda_step -- recurrent decode over L <= 8 tokens, returning all L outputs and
  * committing the state only through the accepted prefix, as ReplaySSM advances
  * KDA state only through accepted tokens ("Kimi K3 on Fireworks", rollout
- * section, speculative decoding paragraph). Needs no workspace. */
+ * section, speculative decoding paragraph). Needs no workspace.
+ *
+ * Two-phase use (verify, then replay): a verify call runs the draft tokens with
+ * accept_len = 0, so the committed state is not written. Once a_i of them are
+ * accepted, the next call replays those a_i tokens and verifies the next draft in
+ * one pass: its slots hold [R - a_i padding | the a_i accepted tokens | the new
+ * draft], with first_slot[i] = R - a_i and accept_len[i] = R, so the committed
+ * state advances exactly through the accepted tokens and the outputs of the new
+ * draft are computed from it. state_indices addresses states in a pool (paged
+ * state cache), so sequences keep their slot across calls. */
 kda_status kda_step(const kda_step_args *args, cudaStream_t stream);
 
 /*

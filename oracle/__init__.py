@@ -208,6 +208,35 @@ def step(q, k, v, beta, g, state, accept_len, *, scale: float = 1.0, eps: float 
     return out
 
 
+def step_paged(q, k, v, beta, g, pool, state_indices, first_slot, accept_len, *, scale: float = 1.0,
+               eps: float = EPS, n_threads: int = 0):
+    """Two-phase draft/verify over a pool of states (the ReplaySSM rollout pattern of the
+    "Kimi K3 on Fireworks" page, rollout section, speculative decoding paragraph).
+
+    Sequence i reads state ``pool[state_indices[i]]``; its token slots before
+    ``first_slot[i]`` are padding and are skipped (padding is defined as changing
+    nothing), the real tokens run through the token loop of ``step``, and the state is
+    committed after ``accept_len[i]`` slots, i.e. after ``accept_len[i] - first_slot[i]``
+    real tokens (none if that is not positive).
+    Returns ``{(i, h): (o [L - first_slot[i], dv] of the real slots, committed state)}``.
+    """
+    N, L, H, _ = q.shape
+    out = {}
+    for i in range(N):
+        f, a = int(first_slot[i]), int(accept_len[i])
+        sl = slice(i, i + 1)
+        slot = int(state_indices[i])
+        if f >= L:   # nothing but padding: no outputs, state unchanged
+            for h in range(H):
+                out[(i, h)] = (np.zeros((0, v.shape[3])), pool[slot, h].double().numpy())
+            continue
+        r = step(q[sl, f:], k[sl, f:], v[sl, f:], beta[sl, f:], g[sl, f:], pool[slot:slot + 1],
+                 torch.tensor([max(0, a - f)], dtype=torch.int32), scale=scale, eps=eps, n_threads=n_threads)
+        for h in range(H):
+            out[(i, h)] = r[(0, h)]
+    return out
+
+
 def assemble_fwd(res: dict, cu_seqlens, H: int, dv: int):
     """Stack per-task forward results into o [total, H, dv] and hT [N, H, dk, dv]."""
     cu = [int(x) for x in cu_seqlens.to("cpu").tolist()]

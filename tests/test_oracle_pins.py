@@ -237,6 +237,51 @@ def test_decode_equals_forward():
                 np.testing.assert_array_equal(s_s, state[i, h].double().numpy())
 
 
+def test_paged_decode_verify_then_replay():
+    # Verify a draft with accept 0 (state untouched), then in one call replay the accepted
+    # prefix right-aligned after padding and verify the next draft: the committed state and
+    # the new draft's outputs equal the token loop run over the accepted tokens followed by
+    # the new draft (the forward recurrence itself, not the decode routine).
+    N, L1, L2, H, d = 3, 4, 3, 2, 16
+    R = L1
+    gen = torch.Generator().manual_seed(21)
+    mk = lambda L: ([torch.randn(N, L, H, d, generator=gen) for _ in range(3)],
+                    torch.sigmoid(torch.randn(N, L, H, generator=gen)),
+                    torch.nn.functional.logsigmoid(torch.randn(N, L, H, d, generator=gen) + 3))
+    (q1, k1, v1), b1, g1 = mk(L1)
+    (q2, k2, v2), b2, g2 = mk(L2)
+    P = 5
+    pool = torch.randn(P, H, d, d, generator=gen) * 0.02
+    idx = torch.tensor([3, 0, 4], dtype=torch.int32)
+    acc = [2, 0, 4]
+    # phase 1: verify only
+    r1 = oracle.step_paged(q1, k1, v1, b1, g1, pool, idx, [0] * N, [0] * N)
+    for i in range(N):
+        for h in range(H):
+            np.testing.assert_array_equal(r1[(i, h)][1], pool[int(idx[i]), h].double().numpy())
+    # phase 2: [pad | accepted prefix | next draft], first_slot = R - a, commit after R slots
+    L = R + L2
+    cat = lambda a1, a2, zero_shape: torch.stack(
+        [torch.cat([torch.zeros(R - acc[i], *zero_shape), a1[i, :acc[i]], a2[i]], 0) for i in range(N)])
+    q = cat(q1, q2, (H, d)); k = cat(k1, k2, (H, d)); v = cat(v1, v2, (H, d))
+    g = cat(g1, g2, (H, d)); beta = cat(b1, b2, (H,))
+    first = [R - a for a in acc]
+    r2 = oracle.step_paged(q, k, v, beta, g, pool, idx, first, [R] * N)
+    for i in range(N):
+        a = acc[i]
+        qq = torch.cat([q1[i, :a], q2[i]]); kk = torch.cat([k1[i, :a], k2[i]]); vv = torch.cat([v1[i, :a], v2[i]])
+        bb = torch.cat([b1[i, :a], b2[i]]); gg = torch.cat([g1[i, :a], g2[i]])
+        s0 = pool[int(idx[i])][None]
+        o_f, _ = run_fwd(qq, kk, vv, bb, gg, [a + L2], s0)
+        if a:
+            _, h_a = run_fwd(qq[:a], kk[:a], vv[:a], bb[:a], gg[:a], [a], s0)
+        for h in range(H):
+            o_s, s_s = r2[(i, h)]
+            np.testing.assert_allclose(o_s, o_f[:, h], rtol=1e-12, atol=1e-14)
+            ref = h_a[0, h] if a else pool[int(idx[i]), h].double().numpy()
+            np.testing.assert_allclose(s_s, ref, rtol=1e-12, atol=1e-14)
+
+
 def test_contraction_bound():
     """|k^|<=1, beta in [0,1], g<=0 make (I - beta k^k^T) Diag(e^g) a contraction:
     |S_t|_F <= |S_{t-1}|_F + beta |v_t|."""

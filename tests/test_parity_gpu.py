@@ -222,6 +222,105 @@ def test_step_equals_forward(kda):
         assert rel(st[i].cpu(), hf[0].cpu()) < 1e-2
 
 
+def _paged_case(N, L, H, P, seed):
+    d = make_decode_batch(N, L, H, "bf16", seed=seed)
+    gen = torch.Generator().manual_seed(seed + 7)
+    pool = torch.randn(P, H, 128, 128, generator=gen) * 0.02
+    idx = torch.randperm(P, generator=gen)[:N].to(torch.int32)
+    first = torch.randint(0, L + 1, (N,), generator=gen, dtype=torch.int32)
+    acc = torch.randint(0, L + 1, (N,), generator=gen, dtype=torch.int32)
+    return d, pool, idx, first, acc
+
+
+def check_paged(kda, d, pool, idx, first, acc):
+    N, L, H, _ = d.q.shape
+    st = pool.clone().cuda()
+    o = torch.full(d.v.shape, 7.0, dtype=d.v.dtype, device="cuda")   # padded slots keep this
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_step(d.q.cuda(), d.k.cuda(), d.v.cuda(), d.beta.cuda(), d.g.cuda(), st, acc.cuda(), out=o,
+                 state_indices=idx.cuda(), first_slot=first.cuda(), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    res = oracle.step_paged(d.q, d.k, d.v, d.beta, d.g, pool, idx.tolist(), first.tolist(), acc.tolist())
+    o, st = o.float().cpu(), st.cpu()
+    touched = set()
+    for i in range(N):
+        f, slot = int(first[i]), int(idx[i])
+        touched.add(slot)
+        assert torch.all(o[i, :f] == 7.0), i
+        for h in range(H):
+            o_ref, s_ref = res[(i, h)]
+            if f < L:
+                assert rel(o[i, f:, h], o_ref) <= TOL["bf16"], (i, h)
+            assert rel(st[slot, h], s_ref) <= TOL["bf16"], (i, h)
+    for slot in range(pool.shape[0]):
+        if slot not in touched:
+            assert torch.equal(st[slot], pool[slot]), slot
+
+
+def test_step_paged_pool(kda):
+    check_paged(kda, *_paged_case(6, 4, 3, 11, seed=31))
+
+
+def test_step_paged_full_padding_and_eight_slots(kda):
+    d, pool, idx, first, acc = _paged_case(5, 8, 2, 9, seed=32)
+    first[0], acc[0] = 8, 8       # all padding: nothing written, state unchanged
+    first[1], acc[1] = 3, 2       # commit point inside the padding: state unchanged
+    check_paged(kda, d, pool, idx, first, acc)
+
+
+def test_step_verify_then_replay(kda):
+    # phase 1 verifies a draft without committing; phase 2 replays the accepted prefix and
+    # verifies the next draft in one call (padding first): committed states and the new draft's
+    # outputs match the oracle's token loop over accepted prefix + new draft
+    N, L1, L2, H, P = 4, 4, 4, 2, 6
+    d1 = make_decode_batch(N, L1, H, "bf16", seed=41)
+    d2 = make_decode_batch(N, L2, H, "bf16", seed=42)
+    gen = torch.Generator().manual_seed(43)
+    pool = torch.randn(P, H, 128, 128, generator=gen) * 0.02
+    idx = torch.tensor([5, 1, 2, 0], dtype=torch.int32)
+    acc = torch.tensor([3, 0, 4, 1], dtype=torch.int32)
+    st = pool.clone().cuda()
+    zeros = torch.zeros(N, dtype=torch.int32, device="cuda")
+    kda.kda_step(d1.q.cuda(), d1.k.cuda(), d1.v.cuda(), d1.beta.cuda(), d1.g.cuda(), st, zeros,
+                 state_indices=idx.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(st.cpu(), pool)
+    R = L1
+    cat = lambda a1, a2: torch.stack([torch.cat([torch.zeros_like(a1[i, :R - int(acc[i])]), a1[i, :int(acc[i])],
+                                                 a2[i]], 0) for i in range(N)])
+    q, k, v = cat(d1.q, d2.q), cat(d1.k, d2.k), cat(d1.v, d2.v)
+    beta, g = cat(d1.beta, d2.beta), cat(d1.g, d2.g)
+    first = (R - acc).to(torch.int32)
+    o = kda.kda_step(q.cuda(), k.cuda(), v.cuda(), beta.cuda(), g.cuda(), st, torch.full((N,), R, dtype=torch.int32),
+                     state_indices=idx.cuda(), first_slot=first.cuda())
+    torch.cuda.synchronize()
+    for i in range(N):
+        a = int(acc[i])
+        qq = torch.cat([d1.q[i, :a], d2.q[i]])[None]; kk = torch.cat([d1.k[i, :a], d2.k[i]])[None]
+        vv = torch.cat([d1.v[i, :a], d2.v[i]])[None]; bb = torch.cat([d1.beta[i, :a], d2.beta[i]])[None]
+        gg = torch.cat([d1.g[i, :a], d2.g[i]])[None]
+        slot = int(idx[i])
+        res = oracle.step(qq, kk, vv, bb, gg, pool[slot:slot + 1], torch.tensor([a], dtype=torch.int32))
+        for h in range(H):
+            o_ref, s_ref = res[(0, h)]
+            assert rel(o[i, R:, h].float().cpu(), o_ref[a:]) <= TOL["bf16"], (i, h)
+            assert rel(st[slot, h].cpu(), s_ref) <= TOL["bf16"], (i, h)
+
+
+def test_step_bad_state_index_reports(kda):
+    d, pool, idx, first, acc = _paged_case(3, 4, 2, 4, seed=51)
+    idx[1] = 4                     # outside the pool of 4 slots
+    st = pool.clone().cuda()
+    o = torch.full(d.v.shape, 7.0, dtype=d.v.dtype, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_step(d.q.cuda(), d.k.cuda(), d.v.cuda(), d.beta.cuda(), d.g.cuda(), st, acc.cuda(), out=o,
+                 state_indices=idx.cuda(), first_slot=first.cuda(), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1                      # KDA_ERR_INVALID_ARG
+    assert torch.all(o[1].float() == 7.0)               # that sequence is left untouched
+
+
 # ---------------------------------------------------------------- full-size workloads (sampled)
 
 def _sampled(b, heads):

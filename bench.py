@@ -245,11 +245,45 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.empty_cache()
     if not args.no_decode:
         out["decode"] = bench_decode(args, dev, lib, stream, peaks)
+    if not args.no_cp:
+        out["cp_forward"] = bench_cp(args, dev, peaks, out["fwd"]["ms"])
     if host is not None:
         out["e2e"] = bench_e2e(args, dev, world, host)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
     return out
+
+
+def bench_cp(args, dev, peaks, fwd_ms, P=4):
+    """Context-parallel forward emulated on one GPU: the sequence cut into P segments,
+    each segment's (M, b) from two forward passes, the combine, and a forward over the
+    segments from their incoming states (what each of P devices would run on its own
+    segment, plus the state exchange)."""
+    import torch
+    import gated_delta_rule_chunked_gb300 as kda
+    from gated_delta_rule_chunked_gb300.inputs import make_workload
+    b = make_workload(WORKLOAD, device=dev)
+    T = b.q.shape[0]
+    cu = b.cu_seqlens.cpu()
+    run = lambda: kda.kda_fwd_cp(b.q, b.k, b.v, b.beta, b.g, cu, b.h0, n_segments=P)
+    for _ in range(max(args.warmup, 3)):
+        run()
+    K = max(3, min(args.steps, 10))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    s.record()
+    for _ in range(K):
+        run()
+    e.record()
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e) / K
+    H = b.q.shape[1]
+    gbs = FWD_BYTES * T * H / (ms * 1e-3) / 1e9
+    return {"workload": f"cp{P}-{WORKLOAD.replace('fwdbwd', 'fwd')}", "segments": P, "ms": ms,
+            "unsplit_fwd_ms": fwd_ms, "tokens_per_s": T / (ms * 1e-3), "gbs_algorithmic": gbs,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"]},
+            "note": "one GPU runs all P segments: 3 forward passes (segment maps, offsets, final) + the combine"}
 
 
 def bench_decode(args, dev, lib, stream, peaks):
@@ -461,6 +495,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cp", action="store_true", help="skip the context-parallel forward emulation")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16384)

@@ -48,23 +48,27 @@ def _stream(device) -> int:
 
 def _check_inputs(q, k, v, beta, g):
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+        if t is None and name == "v":
+            continue
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     if beta.dtype != torch.float32 or g.dtype != torch.float32:
         raise TypeError("beta and g must be float32")
-    if k.dtype != q.dtype or v.dtype != q.dtype:
+    if k.dtype != q.dtype or (v is not None and v.dtype != q.dtype):
         raise TypeError("q, k and v must share one dtype")
 
 
 def fwd_args(q, k, v, beta, g, cu_seqlens=None, h0=None, o=None, hT=None, saved=None,
-             workspace=None, scale: float = 1.0, n_seqs: Optional[int] = None, dev_status=None) -> _lib.FwdArgs:
+             workspace=None, scale: float = 1.0, n_seqs: Optional[int] = None, dev_status=None,
+             h0_identity: bool = False) -> _lib.FwdArgs:
     """Fill the C argument struct for kda_fwd from tensors (no allocation)."""
     a = _lib.FwdArgs()
     total, H, dk = q.shape
     a.n_seqs = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (n_seqs or 1)
-    a.total_tokens, a.heads, a.dk, a.dv, a.chunk = total, H, dk, v.shape[2], 64
+    a.total_tokens, a.heads, a.dk, a.dv, a.chunk = total, H, dk, (v.shape[2] if v is not None else dk), 64
+    a.h0_identity = int(h0_identity)
     a.scale, a.io_dtype = scale, _io_dtype(q)
     a.cu_seqlens = _ptr(cu_seqlens)
     a.q, a.k, a.v, a.beta, a.g = _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g)
@@ -124,6 +128,79 @@ def kda_fwd(q, k, v, beta, g, cu_seqlens=None, h0=None, *, scale: float = 1.0, s
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws_bytes
     _lib.check(lib.kda_fwd(C.byref(a), _stream(dev)))
     return o, hT, saved
+
+
+def _fwd_states(q, k, v, beta, g, cu, h0, N, *, scale, h0_identity=False, out=None, ws=None):
+    """One forward pass for its final states (and outputs into ``out`` when given). With
+    ``ws`` (the workspace of an earlier pass on the same q, k, g, beta, cu) the chunk records
+    are reused and only the scan runs; returns (hT, workspace)."""
+    lib = library()
+    dev = q.device
+    hT = torch.empty((N, q.shape[1], 128, 128), dtype=torch.float32, device=dev)
+    a = fwd_args(q, k, v, beta, g, cu, h0, out, hT, None, None, scale, n_seqs=N, h0_identity=h0_identity)
+    ws_bytes = lib.kda_fwd_workspace_size(C.byref(a))
+    if ws is None:
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    else:
+        a.skip_prep = 1
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws_bytes
+    _lib.check(lib.kda_fwd(C.byref(a), _stream(dev)))
+    return hT, ws
+
+
+def kda_cp_combine(M, b, h0, n_segments: int):
+    """States entering each segment: S_in[:, 0] = h0, S_in[:, k+1] = M[:, k] S_in[:, k] + b[:, k].
+
+    M, b: [N, P, H, 128, 128] fp32 (maps and offsets of the segments); h0: [N, H, 128, 128]
+    fp32 or None. Returns S_in [N, P, H, 128, 128].
+    """
+    lib = library()
+    N, P, H = M.shape[:3]
+    if P != n_segments or b.shape != M.shape or (h0 is not None and h0.shape != (N, H, 128, 128)):
+        raise ValueError("M, b must be [N, P, H, 128, 128] and h0 [N, H, 128, 128]")
+    s_in = torch.empty_like(M)
+    a = _lib.CpArgs(N, P, H, 128, 128, M.data_ptr(), b.data_ptr(), _ptr(h0), s_in.data_ptr())
+    _lib.check(lib.kda_cp_combine(C.byref(a), _stream(M.device)))
+    return s_in
+
+
+def cp_segments(cu_seqlens, n_segments: int, total: Optional[int] = None):
+    """Segment boundaries: every sequence cut into n_segments runs of whole 64-token chunks
+    (as equal as chunk alignment allows; trailing segments may be empty). Host-side."""
+    cu = cu_seqlens.to("cpu", torch.int64).tolist() if cu_seqlens is not None else [0, total]
+    seg = [0]
+    for s0, s1 in zip(cu[:-1], cu[1:]):
+        nch = (s1 - s0 + 63) // 64
+        for kk in range(1, n_segments + 1):
+            seg.append(min(s1, s0 + 64 * ((nch * kk) // n_segments)))
+    return torch.tensor(seg, dtype=torch.int32)
+
+
+def kda_fwd_cp(q, k, v, beta, g, cu_seqlens=None, h0=None, *, n_segments: int, scale: float = 1.0):
+    """Forward by context parallelism, emulated on one device: every sequence is cut into
+    n_segments consecutive segments that are processed independently (as separate
+    sequences), their affine maps combined, and the segments run again from the combined
+    incoming states. Returns (o, hT) of the unsplit forward.
+
+    Pass 1: M = final states from the identity with zero values (each segment's linear map);
+    pass 2: b = final states from zero; combine: the state entering each segment;
+    pass 3: the forward over each segment from its incoming state. The chunk records (they
+    depend on q, k, g and beta only) are computed once, in pass 1.
+    """
+    _check_inputs(q, k, v, beta, g)
+    dev = q.device
+    total, H = q.shape[0], q.shape[1]
+    seg = cp_segments(cu_seqlens, n_segments, total)
+    N = (len(seg) - 1) // n_segments
+    S = N * n_segments
+    segd = _i32(seg, dev)
+    M, ws = _fwd_states(q, k, None, beta, g, segd, None, S, scale=scale, h0_identity=True)
+    b, _ = _fwd_states(q, k, v, beta, g, segd, None, S, scale=scale, ws=ws)       # same records
+    h0c = None if h0 is None else h0.contiguous()
+    s_in = kda_cp_combine(M.view(N, n_segments, H, 128, 128), b.view(N, n_segments, H, 128, 128), h0c, n_segments)
+    o = torch.empty_like(v)
+    hT, _ = _fwd_states(q, k, v, beta, g, segd, s_in.view(S, H, 128, 128), S, scale=scale, out=o, ws=ws)
+    return o, hT.view(N, n_segments, H, 128, 128)[:, -1].contiguous()
 
 
 def kda_bwd(q, k, v, beta, g, dO, saved, cu_seqlens=None, h0=None, dhT=None, *, scale: float = 1.0,

@@ -14,11 +14,12 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT 
 KDA_BF16, KDA_F32 = 0, 1
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
                 4: "KDA_ERR_TIMEOUT"}
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 # every symbol include/kda.h declares
 EXPORTS = ("kda_fwd", "kda_fwd_workspace_size", "kda_saved_size", "kda_bwd", "kda_bwd_workspace_size",
-           "kda_step", "kda_fwd_no_alloc", "kda_set_profile_events", "kda_last_error", "kda_abi_version")
+           "kda_step", "kda_cp_combine", "kda_fwd_no_alloc", "kda_set_profile_events", "kda_last_error",
+           "kda_abi_version")
 NO_ALLOC_SCRATCH_BYTES = 256 * 1024 * 1024
 
 
@@ -30,6 +31,14 @@ class FwdArgs(C.Structure):
         ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p), ("beta", C.c_void_p), ("g", C.c_void_p),
         ("h0", C.c_void_p), ("o", C.c_void_p), ("hT", C.c_void_p), ("saved", C.c_void_p),
         ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("dev_status", C.c_void_p),
+        ("h0_identity", C.c_int32), ("skip_prep", C.c_int32),
+    ]
+
+
+class CpArgs(C.Structure):
+    _fields_ = [
+        ("n_seqs", C.c_int32), ("n_segments", C.c_int32), ("heads", C.c_int32), ("dk", C.c_int32), ("dv", C.c_int32),
+        ("M", C.c_void_p), ("b", C.c_void_p), ("h0", C.c_void_p), ("s_in", C.c_void_p),
     ]
 
 
@@ -76,6 +85,8 @@ def load(path: str = LIB_PATH):
     lib.kda_bwd.restype = C.c_int
     lib.kda_step.argtypes = [C.POINTER(StepArgs), C.c_void_p]
     lib.kda_step.restype = C.c_int
+    lib.kda_cp_combine.argtypes = [C.POINTER(CpArgs), C.c_void_p]
+    lib.kda_cp_combine.restype = C.c_int
     lib.kda_fwd_workspace_size.argtypes = [C.POINTER(FwdArgs)]
     lib.kda_fwd_workspace_size.restype = C.c_size_t
     lib.kda_saved_size.argtypes = [C.POINTER(FwdArgs)]

@@ -159,10 +159,18 @@ kda_status check_fwd(const kda_fwd_args *a, const char *who) {
     return fail(KDA_ERR_INVALID_ARG, "%s: cu_seqlens must be 4-byte aligned", who);
   const void *need[] = {a->q, a->k, a->v, a->g, a->o};
   const char *names[] = {"q", "k", "v", "g", "o"};
+  // v and o may be NULL (zero values / no output) in a bf16 forward that saves nothing
+  const bool vo_optional = a->io_dtype == KDA_BF16 && !a->saved;
   for (int i = 0; i < 5; ++i) {
-    if (!need[i] && a->total_tokens > 0) return fail(KDA_ERR_INVALID_ARG, "%s: required pointer is NULL", names[i]);
+    const bool optional = vo_optional && (i == 2 || i == 4);
+    if (!need[i] && a->total_tokens > 0 && !optional)
+      return fail(KDA_ERR_INVALID_ARG, "%s: required pointer is NULL", names[i]);
     if (!aligned(need[i], 16)) return fail(KDA_ERR_INVALID_ARG, "%s: pointer is not 16-byte aligned", names[i]);
   }
+  if (a->h0_identity && a->io_dtype != KDA_BF16)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: h0_identity needs io_dtype KDA_BF16", who);
+  if (a->skip_prep && (a->io_dtype != KDA_BF16 || a->saved))
+    return fail(KDA_ERR_UNSUPPORTED, "%s: skip_prep needs io_dtype KDA_BF16 and no saved", who);
   if (!a->beta && a->total_tokens > 0) return fail(KDA_ERR_INVALID_ARG, "%s: beta is NULL", who);
   if (!aligned(a->beta, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: beta is not 4-byte aligned", who);
   const void *opt[] = {a->h0, a->hT, a->saved, a->workspace};
@@ -204,7 +212,26 @@ void kda::set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
 
 extern "C" {
 
-int32_t kda_abi_version(void) { return 2; }
+int32_t kda_abi_version(void) { return 3; }
+
+kda_status kda_cp_combine(const kda_cp_args *a, cudaStream_t stream) {
+  if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", "kda_cp_combine");
+  if (a->dk != 128 || a->dv != 128)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: only dk = dv = 128 is supported", "kda_cp_combine");
+  if (a->n_seqs < 0 || a->heads < 1 || a->n_segments < 1)
+    return fail(KDA_ERR_INVALID_ARG, "%s: need n_seqs >= 0, heads >= 1, n_segments >= 1", "kda_cp_combine");
+  if (a->n_seqs == 0) {
+    g_last_error.clear();
+    return KDA_OK;
+  }
+  if (!a->M || !a->b || !a->s_in) return fail(KDA_ERR_INVALID_ARG, "%s: M, b and s_in are required", "kda_cp_combine");
+  if (!aligned(a->M, 16) || !aligned(a->b, 16) || !aligned(a->h0, 16) || !aligned(a->s_in, 16))
+    return fail(KDA_ERR_INVALID_ARG, "%s: M, b, h0 and s_in must be 16-byte aligned", "kda_cp_combine");
+  const cudaError_t e = kda::launch_cp_combine(a->n_seqs, a->n_segments, a->heads, a->M, a->b, a->h0, a->s_in, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_cp_combine");
+  g_last_error.clear();
+  return KDA_OK;
+}
 
 void kda_set_profile_events(cudaEvent_t *events, int32_t n_events) {
   g_prof_events = events;
@@ -281,9 +308,9 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
   pp.tm_q = tm_q;
   pp.tm_k = tm_k;
   pp.tm_g = tm_g;
-  if ((e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
+  if (!a->skip_prep && (e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
-  kda::FwdScanParams sp{geo, a->v, rec, a->h0, a->o, a->hT, a->saved, a->dev_status};
+  kda::FwdScanParams sp{geo, a->v, rec, a->h0, a->o, a->hT, a->saved, a->dev_status, a->h0_identity != 0};
   e = f32 ? kda::launch_fwd_scan(sp, true, pick_slice(a), stream) : kda::launch_fwd_scan_tc(sp, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_fwd scan");
   mark(2, stream);
@@ -300,6 +327,7 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
   if (st != KDA_OK) return st;
   if (f->io_dtype == KDA_F32)
     return fail(KDA_ERR_UNSUPPORTED, "%s: the backward supports io_dtype KDA_BF16 only", "kda_bwd");
+  if (!f->v && f->total_tokens > 0) return fail(KDA_ERR_INVALID_ARG, "%s: v is NULL", "kda_bwd");
   const WsPlan w = plan(f, true);
   if (!a->workspace || a->workspace_bytes < w.bytes)
     return fail(KDA_ERR_INVALID_ARG, "%s: workspace missing or smaller than kda_bwd_workspace_size()", "kda_bwd");

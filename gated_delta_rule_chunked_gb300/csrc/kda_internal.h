@@ -82,6 +82,7 @@ struct FwdScanParams {
   void *saved;             // [max_chunks][H] chunk-start states S^T[v][k] as 128x128 E tiles
                            // (swizzled), or null
   int *status;
+  int h0_identity;         // start every sequence from the identity state (h0 ignored)
 };
 
 struct BwdScanParams {
@@ -133,6 +134,8 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_scan_tc(const BwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_chunk_tc(const BwdChunkParams &p, cudaStream_t s);
 cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_cp_combine(int n_seqs, int n_segments, int heads, const float *M, const float *b, const float *h0,
+                              float *s_in, cudaStream_t s);
 
 // Sets the message that kda_last_error() returns on this host thread.
 void set_last_error(const char *msg);

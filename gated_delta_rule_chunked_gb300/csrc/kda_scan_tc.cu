@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
       for (int cb = 0; cb < 8; ++cb) {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          buf[i] = p.h0 ? p.h0[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f;
+          buf[i] = p.h0_identity ? (16 * cb + i == row ? 1.f : 0.f)
+                                 : (p.h0 ? p.h0[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f);
         tc::st16(tl + set_of(1) + 16 * cb, buf);
       }
       tc::wait_st();
@@ -234,8 +235,8 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int idx = row + 128 * i, r = idx >> 4, ch = idx & 15;
-        vr[i] = make_uint4(0, 0, 0, 0);
-        if (r < clen) vr[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
+        vr[i] = make_uint4(0, 0, 0, 0);   // rows past the end, or no values at all
+        if (v && r < clen) vr[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
       }
     };
     // raw rows -> staging tile -> V^T operand (row = value channel, 64 tokens); then signal
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int tok = 8 * k + (lane >> 2), ch = 4 * qw + (lane & 3);   // 16-byte chunk ch of row tok
-        if (tok < clen)
+        if (o && tok < clen)
           *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + tok) * H + h) * 128 + ch * 8) =
               *reinterpret_cast<const uint4 *>(smem + S::OST + tok * 256 + ch * 16);
       }

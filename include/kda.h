@@ -76,11 +76,13 @@ typedef struct {
                                   N sequences of equal length total/N                   */
     const void *q;             /* [total, H, dk]                                         */
     const void *k;             /* [total, H, dk]                                         */
-    const void *v;             /* [total, H, dv]                                         */
+    const void *v;             /* [total, H, dv], or NULL for zero values (bf16 forward
+                                  without `saved`)                                        */
     const float *beta;         /* [total, H]                                             */
     const float *g;            /* [total, H, dk] log-decay                               */
     const float *h0;           /* [N, H, dk, dv] initial states, or NULL for zero        */
-    void *o;                   /* out [total, H, dv]                                     */
+    void *o;                   /* out [total, H, dv], or NULL: not written (bf16 forward
+                                  without `saved`)                                        */
     float *hT;                 /* out [N, H, dk, dv] final states, or NULL               */
     void *saved;               /* out, kda_saved_size() bytes: what kda_bwd needs from this
                                   forward (chunk-start states; for bf16 also the forward's
@@ -89,6 +91,14 @@ typedef struct {
     void *workspace;           /* scratch, kda_fwd_workspace_size() bytes                */
     size_t workspace_bytes;
     int32_t *dev_status;       /* optional device int32, see above                       */
+    /* ABI version 3: */
+    int32_t h0_identity;       /* nonzero: every sequence starts from the identity state
+                                  (dk = dv), h0 is ignored. With v = NULL the final state
+                                  is then the sequence's linear map on its initial state  */
+    int32_t skip_prep;         /* nonzero: the workspace still holds the chunk records of a
+                                  previous bf16 kda_fwd (without saved) on the same q, k, g,
+                                  beta and sequence layout; only the scan runs (the records
+                                  do not depend on v, h0 or the initial state)            */
 } kda_fwd_args;
 
 /* Backward of kda_fwd: gradients of <dO, o> + <dhT, hT>. */
@@ -171,6 +181,30 @@ size_t kda_bwd_workspace_size(const kda_bwd_args *args);
  * draft are computed from it. state_indices addresses states in a pool (paged
  * state cache), so sequences keep their slot across calls. */
 kda_status kda_step(const kda_step_args *args, cudaStream_t stream);
+
+/*
+ * kda_cp_combine -- context parallelism by segment-affine combine (the pages' CP
+ * paragraphs: the sequence split across devices, with a state exchange between them).
+ * Each sequence is split into P consecutive segments; a segment maps its incoming
+ * state affinely, S_out = M S_in + b, where M (dk x dk) is the final state of a forward
+ * over the segment from the identity with zero values (h0_identity, v = NULL) and b is
+ * the final state of a forward from zero. Given M and b of every segment (computed
+ * independently, e.g. on P devices), this writes the state entering each segment:
+ * S_in[0] = h0, S_in[k+1] = M[k] S_in[k] + b[k]; a forward over each segment from
+ * S_in then reproduces the unsplit forward.
+ */
+typedef struct {
+    int32_t n_seqs;            /* N                                                      */
+    int32_t n_segments;        /* P >= 1 segments per sequence                           */
+    int32_t heads;             /* H                                                      */
+    int32_t dk, dv;            /* 128, 128                                               */
+    const float *M;            /* [N, P, H, dk, dk] fp32                                 */
+    const float *b;            /* [N, P, H, dk, dv] fp32                                 */
+    const float *h0;           /* [N, H, dk, dv] fp32, or NULL for zero                  */
+    float *s_in;               /* out [N, P, H, dk, dv] fp32                             */
+} kda_cp_args;
+
+kda_status kda_cp_combine(const kda_cp_args *args, cudaStream_t stream);
 
 /*
  * kda_fwd_no_alloc -- kda_fwd for callers that cannot allocate device memory.

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.kda_abi_version() == 2
+    assert lib.kda_abi_version() == 3
 
 
 def test_struct_layout_matches_c(tmp_path):

@@ -282,6 +282,47 @@ def test_paged_decode_verify_then_replay():
             np.testing.assert_allclose(s_s, ref, rtol=1e-12, atol=1e-14)
 
 
+def test_state_map_is_affine():
+    # The recurrence is affine in the initial state: the final state from S equals M S + b, with
+    # M the final state from the identity with zero values and b the final state from zero.
+    T, H, d = 37, 2, 16
+    q, k, v, beta, g = rand_inputs(T, H, d, d, seed=61)
+    S = torch.randn(1, H, d, d, generator=torch.Generator().manual_seed(62)) * 0.1
+    eye = torch.eye(d).expand(1, H, d, d).contiguous()
+    _, M = run_fwd(q, k, torch.zeros_like(v), beta, g, [T], eye)
+    _, b = run_fwd(q, k, v, beta, g, [T])
+    _, hS = run_fwd(q, k, v, beta, g, [T], S)
+    for h in range(H):
+        np.testing.assert_allclose(hS[0, h], M[0, h] @ S[0, h].double().numpy() + b[0, h], rtol=1e-12, atol=1e-13)
+
+
+def test_segment_combine_reproduces_unsplit_forward():
+    # Context parallelism: cut the sequence into segments, get each segment's (M, b) on its own,
+    # chain S_in[k+1] = M[k] S_in[k] + b[k] from h0, rerun every segment from S_in[k]: the outputs
+    # and the final state are those of the unsplit forward.
+    T, H, d = 100, 2, 16
+    q, k, v, beta, g = rand_inputs(T, H, d, d, seed=63)
+    h0 = torch.randn(1, H, d, d, generator=torch.Generator().manual_seed(64)) * 0.1
+    o_ref, h_ref = run_fwd(q, k, v, beta, g, [T], h0)
+    cuts = [0, 30, 64, 81, 100]
+    eye = torch.eye(d).expand(1, H, d, d).contiguous()
+    s_in = h0[0].double().numpy()
+    outs = []
+    for a, e in zip(cuts[:-1], cuts[1:]):
+        sl = slice(a, e)
+        s32 = torch.from_numpy(s_in).float()   # a handed-over state is fp32, as h0 is
+        _, M = run_fwd(q[sl], k[sl], torch.zeros_like(v[sl]), beta[sl], g[sl], [e - a], eye)
+        _, b = run_fwd(q[sl], k[sl], v[sl], beta[sl], g[sl], [e - a])
+        o_seg, h_seg = run_fwd(q[sl], k[sl], v[sl], beta[sl], g[sl], [e - a], s32[None])
+        outs.append(o_seg)
+        s_next = np.stack([M[0, h] @ s32[h].double().numpy() + b[0, h] for h in range(H)])
+        np.testing.assert_allclose(h_seg[0], s_next, rtol=1e-11, atol=1e-12)
+        s_in = s_next
+    # against the unsplit forward, up to the fp32 rounding of the three handed-over states
+    np.testing.assert_allclose(np.concatenate(outs, 0), o_ref, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(s_in, h_ref[0], rtol=1e-5, atol=1e-6)
+
+
 def test_contraction_bound():
     """|k^|<=1, beta in [0,1], g<=0 make (I - beta k^k^T) Diag(e^g) a contraction:
     |S_t|_F <= |S_{t-1}|_F + beta |v_t|."""

@@ -321,6 +321,47 @@ def test_step_bad_state_index_reports(kda):
     assert torch.all(o[1].float() == 7.0)               # that sequence is left untouched
 
 
+# ---------------------------------------------------------------- context parallelism (emulated)
+
+def test_cp_combine_vs_fp64_chain(kda):
+    N, P, H = 2, 3, 2
+    gen = torch.Generator().manual_seed(71)
+    M = torch.randn(N, P, H, 128, 128, generator=gen) / 12
+    b = torch.randn(N, P, H, 128, 128, generator=gen) * 0.1
+    h0 = torch.randn(N, H, 128, 128, generator=gen) * 0.1
+    s_in = kda.kda_cp_combine(M.cuda(), b.cuda(), h0.cuda(), P).cpu()
+    for n in range(N):
+        for h in range(H):
+            s = h0[n, h].double()
+            for kk in range(P):
+                assert rel(s_in[n, kk, h], s.numpy()) <= 1e-5, (n, kk, h)
+                s = M[n, kk, h].double() @ s + b[n, kk, h].double()
+
+
+def test_fwd_identity_start_zero_values(kda):
+    # the segment map: final state from the identity with zero values, no outputs written
+    b = make_seq_batch([300, 64], heads=2, io_dtype="bf16", seed=72, h0=False)
+    t = to_dev(b)
+    M, _ = kda._fwd_states(t["q"], t["k"], None, t["beta"], t["g"], t["cu_seqlens"], None, 2, scale=1.0,
+                           h0_identity=True)
+    eye = torch.eye(128).expand(2, 2, 128, 128).contiguous()
+    res = oracle.fwd(b.q, b.k, torch.zeros_like(b.v), b.beta, b.g, b.cu_seqlens, eye)
+    _, m_ref = oracle.assemble_fwd(res, b.cu_seqlens, 2, 128)
+    assert rel(M.cpu(), m_ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("lens,P", [([1000], 3), ([1000], 1), ([100, 900], 4)])
+def test_fwd_cp_matches_unsplit(kda, lens, P):
+    b = make_seq_batch(lens, heads=3, io_dtype="bf16", seed=73 + P, h0=True)
+    t = to_dev(b)
+    o, hT = kda.kda_fwd_cp(t["q"], t["k"], t["v"], t["beta"], t["g"], b.cu_seqlens.cpu(), t["h0"], n_segments=P)
+    res = oracle.fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0)
+    o_ref, h_ref = oracle.assemble_fwd(res, b.cu_seqlens, 3, 128)
+    e_o, e_h = rel(o.float().cpu(), o_ref), rel(hT.cpu(), h_ref)
+    print("cp", lens, P, f"o {e_o:.2e} hT {e_h:.2e}")
+    assert e_o <= TOL["bf16"] and e_h <= TOL["bf16"], (e_o, e_h)
+
+
 # ---------------------------------------------------------------- full-size workloads (sampled)
 
 def _sampled(b, heads):

@@ -247,11 +247,48 @@ def run_ours(args, rank, world, local_rank):
         out["decode"] = bench_decode(args, dev, lib, stream, peaks)
     if not args.no_cp:
         out["cp_forward"] = bench_cp(args, dev, peaks, out["fwd"]["ms"])
+    if not args.no_attnres:
+        out["attnres"] = bench_attnres(args, dev, peaks)
     if host is not None:
         out["e2e"] = bench_e2e(args, dev, world, host)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
     return out
+
+
+def bench_attnres(args, dev, peaks, T=32768, S=9, d=7168):
+    """Attention Residuals at the K3 width: 9 sources x 7168 channels per token, bf16.
+    Algorithmic bytes: forward reads the sources once and writes out; backward reads the
+    sources and d_out once and writes every d_source (the [T, S] statistics are negligible)."""
+    import torch
+    import gated_delta_rule_chunked_gb300 as kda
+    gen = torch.Generator(device=dev).manual_seed(7168)
+    src = [torch.randn(T, d, generator=gen, device=dev).to(torch.bfloat16) for _ in range(S)]
+    w = torch.randn(d, generator=gen, device=dev) / d ** 0.5
+    g = torch.randn(T, d, generator=gen, device=dev).to(torch.bfloat16)
+    K = max(args.steps, 10)
+    res = {}
+    for name in ("fwd", "bwd"):
+        out, stats = kda.attnres_fwd(src, w)
+        run = (lambda: kda.attnres_fwd(src, w)) if name == "fwd" else (lambda: kda.attnres_bwd(src, w, stats, g))
+        for _ in range(max(args.warmup, 3)):
+            run()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        s.record()
+        for _ in range(K):
+            run()
+        e.record()
+        torch.cuda.synchronize(dev)
+        ms = s.elapsed_time(e) / K
+        byts = T * d * 2 * ((S + 1) if name == "fwd" else (2 * S + 1))
+        gbs = byts / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "gbs_algorithmic": gbs,
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": gbs / peaks["hbm_gbs"]}}
+    return {"workload": f"attnres-bf16-T{T}-S{S}-d{d}", **res,
+            "tokens_per_s_fwd_bwd": T / ((res["fwd"]["ms"] + res["bwd"]["ms"]) * 1e-3),
+            "l2": "sources (4.2 GB) larger than L2; no flush"}
 
 
 def bench_cp(args, dev, peaks, fwd_ms, P=4):
@@ -496,6 +533,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cp", action="store_true", help="skip the context-parallel forward emulation")
+    ap.add_argument("--no-attnres", action="store_true", help="skip the Attention Residuals workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16384)

@@ -203,6 +203,59 @@ def kda_fwd_cp(q, k, v, beta, g, cu_seqlens=None, h0=None, *, n_segments: int, s
     return o, hT.view(N, n_segments, H, 128, 128)[:, -1].contiguous()
 
 
+def _attnres_args(sources, w, eps, out=None, stats=None):
+    S = len(sources)
+    if not 1 <= S <= _lib.ATTNRES_MAX_SOURCES:
+        raise ValueError("Attention Residuals takes 1..9 sources")
+    T, d = sources[0].shape
+    for x in sources:
+        if x.shape != (T, d) or x.dtype != sources[0].dtype or not x.is_cuda or not x.is_contiguous():
+            raise ValueError("sources must be contiguous CUDA tensors of one shape [T, d] and dtype")
+    if w.dtype != torch.float32 or w.shape != (d,) or not w.is_contiguous():
+        raise TypeError("w must be a contiguous float32 [d] tensor")
+    a = _lib.AttnresFwdArgs()
+    a.n_sources, a.tokens, a.dim, a.eps, a.io_dtype = S, T, d, eps, _io_dtype(sources[0])
+    for i, x in enumerate(sources):
+        a.src[i] = x.data_ptr()
+    a.w, a.out = w.data_ptr(), _ptr(out)
+    a.alpha, a.rstd, a.logit = (_ptr(t) for t in stats)
+    return a
+
+
+def attnres_fwd(sources, w, *, eps: float = 1e-6):
+    """Attention Residuals forward: out = sum_i softmax_i(r_i (w . x_i)) x_i over the sources
+    (r_i = 1 / RMS(x_i)). Returns (out [T, d], stats) with stats = (alpha, rstd, logit), each
+    [T, S] fp32, which the backward takes."""
+    lib = library()
+    T, d = sources[0].shape
+    dev = sources[0].device
+    out = torch.empty_like(sources[0])
+    stats = tuple(torch.empty((T, len(sources)), dtype=torch.float32, device=dev) for _ in range(3))
+    a = _attnres_args(sources, w, eps, out, stats)
+    _lib.check(lib.kda_attnres_fwd(C.byref(a), _stream(dev)))
+    return out, stats
+
+
+def attnres_bwd(sources, w, stats, d_out, *, eps: float = 1e-6):
+    """Backward of attnres_fwd: returns (d_sources list, dw [d] fp32)."""
+    lib = library()
+    dev = sources[0].device
+    if d_out.shape != sources[0].shape or d_out.dtype != sources[0].dtype or not d_out.is_contiguous():
+        raise ValueError("d_out must match the sources")
+    b = _lib.AttnresBwdArgs()
+    b.fwd = _attnres_args(sources, w, eps, None, stats)
+    d_src = [torch.empty_like(x) for x in sources]
+    dw = torch.empty_like(w)
+    b.d_out, b.dw = d_out.data_ptr(), dw.data_ptr()
+    for i, x in enumerate(d_src):
+        b.d_src[i] = x.data_ptr()
+    ws_bytes = lib.kda_attnres_bwd_workspace_size(C.byref(b))
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    b.workspace, b.workspace_bytes = ws.data_ptr(), ws_bytes
+    _lib.check(lib.kda_attnres_bwd(C.byref(b), _stream(dev)))
+    return d_src, dw
+
+
 def kda_bwd(q, k, v, beta, g, dO, saved, cu_seqlens=None, h0=None, dhT=None, *, scale: float = 1.0,
             n_seqs: Optional[int] = None, initial_state_grad: bool = True, dev_status=None):
     """Backward of kda_fwd (``saved`` from kda_fwd(..., save=True) with the same inputs).

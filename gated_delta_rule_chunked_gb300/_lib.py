@@ -18,8 +18,9 @@ ABI_VERSION = 3
 
 # every symbol include/kda.h declares
 EXPORTS = ("kda_fwd", "kda_fwd_workspace_size", "kda_saved_size", "kda_bwd", "kda_bwd_workspace_size",
-           "kda_step", "kda_cp_combine", "kda_fwd_no_alloc", "kda_set_profile_events", "kda_last_error",
-           "kda_abi_version")
+           "kda_step", "kda_cp_combine", "kda_attnres_fwd", "kda_attnres_bwd", "kda_attnres_bwd_workspace_size",
+           "kda_fwd_no_alloc", "kda_set_profile_events", "kda_last_error", "kda_abi_version")
+ATTNRES_MAX_SOURCES = 9
 NO_ALLOC_SCRATCH_BYTES = 256 * 1024 * 1024
 
 
@@ -39,6 +40,21 @@ class CpArgs(C.Structure):
     _fields_ = [
         ("n_seqs", C.c_int32), ("n_segments", C.c_int32), ("heads", C.c_int32), ("dk", C.c_int32), ("dv", C.c_int32),
         ("M", C.c_void_p), ("b", C.c_void_p), ("h0", C.c_void_p), ("s_in", C.c_void_p),
+    ]
+
+
+class AttnresFwdArgs(C.Structure):
+    _fields_ = [
+        ("n_sources", C.c_int32), ("tokens", C.c_int64), ("dim", C.c_int32), ("eps", C.c_float),
+        ("io_dtype", C.c_int32), ("src", C.c_void_p * ATTNRES_MAX_SOURCES), ("w", C.c_void_p), ("out", C.c_void_p),
+        ("alpha", C.c_void_p), ("rstd", C.c_void_p), ("logit", C.c_void_p),
+    ]
+
+
+class AttnresBwdArgs(C.Structure):
+    _fields_ = [
+        ("fwd", AttnresFwdArgs), ("d_out", C.c_void_p), ("d_src", C.c_void_p * ATTNRES_MAX_SOURCES),
+        ("dw", C.c_void_p), ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
     ]
 
 
@@ -87,6 +103,12 @@ def load(path: str = LIB_PATH):
     lib.kda_step.restype = C.c_int
     lib.kda_cp_combine.argtypes = [C.POINTER(CpArgs), C.c_void_p]
     lib.kda_cp_combine.restype = C.c_int
+    lib.kda_attnres_fwd.argtypes = [C.POINTER(AttnresFwdArgs), C.c_void_p]
+    lib.kda_attnres_fwd.restype = C.c_int
+    lib.kda_attnres_bwd.argtypes = [C.POINTER(AttnresBwdArgs), C.c_void_p]
+    lib.kda_attnres_bwd.restype = C.c_int
+    lib.kda_attnres_bwd_workspace_size.argtypes = [C.POINTER(AttnresBwdArgs)]
+    lib.kda_attnres_bwd_workspace_size.restype = C.c_size_t
     lib.kda_fwd_workspace_size.argtypes = [C.POINTER(FwdArgs)]
     lib.kda_fwd_workspace_size.restype = C.c_size_t
     lib.kda_saved_size.argtypes = [C.POINTER(FwdArgs)]

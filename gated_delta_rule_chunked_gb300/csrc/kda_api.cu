@@ -214,6 +214,85 @@ extern "C" {
 
 int32_t kda_abi_version(void) { return 3; }
 
+namespace {
+kda_status check_attnres(const kda_attnres_fwd_args *a, const char *who) {
+  if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", who);
+  if (a->io_dtype != KDA_BF16 && a->io_dtype != KDA_F32)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: io_dtype must be KDA_BF16 or KDA_F32", who);
+  if (a->n_sources < 1 || a->n_sources > KDA_ATTNRES_MAX_SOURCES || a->tokens < 0 || a->tokens > 0x7fffffffLL)
+    return fail(KDA_ERR_INVALID_ARG, "%s: need 1 <= n_sources <= 9 and 0 <= tokens < 2^31", who);
+  if (a->dim < 8 || a->dim > 16384 || a->dim % 8 != 0)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: dim must be a multiple of 8 in 8..16384", who);
+  if (!(a->eps > 0.f)) return fail(KDA_ERR_INVALID_ARG, "%s: eps must be positive", who);
+  if (a->tokens == 0) return KDA_OK;
+  for (int i = 0; i < a->n_sources; ++i)
+    if (!a->src[i] || !aligned(a->src[i], 16)) return fail(KDA_ERR_INVALID_ARG, "%s: a source is NULL or misaligned", who);
+  if (!a->w || !aligned(a->w, 16)) return fail(KDA_ERR_INVALID_ARG, "%s: w is NULL or misaligned", who);
+  if (!a->alpha || !a->rstd || !a->logit) return fail(KDA_ERR_INVALID_ARG, "%s: alpha, rstd, logit are required", who);
+  return KDA_OK;
+}
+
+kda::AttnresParams attnres_params(const kda_attnres_fwd_args *a) {
+  kda::AttnresParams p{};
+  p.S = a->n_sources;
+  p.T = a->tokens;
+  p.dim = a->dim;
+  p.eps = a->eps;
+  for (int i = 0; i < a->n_sources; ++i) p.src[i] = a->src[i];
+  p.w = a->w;
+  p.out = a->out;
+  p.alpha = a->alpha;
+  p.rstd = a->rstd;
+  p.logit = a->logit;
+  return p;
+}
+}  // namespace
+
+kda_status kda_attnres_fwd(const kda_attnres_fwd_args *a, cudaStream_t stream) {
+  kda_status st = check_attnres(a, "kda_attnres_fwd");
+  if (st != KDA_OK) return st;
+  if (a->tokens == 0) {
+    g_last_error.clear();
+    return KDA_OK;
+  }
+  if (!a->out || !aligned(a->out, 16)) return fail(KDA_ERR_INVALID_ARG, "%s: out is NULL or misaligned", "kda_attnres_fwd");
+  const cudaError_t e = kda::launch_attnres_fwd(attnres_params(a), a->io_dtype == KDA_F32, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_attnres_fwd");
+  g_last_error.clear();
+  return KDA_OK;
+}
+
+size_t kda_attnres_bwd_workspace_size(const kda_attnres_bwd_args *a) {
+  if (!a || a->fwd.dim < 8 || a->fwd.dim > 16384) return 0;
+  return (size_t)kda::attnres_bwd_ctas(a->fwd.tokens, a->fwd.io_dtype == KDA_F32) * a->fwd.dim * sizeof(float);
+}
+
+kda_status kda_attnres_bwd(const kda_attnres_bwd_args *a, cudaStream_t stream) {
+  if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", "kda_attnres_bwd");
+  kda_status st = check_attnres(&a->fwd, "kda_attnres_bwd");
+  if (st != KDA_OK) return st;
+  if (!a->dw || !aligned(a->dw, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: dw is NULL or misaligned", "kda_attnres_bwd");
+  const size_t need = kda_attnres_bwd_workspace_size(a);
+  if (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 16))
+    return fail(KDA_ERR_INVALID_ARG, "%s: workspace missing, misaligned or smaller than kda_attnres_bwd_workspace_size()",
+                "kda_attnres_bwd");
+  if (a->fwd.tokens > 0) {
+    if (!a->d_out || !aligned(a->d_out, 16)) return fail(KDA_ERR_INVALID_ARG, "%s: d_out is NULL or misaligned", "kda_attnres_bwd");
+    for (int i = 0; i < a->fwd.n_sources; ++i)
+      if (!a->d_src[i] || !aligned(a->d_src[i], 16))
+        return fail(KDA_ERR_INVALID_ARG, "%s: a d_src is NULL or misaligned", "kda_attnres_bwd");
+  }
+  kda::AttnresParams p = attnres_params(&a->fwd);
+  p.dout = a->d_out;
+  for (int i = 0; i < a->fwd.n_sources; ++i) p.dsrc[i] = a->d_src[i];
+  p.dw = a->dw;
+  p.partial = static_cast<float *>(a->workspace);
+  const cudaError_t e = kda::launch_attnres_bwd(p, a->fwd.io_dtype == KDA_F32, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_attnres_bwd");
+  g_last_error.clear();
+  return KDA_OK;
+}
+
 kda_status kda_cp_combine(const kda_cp_args *a, cudaStream_t stream) {
   if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", "kda_cp_combine");
   if (a->dk != 128 || a->dv != 128)

@@ -126,6 +126,25 @@ struct StepParams {
   int *status;
 };
 
+struct AttnresParams {
+  int S;
+  long long T;
+  int dim;
+  float eps;
+  const void *src[9];
+  const float *w;
+  void *out;
+  float *alpha, *rstd, *logit;   // [T][S]
+  const void *dout;
+  void *dsrc[9];
+  float *dw;
+  float *partial;                // [backward CTAs][dim]
+};
+
+cudaError_t launch_attnres_fwd(const AttnresParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_attnres_bwd(const AttnresParams &p, bool f32, cudaStream_t s);
+int attnres_bwd_ctas(long long T, bool f32);
+
 cudaError_t launch_chunk_table(const int *cu_in, int n_seqs, long long total, int *cu_out,
                                int *chunk_off, cudaStream_t s);
 cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s);

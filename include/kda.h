@@ -207,6 +207,45 @@ typedef struct {
 kda_status kda_cp_combine(const kda_cp_args *args, cudaStream_t stream);
 
 /*
+ * Attention Residuals ("Kimi K3 on Fireworks", training section, Attention Residuals
+ * paragraph; the second page's model figure): a sublayer combines up to 9 earlier
+ * representations of each token (the embedding, finished blocks, the current block's
+ * partial sum) with softmax weights scored by a learned pseudo-query w:
+ *     r_i = (mean_c x_ic^2 + eps)^(-1/2),   logit_i = r_i (w . x_i),
+ *     alpha = softmax_i(logit),              out = sum_i alpha_i x_i.
+ * One fused pass per token: the normalised sources and weights are never stored
+ * beyond three [T, S] fp32 statistics for the backward.
+ */
+#define KDA_ATTNRES_MAX_SOURCES 9
+
+typedef struct {
+    int32_t n_sources;         /* S, 1..9                                                */
+    int64_t tokens;            /* T                                                      */
+    int32_t dim;               /* d, a multiple of 8, at most 16384                      */
+    float eps;                 /* inside the RMS (1e-6 in the tests)                     */
+    int32_t io_dtype;          /* kda_dtype of the sources, out, d_out, d_src            */
+    const void *src[KDA_ATTNRES_MAX_SOURCES];   /* S tensors [T, d]                     */
+    const float *w;            /* [d] pseudo-query                                       */
+    void *out;                 /* out [T, d]                                             */
+    float *alpha;              /* out [T, S] softmax weights   (kept for the backward)   */
+    float *rstd;               /* out [T, S] r_i               (kept for the backward)   */
+    float *logit;              /* out [T, S] logit_i           (kept for the backward)   */
+} kda_attnres_fwd_args;
+
+typedef struct {
+    kda_attnres_fwd_args fwd;  /* the forward's arguments and statistics (out unused)    */
+    const void *d_out;         /* [T, d]                                                 */
+    void *d_src[KDA_ATTNRES_MAX_SOURCES];       /* out, S tensors [T, d]               */
+    float *dw;                 /* out [d] fp32                                           */
+    void *workspace;           /* kda_attnres_bwd_workspace_size() bytes (dw partials)   */
+    size_t workspace_bytes;
+} kda_attnres_bwd_args;
+
+kda_status kda_attnres_fwd(const kda_attnres_fwd_args *args, cudaStream_t stream);
+kda_status kda_attnres_bwd(const kda_attnres_bwd_args *args, cudaStream_t stream);
+size_t kda_attnres_bwd_workspace_size(const kda_attnres_bwd_args *args);
+
+/*
  * kda_fwd_no_alloc -- kda_fwd for callers that cannot allocate device memory.
  * (This entry point has no counterpart in the pages; it is a deployment aid.)
  *

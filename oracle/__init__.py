@@ -237,6 +237,45 @@ def step_paged(q, k, v, beta, g, pool, state_indices, first_slot, accept_len, *,
     return out
 
 
+def attnres_fwd(sources, w, eps: float = EPS):
+    """Attention Residuals forward in fp64 ("Kimi K3 on Fireworks", training section,
+    Attention Residuals paragraph; the second page's model figure: alpha = softmax of the
+    learned per-sublayer vector against the RMS-normalised sources, then the weighted sum).
+
+    sources: list of S tensors [T, d]; w: [d]. RMSNorm without a gain (any gain folds into w).
+    Returns (out [T, d], alpha [T, S], rstd [T, S], logit [T, S]) as float64 numpy arrays.
+    """
+    X = torch.stack([x.double() for x in sources], 1)              # [T, S, d]
+    wd = w.double()
+    rstd = (X.pow(2).mean(-1) + eps).rsqrt()                        # [T, S]
+    logit = rstd * (X @ wd)                                         # w . (x / rms(x))
+    alpha = torch.softmax(logit, -1)
+    out = (alpha.unsqueeze(-1) * X).sum(1)
+    return out.numpy(), alpha.numpy(), rstd.numpy(), logit.numpy()
+
+
+def attnres_bwd(sources, w, d_out, eps: float = EPS):
+    """Backward of attnres_fwd in fp64, written out step by step (the chain rule through the
+    weighted sum, the softmax and the RMS normalisation). Returns (d_sources [S][T, d], dw [d])."""
+    X = torch.stack([x.double() for x in sources], 1)              # [T, S, d]
+    wd, g = w.double(), d_out.double()
+    d = X.shape[-1]
+    rstd = (X.pow(2).mean(-1) + eps).rsqrt()
+    N = X * rstd.unsqueeze(-1)                                     # normalised sources
+    logit = N @ wd
+    alpha = torch.softmax(logit, -1)
+    # out = sum_i alpha_i x_i
+    dX = alpha.unsqueeze(-1) * g.unsqueeze(1)                       # direct path
+    dalpha = (X * g.unsqueeze(1)).sum(-1)                           # [T, S]
+    dlogit = alpha * (dalpha - (alpha * dalpha).sum(-1, keepdim=True))
+    # logit_i = w . n_i:  dn_i = dlogit_i w, dw = sum dlogit_i n_i
+    dN = dlogit.unsqueeze(-1) * wd
+    dw = (dlogit.unsqueeze(-1) * N).sum((0, 1))
+    # n = x r, r = (mean x^2 + eps)^(-1/2):  dx = r (dn - n mean(dn * n))
+    dX = dX + rstd.unsqueeze(-1) * (dN - N * (dN * N).sum(-1, keepdim=True) / d)
+    return [dX[:, i].numpy() for i in range(X.shape[1])], dw.numpy()
+
+
 def assemble_fwd(res: dict, cu_seqlens, H: int, dv: int):
     """Stack per-task forward results into o [total, H, dv] and hT [N, H, dk, dv]."""
     cu = [int(x) for x in cu_seqlens.to("cpu").tolist()]

@@ -17,8 +17,9 @@
 
 namespace kda {
 
-constexpr int AR_THREADS = 512;
 constexpr int AR_MAXS = 9;
+constexpr int AR_CPT = 4;        // 16-byte chunks per thread and source
+constexpr int AR_MAXW = 32;      // warps per CTA at most
 
 namespace {
 template <typename IO> struct Vec;
@@ -56,6 +57,13 @@ template <> struct Vec<float> {
   }
 };
 
+// Threads per CTA: about AR_CPT chunks each, in whole warps.
+__host__ __device__ inline int ar_threads(int nch) {
+  int t = (nch + AR_CPT - 1) / AR_CPT;
+  t = (t + 31) / 32 * 32;
+  return t < 32 ? 32 : (t > 1024 ? 1024 : t);
+}
+
 // Sum `n` per-thread values over the CTA (fixed order); results in out[0..n) for every thread.
 template <int NMAX>
 __device__ __forceinline__ void block_sum(float (&v)[NMAX], int n, float *red, float *out) {
@@ -79,15 +87,15 @@ __device__ __forceinline__ void block_sum(float (&v)[NMAX], int n, float *red, f
 }  // namespace
 
 template <typename IO>
-__global__ void __launch_bounds__(AR_THREADS) attnres_fwd_kernel(AttnresParams p) {
+__global__ void __launch_bounds__(1024) attnres_fwd_kernel(AttnresParams p) {
   constexpr int N = Vec<IO>::N;
-  __shared__ float red[(AR_THREADS / 32) * 2 * AR_MAXS], tot[2 * AR_MAXS], al[AR_MAXS];
+  __shared__ float red[AR_MAXW * 2 * AR_MAXS], tot[2 * AR_MAXS], al[AR_MAXS];
   const long long t = blockIdx.x;
   const int S = p.S, d = p.dim, nch = d / N;
   float acc[2 * AR_MAXS];
 #pragma unroll
   for (int i = 0; i < 2 * AR_MAXS; ++i) acc[i] = 0.f;
-  for (int c = threadIdx.x; c < nch; c += AR_THREADS) {
+  for (int c = threadIdx.x; c < nch; c += blockDim.x) {
     float w[N], x[N];
 #pragma unroll
     for (int e = 0; e < N; ++e) w[e] = p.w[c * N + e];
@@ -123,7 +131,7 @@ __global__ void __launch_bounds__(AR_THREADS) attnres_fwd_kernel(AttnresParams p
     }
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < nch; c += AR_THREADS) {
+  for (int c = threadIdx.x; c < nch; c += blockDim.x) {
     float o[N], x[N];
 #pragma unroll
     for (int e = 0; e < N; ++e) o[e] = 0.f;
@@ -139,11 +147,11 @@ __global__ void __launch_bounds__(AR_THREADS) attnres_fwd_kernel(AttnresParams p
 }
 
 // Persistent: CTA b takes tokens b, b + grid, ...; each thread owns fixed channel chunks
-// (c = tid + 512 j) and keeps their dw partial sums; partial[b][c] at the end.
+// (c = tid + blockDim j, j < MAXJ) and keeps their dw partial sums; partial[b][c] at the end.
 template <typename IO, int MAXJ>
-__global__ void __launch_bounds__(AR_THREADS) attnres_bwd_kernel(AttnresParams p) {
+__global__ void __launch_bounds__(1024) attnres_bwd_kernel(AttnresParams p) {
   constexpr int N = Vec<IO>::N;
-  __shared__ float red[(AR_THREADS / 32) * AR_MAXS], tot[AR_MAXS];
+  __shared__ float red[AR_MAXW * AR_MAXS], tot[AR_MAXS];
   const int S = p.S, d = p.dim, nch = d / N;
   const float inv_d = 1.f / d;
   float dw[MAXJ][N];
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(AR_THREADS) attnres_bwd_kernel(AttnresParams p
     // pass 1: da_i = g . x_i
 #pragma unroll
     for (int j = 0; j < MAXJ; ++j) {
-      const int c = threadIdx.x + AR_THREADS * j;
+      const int c = threadIdx.x + blockDim.x * j;
       if (c < nch) {
         float g[N], x[N];
         Vec<IO>::load(static_cast<const IO *>(p.dout) + t * d + c * N, g);
@@ -186,7 +194,7 @@ __global__ void __launch_bounds__(AR_THREADS) attnres_bwd_kernel(AttnresParams p
     // pass 2: dx_i and the dw partials
 #pragma unroll
     for (int j = 0; j < MAXJ; ++j) {
-      const int c = threadIdx.x + AR_THREADS * j;
+      const int c = threadIdx.x + blockDim.x * j;
       if (c < nch) {
         float g[N], w[N], x[N], dx[N];
         Vec<IO>::load(static_cast<const IO *>(p.dout) + t * d + c * N, g);
@@ -210,7 +218,7 @@ __global__ void __launch_bounds__(AR_THREADS) attnres_bwd_kernel(AttnresParams p
   }
 #pragma unroll
   for (int j = 0; j < MAXJ; ++j) {
-    const int c = threadIdx.x + AR_THREADS * j;
+    const int c = threadIdx.x + blockDim.x * j;
     if (c < nch)
 #pragma unroll
       for (int e = 0; e < N; ++e) p.partial[(size_t)blockIdx.x * d + c * N + e] = dw[j][e];
@@ -226,12 +234,13 @@ __global__ void attnres_dw_reduce_kernel(const float *partial, int nparts, int d
 }
 
 // Backward grid: as many CTAs as fit on the device at once (the dw partials are per CTA).
-int attnres_bwd_ctas(long long T, bool f32) {
+int attnres_bwd_ctas(long long T, bool f32, int dim) {
   int dev = 0, sms = 0, per = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 1;
-  const cudaError_t e = f32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attnres_bwd_kernel<float, 8>, AR_THREADS, 0)
-                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attnres_bwd_kernel<bf16, 4>, AR_THREADS, 0);
+  const int threads = ar_threads(dim / (f32 ? 4 : 8));
+  const cudaError_t e = f32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attnres_bwd_kernel<float, AR_CPT>, threads, 0)
+                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attnres_bwd_kernel<bf16, AR_CPT>, threads, 0);
   if (e != cudaSuccess || per < 1) per = 1;
   const long long cap = (long long)sms * per;
   return (int)(T < cap ? (T > 0 ? T : 1) : cap);
@@ -239,21 +248,22 @@ int attnres_bwd_ctas(long long T, bool f32) {
 
 cudaError_t launch_attnres_fwd(const AttnresParams &p, bool f32, cudaStream_t s) {
   if (p.T == 0) return cudaSuccess;
+  const int threads = ar_threads(p.dim / (f32 ? 4 : 8));
   if (f32)
-    attnres_fwd_kernel<float><<<(unsigned)p.T, AR_THREADS, 0, s>>>(p);
+    attnres_fwd_kernel<float><<<(unsigned)p.T, threads, 0, s>>>(p);
   else
-    attnres_fwd_kernel<bf16><<<(unsigned)p.T, AR_THREADS, 0, s>>>(p);
+    attnres_fwd_kernel<bf16><<<(unsigned)p.T, threads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attnres_bwd(const AttnresParams &p, bool f32, cudaStream_t s) {
-  const int nparts = attnres_bwd_ctas(p.T, f32);
+  const int nparts = attnres_bwd_ctas(p.T, f32, p.dim);
   if (p.T > 0) {
-    // chunks per thread: at most 16384 / (512 * N) = 4 (bf16) or 8 (fp32)
+    const int threads = ar_threads(p.dim / (f32 ? 4 : 8));   // at most AR_CPT chunks per thread
     if (f32)
-      attnres_bwd_kernel<float, 8><<<nparts, AR_THREADS, 0, s>>>(p);
+      attnres_bwd_kernel<float, AR_CPT><<<nparts, threads, 0, s>>>(p);
     else
-      attnres_bwd_kernel<bf16, 4><<<nparts, AR_THREADS, 0, s>>>(p);
+      attnres_bwd_kernel<bf16, AR_CPT><<<nparts, threads, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   } else {

@@ -143,7 +143,7 @@ struct AttnresParams {
 
 cudaError_t launch_attnres_fwd(const AttnresParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_attnres_bwd(const AttnresParams &p, bool f32, cudaStream_t s);
-int attnres_bwd_ctas(long long T, bool f32);
+int attnres_bwd_ctas(long long T, bool f32, int dim);
 
 cudaError_t launch_chunk_table(const int *cu_in, int n_seqs, long long total, int *cu_out,
                                int *chunk_off, cudaStream_t s);

@@ -246,6 +246,81 @@ kda_status kda_attnres_bwd(const kda_attnres_bwd_args *args, cudaStream_t stream
 size_t kda_attnres_bwd_workspace_size(const kda_attnres_bwd_args *args);
 
 /*
+ * Short convolution on the KDA input side ("Kimi K3 on Fireworks: Fast RL at frontier
+ * scale", rollout section, the paragraph on inline versus disaggregated serving, and its
+ * translation under "选择内联或分离式rollout服务" in "Fireworks 发布 Kimi K3 大规模强化学习
+ * 技术报告": a sequence handed to another pool carries its KDA recurrent state together
+ * with its convolution state). The pages name the convolution state and nothing else;
+ * this library reads it as a causal
+ * depthwise 1-D convolution of width W over the token axis, one filter per channel, with
+ * an optional bias and SiLU, applied to the q, k, v projections before the KDA core:
+ *     z[t, c] = bias[c] + sum_{j < W} weight[c, j] * x[t - (W - 1) + j, c]
+ *     y[t, c] = act(z[t, c]),   act = identity or SiLU (z / (1 + e^-z))
+ * Positions before a sequence's first token read its convolution state: the W - 1 inputs
+ * that preceded it, oldest first (state[n, i, :] is position i - (W - 1)); NULL reads as
+ * zeros. The state after a sequence is its last W - 1 inputs in the same layout (taken
+ * partly from the incoming state when the sequence is shorter than W - 1). Channels are
+ * independent, so x may be one projection [T, H*d] or q, k, v side by side [T, 3*H*d].
+ */
+#define KDA_CONV_MAX_WIDTH 4
+
+typedef enum { KDA_ACT_NONE = 0, KDA_ACT_SILU = 1 } kda_activation;
+
+typedef struct {
+    int32_t n_seqs;            /* N >= 0                                                 */
+    int64_t total_tokens;      /* T = sum of the sequence lengths, < 2^31                */
+    int32_t channels;          /* C, a multiple of 8                                     */
+    int32_t width;             /* W, 1..KDA_CONV_MAX_WIDTH                               */
+    int32_t activation;        /* kda_activation                                         */
+    int32_t io_dtype;          /* kda_dtype of x, y and the states                       */
+    const int32_t *cu_seqlens; /* [N+1] device offsets, or NULL = N equal sequences      */
+    const void *x;             /* [T, C]                                                 */
+    const float *weight;       /* [C, W]; weight[c, W-1] multiplies the current token    */
+    const float *bias;         /* [C] or NULL (zero)                                     */
+    const void *state_in;      /* [N, W-1, C] or NULL (zeros)                            */
+    void *y;                   /* out [T, C]                                             */
+    void *state_out;           /* out [N, W-1, C] or NULL; must not overlap state_in     */
+} kda_conv_args;
+
+typedef struct {
+    kda_conv_args fwd;         /* the forward's arguments (y and state_out unused)       */
+    const void *dy;            /* [T, C] io dtype                                        */
+    const float *d_state_out;  /* [N, W-1, C] fp32 gradient of state_out, or NULL (zero) */
+    float *dx;                 /* out [T, C] fp32                                        */
+    float *dweight;            /* out [C, W] fp32                                        */
+    float *dbias;              /* out [C] fp32, or NULL (not computed)                   */
+    float *d_state_in;         /* out [N, W-1, C] fp32, or NULL (not computed)           */
+    void *workspace;           /* kda_conv_bwd_workspace_size() bytes (per-CTA partials) */
+    size_t workspace_bytes;
+} kda_conv_bwd_args;
+
+/* Decode / draft verification: L token slots per sequence, the state in place, with the
+ * same slot conventions as kda_step (state_indices into a pool of n_slots states; slots
+ * before first_slot[i] are padding that neither reads nor writes anything; the state is
+ * advanced through accept_len[i] slots: the last W - 1 inputs of the committed tokens). */
+typedef struct {
+    int32_t n_seqs, steps;     /* N >= 0, L in 1..8                                      */
+    int32_t channels, width, activation, io_dtype;   /* as in kda_conv_args              */
+    const void *x;             /* [N, L, C]                                              */
+    const float *weight;       /* [C, W]                                                 */
+    const float *bias;         /* [C] or NULL                                            */
+    void *state;               /* [n_slots, W-1, C] io dtype, updated in place           */
+    const int32_t *state_indices;   /* [N] slot of each sequence, or NULL = slot i       */
+    int32_t n_slots;           /* slots in the pool (N when state_indices is NULL)       */
+    const int32_t *accept_len; /* [N] slots to commit (clamped to 0..L), or NULL = L     */
+    const int32_t *first_slot; /* [N] padding slots before the tokens, or NULL = 0       */
+    void *y;                   /* out [N, L, C]; padding slots are not written           */
+    int32_t *dev_status;       /* NULL, or a device int32: KDA_ERR_INVALID_ARG when a
+                                  state index is outside 0..n_slots-1 (that sequence is
+                                  skipped)                                               */
+} kda_conv_step_args;
+
+kda_status kda_conv_fwd(const kda_conv_args *args, cudaStream_t stream);
+kda_status kda_conv_bwd(const kda_conv_bwd_args *args, cudaStream_t stream);
+size_t kda_conv_bwd_workspace_size(const kda_conv_bwd_args *args);
+kda_status kda_conv_step(const kda_conv_step_args *args, cudaStream_t stream);
+
+/*
  * kda_fwd_no_alloc -- kda_fwd for callers that cannot allocate device memory.
  * (This entry point has no counterpart in the pages; it is a deployment aid.)
  *

@@ -276,6 +276,115 @@ def attnres_bwd(sources, w, d_out, eps: float = EPS):
     return [dX[:, i].numpy() for i in range(X.shape[1])], dw.numpy()
 
 
+def _conv_bounds(cu_seqlens, n_seqs, total):
+    """Per-sequence token ranges: from cu_seqlens, else n_seqs equal sequences."""
+    if cu_seqlens is not None:
+        cu = [int(c) for c in cu_seqlens.to("cpu").tolist()]
+    else:
+        n = n_seqs or 1
+        cu = [i * (total // n) for i in range(n + 1)]
+    return list(zip(cu[:-1], cu[1:]))
+
+
+def _conv_act(z, activation: str):
+    return z / (1.0 + torch.exp(-z)) if activation == "silu" else z
+
+
+def conv_fwd(x, weight, bias, cu_seqlens, state_in=None, *, activation: str = "silu", n_seqs=None):
+    """Short causal depthwise convolution in fp64 (the convolution state named in "Kimi K3 on
+    Fireworks: Fast RL at frontier scale", rollout section, inline versus disaggregated
+    serving; kernel width, bias and SiLU are this library's reading, stated in include/kda.h).
+
+    Per sequence, the W - 1 state rows (oldest first) are placed before its tokens and every
+    output is the tap-weighted sum of the W most recent inputs:
+        z[t] = bias + sum_j weight[:, j] * xs[t + j],   xs = [state_in; x_seq]
+    x [T, C], weight [C, W], bias [C] or None, state_in [N, W-1, C] or None.
+    Returns (y [T, C], state_out [N, W-1, C]) as float64 numpy arrays.
+    """
+    X, Wt = x.double(), weight.double()
+    T, C = X.shape
+    W = Wt.shape[1]
+    bounds = _conv_bounds(cu_seqlens, n_seqs, T)
+    y = torch.zeros(T, C, dtype=torch.float64)
+    state_out = torch.zeros(len(bounds), W - 1, C, dtype=torch.float64)
+    for n, (s0, s1) in enumerate(bounds):
+        prev = state_in[n].double() if state_in is not None else torch.zeros(W - 1, C, dtype=torch.float64)
+        xs = torch.cat([prev, X[s0:s1]], 0)
+        L = s1 - s0
+        z = torch.zeros(L, C, dtype=torch.float64) if bias is None else bias.double().expand(L, C).clone()
+        for j in range(W):
+            z += Wt[:, j] * xs[j:j + L]
+        y[s0:s1] = _conv_act(z, activation)
+        state_out[n] = xs[xs.shape[0] - (W - 1):]
+    return y.numpy(), state_out.numpy()
+
+
+def conv_bwd(x, weight, bias, cu_seqlens, state_in, dy, d_state_out=None, *, activation: str = "silu",
+             n_seqs=None):
+    """Backward of conv_fwd in fp64, by the chain rule written out: dz = dy * act'(z), then every
+    tap spreads dz back onto the input row it read (weight[:, j] * dz lands on xs[t + j]) and
+    collects dz * xs[t + j] into dweight[:, j]; the gradient of state_out lands on the last W - 1
+    rows of xs. Returns dict dx [T, C], dweight [C, W], dbias [C], d_state_in [N, W-1, C] (numpy)."""
+    X, Wt, G = x.double(), weight.double(), dy.double()
+    T, C = X.shape
+    W = Wt.shape[1]
+    bounds = _conv_bounds(cu_seqlens, n_seqs, T)
+    dx = torch.zeros(T, C, dtype=torch.float64)
+    dW = torch.zeros(C, W, dtype=torch.float64)
+    db = torch.zeros(C, dtype=torch.float64)
+    dst = torch.zeros(len(bounds), W - 1, C, dtype=torch.float64)
+    for n, (s0, s1) in enumerate(bounds):
+        prev = state_in[n].double() if state_in is not None else torch.zeros(W - 1, C, dtype=torch.float64)
+        xs = torch.cat([prev, X[s0:s1]], 0)
+        L = s1 - s0
+        z = torch.zeros(L, C, dtype=torch.float64) if bias is None else bias.double().expand(L, C).clone()
+        for j in range(W):
+            z += Wt[:, j] * xs[j:j + L]
+        if activation == "silu":
+            sg = 1.0 / (1.0 + torch.exp(-z))
+            dz = G[s0:s1] * sg * (1.0 + z * (1.0 - sg))
+        else:
+            dz = G[s0:s1].clone()
+        dxs = torch.zeros_like(xs)
+        for j in range(W):
+            dxs[j:j + L] += Wt[:, j] * dz
+            dW[:, j] += (dz * xs[j:j + L]).sum(0)
+        db += dz.sum(0)
+        if d_state_out is not None and W > 1:
+            dxs[xs.shape[0] - (W - 1):] += d_state_out[n].double()
+        dx[s0:s1] = dxs[W - 1:]
+        dst[n] = dxs[:W - 1]
+    return {"dx": dx.numpy(), "dweight": dW.numpy(), "dbias": db.numpy(), "d_state_in": dst.numpy()}
+
+
+def conv_step(x, weight, bias, pool, state_indices=None, accept_len=None, first_slot=None, *,
+              activation: str = "silu"):
+    """Decode / verify form of conv_fwd in fp64: x [N, L, C] token slots per sequence, pool
+    [P, W-1, C] states. Slots before first_slot[i] are padding (no output, no state change);
+    sequence i convolves slots first_slot[i]..L-1 from the state of its slot and commits the
+    last W - 1 inputs of slots up to accept_len[i] (nothing when accept_len[i] <= first_slot[i]).
+    Returns (y [N, L, C] with NaN in padding slots, new pool) as float64 numpy arrays."""
+    X, Wt = x.double(), weight.double()
+    N, L, C = X.shape
+    W = Wt.shape[1]
+    new_pool = pool.double().clone()
+    y = torch.full((N, L, C), float("nan"), dtype=torch.float64)
+    for n in range(N):
+        slot = int(state_indices[n]) if state_indices is not None else n
+        F = min(max(int(first_slot[n]), 0), L) if first_slot is not None else 0
+        a = min(max(int(accept_len[n]), 0), L) if accept_len is not None else L
+        xs = torch.cat([pool[slot].double(), X[n, F:]], 0)
+        Lt = L - F
+        z = torch.zeros(Lt, C, dtype=torch.float64) if bias is None else bias.double().expand(Lt, C).clone()
+        for j in range(W):
+            z += Wt[:, j] * xs[j:j + Lt]
+        y[n, F:] = _conv_act(z, activation)
+        if a > F:
+            kept = xs[:W - 1 + a - F]
+            new_pool[slot] = kept[kept.shape[0] - (W - 1):]
+    return y.numpy(), new_pool.numpy()
+
+
 def assemble_fwd(res: dict, cu_seqlens, H: int, dv: int):
     """Stack per-task forward results into o [total, H, dv] and hT [N, H, dk, dv]."""
     cu = [int(x) for x in cu_seqlens.to("cpu").tolist()]

@@ -249,6 +249,8 @@ def run_ours(args, rank, world, local_rank):
         out["cp_forward"] = bench_cp(args, dev, peaks, out["fwd"]["ms"])
     if not args.no_attnres:
         out["attnres"] = bench_attnres(args, dev, peaks)
+    if not args.no_conv:
+        out["short_conv"] = bench_conv(args, dev, peaks)
     if host is not None:
         out["e2e"] = bench_e2e(args, dev, world, host)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -289,6 +291,63 @@ def bench_attnres(args, dev, peaks, T=32768, S=9, d=7168):
     return {"workload": f"attnres-bf16-T{T}-S{S}-d{d}", **res,
             "tokens_per_s_fwd_bwd": T / ((res["fwd"]["ms"] + res["bwd"]["ms"]) * 1e-3),
             "l2": "sources (4.2 GB) larger than L2; no flush"}
+
+
+def _time_ms(run, dev, warmup, K):
+    import torch
+    for _ in range(max(warmup, 3)):
+        run()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    s.record()
+    for _ in range(K):
+        run()
+    e.record()
+    torch.cuda.synchronize(dev)
+    return s.elapsed_time(e) / K
+
+
+def bench_conv(args, dev, peaks, T=32768, H=96, d=128, W=4, N=256, L=4):
+    """Short convolution of the KDA input side on q, k, v side by side (C = 3 x H x d), width
+    4, SiLU, bf16, one sequence of T tokens with its state; and the decode step of N sequences
+    x L slots from a state pool. Algorithmic bytes: forward reads x, writes y; backward reads x
+    and dy, writes dx (fp32); the step reads x and the states, writes y and the states (the
+    weights, bias and [N, W-1, C] states of the training calls are included, all small)."""
+    import torch
+    import gated_delta_rule_chunked_gb300 as kda
+    C = 3 * H * d
+    gen = torch.Generator(device=dev).manual_seed(C)
+    x = torch.randn(T, C, generator=gen, device=dev).to(torch.bfloat16)
+    dy = torch.randn(T, C, generator=gen, device=dev).to(torch.bfloat16)
+    w = torch.randn(C, W, generator=gen, device=dev) / 2
+    b = torch.randn(C, generator=gen, device=dev) * 0.1
+    st = torch.randn(1, W - 1, C, generator=gen, device=dev).to(torch.bfloat16)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    K = max(args.steps, 10)
+    small = C * W * 4 + C * 4 + 2 * (W - 1) * C * 2
+    res = {}
+    for name, run, byts in (
+            ("fwd", lambda: kda.conv_fwd(x, w, b, cu, st), T * C * 4 + small),
+            ("bwd", lambda: kda.conv_bwd(x, w, b, dy, cu, st, None), T * C * 8 + small + (W - 1) * C * 4)):
+        ms = _time_ms(run, dev, args.warmup, K)
+        gbs = byts / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "gbs_algorithmic": gbs,
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": gbs / peaks["hbm_gbs"]}}
+    xs = torch.randn(N, L, C, generator=gen, device=dev).to(torch.bfloat16)
+    pool = torch.randn(N, W - 1, C, generator=gen, device=dev).to(torch.bfloat16)
+    acc = torch.randint(1, L + 1, (N,), generator=gen, device=dev, dtype=torch.int32)
+    ys = torch.empty_like(xs)
+    ms = _time_ms(lambda: kda.conv_step(xs, w, b, pool, acc, out=ys), dev, args.warmup, max(K, 50))
+    byts = N * L * C * 4 + N * (W - 1) * C * 4 + C * W * 4 + C * 4
+    gbs = byts / (ms * 1e-3) / 1e9
+    res["step"] = {"workload": f"conv-step-bf16-N{N}-L{L}-C{C}", "ms": ms, "gbs_algorithmic": gbs,
+                   "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": gbs / peaks["hbm_gbs"]},
+                   "note": f"{byts / 1e6:.0f} MB per call (inputs, outputs and pool together larger than L2); no flush"}
+    return {"workload": f"conv-bf16-T{T}-C{C}-W{W}-silu", **res,
+            "tokens_per_s_fwd_bwd": T / ((res["fwd"]["ms"] + res["bwd"]["ms"]) * 1e-3),
+            "l2": "x and dy (2.4 GB each) larger than L2; no flush"}
 
 
 def bench_cp(args, dev, peaks, fwd_ms, P=4):
@@ -534,6 +593,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cp", action="store_true", help="skip the context-parallel forward emulation")
     ap.add_argument("--no-attnres", action="store_true", help="skip the Attention Residuals workload")
+    ap.add_argument("--no-conv", action="store_true", help="skip the short-convolution workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16384)

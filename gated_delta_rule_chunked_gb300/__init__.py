@@ -256,6 +256,97 @@ def attnres_bwd(sources, w, stats, d_out, *, eps: float = 1e-6):
     return d_src, dw
 
 
+_ACT = {"none": _lib.KDA_ACT_NONE, "silu": _lib.KDA_ACT_SILU}
+
+
+def _conv_args(x, weight, bias, cu, state_in, activation, n_seqs):
+    if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor [T, C]")
+    T, Cc = x.shape
+    if weight.dtype != torch.float32 or weight.dim() != 2 or weight.shape[0] != Cc or not weight.is_contiguous():
+        raise TypeError("weight must be a contiguous float32 [C, W] tensor")
+    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (Cc,)):
+        raise TypeError("bias must be float32 [C]")
+    W = weight.shape[1]
+    if state_in is not None and (state_in.dtype != x.dtype or state_in.shape != (n_seqs, W - 1, Cc)
+                                 or not state_in.is_contiguous()):
+        raise ValueError("state_in must be a contiguous [N, W-1, C] tensor of x's dtype")
+    a = _lib.ConvArgs()
+    a.n_seqs, a.total_tokens, a.channels, a.width = n_seqs, T, Cc, W
+    a.activation, a.io_dtype = _ACT[activation], _io_dtype(x)
+    a.cu_seqlens, a.x, a.weight, a.bias, a.state_in = _ptr(cu), x.data_ptr(), weight.data_ptr(), _ptr(bias), _ptr(state_in)
+    return a
+
+
+def conv_fwd(x, weight, bias=None, cu_seqlens=None, state_in=None, *, activation: str = "silu",
+             n_seqs: Optional[int] = None):
+    """Short causal depthwise convolution (width W = weight.shape[1]) with the convolution
+    state of each sequence. Returns (y [T, C] in x's dtype, state_out [N, W-1, C])."""
+    lib = library()
+    cu = _i32(cu_seqlens, x.device)
+    N = (cu.numel() - 1) if cu is not None else (n_seqs or 1)
+    a = _conv_args(x, weight, bias, cu, state_in, activation, N)
+    y = torch.empty_like(x)
+    state_out = torch.empty((N, weight.shape[1] - 1, x.shape[1]), dtype=x.dtype, device=x.device)
+    a.y, a.state_out = y.data_ptr(), _ptr(state_out) if state_out.numel() else None
+    _lib.check(lib.kda_conv_fwd(C.byref(a), _stream(x.device)))
+    return y, state_out
+
+
+def conv_bwd(x, weight, bias, dy, cu_seqlens=None, state_in=None, d_state_out=None, *, activation: str = "silu",
+             n_seqs: Optional[int] = None):
+    """Backward of conv_fwd: returns a dict of fp32 gradients dx, dweight, dbias (None without a
+    bias) and d_state_in."""
+    lib = library()
+    cu = _i32(cu_seqlens, x.device)
+    N = (cu.numel() - 1) if cu is not None else (n_seqs or 1)
+    if dy.shape != x.shape or dy.dtype != x.dtype or not dy.is_contiguous():
+        raise ValueError("dy must match x")
+    b = _lib.ConvBwdArgs()
+    b.fwd = _conv_args(x, weight, bias, cu, state_in, activation, N)
+    f32 = dict(dtype=torch.float32, device=x.device)
+    W = weight.shape[1]
+    dx, dweight = torch.empty(x.shape, **f32), torch.empty(weight.shape, **f32)
+    dbias = torch.empty(x.shape[1], **f32) if bias is not None else None
+    d_state_in = torch.empty((N, W - 1, x.shape[1]), **f32)
+    if d_state_out is not None:
+        d_state_out = d_state_out.to(torch.float32).contiguous()
+    b.dy, b.d_state_out, b.dx, b.dweight = dy.data_ptr(), _ptr(d_state_out), dx.data_ptr(), dweight.data_ptr()
+    b.dbias, b.d_state_in = _ptr(dbias), _ptr(d_state_in) if d_state_in.numel() else None
+    ws_bytes = lib.kda_conv_bwd_workspace_size(C.byref(b))
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x.device)
+    b.workspace, b.workspace_bytes = ws.data_ptr(), ws_bytes
+    _lib.check(lib.kda_conv_bwd(C.byref(b), _stream(x.device)))
+    return {"dx": dx, "dweight": dweight, "dbias": dbias, "d_state_in": d_state_in}
+
+
+def conv_step(x, weight, bias, state, accept_len=None, *, activation: str = "silu", state_indices=None,
+              first_slot=None, out=None, dev_status=None):
+    """Decode / verify L token slots per sequence through the short convolution: x [N, L, C];
+    ``state`` [N, W-1, C] (or a pool [P, W-1, C] addressed by ``state_indices``) advanced in
+    place through ``accept_len`` slots; slots before ``first_slot`` are padding. Returns y."""
+    lib = library()
+    if x.dim() != 3 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor [N, L, C]")
+    N, L, Cc = x.shape
+    W = weight.shape[1]
+    if state.dtype != x.dtype or state.shape[1:] != (W - 1, Cc) or not state.is_contiguous():
+        raise ValueError("state must be a contiguous [P, W-1, C] tensor of x's dtype")
+    i32 = lambda t: None if t is None else t.to(device=x.device, dtype=torch.int32).contiguous()
+    acc, idx, first = i32(accept_len), i32(state_indices), i32(first_slot)
+    if (idx is None and state.shape[0] != N) or (idx is not None and idx.numel() != N):
+        raise ValueError("state has one slot per sequence unless state_indices [N] addresses a pool")
+    y = torch.empty_like(x) if out is None else out
+    a = _lib.ConvStepArgs()
+    a.n_seqs, a.steps, a.channels, a.width = N, L, Cc, W
+    a.activation, a.io_dtype = _ACT[activation], _io_dtype(x)
+    a.x, a.weight, a.bias, a.state = x.data_ptr(), weight.data_ptr(), _ptr(bias), _ptr(state) if state.numel() else None
+    a.state_indices, a.n_slots, a.accept_len, a.first_slot = _ptr(idx), state.shape[0], _ptr(acc), _ptr(first)
+    a.y, a.dev_status = y.data_ptr(), _ptr(dev_status)
+    _lib.check(lib.kda_conv_step(C.byref(a), _stream(x.device)))
+    return y
+
+
 def kda_bwd(q, k, v, beta, g, dO, saved, cu_seqlens=None, h0=None, dhT=None, *, scale: float = 1.0,
             n_seqs: Optional[int] = None, initial_state_grad: bool = True, dev_status=None):
     """Backward of kda_fwd (``saved`` from kda_fwd(..., save=True) with the same inputs).

@@ -14,13 +14,16 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT 
 KDA_BF16, KDA_F32 = 0, 1
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
                 4: "KDA_ERR_TIMEOUT"}
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 # every symbol include/kda.h declares
 EXPORTS = ("kda_fwd", "kda_fwd_workspace_size", "kda_saved_size", "kda_bwd", "kda_bwd_workspace_size",
            "kda_step", "kda_cp_combine", "kda_attnres_fwd", "kda_attnres_bwd", "kda_attnres_bwd_workspace_size",
+           "kda_conv_fwd", "kda_conv_bwd", "kda_conv_bwd_workspace_size", "kda_conv_step",
            "kda_fwd_no_alloc", "kda_set_profile_events", "kda_last_error", "kda_abi_version")
 ATTNRES_MAX_SOURCES = 9
+CONV_MAX_WIDTH = 4
+KDA_ACT_NONE, KDA_ACT_SILU = 0, 1
 NO_ALLOC_SCRATCH_BYTES = 256 * 1024 * 1024
 
 
@@ -55,6 +58,33 @@ class AttnresBwdArgs(C.Structure):
     _fields_ = [
         ("fwd", AttnresFwdArgs), ("d_out", C.c_void_p), ("d_src", C.c_void_p * ATTNRES_MAX_SOURCES),
         ("dw", C.c_void_p), ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
+    ]
+
+
+class ConvArgs(C.Structure):
+    _fields_ = [
+        ("n_seqs", C.c_int32), ("total_tokens", C.c_int64), ("channels", C.c_int32), ("width", C.c_int32),
+        ("activation", C.c_int32), ("io_dtype", C.c_int32), ("cu_seqlens", C.c_void_p),
+        ("x", C.c_void_p), ("weight", C.c_void_p), ("bias", C.c_void_p), ("state_in", C.c_void_p),
+        ("y", C.c_void_p), ("state_out", C.c_void_p),
+    ]
+
+
+class ConvBwdArgs(C.Structure):
+    _fields_ = [
+        ("fwd", ConvArgs), ("dy", C.c_void_p), ("d_state_out", C.c_void_p), ("dx", C.c_void_p),
+        ("dweight", C.c_void_p), ("dbias", C.c_void_p), ("d_state_in", C.c_void_p),
+        ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
+    ]
+
+
+class ConvStepArgs(C.Structure):
+    _fields_ = [
+        ("n_seqs", C.c_int32), ("steps", C.c_int32), ("channels", C.c_int32), ("width", C.c_int32),
+        ("activation", C.c_int32), ("io_dtype", C.c_int32),
+        ("x", C.c_void_p), ("weight", C.c_void_p), ("bias", C.c_void_p), ("state", C.c_void_p),
+        ("state_indices", C.c_void_p), ("n_slots", C.c_int32), ("accept_len", C.c_void_p),
+        ("first_slot", C.c_void_p), ("y", C.c_void_p), ("dev_status", C.c_void_p),
     ]
 
 
@@ -109,6 +139,14 @@ def load(path: str = LIB_PATH):
     lib.kda_attnres_bwd.restype = C.c_int
     lib.kda_attnres_bwd_workspace_size.argtypes = [C.POINTER(AttnresBwdArgs)]
     lib.kda_attnres_bwd_workspace_size.restype = C.c_size_t
+    lib.kda_conv_fwd.argtypes = [C.POINTER(ConvArgs), C.c_void_p]
+    lib.kda_conv_fwd.restype = C.c_int
+    lib.kda_conv_bwd.argtypes = [C.POINTER(ConvBwdArgs), C.c_void_p]
+    lib.kda_conv_bwd.restype = C.c_int
+    lib.kda_conv_bwd_workspace_size.argtypes = [C.POINTER(ConvBwdArgs)]
+    lib.kda_conv_bwd_workspace_size.restype = C.c_size_t
+    lib.kda_conv_step.argtypes = [C.POINTER(ConvStepArgs), C.c_void_p]
+    lib.kda_conv_step.restype = C.c_int
     lib.kda_fwd_workspace_size.argtypes = [C.POINTER(FwdArgs)]
     lib.kda_fwd_workspace_size.restype = C.c_size_t
     lib.kda_saved_size.argtypes = [C.POINTER(FwdArgs)]

@@ -212,7 +212,7 @@ void kda::set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
 
 extern "C" {
 
-int32_t kda_abi_version(void) { return 3; }
+int32_t kda_abi_version(void) { return 4; }
 
 namespace {
 kda_status check_attnres(const kda_attnres_fwd_args *a, const char *who) {
@@ -290,6 +290,171 @@ kda_status kda_attnres_bwd(const kda_attnres_bwd_args *a, cudaStream_t stream) {
   p.partial = static_cast<float *>(a->workspace);
   const cudaError_t e = kda::launch_attnres_bwd(p, a->fwd.io_dtype == KDA_F32, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_attnres_bwd");
+  g_last_error.clear();
+  return KDA_OK;
+}
+
+namespace {
+kda_status check_conv(const kda_conv_args *a, const char *who) {
+  if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", who);
+  if (a->io_dtype != KDA_BF16 && a->io_dtype != KDA_F32)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: io_dtype must be KDA_BF16 or KDA_F32", who);
+  if (a->width < 1 || a->width > KDA_CONV_MAX_WIDTH)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: width must be 1..4", who);
+  if (a->channels < 8 || a->channels % 8 != 0) return fail(KDA_ERR_UNSUPPORTED, "%s: channels must be a positive multiple of 8", who);
+  if (a->activation != KDA_ACT_NONE && a->activation != KDA_ACT_SILU)
+    return fail(KDA_ERR_INVALID_ARG, "%s: activation must be KDA_ACT_NONE or KDA_ACT_SILU", who);
+  if (a->n_seqs < 0 || a->total_tokens < 0 || a->total_tokens > 0x7fffffffLL)
+    return fail(KDA_ERR_INVALID_ARG, "%s: need n_seqs >= 0 and 0 <= total_tokens < 2^31", who);
+  if (a->n_seqs == 0 && a->total_tokens > 0) return fail(KDA_ERR_INVALID_ARG, "%s: tokens without sequences", who);
+  if (!a->cu_seqlens && a->n_seqs > 0 && a->total_tokens % a->n_seqs != 0)
+    return fail(KDA_ERR_INVALID_ARG, "%s: without cu_seqlens total_tokens must divide into n_seqs equal sequences", who);
+  if (a->cu_seqlens && !aligned(a->cu_seqlens, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: cu_seqlens is misaligned", who);
+  if (a->total_tokens > 0 && (!a->x || !aligned(a->x, 16))) return fail(KDA_ERR_INVALID_ARG, "%s: x is NULL or misaligned", who);
+  if (!a->weight || !aligned(a->weight, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: weight is NULL or misaligned", who);
+  if (a->bias && !aligned(a->bias, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: bias is misaligned", who);
+  if (a->state_in && !aligned(a->state_in, 16)) return fail(KDA_ERR_INVALID_ARG, "%s: state_in is misaligned", who);
+  return KDA_OK;
+}
+
+kda::ConvParams conv_params(const kda_conv_args *a) {
+  kda::ConvParams p{};
+  p.n_seqs = a->n_seqs;
+  p.T = a->total_tokens;
+  p.C = a->channels;
+  p.W = a->width;
+  p.act = a->activation == KDA_ACT_SILU;
+  p.cu = a->cu_seqlens;
+  p.x = a->x;
+  p.w = a->weight;
+  p.bias = a->bias;
+  p.st_in = a->width > 1 ? a->state_in : nullptr;
+  return p;
+}
+
+size_t conv_state_bytes(const kda_conv_args *a, size_t elem) {
+  return (size_t)a->n_seqs * (a->width - 1) * a->channels * elem;
+}
+
+bool overlaps(const void *a, const void *b, size_t n) {
+  const char *x = static_cast<const char *>(a), *y = static_cast<const char *>(b);
+  return x && y && n && x < y + n && y < x + n;
+}
+}  // namespace
+
+kda_status kda_conv_fwd(const kda_conv_args *a, cudaStream_t stream) {
+  kda_status st = check_conv(a, "kda_conv_fwd");
+  if (st != KDA_OK) return st;
+  const bool f32 = a->io_dtype == KDA_F32;
+  if (a->total_tokens > 0 && (!a->y || !aligned(a->y, 16)))
+    return fail(KDA_ERR_INVALID_ARG, "%s: y is NULL or misaligned", "kda_conv_fwd");
+  void *st_out = a->width > 1 ? a->state_out : nullptr;
+  const size_t sbytes = conv_state_bytes(a, f32 ? 4 : 2);
+  if (st_out && !aligned(st_out, 16)) return fail(KDA_ERR_INVALID_ARG, "%s: state_out is misaligned", "kda_conv_fwd");
+  if (st_out && a->width > 1 && overlaps(st_out, a->state_in, sbytes))
+    return fail(KDA_ERR_INVALID_ARG, "%s: state_out overlaps state_in", "kda_conv_fwd");
+  cudaError_t e = cudaSuccess;
+  if (a->total_tokens == 0) {   // every sequence is empty: the state passes through
+    if (st_out && sbytes)
+      e = a->state_in ? cudaMemcpyAsync(st_out, a->state_in, sbytes, cudaMemcpyDeviceToDevice, stream)
+                      : cudaMemsetAsync(st_out, 0, sbytes, stream);
+  } else {
+    kda::ConvParams p = conv_params(a);
+    p.y = a->y;
+    p.st_out = st_out;
+    e = kda::launch_conv_fwd(p, f32, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "kda_conv_fwd");
+  g_last_error.clear();
+  return KDA_OK;
+}
+
+size_t kda_conv_bwd_workspace_size(const kda_conv_bwd_args *a) {
+  if (!a || a->fwd.width < 1 || a->fwd.width > KDA_CONV_MAX_WIDTH || a->fwd.channels < 8) return 0;
+  return (size_t)kda::conv_bwd_groups(a->fwd.total_tokens, a->fwd.channels, a->fwd.width, a->fwd.io_dtype == KDA_F32) *
+         a->fwd.channels * (a->fwd.width + 1) * sizeof(float);
+}
+
+kda_status kda_conv_bwd(const kda_conv_bwd_args *a, cudaStream_t stream) {
+  if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", "kda_conv_bwd");
+  kda_status st = check_conv(&a->fwd, "kda_conv_bwd");
+  if (st != KDA_OK) return st;
+  const kda_conv_args *f = &a->fwd;
+  if (f->total_tokens > 0 && (!a->dy || !aligned(a->dy, 16) || !a->dx || !aligned(a->dx, 16)))
+    return fail(KDA_ERR_INVALID_ARG, "%s: dy and dx are required and 16-byte aligned", "kda_conv_bwd");
+  if (!a->dweight || !aligned(a->dweight, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: dweight is NULL or misaligned", "kda_conv_bwd");
+  if (a->dbias && !aligned(a->dbias, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: dbias is misaligned", "kda_conv_bwd");
+  if ((a->d_state_out && !aligned(a->d_state_out, 16)) || (a->d_state_in && !aligned(a->d_state_in, 16)))
+    return fail(KDA_ERR_INVALID_ARG, "%s: d_state_out / d_state_in misaligned", "kda_conv_bwd");
+  const size_t need = kda_conv_bwd_workspace_size(a);
+  if (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 16))
+    return fail(KDA_ERR_INVALID_ARG, "%s: workspace missing, misaligned or smaller than kda_conv_bwd_workspace_size()",
+                "kda_conv_bwd");
+  kda::ConvParams p = conv_params(f);
+  p.dy = a->dy;
+  p.dso = f->width > 1 ? a->d_state_out : nullptr;
+  p.dx = a->dx;
+  p.dw = a->dweight;
+  p.db = a->dbias;
+  p.dst = f->width > 1 ? a->d_state_in : nullptr;
+  p.partial = static_cast<float *>(a->workspace);
+  p.groups = kda::conv_bwd_groups(f->total_tokens, f->channels, f->width, f->io_dtype == KDA_F32);
+  cudaError_t e = cudaSuccess;
+  const size_t sbytes = conv_state_bytes(f, 4);
+  if (f->total_tokens == 0 && p.dst && sbytes)   // every sequence is empty
+    e = p.dso ? cudaMemcpyAsync(p.dst, p.dso, sbytes, cudaMemcpyDeviceToDevice, stream)
+              : cudaMemsetAsync(p.dst, 0, sbytes, stream);
+  if (e == cudaSuccess) e = kda::launch_conv_bwd(p, f->io_dtype == KDA_F32, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_conv_bwd");
+  g_last_error.clear();
+  return KDA_OK;
+}
+
+kda_status kda_conv_step(const kda_conv_step_args *a, cudaStream_t stream) {
+  const char *who = "kda_conv_step";
+  if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", who);
+  if (a->io_dtype != KDA_BF16 && a->io_dtype != KDA_F32)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: io_dtype must be KDA_BF16 or KDA_F32", who);
+  if (a->width < 1 || a->width > KDA_CONV_MAX_WIDTH)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: width must be 1..4", who);
+  if (a->channels < 8 || a->channels % 8 != 0) return fail(KDA_ERR_UNSUPPORTED, "%s: channels must be a positive multiple of 8", who);
+  if (a->activation != KDA_ACT_NONE && a->activation != KDA_ACT_SILU)
+    return fail(KDA_ERR_INVALID_ARG, "%s: activation must be KDA_ACT_NONE or KDA_ACT_SILU", who);
+  if (a->n_seqs < 0 || a->n_seqs > 65535 || a->steps < 1 || a->steps > 8)
+    return fail(KDA_ERR_INVALID_ARG, "%s: need 0 <= n_seqs <= 65535 and 1 <= steps <= 8", who);
+  if (a->n_seqs == 0) {
+    g_last_error.clear();
+    return KDA_OK;
+  }
+  const int n_slots = a->state_indices ? a->n_slots : a->n_seqs;
+  if (a->state_indices && a->n_slots < 1) return fail(KDA_ERR_INVALID_ARG, "%s: n_slots must be >= 1 with state_indices", who);
+  if (!a->x || !aligned(a->x, 16) || !a->y || !aligned(a->y, 16))
+    return fail(KDA_ERR_INVALID_ARG, "%s: x and y are required and 16-byte aligned", who);
+  if (!a->weight || !aligned(a->weight, 4) || (a->bias && !aligned(a->bias, 4)))
+    return fail(KDA_ERR_INVALID_ARG, "%s: weight is NULL or weight / bias misaligned", who);
+  if (a->width > 1 && (!a->state || !aligned(a->state, 16)))
+    return fail(KDA_ERR_INVALID_ARG, "%s: state is NULL or misaligned", who);
+  if ((a->state_indices && !aligned(a->state_indices, 4)) || (a->accept_len && !aligned(a->accept_len, 4)) ||
+      (a->first_slot && !aligned(a->first_slot, 4)) || (a->dev_status && !aligned(a->dev_status, 4)))
+    return fail(KDA_ERR_INVALID_ARG, "%s: an int32 array is misaligned", who);
+  kda::ConvParams p{};
+  p.n_seqs = a->n_seqs;
+  p.C = a->channels;
+  p.W = a->width;
+  p.act = a->activation == KDA_ACT_SILU;
+  p.x = a->x;
+  p.w = a->weight;
+  p.bias = a->bias;
+  p.y = a->y;
+  p.st_out = a->state;
+  p.L = a->steps;
+  p.n_slots = n_slots;
+  p.idx = a->state_indices;
+  p.acc = a->accept_len;
+  p.first = a->first_slot;
+  p.status = a->dev_status;
+  const cudaError_t e = kda::launch_conv_step(p, a->io_dtype == KDA_F32, stream);
+  if (e != cudaSuccess) return cuda_fail(e, who);
   g_last_error.clear();
   return KDA_OK;
 }

@@ -151,6 +151,30 @@ cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
 cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_scan_tc(const BwdScanParams &p, cudaStream_t s);
+// Short convolution (kda_conv.cu). Forward: x, w, bias, st_in -> y, st_out. Backward adds
+// dy, dso -> dx, dw, db, dst through partial[groups][C][W + 1]. Step: the pool is st_out
+// (in place), idx/acc/first per sequence, L slots.
+struct ConvParams {
+  int n_seqs;
+  long long T;
+  int C, W, act;
+  const int *cu;
+  const void *x;
+  const float *w, *bias;
+  const void *st_in;
+  void *y, *st_out;
+  const void *dy;
+  const float *dso;
+  float *dx, *dw, *db, *dst, *partial;
+  int groups;
+  int L, n_slots;
+  const int *idx, *acc, *first;
+  int *status;
+};
+cudaError_t launch_conv_fwd(const ConvParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_conv_bwd(const ConvParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_conv_step(const ConvParams &p, bool f32, cudaStream_t s);
+int conv_bwd_groups(long long T, int C, int W, bool f32);
 cudaError_t launch_bwd_chunk_tc(const BwdChunkParams &p, cudaStream_t s);
 cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_cp_combine(int n_seqs, int n_segments, int heads, const float *M, const float *b, const float *h0,

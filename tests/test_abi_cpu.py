@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.kda_abi_version() == 3
+    assert lib.kda_abi_version() == 4
 
 
 def test_struct_layout_matches_c(tmp_path):
@@ -49,7 +49,10 @@ def test_struct_layout_matches_c(tmp_path):
     probe = tmp_path / "probe.c"
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kda.h"', "int main(void){"]
     for sname, cls in (("kda_fwd_args", _lib.FwdArgs), ("kda_bwd_args", _lib.BwdArgs),
-                       ("kda_step_args", _lib.StepArgs)):
+                       ("kda_step_args", _lib.StepArgs), ("kda_cp_args", _lib.CpArgs),
+                       ("kda_attnres_fwd_args", _lib.AttnresFwdArgs), ("kda_attnres_bwd_args", _lib.AttnresBwdArgs),
+                       ("kda_conv_args", _lib.ConvArgs), ("kda_conv_bwd_args", _lib.ConvBwdArgs),
+                       ("kda_conv_step_args", _lib.ConvStepArgs)):
         lines.append(f'printf("{sname} %zu\\n", sizeof({sname}));')
         for fname, _ in cls._fields_:
             lines.append(f'printf("{sname}.{fname} %zu\\n", offsetof({sname}, {fname}));')
@@ -60,7 +63,10 @@ def test_struct_layout_matches_c(tmp_path):
                            str(probe), "-o", str(exe)])
     got = dict(line.split() for line in subprocess.check_output([str(exe)], text=True).splitlines())
     for sname, cls in (("kda_fwd_args", _lib.FwdArgs), ("kda_bwd_args", _lib.BwdArgs),
-                       ("kda_step_args", _lib.StepArgs)):
+                       ("kda_step_args", _lib.StepArgs), ("kda_cp_args", _lib.CpArgs),
+                       ("kda_attnres_fwd_args", _lib.AttnresFwdArgs), ("kda_attnres_bwd_args", _lib.AttnresBwdArgs),
+                       ("kda_conv_args", _lib.ConvArgs), ("kda_conv_bwd_args", _lib.ConvBwdArgs),
+                       ("kda_conv_step_args", _lib.ConvStepArgs)):
         assert int(got[sname]) == C.sizeof(cls), sname
         for fname, _ in cls._fields_:
             assert int(got[f"{sname}.{fname}"]) == getattr(cls, fname).offset, f"{sname}.{fname}"
@@ -137,6 +143,37 @@ def test_step_validation(lib):
     assert lib.kda_step(C.byref(a), None) == 2
     a.dk, a.state = 128, None
     assert lib.kda_step(C.byref(a), None) == 1
+
+
+def test_conv_validation(lib):
+    from gated_delta_rule_chunked_gb300 import _lib
+    fake = 1 << 40
+    a = _lib.ConvArgs()
+    a.n_seqs, a.total_tokens, a.channels, a.width, a.activation = 2, 64, 256, 4, _lib.KDA_ACT_SILU
+    a.x = a.weight = a.y = a.state_in = fake
+    a.width = 5
+    assert lib.kda_conv_fwd(C.byref(a), None) == 2     # width > 4
+    a.width, a.channels = 4, 100
+    assert lib.kda_conv_fwd(C.byref(a), None) == 2     # channels not a multiple of 8
+    a.channels, a.activation = 256, 7
+    assert lib.kda_conv_fwd(C.byref(a), None) == 1
+    a.activation, a.total_tokens = _lib.KDA_ACT_SILU, 63
+    assert lib.kda_conv_fwd(C.byref(a), None) == 1     # 63 tokens do not split into 2 equal sequences
+    a.total_tokens, a.state_out = 64, fake + 16         # overlaps state_in
+    assert lib.kda_conv_fwd(C.byref(a), None) == 1
+    a.state_out, a.x = None, fake + 4
+    assert lib.kda_conv_fwd(C.byref(a), None) == 1     # misaligned x
+    b = _lib.ConvBwdArgs()
+    b.fwd = a
+    b.fwd.x = fake
+    b.dy, b.dx, b.dweight = fake, fake, fake
+    assert lib.kda_conv_bwd(C.byref(b), None) == 1     # no workspace
+    s = _lib.ConvStepArgs()
+    s.n_seqs, s.steps, s.channels, s.width = 4, 9, 256, 4
+    s.x = s.weight = s.state = s.y = fake
+    assert lib.kda_conv_step(C.byref(s), None) == 1    # steps > 8
+    s.steps, s.state = 4, None
+    assert lib.kda_conv_step(C.byref(s), None) == 1
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -135,6 +135,7 @@ struct AttnresParams {
   const float *w;
   void *out;
   float *alpha, *rstd, *logit;   // [T][S]
+  int *status;                   // optional status word (a bounded wait that gave up)
   const void *dout;
   void *dsrc[9];
   float *dw;

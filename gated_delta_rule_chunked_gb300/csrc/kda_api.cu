@@ -264,8 +264,9 @@ kda_status kda_attnres_fwd(const kda_attnres_fwd_args *a, cudaStream_t stream) {
 
 size_t kda_attnres_bwd_workspace_size(const kda_attnres_bwd_args *a) {
   if (!a || a->fwd.dim < 8 || a->fwd.dim > 16384) return 0;
-  return (size_t)kda::attnres_bwd_ctas(a->fwd.tokens, a->fwd.io_dtype == KDA_F32, a->fwd.dim) * a->fwd.dim *
-         sizeof(float);
+  if (a->fwd.n_sources < 1 || a->fwd.n_sources > KDA_ATTNRES_MAX_SOURCES) return 0;
+  return (size_t)kda::attnres_bwd_ctas(a->fwd.tokens, a->fwd.io_dtype == KDA_F32, a->fwd.dim, a->fwd.n_sources) *
+         a->fwd.dim * sizeof(float);
 }
 
 kda_status kda_attnres_bwd(const kda_attnres_bwd_args *a, cudaStream_t stream) {

@@ -22,8 +22,6 @@
 namespace kda {
 
 constexpr int AR_MAXS = 9;
-constexpr int AR_CPT = 4;        // 16-byte chunks per thread and source
-constexpr int AR_MAXW = 32;      // warps per CTA at most
 
 namespace {
 template <typename IO> struct Vec;
@@ -60,13 +58,6 @@ template <> struct Vec<float> {
     *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
   }
 };
-
-// Threads per CTA: about AR_CPT chunks each, in whole warps.
-__host__ __device__ inline int ar_threads(int nch) {
-  int t = (nch + AR_CPT - 1) / AR_CPT;
-  t = (t + 31) / 32 * 32;
-  return t < 32 ? 32 : (t > 1024 ? 1024 : t);
-}
 
 // Sum `n` per-thread values over the CTA (fixed order); results in out[0..n) for every thread.
 template <int NMAX>
@@ -200,82 +191,136 @@ __global__ void __cluster_dims__(AR_CL, 1, 1) __launch_bounds__(256) attnres_fwd
   cluster_wait();   // no CTA leaves while a peer may still read its sums
 }
 
-// Persistent: CTA b takes tokens b, b + grid, ...; each thread owns fixed channel chunks
-// (c = tid + blockDim j, j < MAXJ) and keeps their dw partial sums; partial[b][c] at the end.
-template <typename IO, int MAXJ>
-__global__ void __launch_bounds__(1024) attnres_bwd_kernel(AttnresParams p) {
+// Persistent clusters: cluster k of K takes tokens k, k + K, ...; CTA q of the cluster owns
+// channel chunks [q per, (q+1) per) (a thread chunks tid + blockDim j, j < J). Per token the
+// S source slices and the d_out slice are staged by bulk copies, double-buffered (the next
+// token's copies land while this one is computed); pass 1 sums g . x_i over the quarter and
+// the cluster adds the four partial sums through distributed shared memory (rank order);
+// pass 2 writes dx_i and accumulates the quarter's dw in registers; partial[k][c] at the end.
+template <typename IO, int J>
+__global__ void __cluster_dims__(AR_CL, 1, 1) __launch_bounds__(256) attnres_bwd_kernel(AttnresParams p) {
   constexpr int N = Vec<IO>::N;
-  __shared__ float red[AR_MAXW * AR_MAXS], tot[AR_MAXS];
-  const int S = p.S, d = p.dim, nch = d / N;
+  extern __shared__ __align__(128) char ar_smem[];
+  __shared__ float red[8 * AR_MAXS], part[AR_MAXS], st[3][AR_MAXS], dl[AR_MAXS];
+  __shared__ __align__(8) uint64_t bar[2];
+  const int tid = threadIdx.x;
+  const uint32_t q = cluster_rank();
+  const long long K = gridDim.x / AR_CL, kc = blockIdx.x / AR_CL;
+  const int S = p.S, d = p.dim, nch = d / N, per = (nch + AR_CL - 1) / AR_CL;
+  const int cbeg = (int)q * per, cend = min(cbeg + per, nch), nown = max(cend - cbeg, 0);
+  const size_t slab = (size_t)(S + 1) * per;   // 16-byte chunks per buffer: S sources, then d_out
+  uint4 *buf = reinterpret_cast<uint4 *>(ar_smem);
   const float inv_d = 1.f / d;
-  float dw[MAXJ][N];
-#pragma unroll
-  for (int j = 0; j < MAXJ; ++j)
-#pragma unroll
-    for (int e = 0; e < N; ++e) dw[j][e] = 0.f;
-  for (long long t = blockIdx.x; t < p.T; t += gridDim.x) {
-    float al[AR_MAXS], rs[AR_MAXS], lg[AR_MAXS], da[AR_MAXS];
-#pragma unroll
-    for (int i = 0; i < AR_MAXS; ++i) {
-      al[i] = i < S ? p.alpha[t * S + i] : 0.f;
-      rs[i] = i < S ? p.rstd[t * S + i] : 0.f;
-      lg[i] = i < S ? p.logit[t * S + i] : 0.f;
-      da[i] = 0.f;
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](long long t, int b) {   // thread 0
+    fence_proxy_async();
+    mbar_expect_tx(&bar[b], (uint32_t)((S + 1) * nown * 16));
+    if (nown > 0) {
+      for (int i = 0; i < S; ++i)
+        bulk_g2s(buf + b * slab + (size_t)i * per, static_cast<const IO *>(p.src[i]) + t * d + (size_t)cbeg * N,
+                 (uint32_t)(nown * 16), &bar[b]);
+      bulk_g2s(buf + b * slab + (size_t)S * per, static_cast<const IO *>(p.dout) + t * d + (size_t)cbeg * N,
+               (uint32_t)(nown * 16), &bar[b]);
     }
-    // pass 1: da_i = g . x_i
+  };
+  float w[J][N], dwa[J][N];
 #pragma unroll
-    for (int j = 0; j < MAXJ; ++j) {
-      const int c = threadIdx.x + blockDim.x * j;
-      if (c < nch) {
+  for (int j = 0; j < J; ++j) {
+    const int c = tid + blockDim.x * j;
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+      w[j][e] = c < nown ? p.w[(cbeg + c) * N + e] : 0.f;
+      dwa[j][e] = 0.f;
+    }
+  }
+  const bool dbl = p.nbuf == 2;   // one buffer when two do not fit: the copies then wait for the previous token
+  if (tid == 0 && dbl && kc < p.T) issue(kc, 0);
+  bool ok_all = true;
+  int it = 0;
+  for (long long t = kc; t < p.T; t += K, ++it) {
+    const int b = dbl ? (it & 1) : 0;
+    __syncthreads();   // the buffer being refilled (the previous token's) and st, dl are consumed
+    if (tid == 0) {
+      if (!dbl) issue(t, 0);
+      else if (t + K < p.T) issue(t + K, b ^ 1);
+    }
+    if (tid < S) {
+      st[0][tid] = p.alpha[t * S + tid];
+      st[1][tid] = p.rstd[t * S + tid];
+      st[2][tid] = p.logit[t * S + tid];
+    }
+    ok_all &= mbar_wait(&bar[b], (uint32_t)((dbl ? it >> 1 : it) & 1));   // on a timeout carry on: the cluster barriers must be met
+    const uint4 *xb = buf + b * slab;
+    // pass 1: this quarter's g . x_i
+    float da[AR_MAXS];
+#pragma unroll
+    for (int i = 0; i < AR_MAXS; ++i) da[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int c = tid + blockDim.x * j;
+      if (c < nown) {
         float g[N], x[N];
-        Vec<IO>::load(static_cast<const IO *>(p.dout) + t * d + c * N, g);
+        Vec<IO>::unpack(xb[(size_t)S * per + c], g);
 #pragma unroll
         for (int i = 0; i < AR_MAXS; ++i)
           if (i < S) {
-            Vec<IO>::load(static_cast<const IO *>(p.src[i]) + t * d + c * N, x);
+            Vec<IO>::unpack(xb[(size_t)i * per + c], x);
 #pragma unroll
             for (int e = 0; e < N; ++e) da[i] = fmaf(g[e], x[e], da[i]);
           }
       }
     }
-    block_sum(da, S, red, tot);
-    float mean = 0.f, dl[AR_MAXS];
+    block_sum(da, S, red, part);
+    cluster_arrive();
+    cluster_wait();
+    if (tid < 32) {   // lane i: the token's g . x_i, then dlogit_i = alpha_i (g . x_i - sum_j alpha_j g . x_j)
+      float v = 0.f;
+      if (tid < S)
 #pragma unroll
-    for (int i = 0; i < AR_MAXS; ++i)
-      if (i < S) mean = fmaf(al[i], tot[i], mean);
+        for (uint32_t r = 0; r < AR_CL; ++r) v += ld_peer(&part[tid], r);
+      const float a = tid < S ? st[0][tid] : 0.f;
+      float m = a * v;
 #pragma unroll
-    for (int i = 0; i < AR_MAXS; ++i) dl[i] = i < S ? al[i] * (tot[i] - mean) : 0.f;
+      for (int o = 16; o; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+      if (tid < S) dl[tid] = a * (v - m);
+    }
+    cluster_arrive();   // done reading the peers' sums
+    __syncthreads();    // dl
     // pass 2: dx_i and the dw partials
 #pragma unroll
-    for (int j = 0; j < MAXJ; ++j) {
-      const int c = threadIdx.x + blockDim.x * j;
-      if (c < nch) {
-        float g[N], w[N], x[N], dx[N];
-        Vec<IO>::load(static_cast<const IO *>(p.dout) + t * d + c * N, g);
-#pragma unroll
-        for (int e = 0; e < N; ++e) w[e] = p.w[c * N + e];
+    for (int j = 0; j < J; ++j) {
+      const int c = tid + blockDim.x * j;
+      if (c < nown) {
+        float g[N], x[N], dx[N];
+        Vec<IO>::unpack(xb[(size_t)S * per + c], g);
 #pragma unroll
         for (int i = 0; i < AR_MAXS; ++i)
           if (i < S) {
-            Vec<IO>::load(static_cast<const IO *>(p.src[i]) + t * d + c * N, x);
-            const float a = rs[i] * dl[i], b = rs[i] * lg[i] * inv_d;
+            Vec<IO>::unpack(xb[(size_t)i * per + c], x);
+            const float al = st[0][i], rs = st[1][i], a = rs * dl[i], bb = rs * st[2][i] * inv_d;
 #pragma unroll
             for (int e = 0; e < N; ++e) {
-              dx[e] = fmaf(al[i], g[e], a * (w[e] - x[e] * b));
-              dw[j][e] = fmaf(a, x[e], dw[j][e]);
+              dx[e] = fmaf(al, g[e], a * (w[j][e] - x[e] * bb));
+              dwa[j][e] = fmaf(a, x[e], dwa[j][e]);
             }
-            Vec<IO>::store(static_cast<IO *>(p.dsrc[i]) + t * d + c * N, dx);
+            Vec<IO>::store(static_cast<IO *>(p.dsrc[i]) + t * d + (size_t)(cbeg + c) * N, dx);
           }
       }
     }
-    __syncthreads();   // `tot` is reused by the next token
+    cluster_wait();   // every peer has read this token's sums before they are rewritten
   }
+  if (!ok_all) report(p.status, ERR_TIMEOUT);
 #pragma unroll
-  for (int j = 0; j < MAXJ; ++j) {
-    const int c = threadIdx.x + blockDim.x * j;
-    if (c < nch)
+  for (int j = 0; j < J; ++j) {
+    const int c = tid + blockDim.x * j;
+    if (c < nown)
 #pragma unroll
-      for (int e = 0; e < N; ++e) p.partial[(size_t)blockIdx.x * d + c * N + e] = dw[j][e];
+      for (int e = 0; e < N; ++e) p.partial[(size_t)kc * d + (size_t)(cbeg + c) * N + e] = dwa[j][e];
   }
 }
 
@@ -287,17 +332,48 @@ __global__ void attnres_dw_reduce_kernel(const float *partial, int nparts, int d
   dw[c] = s;
 }
 
-// Backward grid: as many CTAs as fit on the device at once (the dw partials are per CTA).
-int attnres_bwd_ctas(long long T, bool f32, int dim) {
-  int dev = 0, sms = 0, per = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 1;
-  const int threads = ar_threads(dim / (f32 ? 4 : 8));
-  const cudaError_t e = f32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attnres_bwd_kernel<float, AR_CPT>, threads, 0)
-                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attnres_bwd_kernel<bf16, AR_CPT>, threads, 0);
-  if (e != cudaSuccess || per < 1) per = 1;
-  const long long cap = (long long)sms * per;
-  return (int)(T < cap ? (T > 0 ? T : 1) : cap);
+namespace {
+struct BwdShape {
+  int per, J, threads, nbuf, smem;
+};
+BwdShape bwd_shape(bool f32, int dim, int S) {
+  BwdShape b;
+  b.per = (dim / (f32 ? 4 : 8) + AR_CL - 1) / AR_CL;
+  b.J = b.per <= 256 ? 1 : (b.per <= 512 ? 2 : 4);
+  b.threads = (b.per + b.J - 1) / b.J;
+  b.threads = (b.threads + 31) / 32 * 32;
+  if (b.threads < 32) b.threads = 32;
+  b.nbuf = 2 * (S + 1) * b.per * 16 <= 200 * 1024 ? 2 : 1;
+  b.smem = b.nbuf * (S + 1) * b.per * 16;
+  return b;
+}
+const void *bwd_fn(bool f32, int J) {
+  if (f32)
+    return J == 1 ? reinterpret_cast<const void *>(attnres_bwd_kernel<float, 1>)
+                  : J == 2 ? reinterpret_cast<const void *>(attnres_bwd_kernel<float, 2>)
+                           : reinterpret_cast<const void *>(attnres_bwd_kernel<float, 4>);
+  return J == 1 ? reinterpret_cast<const void *>(attnres_bwd_kernel<bf16, 1>)
+                : J == 2 ? reinterpret_cast<const void *>(attnres_bwd_kernel<bf16, 2>)
+                         : reinterpret_cast<const void *>(attnres_bwd_kernel<bf16, 4>);
+}
+}  // namespace
+
+// Backward clusters: as many as the device holds at once, at most one per token (the dw
+// partials are one row per cluster, so this also sizes the workspace).
+int attnres_bwd_ctas(long long T, bool f32, int dim, int S) {
+  const BwdShape b = bwd_shape(f32, dim, S);
+  const void *fn = bwd_fn(f32, b.J);
+  int n = 0;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, b.smem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(AR_CL, 1, 1);
+    cfg.blockDim = dim3(b.threads, 1, 1);
+    cfg.dynamicSmemBytes = b.smem;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  if (n < 1) n = 1;
+  return (int)(T < n ? (T > 0 ? T : 1) : n);
 }
 
 cudaError_t launch_attnres_fwd(const AttnresParams &p, bool f32, cudaStream_t s) {
@@ -315,14 +391,14 @@ cudaError_t launch_attnres_fwd(const AttnresParams &p, bool f32, cudaStream_t s)
 }
 
 cudaError_t launch_attnres_bwd(const AttnresParams &p, bool f32, cudaStream_t s) {
-  const int nparts = attnres_bwd_ctas(p.T, f32, p.dim);
+  const int nparts = attnres_bwd_ctas(p.T, f32, p.dim, p.S);
   if (p.T > 0) {
-    const int threads = ar_threads(p.dim / (f32 ? 4 : 8));   // at most AR_CPT chunks per thread
-    if (f32)
-      attnres_bwd_kernel<float, AR_CPT><<<nparts, threads, 0, s>>>(p);
-    else
-      attnres_bwd_kernel<bf16, AR_CPT><<<nparts, threads, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
+    const BwdShape b = bwd_shape(f32, p.dim, p.S);
+    AttnresParams q = p;
+    q.nbuf = b.nbuf;
+    void *args[] = {&q};
+    cudaError_t e = cudaLaunchKernel(bwd_fn(f32, b.J), dim3((unsigned)(nparts * AR_CL)), dim3(b.threads), args,
+                                     (size_t)b.smem, s);
     if (e != cudaSuccess) return e;
   } else {
     cudaError_t e = cudaMemsetAsync(p.partial, 0, (size_t)p.dim * sizeof(float), s);

@@ -136,6 +136,7 @@ struct AttnresParams {
   void *out;
   float *alpha, *rstd, *logit;   // [T][S]
   int *status;                   // optional status word (a bounded wait that gave up)
+  int nbuf;                      // backward: staging buffers per CTA (set by the launcher)
   const void *dout;
   void *dsrc[9];
   float *dw;
@@ -144,7 +145,7 @@ struct AttnresParams {
 
 cudaError_t launch_attnres_fwd(const AttnresParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_attnres_bwd(const AttnresParams &p, bool f32, cudaStream_t s);
-int attnres_bwd_ctas(long long T, bool f32, int dim);
+int attnres_bwd_ctas(long long T, bool f32, int dim, int S);
 
 cudaError_t launch_chunk_table(const int *cu_in, int n_seqs, long long total, int *cu_out,
                                int *chunk_off, cudaStream_t s);

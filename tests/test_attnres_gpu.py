@@ -58,6 +58,13 @@ def test_attnres_f32(kda):
     check(kda, 20, 3, 256, "f32", seed=9)
 
 
+@pytest.mark.parametrize("io,d,S", [("f32", 16384, 9), ("bf16", 16384, 9), ("bf16", 8, 2), ("f32", 72, 5)])
+def test_attnres_widths(kda, io, d, S):
+    # the widest rows (several chunks per thread, one staging buffer), and rows narrower
+    # than one chunk per CTA of the cluster
+    check(kda, 7, S, d, io, seed=d + S)
+
+
 def test_attnres_no_tokens(kda):
     src = [torch.empty(0, 64, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     w = torch.randn(64, device="cuda")

@@ -50,7 +50,8 @@ FWD_STAGES = ["fwd.table", "fwd.prep", "fwd.scan"]
 BWD_STAGES = ["bwd.table", "bwd.dscan", "bwd.chunk"]
 KERNEL_SRC = {"fwd.prep": "kda_prep.cu", "fwd.scan": "kda_scan_tc.cu",
               "bwd.dscan": "kda_scan_tc.cu", "bwd.chunk": "kda_bwd_tc.cu",
-              "decode": "kda_step.cu"}
+              "decode": "kda_step.cu", "attnres.fwd": "kda_attnres.cu", "attnres.bwd": "kda_attnres.cu",
+              "conv.fwd": "kda_conv.cu", "conv.bwd": "kda_conv.cu", "conv.step": "kda_conv.cu"}
 
 
 def load_peaks():
@@ -247,10 +248,11 @@ def run_ours(args, rank, world, local_rank):
         out["decode"] = bench_decode(args, dev, lib, stream, peaks)
     if not args.no_cp:
         out["cp_forward"] = bench_cp(args, dev, peaks, out["fwd"]["ms"])
+    small = {"T": args.seq_len} if args.seq_len else {}   # profiling runs only
     if not args.no_attnres:
-        out["attnres"] = bench_attnres(args, dev, peaks)
+        out["attnres"] = bench_attnres(args, dev, peaks, **small)
     if not args.no_conv:
-        out["short_conv"] = bench_conv(args, dev, peaks)
+        out["short_conv"] = bench_conv(args, dev, peaks, **small)
     if host is not None:
         out["e2e"] = bench_e2e(args, dev, world, host)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -285,9 +287,10 @@ def bench_attnres(args, dev, peaks, T=32768, S=9, d=7168):
         ms = s.elapsed_time(e) / K
         byts = T * d * 2 * ((S + 1) if name == "fwd" else (2 * S + 1))
         gbs = byts / (ms * 1e-3) / 1e9
-        res[name] = {"ms": ms, "gbs_algorithmic": gbs,
+        res[name] = {"ms": ms, "gbs_algorithmic": gbs, "algorithmic_bytes_per_launch": byts,
                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": gbs / peaks["hbm_gbs"]}}
+                                  "frac": gbs / peaks["hbm_gbs"],
+                                  "traffic": recorded_traffic(f"attnres.{name}") if T == 32768 else None}}
     return {"workload": f"attnres-bf16-T{T}-S{S}-d{d}", **res,
             "tokens_per_s_fwd_bwd": T / ((res["fwd"]["ms"] + res["bwd"]["ms"]) * 1e-3),
             "l2": "sources (4.2 GB) larger than L2; no flush"}
@@ -331,9 +334,10 @@ def bench_conv(args, dev, peaks, T=32768, H=96, d=128, W=4, N=256, L=4):
             ("bwd", lambda: kda.conv_bwd(x, w, b, dy, cu, st, None), T * C * 8 + small + (W - 1) * C * 4)):
         ms = _time_ms(run, dev, args.warmup, K)
         gbs = byts / (ms * 1e-3) / 1e9
-        res[name] = {"ms": ms, "gbs_algorithmic": gbs,
+        res[name] = {"ms": ms, "gbs_algorithmic": gbs, "algorithmic_bytes_per_launch": byts,
                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": gbs / peaks["hbm_gbs"]}}
+                                  "frac": gbs / peaks["hbm_gbs"],
+                                  "traffic": recorded_traffic(f"conv.{name}") if T == 32768 else None}}
     xs = torch.randn(N, L, C, generator=gen, device=dev).to(torch.bfloat16)
     pool = torch.randn(N, W - 1, C, generator=gen, device=dev).to(torch.bfloat16)
     acc = torch.randint(1, L + 1, (N,), generator=gen, device=dev, dtype=torch.int32)
@@ -342,8 +346,9 @@ def bench_conv(args, dev, peaks, T=32768, H=96, d=128, W=4, N=256, L=4):
     byts = N * L * C * 4 + N * (W - 1) * C * 4 + C * W * 4 + C * 4
     gbs = byts / (ms * 1e-3) / 1e9
     res["step"] = {"workload": f"conv-step-bf16-N{N}-L{L}-C{C}", "ms": ms, "gbs_algorithmic": gbs,
+                   "algorithmic_bytes_per_launch": byts,
                    "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                "frac": gbs / peaks["hbm_gbs"]},
+                                "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("conv.step")},
                    "note": f"{byts / 1e6:.0f} MB per call (inputs, outputs and pool together larger than L2); no flush"}
     return {"workload": f"conv-bf16-T{T}-C{C}-W{W}-silu", **res,
             "tokens_per_s_fwd_bwd": T / ((res["fwd"]["ms"] + res["bwd"]["ms"]) * 1e-3),

@@ -5,7 +5,8 @@
 // per sequence, positions before its first token read its convolution state (the W - 1
 // inputs that preceded it, oldest first). All three kernels are memory-bound streams.
 // Forward and backward: a CTA owns a tile of channels (a thread one 16-byte group: 8 bf16
-// or 4 fp32; 4 channels in the backward) and a contiguous token range, one CTA pair per SM;
+// or 4 fp32; 4 channels in the backward and the step) and a contiguous token range, one CTA
+// pair per SM;
 // one thread streams the tile's rows into a ring of shared-memory stages with bulk copies
 // (about 64 KB in flight per CTA, independent of registers), every thread walks the rows in
 // order keeping the W - 1 previous inputs in registers, so each input row is read from
@@ -496,8 +497,8 @@ __global__ void conv_dw_reduce_kernel(const float *partial, int groups, int C, i
 }
 
 template <typename IO, int W>
-__global__ void __launch_bounds__(CONV_THREADS) conv_step_kernel(const ConvParams p) {
-  constexpr int V = 16 / (int)sizeof(IO);
+__global__ void __launch_bounds__(CONV_THREADS, sizeof(IO) == 2 ? 4 : 3) conv_step_kernel(const ConvParams p) {
+  constexpr int V = 4;   // 4 channels a thread: few registers, many warps for a latency-bound call
   constexpr int WP = W > 1 ? W - 1 : 1;
   constexpr bool FAST = sizeof(IO) == 2;
   using IOV = ConvIO<IO, V>;
@@ -599,7 +600,7 @@ cudaError_t bwd_t(const ConvParams &p, cudaStream_t s) {
 }
 template <typename IO>
 cudaError_t step_t(const ConvParams &p, cudaStream_t s) {
-  constexpr int V = 16 / (int)sizeof(IO);
+  constexpr int V = 4;
   const dim3 grid((unsigned)((p.C / V + CONV_THREADS - 1) / CONV_THREADS), (unsigned)p.n_seqs);
   switch (p.W) {
     case 1: conv_step_kernel<IO, 1><<<grid, CONV_THREADS, 0, s>>>(p); break;

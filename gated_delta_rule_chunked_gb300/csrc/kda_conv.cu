@@ -268,7 +268,23 @@ __global__ void __launch_bounds__(CONV_THREADS, 2) conv_fwd_kernel(const ConvPar
     }
     const char *stage = ring + (size_t)slot * CONV_STAGE + tid * 16;
     const long long tb = T0 + k * ROWS;
-    if (active)
+    if (active && s.s1 > tb + ROWS && tb + ROWS <= T1) {   // a whole stage inside one sequence, not its last row
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) {
+        const long long t = tb + r;
+        const Raw xr = *reinterpret_cast<const Raw *>(stage + r * ROWB);
+        float xv[V], z[V];
+        IOV::unpack(xr, xv);
+        conv_point<IO, V, W, WP>(w, b, win, xv, z);
+        if (p.act)
+#pragma unroll
+          for (int e = 0; e < V; ++e) z[e] *= sigm<FAST>(z[e]);
+        IOV::store(static_cast<IO *>(p.y) + t * p.C + c0, z);
+#pragma unroll
+        for (int i = 0; i + 1 < W - 1; ++i) win[i] = win[i + 1];
+        if (W > 1) win[WP - 1] = xr;
+      }
+    } else if (active)
 #pragma unroll 4
       for (int r = 0; r < ROWS; ++r) {
         const long long t = tb + r;
@@ -404,7 +420,50 @@ __global__ void __launch_bounds__(CONV_THREADS, 2) conv_bwd_kernel(const ConvPar
       }
       const char *stage = ring + (size_t)slot * CONV_STAGE + tid * V * (int)sizeof(IO);
       const long long tb = T0 + k * ROWS;
-      if (active && !done)
+      // a stage inside one sequence and inside the range, away from its edges: every row is
+      // owned, every row leaving the window is an owned input row with no state-out gradient
+      const bool plain = s.s1 >= tb + ROWS && tb + ROWS <= T1 && tb - W >= T0 && tb - W >= s.s0;
+      if (active && !done && plain) {
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+          const long long t = tb + r;
+          const Raw xr = *reinterpret_cast<const Raw *>(stage + (2 * r) * ROWB);
+          const Raw gr = *reinterpret_cast<const Raw *>(stage + (2 * r + 1) * ROWB);
+          *reinterpret_cast<float4 *>(p.dx + (t - W) * p.C + c0) =
+              make_float4(pend[W - 1][0], pend[W - 1][1], pend[W - 1][2], pend[W - 1][3]);
+#pragma unroll
+          for (int m = W - 1; m > 0; --m)
+#pragma unroll
+            for (int e = 0; e < V; ++e) pend[m][e] = pend[m - 1][e];
+          float xv[V], gv[V], wf[WP][V], z[V], dz[V];
+          IOV::unpack(xr, xv);
+          IOV::unpack(gr, gv);
+#pragma unroll
+          for (int j = 0; j < W - 1; ++j) IOV::unpack(win[j], wf[j]);
+#pragma unroll
+          for (int e = 0; e < V; ++e) {
+            z[e] = fmaf(w[W - 1][e], xv[e], b[e]);
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j) z[e] = fmaf(w[j][e], wf[j][e], z[e]);
+            if (p.act) {
+              const float sg = sigm<FAST>(z[e]);
+              dz[e] = gv[e] * sg * fmaf(z[e], 1.f - sg, 1.f);
+            } else {
+              dz[e] = gv[e];
+            }
+            pend[0][e] = w[W - 1][e] * dz[e];
+#pragma unroll
+            for (int m = 1; m < W; ++m) pend[m][e] = fmaf(w[W - 1 - m][e], dz[e], pend[m][e]);
+            dbp[e] += dz[e];
+            dwp[W - 1][e] = fmaf(dz[e], xv[e], dwp[W - 1][e]);
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j) dwp[j][e] = fmaf(dz[e], wf[j][e], dwp[j][e]);
+          }
+#pragma unroll
+          for (int i = 0; i + 1 < W - 1; ++i) win[i] = win[i + 1];
+          if (W > 1) win[WP - 1] = xr;
+        }
+      } else if (active && !done)
 #pragma unroll 2
         for (int r = 0; r < ROWS; ++r) {
           const long long t = tb + r;

@@ -83,6 +83,13 @@ def test_conv_equal_sequences_without_offsets(kda):
     run_check(kda, [96, 96, 96], 264, 4, "bf16", "silu", seed=6, equal=True)
 
 
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_conv_long_ranges_varlen(kda, io):
+    # wide rows give each CTA a token range of about a hundred rows: whole stages inside a
+    # sequence take the backward's plain path, the others the general one
+    run_check(kda, [700, 3, 500, 397], 18432, 4, io, "silu", seed=21 if io == "bf16" else 22)
+
+
 def test_conv_many_short_sequences(kda):
     gen = np.random.default_rng(7)
     lens = [int(v) for v in gen.integers(0, 9, size=150)]

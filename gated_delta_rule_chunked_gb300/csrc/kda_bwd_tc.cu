@@ -279,7 +279,10 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   using S = BcSmem;
   extern __shared__ __align__(1024) char smem_raw[];
   char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int chunk = blockIdx.x, h = blockIdx.y, H = p.geo.heads;
+  // head-fastest block order: the CTAs resident at one time cover whole token rows
+  // [t][all heads][d] and consecutive chunk records (DRAM pages read whole), not one head's
+  // rows strided by heads x d
+  const int H = p.geo.heads, h = (int)(blockIdx.x % (unsigned)H), chunk = (int)(blockIdx.x / (unsigned)H);
   ChunkRef ref;
   if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -791,7 +794,9 @@ cudaError_t launch_bwd_chunk_tc(const BwdChunkParams &p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kda_bwd_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        BcSmem::BYTES);
   if (e != cudaSuccess) return e;
-  kda_bwd_chunk_tc_kernel<<<dim3(p.geo.max_chunks, p.geo.heads), BC_THREADS, BcSmem::BYTES, s>>>(p);
+  const long long blocks = (long long)p.geo.max_chunks * p.geo.heads;   // head-fastest: see the kernel
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kda_bwd_chunk_tc_kernel<<<(unsigned)blocks, BC_THREADS, BcSmem::BYTES, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -183,7 +183,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
   using S = PrepSmem2;
   constexpr bool PRECISE = sizeof(E) == 4;   // fp32 I/O: exact fp32 products
   extern __shared__ __align__(128) char smem[];
-  const int chunk = blockIdx.x, h = blockIdx.y, H = p.geo.heads;
+  // head-fastest block order: the CTAs resident at one time cover whole token rows
+  // [t][all heads][d] and consecutive chunk records (DRAM pages read whole), not one head's
+  // rows strided by heads x d
+  const int H = p.geo.heads, h = (int)(blockIdx.x % (unsigned)H), chunk = (int)(blockIdx.x / (unsigned)H);
   ChunkRef ref;
   if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
@@ -522,8 +525,9 @@ static cudaError_t launch_prep_t(const PrepParams &p, cudaStream_t s) {
   auto kern = kda_prep_kernel<E>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.geo.max_chunks, p.geo.heads);
-  kern<<<grid, PREP_THREADS, S::BYTES, s>>>(p);
+  const long long blocks = (long long)p.geo.max_chunks * p.geo.heads;   // head-fastest: see the kernel
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)blocks, PREP_THREADS, S::BYTES, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -305,7 +305,8 @@ typedef struct {
     const float *weight;       /* [C, W]                                                 */
     const float *bias;         /* [C] or NULL                                            */
     void *state;               /* [n_slots, W-1, C] io dtype, updated in place           */
-    const int32_t *state_indices;   /* [N] slot of each sequence, or NULL = slot i       */
+    const int32_t *state_indices;   /* [N] slot of each sequence, or NULL = slot i; the
+                                       slots of sequences that commit must be distinct  */
     int32_t n_slots;           /* slots in the pool (N when state_indices is NULL)       */
     const int32_t *accept_len; /* [N] slots to commit (clamped to 0..L), or NULL = L     */
     const int32_t *first_slot; /* [N] padding slots before the tokens, or NULL = 0       */

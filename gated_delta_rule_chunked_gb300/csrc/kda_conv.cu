@@ -8,7 +8,7 @@
 // or 4 fp32; 4 channels in the backward and the step) and a contiguous token range, one CTA
 // pair per SM;
 // one thread streams the tile's rows into a ring of shared-memory stages with bulk copies
-// (about 64 KB in flight per CTA, independent of registers), every thread walks the rows in
+// (up to 96 KB in flight per CTA, independent of registers), every thread walks the rows in
 // order keeping the W - 1 previous inputs in registers, so each input row is read from
 // memory once (plus W - 1 rows at the range edges) and each output row written once with
 // coalesced 16-byte stores.
@@ -124,8 +124,8 @@ __device__ __forceinline__ SeqSpan seq_of(const ConvParams &p, long long t) {
   return s;
 }
 
-// Input at position pos (relative to nothing: a token index) of sequence s, for pos >= s0 - (W-1):
-// a token row, or a state row (zero without a state).
+// Input at token index pos of sequence s (pos >= s0 - (W-1)): a token row, or, before the
+// sequence's first token, a row of its state (zero without a state).
 template <typename IO, int V, int W>
 __device__ __forceinline__ typename ConvIO<IO, V>::Raw input_at(const ConvParams &p, const SeqSpan &s, long long pos,
                                                                 int c0) {

@@ -77,3 +77,16 @@ def test_backward_central_differences():
         wp[c] += h
         wm[c] -= h
         np.testing.assert_allclose((loss(src, wp) - loss(src, wm)) / (2 * h), dw[c], rtol=1e-6, atol=1e-8)
+
+
+def test_constant_source_closed_form():
+    # x = c everywhere: RMS = |c| (up to eps), so r = (c^2 + eps)^(-1/2) and logit = r c sum(w)
+    d, eps = 16, 1e-6
+    w = torch.linspace(-1.0, 2.0, d)
+    src = [torch.full((1, d), 3.0), torch.full((1, d), -0.5)]
+    _, alpha, rstd, logit = oracle.attnres_fwd(src, w, eps=eps)
+    r = np.array([(9.0 + eps) ** -0.5, (0.25 + eps) ** -0.5])
+    np.testing.assert_allclose(rstd[0], r, rtol=1e-14)
+    np.testing.assert_allclose(logit[0], r * np.array([3.0, -0.5]) * float(w.double().sum()), rtol=1e-13)
+    e = np.exp(logit[0] - logit[0].max())
+    np.testing.assert_allclose(alpha[0], e / e.sum(), rtol=1e-14)

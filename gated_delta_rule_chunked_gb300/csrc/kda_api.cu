@@ -556,7 +556,9 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
   pp.tm_g = tm_g;
   if (!a->skip_prep && (e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
-  kda::FwdScanParams sp{geo, a->v, rec, a->h0, a->o, a->hT, a->saved, a->dev_status, a->h0_identity != 0};
+  kda::FwdScanParams sp{geo, a->v, rec, a->h0, a->o, a->hT, a->saved, a->dev_status, a->h0_identity != 0, {}};
+  if (!f32 && a->v && !map_tokens(&sp.tm_v, a->v, false, a->total_tokens, a->heads, 64, true))
+    return fail(KDA_ERR_CUDA, "%s: could not encode the TMA tensor maps", "kda_fwd");
   e = f32 ? kda::launch_fwd_scan(sp, true, pick_slice(a), stream) : kda::launch_fwd_scan_tc(sp, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_fwd scan");
   mark(2, stream);

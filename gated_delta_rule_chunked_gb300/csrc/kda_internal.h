@@ -83,6 +83,7 @@ struct FwdScanParams {
                            // (swizzled), or null
   int *status;
   int h0_identity;         // start every sequence from the identity state (h0 ignored)
+  CUtensorMap tm_v;        // bf16 scan: v as boxes of 64 channels x 1 head x 64 tokens, 128-byte swizzle
 };
 
 struct BwdScanParams {

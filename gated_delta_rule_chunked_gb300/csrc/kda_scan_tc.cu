@@ -1,7 +1,7 @@
 // kda_scan_tc.cu -- the forward inter-chunk state passing on 5th-generation tensor cores.
 //
-// One CTA per (sequence, head): 4 state warps run the chain below, 4 io warps load
-// and transpose the next chunk's values and write the outputs. The 128x128 fp32 state lives in tensor
+// One CTA per (sequence, head): 4 state warps run the chain below, 4 io warps write
+// the outputs. The 128x128 fp32 state lives in tensor
 // memory for the whole sequence, transposed: TMEM lane m = value channel m,
 // column n = key channel n (S^T). Thread t of warp w owns lane 32w + t, so every
 // elementwise pass is a row pass. TMEM: two sets of 256 columns, [S^T | O^T | U^T]. Per 64-token chunk, with the record of the prep kernel
@@ -9,9 +9,10 @@
 // WY/UT transform into one operand):
 //
 //   pass A : S^T -> bf16 operand tile (the saved chunk-start state is a bulk
-//            copy of it); S^T <- S^T Diag(gC) in TMEM; values V^T -> operand tile
+//            copy of it); S^T <- S^T Diag(gC) in TMEM
 //   phase 1: [O^T | U^T]  = S^T [Qt; -W]^T          (M=128, N=128, K=128)
-//            U^T         += V^T Tb^T                 (M=128, N=64,  K=64)
+//            U^T         += V^T Tb^T                 (M=128, N=64,  K=64; V^T read MN-major
+//                                                     straight from the TMA boxes of V's rows)
 //   pass B : U^T -> bf16 operand tile
 //   phase 2: [S^T | O^T] += U^T [Kh^T; Bm]^T         (M=128, N=192, K=64)
 // TMEM holds two sets of [S^T | O^T | U^T], alternating per chunk, so the previous
@@ -20,7 +21,7 @@
 // i.e. U = Tb (V - Kt S), O = Qt S + Bm U, S <- gC*S + Kh^T U. One thread issues
 // the MMAs; completion is signalled through mbarriers (tcgen05.commit). The next
 // chunk's record arrives by TMA bulk copy into the second of two buffers, and
-// the next chunk's values are loaded into registers one chunk ahead. Every wait
+// the next chunk's values arrive by TMA as soon as phase 1 has read this chunk's. Every wait
 // is bounded; on a timeout the kernel reports KDA_ERR_TIMEOUT, frees its tensor
 // memory and returns.
 #include "kda_common.cuh"
@@ -34,7 +35,7 @@ struct TcScanSmem {
   static constexpr int REC0 = 0, REC1 = RECS;
   static constexpr int AS = 2 * RECS;        // S^T bf16 [128][K=128]: two 16 KB blocks (also the saved state)
   static constexpr int AU = AS + 32768;      // U^T bf16 [128][K=64]; raw value rows before pass B
-  static constexpr int AV = AU + 16384;      // V^T bf16 [128][K=64]
+  static constexpr int AV = AU + 16384;      // V [64 tok][128] bf16 as two 64-channel SW128 boxes (V^T MN-major)
   static constexpr int OST = AV + 16384;     // staging [64 tok][128] bf16: raw values in, outputs out (io warps)
   static constexpr int BAR = OST + 16384;    // 6 mbarriers (see the kernel)
   static constexpr int TSLOT = BAR + 64;
@@ -47,7 +48,14 @@ __device__ __forceinline__ void tc_issue_record(char *dst, const char *src, uint
   bulk_g2s(dst, src, TcRec::BYTES, bar);
 }
 
-__global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p) {
+// V rows of chunk j (two 64-channel boxes, 128-byte swizzle) into the V tile, completing on bar.
+__device__ __forceinline__ void tc_issue_v(char *dst, const FwdScanParams &p, int h, long long t0, uint64_t *bar) {
+  mbar_expect_tx(bar, 16384);
+  tc::tma_load_3d(dst, &p.tm_v, 0, h, (int)t0, bar);
+  tc::tma_load_3d(dst + 8192, &p.tm_v, 64, h, (int)t0, bar);
+}
+
+__global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_constant__ FwdScanParams p) {
   using S = TcScanSmem;
   extern __shared__ __align__(1024) char smem_raw[];
   // operand tiles need 1024-byte alignment in the shared window
@@ -65,10 +73,9 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
   const size_t sh = (size_t)seq * H + h;
 
   // bar[0..1]: record buffers; bar[2]: phase 1 done; bar[3]: phase 2 done (MMA commits);
-  // bar[4]: V^T of the next chunk staged (128 io arrivals); bar[5]: O^T of a chunk read out
+  // bar[4]: the V tile of a chunk landed (TMA); bar[5]: O^T of a chunk read out (128 io arrivals)
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
-    mbar_init(&bar[4], 128);
+    for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
     mbar_init(&bar[5], 128);
     fence_mbar_init();
   }
@@ -103,13 +110,19 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
       tc::wait_st();
     }
     // shared-memory descriptors: the start-address field takes byte offsets >> 4 directly
-    const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS)), d_au = tc::desc_sw128(smem_u32(smem + S::AU)),
-                   d_av = tc::desc_sw128(smem_u32(smem + S::AV));
+    const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS)), d_au = tc::desc_sw128(smem_u32(smem + S::AU));
     const uint64_t d_rec0 = tc::desc_sw128(smem_u32(smem + S::REC0)), d_rec1 = tc::desc_sw128(smem_u32(smem + S::REC1));
     if (tid == 0 && nch > 0) {
       tc_issue_record(smem + S::REC0, rec_of(0), &bar[0]);
       if (nch > 1) tc_issue_record(smem + S::REC1, rec_of(1), &bar[1]);
+      if (v) tc_issue_v(smem + S::AV, p, h, s0, &bar[4]);
     }
+    if (!v) {   // zero values: the V tile stays zero
+      for (int idx = tid; idx < 16384 / 16; idx += 128)
+        *reinterpret_cast<uint4 *>(smem + S::AV + 16 * idx) = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async();
+    }
+    const uint64_t idesc_v = tc::idesc_bf16_mn(128, 64, true, false);
     int done = 0;   // chunks whose phase 2 was issued
     for (int j = 0; j < nch; ++j) {
       const int b = j & 1;
@@ -146,14 +159,22 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
         }
         tc::wait_st();
       }
+      if (v) {   // chunk j's V tile (issued a chunk step ago); a sequence's last chunk: rows past its end zeroed
+        ok &= mbar_wait(&bar[4], j & 1);
+        const int clen = (int)(s1 - (s0 + (long long)j * CH) < CH ? s1 - (s0 + (long long)j * CH) : CH);
+        if (clen < CH && ok)
+          for (int idx = tid; idx < (CH - clen) * 16; idx += 128) {
+            const int r = clen + (idx >> 4), c = idx & 15;
+            *reinterpret_cast<uint4 *>(smem + S::AV + (c >> 3) * 8192 + r * 128 + 16 * (c & 7)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+      }
       fence_proxy_async();
       tc::fence_before();
-      named_sync(1, 128);
+      if (!named_sync_and(1, 128, ok)) break;
       if (tid == 0) {
-        const bool ready = mbar_wait(&bar[4], j & 1);          // V^T of chunk j staged
         tc::fence_after();
-        ok &= ready;
-        if (ready) {
+        {
           const uint64_t d_rb = b ? d_rec1 : d_rec0, d_b1 = d_rb + (TcRec::B1 >> 4), d_tb = d_rb + (TcRec::TB >> 4);
           const uint32_t dO = tmem + colO(j);
 #pragma unroll
@@ -164,7 +185,8 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
               tc::mma_bf16(dO, d_as + off, d_b1 + off, tc::idesc_bf16(128, 128), (kb | ks) != 0);
             }
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) tc::mma_bf16(dO + 64, d_av + 2 * ks, d_tb + 2 * ks, tc::idesc_bf16(128, 64), 1);
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16(dO + 64, tc::desc_sw128_mn(smem_u32(smem + S::AV) + 2048u * ks, 8192), d_tb + 2 * ks, idesc_v, 1);
           tc::commit(&bar[2]);
         }
       } else if (tid == 32 && p.saved) {
@@ -174,6 +196,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
       }
       ok &= mbar_wait(&bar[2], j & 1);
       tc::fence_after();
+      if (tid == 32 && v && j + 1 < nch) tc_issue_v(smem + S::AV, p, h, s0 + (long long)(j + 1) * CH, &bar[4]);
       // pass B: U^T -> operand tile
       {
         uint32_t r[64];
@@ -228,40 +251,6 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
     if (tid == 32 && p.saved) bulk_wait_all();   // saved states complete before the CTA leaves
   } else {
     // ------------------------------------------------------------ io warps
-    // values of chunk j: 16-byte coalesced loads (row r = idx / 16, chunk idx % 16) held in registers
-    auto load_v = [&](int j, uint4 (&vr)[8]) {
-      const long long t0 = s0 + (long long)j * CH;
-      const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int idx = row + 128 * i, r = idx >> 4, ch = idx & 15;
-        vr[i] = make_uint4(0, 0, 0, 0);   // rows past the end, or no values at all
-        if (v && r < clen) vr[i] = __ldg(reinterpret_cast<const uint4 *>(v + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
-      }
-    };
-    // raw rows -> staging tile -> V^T operand (row = value channel, 64 tokens); then signal
-    auto stage_v = [&](const uint4 (&vr)[8]) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int idx = row + 128 * i;
-        *reinterpret_cast<uint4 *>(smem + S::OST + (idx >> 4) * 256 + (idx & 15) * 16) = vr[i];
-      }
-      named_sync(2, 128);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t lo = *reinterpret_cast<const unsigned short *>(smem + S::OST + (8 * c + 2 * e) * 256 + row * 2);
-          const uint32_t hi = *reinterpret_cast<const unsigned short *>(smem + S::OST + (8 * c + 2 * e + 1) * 256 + row * 2);
-          w[e] = lo | (hi << 16);
-        }
-        *reinterpret_cast<uint4 *>(smem + S::AV + tc::sw128_off(128, row, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      fence_proxy_async();
-      named_sync(2, 128);   // the staging tile is free again
-      mbar_arrive(&bar[4]);
-    };
     // O^T of chunk j (TMEM) -> o. Each warp transposes its 32 value channels through its
     // own columns of the staging tile, then writes 64-byte row pieces with 16-byte stores.
     auto store_o = [&](int j) {
@@ -283,19 +272,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(FwdScanParams p
       }
       __syncwarp();
     };
-    uint4 vr[8];
-    if (nch > 0) {
-      load_v(0, vr);
-      stage_v(vr);
-    }
-    if (nch > 1) load_v(1, vr);
     for (int j = 0; j < nch; ++j) {
-      if (j + 1 < nch) {
-        ok &= mbar_wait(&bar[2], j & 1);   // phase 1 of chunk j has read the V^T tile
-        if (!named_sync_and(2, 128, ok)) break;
-        stage_v(vr);                       // chunk j + 1, loaded a whole step earlier
-        if (j + 2 < nch) load_v(j + 2, vr);
-      }
       ok &= mbar_wait(&bar[3], j & 1);     // phase 2 of chunk j has completed O^T
       tc::fence_after();
       if (!named_sync_and(2, 128, ok)) break;

@@ -617,7 +617,7 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
                                           stream);
   if (e != cudaSuccess) return cuda_fail(e, "kda_bwd chunk table");
   mark(0, stream);
-  kda::BwdScanParams bp{geo, a->dO, sd + sv.rec, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status};
+  kda::BwdScanParams bp{geo, a->dO, sd + sv.rec, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status, cp.tm_do};
   if ((e = kda::launch_bwd_scan_tc(bp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd dS scan");
   mark(1, stream);
   cp.geo = geo;

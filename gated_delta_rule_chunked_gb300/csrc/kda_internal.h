@@ -95,6 +95,7 @@ struct BwdScanParams {
   float *dh0;
   void *dsaved;            // [max_chunks][H] 128x128 E tiles (swizzled): dS^T[v][k] at each chunk end
   int *status;
+  CUtensorMap tm_do;       // dO as boxes of 64 channels x 1 head x 64 tokens, 128-byte swizzle
 };
 
 struct BwdChunkParams {

@@ -298,13 +298,13 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
 }
 
 // ----------------------------------------------------------------- backward
-// Reverse dS scan, same arrangement (4 state warps, 4 io warps staging dO^T and
-// writing dv): dS^T in TMEM columns [0,128), dU^T in
+// Reverse dS scan, same arrangement (4 state warps, 4 io warps writing dv; dO arrives
+// by TMA as two 64-channel boxes of 128-byte-swizzled rows, read MN-major as dO^T): dS^T in TMEM columns [0,128), dU^T in
 // [128,192), dV^T in [192,256). Per chunk (last to first), with the forward's record
 // read MN-major (its [Qt; -W], [Kh^T; Bm] and Tb tiles are the transposes of what the
 // products here take K-major):
 //   pass A : dS^T -> bf16 operand tile (saved as the chunk-end dS by one bulk copy);
-//            dS^T <- dS^T Diag(gC); dO^T -> operand tile (K-block 0 of A2)
+//            dS^T <- dS^T Diag(gC)
 //   phase 1: dU^T  = dO^T Bm + dS^T Kh^T           (M=128, N=64, K=64 + 128)
 //   pass B : dU^T -> operand tile (K-block 1 of A2)
 //   phase 2: dS^T += [dO^T | dU^T] [Qt^T | -W^T]^T  (M=128, N=128, K=128)
@@ -314,14 +314,22 @@ struct TcBwdSmem {
   static constexpr int RECS = (TcRec::BYTES + 1023) / 1024 * 1024;
   static constexpr int REC0 = 0, REC1 = RECS;
   static constexpr int AS = 2 * RECS;        // dS^T bf16 [128][K=128]
-  static constexpr int A2 = AS + 32768;      // [dO^T | dU^T] bf16 [128][K=128]
-  static constexpr int DST = A2 + 32768;     // staging: raw dO rows in, dv rows out (io warps)
+  static constexpr int A2 = AS + 32768;      // K-block 0: dO [64 tok][128] as two SW128 boxes (dO^T MN-major);
+                                             // K-block 1: dU^T bf16 [128][K=64] (K-major)
+  static constexpr int DST = A2 + 32768;     // staging: dv rows out (io warps)
   static constexpr int BAR = DST + 16384;
   static constexpr int TSLOT = BAR + 64;   // 6 mbarriers (see the kernel)
   static constexpr int BYTES = TSLOT + 32 + 1024;
 };
 
-__global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p) {
+// dO rows of chunk j into K-block 0 of A2 (two 64-channel boxes), completing on bar.
+__device__ __forceinline__ void tc_issue_do(char *dst, const BwdScanParams &p, int h, long long t0, uint64_t *bar) {
+  mbar_expect_tx(bar, 16384);
+  tc::tma_load_3d(dst, &p.tm_do, 0, h, (int)t0, bar);
+  tc::tma_load_3d(dst + 8192, &p.tm_do, 64, h, (int)t0, bar);
+}
+
+__global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(const __grid_constant__ BwdScanParams p) {
   using S = TcBwdSmem;
   extern __shared__ __align__(1024) char smem_raw[];
   char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -333,15 +341,15 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
   const int row = tid & 127, qw = warp & 3;   // row = TMEM lane = value channel
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + S::TSLOT);
-  const bf16 *dO = (const bf16 *)p.dO;
   const size_t sh = (size_t)seq * H + h;
 
   // bar[0..1]: record buffers; bar[2]: phase 1 done; bar[3]: phase 2 done (MMA commits);
-  // bar[4]: dO^T of the next chunk staged (128 io arrivals); bar[5]: dV^T of a chunk read out
+  // bar[4]: the dO tile of a chunk landed (TMA); bar[5]: dV^T of a chunk read out (128 io
+  // arrivals); bar[6]: phase 2's products that read the dO tile done (MMA commit)
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
-    mbar_init(&bar[4], 128);
+    for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
     mbar_init(&bar[5], 128);
+    mbar_init(&bar[6], 1);
     fence_mbar_init();
   }
   if (warp == 0) tc::alloc(tslot, 256);
@@ -373,9 +381,11 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
     }
     const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS)), d_a2 = tc::desc_sw128(smem_u32(smem + S::A2));
     if (tid == 0 && nch > 0) {
+      tc_issue_do(smem + S::A2, p, h, s0 + (long long)(nch - 1) * CH, &bar[4]);
       issue(smem + S::REC0, rec_of(nch - 1), &bar[0]);
       if (nch > 1) issue(smem + S::REC1, rec_of(nch - 2), &bar[1]);
     }
+    const uint32_t s_do = smem_u32(smem + S::A2);   // dO^T, MN-major: k-step ks at +2048 ks, channel atoms 8 KB apart
     int done = 0;
     for (int it = 0; it < nch; ++it) {
       const int j = nch - 1 - it, b = it & 1;
@@ -410,20 +420,30 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
         }
         tc::wait_st();
       }
+      {   // this chunk's dO tile; a sequence's last chunk (the first one here): rows past its end zeroed
+        ok &= mbar_wait(&bar[4], it & 1);
+        const long long t0 = s0 + (long long)j * CH;
+        const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
+        if (clen < CH && ok)
+          for (int idx = tid; idx < (CH - clen) * 16; idx += 128) {
+            const int r = clen + (idx >> 4), c = idx & 15;
+            *reinterpret_cast<uint4 *>(smem + S::A2 + (c >> 3) * 8192 + r * 128 + 16 * (c & 7)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+      }
       fence_proxy_async();
       tc::fence_before();
-      named_sync(1, 128);
+      if (!named_sync_and(1, 128, ok)) break;
       if (tid == 0) {
-        const bool ready = mbar_wait(&bar[4], it & 1);   // dO^T of this chunk staged in K-block 0 of A2
         tc::fence_after();
-        ok &= ready;
-        if (ready) {
+        {
           // B(n = j, k = r) = Bm[r][j]: rows r of the record's Bm tile -> MN-major
           const uint32_t s_b2 = smem_u32(rb) + TcRec::B2;
           constexpr uint32_t idn = tc::idesc_bf16_mn(128, 64, false, true);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + 128, d_a2 + 2 * ks, tc::desc_sw128_mn(s_b2 + 16384 + 2048 * ks, 8192), idn, ks > 0);
+            tc::mma_bf16(tmem + 128, tc::desc_sw128_mn(s_do + 2048 * ks, 8192),
+                         tc::desc_sw128_mn(s_b2 + 16384 + 2048 * ks, 8192), tc::idesc_bf16_mn(128, 64, true, true), ks > 0);
           // B(n = j, k = dk) = Kh[j][dk] = Kh^T rows dk -> MN-major
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb)
@@ -467,12 +487,15 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
           // two 64-channel atoms 16 KB apart
           const uint32_t s_rb = smem_u32(rb);
 #pragma unroll
-          for (int kb = 0; kb < 2; ++kb)
+          for (int ks = 0; ks < 4; ++ks)   // K-block 0: dO^T, MN-major
+            tc::mma_bf16(tmem, tc::desc_sw128_mn(s_do + 2048 * ks, 8192),
+                         tc::desc_sw128_mn(s_rb + TcRec::B1 + 2048 * ks, 16384), tc::idesc_bf16_mn(128, 128, true, true), 1);
+          tc::commit(&bar[6]);             // the dO tile is read: the io warps refill it
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc::mma_bf16(tmem, d_a2 + ((kb * 16384 + 32 * ks) >> 4),
-                           tc::desc_sw128_mn(s_rb + TcRec::B1 + 8192 * kb + 2048 * ks, 16384),
-                           tc::idesc_bf16_mn(128, 128, false, true), 1);
+          for (int ks = 0; ks < 4; ++ks)   // K-block 1: dU^T, K-major
+            tc::mma_bf16(tmem, d_a2 + ((16384 + 32 * ks) >> 4),
+                         tc::desc_sw128_mn(s_rb + TcRec::B1 + 8192 + 2048 * ks, 16384),
+                         tc::idesc_bf16_mn(128, 128, false, true), 1);
           // B(n = j, k = r) = Tb[r][j]: rows r of the record's Tb tile -> MN-major
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
@@ -502,39 +525,6 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
     if (tid == 32) bulk_wait_all();   // saved dS complete before the CTA leaves
   } else {
     // ------------------------------------------------------------ io warps
-    auto load_do = [&](int j, uint4 (&x)[8]) {
-      const long long t0 = s0 + (long long)j * CH;
-      const int clen = (int)(s1 - t0 < CH ? s1 - t0 : CH);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int idx = row + 128 * i, r = idx >> 4, ch = idx & 15;
-        x[i] = make_uint4(0, 0, 0, 0);
-        if (r < clen) x[i] = __ldg(reinterpret_cast<const uint4 *>(dO + ((size_t)(t0 + r) * H + h) * 128 + ch * 8));
-      }
-    };
-    // raw dO rows -> staging tile -> dO^T operand (K-block 0 of A2: row = value channel); then signal
-    auto stage_do = [&](const uint4 (&x)[8]) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int idx = row + 128 * i;
-        *reinterpret_cast<uint4 *>(smem + S::DST + (idx >> 4) * 256 + (idx & 15) * 16) = x[i];
-      }
-      named_sync(2, 128);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t lo = *reinterpret_cast<const unsigned short *>(smem + S::DST + (8 * c + 2 * e) * 256 + row * 2);
-          const uint32_t hi = *reinterpret_cast<const unsigned short *>(smem + S::DST + (8 * c + 2 * e + 1) * 256 + row * 2);
-          w[e] = lo | (hi << 16);
-        }
-        *reinterpret_cast<uint4 *>(smem + S::A2 + tc::sw128_off(128, row, 8 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      fence_proxy_async();
-      named_sync(2, 128);   // the staging tile is free again
-      mbar_arrive(&bar[4]);
-    };
     // dV^T (TMEM) -> dv rows of chunk j (fp32). Each warp transposes its 32 value channels
     // through its own 4 KB of the staging tile, 32 tokens at a time, and writes 128-byte
     // row pieces with 16-byte stores.
@@ -560,21 +550,19 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(BwdScanParams p
         __syncwarp();
       }
     };
-    uint4 dr[8];
-    if (nch > 0) {
-      load_do(nch - 1, dr);
-      stage_do(dr);
-    }
-    if (nch > 1) load_do(nch - 2, dr);
     for (int it = 0; it < nch; ++it) {
       const int j = nch - 1 - it;
-      ok &= mbar_wait(&bar[3], it & 1);   // phase 2 of this chunk: A2 and dV^T are final
+      if (it + 1 < nch) {   // phase 2 has read this chunk's dO tile: the next chunk's dO into it
+        const bool rd = mbar_wait(&bar[6], it & 1);
+        ok &= rd;
+        if (tid == 128 && rd) {
+          tc::fence_after();
+          tc_issue_do(smem + S::A2, p, h, s0 + (long long)(j - 1) * CH, &bar[4]);
+        }
+      }
+      ok &= mbar_wait(&bar[3], it & 1);   // phase 2 of this chunk: dV^T is final
       tc::fence_after();
       if (!named_sync_and(2, 128, ok)) break;
-      if (it + 1 < nch) {
-        stage_do(dr);                      // the next chunk's dO, loaded a whole step earlier
-        if (it + 2 < nch) load_do(j - 2, dr);
-      }
       store_dv(j);
       named_sync(2, 128);                  // every warp is done with the staging tile
       tc::fence_before();

@@ -189,14 +189,18 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
             tc::mma_bf16(dO + 64, tc::desc_sw128_mn(smem_u32(smem + S::AV) + 2048u * ks, 8192), d_tb + 2 * ks, idesc_v, 1);
           tc::commit(&bar[2]);
         }
-      } else if (tid == 32 && p.saved) {
-        // the chunk-start state leaves as one bulk copy of the operand tile
-        bulk_s2g((bf16 *)p.saved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
-        bulk_commit();
       }
       ok &= mbar_wait(&bar[2], j & 1);
       tc::fence_after();
-      if (tid == 32 && v && j + 1 < nch) tc_issue_v(smem + S::AV, p, h, s0 + (long long)(j + 1) * CH, &bar[4]);
+      if (tid == 32) {
+        // the next chunk's values first, then the chunk-start state, which leaves as one bulk
+        // copy of the operand tile (it has until the next pass A to read the tile)
+        if (v && j + 1 < nch) tc_issue_v(smem + S::AV, p, h, s0 + (long long)(j + 1) * CH, &bar[4]);
+        if (p.saved) {
+          bulk_s2g((bf16 *)p.saved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
+          bulk_commit();
+        }
+      }
       // pass B: U^T -> operand tile
       {
         uint32_t r[64];

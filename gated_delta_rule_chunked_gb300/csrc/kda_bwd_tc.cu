@@ -279,19 +279,14 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   using S = BcSmem;
   extern __shared__ __align__(1024) char smem_raw[];
   char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  // head-fastest block order: the CTAs resident at one time cover whole token rows
-  // [t][all heads][d] and consecutive chunk records (DRAM pages read whole), not one head's
-  // rows strided by heads x d
-  const int H = p.geo.heads, h = (int)(blockIdx.x % (unsigned)H), chunk = (int)(blockIdx.x / (unsigned)H);
-  ChunkRef ref;
-  if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) return;
+  const int H = p.geo.heads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qw = warp & 3, hf = warp >> 2;          // lane quarter, column half
   const int row = 32 * qw + lane;                   // TMEM lane of this thread
   const int r64 = 16 * qw + (lane & 15);            // row of this lane in an M = 64 accumulator (lanes < 16)
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);   // [0] loads, [1..4] groups A-D, [5..8] rounds, [9] A
+  // [0] loads, [1..4] groups A-D, [5..8] rounds, [9] A, [10] the next block's prefetched tiles
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + S::TSLOT);
-  const size_t rid = (size_t)chunk * H + h;
   float *sb = reinterpret_cast<float *>(smem + S::SB);
   float *rq0 = reinterpret_cast<float *>(smem + S::RQ0), *rk = reinterpret_cast<float *>(smem + S::RK);
   float(*tot)[128] = (float(*)[128])(smem + S::TOT);
@@ -300,7 +295,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   float(*dvp)[128] = (float(*)[128])(smem + S::DV);
 
   if (tid == 0) {
-    for (int i = 0; i < 10; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < 11; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
   }
   if (warp == 0) tc::alloc(tslot, 512);
@@ -314,6 +309,25 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
     if (warp == 0) tc::dealloc(tmem, 512);
   };
 
+  // Persistent: CTA b runs blocks b, b + grid, ... in head-fastest order (the CTAs resident at
+  // one time cover whole token rows [t][all heads][d] and consecutive chunk records). While a
+  // block's round epilogues run, the next block's dO, T and first S^T block are fetched into
+  // the tiles the rounds no longer use.
+  const long long nblk = (long long)p.geo.max_chunks * H;
+  int it = 0;
+  for (long long blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
+  const int h = (int)(blk % H), chunk = (int)(blk / H);
+  ChunkRef ref;
+  if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) break;
+  const uint32_t ph = (uint32_t)(it & 1);
+  const bool pre = it > 0;   // the previous block prefetched this block's dO, T and S^T block 0
+  const long long nb = blk + gridDim.x;   // the block this CTA runs next, if any
+  ChunkRef nr;
+  const bool have_next = nb < nblk && chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, (int)(nb / H), nr);
+  const int nh = (int)(nb % H);
+  const size_t nrid = (size_t)(nb / H) * H + nh;
+  const size_t rid = (size_t)chunk * H + h;
+
   // ---------------------------------------------------------------- loads
   // bulk copies of the saved tiles and the record; TMA boxes of this chunk's V, dO, q, k rows
   // (rows past the tensor read as zero) and of T
@@ -321,20 +335,27 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   if (tid == 0) {
     const char *rb = (const char *)p.img + rid * TcRec::BYTES;
     fence_proxy_async();
-    mbar_expect_tx(&bar[0], 2 * 32768 + (TcRec::TB - TcRec::B2) + (TcRec::BYTES - TcRec::TB) + KtRec::BYTES +
-                                5 * 16384);
-    bulk_g2s(smem + S::SS, (const char *)p.saved + rid * 32768, 32768, &bar[0]);
+    mbar_expect_tx(&bar[0], (pre ? 16384 : 32768) + 32768 + (TcRec::TB - TcRec::B2) + (TcRec::BYTES - TcRec::TB) +
+                                KtRec::BYTES + (pre ? 3 : 5) * 16384);
+    if (pre)
+      bulk_g2s(smem + S::SS + 16384, (const char *)p.saved + rid * 32768 + 16384, 16384, &bar[0]);
+    else
+      bulk_g2s(smem + S::SS, (const char *)p.saved + rid * 32768, 32768, &bar[0]);
     bulk_g2s(smem + S::SDS, (const char *)p.dsaved + rid * 32768, 32768, &bar[0]);
     bulk_g2s(smem + S::KHT, rb + TcRec::B2, TcRec::TB - TcRec::B2, &bar[0]);        // Kh^T, Bm
     bulk_g2s(smem + S::TB, rb + TcRec::TB, TcRec::BYTES - TcRec::TB, &bar[0]);      // Tb, e^{G_last}
     bulk_g2s(smem + S::KT, (const char *)p.kt + rid * KtRec::BYTES, KtRec::BYTES, &bar[0]);   // Kt
     tc::tma_load_3d(smem + S::V, &p.tm_v, 0, h, t0i, &bar[0]);
-    tc::tma_load_3d(smem + S::DO, &p.tm_do, 0, h, t0i, &bar[0]);
-    tc::tma_load_3d(smem + S::DO + 8192, &p.tm_do, 64, h, t0i, &bar[0]);
+    if (!pre) {
+      tc::tma_load_3d(smem + S::DO, &p.tm_do, 0, h, t0i, &bar[0]);
+      tc::tma_load_3d(smem + S::DO + 8192, &p.tm_do, 64, h, t0i, &bar[0]);
+    }
     tc::tma_load_3d(smem + S::QR, &p.tm_q, 0, h, t0i, &bar[0]);
     tc::tma_load_3d(smem + S::KR, &p.tm_k, 0, h, t0i, &bar[0]);
-    tc::tma_load_2d(smem + S::TK, &p.tm_aux, 0, arow + 64, &bar[0]);
-    tc::tma_load_2d(smem + S::TK + 8192, &p.tm_aux, 32, arow + 64, &bar[0]);
+    if (!pre) {
+      tc::tma_load_2d(smem + S::TK, &p.tm_aux, 0, arow + 64, &bar[0]);
+      tc::tma_load_2d(smem + S::TK + 8192, &p.tm_aux, 32, arow + 64, &bar[0]);
+    }
   }
   if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
   // while the copies land: the gate scan (thread = channel pair x sub-block), from global memory;
@@ -358,7 +379,8 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
     tot[a][c0] = run.x;
     tot[a][c0 + 1] = run.y;
   }
-  bool ok = mbar_wait(&bar[0], 0);
+  bool ok = mbar_wait(&bar[0], ph);
+  if (pre) ok &= mbar_wait(&bar[10], (uint32_t)((it - 1) & 1));
   if (ref.len < CH && ok) {
     // a sequence's last chunk: rows past its end read as zero (the boxes hold the next sequence's rows)
     for (int idx = tid; idx < (CH - ref.len) * 16; idx += BC_THREADS) {
@@ -459,7 +481,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       reinterpret_cast<float *>(smem + S::TAIL)[c] = ((s4[0] + s4[1]) + (s4[2] + s4[3]) + xch[c]) * exp2f(e3);
     }
   }
-  ok = __all_sync(0xffffffffu, mbar_wait(&bar[1], 0));
+  ok = __all_sync(0xffffffffu, mbar_wait(&bar[1], ph));
   tc::fence_after();
   // E: 32 columns of a [channel][tok] accumulator -> bf16 operand tile rows = channel (K-major over tok)
   auto to_tile = [&](uint32_t col, uint32_t tile_off) {
@@ -511,7 +533,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       tc::mma_bf16(tmem + T_DTB, mnmaj(s_dut, ks, 8192), mnmaj(s_vpt, ks, 8192), tc::idesc_bf16_mn(64, 64, true, true), ks > 0);
     tc::commit(&bar[2]);
   }
-  ok = __all_sync(0xffffffffu, mbar_wait(&bar[2], 0));
+  ok = __all_sync(0xffffffffu, mbar_wait(&bar[2], ph));
   tc::fence_after();
   if (ok) {
     to_tile(T_U, S::UT);     // U^T (the V'^T tile is done)
@@ -597,7 +619,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       tc::mma_tf32(tmem + T_X, kmaj(s_dt, ks, (uint32_t)(S::DT1 - S::DT0)), kmaj(s_tk, ks, 8192), tc::idesc_tf32(64, 64), ks > 0);
     tc::commit(&bar[3]);
   }
-  ok = __all_sync(0xffffffffu, mbar_wait(&bar[3], 0));
+  ok = __all_sync(0xffffffffu, mbar_wait(&bar[3], ph));
   tc::fence_after();
   float tcol[16];   // T[m0 + e][r] for the in-place transpose of T (thread: r = tid % 64, m0 = 16 (tid / 64))
   if (ok) {
@@ -694,7 +716,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       st2((bf16 *)(smem + S::RF + o), kf.x * ks_ * y0, kf.y * ks_ * y1);
     }
   }
-  ok = __all_sync(0xffffffffu, mbar_wait(&bar[4], 0) && mbar_wait(&bar[9], 0));
+  ok = __all_sync(0xffffffffu, mbar_wait(&bar[4], ph) && mbar_wait(&bar[9], ph));
   tc::fence_after();
   float *db2 = reinterpret_cast<float *>(smem + S::DB2P);
   if (ok) {
@@ -731,6 +753,18 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   tc::fence_before();
   if (!__syncthreads_and(ok)) return fail_out();
   tc::fence_after();
+  {   // the next block's dO, T and S^T block 0 into the dO/A, T and X^T tiles, free from here on
+    if (tid == 32 && have_next) {
+      const int nt0 = (int)nr.t0, narow = (int)nrid * 128;
+      fence_proxy_async();
+      mbar_expect_tx(&bar[10], 3 * 16384);
+      bulk_g2s(smem + S::SS, (const char *)p.saved + nrid * 32768, 16384, &bar[10]);
+      tc::tma_load_3d(smem + S::DO, &p.tm_do, 0, nh, nt0, &bar[10]);
+      tc::tma_load_3d(smem + S::DO + 8192, &p.tm_do, 64, nh, nt0, &bar[10]);
+      tc::tma_load_2d(smem + S::TK, &p.tm_aux, 0, narow + 64, &bar[10]);
+      tc::tma_load_2d(smem + S::TK + 8192, &p.tm_aux, 32, narow + 64, &bar[10]);
+    }
+  }
   if (tid < ref.len) {   // ref.len <= 64
     const float *db1 = reinterpret_cast<const float *>(smem + S::DB1P);
     p.dbeta[(size_t)(ref.t0 + tid) * H + h] =
@@ -771,7 +805,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
 #pragma unroll 1
   for (int idx = 0; idx < NSUB; ++idx) {
     const uint32_t base = (idx & 1) ? T_R1 : T_R0;
-    ok = mbar_wait(&bar[5 + idx], 0);
+    ok = mbar_wait(&bar[5 + idx], ph);
     tc::fence_before();
     if (!__syncthreads_and(ok)) return fail_out();
     tc::fence_after();
@@ -785,6 +819,10 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
     }
   }
   tc::fence_before();
+  __syncthreads();   // every tile of this block is consumed
+  tc::fence_after();
+  }
+  tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, 512);
 }
@@ -795,8 +833,12 @@ cudaError_t launch_bwd_chunk_tc(const BwdChunkParams &p, cudaStream_t s) {
                                        BcSmem::BYTES);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.geo.max_chunks * p.geo.heads;   // head-fastest: see the kernel
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kda_bwd_chunk_tc_kernel<<<(unsigned)blocks, BC_THREADS, BcSmem::BYTES, s>>>(p);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms < 1)
+    sms = 1;
+  const long long grid = blocks < sms ? blocks : sms;   // one persistent CTA per SM
+  kda_bwd_chunk_tc_kernel<<<(unsigned)grid, BC_THREADS, BcSmem::BYTES, s>>>(p);
   return cudaGetLastError();
 }
 

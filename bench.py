@@ -514,6 +514,7 @@ def bench_e2e(args, dev, world, host):
     for i in range(2):                                 # warm-up: both slots allocated
         issue(i)
     torch.cuda.synchronize(dev)
+    link = host_link_gbs(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(s_in)
     for i in range(2, 2 + K):
@@ -524,7 +525,31 @@ def bench_e2e(args, dev, world, host):
     ms = reduce_max(ms, world)
     return {"value": world * total / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "pipelining": "copy-in, compute and copy-out on three streams, two buffers each"}
+            "pipelining": "copy-in, compute and copy-out on three streams, two buffers each",
+            "host_link_gbs": link,
+            "note": "bound by the host link (inputs in, fp32 gradients out) and by how the copies overlap the "
+                    "compute kernels; host_link_gbs is the pinned copy rate measured just before the timed steps"}
+
+
+def host_link_gbs(dev, n=1 << 30):
+    """Pinned host<->device copy rate right now (one direction at a time, best of 3)."""
+    import torch
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        best = None
+        for _ in range(3):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            dst.copy_(src, non_blocking=True)
+            e.record()
+            torch.cuda.synchronize(dev)
+            ms = s.elapsed_time(e)
+            best = ms if best is None else min(best, ms)
+        out[name] = round(n / (best * 1e-3) / 1e9, 1)
+    del h, d
+    return out
 
 
 # ----------------------------------------------------------------------------- oracle

@@ -348,10 +348,12 @@ def conv_step(x, weight, bias, state, accept_len=None, *, activation: str = "sil
 
 
 def kda_bwd(q, k, v, beta, g, dO, saved, cu_seqlens=None, h0=None, dhT=None, *, scale: float = 1.0,
-            n_seqs: Optional[int] = None, initial_state_grad: bool = True, dev_status=None):
+            n_seqs: Optional[int] = None, initial_state_grad: bool = True, dev_status=None, out=None):
     """Backward of kda_fwd (``saved`` from kda_fwd(..., save=True) with the same inputs).
 
-    Returns a dict of fp32 gradients: dq, dk, dv, dbeta, dg and dh0 (or None).
+    Returns a dict of fp32 gradients: dq, dk, dv, dbeta, dg and dh0 (or None). ``out``, a dict
+    with the same keys, supplies the gradient tensors to write (contiguous fp32 of the inputs'
+    shapes; dh0 [N, H, 128, 128]) instead of fresh ones.
     """
     lib = library()
     _check_inputs(q, k, v, beta, g)
@@ -360,9 +362,21 @@ def kda_bwd(q, k, v, beta, g, dO, saved, cu_seqlens=None, h0=None, dhT=None, *, 
     N = (cu.numel() - 1) if cu is not None else (n_seqs or 1)
     H = q.shape[1]
     f32 = dict(dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty(q.shape, **f32), torch.empty(k.shape, **f32), torch.empty(v.shape, **f32)
-    dg, dbeta = torch.empty(g.shape, **f32), torch.empty(beta.shape, **f32)
-    dh0 = torch.empty((N, H, 128, 128), **f32) if initial_state_grad else None
+    if out is not None:
+        want = {"dq": q.shape, "dk": k.shape, "dv": v.shape, "dg": g.shape, "dbeta": beta.shape}
+        for name, shape in want.items():
+            t = out[name]
+            if t.dtype != torch.float32 or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or t.device != dev:
+                raise ValueError(f"out[{name!r}] must be a contiguous float32 tensor of shape {tuple(shape)} on {dev}")
+        dq, dk, dv, dg, dbeta = (out[n] for n in ("dq", "dk", "dv", "dg", "dbeta"))
+        dh0 = out.get("dh0") if initial_state_grad else None
+        if dh0 is not None and (dh0.dtype != torch.float32 or tuple(dh0.shape) != (N, H, 128, 128)
+                                or not dh0.is_contiguous()):
+            raise ValueError("out['dh0'] must be a contiguous float32 [N, H, 128, 128] tensor")
+    else:
+        dq, dk, dv = torch.empty(q.shape, **f32), torch.empty(k.shape, **f32), torch.empty(v.shape, **f32)
+        dg, dbeta = torch.empty(g.shape, **f32), torch.empty(beta.shape, **f32)
+        dh0 = torch.empty((N, H, 128, 128), **f32) if initial_state_grad else None
     fa = fwd_args(q, k, v, beta, g, cu, h0, None, None, saved, None, scale, n_seqs=N, dev_status=dev_status)
     b = bwd_args(fa, dO, dq, dk, dv, dbeta, dg, dh0, dhT)
     ws_bytes = lib.kda_bwd_workspace_size(C.byref(b))

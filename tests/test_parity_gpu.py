@@ -174,6 +174,18 @@ def test_bwd_is_deterministic(kda):
         assert torch.equal(g1[name], g2[name]), name
 
 
+def test_bwd_into_caller_buffers(kda):
+    # out= writes the same gradients into the caller's tensors (reused across calls)
+    b = make_seq_batch([300], heads=2, io_dtype="bf16", seed=103, h0=True, grad=True)
+    t, o, hT, saved = run_fwd(kda, b, save=True)
+    g1 = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, None, t["h0"])
+    out = {n: torch.full_like(v, float("nan")) for n, v in g1.items() if v is not None}
+    g2 = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, None, t["h0"], out=out)
+    for name in out:
+        assert g2[name].data_ptr() == out[name].data_ptr(), name
+        assert torch.equal(g1[name], out[name]), name
+
+
 # ---------------------------------------------------------------- decode
 
 def check_step(kda, d, tol):

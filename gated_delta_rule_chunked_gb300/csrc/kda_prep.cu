@@ -74,7 +74,8 @@ cudaError_t launch_chunk_table(const int *cu_in, int n_seqs, long long total, in
 
 // ------------------------------------------------------------ the prep kernel
 constexpr int PREP_THREADS = 256;
-constexpr int LDF = 132;   // padded fp32 row of the 64x128 factor tiles (conflict-free fragments)
+constexpr int LDF = 136;   // padded fp32 row of the 64x128 factor tiles: 136 = 8 (mod 32) makes the
+                           // 8-byte fragment reads of the Gram products and the Kt reads of W conflict-free
 constexpr int LDS64 = 68;  // padded fp32 row of 64x64 tiles
 constexpr int LDP = 24;    // padded fp32 row of the 16x16 solver scratch
 
@@ -94,40 +95,62 @@ struct PrepSmem2 {
   static_assert(SCR + 4 * 16 * LDP * 4 <= DV, "solver tiles overlap the vectors");
 };
 
+__device__ __forceinline__ void zero4(float (&a)[4]) { a[0] = a[1] = a[2] = a[3] = 0.f; }
+// x rounded to TF32 (nearest, ties away), kept as an fp32 value
+__device__ __forceinline__ float rtf32(float x) { return __uint_as_float(tf32(x)); }
+
 __device__ __forceinline__ void pair_of(int p, int &a, int &b) {
   a = p >= 6 ? 3 : (p >= 3 ? 2 : (p >= 1 ? 1 : 0));
   b = p - a * (a + 1) / 2;
 }
 
-// acc[nt] (16 rows x 16 cols) += X[16 rows][0:128] * (R[16 rows][0:128] * dvec)^T
-template <bool PRECISE>
-__device__ __forceinline__ void gram16(float (&acc)[2][4], const float *X, const float *Rr, const float *dvec) {
+// Gram units. Unit u = (pair, n-tile): rows 16 pa.. of KL and of QL against the 8 columns
+// 16 pb + 8 nt.. of R scaled by the pair factors D_{pa,pb}:
+//   ak += KL_pa diag(d) R_cols^T (the A side),  aq += QL_pa diag(d) R_cols^T (the B side),
+// both 16 x 8 in the m16n8 accumulator layout. The two products share the scaled R
+// fragments. In the TF32 form the contraction order inside each group of 8 channels is
+// permuted (fragment k = q reads channel 2q, k = q + 4 reads 2q + 1), so every fragment pair
+// is one 8-byte shared-memory read; KL and QL hold values already rounded to TF32. NU units
+// per warp run interleaved (independent accumulator chains).
+struct GramUnit {
+  const float *kl, *ql, *rr, *d;   // KL, QL rows of the row block; R rows of the n-tile; pair factors
+};
+template <bool PRECISE, int NU>
+__device__ __forceinline__ void gram_units(float (&ak)[3][4], float (&aq)[3][4], const GramUnit (&u)[3]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   if constexpr (PRECISE) {
-    for (int c = 0; c < 128; ++c) {
-      const float x0 = X[g * LDF + c], x1 = X[(g + 8) * LDF + c], d = dvec[c];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const float r0 = Rr[(8 * nt + 2 * q) * LDF + c] * d, r1 = Rr[(8 * nt + 2 * q + 1) * LDF + c] * d;
-        acc[nt][0] = fmaf(x0, r0, acc[nt][0]);
-        acc[nt][1] = fmaf(x0, r1, acc[nt][1]);
-        acc[nt][2] = fmaf(x1, r0, acc[nt][2]);
-        acc[nt][3] = fmaf(x1, r1, acc[nt][3]);
+    for (int v = 0; v < NU; ++v)
+      for (int c = 0; c < 128; ++c) {
+        const float d = u[v].d[c];
+        const float k0 = u[v].kl[g * LDF + c], k1 = u[v].kl[(g + 8) * LDF + c];
+        const float q0 = u[v].ql[g * LDF + c], q1 = u[v].ql[(g + 8) * LDF + c];
+        const float r0 = u[v].rr[(2 * q) * LDF + c] * d, r1 = u[v].rr[(2 * q + 1) * LDF + c] * d;
+        ak[v][0] = fmaf(k0, r0, ak[v][0]);
+        ak[v][1] = fmaf(k0, r1, ak[v][1]);
+        ak[v][2] = fmaf(k1, r0, ak[v][2]);
+        ak[v][3] = fmaf(k1, r1, ak[v][3]);
+        aq[v][0] = fmaf(q0, r0, aq[v][0]);
+        aq[v][1] = fmaf(q0, r1, aq[v][1]);
+        aq[v][2] = fmaf(q1, r0, aq[v][2]);
+        aq[v][3] = fmaf(q1, r1, aq[v][3]);
       }
-    }
   } else {
-#pragma unroll 4
+#pragma unroll 2
     for (int kk = 0; kk < 128; kk += 8) {
-      uint32_t a[4];
-      a[0] = tf32(X[g * LDF + kk + q]);
-      a[1] = tf32(X[(g + 8) * LDF + kk + q]);
-      a[2] = tf32(X[g * LDF + kk + q + 4]);
-      a[3] = tf32(X[(g + 8) * LDF + kk + q + 4]);
-      const float d0 = dvec[kk + q], d1 = dvec[kk + q + 4];
+      const int c = kk + 2 * q;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const float *rr = Rr + (8 * nt + g) * LDF + kk;
-        mma1688(acc[nt], a, tf32(rr[q] * d0), tf32(rr[q + 4] * d1));
+      for (int v = 0; v < NU; ++v) {
+        const float2 d = ld2(u[v].d + c), r = ld2(u[v].rr + g * LDF + c);
+        const uint32_t b0 = tf32(r.x * d.x), b1 = tf32(r.y * d.y);
+        const float2 k0 = ld2(u[v].kl + g * LDF + c), k1 = ld2(u[v].kl + (g + 8) * LDF + c);
+        const float2 q0 = ld2(u[v].ql + g * LDF + c), q1 = ld2(u[v].ql + (g + 8) * LDF + c);
+        const uint32_t fa[4] = {__float_as_uint(k0.x), __float_as_uint(k1.x), __float_as_uint(k0.y),
+                                __float_as_uint(k1.y)};
+        const uint32_t fq[4] = {__float_as_uint(q0.x), __float_as_uint(q1.x), __float_as_uint(q0.y),
+                                __float_as_uint(q1.y)};
+        mma1688(ak[v], fa, b0, b1);
+        mma1688(aq[v], fq, b0, b1);
       }
     }
   }
@@ -323,8 +346,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
       const float qh0 = qv.x * rq[r], qh1 = qv.y * rq[r], kh0 = kv.x * rk[r], kh1 = kv.y * rk[r];
       const float kl0 = kh0 * x0, kl1 = kh1 * x1, ql0 = qh0 * x0, ql1 = qh1 * x1;
       const float rr0 = kh0 * y0, rr1 = kh1 * y1;
-      *reinterpret_cast<float2 *>(KL + r * LDF + c0) = make_float2(kl0, kl1);
-      *reinterpret_cast<float2 *>(QL + r * LDF + c0) = make_float2(ql0, ql1);
+      // the Gram products read KL and QL as TF32 operands: round them once here
+      *reinterpret_cast<float2 *>(KL + r * LDF + c0) = PRECISE ? make_float2(kl0, kl1) : make_float2(rtf32(kl0), rtf32(kl1));
+      *reinterpret_cast<float2 *>(QL + r * LDF + c0) = PRECISE ? make_float2(ql0, ql1) : make_float2(rtf32(ql0), rtf32(ql1));
       *reinterpret_cast<float2 *>(RR + r * LDF + c0) = make_float2(rr0, rr1);
       kh0v[i] = rr0 * fa0;                        // Kh = k^ exp(G_last - G_r)
       kh1v[i] = rr1 * fa1;
@@ -356,18 +380,24 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
     }
   }
   __syncthreads();
-  // 3. Gram products: 20 tasks (pair, A|B), warp w takes tasks w, w+8, w+16
-  float acc[3][2][4];
+  // 3. Gram products: 20 units (pair, n-tile), warp w takes units w, w + 8, w + 16
+  float acc[3][4], accq[3][4];
+  {
+    GramUnit un[3];
 #pragma unroll
-  for (int u = 0; u < 3; ++u) {
-    zero(acc[u]);
-    const int task = warp + 8 * u;
-    if (task < 20) {
+    for (int v = 0; v < 3; ++v) {
+      zero4(acc[v]);
+      zero4(accq[v]);
+      const int unit = min(warp + 8 * v, 19), pr = unit >> 1;
       int pa, pb;
-      pair_of(task >> 1, pa, pb);
-      const float *X = (task & 1) ? QL : KL;
-      gram16<PRECISE>(acc[u], X + pa * SUB * LDF, RR + pb * SUB * LDF, dv[task >> 1]);
+      pair_of(pr, pa, pb);
+      un[v].kl = KL + pa * SUB * LDF;
+      un[v].ql = QL + pa * SUB * LDF;
+      un[v].rr = RR + (pb * SUB + 8 * (unit & 1)) * LDF;
+      un[v].d = dv[pr];
     }
+    if (warp < 4) gram_units<PRECISE, 3>(acc, accq, un);
+    else gram_units<PRECISE, 2>(acc, accq, un);
   }
   __syncthreads();   // QL and R are free from here on
   {
@@ -375,27 +405,23 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
     Tile<E, 64> bm((E *)(trec + L.bm));
     float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) : nullptr;
 #pragma unroll
-    for (int u = 0; u < 3; ++u) {
-      const int task = warp + 8 * u;
-      if (task >= 20) continue;
+    for (int v = 0; v < 3; ++v) {
+      const int unit = warp + 8 * v;
+      if (unit >= 20) continue;
       int pa, pb;
-      pair_of(task >> 1, pa, pb);
+      pair_of(unit >> 1, pa, pb);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = pa * SUB + g + 8 * hh, j = pb * SUB + 8 * nt + 2 * q;
-          const float v0 = acc[u][nt][2 * hh], v1 = acc[u][nt][2 * hh + 1];
-          if (task & 1) {
-            const float b0 = j <= r ? v0 : 0.f, b1 = j + 1 <= r ? v1 : 0.f;
-            if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), b0, b1);
-            if (trec) st2(bm.at(r, j), b0, b1);
-          } else {
-            const float a0 = j < r ? v0 : 0.f, a1 = j + 1 < r ? v1 : 0.f;
-            *reinterpret_cast<float2 *>(Lm + r * LDS64 + j) = make_float2(sb[r] * a0, sb[r] * a1);
-            if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(a0, a1);
-          }
-        }
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = pa * SUB + g + 8 * hh, j = pb * SUB + 8 * (unit & 1) + 2 * q;
+        const float v0 = accq[v][2 * hh], v1 = accq[v][2 * hh + 1];
+        const float b0 = j <= r ? v0 : 0.f, b1 = j + 1 <= r ? v1 : 0.f;
+        if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), b0, b1);
+        if (trec) st2(bm.at(r, j), b0, b1);
+        const float w0 = acc[v][2 * hh], w1 = acc[v][2 * hh + 1];
+        const float a0 = j < r ? w0 : 0.f, a1 = j + 1 < r ? w1 : 0.f;
+        *reinterpret_cast<float2 *>(Lm + r * LDS64 + j) = make_float2(sb[r] * a0, sb[r] * a1);
+        if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(a0, a1);
+      }
     }
     // zero the sub-blocks of Bm above the diagonal
     for (int idx = tid; idx < 64 * 32; idx += PREP_THREADS) {

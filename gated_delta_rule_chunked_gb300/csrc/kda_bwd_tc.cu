@@ -30,7 +30,11 @@
 // (M = 128 channels, N = K = 16 MMAs), then dq^ = dQL x, dk^ = dKL x + dR y,
 // dG = dQL QL + dKL KL - dR R, dg = reverse cumulative sum of dG inside the chunk
 // plus e^{G_last} (dgC + sum_r dKh_r Kh_r), and the L2-norm backward gives dq, dk.
-// dQt, dKt and dKh never leave tensor memory.
+// dQt, dKt and dKh never leave tensor memory. The diagonal of Bm, Bm_rr = q^_r . k^_r,
+// does not depend on the gates: it is left out of the factor products (whose two
+// contributions to dG_r would cancel only up to the rounding of the bf16 factor tiles,
+// an error that does not shrink with dg under strong decay) and enters dq^ and dk^
+// directly as dBm_rr k^_r and dBm_rr q^_r.
 //
 // Waits are bounded; on a timeout the CTA reports KDA_ERR_TIMEOUT, frees its tensor
 // memory and returns.
@@ -62,7 +66,8 @@ struct BcSmem {
   static constexpr int XS = CSUM + 1024;               // [2][128] half-block sums of dG
   static constexpr int RD = XS + 1024;                 // [2][4][16] partial row dots
   static constexpr int DB1P = RD + 512, DB2P = DB1P + 1024, SB = DB2P + 512, XCH = SB + 256;
-  static constexpr int END = XCH + 512;
+  static constexpr int DBD = XCH + 512;                // [64] diagonal of dBm (fp32)
+  static constexpr int END = DBD + 256;
   static constexpr int BYTES = END + 1024;             // + alignment slack
   // regions reused once their first contents are consumed
   static constexpr int VPT = KT, UT = KT;              // V'^T, then U^T [v][tok] (groups A, B)
@@ -143,6 +148,7 @@ __device__ __forceinline__ void round_epilogue(RoundCtx &x, const int t, uint32_
   const float(*fv)[128] = (const float(*)[128])(x.smem + S::FV);
   const float(*dvp)[128] = (const float(*)[128])(x.smem + S::DV);
   const float *rq0 = (const float *)(x.smem + S::RQ0), *rk = (const float *)(x.smem + S::RK);
+  const float *dbd = (const float *)(x.smem + S::DBD);
   const float pa = pv[t][c], fa = fv[t][c], tt = tot[t][c];
   // tensor memory: the round's pair products (t + 6 blocks of 8 columns for this thread) and
   // dQt^T, dKt^T, dKh^T, issued together (warp-uniform predicates) with one wait
@@ -193,8 +199,9 @@ __device__ __forceinline__ void round_epilogue(RoundCtx &x, const int t, uint32_
     const float qh = qv[i] * rq0[r], kh = kv[i] * rk[r];
     const float ql = p.scale * qh * xx, kl = kh * xx, rr = kh * yy;
     const float dQL = fmaf(gq[i], pa, tq[i]), dKL = fmaf(-gk[i], pa, tk[i]), dR = fmaf(gh[i], fa, tw[i]);
-    dq_[i] = dQL * xx;
-    dk_[i] = fmaf(dKL, xx, dR * yy);
+    const float bd = dbd[r];   // dBm_rr: Bm_rr = (scale q^_r) . k^_r
+    dq_[i] = fmaf(bd, kh, dQL * xx);
+    dk_[i] = fmaf(dKL, xx, fmaf(dR, yy, bd * p.scale * qh));
     dG[i] = fmaf(dQL, ql, fmaf(dKL, kl, -dR * rr));   // natural-log units
     rv[i] = qh * dq_[i];
     rv[8 + i] = kh * dk_[i];
@@ -634,39 +641,30 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
 #pragma unroll
       for (int e = 0; e < 16; ++e) tcol[e] = *reinterpret_cast<const float *>(smem + S::TK + tc::sw128_off32(64, m0 + e, r));
     }
-    // dBm (masked j <= r) -> bf16 dBm [r][j] and dBm^T [j][r] operand tiles (over the dead dT blocks)
+    // dBm (strictly lower, j < r) -> bf16 dBm [r][j] and dBm^T [j][r] operand tiles (over the
+    // dead dT blocks); its diagonal, in fp32, to DBD
     float v[32];
     ld32(tl + T_DBM + 32 * hf, v);
     tc::wait_ld();
     if (lane < 16) {
+      float diag = 0.f;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         float x8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x8[e] = (32 * hf + 8 * cb + e <= r64) ? v[8 * cb + e] : 0.f;
+        for (int e = 0; e < 8; ++e) {
+          const int j = 32 * hf + 8 * cb + e;
+          x8[e] = j < r64 ? v[8 * cb + e] : 0.f;
+          if (j == r64) diag = v[8 * cb + e];
+        }
         *reinterpret_cast<uint4 *>(smem + S::DBM + tc::sw128_off(64, r64, 32 * hf + 8 * cb)) = tc::pack8(x8);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
           *reinterpret_cast<bf16 *>(smem + S::DBMT + tc::sw128_off(64, 32 * hf + 8 * cb + e, r64)) =
               __float2bfloat16_rn(x8[e]);
       }
+      if ((r64 >> 5) == hf) reinterpret_cast<float *>(smem + S::DBD)[r64] = diag;
     }
-    // sum_r dKh_rc Kh_rc (the e^{G_last} term of dg through Kh), over this warp's 32 rows:
-    // row c of the Kh^T tile, 16-byte chunks
-    ld32(tl + T_DKH + 32 * hf, v);
-    tc::wait_ld();
-    float cs = 0.f;
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-      const uint4 w = *reinterpret_cast<const uint4 *>(smem + S::KHT + tc::sw128_off(128, row, 32 * hf + 8 * cb));
-      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv[e]));
-        cs = fmaf(v[8 * cb + 2 * e], kk.x, fmaf(v[8 * cb + 2 * e + 1], kk.y, cs));
-      }
-    }
-    reinterpret_cast<float *>(smem + S::CSUM)[hf * 128 + row] = cs;
     // X -> X^T [j][m] (fp32 K-major over m) over the dead S^T tile
     ld32(tl + T_X + 32 * hf, v);
     tc::wait_ld();
@@ -799,8 +797,23 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   }
   RoundCtx rc{&p, &ref, smem, tl, row, hf, qw, lane, h, 0.f};
   {
-    const float *cs2 = reinterpret_cast<const float *>(smem + S::CSUM);
-    rc.run = reinterpret_cast<const float *>(smem + S::TAIL)[row] + (cs2[row] + cs2[128 + row]);
+    // sum_r dKh_rc Kh_rc (the e^{G_last} term of dg through Kh) over this thread's 32 rows, with Kh
+    // in fp32 formed exactly as the round epilogues form R F_t: every row's dG takes this product
+    // back out, so the two must agree to fp32 rounding (the record's bf16 Kh would leave an error
+    // that does not shrink with dg)
+    float v[32];
+    ld32(tl + T_DKH + 32 * hf, v);
+    tc::wait_ld();
+    const bf16 *sk_ = (const bf16 *)(smem + S::KR);
+    const float *csb = (const float *)(smem + (hf ? S::CSB : S::CSA)) + row;
+    float cs = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int r = 32 * hf + i, t = r >> 4;
+      const float kh = to_f(sk_[r * D + row]) * rk[r], yy = exp2f(tot[t][row] - csb[i * 128]);
+      cs += v[i] * fv[t][row] * (kh * yy);
+    }
+    reinterpret_cast<float *>(smem + S::CSUM)[hf * 128 + row] = cs;
   }
 #pragma unroll 1
   for (int idx = 0; idx < NSUB; ++idx) {
@@ -809,6 +822,10 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
     tc::fence_before();
     if (!__syncthreads_and(ok)) return fail_out();
     tc::fence_after();
+    if (idx == 0) {   // both halves of the Kh sum are in place after the barrier above
+      const float *cs2 = reinterpret_cast<const float *>(smem + S::CSUM);
+      rc.run = reinterpret_cast<const float *>(smem + S::TAIL)[row] + (cs2[row] + cs2[128 + row]);
+    }
     round_epilogue(rc, NSUB - 1 - idx, base);
     tc::fence_before();
     __syncthreads();   // this buffer is read out

@@ -186,6 +186,39 @@ def test_bwd_into_caller_buffers(kda):
         assert torch.equal(g1[name], out[name]), name
 
 
+def _strong_gates(b, kind, seed):
+    """Replace the batch's log-decay with gates at the documented bound (every g >= -5)."""
+    gen = torch.Generator().manual_seed(seed)
+    if kind == "const":        # every 16-token sub-block sums to exactly -80 on every channel
+        b.g = torch.full_like(b.g, -5.0)
+    elif kind == "uniform":    # g ~ U[-5, 0]
+        b.g = -5.0 * torch.rand(b.g.shape, generator=gen, dtype=torch.float32)
+    else:                      # channels alternate between the bound and a slow decay
+        g = torch.full_like(b.g, -5.0)
+        g[..., 1::2] = -0.01
+        b.g = g
+    return b
+
+
+@pytest.mark.parametrize("kind", ["const", "uniform", "mixed"])
+def test_fwd_gates_at_bound_bf16(kda, kind):
+    b = _strong_gates(make_seq_batch([200, 1, 64, 130], heads=3, io_dtype="bf16", seed=110, h0=True), kind, 7)
+    check_fwd(kda, b, TOL["bf16"])
+
+
+@pytest.mark.parametrize("kind", ["const", "mixed"])
+def test_fwd_gates_at_bound_f32(kda, kind):
+    b = _strong_gates(make_seq_batch([333, 64], heads=2, io_dtype="f32", seed=111, h0=True), kind, 8)
+    check_fwd(kda, b, TOL["f32"])
+
+
+@pytest.mark.parametrize("kind", ["const", "uniform", "mixed"])
+def test_bwd_gates_at_bound_bf16(kda, kind):
+    b = _strong_gates(make_seq_batch([200, 1, 64, 129], heads=3, io_dtype="bf16", seed=112, h0=True, grad=True),
+                      kind, 9)
+    check_bwd(kda, b, TOL["bf16"])
+
+
 # ---------------------------------------------------------------- decode
 
 def check_step(kda, d, tol):

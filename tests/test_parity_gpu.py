@@ -244,6 +244,15 @@ def test_step_f32(kda):
     check_step(kda, make_decode_batch(4, 4, 2, "f32", seed=3), TOL["f32"])
 
 
+def test_step_gates_at_bound(kda):
+    # decode applies exp(g) token by token: strong decay needs no factoring, checked anyway
+    d = make_decode_batch(4, 4, 3, "bf16", seed=6)
+    gen = torch.Generator().manual_seed(60)
+    d.g = -5.0 * torch.rand(d.g.shape, generator=gen, dtype=torch.float32)
+    d.g[1] = -5.0
+    check_step(kda, d, TOL["bf16"])
+
+
 def test_step_accept_zero_leaves_state(kda):
     d = make_decode_batch(3, 4, 2, "bf16", seed=4)
     d.accept_len[:] = torch.tensor([0, 4, 0], dtype=torch.int32)
@@ -404,6 +413,18 @@ def test_fwd_cp_matches_unsplit(kda, lens, P):
     o_ref, h_ref = oracle.assemble_fwd(res, b.cu_seqlens, 3, 128)
     e_o, e_h = rel(o.float().cpu(), o_ref), rel(hT.cpu(), h_ref)
     print("cp", lens, P, f"o {e_o:.2e} hT {e_h:.2e}")
+    assert e_o <= TOL["bf16"] and e_h <= TOL["bf16"], (e_o, e_h)
+
+
+def test_fwd_cp_gates_at_bound(kda):
+    # the segment maps M of strongly decaying segments are tiny (entries underflow): the
+    # chained states must still match the unsplit forward
+    b = _strong_gates(make_seq_batch([700, 300], heads=2, io_dtype="bf16", seed=74, h0=True), "uniform", 10)
+    t = to_dev(b)
+    o, hT = kda.kda_fwd_cp(t["q"], t["k"], t["v"], t["beta"], t["g"], b.cu_seqlens.cpu(), t["h0"], n_segments=4)
+    res = oracle.fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0)
+    o_ref, h_ref = oracle.assemble_fwd(res, b.cu_seqlens, 2, 128)
+    e_o, e_h = rel(o.float().cpu(), o_ref), rel(hT.cpu(), h_ref)
     assert e_o <= TOL["bf16"] and e_h <= TOL["bf16"], (e_o, e_h)
 
 

@@ -483,16 +483,21 @@ def bench_e2e(args, dev, world, host):
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_c = [torch.cuda.Event() for _ in range(2)]
     d2h = 0
+    spans = []   # per step: (copy-in start, end, copy-out start, end) events, to report the link rate seen
 
     def issue(i):
         nonlocal d2h
         slot = i & 1
         d = dev_in[slot]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        spans.append(ev)
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(ev_c[slot])          # step i-2 has finished reading this buffer
+            ev[0].record(s_in)
             for n in names:
                 d[n].copy_(host[n], non_blocking=True)
+            ev[1].record(s_in)
             ev_in[slot].record(s_in)
         with torch.cuda.stream(s_c):
             s_c.wait_event(ev_in[slot])
@@ -506,10 +511,12 @@ def bench_e2e(args, dev, world, host):
                 out_host[slot] = {n: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for n, v in gr.items()
                                   if v is not None}
                 d2h = sum(v.numel() * v.element_size() for v in out_host[slot].values())
+            ev[2].record(s_out)
             for n, v in gr.items():
                 if v is not None:
                     out_host[slot][n].copy_(v, non_blocking=True)
                     v.record_stream(s_out)
+            ev[3].record(s_out)
 
     for i in range(2):                                 # warm-up: both slots allocated
         issue(i)
@@ -523,12 +530,20 @@ def bench_e2e(args, dev, world, host):
     torch.cuda.synchronize(dev)
     ms = start.elapsed_time(end) / K
     ms = reduce_max(ms, world)
+    timed = spans[2:]
+    cin = sorted(ev[0].elapsed_time(ev[1]) for ev in timed)
+    cout = sorted(ev[2].elapsed_time(ev[3]) for ev in timed)
+    seen = {"h2d": round(h2d / (cin[len(cin) // 2] * 1e-3) / 1e9, 1),
+            "d2h": round(d2h / (cout[len(cout) // 2] * 1e-3) / 1e9, 1),
+            "copy_in_ms": round(cin[len(cin) // 2], 2), "copy_out_ms": round(cout[len(cout) // 2], 2)}
     return {"value": world * total / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
             "pipelining": "copy-in, compute and copy-out on three streams, two buffers each",
             "host_link_gbs": link,
+            "link_during_steps_gbs": seen,
             "note": "bound by the host link (inputs in, fp32 gradients out) and by how the copies overlap the "
-                    "compute kernels; host_link_gbs is the pinned copy rate measured just before the timed steps"}
+                    "compute kernels; host_link_gbs is the pinned copy rate measured just before the timed steps, "
+                    "link_during_steps_gbs the median rate of the timed steps' own copies (the two directions overlap)"}
 
 
 def host_link_gbs(dev, n=1 << 30):

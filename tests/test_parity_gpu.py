@@ -165,6 +165,28 @@ def test_bwd_many_heads(kda):
     check_bwd(kda, b, TOL["bf16"], tasks=[(0, 0), (0, 57), (1, 95)])
 
 
+def test_bwd_zero_state_no_dhT_scaled(kda):
+    # h0 = 0 (not passed), no final-state gradient, q scale != 1: dh0 is still the gradient at h0 = 0
+    b = make_seq_batch([130, 64, 1], heads=2, io_dtype="bf16", seed=113, h0=False, grad=True)
+    assert b.h0 is None
+    t = to_dev(b)
+    sc = 128 ** -0.5
+    o, hT, saved = kda.kda_fwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["cu_seqlens"], None, save=True, scale=sc)
+    gr = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, t["cu_seqlens"], None, None,
+                     scale=sc)
+    torch.cuda.synchronize()
+    res = oracle.bwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.dO, None, None, scale=sc)
+    cu = [int(x) for x in b.cu_seqlens.tolist()]
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        got, ref = [], []
+        for (i, h), r in res.items():
+            g_ = gr[name].cpu()
+            got.append((g_[i, h] if name == "dh0" else g_[cu[i]:cu[i + 1], h]).numpy().ravel())
+            ref.append(r[name].ravel())
+        e = rel(np.concatenate(got), np.concatenate(ref))
+        assert e <= TOL["bf16"], (name, e)
+
+
 def test_bwd_is_deterministic(kda):
     b = make_seq_batch([300], heads=2, io_dtype="bf16", seed=102, h0=True, grad=True)
     t, o, hT, saved = run_fwd(kda, b, save=True)

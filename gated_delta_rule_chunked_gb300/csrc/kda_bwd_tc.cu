@@ -65,9 +65,10 @@ struct BcSmem {
   static constexpr int CSUM = TAIL + 512;              // [2][128] halves of sum_r dKh_rc Kh_rc
   static constexpr int XS = CSUM + 1024;               // [2][128] half-block sums of dG
   static constexpr int RD = XS + 1024;                 // [2][4][16] partial row dots
-  static constexpr int DB1P = RD + 512, DB2P = DB1P + 1024, SB = DB2P + 512, XCH = SB + 256;
-  static constexpr int DBD = XCH + 512;                // [64] diagonal of dBm (fp32)
-  static constexpr int END = DBD + 256;
+  static constexpr int DB1P = RD + 512, DB2P = DB1P + 1024, SB = DB2P + 512;
+  static constexpr int DBD = SB + 256;                 // [64] diagonal of dBm (fp32)
+  static constexpr int DGCP = DBD + 256;               // [16][128] partial row dots of S and dS
+  static constexpr int END = DGCP + 8192;
   static constexpr int BYTES = END + 1024;             // + alignment slack
   // regions reused once their first contents are consumed
   static constexpr int VPT = KT, UT = KT;              // V'^T, then U^T [v][tok] (groups A, B)
@@ -471,21 +472,37 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       rk[r] = rsqrtf(sk + 1e-6f);
     }
   }
-  // dgC_c e^{G_last} (two threads per channel)
+  // dgC_c e^{G_last}, dgC_c = sum_v S_cv dS_cv: 16-byte chunks (8 channels) of the S^T and dS^T
+  // tiles, thread = (chunk j, 8 rows v), then the 16 row groups summed in a fixed order
   {
-    const TileSW<128> sS((bf16 *)(smem + S::SS)), sdS((bf16 *)(smem + S::SDS));
-    const int c = tid & 127, half = tid >> 7;
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int vv = 64 * half; vv < 64 * half + 64; vv += 4)
+    const int j = tid & 15, vg = tid >> 4;
+    float acc[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) s4[u] = fmaf(to_f(*sS.at(vv + u, c)), to_f(*sdS.at(vv + u, c)), s4[u]);
-    float *xch = reinterpret_cast<float *>(smem + S::XCH);
-    if (half) xch[c] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t o = tc::sw128_off(128, 8 * vg + i, 8 * j);
+      const uint4 x = *reinterpret_cast<const uint4 *>(smem + S::SS + o);
+      const uint4 y = *reinterpret_cast<const uint4 *>(smem + S::SDS + o);
+      const uint32_t xv[4] = {x.x, x.y, x.z, x.w}, yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xv[e]));
+        const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&yv[e]));
+        acc[2 * e] = fmaf(fx.x, fy.x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(fx.y, fy.y, acc[2 * e + 1]);
+      }
+    }
+    float *part = reinterpret_cast<float *>(smem + S::DGCP);
+    *reinterpret_cast<float4 *>(part + vg * 128 + 8 * j) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4 *>(part + vg * 128 + 8 * j + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     __syncthreads();
-    if (!half) {
-      const float e3 = (tot[0][c] + tot[1][c]) + (tot[2][c] + tot[3][c]);
-      reinterpret_cast<float *>(smem + S::TAIL)[c] = ((s4[0] + s4[1]) + (s4[2] + s4[3]) + xch[c]) * exp2f(e3);
+    if (tid < 128) {
+      float sdg = 0.f;
+#pragma unroll
+      for (int g2 = 0; g2 < 16; ++g2) sdg += part[g2 * 128 + tid];
+      const float e3 = (tot[0][tid] + tot[1][tid]) + (tot[2][tid] + tot[3][tid]);
+      reinterpret_cast<float *>(smem + S::TAIL)[tid] = sdg * exp2f(e3);
     }
   }
   ok = __all_sync(0xffffffffu, mbar_wait(&bar[1], ph));

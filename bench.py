@@ -477,6 +477,7 @@ def bench_e2e(args, dev, world, host):
     total = host["q"].shape[0]
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     K = max(2, min(args.steps, 8))
+    link = host_link_gbs(dev)   # before the pipeline's own pinned and device buffers exist
     s_in, s_c, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     dev_in = [{n: torch.empty(host[n].shape, dtype=host[n].dtype, device=dev) for n in names} for _ in range(2)]
     out_host = [None, None]
@@ -489,7 +490,7 @@ def bench_e2e(args, dev, world, host):
         nonlocal d2h
         slot = i & 1
         d = dev_in[slot]
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         spans.append(ev)
         with torch.cuda.stream(s_in):
             if i >= 2:
@@ -501,9 +502,11 @@ def bench_e2e(args, dev, world, host):
             ev_in[slot].record(s_in)
         with torch.cuda.stream(s_c):
             s_c.wait_event(ev_in[slot])
+            ev[4].record(s_c)
             cu = d["cu_seqlens"]
             o, hT, saved = kda.kda_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], cu, d["h0"], save=True)
             gr = kda.kda_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["dO"], saved, cu, d["h0"])
+            ev[5].record(s_c)
             ev_c[slot].record(s_c)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_c[slot])
@@ -518,31 +521,35 @@ def bench_e2e(args, dev, world, host):
                     v.record_stream(s_out)
             ev[3].record(s_out)
 
-    for i in range(2):                                 # warm-up: both slots allocated
+    W = 4                                              # warm-up: both slots allocated and used twice
+    for i in range(W):
         issue(i)
     torch.cuda.synchronize(dev)
-    link = host_link_gbs(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(s_in)
-    for i in range(2, 2 + K):
+    for i in range(W, W + K):
         issue(i)
     end.record(s_out)
     torch.cuda.synchronize(dev)
     ms = start.elapsed_time(end) / K
     ms = reduce_max(ms, world)
-    timed = spans[2:]
+    timed = spans[W:]
     cin = sorted(ev[0].elapsed_time(ev[1]) for ev in timed)
     cout = sorted(ev[2].elapsed_time(ev[3]) for ev in timed)
     seen = {"h2d": round(h2d / (cin[len(cin) // 2] * 1e-3) / 1e9, 1),
             "d2h": round(d2h / (cout[len(cout) // 2] * 1e-3) / 1e9, 1),
             "copy_in_ms": round(cin[len(cin) // 2], 2), "copy_out_ms": round(cout[len(cout) // 2], 2)}
+    # per timed step, ms from the start of the timed region: copy-in, compute and copy-out spans
+    timeline = [[round(start.elapsed_time(ev[a]), 1) for a in (0, 1, 4, 5, 2, 3)] for ev in timed]
     return {"value": world * total / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
             "pipelining": "copy-in, compute and copy-out on three streams, two buffers each",
             "host_link_gbs": link,
             "link_during_steps_gbs": seen,
+            "timeline_ms": {"columns": ["in_start", "in_end", "compute_start", "compute_end", "out_start",
+                                        "out_end"], "steps": timeline},
             "note": "bound by the host link (inputs in, fp32 gradients out) and by how the copies overlap the "
-                    "compute kernels; host_link_gbs is the pinned copy rate measured just before the timed steps, "
+                    "compute kernels; host_link_gbs is the pinned copy rate measured alone before the pipeline starts, "
                     "link_during_steps_gbs the median rate of the timed steps' own copies (the two directions overlap)"}
 
 

@@ -433,7 +433,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
     }
   }
   __syncthreads();
-  // 4. T = (I + Lm)^-1: diagonal sub-blocks by forward substitution (warps 0..3)
+  // 4. T = (I + Lm)^-1: diagonal sub-blocks by forward substitution (warps 0..3), then the
+  //    off-diagonal blocks level by level on warps 0..3. With a forward record, warps 4..7 form
+  //    W = T (Diag(beta) Kt) one 16-row block at a time as soon as that block of T is final
+  //    (row block a needs T_ab, b <= a: final after level a), and warps 0..3 write T's outputs
+  //    while the last block of W is formed.
   {
     const float *Lm = (const float *)(smem + S::LM);
     float *T = (float *)(smem + S::TT);
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
         for (int i = 0; i < SUB; ++i) T[(ab * SUB + i) * LDS64 + ab * SUB + j] = x[i];
       }
     } else {
-      // warps 4..7 zero the blocks above the diagonal and turn KL into Kt = KL exp(E_{a-1})
+      // warps 4..7 zero the blocks above the diagonal and turn KL into Diag(beta) Kt, Kt = KL exp(E_{a-1})
       for (int idx = tid - 128; idx < 64 * 64; idx += 128) {
         const int r = idx >> 6, j = idx & 63;
         if ((j >> 4) > (r >> 4)) T[r * LDS64 + j] = 0.f;
@@ -464,11 +468,48 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
           const int r = idx >> 6, c = (idx & 63) * 2;
           float2 *kp = reinterpret_cast<float2 *>(KL + r * LDF + c);
           const float2 kv = *kp;
-          *kp = make_float2(kv.x * pvv[r >> 4][c], kv.y * pvv[r >> 4][c + 1]);
+          const float br = sb[r];
+          *kp = make_float2(kv.x * pvv[r >> 4][c] * br, kv.y * pvv[r >> 4][c + 1] * br);
         }
       }
     }
     __syncthreads();
+    // outputs of T: Tb = T Diag(beta) into the record, T for the backward (threads [t0, t0 + nt))
+    auto write_t = [&](int t0, int nth) {
+      Tile<E, 64> tb((E *)(trec + L.tb));
+      float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) + 64 * 64 : nullptr;
+      for (int idx = tid - t0; idx < 64 * 32; idx += nth) {
+        const int r = idx >> 5, j = (idx & 31) * 2;
+        const float t0v = T[r * LDS64 + j], t1v = T[r * LDS64 + j + 1];
+        const float b0 = t0v * sb[j], b1 = t1v * sb[j + 1];
+        if (tcrec) st2((E *)(rec + TcRec::TB + tc::sw128_off(64, r, j)), b0, b1);
+        if (trec) st2(tb.at(r, j), b0, b1);
+        if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(t0v, t1v);
+      }
+    };
+    // one 16-row block of W (B1 rows 64.. hold -W[tok][dk]) on warps 4..7, 32 columns each
+    auto w_block = [&](int mt) {
+      const int n0 = 32 * (warp - NSUB);
+      float wacc[4][4];
+      zero(wacc);
+      for (int kk = 0; kk < 16 * (mt + 1); kk += 8) {
+        uint32_t af[4];
+        af[0] = tf32(T[(16 * mt + g) * LDS64 + kk + q]);
+        af[1] = tf32(T[(16 * mt + g + 8) * LDS64 + kk + q]);
+        af[2] = tf32(T[(16 * mt + g) * LDS64 + kk + q + 4]);
+        af[3] = tf32(T[(16 * mt + g + 8) * LDS64 + kk + q + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+          mma1688(wacc[nt], af, tf32(KL[(kk + q) * LDF + n0 + 8 * nt + g]), tf32(KL[(kk + q + 4) * LDF + n0 + 8 * nt + g]));
+      }
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = 16 * mt + g + 8 * hh, c = n0 + 8 * nt + 2 * q;
+          st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, 64 + r, c)), -wacc[nt][2 * hh], -wacc[nt][2 * hh + 1]);
+        }
+    };
     // off-diagonal sub-blocks by levels: T_ab = -T_aa * sum_{m=b}^{a-1} Lm_am T_mb
     float *P = (float *)(smem + S::SCR) + warp * 16 * LDP;
     for (int d = 1; d < NSUB; ++d) {
@@ -494,53 +535,17 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
           *reinterpret_cast<float2 *>(dst + 8 * LDS64) = make_float2(-tacc[nt][2], -tacc[nt][3]);
         }
         __syncwarp();
+      } else if (tcrec && warp >= NSUB) {
+        w_block(d - 1);   // rows of T final since level d - 1
       }
       __syncthreads();
     }
-  }
-  // 5. Tb = T Diag(beta) (fp32 in place, and into the record); T for the backward
-  {
-    float *T = (float *)(smem + S::TT);
-    Tile<E, 64> tb((E *)(trec + L.tb));
-    float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) + 64 * 64 : nullptr;
-    for (int idx = tid; idx < 64 * 32; idx += PREP_THREADS) {
-      const int r = idx >> 5, j = (idx & 31) * 2;
-      const float t0 = T[r * LDS64 + j], t1 = T[r * LDS64 + j + 1];
-      const float b0 = t0 * sb[j], b1 = t1 * sb[j + 1];
-      if (tcrec) st2((E *)(rec + TcRec::TB + tc::sw128_off(64, r, j)), b0, b1);
-      if (trec) st2(tb.at(r, j), b0, b1);
-      if (tcrec) *reinterpret_cast<float2 *>(T + r * LDS64 + j) = make_float2(b0, b1);
-      if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(t0, t1);
-    }
-  }
-  if (tcrec) {
-    __syncthreads();
-    // 6. W = Tb Kt (64 x 128): forward B1 rows 64..127 hold -W[tok][dk].
-    //    Warp: rows 16*(w&3), columns 64*(w>>2).
-    const float *Tb = (const float *)(smem + S::TT);
-    const int mt = warp & 3, nh = warp >> 2;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float wacc[4][4];
-      zero(wacc);
-      const int n0 = 64 * nh + 32 * half;
-      for (int kk = 0; kk < 16 * (mt + 1); kk += 8) {
-        uint32_t af[4];
-        af[0] = tf32(Tb[(16 * mt + g) * LDS64 + kk + q]);
-        af[1] = tf32(Tb[(16 * mt + g + 8) * LDS64 + kk + q]);
-        af[2] = tf32(Tb[(16 * mt + g) * LDS64 + kk + q + 4]);
-        af[3] = tf32(Tb[(16 * mt + g + 8) * LDS64 + kk + q + 4]);
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-          mma1688(wacc[nt], af, tf32(KL[(kk + q) * LDF + n0 + 8 * nt + g]), tf32(KL[(kk + q + 4) * LDF + n0 + 8 * nt + g]));
-      }
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * mt + g + 8 * hh, c = n0 + 8 * nt + 2 * q;
-          st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, 64 + r, c)), -wacc[nt][2 * hh], -wacc[nt][2 * hh + 1]);
-        }
+    // T is final: the last block of W on warps 4..7 while warps 0..3 write T's outputs
+    if (tcrec) {
+      if (warp >= NSUB) w_block(NSUB - 1);
+      else write_t(0, 128);
+    } else {
+      write_t(0, PREP_THREADS);
     }
   }
 }

@@ -50,6 +50,7 @@ FWD_STAGES = ["fwd.table", "fwd.prep", "fwd.scan"]
 BWD_STAGES = ["bwd.table", "bwd.dscan", "bwd.chunk"]
 KERNEL_SRC = {"fwd.prep": "kda_prep.cu", "fwd.scan": "kda_scan_tc.cu",
               "bwd.dscan": "kda_scan_tc.cu", "bwd.chunk": "kda_bwd_tc.cu",
+              "fwd.prep.inference": "kda_prep.cu", "fwd.scan.inference": "kda_scan_tc.cu",
               "decode": "kda_step.cu", "attnres.fwd": "kda_attnres.cu", "attnres.bwd": "kda_attnres.cu",
               "conv.fwd": "kda_conv.cu", "conv.bwd": "kda_conv.cu", "conv.step": "kda_conv.cu"}
 
@@ -86,6 +87,13 @@ def recorded_traffic(kernel):
     return None
 
 
+def scaled_traffic(kernel, units, ref_units=32768 * 96):
+    """Recorded DRAM bytes per launch of the T=32768 x 96-head workload, scaled to `units`
+    token-heads (the chunk-parallel and scan kernels move a fixed amount per chunk-head)."""
+    t = recorded_traffic(kernel)
+    return None if t is None else t * units / ref_units
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -120,90 +128,181 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- ours
-def run_ours(args, rank, world, local_rank):
+class ChunkedCase:
+    """Resident buffers of one chunked workload, two input sets (different seeds) that the
+    timed steps alternate between, so no step re-reads the previous step's inputs. `mode`
+    "fwdbwd": training forward (saves what the backward needs) + backward; "fwd": the
+    inference forward (no saved, records in the workspace)."""
+
+    def __init__(self, lib, dev, name, mode, status, seq_len=0):
+        import torch
+        import gated_delta_rule_chunked_gb300 as kda
+        from gated_delta_rule_chunked_gb300.inputs import make_workload, WORKLOADS
+        over = {"seq_lens": (seq_len,)} if seq_len else {}
+        seed = WORKLOADS[name].seed
+        self.sets = [make_workload(name, device=dev, **over, **({"seed": seed + 5000} if i else {}))
+                     for i in range(2)]
+        b = self.sets[0]
+        self.T, self.H, self.N = b.total, b.heads, b.n_seqs
+        self.mode = mode
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.o = torch.empty_like(b.v)
+        self.hT = torch.empty((self.N, self.H, D, D), **f32)
+        fa = kda.fwd_args(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, self.o, self.hT)
+        self.saved = (torch.empty(lib.kda_saved_size(C.byref(fa)), dtype=torch.uint8, device=dev)
+                      if mode == "fwdbwd" else None)
+        fa = kda.fwd_args(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, self.o, self.hT, self.saved)
+        self.fws = torch.empty(lib.kda_fwd_workspace_size(C.byref(fa)), dtype=torch.uint8, device=dev)
+        self.fa, self.ba = [], []
+        if mode == "fwdbwd":
+            self.grads = {n: torch.empty(sh, **f32) for n, sh in
+                          (("dq", b.q.shape), ("dk", b.k.shape), ("dv", b.v.shape), ("dg", b.g.shape),
+                           ("dbeta", b.beta.shape), ("dh0", (self.N, self.H, D, D)))}
+        for x in self.sets:
+            a = kda.fwd_args(x.q, x.k, x.v, x.beta, x.g, x.cu_seqlens, x.h0, self.o, self.hT, self.saved, self.fws,
+                             dev_status=status)
+            self.fa.append(a)
+            if mode == "fwdbwd":
+                gr = self.grads
+                ba = kda.bwd_args(a, x.dO, gr["dq"], gr["dk"], gr["dv"], gr["dbeta"], gr["dg"], gr["dh0"])
+                if not hasattr(self, "bws"):
+                    self.bws = torch.empty(lib.kda_bwd_workspace_size(C.byref(ba)), dtype=torch.uint8, device=dev)
+                self.ba.append(kda.bwd_args(a, x.dO, gr["dq"], gr["dk"], gr["dv"], gr["dbeta"], gr["dg"], gr["dh0"],
+                                            None, self.bws))
+
+    def stages(self):
+        return FWD_STAGES + (BWD_STAGES if self.mode == "fwdbwd" else [])
+
+    def step(self, lib, sptr, i, arrays=None):
+        from gated_delta_rule_chunked_gb300 import _lib
+        k = i & 1
+        if arrays is not None:
+            lib.kda_set_profile_events(C.cast(arrays[0], C.c_void_p), len(FWD_STAGES))
+        _lib.check(lib.kda_fwd(C.byref(self.fa[k]), sptr))
+        if self.mode == "fwdbwd":
+            if arrays is not None:
+                lib.kda_set_profile_events(C.cast(arrays[1], C.c_void_p), len(BWD_STAGES))
+            _lib.check(lib.kda_bwd(C.byref(self.ba[k]), sptr))
+        if arrays is not None:
+            lib.kda_set_profile_events(None, 0)
+
+
+def time_case(case, lib, dev, stream, K, W, world=1, on_start=None):
+    """W untimed steps, then K timed steps bracketed by a barrier and synchronisation; per-kernel
+    device times from the events the library records after each launch. Returns (ms per step
+    as the max over ranks, per-kernel ms)."""
     import torch
-    import gated_delta_rule_chunked_gb300 as kda
-    from gated_delta_rule_chunked_gb300 import _lib
-    from gated_delta_rule_chunked_gb300.inputs import make_workload
-
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    lib = kda.library()
-    stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
-
-    b = make_workload(WORKLOAD, device=dev, **({"seq_lens": (args.seq_len,)} if args.seq_len else {}))
-    T, H, N = b.total, b.heads, b.n_seqs
-    f32 = dict(dtype=torch.float32, device=dev)
-    o = torch.empty_like(b.v)
-    hT = torch.empty((N, H, D, D), **f32)
-    fa = kda.fwd_args(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, o, hT, None, None)
-    saved = torch.empty(lib.kda_saved_size(C.byref(fa)), dtype=torch.uint8, device=dev)
-    fws = torch.empty(lib.kda_fwd_workspace_size(C.byref(fa)), dtype=torch.uint8, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)   # a kernel that gives up a bounded wait writes here
-    fa = kda.fwd_args(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0, o, hT, saved, fws, dev_status=status)
-    grads = {n: torch.empty(s, **f32) for n, s in
-             (("dq", b.q.shape), ("dk", b.k.shape), ("dv", b.v.shape), ("dg", b.g.shape), ("dbeta", b.beta.shape),
-              ("dh0", (N, H, D, D)))}
-    ba = kda.bwd_args(fa, b.dO, grads["dq"], grads["dk"], grads["dv"], grads["dbeta"], grads["dg"], grads["dh0"])
-    bws = torch.empty(lib.kda_bwd_workspace_size(C.byref(ba)), dtype=torch.uint8, device=dev)
-    ba = kda.bwd_args(fa, b.dO, grads["dq"], grads["dk"], grads["dv"], grads["dbeta"], grads["dg"], grads["dh0"],
-                      None, bws)
-
-    # per-kernel events: [start, fwd stages..., bwd stages...] per step
-    nst = 1 + len(FWD_STAGES) + len(BWD_STAGES)
-    K = args.steps
+    names = case.stages()
+    nst = 1 + len(names)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(K)]
     for row in evs:
         for e in row:
             e.record(stream)          # materialise the events so their handles exist
     torch.cuda.synchronize(dev)
     arrays = [((C.c_void_p * len(FWD_STAGES))(*[e.cuda_event for e in row[1:1 + len(FWD_STAGES)]]),
-               (C.c_void_p * len(BWD_STAGES))(*[e.cuda_event for e in row[1 + len(FWD_STAGES):]])) for row in evs]
-
-    def step(i=None):
-        if i is not None:
-            lib.kda_set_profile_events(C.cast(arrays[i][0], C.c_void_p), len(FWD_STAGES))
-        _lib.check(lib.kda_fwd(C.byref(fa), sptr))
-        if i is not None:
-            lib.kda_set_profile_events(C.cast(arrays[i][1], C.c_void_p), len(BWD_STAGES))
-        _lib.check(lib.kda_bwd(C.byref(ba), sptr))
-        if i is not None:
-            lib.kda_set_profile_events(None, 0)
-
-    for _ in range(args.warmup):
-        step()
+               (C.c_void_p * len(BWD_STAGES))(*[e.cuda_event for e in row[1 + len(FWD_STAGES):]]))
+              for row in evs]
+    for i in range(W):
+        case.step(lib, sptr, i)
     torch.cuda.synchronize(dev)
     barrier(world)
-    clocks = ClockSampler(local_rank) if rank == 0 else None
+    extra = on_start() if on_start else None
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     t_start.record(stream)
     for i in range(K):
         evs[i][0].record(stream)
-        step(i)
+        case.step(lib, sptr, W + i, arrays[i])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
-    ms_step_local = t_start.elapsed_time(t_end) / K
-    if int(status.item()) != 0:
-        raise SystemExit(f"device status {int(status.item())}: a kernel gave up a bounded wait; no number reported")
+    ms_local = t_start.elapsed_time(t_end) / K
     barrier(world)
-    ck = clocks.stop() if clocks else None
-    ms_step = reduce_max(ms_step_local, world)
-
-    # per-kernel device time (mean over steps)
-    names = ["start"] + FWD_STAGES + BWD_STAGES
-    per = {n: 0.0 for n in names[1:]}
+    per = {n: 0.0 for n in names}
     for row in evs:
         for j in range(1, nst):
-            per[names[j]] += row[j - 1].elapsed_time(row[j]) / K
+            per[names[j - 1]] += row[j - 1].elapsed_time(row[j]) / K
+    return reduce_max(ms_local, world), per, extra
+
+
+def summarize(case, per, peaks, ms=None):
+    """tokens/s, algorithmic GB/s and roofline fractions of one timed chunked workload."""
+    units = case.T * case.H
     fwd_ms = sum(per[n] for n in FWD_STAGES)
-    bwd_ms = sum(per[n] for n in BWD_STAGES)
+    out = {"fwd": {"ms": fwd_ms, "tokens_per_s": case.T / (fwd_ms * 1e-3),
+                   "gbs_algorithmic": FWD_BYTES * units / (fwd_ms * 1e-3) / 1e9,
+                   "roofline_frac": FWD_BYTES * units / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
+    if case.mode == "fwdbwd":
+        bwd_ms = sum(per[n] for n in BWD_STAGES)
+        out["bwd"] = {"ms": bwd_ms, "tokens_per_s": case.T / (bwd_ms * 1e-3),
+                      "gbs_algorithmic": BWD_BYTES * units / (bwd_ms * 1e-3) / 1e9,
+                      "roofline_frac": BWD_BYTES * units / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    if ms is not None:
+        byts = (FWD_BYTES + (BWD_BYTES if case.mode == "fwdbwd" else 0)) * units
+        out["step"] = {"ms": ms, "tokens_per_s": case.T / (ms * 1e-3), "gbs_algorithmic": byts / (ms * 1e-3) / 1e9,
+                       "roofline_frac": byts / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    out["kernels_ms"] = {k: round(v, 4) for k, v in per.items()}
+    return out
+
+
+def bench_range(args, lib, dev, stream, peaks, status):
+    """The pages' sequence-length range (4K-128K tokens) and the inference forward: the
+    T=4096 forward, the T=32768 forward without saved (inference), the 131,072 packed
+    varlen tokens (8 sequences) fwd+bwd and one 131,072-token sequence fwd+bwd. Every
+    line alternates two resident input sets per timed step."""
+    import torch
+    res = {}
+    for name, mode, key in (("fwd-bf16-T4096-H96", "fwd", "fwd_T4096"),
+                            ("fwdbwd-bf16-T32768-H96", "fwd", "fwd_T32768_inference"),
+                            ("fwdbwd-bf16-varlen8-T131072-H96", "fwdbwd", "fwdbwd_varlen8_T131072"),
+                            ("fwdbwd-bf16-T131072-H96", "fwdbwd", "fwdbwd_T131072")):
+        if args.seq_len and "131072" in name:
+            continue
+        case = ChunkedCase(lib, dev, name, mode, status, seq_len=args.seq_len if "T32768" in name else 0)
+        K = max(3, min(args.steps, 20 if case.T <= 32768 else 5))
+        ms, per, _ = time_case(case, lib, dev, stream, K, max(args.warmup, 3))
+        if int(status.item()) != 0:
+            raise SystemExit(f"device status {int(status.item())} in {name}: no number reported")
+        line = {"workload": name, "mode": "training fwd + bwd" if mode == "fwdbwd" else "inference forward (no saved)",
+                "tokens": case.T, "sequences": case.N, "steps": K, **summarize(case, per, peaks, ms)}
+        dom = max((k for k in per if k in KERNEL_BYTES), key=lambda n: per[n])
+        ach = KERNEL_BYTES[dom] * case.T * case.H / (per[dom] * 1e-3) / 1e9
+        line["roofline"] = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": ach / peaks["hbm_gbs"],
+                            "traffic": scaled_traffic(dom if mode == "fwdbwd" else dom + ".inference",
+                                                      case.T * case.H)}
+        res[key] = line
+        del case
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import gated_delta_rule_chunked_gb300 as kda
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = kda.library()
+    stream = torch.cuda.current_stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)   # a kernel that gives up a bounded wait writes here
+
+    case = ChunkedCase(lib, dev, WORKLOAD, "fwdbwd", status, seq_len=args.seq_len)
+    T, H, N = case.T, case.H, case.N
+    K = args.steps
+    clocks_box = []
+    ms_step, per, _ = time_case(case, lib, dev, stream, K, args.warmup, world,
+                                on_start=lambda: clocks_box.append(ClockSampler(local_rank) if rank == 0 else None))
+    ck = clocks_box[0].stop() if clocks_box and clocks_box[0] else None
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())}: a kernel gave up a bounded wait; no number reported")
 
     peaks = load_peaks()
     tok = T
     units = T * H
+    summ = summarize(case, per, peaks)
+    fwd_ms, bwd_ms = summ["fwd"]["ms"], summ["bwd"]["ms"]
     dom = max(KERNEL_BYTES, key=lambda n: per[n])
     dom_bytes = KERNEL_BYTES[dom] * units
     achieved = dom_bytes / (per[dom] * 1e-3) / 1e9
@@ -218,14 +317,11 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; q,k,v,dO ~ N(0,1) bf16, beta=sigmoid(N(0,1)), g=logsigmoid(N(3,1)), h0 ~ N(0,0.02))",
         "config": {"workload": WORKLOAD, "batch": N, "seq_len": T, "heads": H, "head_dim": D, "chunk": 64,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs (4.8 GB) larger than L2; no flush"},
-        "fwd": {"ms": fwd_ms, "tokens_per_s": tok / (fwd_ms * 1e-3),
-                "gbs_algorithmic": FWD_BYTES * units / (fwd_ms * 1e-3) / 1e9,
-                "roofline_frac": FWD_BYTES * units / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-        "bwd": {"ms": bwd_ms, "tokens_per_s": tok / (bwd_ms * 1e-3),
-                "gbs_algorithmic": BWD_BYTES * units / (bwd_ms * 1e-3) / 1e9,
-                "roofline_frac": BWD_BYTES * units / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-        "kernels_ms": {k: round(v, 4) for k, v in per.items()},
+                   "l2": "inputs (4.8 GB per set) larger than L2; no flush; the timed steps alternate between two "
+                         "resident input sets drawn with different seeds"},
+        "fwd": summ["fwd"],
+        "bwd": summ["bwd"],
+        "kernels_ms": summ["kernels_ms"],
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": dom_bytes, "peak_source": peaks["source"]},
@@ -240,14 +336,17 @@ def run_ours(args, rank, world, local_rank):
         out["config"]["workload"] += f" (T overridden to {T})"
     host = None
     if not args.no_e2e:
+        b = case.sets[0]
         host = {n: getattr(b, n).to("cpu").pin_memory() for n in ("q", "k", "v", "beta", "g", "h0", "dO")}
         host["cu_seqlens"] = b.cu_seqlens.to("cpu")
-    del b, grads, saved, fws, bws, o, hT
+    del case
     torch.cuda.empty_cache()
     if host is not None:   # first after the step, on an empty allocator cache
         out["e2e"] = bench_e2e(args, dev, world, host)
         del host
         torch.cuda.empty_cache()
+    if not args.no_range:
+        out["range"] = bench_range(args, lib, dev, stream, peaks, status)
     if not args.no_decode:
         out["decode"] = bench_decode(args, dev, lib, stream, peaks)
     if not args.no_cp:
@@ -649,6 +748,7 @@ def main():
     ap.add_argument("--no-attnres", action="store_true", help="skip the Attention Residuals workload")
     ap.add_argument("--no-conv", action="store_true", help="skip the short-convolution workload")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-range", action="store_true", help="skip the 4K / inference / 128K / varlen lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16384)
     ap.add_argument("--ref-sample-tokens", type=int, default=2048)

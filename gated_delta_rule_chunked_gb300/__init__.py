@@ -164,43 +164,32 @@ def kda_cp_combine(M, b, h0, n_segments: int):
     return s_in
 
 
-def cp_segments(cu_seqlens, n_segments: int, total: Optional[int] = None):
-    """Segment boundaries: every sequence cut into n_segments runs of whole 64-token chunks
-    (as equal as chunk alignment allows; trailing segments may be empty). Host-side."""
-    cu = cu_seqlens.to("cpu", torch.int64).tolist() if cu_seqlens is not None else [0, total]
-    seg = [0]
-    for s0, s1 in zip(cu[:-1], cu[1:]):
-        nch = (s1 - s0 + 63) // 64
-        for kk in range(1, n_segments + 1):
-            seg.append(min(s1, s0 + 64 * ((nch * kk) // n_segments)))
-    return torch.tensor(seg, dtype=torch.int32)
-
-
-def kda_fwd_cp(q, k, v, beta, g, cu_seqlens=None, h0=None, *, n_segments: int, scale: float = 1.0):
-    """Forward by context parallelism, emulated on one device: every sequence is cut into
-    n_segments consecutive segments that are processed independently (as separate
-    sequences), their affine maps combined, and the segments run again from the combined
-    incoming states. Returns (o, hT) of the unsplit forward.
-
-    Pass 1: M = final states from the identity with zero values (each segment's linear map);
-    pass 2: b = final states from zero; combine: the state entering each segment;
-    pass 3: the forward over each segment from its incoming state. The chunk records (they
-    depend on q, k, g and beta only) are computed once, in pass 1.
+def kda_fwd_cp(q, k, v, beta, g, cu_seqlens=None, h0=None, *, n_segments: int, scale: float = 1.0,
+               n_seqs: Optional[int] = None, dev_status=None):
+    """Forward by context parallelism, emulated on one device (libkda's kda_fwd_cp): every
+    sequence is cut into n_segments consecutive runs of whole chunks that are processed
+    independently (as separate sequences), their affine maps combined, and the segments run
+    again from the combined incoming states. Returns (o, hT) of the unsplit forward.
     """
+    lib = library()
     _check_inputs(q, k, v, beta, g)
     dev = q.device
-    total, H = q.shape[0], q.shape[1]
-    seg = cp_segments(cu_seqlens, n_segments, total)
-    N = (len(seg) - 1) // n_segments
-    S = N * n_segments
-    segd = _i32(seg, dev)
-    M, ws = _fwd_states(q, k, None, beta, g, segd, None, S, scale=scale, h0_identity=True)
-    b, _ = _fwd_states(q, k, v, beta, g, segd, None, S, scale=scale, ws=ws)       # same records
-    h0c = None if h0 is None else h0.contiguous()
-    s_in = kda_cp_combine(M.view(N, n_segments, H, 128, 128), b.view(N, n_segments, H, 128, 128), h0c, n_segments)
+    cu = _i32(cu_seqlens, dev)
+    N = (cu.numel() - 1) if cu is not None else (n_seqs or 1)
+    H = q.shape[1]
     o = torch.empty_like(v)
-    hT, _ = _fwd_states(q, k, v, beta, g, segd, s_in.view(S, H, 128, 128), S, scale=scale, out=o, ws=ws)
-    return o, hT.view(N, n_segments, H, 128, 128)[:, -1].contiguous()
+    hT = torch.empty((N, H, 128, 128), dtype=torch.float32, device=dev)
+    c = _lib.FwdCpArgs()
+    c.fwd = fwd_args(q, k, v, beta, g, cu, None if h0 is None else h0.contiguous(), o, hT, None, None, scale,
+                     n_seqs=N, dev_status=dev_status)
+    c.n_segments = n_segments
+    ws_bytes = lib.kda_fwd_cp_workspace_size(C.byref(c))
+    if ws_bytes == 0:
+        raise KdaError(_lib.KDA_ERR_INVALID_ARG, lib.kda_last_error().decode())
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    c.workspace, c.workspace_bytes = ws.data_ptr(), ws_bytes
+    _lib.check(lib.kda_fwd_cp(C.byref(c), _stream(dev)))
+    return o, hT
 
 
 def _attnres_args(sources, w, eps, out=None, stats=None):

@@ -14,11 +14,11 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT 
 KDA_BF16, KDA_F32 = 0, 1
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
                 4: "KDA_ERR_TIMEOUT"}
-ABI_VERSION = 4
+ABI_VERSION = 5
 
 # every symbol include/kda.h declares
 EXPORTS = ("kda_fwd", "kda_fwd_workspace_size", "kda_saved_size", "kda_bwd", "kda_bwd_workspace_size",
-           "kda_step", "kda_cp_combine", "kda_attnres_fwd", "kda_attnres_bwd", "kda_attnres_bwd_workspace_size",
+           "kda_step", "kda_cp_combine", "kda_fwd_cp", "kda_fwd_cp_workspace_size", "kda_attnres_fwd", "kda_attnres_bwd", "kda_attnres_bwd_workspace_size",
            "kda_conv_fwd", "kda_conv_bwd", "kda_conv_bwd_workspace_size", "kda_conv_step",
            "kda_fwd_no_alloc", "kda_set_profile_events", "kda_last_error", "kda_abi_version")
 ATTNRES_MAX_SOURCES = 9
@@ -36,7 +36,13 @@ class FwdArgs(C.Structure):
         ("h0", C.c_void_p), ("o", C.c_void_p), ("hT", C.c_void_p), ("saved", C.c_void_p),
         ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("dev_status", C.c_void_p),
         ("h0_identity", C.c_int32), ("skip_prep", C.c_int32),
+        ("wait_limit_ns", C.c_int64), ("debug_starve", C.c_int32),
     ]
+
+
+class FwdCpArgs(C.Structure):
+    _fields_ = [("fwd", FwdArgs), ("n_segments", C.c_int32), ("workspace", C.c_void_p),
+                ("workspace_bytes", C.c_size_t)]
 
 
 class CpArgs(C.Structure):
@@ -133,6 +139,10 @@ def load(path: str = LIB_PATH):
     lib.kda_step.restype = C.c_int
     lib.kda_cp_combine.argtypes = [C.POINTER(CpArgs), C.c_void_p]
     lib.kda_cp_combine.restype = C.c_int
+    lib.kda_fwd_cp.argtypes = [C.POINTER(FwdCpArgs), C.c_void_p]
+    lib.kda_fwd_cp.restype = C.c_int
+    lib.kda_fwd_cp_workspace_size.argtypes = [C.POINTER(FwdCpArgs)]
+    lib.kda_fwd_cp_workspace_size.restype = C.c_size_t
     lib.kda_attnres_fwd.argtypes = [C.POINTER(AttnresFwdArgs), C.c_void_p]
     lib.kda_attnres_fwd.restype = C.c_int
     lib.kda_attnres_bwd.argtypes = [C.POINTER(AttnresBwdArgs), C.c_void_p]

@@ -179,6 +179,9 @@ kda_status check_fwd(const kda_fwd_args *a, const char *who) {
     if (!aligned(opt[i], 16)) return fail(KDA_ERR_INVALID_ARG, "%s: pointer is not 16-byte aligned", onames[i]);
   if (a->dev_status && !aligned(a->dev_status, 4))
     return fail(KDA_ERR_INVALID_ARG, "%s: dev_status is not 4-byte aligned", who);
+  if (a->wait_limit_ns < 0) return fail(KDA_ERR_INVALID_ARG, "%s: wait_limit_ns must be >= 0", who);
+  if (a->debug_starve && a->io_dtype != KDA_BF16)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: debug_starve needs io_dtype KDA_BF16", who);
   return KDA_OK;
 }
 
@@ -212,7 +215,7 @@ void kda::set_last_error(const char *msg) { g_last_error = msg ? msg : ""; }
 
 extern "C" {
 
-int32_t kda_abi_version(void) { return 4; }
+int32_t kda_abi_version(void) { return 5; }
 
 namespace {
 kda_status check_attnres(const kda_attnres_fwd_args *a, const char *who) {
@@ -556,7 +559,9 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
   pp.tm_g = tm_g;
   if (!a->skip_prep && (e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
-  kda::FwdScanParams sp{geo, a->v, rec, a->h0, a->o, a->hT, a->saved, a->dev_status, a->h0_identity != 0, {}};
+  kda::FwdScanParams sp{geo, a->v, rec, a->h0, a->o, a->hT, a->saved, a->dev_status, a->h0_identity != 0, {},
+                        a->wait_limit_ns > 0 ? (unsigned long long)a->wait_limit_ns : 2000000000ull,
+                        a->debug_starve != 0};
   if (!f32 && a->v && !map_tokens(&sp.tm_v, a->v, false, a->total_tokens, a->heads, 64, true))
     return fail(KDA_ERR_CUDA, "%s: could not encode the TMA tensor maps", "kda_fwd");
   e = f32 ? kda::launch_fwd_scan(sp, true, pick_slice(a), stream) : kda::launch_fwd_scan_tc(sp, stream);
@@ -640,6 +645,114 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
   cp.status = f->dev_status;
   if ((e = kda::launch_bwd_chunk_tc(cp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd chunk grads");
   mark(2, stream);
+  g_last_error.clear();
+  return KDA_OK;
+}
+
+namespace {
+// Workspace of kda_fwd_cp: the segment table, the workspace of the segmented forward
+// (N * P sequences), and three [N * P][H][128][128] fp32 state arrays (M, b, S_in; the
+// last pass writes the segments' final states over M).
+struct CpPlan {
+  size_t seg, fws, M, b, s_in, bytes, fws_bytes;
+};
+
+CpPlan cp_plan(const kda_fwd_cp_args *c) {
+  CpPlan w{};
+  kda_fwd_args f = c->fwd;
+  f.n_seqs = c->fwd.n_seqs * c->n_segments;
+  const size_t nseg = (size_t)f.n_seqs;
+  w.seg = 0;
+  w.fws = round_up((nseg + 1) * 4, 256);
+  w.fws_bytes = plan(&f, false).bytes;
+  const size_t st = nseg * (size_t)c->fwd.heads * 128 * 128 * sizeof(float);
+  w.M = round_up(w.fws + w.fws_bytes, 256);
+  w.b = w.M + st;
+  w.s_in = w.b + st;
+  w.bytes = w.s_in + st;
+  return w;
+}
+
+kda_status check_cp(const kda_fwd_cp_args *c, const char *who) {
+  if (!c) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", who);
+  kda_fwd_args f = c->fwd;   // fwd.workspace is ignored (this call takes its own)
+  f.workspace = nullptr;
+  f.workspace_bytes = 0;
+  kda_status st = check_fwd(&f, who);
+  if (st != KDA_OK) return st;
+  if (c->fwd.io_dtype != KDA_BF16 || c->fwd.saved || c->fwd.h0_identity || c->fwd.skip_prep || c->fwd.debug_starve)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: needs io_dtype KDA_BF16, no saved, h0_identity = skip_prep = debug_starve = 0",
+                who);
+  if (c->n_segments < 1 || (long long)c->n_segments * c->fwd.n_seqs > 0x7fffffffLL / 64)
+    return fail(KDA_ERR_INVALID_ARG, "%s: need n_segments >= 1 (and n_seqs * n_segments < 2^25)", who);
+  if (c->fwd.total_tokens > 0 && (!c->fwd.v || !c->fwd.o))
+    return fail(KDA_ERR_INVALID_ARG, "%s: v and o are required", who);
+  return KDA_OK;
+}
+}  // namespace
+
+size_t kda_fwd_cp_workspace_size(const kda_fwd_cp_args *c) {
+  if (check_cp(c, "kda_fwd_cp_workspace_size") != KDA_OK) return 0;
+  return cp_plan(c).bytes;
+}
+
+kda_status kda_fwd_cp(const kda_fwd_cp_args *c, cudaStream_t stream) {
+  kda_status st = check_cp(c, "kda_fwd_cp");
+  if (st != KDA_OK) return st;
+  const CpPlan w = cp_plan(c);
+  if (!c->workspace || c->workspace_bytes < w.bytes || !aligned(c->workspace, 16))
+    return fail(KDA_ERR_INVALID_ARG, "%s: workspace missing, misaligned or smaller than kda_fwd_cp_workspace_size()",
+                "kda_fwd_cp");
+  const kda_fwd_args &f = c->fwd;
+  const int N = f.n_seqs, P = c->n_segments, H = f.heads;
+  if (f.total_tokens == 0) {   // every segment empty: hT = h0
+    if (f.hT) {
+      const size_t n = (size_t)N * H * 128 * 128 * 4;
+      cudaError_t e = f.h0 ? cudaMemcpyAsync(f.hT, f.h0, n, cudaMemcpyDeviceToDevice, stream)
+                           : cudaMemsetAsync(f.hT, 0, n, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "kda_fwd_cp");
+    }
+    g_last_error.clear();
+    return KDA_OK;
+  }
+  char *ws = static_cast<char *>(c->workspace);
+  int *seg = reinterpret_cast<int *>(ws + w.seg);
+  float *M = reinterpret_cast<float *>(ws + w.M), *b = reinterpret_cast<float *>(ws + w.b);
+  float *s_in = reinterpret_cast<float *>(ws + w.s_in);
+  cudaError_t e = kda::launch_cp_segments(f.cu_seqlens, N, f.total_tokens, P, seg, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_fwd_cp segments");
+  // the segmented problem: N * P sequences with the segment table as offsets
+  kda_fwd_args s = f;
+  s.n_seqs = N * P;
+  s.cu_seqlens = seg;
+  s.workspace = ws + w.fws;
+  s.workspace_bytes = w.fws_bytes;
+  // pass 1: chunk records and the segment maps M (identity start, zero values, no outputs)
+  kda_fwd_args p1 = s;
+  p1.v = nullptr;
+  p1.o = nullptr;
+  p1.h0 = nullptr;
+  p1.hT = M;
+  p1.h0_identity = 1;
+  if ((st = kda_fwd(&p1, stream)) != KDA_OK) return st;
+  // pass 2: the segment offsets b (zero start, same records)
+  kda_fwd_args p2 = s;
+  p2.o = nullptr;
+  p2.h0 = nullptr;
+  p2.hT = b;
+  p2.skip_prep = 1;
+  if ((st = kda_fwd(&p2, stream)) != KDA_OK) return st;
+  // combine: the state entering each segment
+  if ((e = kda::launch_cp_combine(N, P, H, M, b, f.h0, s_in, stream)) != cudaSuccess)
+    return cuda_fail(e, "kda_fwd_cp combine");
+  // pass 3: every segment from its entering state; its final states land over M
+  kda_fwd_args p3 = s;
+  p3.h0 = s_in;
+  p3.hT = M;
+  p3.skip_prep = 1;
+  if ((st = kda_fwd(&p3, stream)) != KDA_OK) return st;
+  if (f.hT && (e = kda::launch_cp_last(M, N, P, H, f.hT, stream)) != cudaSuccess)
+    return cuda_fail(e, "kda_fwd_cp final states");
   g_last_error.clear();
   return KDA_OK;
 }

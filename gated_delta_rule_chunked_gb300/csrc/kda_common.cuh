@@ -254,11 +254,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 // Wait for phase `parity` of `bar`, giving up after ~2 s. Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // default limit of every bounded wait (about 2 s)
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > 2000000000ull) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }

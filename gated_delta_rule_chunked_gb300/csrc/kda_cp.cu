@@ -79,4 +79,33 @@ cudaError_t launch_cp_combine(int n_seqs, int n_segments, int heads, const float
   return cudaGetLastError();
 }
 
+// Segment table: segment k of sequence i (k = 0..P-1) starts at s0 + 64 floor(nch k / P),
+// capped at the sequence end s1 (nch = the sequence's chunk count); seg[N P] = the end.
+__global__ void kda_cp_segments_kernel(const int *cu, int n_seqs, long long total, int P, int *seg) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long n = (long long)n_seqs * P;
+  if (idx == 0) seg[n] = cu ? cu[n_seqs] : (int)total;
+  if (idx >= n) return;
+  const int i = (int)(idx / P), k = (int)(idx % P);
+  const long long per = total / n_seqs;
+  const long long s0 = cu ? cu[i] : per * i, s1 = cu ? cu[i + 1] : per * (i + 1);
+  const long long nch = (s1 - s0 + CH - 1) / CH;
+  const long long start = s0 + (long long)CH * ((nch * k) / P);
+  seg[idx] = (int)(start < s1 ? start : s1);
+}
+
+cudaError_t launch_cp_segments(const int *cu, int n_seqs, long long total, int P, int *seg, cudaStream_t s) {
+  const long long n = (long long)n_seqs * P;
+  const unsigned blocks = (unsigned)((n + 255) / 256);
+  kda_cp_segments_kernel<<<blocks ? blocks : 1, 256, 0, s>>>(cu, n_seqs, total, P, seg);
+  return cudaGetLastError();
+}
+
+// Final state of each sequence = the final state of its last segment.
+cudaError_t launch_cp_last(const float *hseg, int n_seqs, int P, int heads, float *hT, cudaStream_t s) {
+  const size_t blk = (size_t)heads * D * D * sizeof(float);
+  return cudaMemcpy2DAsync(hT, blk, hseg + (size_t)(P - 1) * heads * D * D, (size_t)P * blk, blk, (size_t)n_seqs,
+                           cudaMemcpyDeviceToDevice, s);
+}
+
 }  // namespace kda

@@ -84,6 +84,8 @@ struct FwdScanParams {
   int *status;
   int h0_identity;         // start every sequence from the identity state (h0 ignored)
   CUtensorMap tm_v;        // bf16 scan: v as boxes of 64 channels x 1 head x 64 tokens, 128-byte swizzle
+  unsigned long long wait_ns;   // limit of every bounded wait of the tcgen05 scan
+  int starve;              // testing aid: CTA 0 issues none of its first copies (its waits run out)
 };
 
 struct BwdScanParams {
@@ -183,6 +185,10 @@ cudaError_t launch_bwd_chunk_tc(const BwdChunkParams &p, cudaStream_t s);
 cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_cp_combine(int n_seqs, int n_segments, int heads, const float *M, const float *b, const float *h0,
                               float *s_in, cudaStream_t s);
+// Segment offsets [N * P + 1] of P chunk-aligned segments per sequence (cu NULL: N equal sequences)
+cudaError_t launch_cp_segments(const int *cu, int n_seqs, long long total, int P, int *seg, cudaStream_t s);
+// hT[n] = hseg[n * P + P - 1] for the N sequences ([N][H][128][128] fp32 each)
+cudaError_t launch_cp_last(const float *hseg, int n_seqs, int P, int heads, float *hT, cudaStream_t s);
 
 // Sets the message that kda_last_error() returns on this host thread.
 void set_last_error(const char *msg);

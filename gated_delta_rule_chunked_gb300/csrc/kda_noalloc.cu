@@ -17,7 +17,13 @@
 //  * every call uses the same array, so calls whose work overlaps on the GPU
 //    (other streams, other host threads) race; the array keeps the previous
 //    call's contents -- the forward writes every scratch byte it reads before
-//    reading it, so nothing needs clearing.
+//    reading it, so nothing needs clearing. That is why skip_prep (which reads
+//    chunk records left in the scratch by an earlier call) is rejected here:
+//    the earlier call may have been another caller's problem;
+//  * the cached address belongs to the device's current context: after
+//    cudaDeviceReset (or a release and re-creation of the primary context) the
+//    array is loaded again elsewhere, so the entry point must not be used
+//    across a reset.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -55,8 +61,17 @@ cudaError_t scratch_ptr(void **out) {
 
 extern "C" kda_status kda_fwd_no_alloc(const kda_fwd_args *args, cudaStream_t stream) {
   if (!args) return kda_fwd(args, stream);   // reports the NULL-args error
-  const size_t need = kda_fwd_workspace_size(args);
-  if (need == 0) return kda_fwd(args, stream);   // invalid arguments: kda_fwd reports which
+  if (args->skip_prep) {
+    kda::set_last_error(
+        "kda_fwd_no_alloc: skip_prep is not supported (the shared static scratch may hold another call's chunk records)");
+    return KDA_ERR_UNSUPPORTED;
+  }
+  // the caller's workspace fields are ignored: size and run a copy without them
+  kda_fwd_args a = *args;
+  a.workspace = nullptr;
+  a.workspace_bytes = 0;
+  const size_t need = kda_fwd_workspace_size(&a);
+  if (need == 0) return kda_fwd(&a, stream);   // invalid arguments: kda_fwd reports which
   if (need > (size_t)KDA_NO_ALLOC_SCRATCH_BYTES) {
     char msg[256];
     std::snprintf(msg, sizeof msg,
@@ -74,7 +89,6 @@ extern "C" kda_status kda_fwd_no_alloc(const kda_fwd_args *args, cudaStream_t st
     kda::set_last_error(msg);
     return KDA_ERR_CUDA;
   }
-  kda_fwd_args a = *args;
   a.workspace = ptr;
   a.workspace_bytes = KDA_NO_ALLOC_SCRATCH_BYTES;
   return kda_fwd(&a, stream);

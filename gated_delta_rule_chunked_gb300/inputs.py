@@ -46,7 +46,8 @@ class Workload:
     seed: int = 0
 
 
-# The five workloads of the KDA hot path. Seeds are 1000 + the workload index.
+# The five workloads of the KDA hot path, and a 128K-token point for the benchmark.
+# Seeds are 1000 + the workload index.
 WORKLOADS = {
     "fwd-f32-T512-H2": Workload("fwd-f32-T512-H2", "fwd", "f32", 2, seq_lens=(512,), seed=1000),
     "fwd-bf16-T4096-H96": Workload("fwd-bf16-T4096-H96", "fwd", "bf16", 96, seq_lens=(4096,), seed=1001),
@@ -57,6 +58,9 @@ WORKLOADS = {
                                                 h0=True, seed=1003),
     "decode-bf16-N256-L4-H96": Workload("decode-bf16-N256-L4-H96", "decode", "bf16", 96,
                                         n_seqs=256, steps=4, h0=True, seed=1004),
+    # the long end of the pages' 4K-128K sequence range, one sequence (benchmark only)
+    "fwdbwd-bf16-T131072-H96": Workload("fwdbwd-bf16-T131072-H96", "fwdbwd", "bf16", 96,
+                                        seq_lens=(131072,), h0=True, seed=1005),
 }
 
 

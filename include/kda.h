@@ -99,6 +99,15 @@ typedef struct {
                                   previous bf16 kda_fwd (without saved) on the same q, k, g,
                                   beta and sequence layout; only the scan runs (the records
                                   do not depend on v, h0 or the initial state)            */
+    /* ABI version 5: testing aids for the bounded waits of the bf16 state scan (leave 0) */
+    int64_t wait_limit_ns;     /* limit of every bounded wait in the bf16 state scan, in ns;
+                                  0 = the default of about 2 s                            */
+    int32_t debug_starve;      /* nonzero (bf16 only): the scan's first CTA (sequence 0,
+                                  head 0) issues none of its first copies, so its waits
+                                  run out after wait_limit_ns; it writes KDA_ERR_TIMEOUT to
+                                  *dev_status, leaves that head's o and hT unwritten and
+                                  exits with nothing in flight. Nothing faults or hangs;
+                                  the context stays usable                                */
 } kda_fwd_args;
 
 /* Backward of kda_fwd: gradients of <dO, o> + <dhT, hT>. */
@@ -205,6 +214,36 @@ typedef struct {
 } kda_cp_args;
 
 kda_status kda_cp_combine(const kda_cp_args *args, cudaStream_t stream);
+
+/*
+ * kda_fwd_cp -- the whole context-parallel forward on one device: each sequence of
+ * args->fwd is cut into n_segments consecutive runs of whole 64-token chunks (as
+ * equal as chunk alignment allows; trailing segments of a short sequence may be
+ * empty), and the segments are processed as independent sequences the way P devices
+ * would process their own segment ("Kimi K3 on Fireworks", training section, CP
+ * bullet: contiguous token ranges kept for KDA's recurrent state propagation):
+ *   1. the chunk records of every segment (they depend on q, k, g, beta only);
+ *   2. each segment's map M: final state from the identity with zero values;
+ *   3. each segment's offset b: final state from zero;
+ *   4. kda_cp_combine: the state entering each segment;
+ *   5. a forward over every segment from its entering state, writing o, and the
+ *      final state of each sequence's last segment to hT.
+ * The result equals kda_fwd on args->fwd up to rounding. Everything is enqueued on
+ * `stream`; nothing is copied to the host. Supported: io_dtype KDA_BF16, saved = NULL,
+ * h0_identity = skip_prep = 0 (the other kda_fwd_args fields as for kda_fwd; fwd.
+ * workspace is ignored: this call takes its own).
+ */
+typedef struct {
+    kda_fwd_args fwd;          /* the unsplit forward (o required, hT optional)           */
+    int32_t n_segments;        /* P >= 1                                                  */
+    void *workspace;           /* kda_fwd_cp_workspace_size() bytes: segment table,
+                                  records, and the M, b and entering states of the
+                                  N * P segments (3 x 64 KiB per segment and head)         */
+    size_t workspace_bytes;
+} kda_fwd_cp_args;
+
+kda_status kda_fwd_cp(const kda_fwd_cp_args *args, cudaStream_t stream);
+size_t kda_fwd_cp_workspace_size(const kda_fwd_cp_args *args);
 
 /*
  * Attention Residuals ("Kimi K3 on Fireworks", training section, Attention Residuals
@@ -341,8 +380,19 @@ kda_status kda_conv_step(const kda_conv_step_args *args, cudaStream_t stream);
  *  - All calls share the one array: calls whose work overlaps on the GPU (other
  *    streams or host threads) race. The array keeps the last call's contents;
  *    the forward writes every scratch byte before reading it, so nothing needs
- *    clearing between calls.
- * Outputs (o, hT, saved) are identical to kda_fwd's on the same inputs.
+ *    clearing between calls. For the same reason args->skip_prep, which would
+ *    read chunk records an earlier call left in the scratch, is rejected with
+ *    KDA_ERR_UNSUPPORTED.
+ *  - The cached address is valid for the device's current context only: do not
+ *    use this entry point across cudaDeviceReset (or a release and re-creation
+ *    of the primary context).
+ *  - The scratch holds the chunk table and the chunk records: per (chunk, head)
+ *    66,048 bytes for bf16 I/O and 131,584 bytes for fp32 I/O, counted over
+ *    (total_tokens / 64 + n_seqs) chunks. So (total_tokens / 64 + n_seqs) x heads
+ *    may be at most about 4,060 (bf16) or 2,040 (fp32): at 96 heads one sequence
+ *    of up to about 2,600 (bf16) or 1,280 (fp32) tokens. kda_fwd_workspace_size()
+ *    gives the exact figure.
+ * Outputs (o, hT, saved) are bit-identical to kda_fwd's on the same inputs.
  */
 #define KDA_NO_ALLOC_SCRATCH_BYTES (256u * 1024u * 1024u)
 kda_status kda_fwd_no_alloc(const kda_fwd_args *args, cudaStream_t stream);
@@ -350,8 +400,8 @@ kda_status kda_fwd_no_alloc(const kda_fwd_args *args, cudaStream_t stream);
 /* Per-kernel timing hook for benchmarks. When `events` is not NULL, every later
  * kda_fwd / kda_bwd / kda_step call records events[i] on its stream right after
  * enqueueing its i-th kernel (i < n_events): kda_fwd has 3 kernels (chunk table,
- * chunk prep, state scan), kda_bwd 5 (chunk table, chunk prep, reverse dS scan,
- * state-side gradients, intra-chunk gradients), kda_step 1. Elapsed times
+ * chunk prep, state scan), kda_bwd 3 (chunk table, reverse dS scan, chunk-local
+ * gradients), kda_step 1. Elapsed times
  * between consecutive events (and one the caller records before the call) give
  * each kernel's device time. The caller owns the events and the array, which
  * must stay valid until the hook is cleared with kda_set_profile_events(NULL, 0).

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.kda_abi_version() == 4
+    assert lib.kda_abi_version() == 5
 
 
 def test_struct_layout_matches_c(tmp_path):
@@ -50,6 +50,7 @@ def test_struct_layout_matches_c(tmp_path):
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kda.h"', "int main(void){"]
     for sname, cls in (("kda_fwd_args", _lib.FwdArgs), ("kda_bwd_args", _lib.BwdArgs),
                        ("kda_step_args", _lib.StepArgs), ("kda_cp_args", _lib.CpArgs),
+                       ("kda_fwd_cp_args", _lib.FwdCpArgs),
                        ("kda_attnres_fwd_args", _lib.AttnresFwdArgs), ("kda_attnres_bwd_args", _lib.AttnresBwdArgs),
                        ("kda_conv_args", _lib.ConvArgs), ("kda_conv_bwd_args", _lib.ConvBwdArgs),
                        ("kda_conv_step_args", _lib.ConvStepArgs)):
@@ -64,6 +65,7 @@ def test_struct_layout_matches_c(tmp_path):
     got = dict(line.split() for line in subprocess.check_output([str(exe)], text=True).splitlines())
     for sname, cls in (("kda_fwd_args", _lib.FwdArgs), ("kda_bwd_args", _lib.BwdArgs),
                        ("kda_step_args", _lib.StepArgs), ("kda_cp_args", _lib.CpArgs),
+                       ("kda_fwd_cp_args", _lib.FwdCpArgs),
                        ("kda_attnres_fwd_args", _lib.AttnresFwdArgs), ("kda_attnres_bwd_args", _lib.AttnresBwdArgs),
                        ("kda_conv_args", _lib.ConvArgs), ("kda_conv_bwd_args", _lib.ConvBwdArgs),
                        ("kda_conv_step_args", _lib.ConvStepArgs)):
@@ -185,3 +187,36 @@ def test_binding_fails_loudly_without_library(tmp_path):
             _lib.load(str(tmp_path / "missing.so"))
     finally:
         _lib._lib = saved
+
+
+def test_fwd_wait_fields_validation(lib):
+    from gated_delta_rule_chunked_gb300 import _lib
+    assert lib.kda_fwd(C.byref(_fwd_args(wait_limit_ns=-1)), None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_fwd(C.byref(_fwd_args(debug_starve=1, io_dtype=_lib.KDA_F32)), None) == _lib.KDA_ERR_UNSUPPORTED
+
+
+def _cp_args(n_segments=4, **over):
+    from gated_delta_rule_chunked_gb300 import _lib
+    c = _lib.FwdCpArgs()
+    c.fwd = _fwd_args(**over)
+    c.n_segments = n_segments
+    return c
+
+
+def test_fwd_cp_validation_and_workspace(lib):
+    from gated_delta_rule_chunked_gb300 import _lib
+    c = _cp_args()
+    need = lib.kda_fwd_cp_workspace_size(C.byref(c))
+    # three [N P][H][128][128] fp32 state arrays at least (N = 1, P = 4, H = 2)
+    assert need >= 3 * 4 * 2 * 128 * 128 * 4
+    assert lib.kda_fwd_cp_workspace_size(C.byref(_cp_args(n_segments=8))) > need
+    assert lib.kda_fwd_cp(C.byref(c), None) == _lib.KDA_ERR_INVALID_ARG          # no workspace
+    c.workspace, c.workspace_bytes = 1 << 40, need - 256
+    assert lib.kda_fwd_cp(C.byref(c), None) == _lib.KDA_ERR_INVALID_ARG          # too small
+    assert lib.kda_fwd_cp(C.byref(_cp_args(n_segments=0)), None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_fwd_cp(C.byref(_cp_args(io_dtype=_lib.KDA_F32)), None) == _lib.KDA_ERR_UNSUPPORTED
+    assert lib.kda_fwd_cp(C.byref(_cp_args(saved=1 << 40)), None) == _lib.KDA_ERR_UNSUPPORTED
+    assert lib.kda_fwd_cp(C.byref(_cp_args(h0_identity=1)), None) == _lib.KDA_ERR_UNSUPPORTED
+    assert lib.kda_fwd_cp(C.byref(_cp_args(v=None)), None) == _lib.KDA_ERR_INVALID_ARG   # v required
+    # the caller's fwd.workspace is ignored: a misaligned one does not fail the size query
+    assert lib.kda_fwd_cp_workspace_size(C.byref(_cp_args(workspace=3))) == need

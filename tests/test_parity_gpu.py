@@ -438,6 +438,20 @@ def test_fwd_cp_matches_unsplit(kda, lens, P):
     assert e_o <= TOL["bf16"] and e_h <= TOL["bf16"], (e_o, e_h)
 
 
+def test_fwd_cp_equal_sequences_without_offsets_and_no_h0(kda):
+    # cu_seqlens = NULL (two equal sequences), zero initial state, 5 segments of a 640-token
+    # sequence (10 chunks: segments of 2 chunks each); bit-identical to a second call
+    b = make_seq_batch([640, 640], heads=2, io_dtype="bf16", seed=75)
+    t = to_dev(b)
+    o, hT = kda.kda_fwd_cp(t["q"], t["k"], t["v"], t["beta"], t["g"], None, None, n_segments=5, n_seqs=2)
+    o2, hT2 = kda.kda_fwd_cp(t["q"], t["k"], t["v"], t["beta"], t["g"], None, None, n_segments=5, n_seqs=2)
+    res = oracle.fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, None)
+    o_ref, h_ref = oracle.assemble_fwd(res, b.cu_seqlens, 2, 128)
+    e_o, e_h = rel(o.float().cpu(), o_ref), rel(hT.cpu(), h_ref)
+    assert e_o <= TOL["bf16"] and e_h <= TOL["bf16"], (e_o, e_h)
+    assert torch.equal(o, o2) and torch.equal(hT, hT2)
+
+
 def test_fwd_cp_gates_at_bound(kda):
     # the segment maps M of strongly decaying segments are tiny (entries underflow): the
     # chained states must still match the unsplit forward
@@ -461,8 +475,10 @@ def _sampled(b, heads):
 
 
 @pytest.mark.parametrize("name,tasks", [
-    ("fwdbwd-bf16-T32768-H96", [(0, 0), (0, 95)]),
-    ("fwdbwd-bf16-varlen8-T131072-H96", [(0, 1), (7, 94)]),
+    # six heads spread over the 96 (first, last and middle ones: different CTAs of every kernel)
+    ("fwdbwd-bf16-T32768-H96", [(0, 0), (0, 19), (0, 38), (0, 57), (0, 76), (0, 95)]),
+    # one head in each of the eight packed sequences, first to last head
+    ("fwdbwd-bf16-varlen8-T131072-H96", [(0, 1), (1, 13), (2, 27), (3, 40), (4, 55), (5, 68), (6, 81), (7, 94)]),
 ])
 def test_fullsize_fwd_bwd_sampled(kda, name, tasks):
     dev = torch.device("cuda")
@@ -488,6 +504,8 @@ def test_fullsize_fwd_bwd_sampled(kda, name, tasks):
             errs[f"{n}[{i},{h}]"] = rel(g_, r_)
     bad = {k: v for k, v in errs.items() if not v <= TOL["bf16"]}
     print(name, {k: f"{v:.2e}" for k, v in errs.items()})
+    worst = max(errs, key=errs.get)
+    print(f"{name}: largest error {worst} = {errs[worst]:.2e} (tolerance {TOL['bf16']:.0e})")
     assert not bad, errs
 
 

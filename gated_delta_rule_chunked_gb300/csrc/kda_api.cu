@@ -557,7 +557,8 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
   pp.tm_q = tm_q;
   pp.tm_k = tm_k;
   pp.tm_g = tm_g;
-  if (!a->skip_prep && (e = kda::launch_prep(pp, f32, stream)) != cudaSuccess) return cuda_fail(e, "kda_fwd prep");
+  if (!a->skip_prep && (e = f32 ? kda::launch_prep(pp, true, stream) : kda::launch_prep_tc(pp, stream)) != cudaSuccess)
+    return cuda_fail(e, "kda_fwd prep");
   mark(1, stream);
   kda::FwdScanParams sp{geo, a->v, rec, a->h0, a->o, a->hT, a->saved, a->dev_status, a->h0_identity != 0, {},
                         a->wait_limit_ns > 0 ? (unsigned long long)a->wait_limit_ns : 2000000000ull,

@@ -153,7 +153,8 @@ int attnres_bwd_ctas(long long T, bool f32, int dim, int S);
 
 cudaError_t launch_chunk_table(const int *cu_in, int n_seqs, long long total, int *cu_out,
                                int *chunk_off, cudaStream_t s);
-cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s);      // fp32 I/O (exact fp32 products)
+cudaError_t launch_prep_tc(const PrepParams &p, cudaStream_t s);            // bf16 I/O (tcgen05)
 cudaError_t launch_fwd_scan(const FwdScanParams &p, bool f32, int dv_slice, cudaStream_t s);
 cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s);
 cudaError_t launch_bwd_scan_tc(const BwdScanParams &p, cudaStream_t s);

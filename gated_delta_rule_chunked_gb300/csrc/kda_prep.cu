@@ -1,4 +1,5 @@
-// kda_prep.cu -- chunk table and the chunk-parallel intra-chunk kernel.
+// kda_prep.cu -- chunk table and the chunk-parallel intra-chunk kernel of the fp32-I/O forward
+// (the bf16 forward's intra-chunk kernel runs on tcgen05: kda_prep_tc.cu).
 //
 // For every (64-token chunk, head), independently of all other chunks:
 //   1. Q/K L2 normalisation (the benchmark caption of the first page counts
@@ -6,10 +7,10 @@
 //   2. the gate scan G_r = sum_{i<=r} g_i per key channel, restarted per chunk
 //      (kept in log2 units);
 //   3. the gated Gram blocks A_rj = sum_c k^_rc k^_jc exp(G_rc-G_jc) (j<r) and
-//      B_rj = sum_c q^_rc k^_jc exp(G_rc-G_jc) (j<=r) on TF32 tensor cores
-//      (these dot products cancel heavily, so bf16 operands are not enough);
+//      B_rj = sum_c q^_rc k^_jc exp(G_rc-G_jc) (j<=r) in exact fp32 products (the fp32
+//      I/O tolerance leaves no room for TF32 operands);
 //   4. the WY/UT transform T = (I + Diag(beta) A)^-1 (16x16 diagonal blocks by
-//      forward substitution, off-diagonal blocks by TF32 block products);
+//      forward substitution, off-diagonal blocks by fp32 block products);
 //   5. the operands the sequential state scan needs, written as one record.
 //
 // Gating factorisation. exp(G_r - G_j) is split into two bounded factors so the
@@ -84,11 +85,10 @@ struct PrepSmem2 {
   static constexpr int KL = 0, QL = TILE, R = 2 * TILE;     // fp32 [64][LDF] each
   static constexpr int DV = 3 * TILE;                        // fp32 [10][128] pair factors
   static constexpr int TOT = DV + 10 * 512;                  // fp32 [4][128] sub-block gate sums
-  static constexpr int PV = TOT + 4 * 512;                   // fp32 [4][128] exp(E_{a-1})
-  static constexpr int RQ = PV + 4 * 512, RK = RQ + 256, BETA = RK + 256;
+  static constexpr int RQ = TOT + 4 * 512, RK = RQ + 256, BETA = RK + 256;
   static constexpr int BAR = BETA + 256;                     // mbarrier of the staging copies
   static constexpr int BYTES = BAR + 16;
-  // after the Gram products QL and R are dead; KL lives on (it becomes Kt)
+  // after the Gram products QL and R are dead
   static constexpr int LM = QL;                              // fp32 [64][LDS64]  Diag(beta) A
   static constexpr int TT = LM + 64 * LDS64 * 4;             // fp32 [64][LDS64]  T, then T Diag(beta)
   static constexpr int SCR = TT + 64 * LDS64 * 4;            // fp32 4 x [16][LDP]
@@ -96,8 +96,6 @@ struct PrepSmem2 {
 };
 
 __device__ __forceinline__ void zero4(float (&a)[4]) { a[0] = a[1] = a[2] = a[3] = 0.f; }
-// x rounded to TF32 (nearest, ties away), kept as an fp32 value
-__device__ __forceinline__ float rtf32(float x) { return __uint_as_float(tf32(x)); }
 
 __device__ __forceinline__ void pair_of(int p, int &a, int &b) {
   a = p >= 6 ? 3 : (p >= 3 ? 2 : (p >= 1 ? 1 : 0));
@@ -115,96 +113,48 @@ __device__ __forceinline__ void pair_of(int p, int &a, int &b) {
 struct GramUnit {
   const float *kl, *ql, *rr, *d;   // KL, QL rows of the row block; R rows of the n-tile; pair factors
 };
-template <bool PRECISE, int NU>
+template <int NU>
 __device__ __forceinline__ void gram_units(float (&ak)[3][4], float (&aq)[3][4], const GramUnit (&u)[3]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-  if constexpr (PRECISE) {
 #pragma unroll
-    for (int v = 0; v < NU; ++v)
-      for (int c = 0; c < 128; ++c) {
-        const float d = u[v].d[c];
-        const float k0 = u[v].kl[g * LDF + c], k1 = u[v].kl[(g + 8) * LDF + c];
-        const float q0 = u[v].ql[g * LDF + c], q1 = u[v].ql[(g + 8) * LDF + c];
-        const float r0 = u[v].rr[(2 * q) * LDF + c] * d, r1 = u[v].rr[(2 * q + 1) * LDF + c] * d;
-        ak[v][0] = fmaf(k0, r0, ak[v][0]);
-        ak[v][1] = fmaf(k0, r1, ak[v][1]);
-        ak[v][2] = fmaf(k1, r0, ak[v][2]);
-        ak[v][3] = fmaf(k1, r1, ak[v][3]);
-        aq[v][0] = fmaf(q0, r0, aq[v][0]);
-        aq[v][1] = fmaf(q0, r1, aq[v][1]);
-        aq[v][2] = fmaf(q1, r0, aq[v][2]);
-        aq[v][3] = fmaf(q1, r1, aq[v][3]);
-      }
-  } else {
-#pragma unroll 2
-    for (int kk = 0; kk < 128; kk += 8) {
-      const int c = kk + 2 * q;
-#pragma unroll
-      for (int v = 0; v < NU; ++v) {
-        const float2 d = ld2(u[v].d + c), r = ld2(u[v].rr + g * LDF + c);
-        const uint32_t b0 = tf32(r.x * d.x), b1 = tf32(r.y * d.y);
-        const float2 k0 = ld2(u[v].kl + g * LDF + c), k1 = ld2(u[v].kl + (g + 8) * LDF + c);
-        const float2 q0 = ld2(u[v].ql + g * LDF + c), q1 = ld2(u[v].ql + (g + 8) * LDF + c);
-        const uint32_t fa[4] = {__float_as_uint(k0.x), __float_as_uint(k1.x), __float_as_uint(k0.y),
-                                __float_as_uint(k1.y)};
-        const uint32_t fq[4] = {__float_as_uint(q0.x), __float_as_uint(q1.x), __float_as_uint(q0.y),
-                                __float_as_uint(q1.y)};
-        mma1688(ak[v], fa, b0, b1);
-        mma1688(aq[v], fq, b0, b1);
-      }
+  for (int v = 0; v < NU; ++v)
+    for (int c = 0; c < 128; ++c) {
+      const float d = u[v].d[c];
+      const float k0 = u[v].kl[g * LDF + c], k1 = u[v].kl[(g + 8) * LDF + c];
+      const float q0 = u[v].ql[g * LDF + c], q1 = u[v].ql[(g + 8) * LDF + c];
+      const float r0 = u[v].rr[(2 * q) * LDF + c] * d, r1 = u[v].rr[(2 * q + 1) * LDF + c] * d;
+      ak[v][0] = fmaf(k0, r0, ak[v][0]);
+      ak[v][1] = fmaf(k0, r1, ak[v][1]);
+      ak[v][2] = fmaf(k1, r0, ak[v][2]);
+      ak[v][3] = fmaf(k1, r1, ak[v][3]);
+      aq[v][0] = fmaf(q0, r0, aq[v][0]);
+      aq[v][1] = fmaf(q0, r1, aq[v][1]);
+      aq[v][2] = fmaf(q1, r0, aq[v][2]);
+      aq[v][3] = fmaf(q1, r1, aq[v][3]);
     }
-  }
 }
 
-// acc (16x16) += A[16][16] * B[16][16], row-major fp32 with leading dims lda, ldb.
-template <bool PRECISE>
+// acc (16x16) += A[16][16] * B[16][16], row-major fp32 with leading dims lda, ldb, in the m16n8
+// accumulator layout (exact fp32 FMAs).
 __device__ __forceinline__ void mm16(float (&acc)[2][4], const float *A, int lda, const float *B, int ldb) {
   const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-  if constexpr (PRECISE) {
 #pragma unroll 4
-    for (int k = 0; k < 16; ++k) {
-      const float a0 = A[g * lda + k], a1 = A[(g + 8) * lda + k];
+  for (int k = 0; k < 16; ++k) {
+    const float a0 = A[g * lda + k], a1 = A[(g + 8) * lda + k];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const float b0 = B[k * ldb + 8 * nt + 2 * q], b1 = B[k * ldb + 8 * nt + 2 * q + 1];
-        acc[nt][0] = fmaf(a0, b0, acc[nt][0]);
-        acc[nt][1] = fmaf(a0, b1, acc[nt][1]);
-        acc[nt][2] = fmaf(a1, b0, acc[nt][2]);
-        acc[nt][3] = fmaf(a1, b1, acc[nt][3]);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int kk = 0; kk < 16; kk += 8) {
-      uint32_t a[4];
-      a[0] = tf32(A[g * lda + kk + q]);
-      a[1] = tf32(A[(g + 8) * lda + kk + q]);
-      a[2] = tf32(A[g * lda + kk + q + 4]);
-      a[3] = tf32(A[(g + 8) * lda + kk + q + 4]);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-        mma1688(acc[nt], a, tf32(B[(kk + q) * ldb + 8 * nt + g]), tf32(B[(kk + q + 4) * ldb + 8 * nt + g]));
+    for (int nt = 0; nt < 2; ++nt) {
+      const float b0 = B[k * ldb + 8 * nt + 2 * q], b1 = B[k * ldb + 8 * nt + 2 * q + 1];
+      acc[nt][0] = fmaf(a0, b0, acc[nt][0]);
+      acc[nt][1] = fmaf(a0, b1, acc[nt][1]);
+      acc[nt][2] = fmaf(a1, b0, acc[nt][2]);
+      acc[nt][3] = fmaf(a1, b1, acc[nt][3]);
     }
   }
 }
 
-// Two consecutive channels of one staged row, held in registers in the io type.
-template <typename E> struct Pair;
-template <> struct Pair<bf16> {
-  typedef __nv_bfloat162 T;
-  static __device__ __forceinline__ T load(const bf16 *p) { return *reinterpret_cast<const T *>(p); }
-  static __device__ __forceinline__ float2 get(T v) { return __bfloat1622float2(v); }
-};
-template <> struct Pair<float> {
-  typedef float2 T;
-  static __device__ __forceinline__ T load(const float *p) { return *reinterpret_cast<const T *>(p); }
-  static __device__ __forceinline__ float2 get(T v) { return v; }
-};
-
-template <typename E>
 __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_constant__ PrepParams p) {
   using S = PrepSmem2;
-  constexpr bool PRECISE = sizeof(E) == 4;   // fp32 I/O: exact fp32 products
+  typedef float E;
   extern __shared__ __align__(128) char smem[];
   // head-fastest block order: the CTAs resident at one time cover whole token rows
   // [t][all heads][d] and consecutive chunk records (DRAM pages read whole), not one head's
@@ -213,19 +163,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
   ChunkRef ref;
   if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
-  // tcgen05 record (bf16 forward) or the tile record (fp32 forward, backward)
-  const bool tcrec = !PRECISE && (p.tc_layout & 1);   // forward tcgen05 record
-  const bool bwdrec = !PRECISE && (p.tc_layout & 2);  // backward extras: Kt, A and T
   float *rq = (float *)(smem + S::RQ), *rk = (float *)(smem + S::RK), *sb = (float *)(smem + S::BETA);
   float *KL = (float *)(smem + S::KL), *QL = (float *)(smem + S::QL), *RR = (float *)(smem + S::R);
   float(*dv)[128] = (float(*)[128])(smem + S::DV);
   float(*tot)[128] = (float(*)[128])(smem + S::TOT);
-  float(*pvv)[128] = (float(*)[128])(smem + S::PV);
   const ImgLayout L(sizeof(E));
   const size_t rid = (size_t)chunk * H + h;
-  char *rec = tcrec ? (char *)p.img + rid * TcRec::BYTES : nullptr;                       // forward tcgen05 record
-  char *trec = PRECISE ? (char *)p.img + rid * L.bytes : nullptr;                         // fp32 tile record
-  char *recb = bwdrec ? (char *)p.img2 + rid * KtRec::BYTES : nullptr;
+  char *trec = (char *)p.img + rid * L.bytes;   // the tile record the fp32 scan reads
 
   // 0. stage the chunk's q, k (io type) and g (fp32) in shared memory with three TMA boxes:
   //    q in the KL tile, k in the R tile (plain rows), g in the QL tile (dense 128-float rows);
@@ -287,14 +231,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
   // 2. gate scan and factors: thread = (channel pair cp, sub-block a)
   const int cp = tid & 63, a = tid >> 6, c0 = 2 * cp;
   float2 cs[SUB];
-  typename Pair<E>::T qpair[SUB], kpair[SUB];   // this thread's raw q, k (rows a*SUB.., channels c0, c0+1)
+  float2 qpair[SUB], kpair[SUB];   // this thread's raw q, k (rows a*SUB.., channels c0, c0+1)
   {
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
       cs[i] = *reinterpret_cast<const float2 *>(QL + r * D + c0);
-      qpair[i] = Pair<E>::load(sq_ + r * D + c0);
-      kpair[i] = Pair<E>::load(sk_ + r * D + c0);
+      qpair[i] = ld2(sq_ + r * D + c0);
+      kpair[i] = ld2(sk_ + r * D + c0);
     }
     float2 run = make_float2(0.f, 0.f);
 #pragma unroll
@@ -333,51 +277,27 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
     const float pa0 = exp2f(em[0]), pa1 = exp2f(em[1]);                       // exp(E_{a-1})
     const float fa0 = exp2f(e3[0] - ea[0]), fa1 = exp2f(e3[1] - ea[1]);       // exp(E_3 - E_a)
     const float ta0 = tot[a][c0], ta1 = tot[a][c0 + 1];                       // E_a - E_{a-1}
-    pvv[a][c0] = pa0;
-    pvv[a][c0 + 1] = pa1;
     Tile<E, 128> tqt((E *)(trec + L.qt)), tkt((E *)(trec + L.kt)), tkh((E *)(trec + L.kh));
     float kh0v[SUB], kh1v[SUB];
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
       const int r = a * SUB + i;
-      const float2 qv = Pair<E>::get(qpair[i]), kv = Pair<E>::get(kpair[i]);
+      const float2 qv = qpair[i], kv = kpair[i];
       const float x0 = exp2f(cs[i].x), x1 = exp2f(cs[i].y);
       const float y0 = exp2f(ta0 - cs[i].x), y1 = exp2f(ta1 - cs[i].y);
       const float qh0 = qv.x * rq[r], qh1 = qv.y * rq[r], kh0 = kv.x * rk[r], kh1 = kv.y * rk[r];
       const float kl0 = kh0 * x0, kl1 = kh1 * x1, ql0 = qh0 * x0, ql1 = qh1 * x1;
       const float rr0 = kh0 * y0, rr1 = kh1 * y1;
-      // the Gram products read KL and QL as TF32 operands: round them once here
-      *reinterpret_cast<float2 *>(KL + r * LDF + c0) = PRECISE ? make_float2(kl0, kl1) : make_float2(rtf32(kl0), rtf32(kl1));
-      *reinterpret_cast<float2 *>(QL + r * LDF + c0) = PRECISE ? make_float2(ql0, ql1) : make_float2(rtf32(ql0), rtf32(ql1));
+      *reinterpret_cast<float2 *>(KL + r * LDF + c0) = make_float2(kl0, kl1);
+      *reinterpret_cast<float2 *>(QL + r * LDF + c0) = make_float2(ql0, ql1);
       *reinterpret_cast<float2 *>(RR + r * LDF + c0) = make_float2(rr0, rr1);
       kh0v[i] = rr0 * fa0;                        // Kh = k^ exp(G_last - G_r)
       kh1v[i] = rr1 * fa1;
-      if (tcrec)   // B1 rows 0..63: Qt[tok][dk] = q^ exp(G_r)
-        st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, r, c0)), ql0 * pa0, ql1 * pa1);
-      if (trec) {
-        st2(tqt.at(r, c0), ql0 * pa0, ql1 * pa1);                 // Qt = q^ exp(G_r)
-        st2(tkt.at(r, c0), kl0 * pa0, kl1 * pa1);                 // Kt = k^ exp(G_r)
-        st2(tkh.at(r, c0), kh0v[i], kh1v[i]);
-      }
-      if (bwdrec) st2((E *)(recb + tc::sw128_off(64, r, c0)), kl0 * pa0, kl1 * pa1);   // Kt[tok][dk]
+      st2(tqt.at(r, c0), ql0 * pa0, ql1 * pa1);                 // Qt = q^ exp(G_r)
+      st2(tkt.at(r, c0), kl0 * pa0, kl1 * pa1);                 // Kt = k^ exp(G_r)
+      st2(tkh.at(r, c0), kh0v[i], kh1v[i]);
     }
-    if (tcrec) {
-      // B2 rows 0..127: Kh^T[dk][tok]; this thread holds 16 tokens of channels c0, c0 + 1
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int k0 = a * SUB + 8 * half;
-        float t0[8], t1[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { t0[i] = kh0v[8 * half + i]; t1[i] = kh1v[8 * half + i]; }
-        *reinterpret_cast<uint4 *>(rec + TcRec::B2 + tc::sw128_off(192, c0, k0)) = tc::pack8(t0);
-        *reinterpret_cast<uint4 *>(rec + TcRec::B2 + tc::sw128_off(192, c0 + 1, k0)) = tc::pack8(t1);
-      }
-    }
-    if (a == 0) {
-      const float2 gc = make_float2(exp2f(e3[0]), exp2f(e3[1]));
-      if (tcrec) *reinterpret_cast<float2 *>(rec + TcRec::GC + c0 * 4) = gc;
-      if (trec) *reinterpret_cast<float2 *>(trec + L.gc + c0 * 4) = gc;
-    }
+    if (a == 0) *reinterpret_cast<float2 *>(trec + L.gc + c0 * 4) = make_float2(exp2f(e3[0]), exp2f(e3[1]));
   }
   __syncthreads();
   // 3. Gram products: 20 units (pair, n-tile), warp w takes units w, w + 8, w + 16
@@ -396,14 +316,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
       un[v].rr = RR + (pb * SUB + 8 * (unit & 1)) * LDF;
       un[v].d = dv[pr];
     }
-    if (warp < 4) gram_units<PRECISE, 3>(acc, accq, un);
-    else gram_units<PRECISE, 2>(acc, accq, un);
+    if (warp < 4) gram_units<3>(acc, accq, un);
+    else gram_units<2>(acc, accq, un);
   }
   __syncthreads();   // QL and R are free from here on
   {
     float *Lm = (float *)(smem + S::LM);
     Tile<E, 64> bm((E *)(trec + L.bm));
-    float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) : nullptr;
 #pragma unroll
     for (int v = 0; v < 3; ++v) {
       const int unit = warp + 8 * v;
@@ -415,29 +334,24 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
         const int r = pa * SUB + g + 8 * hh, j = pb * SUB + 8 * (unit & 1) + 2 * q;
         const float v0 = accq[v][2 * hh], v1 = accq[v][2 * hh + 1];
         const float b0 = j <= r ? v0 : 0.f, b1 = j + 1 <= r ? v1 : 0.f;
-        if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), b0, b1);
-        if (trec) st2(bm.at(r, j), b0, b1);
+        st2(bm.at(r, j), b0, b1);
         const float w0 = acc[v][2 * hh], w1 = acc[v][2 * hh + 1];
         const float a0 = j < r ? w0 : 0.f, a1 = j + 1 < r ? w1 : 0.f;
         *reinterpret_cast<float2 *>(Lm + r * LDS64 + j) = make_float2(sb[r] * a0, sb[r] * a1);
-        if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(a0, a1);
       }
     }
     // zero the sub-blocks of Bm above the diagonal
     for (int idx = tid; idx < 64 * 32; idx += PREP_THREADS) {
       const int r = idx >> 5, j = (idx & 31) * 2;
       if ((j >> 4) > (r >> 4)) {
-        if (tcrec) st2((E *)(rec + TcRec::B2 + tc::sw128_off(192, 128 + r, j)), 0.f, 0.f);
-        if (trec) st2(bm.at(r, j), 0.f, 0.f);
+        st2(bm.at(r, j), 0.f, 0.f);
       }
     }
   }
   __syncthreads();
   // 4. T = (I + Lm)^-1: diagonal sub-blocks by forward substitution (warps 0..3), then the
-  //    off-diagonal blocks level by level on warps 0..3. With a forward record, warps 4..7 form
-  //    W = T (Diag(beta) Kt) one 16-row block at a time as soon as that block of T is final
-  //    (row block a needs T_ab, b <= a: final after level a), and warps 0..3 write T's outputs
-  //    while the last block of W is formed.
+  //    off-diagonal blocks level by level on warps 0..3; then Tb = T Diag(beta) into the record
+  //    (and T for the backward).
   {
     const float *Lm = (const float *)(smem + S::LM);
     float *T = (float *)(smem + S::TT);
@@ -458,58 +372,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
         for (int i = 0; i < SUB; ++i) T[(ab * SUB + i) * LDS64 + ab * SUB + j] = x[i];
       }
     } else {
-      // warps 4..7 zero the blocks above the diagonal and turn KL into Diag(beta) Kt, Kt = KL exp(E_{a-1})
+      // warps 4..7 zero the blocks above the diagonal
       for (int idx = tid - 128; idx < 64 * 64; idx += 128) {
         const int r = idx >> 6, j = idx & 63;
         if ((j >> 4) > (r >> 4)) T[r * LDS64 + j] = 0.f;
       }
-      if (tcrec) {
-        for (int idx = tid - 128; idx < 64 * 64; idx += 128) {
-          const int r = idx >> 6, c = (idx & 63) * 2;
-          float2 *kp = reinterpret_cast<float2 *>(KL + r * LDF + c);
-          const float2 kv = *kp;
-          const float br = sb[r];
-          *kp = make_float2(kv.x * pvv[r >> 4][c] * br, kv.y * pvv[r >> 4][c + 1] * br);
-        }
-      }
     }
     __syncthreads();
-    // outputs of T: Tb = T Diag(beta) into the record, T for the backward (threads [t0, t0 + nt))
-    auto write_t = [&](int t0, int nth) {
-      Tile<E, 64> tb((E *)(trec + L.tb));
-      float *aux = p.aux ? p.aux + ((size_t)chunk * H + h) * (2 * 64 * 64) + 64 * 64 : nullptr;
-      for (int idx = tid - t0; idx < 64 * 32; idx += nth) {
-        const int r = idx >> 5, j = (idx & 31) * 2;
-        const float t0v = T[r * LDS64 + j], t1v = T[r * LDS64 + j + 1];
-        const float b0 = t0v * sb[j], b1 = t1v * sb[j + 1];
-        if (tcrec) st2((E *)(rec + TcRec::TB + tc::sw128_off(64, r, j)), b0, b1);
-        if (trec) st2(tb.at(r, j), b0, b1);
-        if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(t0v, t1v);
-      }
-    };
-    // one 16-row block of W (B1 rows 64.. hold -W[tok][dk]) on warps 4..7, 32 columns each
-    auto w_block = [&](int mt) {
-      const int n0 = 32 * (warp - NSUB);
-      float wacc[4][4];
-      zero(wacc);
-      for (int kk = 0; kk < 16 * (mt + 1); kk += 8) {
-        uint32_t af[4];
-        af[0] = tf32(T[(16 * mt + g) * LDS64 + kk + q]);
-        af[1] = tf32(T[(16 * mt + g + 8) * LDS64 + kk + q]);
-        af[2] = tf32(T[(16 * mt + g) * LDS64 + kk + q + 4]);
-        af[3] = tf32(T[(16 * mt + g + 8) * LDS64 + kk + q + 4]);
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-          mma1688(wacc[nt], af, tf32(KL[(kk + q) * LDF + n0 + 8 * nt + g]), tf32(KL[(kk + q + 4) * LDF + n0 + 8 * nt + g]));
-      }
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = 16 * mt + g + 8 * hh, c = n0 + 8 * nt + 2 * q;
-          st2((E *)(rec + TcRec::B1 + tc::sw128_off(128, 64 + r, c)), -wacc[nt][2 * hh], -wacc[nt][2 * hh + 1]);
-        }
-    };
     // off-diagonal sub-blocks by levels: T_ab = -T_aa * sum_{m=b}^{a-1} Lm_am T_mb
     float *P = (float *)(smem + S::SCR) + warp * 16 * LDP;
     for (int d = 1; d < NSUB; ++d) {
@@ -518,7 +387,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
         float pacc[2][4];
         zero(pacc);
         for (int m = b; m < ab; ++m)
-          mm16<PRECISE>(pacc, Lm + ab * SUB * LDS64 + m * SUB, LDS64, T + m * SUB * LDS64 + b * SUB, LDS64);
+          mm16(pacc, Lm + ab * SUB * LDS64 + m * SUB, LDS64, T + m * SUB * LDS64 + b * SUB, LDS64);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           *reinterpret_cast<float2 *>(P + g * LDP + 8 * nt + 2 * q) = make_float2(pacc[nt][0], pacc[nt][1]);
@@ -527,7 +396,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
         __syncwarp();
         float tacc[2][4];
         zero(tacc);
-        mm16<PRECISE>(tacc, T + ab * SUB * LDS64 + ab * SUB, LDS64, P, LDP);
+        mm16(tacc, T + ab * SUB * LDS64 + ab * SUB, LDS64, P, LDP);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           float *dst = T + (ab * SUB + g) * LDS64 + b * SUB + 8 * nt + 2 * q;
@@ -535,36 +404,28 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
           *reinterpret_cast<float2 *>(dst + 8 * LDS64) = make_float2(-tacc[nt][2], -tacc[nt][3]);
         }
         __syncwarp();
-      } else if (tcrec && warp >= NSUB) {
-        w_block(d - 1);   // rows of T final since level d - 1
       }
       __syncthreads();
     }
-    // T is final: the last block of W on warps 4..7 while warps 0..3 write T's outputs
-    if (tcrec) {
-      if (warp >= NSUB) w_block(NSUB - 1);
-      else write_t(0, 128);
-    } else {
-      write_t(0, PREP_THREADS);
+    Tile<E, 64> tb((E *)(trec + L.tb));
+    for (int idx = tid; idx < 64 * 32; idx += PREP_THREADS) {
+      const int r = idx >> 5, j = (idx & 31) * 2;
+      const float t0v = T[r * LDS64 + j], t1v = T[r * LDS64 + j + 1];
+      st2(tb.at(r, j), t0v * sb[j], t1v * sb[j + 1]);
     }
   }
 }
 
-template <typename E>
-static cudaError_t launch_prep_t(const PrepParams &p, cudaStream_t s) {
+cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s) {
+  if (p.geo.max_chunks == 0) return cudaSuccess;
+  if (!f32) return cudaErrorInvalidValue;   // the bf16 forward runs launch_prep_tc
   using S = PrepSmem2;
-  auto kern = kda_prep_kernel<E>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+  cudaError_t e = cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.geo.max_chunks * p.geo.heads;   // head-fastest: see the kernel
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)blocks, PREP_THREADS, S::BYTES, s>>>(p);
+  kda_prep_kernel<<<(unsigned)blocks, PREP_THREADS, S::BYTES, s>>>(p);
   return cudaGetLastError();
-}
-
-cudaError_t launch_prep(const PrepParams &p, bool f32, cudaStream_t s) {
-  if (p.geo.max_chunks == 0) return cudaSuccess;
-  return f32 ? launch_prep_t<float>(p, s) : launch_prep_t<bf16>(p, s);
 }
 
 }  // namespace kda

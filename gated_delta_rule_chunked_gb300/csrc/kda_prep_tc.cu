@@ -78,6 +78,13 @@ __host__ __device__ constexpr int stack_off(int a) { return 8 * a * (a + 1); }
 __host__ __device__ constexpr int pair_idx(int a, int ap) { return a * (7 - a) / 2 + (ap - a - 1); }
 
 __device__ __forceinline__ float rtf32(float x) { return __uint_as_float(tf32(x)); }
+// 2^x by the hardware approximation (relative error about 2^-22), results below 2^-126 flushed to
+// zero: every gating factor here multiplies O(1) values, so such results are negligible
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // byte offset of fp32 element (row, k) of a K-major SW128 tile with `rows` rows
 __device__ __forceinline__ uint32_t o32(int rows, int row, int k) { return tc::sw128_off32(rows, row, k); }
@@ -240,11 +247,11 @@ __global__ void __launch_bounds__(PT_THREADS, 2) kda_prep_tc_kernel(const __grid
       em[0] = 0.f;
 #pragma unroll
       for (int b = 0; b < NSUB; ++b) em[b + 1] = em[b] + tot[b][c];
-      if (a == 0) *reinterpret_cast<float *>(rec + TcRec::GC + 4 * c) = exp2f(em[NSUB]);   // e^{G_last}
-      pam[a * 128 + c] = exp2f(em[a]);
+      if (a == 0) *reinterpret_cast<float *>(rec + TcRec::GC + 4 * c) = ex2(em[NSUB]);   // e^{G_last}
+      pam[a * 128 + c] = ex2(em[a]);
 #pragma unroll
       for (int ap = 1; ap < NSUB; ++ap)
-        if (ap > a) pfm[pair_idx(a, ap) * 128 + c] = exp2f(em[ap] - em[a]);
+        if (ap > a) pfm[pair_idx(a, ap) * 128 + c] = ex2(em[ap] - em[a]);
       // Kh = k^ e^{G_last - G} into the record (B2 rows 0..127, transposed: row c, tokens 16a..)
       const float ftail = em[NSUB] - em[a];
 #pragma unroll
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(PT_THREADS, 2) kda_prep_tc_kernel(const __grid
         for (int e = 0; e < 8; ++e) {
           const int i = i8 + e, r = a * SUB + i;
           const float csr = hh ? cs1[i] : cs0[i];
-          khv[e] = (hh ? __high2float(kk[i]) : __low2float(kk[i])) * rk[r] * exp2f(ftail - csr);
+          khv[e] = (hh ? __high2float(kk[i]) : __low2float(kk[i])) * rk[r] * ex2(ftail - csr);
           csm[r * D + c] = csr;
         }
         *reinterpret_cast<uint4 *>(rec + TcRec::B2 + tc::sw128_off(192, c, a * SUB + i8)) = tc::pack8(khv);
@@ -309,10 +316,10 @@ __global__ void __launch_bounds__(PT_THREADS, 2) kda_prep_tc_kernel(const __grid
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float kh = kvv[e] * rkr;
-          const float x = exp2f(csv[e]);            // e^{G_r - E_{a-1}} <= 1
+          const float x = ex2(csv[e]);            // e^{G_r - E_{a-1}} <= 1
           kl[e] = kh * x;
           ql[e] = qvv[e] * rqr * x;
-          rn[e] = kh * exp2f(-csv[e]);              // k^_r e^{E_{a-1} - G_r}: the right factor of block a
+          rn[e] = kh * ex2(-csv[e]);              // k^_r e^{E_{a-1} - G_r}: the right factor of block a
           bk[g][s2][e] = br * kl[e] * pav[e];
         }
         const int kk = 32 * bf + 4 * q8;            // column inside the buffer's two K-blocks

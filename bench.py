@@ -48,9 +48,9 @@ KERNEL_BYTES = {
 }
 FWD_STAGES = ["fwd.table", "fwd.prep", "fwd.scan"]
 BWD_STAGES = ["bwd.table", "bwd.dscan", "bwd.chunk"]
-KERNEL_SRC = {"fwd.prep": "kda_prep.cu", "fwd.scan": "kda_scan_tc.cu",
+KERNEL_SRC = {"fwd.prep": "kda_prep_tc.cu", "fwd.scan": "kda_scan_tc.cu",
               "bwd.dscan": "kda_scan_tc.cu", "bwd.chunk": "kda_bwd_tc.cu",
-              "fwd.prep.inference": "kda_prep.cu", "fwd.scan.inference": "kda_scan_tc.cu",
+              "fwd.prep.inference": "kda_prep_tc.cu", "fwd.scan.inference": "kda_scan_tc.cu",
               "decode": "kda_step.cu", "attnres.fwd": "kda_attnres.cu", "attnres.bwd": "kda_attnres.cu",
               "conv.fwd": "kda_conv.cu", "conv.bwd": "kda_conv.cu", "conv.step": "kda_conv.cu"}
 
@@ -306,7 +306,7 @@ def run_ours(args, rank, world, local_rank):
     dom = max(KERNEL_BYTES, key=lambda n: per[n])
     dom_bytes = KERNEL_BYTES[dom] * units
     achieved = dom_bytes / (per[dom] * 1e-3) / 1e9
-    traffic = recorded_traffic(dom)
+    traffic = recorded_traffic(dom) if not args.seq_len else None   # recorded for T = 32768
     step_bytes = (FWD_BYTES + BWD_BYTES) * units
     out = {
         "metric": "KDA fwd+bwd tokens/s (H=96, d=128, T=32768, bf16 I/O, fp32 state/grads)",

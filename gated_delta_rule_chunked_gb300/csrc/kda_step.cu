@@ -23,8 +23,9 @@
 //
 // Two-phase draft/verify: the state of a sequence may sit in any slot of a pool
 // (state_indices), and a call's leading slots may be padding (first_slot): a
-// padded slot has zero inputs, beta = 0 and g = 0, so it leaves S and every other
-// token's quantities exactly as they were, and its output is not written. A call
+// padded slot stands for zero inputs, beta = 0 and g = 0, which leave S and every
+// other token's quantities exactly as they were, so the kernel skips it (its inputs
+// are not read, its output is not written). A call
 // can thus replay a sequence's accepted draft tokens (right-aligned before the new
 // draft) and commit after them while verifying the next draft in the same pass.
 #include "kda_common.cuh"
@@ -63,17 +64,22 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seq = blockIdx.x / p.heads, h = blockIdx.x % p.heads;
-  const int L = p.steps, H = p.heads, NV = 2 * L;
-  int A = p.accept_len ? p.accept_len[seq] : L;
-  A = A < 0 ? 0 : (A > L ? L : A);
-  // slots before F are padding: zero inputs, beta = 0 and g = 0 make them exact identities
+  const int LS = p.steps, H = p.heads;   // token slots of the call
+  int A = p.accept_len ? p.accept_len[seq] : LS;
+  A = A < 0 ? 0 : (A > LS ? LS : A);
+  // slots before F are padding: zero inputs, beta = 0 and g = 0 make them exact identities, so
+  // only the L = LS - F real slots are evaluated (real token l is slot F + l) and the state is
+  // committed after A - F of them
   int F = p.first_slot ? p.first_slot[seq] : 0;
-  F = F < 0 ? 0 : (F > L ? L : F);
+  F = F < 0 ? 0 : (F > LS ? LS : F);
+  const int L = LS - F, NV = 2 * L;
+  A = A > F ? A - F : 0;
   const int slot = p.state_indices ? p.state_indices[seq] : seq;
   if (p.state_indices && (slot < 0 || slot >= p.n_slots)) {   // block-uniform
     if (tid == 0) report(p.status, KDA_ERR_INVALID_ARG_CODE);
     return;
   }
+  if (L == 0) return;   // padding only: no output, the state is unchanged
   float *red = step_red, *W = step_red + 8 * NV * D;
 
   // state rows [16 warp, +16), columns [4 lane, +4) as two column pairs
@@ -91,14 +97,13 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
            *v = static_cast<const IO *>(p.v);
   for (int idx = tid; idx < L * D; idx += STEP_THREADS) {
     const int l = idx / D, c = idx % D;
-    const size_t off = (((size_t)seq * L + l) * H + h) * D + c;
-    const bool pad = l < F;
-    sm.q[l][c] = pad ? 0.f : ld_io(q + off);
-    sm.k[l][c] = pad ? 0.f : ld_io(k + off);
-    sm.v[l][c] = pad ? 0.f : ld_io(v + off);
-    sm.G[l][c] = pad ? 0.f : p.g[off];
+    const size_t off = (((size_t)seq * LS + F + l) * H + h) * D + c;
+    sm.q[l][c] = ld_io(q + off);
+    sm.k[l][c] = ld_io(k + off);
+    sm.v[l][c] = ld_io(v + off);
+    sm.G[l][c] = p.g[off];
   }
-  if (tid < L) sm.beta[tid] = tid < F ? 0.f : p.beta[((size_t)seq * L + tid) * H + h];
+  if (tid < L) sm.beta[tid] = p.beta[((size_t)seq * LS + F + tid) * H + h];
   __syncthreads();
 
   // L2 normalisation (one warp per token) and the running gate sums (one thread per channel)
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
         u[l] = sm.beta[l] * (sm.v[l][tid] - w);
         ol = fmaf(sm.b[l][l], u[l], ol);
         sm.U[l][tid] = u[l];
-        if (l >= F) o[(((size_t)seq * L + l) * H + h) * D + tid] = from_f<IO>(ol);
+        o[(((size_t)seq * LS + F + l) * H + h) * D + tid] = from_f<IO>(ol);
       }
     }
   }

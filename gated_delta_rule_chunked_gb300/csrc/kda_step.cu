@@ -56,7 +56,8 @@ struct StepSmem {
   float beta[STEP_MAX_L];
 };
 
-template <typename IO>
+// PAD: the call has padded leading slots (first_slot given); without them F = 0 is a constant.
+template <typename IO, bool PAD>
 __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p) {
   __shared__ __align__(16) StepSmem sm;
   // partials [8 row groups][2L vectors][D], then the reduced sums [2L][D]
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
   // slots before F are padding: zero inputs, beta = 0 and g = 0 make them exact identities, so
   // only the L = LS - F real slots are evaluated (real token l is slot F + l) and the state is
   // committed after A - F of them
-  int F = p.first_slot ? p.first_slot[seq] : 0;
+  int F = PAD ? p.first_slot[seq] : 0;
   F = F < 0 ? 0 : (F > LS ? LS : F);
   const int L = LS - F, NV = 2 * L;
   A = A > F ? A - F : 0;
@@ -279,23 +280,25 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
   }
 }
 
-template <typename IO>
+template <typename IO, bool PAD>
 static cudaError_t launch_step_t(const StepParams &p, unsigned grid, cudaStream_t s) {
   // Dynamic shared memory: 8 row-group partials plus the reduced sums, 2L vectors each.
   constexpr int max_smem = (8 + 1) * 2 * STEP_MAX_L * D * (int)sizeof(float);
   const int smem = (8 + 1) * 2 * p.steps * D * (int)sizeof(float);
   // static + dynamic exceeds the 48 KiB default: opt in (per device, idempotent)
   const cudaError_t e =
-      cudaFuncSetAttribute(kda_step_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+      cudaFuncSetAttribute(kda_step_kernel<IO, PAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   if (e != cudaSuccess) return e;
-  kda_step_kernel<IO><<<grid, STEP_THREADS, smem, s>>>(p);
+  kda_step_kernel<IO, PAD><<<grid, STEP_THREADS, smem, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s) {
   const unsigned grid = (unsigned)((long long)p.n_seqs * p.heads);
   if (grid == 0) return cudaSuccess;
-  return f32 ? launch_step_t<float>(p, grid, s) : launch_step_t<bf16>(p, grid, s);
+  const bool pad = p.first_slot != nullptr;
+  if (f32) return pad ? launch_step_t<float, true>(p, grid, s) : launch_step_t<float, false>(p, grid, s);
+  return pad ? launch_step_t<bf16, true>(p, grid, s) : launch_step_t<bf16, false>(p, grid, s);
 }
 
 }  // namespace kda

@@ -36,6 +36,8 @@ D = 128
 # algorithmic bytes per token and head (inputs read once, outputs written once)
 FWD_BYTES = 3 * 256 + 512 + 4 + 256          # q,k,v bf16 + g fp32 + beta + o bf16        = 1540
 BWD_BYTES = 3 * 256 + 512 + 4 + 256 + 3 * 512 + 512 + 4   # + dO, dq/dk/dv/dg fp32, dbeta = 3592
+FWD_BYTES_F32 = 3 * 512 + 512 + 4 + 512      # the same tensors with fp32 q, k, v, o      = 2564
+BWD_BYTES_F32 = 3 * 512 + 512 + 4 + 512 + 3 * 512 + 512 + 4   # fp32 q, k, v, dO            = 4616
 FWD_FLOP = 10 * 64 * D + 6 * D * D           # 180,224
 BWD_FLOP = 24 * 64 * D + 12 * D * D          # 393,216
 DEC_BYTES = 2 * D * D * 4 + 4 * (3 * 256 + 512 + 4 + 256)   # per (sequence, head) per 4-token call
@@ -134,17 +136,22 @@ class ChunkedCase:
     "fwdbwd": training forward (saves what the backward needs) + backward; "fwd": the
     inference forward (no saved, records in the workspace)."""
 
-    def __init__(self, lib, dev, name, mode, status, seq_len=0):
+    def __init__(self, lib, dev, name, mode, status, seq_len=0, over=None):
         import torch
         import gated_delta_rule_chunked_gb300 as kda
         from gated_delta_rule_chunked_gb300.inputs import make_workload, WORKLOADS
-        over = {"seq_lens": (seq_len,)} if seq_len else {}
+        over = dict(over or {})
+        if seq_len:
+            over["seq_lens"] = (seq_len,)
         seed = WORKLOADS[name].seed
         self.sets = [make_workload(name, device=dev, **over, **({"seed": seed + 5000} if i else {}))
                      for i in range(2)]
         b = self.sets[0]
         self.T, self.H, self.N = b.total, b.heads, b.n_seqs
         self.mode = mode
+        f32io = b.q.dtype == torch.float32
+        self.fwd_bytes = FWD_BYTES_F32 if f32io else FWD_BYTES
+        self.bwd_bytes = BWD_BYTES_F32 if f32io else BWD_BYTES
         f32 = dict(dtype=torch.float32, device=dev)
         self.o = torch.empty_like(b.v)
         self.hT = torch.empty((self.N, self.H, D, D), **f32)
@@ -231,15 +238,15 @@ def summarize(case, per, peaks, ms=None):
     units = case.T * case.H
     fwd_ms = sum(per[n] for n in FWD_STAGES)
     out = {"fwd": {"ms": fwd_ms, "tokens_per_s": case.T / (fwd_ms * 1e-3),
-                   "gbs_algorithmic": FWD_BYTES * units / (fwd_ms * 1e-3) / 1e9,
-                   "roofline_frac": FWD_BYTES * units / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
+                   "gbs_algorithmic": case.fwd_bytes * units / (fwd_ms * 1e-3) / 1e9,
+                   "roofline_frac": case.fwd_bytes * units / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
     if case.mode == "fwdbwd":
         bwd_ms = sum(per[n] for n in BWD_STAGES)
         out["bwd"] = {"ms": bwd_ms, "tokens_per_s": case.T / (bwd_ms * 1e-3),
-                      "gbs_algorithmic": BWD_BYTES * units / (bwd_ms * 1e-3) / 1e9,
-                      "roofline_frac": BWD_BYTES * units / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+                      "gbs_algorithmic": case.bwd_bytes * units / (bwd_ms * 1e-3) / 1e9,
+                      "roofline_frac": case.bwd_bytes * units / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     if ms is not None:
-        byts = (FWD_BYTES + (BWD_BYTES if case.mode == "fwdbwd" else 0)) * units
+        byts = (case.fwd_bytes + (case.bwd_bytes if case.mode == "fwdbwd" else 0)) * units
         out["step"] = {"ms": ms, "tokens_per_s": case.T / (ms * 1e-3), "gbs_algorithmic": byts / (ms * 1e-3) / 1e9,
                        "roofline_frac": byts / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     out["kernels_ms"] = {k: round(v, 4) for k, v in per.items()}
@@ -275,6 +282,21 @@ def bench_range(args, lib, dev, stream, peaks, status):
         res[key] = line
         del case
         torch.cuda.empty_cache()
+    # fp32 I/O fwd + bwd: the fp32 workload's recipe at 4096 tokens x 96 heads
+    case = ChunkedCase(lib, dev, "fwd-f32-T512-H2", "fwdbwd", status,
+                       over={"kind": "fwdbwd", "seq_lens": (4096,), "heads": 96})
+    K = max(3, min(args.steps, 10))
+    ms, per, _ = time_case(case, lib, dev, stream, K, max(args.warmup, 3))
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())} in the fp32 line: no number reported")
+    res["fwdbwd_f32_T4096"] = {
+        "workload": "fwdbwd-f32-T4096-H96 (the recipe of fwd-f32-T512-H2 at 4096 tokens x 96 heads, dO drawn after)",
+        "mode": "training fwd + bwd, fp32 I/O", "tokens": case.T, "sequences": case.N, "steps": K,
+        **summarize(case, per, peaks, ms),
+        "note": "fp32 products on the CUDA cores (the 1e-4 tolerance of fp32 I/O); bwd.dscan includes the "
+                "backward's re-run of the chunk prep, bwd.chunk its state-side and intra-chunk kernels"}
+    del case
+    torch.cuda.empty_cache()
     return res
 
 

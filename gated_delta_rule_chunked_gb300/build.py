@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkda.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["kda_api.cu", "kda_step.cu", "kda_prep.cu", "kda_prep_tc.cu", "kda_scan.cu", "kda_scan_tc.cu", "kda_bwd_tc.cu", "kda_conv.cu",
+SOURCES = ["kda_api.cu", "kda_step.cu", "kda_prep.cu", "kda_prep_tc.cu", "kda_scan.cu", "kda_scan_tc.cu", "kda_bwd_tc.cu", "kda_bwd_f32.cu", "kda_conv.cu",
            "kda_cp.cu", "kda_attnres.cu", "kda_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -53,7 +53,7 @@ size_t elem_size(int io) { return io == KDA_F32 ? 4 : 2; }
 
 // Workspace carving shared by the forward and the backward.
 struct WsPlan {
-  size_t cu, choff, img, dsaved, bytes;
+  size_t cu, choff, img, dsaved, aux, scratch, bytes;
 };
 
 WsPlan plan(const kda_fwd_args *a, bool bwd) {
@@ -70,6 +70,14 @@ WsPlan plan(const kda_fwd_args *a, bool bwd) {
   } else {
     w.dsaved = round_up(end, 256);
     end = w.dsaved + mc * H * 128 * 128 * elem_size(a->io_dtype);
+    if (a->io_dtype == KDA_F32) {   // the fp32 backward recomputes the records, A and T
+      w.img = round_up(end, 256);
+      end = w.img + mc * H * L.bytes;
+      w.aux = round_up(end, 256);
+      end = w.aux + mc * H * 2 * 64 * 64 * sizeof(float);
+      w.scratch = round_up(end, 256);
+      end = w.scratch + mc * H * kda::BWD_F32_SCRATCH * sizeof(float);
+    }
   }
   w.bytes = round_up(end, 256);
   return w;
@@ -572,6 +580,65 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
   return KDA_OK;
 }
 
+namespace {
+// fp32 I/O: the prep runs again into the workspace (records, A, T), then the fp32 dS scan and
+// the two fp32 chunk kernels (kda_bwd_f32.cu). `saved` holds the chunk-start states only.
+kda_status bwd_f32(const kda_bwd_args *a, const WsPlan &w, cudaStream_t stream) {
+  const kda_fwd_args *f = &a->fwd;
+  char *ws = static_cast<char *>(a->workspace);
+  const long long T = f->total_tokens;
+  CUtensorMap tm_q, tm_k, tm_g;
+  if (!map_tokens(&tm_q, f->q, true, T, f->heads, 128, false) || !map_tokens(&tm_k, f->k, true, T, f->heads, 128, false) ||
+      !map_tokens(&tm_g, f->g, true, T, f->heads, 128, false))
+    return fail(KDA_ERR_CUDA, "%s: could not encode the TMA tensor maps", "kda_bwd");
+  kda::SeqGeom geo = geom(f, ws, w);
+  cudaError_t e = kda::launch_chunk_table(f->cu_seqlens, f->n_seqs, T, reinterpret_cast<int *>(ws + w.cu),
+                                          reinterpret_cast<int *>(ws + w.choff), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kda_bwd chunk table");
+  mark(0, stream);
+  kda::PrepParams pp{};
+  pp.geo = geo;
+  pp.q = f->q;
+  pp.k = f->k;
+  pp.g = f->g;
+  pp.beta = f->beta;
+  pp.scale = f->scale;
+  pp.img = ws + w.img;
+  pp.aux = reinterpret_cast<float *>(ws + w.aux);
+  pp.status = f->dev_status;
+  pp.tm_q = tm_q;
+  pp.tm_k = tm_k;
+  pp.tm_g = tm_g;
+  if ((e = kda::launch_prep(pp, true, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd prep");
+  kda::BwdScanParams bp{geo, a->dO, ws + w.img, a->dhT, a->dv, a->dh0, ws + w.dsaved, f->dev_status, {}};
+  if ((e = kda::launch_bwd_scan_f32(bp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd dS scan");
+  mark(1, stream);
+  kda::BwdF32Params cp{};
+  cp.geo = geo;
+  cp.q = static_cast<const float *>(f->q);
+  cp.k = static_cast<const float *>(f->k);
+  cp.v = static_cast<const float *>(f->v);
+  cp.dO = static_cast<const float *>(a->dO);
+  cp.g = f->g;
+  cp.beta = f->beta;
+  cp.scale = f->scale;
+  cp.img = ws + w.img;
+  cp.aux = reinterpret_cast<const float *>(ws + w.aux);
+  cp.saved = static_cast<const float *>(f->saved);
+  cp.dsaved = reinterpret_cast<const float *>(ws + w.dsaved);
+  cp.dq = a->dq;
+  cp.dk = a->dk;
+  cp.dg = a->dg;
+  cp.dbeta = a->dbeta;
+  cp.scratch = reinterpret_cast<float *>(ws + w.scratch);
+  cp.status = f->dev_status;
+  if ((e = kda::launch_bwd_chunk_f32(cp, stream)) != cudaSuccess) return cuda_fail(e, "kda_bwd chunk grads");
+  mark(2, stream);
+  g_last_error.clear();
+  return KDA_OK;
+}
+}  // namespace
+
 kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
   if (!a) return fail(KDA_ERR_INVALID_ARG, "%s: args is NULL", "kda_bwd");
   const kda_fwd_args *f = &a->fwd;
@@ -579,8 +646,6 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
   if (!fcheck.o) fcheck.o = a->dq;   // o is not used by the backward
   kda_status st = check_fwd(&fcheck, "kda_bwd");
   if (st != KDA_OK) return st;
-  if (f->io_dtype == KDA_F32)
-    return fail(KDA_ERR_UNSUPPORTED, "%s: the backward supports io_dtype KDA_BF16 only", "kda_bwd");
   if (!f->v && f->total_tokens > 0) return fail(KDA_ERR_INVALID_ARG, "%s: v is NULL", "kda_bwd");
   const WsPlan w = plan(f, true);
   if (!a->workspace || a->workspace_bytes < w.bytes)
@@ -606,6 +671,7 @@ kda_status kda_bwd(const kda_bwd_args *a, cudaStream_t stream) {
     return KDA_OK;
   }
   char *ws = static_cast<char *>(a->workspace);
+  if (f->io_dtype == KDA_F32) return bwd_f32(a, w, stream);
   // the chunk records were written by the forward's prep into `saved`
   const SavedPlan sv = saved_plan(f);
   char *sd = static_cast<char *>(f->saved);

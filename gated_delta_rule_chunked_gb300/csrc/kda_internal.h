@@ -116,6 +116,25 @@ struct BwdChunkParams {
   int *status;
 };
 
+// fp32-I/O backward (kda_bwd_f32.cu). The records and {A, T} come from a prep run into the
+// backward's workspace; `saved` holds the forward's chunk-start states S[k][v] and `dsaved`
+// the dS scan's chunk-end gradients dS[k][v] (fp32 tiles, swizzled as Tile<float, 128>).
+// The state-side kernel leaves dQt, dKt and dKh in the dq, dk and dg arrays and dBm, dA and
+// dgC e^{G_last} in `scratch` (BWD_F32_SCRATCH floats per chunk-head); the intra-chunk
+// kernel turns them into the final dq, dk and dg.
+constexpr int BWD_F32_SCRATCH = 2 * 64 * 64 + 128;
+struct BwdF32Params {
+  SeqGeom geo;
+  const float *q, *k, *v, *dO, *g, *beta;
+  float scale;
+  const void *img;              // [max_chunks][H] fp32 tile records (ImgLayout)
+  const float *aux;             // [max_chunks][H] x {A, T}
+  const float *saved, *dsaved;  // [max_chunks][H] 128 x 128
+  float *dq, *dk, *dg, *dbeta;
+  float *scratch;               // [max_chunks][H][BWD_F32_SCRATCH]
+  int *status;
+};
+
 struct StepParams {
   int n_seqs, steps, heads;
   float scale;
@@ -183,6 +202,8 @@ cudaError_t launch_conv_bwd(const ConvParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_conv_step(const ConvParams &p, bool f32, cudaStream_t s);
 int conv_bwd_groups(long long T, int C, int W, bool f32);
 cudaError_t launch_bwd_chunk_tc(const BwdChunkParams &p, cudaStream_t s);
+cudaError_t launch_bwd_scan_f32(const BwdScanParams &p, cudaStream_t s);    // fp32 I/O dS scan
+cudaError_t launch_bwd_chunk_f32(const BwdF32Params &p, cudaStream_t s);   // fp32 I/O chunk gradients
 cudaError_t launch_step(const StepParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_cp_combine(int n_seqs, int n_segments, int heads, const float *M, const float *b, const float *h0,
                               float *s_in, cudaStream_t s);

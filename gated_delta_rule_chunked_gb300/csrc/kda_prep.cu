@@ -11,7 +11,8 @@
 //      I/O tolerance leaves no room for TF32 operands);
 //   4. the WY/UT transform T = (I + Diag(beta) A)^-1 (16x16 diagonal blocks by
 //      forward substitution, off-diagonal blocks by fp32 block products);
-//   5. the operands the sequential state scan needs, written as one record.
+//   5. the operands the sequential state scan needs, written as one record, and, for the
+//      backward, A (strict lower, without beta) and T in plain fp32 [64][64] arrays.
 //
 // Gating factorisation. exp(G_r - G_j) is split into two bounded factors so the
 // Gram products run as plain matrix multiplies. With 16-token sub-blocks and
@@ -170,6 +171,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
   const ImgLayout L(sizeof(E));
   const size_t rid = (size_t)chunk * H + h;
   char *trec = (char *)p.img + rid * L.bytes;   // the tile record the fp32 scan reads
+  // the backward's copy of A (strict lower, without beta) and T, plain [64][64] fp32 each
+  float *aux = p.aux ? p.aux + rid * 2 * 64 * 64 : nullptr;
 
   // 0. stage the chunk's q, k (io type) and g (fp32) in shared memory with three TMA boxes:
   //    q in the KL tile, k in the R tile (plain rows), g in the QL tile (dense 128-float rows);
@@ -338,13 +341,15 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
         const float w0 = acc[v][2 * hh], w1 = acc[v][2 * hh + 1];
         const float a0 = j < r ? w0 : 0.f, a1 = j + 1 < r ? w1 : 0.f;
         *reinterpret_cast<float2 *>(Lm + r * LDS64 + j) = make_float2(sb[r] * a0, sb[r] * a1);
+        if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(a0, a1);
       }
     }
-    // zero the sub-blocks of Bm above the diagonal
+    // zero the sub-blocks of Bm (and of A for the backward) above the diagonal
     for (int idx = tid; idx < 64 * 32; idx += PREP_THREADS) {
       const int r = idx >> 5, j = (idx & 31) * 2;
       if ((j >> 4) > (r >> 4)) {
         st2(bm.at(r, j), 0.f, 0.f);
+        if (aux) *reinterpret_cast<float2 *>(aux + r * 64 + j) = make_float2(0.f, 0.f);
       }
     }
   }
@@ -412,6 +417,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const __grid_
       const int r = idx >> 5, j = (idx & 31) * 2;
       const float t0v = T[r * LDS64 + j], t1v = T[r * LDS64 + j + 1];
       st2(tb.at(r, j), t0v * sb[j], t1v * sb[j + 1]);
+      if (aux) *reinterpret_cast<float2 *>(aux + 64 * 64 + r * 64 + j) = make_float2(t0v, t1v);
     }
   }
 }

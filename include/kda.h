@@ -172,7 +172,12 @@ size_t kda_fwd_workspace_size(const kda_fwd_args *args);
 size_t kda_saved_size(const kda_fwd_args *args);
 
 /* kda_bwd -- gradients for q, k, v, beta, g and the initial state (the pages
- * report a matching backward kernel next to the forward one). */
+ * report a matching backward kernel next to the forward one). `fwd.saved` is the
+ * buffer a kda_fwd with the same inputs filled. bf16 I/O runs on the tensor cores
+ * (bf16 operands, fp32 accumulation; within 1e-2 of the exact gradients); fp32 I/O
+ * forms every product in fp32 on the CUDA cores (within 1e-4) and recomputes the
+ * chunk records, A and T in its workspace, which is therefore larger: about 260 KB
+ * per (chunk, head) against 32 KB for bf16. */
 kda_status kda_bwd(const kda_bwd_args *args, cudaStream_t stream);
 size_t kda_bwd_workspace_size(const kda_bwd_args *args);
 
@@ -399,9 +404,10 @@ kda_status kda_fwd_no_alloc(const kda_fwd_args *args, cudaStream_t stream);
 
 /* Per-kernel timing hook for benchmarks. When `events` is not NULL, every later
  * kda_fwd / kda_bwd / kda_step call records events[i] on its stream right after
- * enqueueing its i-th kernel (i < n_events): kda_fwd has 3 kernels (chunk table,
- * chunk prep, state scan), kda_bwd 3 (chunk table, reverse dS scan, chunk-local
- * gradients), kda_step 1. Elapsed times
+ * enqueueing its i-th stage (i < n_events): kda_fwd has 3 (chunk table, chunk prep,
+ * state scan), kda_bwd 3 (chunk table, reverse dS scan, chunk-local gradients; for
+ * fp32 I/O the second stage also re-runs the chunk prep and the third is two
+ * kernels), kda_step 1. Elapsed times
  * between consecutive events (and one the caller records before the call) give
  * each kernel's device time. The caller owns the events and the array, which
  * must stay valid until the hook is cleared with kda_set_profile_events(NULL, 0).

@@ -127,11 +127,17 @@ def test_workspace_sizes_scale_with_problem(lib):
     assert dsb <= lib.kda_bwd_workspace_size(C.byref(b)) <= dsb + 4 * 256 + 8 * (1 + 1) + 4096
 
 
-def test_bwd_fp32_is_reported_unsupported(lib):
+def test_bwd_fp32_workspace(lib):
+    # fp32: `saved` holds the chunk-start states only; the backward's workspace takes the chunk-end
+    # gradients dS, the recomputed records, A and T, and the per-chunk scratch of the chunk kernels
     from gated_delta_rule_chunked_gb300 import _lib
+    a = _fwd_args(total_tokens=4096, heads=8, io_dtype=_lib.KDA_F32)
+    n = (4096 // 64 + 1) * 8
+    assert n * 128 * 128 * 4 <= lib.kda_saved_size(C.byref(a)) <= n * 128 * 128 * 4 + 256
     b = _lib.BwdArgs()
-    b.fwd = _fwd_args(io_dtype=_lib.KDA_F32)
-    assert lib.kda_bwd(C.byref(b), None) == 2
+    b.fwd = a
+    per = 128 * 128 * 4 + (3 * 64 * 128 + 2 * 64 * 64) * 4 + 512 + 2 * 64 * 64 * 4 + (2 * 64 * 64 + 128) * 4
+    assert n * per <= lib.kda_bwd_workspace_size(C.byref(b)) <= n * per + 6 * 256 + 4096
 
 
 def test_step_validation(lib):

@@ -160,14 +160,26 @@ def test_bwd_bf16_ragged(kda, lens):
     check_bwd(kda, b, TOL["bf16"])
 
 
+@pytest.mark.parametrize("lens", [[64], [130], [200, 1, 64, 129]])
+def test_bwd_f32_ragged(kda, lens):
+    b = make_seq_batch(lens, heads=2, io_dtype="f32", seed=120 + sum(lens), h0=True, grad=True)
+    check_bwd(kda, b, TOL["f32"])
+
+
+def test_bwd_f32_workload_T512_H2(kda):
+    # the fp32 workload's inputs (one 512-token sequence, two heads, zero initial state), dO drawn after them
+    check_bwd(kda, make_workload("fwd-f32-T512-H2", kind="fwdbwd"), TOL["f32"])
+
+
 def test_bwd_many_heads(kda):
     b = make_seq_batch([150, 90], heads=96, io_dtype="bf16", seed=101, h0=True, grad=True)
     check_bwd(kda, b, TOL["bf16"], tasks=[(0, 0), (0, 57), (1, 95)])
 
 
-def test_bwd_zero_state_no_dhT_scaled(kda):
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_bwd_zero_state_no_dhT_scaled(kda, io):
     # h0 = 0 (not passed), no final-state gradient, q scale != 1: dh0 is still the gradient at h0 = 0
-    b = make_seq_batch([130, 64, 1], heads=2, io_dtype="bf16", seed=113, h0=False, grad=True)
+    b = make_seq_batch([130, 64, 1], heads=2, io_dtype=io, seed=113, h0=False, grad=True)
     assert b.h0 is None
     t = to_dev(b)
     sc = 128 ** -0.5
@@ -184,11 +196,12 @@ def test_bwd_zero_state_no_dhT_scaled(kda):
             got.append((g_[i, h] if name == "dh0" else g_[cu[i]:cu[i + 1], h]).numpy().ravel())
             ref.append(r[name].ravel())
         e = rel(np.concatenate(got), np.concatenate(ref))
-        assert e <= TOL["bf16"], (name, e)
+        assert e <= TOL[io], (name, e)
 
 
-def test_bwd_is_deterministic(kda):
-    b = make_seq_batch([300], heads=2, io_dtype="bf16", seed=102, h0=True, grad=True)
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_bwd_is_deterministic(kda, io):
+    b = make_seq_batch([300], heads=2, io_dtype=io, seed=102, h0=True, grad=True)
     t, o, hT, saved = run_fwd(kda, b, save=True)
     g1 = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, None, t["h0"])
     g2 = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, None, t["h0"])
@@ -239,6 +252,12 @@ def test_bwd_gates_at_bound_bf16(kda, kind):
     b = _strong_gates(make_seq_batch([200, 1, 64, 129], heads=3, io_dtype="bf16", seed=112, h0=True, grad=True),
                       kind, 9)
     check_bwd(kda, b, TOL["bf16"])
+
+
+@pytest.mark.parametrize("kind", ["const", "uniform", "mixed"])
+def test_bwd_gates_at_bound_f32(kda, kind):
+    b = _strong_gates(make_seq_batch([333, 64], heads=2, io_dtype="f32", seed=114, h0=True, grad=True), kind, 11)
+    check_bwd(kda, b, TOL["f32"])
 
 
 # ---------------------------------------------------------------- decode

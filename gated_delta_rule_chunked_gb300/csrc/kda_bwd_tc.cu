@@ -322,21 +322,33 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   // block's round epilogues run, the next block's dO, T and first S^T block are fetched into
   // the tiles the rounds no longer use.
   const long long nblk = (long long)p.geo.max_chunks * H;
+  // the chunk of the block this CTA runs next is looked up one block ahead (during the
+  // current block's products), so a block starts with its loads
+  ChunkRef cur;
+  bool have_cur = blockIdx.x < nblk && chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, (int)(blockIdx.x / H), cur);
   int it = 0;
-  for (long long blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
+  for (long long blk = blockIdx.x; have_cur; blk += gridDim.x, ++it) {
   const int h = (int)(blk % H), chunk = (int)(blk / H);
-  ChunkRef ref;
-  if (!chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, chunk, ref)) break;
+  const ChunkRef ref = cur;
   const uint32_t ph = (uint32_t)(it & 1);
   const bool pre = it > 0;   // the previous block prefetched this block's dO, T and S^T block 0
   const long long nb = blk + gridDim.x;   // the block this CTA runs next, if any
-  ChunkRef nr;
-  const bool have_next = nb < nblk && chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, (int)(nb / H), nr);
   const int nh = (int)(nb % H);
   const size_t nrid = (size_t)(nb / H) * H + nh;
   const size_t rid = (size_t)chunk * H + h;
 
   // ---------------------------------------------------------------- loads
+  // The gate rows first (thread = channel pair x sub-block, plain loads into registers) and this
+  // token's beta: their latency then overlaps the copy issue and the copies.
+  const int cp = tid & 63, a = tid >> 6, c0 = 2 * cp;
+  float2 csr[SUB];
+#pragma unroll
+  for (int i = 0; i < SUB; ++i) {
+    const int rr = a * SUB + i;
+    csr[i] = rr < ref.len ? *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + rr) * H + h) * D + c0)
+                          : make_float2(0.f, 0.f);
+  }
+  const float beta_t = tid < 64 && tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
   // bulk copies of the saved tiles and the record; TMA boxes of this chunk's V, dO, q, k rows
   // (rows past the tensor read as zero) and of T
   const int t0i = (int)ref.t0, arow = (int)rid * 128;
@@ -365,18 +377,9 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       tc::tma_load_2d(smem + S::TK + 8192, &p.tm_aux, 32, arow + 64, &bar[0]);
     }
   }
-  if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
-  // while the copies land: the gate scan (thread = channel pair x sub-block), from global memory;
-  // the local sums G_r - E_{a-1} (log2) stay in registers for the factor tiles
-  const int cp = tid & 63, a = tid >> 6, c0 = 2 * cp;
-  float2 csr[SUB];
+  // while the copies land: the gate scan; the local sums G_r - E_{a-1} (log2) stay in registers
+  // for the factor tiles
   {
-#pragma unroll
-    for (int i = 0; i < SUB; ++i) {
-      const int rr = a * SUB + i;
-      csr[i] = rr < ref.len ? *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + rr) * H + h) * D + c0)
-                            : make_float2(0.f, 0.f);
-    }
     float2 run = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < SUB; ++i) {
@@ -387,6 +390,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
     tot[a][c0] = run.x;
     tot[a][c0 + 1] = run.y;
   }
+  if (tid < 64) sb[tid] = beta_t;
   bool ok = mbar_wait(&bar[0], ph);
   if (pre) ok &= mbar_wait(&bar[10], (uint32_t)((it - 1) & 1));
   if (ref.len < CH && ok) {
@@ -425,6 +429,8 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       tc::mma_bf16(tmem + T_DQ, mnmaj(s_ss, ks, 16384), kmaj(s_do, ks, 8192), tc::idesc_bf16_mn(128, 64, true, false), ks > 0);
     tc::commit(&bar[1]);
   }
+  ChunkRef nr;
+  const bool have_next = nb < nblk && chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, (int)(nb / H), nr);
   {
     // gate factors: E_{a-1}, E_3 per channel; pair factors D_ab, P_a, F_a
     float em[2] = {0.f, 0.f}, e3[2] = {0.f, 0.f}, eb[2] = {0.f, 0.f};
@@ -855,6 +861,8 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   tc::fence_before();
   __syncthreads();   // every tile of this block is consumed
   tc::fence_after();
+  cur = nr;
+  have_cur = have_next;
   }
   tc::fence_before();
   __syncthreads();

@@ -98,6 +98,15 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
   }
 }
 
+// 2^x by the hardware approximation (relative error about 2^-22), results below 2^-126 flushed to
+// zero: every gating factor here is at most 1 and multiplies O(1) values. The round epilogues and
+// the Kh sum both form their factors with it, so the two agree to the last bit.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Warp-collective: 8 consecutive fp32 columns of TMEM lane (lane base + thread).
 __device__ __forceinline__ void ld8(uint32_t taddr, float (&v)[8]) {
   uint32_t r[8];
@@ -128,8 +137,11 @@ struct RoundCtx {
 
 // Epilogue of round t (rows 16t..16t+15): this thread has channel c and rows 16t + 8 hf + i.
 // One copy of the code for all four rounds (t is a run-time value): the kernel is long and
-// runs one CTA per SM, so its instruction footprint matters.
-__device__ __forceinline__ void round_epilogue(RoundCtx &x, const int t, uint32_t base) {
+// runs one CTA per SM, so its instruction footprint matters. `after_read` runs right after the
+// CTA barrier that follows every thread's tensor-memory reads (it issues the round that reuses
+// this buffer).
+template <class AfterRead>
+__device__ __forceinline__ void round_epilogue(RoundCtx &x, const int t, uint32_t base, AfterRead after_read) {
   using S = BcSmem;
   const BwdChunkParams &p = *x.p;
   const int c = x.c, hf = x.hf;
@@ -196,7 +208,7 @@ __device__ __forceinline__ void round_epilogue(RoundCtx &x, const int t, uint32_
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = 16 * t + 8 * hf + i;
-    const float xx = exp2f(csv[i]), yy = exp2f(tt - csv[i]);
+    const float xx = ex2(csv[i]), yy = ex2(tt - csv[i]);
     const float qh = qv[i] * rq0[r], kh = kv[i] * rk[r];
     const float ql = p.scale * qh * xx, kl = kh * xx, rr = kh * yy;
     const float dQL = fmaf(gq[i], pa, tq[i]), dKL = fmaf(-gk[i], pa, tk[i]), dR = fmaf(gh[i], fa, tw[i]);
@@ -270,7 +282,10 @@ __device__ __forceinline__ void round_epilogue(RoundCtx &x, const int t, uint32_
     sdg += dG[i];
   }
   xs[hf * 128 + c] = sdg;
-  __syncthreads();
+  tc::fence_before();
+  __syncthreads();   // the half sums are in place and every thread's reads of this buffer are done
+  tc::fence_after();
+  after_read();
   const float other = xs[(1 - hf) * 128 + c];
   float acc = x.run + (hf ? 0.f : other);
 #pragma unroll
@@ -729,7 +744,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       const float2 run = csr[i];
       *reinterpret_cast<float2 *>(smem + (r < 32 ? S::CSA + r * 512 : S::CSB + (r - 32) * 512) + c0 * 4) = run;
       const float2 qf = ld2(sq_ + r * D + c0), kf = ld2(sk_ + r * D + c0);
-      const float x0 = exp2f(run.x), x1 = exp2f(run.y), y0 = exp2f(ta0 - run.x), y1 = exp2f(ta1 - run.y);
+      const float x0 = ex2(run.x), x1 = ex2(run.y), y0 = ex2(ta0 - run.x), y1 = ex2(ta1 - run.y);
       const float qs = p.scale * rq0[r], ks_ = rk[r];
       const uint32_t o = tc::sw128_off(64, r, c0);
       st2((bf16 *)(smem + S::QLF + o), qf.x * qs * x0, qf.y * qs * x1);
@@ -833,7 +848,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int r = 32 * hf + i, t = r >> 4;
-      const float kh = to_f(sk_[r * D + row]) * rk[r], yy = exp2f(tot[t][row] - csb[i * 128]);
+      const float kh = to_f(sk_[r * D + row]) * rk[r], yy = ex2(tot[t][row] - csb[i * 128]);
       cs += v[i] * fv[t][row] * (kh * yy);
     }
     reinterpret_cast<float *>(smem + S::CSUM)[hf * 128 + row] = cs;
@@ -849,14 +864,12 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       const float *cs2 = reinterpret_cast<const float *>(smem + S::CSUM);
       rc.run = reinterpret_cast<const float *>(smem + S::TAIL)[row] + (cs2[row] + cs2[128 + row]);
     }
-    round_epilogue(rc, NSUB - 1 - idx, base);
-    tc::fence_before();
-    __syncthreads();   // this buffer is read out
-    tc::fence_after();
-    if (tid == 0 && idx < 2) {
-      issue_round(1 - idx, base);
-      tc::commit(&bar[7 + idx]);
-    }
+    round_epilogue(rc, NSUB - 1 - idx, base, [&]() {
+      if (tid == 0 && idx < 2) {   // the round after next into this buffer
+        issue_round(1 - idx, base);
+        tc::commit(&bar[7 + idx]);
+      }
+    });
   }
   tc::fence_before();
   __syncthreads();   // every tile of this block is consumed

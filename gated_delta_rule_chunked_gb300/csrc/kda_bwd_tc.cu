@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   float(*dvp)[128] = (float(*)[128])(smem + S::DV);
 
   if (tid == 0) {
-    for (int i = 0; i < 11; ++i) mbar_init(&bar[i], 1);
+    // groups A-C and the rounds are issued by two threads (one commit each), the rest by one
+    for (int i = 0; i < 11; ++i) mbar_init(&bar[i], (i >= 1 && i <= 3) || (i >= 5 && i <= 8) ? 2 : 1);
     fence_mbar_init();
   }
   if (warp == 0) tc::alloc(tslot, 512);
@@ -429,19 +430,24 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
                  s_do = smem_u32(smem + S::DO);
 
   // ---------------------------------------------------------------- group A
+  // Every MMA costs its issuing thread about 50 cycles whatever its size, so each group's
+  // independent accumulator chains are split between two threads in different warps (0 and 32),
+  // each committing once to the group's barrier (two arrivals).
   if (tid == 0) {
     // (Kt S)^T [v][j] = S^T Kt^T; V'^T = V^T - (Kt S)^T in the epilogue
     for (int ks = 0; ks < 8; ++ks)
       tc::mma_bf16(tmem + T_VP, kmaj(s_ss, ks, 16384), kmaj(s_kt, ks, 8192), tc::idesc_bf16(128, 64), ks > 0);
+    // dQt^T [k][r] = S dO^T: A = S (k rows) MN-major over S^T, B = dO [r][v] K-major
+    for (int ks = 0; ks < 8; ++ks)
+      tc::mma_bf16(tmem + T_DQ, mnmaj(s_ss, ks, 16384), kmaj(s_do, ks, 8192), tc::idesc_bf16_mn(128, 64, true, false), ks > 0);
+    tc::commit(&bar[1]);
+  } else if (tid == 32) {
     // dU^T [v][j] = dO^T Bm + dS^T Kh^T: B(n = j, k = r) = Bm[r][j] and B(n = j, k = dk) = Kh^T[dk][j],
     // both rows k of the record's tiles -> MN-major
     for (int ks = 0; ks < 4; ++ks)
       tc::mma_bf16(tmem + T_DU, mnmaj(s_do, ks, 8192), mnmaj(s_bm, ks, 8192), tc::idesc_bf16_mn(128, 64, true, true), ks > 0);
     for (int ks = 0; ks < 8; ++ks)
       tc::mma_bf16(tmem + T_DU, kmaj(s_sds, ks, 16384), mnmaj(s_kht, ks, 8192), tc::idesc_bf16_mn(128, 64, false, true), 1);
-    // dQt^T [k][r] = S dO^T: A = S (k rows) MN-major over S^T, B = dO [r][v] K-major
-    for (int ks = 0; ks < 8; ++ks)
-      tc::mma_bf16(tmem + T_DQ, mnmaj(s_ss, ks, 16384), kmaj(s_do, ks, 8192), tc::idesc_bf16_mn(128, 64, true, false), ks > 0);
     tc::commit(&bar[1]);
   }
   ChunkRef nr;
@@ -573,6 +579,8 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
     // dV'^T [v][j] = dU^T Tb: B(n = j, k = r) = Tb[r][j] -> MN-major
     for (int ks = 0; ks < 4; ++ks)
       tc::mma_bf16(tmem + T_DV, kmaj(s_dut, ks, 0), mnmaj(s_tb, ks, 8192), tc::idesc_bf16_mn(128, 64, false, true), ks > 0);
+    tc::commit(&bar[2]);
+  } else if (tid == 32) {
     // dTb [r][j] = dU V'^T (M = 64): A(m = r, k = v) = dU^T tile[v][r], B(n = j, k = v) = V'^T tile[v][j]
     for (int ks = 0; ks < 8; ++ks)
       tc::mma_bf16(tmem + T_DTB, mnmaj(s_dut, ks, 8192), mnmaj(s_vpt, ks, 8192), tc::idesc_bf16_mn(64, 64, true, true), ks > 0);
@@ -655,6 +663,8 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
     // dKh^T [k][r] = dS U^T: A = dS (k rows) MN-major over dS^T, B(n = r, k = v) = U^T tile[v][r] MN-major
     for (int ks = 0; ks < 8; ++ks)
       tc::mma_bf16(tmem + T_DKH, mnmaj(s_sds, ks, 16384), mnmaj(s_ut, ks, 8192), tc::idesc_bf16_mn(128, 64, true, true), ks > 0);
+    tc::commit(&bar[3]);
+  } else if (tid == 32) {
     // S dV'^T [k][r] = -dKt^T: A = S (k rows) MN-major over S^T, B(n = r, k = v) = dV'^T tile[v][r] MN-major
     for (int ks = 0; ks < 8; ++ks)
       tc::mma_bf16(tmem + T_DKT, mnmaj(s_ss, ks, 16384), mnmaj(s_dvt, ks, 8192), tc::idesc_bf16_mn(128, 64, true, true), ks > 0);
@@ -810,27 +820,26 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   // ---------------------------------------------------------------- rounds (intra-chunk gradients)
   // Round t: P_tb = R_b^T dBm_tb^T, Q_tb = R_b^T dA_tb^T (b <= t), W_at = QL_a^T dBm_at + KL_a^T dA_at
   // (a >= t); M = 128 channels, N = K = 16. Rounds run t = 3, 2, 1, 0 (the dg suffix order) in two
-  // TMEM buffers, the next but one issued as soon as a buffer is read out.
+  // TMEM buffers, the next but one issued as soon as a buffer is read out. Two threads issue each
+  // round: part 0 the P products and the W sums of even a - t, part 1 the Q products and the rest.
   const uint32_t s_rf = smem_u32(smem + S::RF), s_qlf = smem_u32(smem + S::QLF), s_klf = smem_u32(smem + S::KLF),
                  s_dbm = smem_u32(smem + S::DBM), s_dbmt = smem_u32(smem + S::DBMT), s_da = smem_u32(smem + S::DA),
                  s_dat = smem_u32(smem + S::DAT);
-  auto issue_round = [&](int t, uint32_t base) {
+  auto issue_round = [&](int t, uint32_t base, int part) {
     const uint32_t idn = tc::idesc_bf16_mn(128, 16, true, false);
-    for (int b = 0; b <= t; ++b) {
-      const uint64_t ar = mnmaj(s_rf, b, 8192);
-      tc::mma_bf16(tmem + base + 16 * b, ar, tc::desc_sw128(s_dbm + 2048 * t + 32 * b), idn, 0);
-      tc::mma_bf16(tmem + base + 16 * (t + 1) + 16 * b, ar, tc::desc_sw128(s_da + 2048 * t + 32 * b), idn, 0);
-    }
-    for (int aa = t; aa < NSUB; ++aa) {
+    const uint32_t s_bb = part ? s_da : s_dbm, off = part ? 16 * (t + 1) : 0;
+    for (int b = 0; b <= t; ++b)
+      tc::mma_bf16(tmem + base + off + 16 * b, mnmaj(s_rf, b, 8192), tc::desc_sw128(s_bb + 2048 * t + 32 * b), idn, 0);
+    for (int aa = t + part; aa < NSUB; aa += 2) {
       const uint32_t col = base + 32 * (t + 1) + 16 * (aa - t);
       tc::mma_bf16(tmem + col, mnmaj(s_qlf, aa, 8192), tc::desc_sw128(s_dbmt + 2048 * t + 32 * aa), idn, 0);
       tc::mma_bf16(tmem + col, mnmaj(s_klf, aa, 8192), tc::desc_sw128(s_dat + 2048 * t + 32 * aa), idn, 1);
     }
   };
-  if (tid == 0) {
-    issue_round(3, T_R0);
+  if (tid == 0 || tid == 32) {
+    issue_round(3, T_R0, tid >> 5);
     tc::commit(&bar[5]);
-    issue_round(2, T_R1);
+    issue_round(2, T_R1, tid >> 5);
     tc::commit(&bar[6]);
   }
   RoundCtx rc{&p, &ref, smem, tl, row, hf, qw, lane, h, 0.f};
@@ -865,8 +874,8 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       rc.run = reinterpret_cast<const float *>(smem + S::TAIL)[row] + (cs2[row] + cs2[128 + row]);
     }
     round_epilogue(rc, NSUB - 1 - idx, base, [&]() {
-      if (tid == 0 && idx < 2) {   // the round after next into this buffer
-        issue_round(1 - idx, base);
+      if ((tid == 0 || tid == 32) && idx < 2) {   // the round after next into this buffer
+        issue_round(1 - idx, base, tid >> 5);
         tc::commit(&bar[7 + idx]);
       }
     });

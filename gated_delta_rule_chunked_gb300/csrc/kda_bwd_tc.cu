@@ -77,8 +77,8 @@ struct BcSmem {
   static constexpr int XT = SS;                        // X^T [j][m] fp32 K-major (group D)
   static constexpr int AS = DO;                        // A fp32 [64][64] in the layout of T (group D)
   static constexpr int CSA = SS + 16384, CSB = KHT;    // local gate sums (log2) of rows 0..31, 32..63: [32][128] fp32
-  static constexpr int DBM = BM, DBMT = TB;            // dBm [r][j], dBm^T [j][r] bf16 (rounds)
-  static constexpr int DA = V, DAT = V + 8192;         // dA [r][j], dA^T [j][r] bf16 (rounds)
+  static constexpr int DBM = BM;                       // dBm [r][j] bf16 (rounds; read K-major and MN-major)
+  static constexpr int DA = V;                         // dA [r][j] bf16 (rounds; read K-major and MN-major)
   static constexpr int QLF = SDS, KLF = SDS + 16384, RF = KT;   // factor tiles [r][c] bf16 (rounds)
 };
 
@@ -706,10 +706,6 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
           if (j == r64) diag = v[8 * cb + e];
         }
         *reinterpret_cast<uint4 *>(smem + S::DBM + tc::sw128_off(64, r64, 32 * hf + 8 * cb)) = tc::pack8(x8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          *reinterpret_cast<bf16 *>(smem + S::DBMT + tc::sw128_off(64, 32 * hf + 8 * cb + e, r64)) =
-              __float2bfloat16_rn(x8[e]);
       }
       if ((r64 >> 5) == hf) reinterpret_cast<float *>(smem + S::DBD)[r64] = diag;
     }
@@ -788,9 +784,6 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
           x8[e] = br * dl;
         }
         *reinterpret_cast<uint4 *>(smem + S::DA + tc::sw128_off(64, r64, j0)) = tc::pack8(x8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          *reinterpret_cast<bf16 *>(smem + S::DAT + tc::sw128_off(64, j0 + e, r64)) = __float2bfloat16_rn(x8[e]);
       }
       db2[hf * 64 + r64] = part;
     }
@@ -823,17 +816,17 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   // TMEM buffers, the next but one issued as soon as a buffer is read out. Two threads issue each
   // round: part 0 the P products and the W sums of even a - t, part 1 the Q products and the rest.
   const uint32_t s_rf = smem_u32(smem + S::RF), s_qlf = smem_u32(smem + S::QLF), s_klf = smem_u32(smem + S::KLF),
-                 s_dbm = smem_u32(smem + S::DBM), s_dbmt = smem_u32(smem + S::DBMT), s_da = smem_u32(smem + S::DA),
-                 s_dat = smem_u32(smem + S::DAT);
+                 s_dbm = smem_u32(smem + S::DBM), s_da = smem_u32(smem + S::DA);
   auto issue_round = [&](int t, uint32_t base, int part) {
-    const uint32_t idn = tc::idesc_bf16_mn(128, 16, true, false);
+    const uint32_t idn = tc::idesc_bf16_mn(128, 16, true, false), idw = tc::idesc_bf16_mn(128, 16, true, true);
     const uint32_t s_bb = part ? s_da : s_dbm, off = part ? 16 * (t + 1) : 0;
     for (int b = 0; b <= t; ++b)
       tc::mma_bf16(tmem + base + off + 16 * b, mnmaj(s_rf, b, 8192), tc::desc_sw128(s_bb + 2048 * t + 32 * b), idn, 0);
     for (int aa = t + part; aa < NSUB; aa += 2) {
       const uint32_t col = base + 32 * (t + 1) + 16 * (aa - t);
-      tc::mma_bf16(tmem + col, mnmaj(s_qlf, aa, 8192), tc::desc_sw128(s_dbmt + 2048 * t + 32 * aa), idn, 0);
-      tc::mma_bf16(tmem + col, mnmaj(s_klf, aa, 8192), tc::desc_sw128(s_dat + 2048 * t + 32 * aa), idn, 1);
+      // B(n = j in block t, k = r in block a) = dBm[r][j]: the rows r of the dBm (dA) tile, read MN-major
+      tc::mma_bf16(tmem + col, mnmaj(s_qlf, aa, 8192), tc::desc_sw128_mn(s_dbm + 2048 * aa + 32 * t, 8192), idw, 0);
+      tc::mma_bf16(tmem + col, mnmaj(s_klf, aa, 8192), tc::desc_sw128_mn(s_da + 2048 * aa + 32 * t, 8192), idw, 1);
     }
   };
   if (tid == 0 || tid == 32) {

@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   const int h = (int)(blk % H), chunk = (int)(blk / H);
   const ChunkRef ref = cur;
   const uint32_t ph = (uint32_t)(it & 1);
-  const bool pre = it > 0;   // the previous block prefetched this block's dO, T and S^T block 0
+  const bool pre = it > 0;   // the previous block prefetched this block's dO, T, S^T block 0 and Tb
   const long long nb = blk + gridDim.x;   // the block this CTA runs next, if any
   const int nh = (int)(nb % H);
   const size_t nrid = (size_t)(nb / H) * H + nh;
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   if (tid == 0) {
     const char *rb = (const char *)p.img + rid * TcRec::BYTES;
     fence_proxy_async();
-    mbar_expect_tx(&bar[0], (pre ? 16384 : 32768) + 32768 + (TcRec::TB - TcRec::B2) + (TcRec::BYTES - TcRec::TB) +
+    mbar_expect_tx(&bar[0], (pre ? 16384 : 32768) + 32768 + (TcRec::TB - TcRec::B2) + (pre ? 0 : TcRec::BYTES - TcRec::TB) +
                                 KtRec::BYTES + (pre ? 3 : 5) * 16384);
     if (pre)
       bulk_g2s(smem + S::SS + 16384, (const char *)p.saved + rid * 32768 + 16384, 16384, &bar[0]);
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       bulk_g2s(smem + S::SS, (const char *)p.saved + rid * 32768, 32768, &bar[0]);
     bulk_g2s(smem + S::SDS, (const char *)p.dsaved + rid * 32768, 32768, &bar[0]);
     bulk_g2s(smem + S::KHT, rb + TcRec::B2, TcRec::TB - TcRec::B2, &bar[0]);        // Kh^T, Bm
-    bulk_g2s(smem + S::TB, rb + TcRec::TB, TcRec::BYTES - TcRec::TB, &bar[0]);      // Tb, e^{G_last}
+    if (!pre) bulk_g2s(smem + S::TB, rb + TcRec::TB, TcRec::BYTES - TcRec::TB, &bar[0]);   // Tb, e^{G_last}
     bulk_g2s(smem + S::KT, (const char *)p.kt + rid * KtRec::BYTES, KtRec::BYTES, &bar[0]);   // Kt
     tc::tma_load_3d(smem + S::V, &p.tm_v, 0, h, t0i, &bar[0]);
     if (!pre) {
@@ -792,12 +792,13 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   tc::fence_before();
   if (!__syncthreads_and(ok)) return fail_out();
   tc::fence_after();
-  {   // the next block's dO, T and S^T block 0 into the dO/A, T and X^T tiles, free from here on
+  {   // the next block's dO, T, S^T block 0 and Tb into the dO/A, T, X^T and dT tiles, free from here on
     if (tid == 32 && have_next) {
       const int nt0 = (int)nr.t0, narow = (int)nrid * 128;
       fence_proxy_async();
-      mbar_expect_tx(&bar[10], 3 * 16384);
+      mbar_expect_tx(&bar[10], 3 * 16384 + (TcRec::BYTES - TcRec::TB));
       bulk_g2s(smem + S::SS, (const char *)p.saved + nrid * 32768, 16384, &bar[10]);
+      bulk_g2s(smem + S::TB, (const char *)p.img + nrid * TcRec::BYTES + TcRec::TB, TcRec::BYTES - TcRec::TB, &bar[10]);
       tc::tma_load_3d(smem + S::DO, &p.tm_do, 0, nh, nt0, &bar[10]);
       tc::tma_load_3d(smem + S::DO + 8192, &p.tm_do, 64, nh, nt0, &bar[10]);
       tc::tma_load_2d(smem + S::TK, &p.tm_aux, 0, narow + 64, &bar[10]);

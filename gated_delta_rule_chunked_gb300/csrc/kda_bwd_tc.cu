@@ -354,17 +354,10 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
   const size_t rid = (size_t)chunk * H + h;
 
   // ---------------------------------------------------------------- loads
-  // The gate rows first (thread = channel pair x sub-block, plain loads into registers) and this
-  // token's beta: their latency then overlaps the copy issue and the copies.
-  const int cp = tid & 63, a = tid >> 6, c0 = 2 * cp;
-  float2 csr[SUB];
-#pragma unroll
-  for (int i = 0; i < SUB; ++i) {
-    const int rr = a * SUB + i;
-    csr[i] = rr < ref.len ? *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + rr) * H + h) * D + c0)
-                          : make_float2(0.f, 0.f);
-  }
-  const float beta_t = tid < 64 && tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
+  // Thread 0 issues the block's copies first; every thread then loads its gate rows (thread =
+  // channel pair x sub-block, plain loads into registers) and this token's beta, whose latency
+  // overlaps the copies. (The plain loads queue behind the previous block's gradient stores, so
+  // issuing them before the copies would hold the copies back.)
   // bulk copies of the saved tiles and the record; TMA boxes of this chunk's V, dO, q, k rows
   // (rows past the tensor read as zero) and of T
   const int t0i = (int)ref.t0, arow = (int)rid * 128;
@@ -393,6 +386,15 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       tc::tma_load_2d(smem + S::TK + 8192, &p.tm_aux, 32, arow + 64, &bar[0]);
     }
   }
+  const int cp = tid & 63, a = tid >> 6, c0 = 2 * cp;
+  float2 csr[SUB];
+#pragma unroll
+  for (int i = 0; i < SUB; ++i) {
+    const int rr = a * SUB + i;
+    csr[i] = rr < ref.len ? *reinterpret_cast<const float2 *>(p.g + ((size_t)(ref.t0 + rr) * H + h) * D + c0)
+                          : make_float2(0.f, 0.f);
+  }
+  const float beta_t = tid < 64 && tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
   // while the copies land: the gate scan; the local sums G_r - E_{a-1} (log2) stay in registers
   // for the factor tiles
   {

@@ -670,10 +670,11 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
     // S dV'^T [k][r] = -dKt^T: A = S (k rows) MN-major over S^T, B(n = r, k = v) = dV'^T tile[v][r] MN-major
     for (int ks = 0; ks < 8; ++ks)
       tc::mma_bf16(tmem + T_DKT, mnmaj(s_ss, ks, 16384), mnmaj(s_dvt, ks, 8192), tc::idesc_bf16_mn(128, 64, true, true), ks > 0);
-    // X [r][m] = dT T^T (M = 64, tf32): A = dT [r][j], B = T [m][j], both K-major
+    // X = dT T^T (tf32), formed transposed so each TMEM lane holds a row of the X^T operand tile:
+    // X^T [m][r] = T dT^T, A = T [m][j], B = dT [r][j], both K-major (M = N = 64)
     const uint32_t s_dt = smem_u32(smem + S::DT0), s_tk = smem_u32(smem + S::TK);
     for (int ks = 0; ks < 8; ++ks)
-      tc::mma_tf32(tmem + T_X, kmaj(s_dt, ks, (uint32_t)(S::DT1 - S::DT0)), kmaj(s_tk, ks, 8192), tc::idesc_tf32(64, 64), ks > 0);
+      tc::mma_tf32(tmem + T_X, kmaj(s_tk, ks, 8192), kmaj(s_dt, ks, (uint32_t)(S::DT1 - S::DT0)), tc::idesc_tf32(64, 64), ks > 0);
     tc::commit(&bar[3]);
   }
   ok = __all_sync(0xffffffffu, mbar_wait(&bar[3], ph));
@@ -711,13 +712,14 @@ __global__ void __launch_bounds__(BC_THREADS, 1) kda_bwd_chunk_tc_kernel(const _
       }
       if ((r64 >> 5) == hf) reinterpret_cast<float *>(smem + S::DBD)[r64] = diag;
     }
-    // X -> X^T [j][m] (fp32 K-major over m) over the dead S^T tile
+    // X^T [j][m] (fp32 K-major over m) over the dead S^T tile, row by row
     ld32(tl + T_X + 32 * hf, v);
     tc::wait_ld();
     if (lane < 16) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        *reinterpret_cast<float *>(smem + S::XT + tc::sw128_off32(64, 32 * hf + i, r64)) = v[i];
+      for (int q4 = 0; q4 < 8; ++q4)
+        *reinterpret_cast<float4 *>(smem + S::XT + tc::sw128_off32(64, r64, 32 * hf + 4 * q4)) =
+            make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
     }
   }
   if (!__syncthreads_and(ok)) return fail_out();

@@ -171,9 +171,10 @@ def test_bwd_f32_workload_T512_H2(kda):
     check_bwd(kda, make_workload("fwd-f32-T512-H2", kind="fwdbwd"), TOL["f32"])
 
 
-def test_bwd_many_heads(kda):
-    b = make_seq_batch([150, 90], heads=96, io_dtype="bf16", seed=101, h0=True, grad=True)
-    check_bwd(kda, b, TOL["bf16"], tasks=[(0, 0), (0, 57), (1, 95)])
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_bwd_many_heads(kda, io):
+    b = make_seq_batch([150, 90], heads=96, io_dtype=io, seed=101, h0=True, grad=True)
+    check_bwd(kda, b, TOL[io], tasks=[(0, 0), (0, 57), (1, 95)])
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])
@@ -209,13 +210,16 @@ def test_bwd_is_deterministic(kda, io):
         assert torch.equal(g1[name], g2[name]), name
 
 
-def test_bwd_into_caller_buffers(kda):
-    # out= writes the same gradients into the caller's tensors (reused across calls)
-    b = make_seq_batch([300], heads=2, io_dtype="bf16", seed=103, h0=True, grad=True)
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_bwd_into_caller_buffers(kda, io):
+    # out= writes the same gradients into the caller's tensors (reused across calls); the tensors
+    # start as NaN, so a kernel that read an output before writing it would show (the fp32 path
+    # keeps intermediates in dq, dk and dg between its two chunk kernels)
+    b = make_seq_batch([300, 77], heads=2, io_dtype=io, seed=103, h0=True, grad=True)
     t, o, hT, saved = run_fwd(kda, b, save=True)
-    g1 = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, None, t["h0"])
+    g1 = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, t["cu_seqlens"], t["h0"])
     out = {n: torch.full_like(v, float("nan")) for n, v in g1.items() if v is not None}
-    g2 = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, None, t["h0"], out=out)
+    g2 = kda.kda_bwd(t["q"], t["k"], t["v"], t["beta"], t["g"], t["dO"], saved, t["cu_seqlens"], t["h0"], out=out)
     for name in out:
         assert g2[name].data_ptr() == out[name].data_ptr(), name
         assert torch.equal(g1[name], out[name]), name

@@ -172,6 +172,14 @@ def test_bwd_f32_workload_T512_H2(kda):
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_bwd_empty_sequences(kda, io):
+    # empty sequences between and around non-empty ones: their dh0 is dhT (nothing to pass back through)
+    b = make_seq_batch([0, 70, 0, 65, 0], heads=2, io_dtype=io, seed=115, h0=True, grad=True)
+    errs = check_bwd(kda, b, TOL[io])
+    assert all(v <= TOL[io] for v in errs.values())
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
 def test_bwd_many_heads(kda, io):
     b = make_seq_batch([150, 90], heads=96, io_dtype=io, seed=101, h0=True, grad=True)
     check_bwd(kda, b, TOL[io], tasks=[(0, 0), (0, 57), (1, 95)])

@@ -260,11 +260,12 @@ def bench_range(args, lib, dev, stream, peaks, status):
     line alternates two resident input sets per timed step."""
     import torch
     res = {}
+    want = set(x for x in args.range_lines.split(",") if x)
     for name, mode, key in (("fwd-bf16-T4096-H96", "fwd", "fwd_T4096"),
                             ("fwdbwd-bf16-T32768-H96", "fwd", "fwd_T32768_inference"),
                             ("fwdbwd-bf16-varlen8-T131072-H96", "fwdbwd", "fwdbwd_varlen8_T131072"),
                             ("fwdbwd-bf16-T131072-H96", "fwdbwd", "fwdbwd_T131072")):
-        if args.seq_len and "131072" in name:
+        if (args.seq_len and "131072" in name) or (want and key not in want):
             continue
         case = ChunkedCase(lib, dev, name, mode, status, seq_len=args.seq_len if "T32768" in name else 0)
         K = max(3, min(args.steps, 20 if case.T <= 32768 else 5))
@@ -283,6 +284,8 @@ def bench_range(args, lib, dev, stream, peaks, status):
         del case
         torch.cuda.empty_cache()
     # fp32 I/O fwd + bwd: the fp32 workload's recipe at 4096 tokens x 96 heads
+    if want and "fwdbwd_f32_T4096" not in want:
+        return res
     case = ChunkedCase(lib, dev, "fwd-f32-T512-H2", "fwdbwd", status,
                        over={"kind": "fwdbwd", "seq_lens": (4096,), "heads": 96})
     K = max(3, min(args.steps, 10))
@@ -771,6 +774,9 @@ def main():
     ap.add_argument("--no-conv", action="store_true", help="skip the short-convolution workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-range", action="store_true", help="skip the 4K / inference / 128K / varlen lines")
+    ap.add_argument("--range-lines", default="", help="comma-separated keys of the range lines to run "
+                    "(fwd_T4096, fwd_T32768_inference, fwdbwd_varlen8_T131072, fwdbwd_T131072, fwdbwd_f32_T4096; "
+                    "default all; profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=16384)
     ap.add_argument("--ref-sample-tokens", type=int, default=2048)

@@ -167,18 +167,16 @@ kda_status check_fwd(const kda_fwd_args *a, const char *who) {
     return fail(KDA_ERR_INVALID_ARG, "%s: cu_seqlens must be 4-byte aligned", who);
   const void *need[] = {a->q, a->k, a->v, a->g, a->o};
   const char *names[] = {"q", "k", "v", "g", "o"};
-  // v and o may be NULL (zero values / no output) in a bf16 forward that saves nothing
-  const bool vo_optional = a->io_dtype == KDA_BF16 && !a->saved;
+  // v and o may be NULL (zero values / no output) in a forward that saves nothing
+  const bool vo_optional = !a->saved;
   for (int i = 0; i < 5; ++i) {
     const bool optional = vo_optional && (i == 2 || i == 4);
     if (!need[i] && a->total_tokens > 0 && !optional)
       return fail(KDA_ERR_INVALID_ARG, "%s: required pointer is NULL", names[i]);
     if (!aligned(need[i], 16)) return fail(KDA_ERR_INVALID_ARG, "%s: pointer is not 16-byte aligned", names[i]);
   }
-  if (a->h0_identity && a->io_dtype != KDA_BF16)
-    return fail(KDA_ERR_UNSUPPORTED, "%s: h0_identity needs io_dtype KDA_BF16", who);
-  if (a->skip_prep && (a->io_dtype != KDA_BF16 || a->saved))
-    return fail(KDA_ERR_UNSUPPORTED, "%s: skip_prep needs io_dtype KDA_BF16 and no saved", who);
+  if (a->skip_prep && a->saved)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: skip_prep needs no saved", who);
   if (!a->beta && a->total_tokens > 0) return fail(KDA_ERR_INVALID_ARG, "%s: beta is NULL", who);
   if (!aligned(a->beta, 4)) return fail(KDA_ERR_INVALID_ARG, "%s: beta is not 4-byte aligned", who);
   const void *opt[] = {a->h0, a->hT, a->saved, a->workspace};
@@ -747,9 +745,8 @@ kda_status check_cp(const kda_fwd_cp_args *c, const char *who) {
   f.workspace_bytes = 0;
   kda_status st = check_fwd(&f, who);
   if (st != KDA_OK) return st;
-  if (c->fwd.io_dtype != KDA_BF16 || c->fwd.saved || c->fwd.h0_identity || c->fwd.skip_prep || c->fwd.debug_starve)
-    return fail(KDA_ERR_UNSUPPORTED, "%s: needs io_dtype KDA_BF16, no saved, h0_identity = skip_prep = debug_starve = 0",
-                who);
+  if (c->fwd.saved || c->fwd.h0_identity || c->fwd.skip_prep || c->fwd.debug_starve)
+    return fail(KDA_ERR_UNSUPPORTED, "%s: needs no saved and h0_identity = skip_prep = debug_starve = 0", who);
   if (c->n_segments < 1 || (long long)c->n_segments * c->fwd.n_seqs > 0x7fffffffLL / 64)
     return fail(KDA_ERR_INVALID_ARG, "%s: need n_segments >= 1 (and n_seqs * n_segments < 2^25)", who);
   if (c->fwd.total_tokens > 0 && (!c->fwd.v || !c->fwd.o))

@@ -84,8 +84,8 @@ __global__ void __launch_bounds__(128 * NG, 1) kda_fwd_scan_kernel(FwdScanParams
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int r = 16 * warp + g8 + 8 * hh;
-        vf[nt][hh] = make_float2(0.f, 0.f);
-        if (r < clen) vf[nt][hh] = ld2(v + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + 8 * nt + 2 * q4);
+        vf[nt][hh] = make_float2(0.f, 0.f);   // v == NULL: zero values
+        if (r < clen && v) vf[nt][hh] = ld2(v + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + 8 * nt + 2 * q4);
       }
   };
 
@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(128 * NG, 1) kda_fwd_scan_kernel(FwdScanParams
       for (int hh = 0; hh < 2; ++hh) {
         const int c = 32 * warp + 16 * mt + g8 + 8 * hh, vv = z * DVS + 8 * nt + 2 * q4;
         float2 x = make_float2(0.f, 0.f);
-        if (p.h0) x = *reinterpret_cast<const float2 *>(p.h0 + (((size_t)seq * H + h) * 128 + c) * 128 + vv);
+        if (p.h0_identity) x = make_float2(c == vv ? 1.f : 0.f, c == vv + 1 ? 1.f : 0.f);
+        else if (p.h0) x = *reinterpret_cast<const float2 *>(p.h0 + (((size_t)seq * H + h) * 128 + c) * 128 + vv);
         accS[mt][nt][2 * hh] = x.x;
         accS[mt][nt][2 * hh + 1] = x.y;
         st2(sS.at(c, 8 * nt + 2 * q4), x.x, x.y);
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(128 * NG, 1) kda_fwd_scan_kernel(FwdScanParams
       constexpr int EPC = 16 / sizeof(E), CPR = DVS / EPC;
       for (int idx = tid & 127; idx < 64 * CPR; idx += 128) {
         const int r = idx / CPR, ch = idx % CPR;
-        if (r < clen)
+        if (r < clen && o)   // o == NULL: no outputs
           *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + r) * H + h) * 128 + z * DVS + ch * EPC) =
               *reinterpret_cast<const uint4 *>(sO.at(r, ch * EPC));
       }

@@ -76,12 +76,12 @@ typedef struct {
                                   N sequences of equal length total/N                   */
     const void *q;             /* [total, H, dk]                                         */
     const void *k;             /* [total, H, dk]                                         */
-    const void *v;             /* [total, H, dv], or NULL for zero values (bf16 forward
+    const void *v;             /* [total, H, dv], or NULL for zero values (a forward
                                   without `saved`)                                        */
     const float *beta;         /* [total, H]                                             */
     const float *g;            /* [total, H, dk] log-decay                               */
     const float *h0;           /* [N, H, dk, dv] initial states, or NULL for zero        */
-    void *o;                   /* out [total, H, dv], or NULL: not written (bf16 forward
+    void *o;                   /* out [total, H, dv], or NULL: not written (a forward
                                   without `saved`)                                        */
     float *hT;                 /* out [N, H, dk, dv] final states, or NULL               */
     void *saved;               /* out, kda_saved_size() bytes: what kda_bwd needs from this
@@ -96,9 +96,10 @@ typedef struct {
                                   (dk = dv), h0 is ignored. With v = NULL the final state
                                   is then the sequence's linear map on its initial state  */
     int32_t skip_prep;         /* nonzero: the workspace still holds the chunk records of a
-                                  previous bf16 kda_fwd (without saved) on the same q, k, g,
-                                  beta and sequence layout; only the scan runs (the records
-                                  do not depend on v, h0 or the initial state)            */
+                                  previous kda_fwd (without saved, same io_dtype) on the
+                                  same q, k, g, beta and sequence layout; only the scan
+                                  runs (the records do not depend on v, h0 or the initial
+                                  state)                                                  */
     /* ABI version 5: testing aids for the bounded waits of the bf16 state scan (leave 0) */
     int64_t wait_limit_ns;     /* limit of every bounded wait in the bf16 state scan, in ns;
                                   0 = the default of about 2 s                            */
@@ -234,9 +235,10 @@ kda_status kda_cp_combine(const kda_cp_args *args, cudaStream_t stream);
  *   5. a forward over every segment from its entering state, writing o, and the
  *      final state of each sequence's last segment to hT.
  * The result equals kda_fwd on args->fwd up to rounding. Everything is enqueued on
- * `stream`; nothing is copied to the host. Supported: io_dtype KDA_BF16, saved = NULL,
- * h0_identity = skip_prep = 0 (the other kda_fwd_args fields as for kda_fwd; fwd.
- * workspace is ignored: this call takes its own).
+ * `stream`; nothing is copied to the host. Supported: io_dtype KDA_BF16 or KDA_F32 (fp32
+ * products throughout, like kda_fwd), saved = NULL, h0_identity = skip_prep = 0 (the
+ * other kda_fwd_args fields as for kda_fwd; fwd.workspace is ignored: this call takes
+ * its own).
  */
 typedef struct {
     kda_fwd_args fwd;          /* the unsplit forward (o required, hT optional)           */

@@ -445,28 +445,30 @@ def test_cp_combine_vs_fp64_chain(kda):
                 s = M[n, kk, h].double() @ s + b[n, kk, h].double()
 
 
-def test_fwd_identity_start_zero_values(kda):
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_fwd_identity_start_zero_values(kda, io):
     # the segment map: final state from the identity with zero values, no outputs written
-    b = make_seq_batch([300, 64], heads=2, io_dtype="bf16", seed=72, h0=False)
+    b = make_seq_batch([300, 64], heads=2, io_dtype=io, seed=72, h0=False)
     t = to_dev(b)
     M, _ = kda._fwd_states(t["q"], t["k"], None, t["beta"], t["g"], t["cu_seqlens"], None, 2, scale=1.0,
                            h0_identity=True)
     eye = torch.eye(128).expand(2, 2, 128, 128).contiguous()
     res = oracle.fwd(b.q, b.k, torch.zeros_like(b.v), b.beta, b.g, b.cu_seqlens, eye)
     _, m_ref = oracle.assemble_fwd(res, b.cu_seqlens, 2, 128)
-    assert rel(M.cpu(), m_ref) <= TOL["bf16"]
+    assert rel(M.cpu(), m_ref) <= TOL[io]
 
 
-@pytest.mark.parametrize("lens,P", [([1000], 3), ([1000], 1), ([100, 900], 4)])
-def test_fwd_cp_matches_unsplit(kda, lens, P):
-    b = make_seq_batch(lens, heads=3, io_dtype="bf16", seed=73 + P, h0=True)
+@pytest.mark.parametrize("lens,P,io", [([1000], 3, "bf16"), ([1000], 1, "bf16"), ([100, 900], 4, "bf16"),
+                                       ([1000], 3, "f32"), ([100, 900], 4, "f32")])
+def test_fwd_cp_matches_unsplit(kda, lens, P, io):
+    b = make_seq_batch(lens, heads=3, io_dtype=io, seed=73 + P, h0=True)
     t = to_dev(b)
     o, hT = kda.kda_fwd_cp(t["q"], t["k"], t["v"], t["beta"], t["g"], b.cu_seqlens.cpu(), t["h0"], n_segments=P)
     res = oracle.fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0)
     o_ref, h_ref = oracle.assemble_fwd(res, b.cu_seqlens, 3, 128)
     e_o, e_h = rel(o.float().cpu(), o_ref), rel(hT.cpu(), h_ref)
-    print("cp", lens, P, f"o {e_o:.2e} hT {e_h:.2e}")
-    assert e_o <= TOL["bf16"] and e_h <= TOL["bf16"], (e_o, e_h)
+    print("cp", lens, P, io, f"o {e_o:.2e} hT {e_h:.2e}")
+    assert e_o <= TOL[io] and e_h <= TOL[io], (e_o, e_h)
 
 
 def test_fwd_cp_equal_sequences_without_offsets_and_no_h0(kda):
@@ -483,16 +485,17 @@ def test_fwd_cp_equal_sequences_without_offsets_and_no_h0(kda):
     assert torch.equal(o, o2) and torch.equal(hT, hT2)
 
 
-def test_fwd_cp_gates_at_bound(kda):
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_fwd_cp_gates_at_bound(kda, io):
     # the segment maps M of strongly decaying segments are tiny (entries underflow): the
     # chained states must still match the unsplit forward
-    b = _strong_gates(make_seq_batch([700, 300], heads=2, io_dtype="bf16", seed=74, h0=True), "uniform", 10)
+    b = _strong_gates(make_seq_batch([700, 300], heads=2, io_dtype=io, seed=74, h0=True), "uniform", 10)
     t = to_dev(b)
     o, hT = kda.kda_fwd_cp(t["q"], t["k"], t["v"], t["beta"], t["g"], b.cu_seqlens.cpu(), t["h0"], n_segments=4)
     res = oracle.fwd(b.q, b.k, b.v, b.beta, b.g, b.cu_seqlens, b.h0)
     o_ref, h_ref = oracle.assemble_fwd(res, b.cu_seqlens, 2, 128)
     e_o, e_h = rel(o.float().cpu(), o_ref), rel(hT.cpu(), h_ref)
-    assert e_o <= TOL["bf16"] and e_h <= TOL["bf16"], (e_o, e_h)
+    assert e_o <= TOL[io] and e_h <= TOL[io], (e_o, e_h)
 
 
 # ---------------------------------------------------------------- full-size workloads (sampled)

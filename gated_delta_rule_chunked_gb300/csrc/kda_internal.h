@@ -147,6 +147,7 @@ struct StepParams {
   int n_slots;                // pool size with state_indices
   const int *first_slot;      // [N] leading padding slots, or null (0)
   int *status;
+  int prefetch_dist;          // set by the launcher: CTA b prefetches the state of CTA b + prefetch_dist
 };
 
 struct AttnresParams {

@@ -92,6 +92,32 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
     S[r][0] = make_float2(t.x, t.y);
     S[r][1] = make_float2(t.z, t.w);
   }
+  // With two CTAs per SM the loads above leave HBM idle while the CTAs compute. Keep it busy
+  // by asking for the state and the token rows of the CTA that starts about one wave later
+  // (they are in L2 by the time that CTA loads them): bulk L2 prefetches, no registers held.
+  if (warp < 2 && p.prefetch_dist > 0) {
+    const long long nb = (long long)blockIdx.x + p.prefetch_dist;
+    if (nb < (long long)gridDim.x) {
+      const int nseq = (int)(nb / H), nh = (int)(nb % H);
+      if (warp == 0 && lane < 4) {   // the state, four quarters of 16 KiB
+        const int nslot = p.state_indices ? p.state_indices[nseq] : nseq;
+        if (!p.state_indices || (nslot >= 0 && nslot < p.n_slots)) {
+          const float *ns = p.state + ((size_t)nslot * H + nh) * D * D + (size_t)lane * (D * D / 4);
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(ns)),
+                       "r"(D * D * (int)sizeof(float) / 4)
+                       : "memory");
+        }
+      } else if (warp == 1 && lane < 4 * LS) {   // one row of q, k, v or g per lane, all LS slots
+        const int arr = lane / LS, l = lane % LS;
+        const size_t row = ((size_t)nseq * LS + l) * H + nh;
+        const int esz = arr == 3 ? (int)sizeof(float) : (int)sizeof(IO);
+        const void *base = arr == 0 ? p.q : arr == 1 ? p.k : arr == 2 ? p.v : static_cast<const void *>(p.g);
+        const char *src = static_cast<const char *>(base) + row * D * esz;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(src)), "r"(D * esz)
+                     : "memory");
+      }
+    }
+  }
 
   // the call's tokens into shared memory
   const IO *q = static_cast<const IO *>(p.q), *k = static_cast<const IO *>(p.k),
@@ -289,7 +315,17 @@ static cudaError_t launch_step_t(const StepParams &p, unsigned grid, cudaStream_
   const cudaError_t e =
       cudaFuncSetAttribute(kda_step_kernel<IO, PAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   if (e != cudaSuccess) return e;
-  kda_step_kernel<IO, PAD><<<grid, STEP_THREADS, smem, s>>>(p);
+  // prefetch distance: the CTAs resident at once (one wave)
+  int dev = 0, sms = 0, per_sm = 0;
+  StepParams q = p;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_step_kernel<IO, PAD>, STEP_THREADS, smem) ==
+          cudaSuccess)
+    q.prefetch_dist = sms * per_sm;
+  else
+    q.prefetch_dist = 0;
+  kda_step_kernel<IO, PAD><<<grid, STEP_THREADS, smem, s>>>(q);
   return cudaGetLastError();
 }
 

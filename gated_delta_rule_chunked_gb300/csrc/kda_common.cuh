@@ -235,6 +235,12 @@ __device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// Ask for `bytes` (a multiple of 16, from a 16-byte aligned address) of global memory to be
+// brought into L2; nothing waits for it and no register or shared memory is held.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(__cvta_generic_to_global(src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }

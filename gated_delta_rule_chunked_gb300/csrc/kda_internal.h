@@ -70,6 +70,7 @@ struct PrepParams {
                            //       bit 1 = write the backward extras: Kt (img2) and aux
   void *img2;              // [max_chunks][H] KtRec tiles (bit 1)
   int *status;
+  int prefetch_dist;       // tcgen05 prep: CTA b brings the staging boxes of CTA b + prefetch_dist into L2
 };
 
 struct FwdScanParams {

@@ -171,6 +171,18 @@ __global__ void __launch_bounds__(PT_THREADS, 2) kda_prep_tc_kernel(const __grid
       tc::tma_load_3d(smem + S::STG, &p.tm_g, 0, h, t0i, &bar[0]);
     }
     if (tid < 64) sb[tid] = tid < ref.len ? p.beta[(size_t)(ref.t0 + tid) * H + h] : 0.f;
+    if (warp == 2 && p.prefetch_dist > 0) {
+      // the staging boxes and betas of the CTA that starts about one wave later, into L2
+      const long long nbk = (long long)blockIdx.x + p.prefetch_dist;
+      ChunkRef nref;
+      if (nbk < (long long)gridDim.x &&
+          chunk_lookup(p.geo.chunk_off, p.geo.cu, p.geo.n_seqs, (int)(nbk / H), nref)) {
+        const int nh = (int)(nbk % H);
+        if (lane == 0) tc::tma_prefetch_3d(&p.tm_q, 0, nh, (int)nref.t0);
+        if (lane == 1) tc::tma_prefetch_3d(&p.tm_k, 0, nh, (int)nref.t0);
+        if (lane == 2) tc::tma_prefetch_3d(&p.tm_g, 0, nh, (int)nref.t0);
+      }
+    }
     const bool ok = mbar_wait(&bar[0], 0);
     if (ok && ref.len < CH) {   // the boxes hold the next sequence's rows there
       for (int idx = tid; idx < (CH - ref.len) * 16; idx += PT_THREADS) {
@@ -619,7 +631,14 @@ cudaError_t launch_prep_tc(const PrepParams &p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)p.geo.max_chunks * p.geo.heads;   // head-fastest: see the kernel
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kda_prep_tc_kernel<<<(unsigned)blocks, PT_THREADS, PtSmem::BYTES, s>>>(p);
+  // prefetch distance: the CTAs resident at once (one wave)
+  int dev = 0, sms = 0, per_sm = 0;
+  PrepParams q = p;
+  q.prefetch_dist = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_prep_tc_kernel, PT_THREADS, PtSmem::BYTES) == cudaSuccess)
+    q.prefetch_dist = sms * per_sm;
+  kda_prep_tc_kernel<<<(unsigned)blocks, PT_THREADS, PtSmem::BYTES, s>>>(q);
   return cudaGetLastError();
 }
 

@@ -36,10 +36,13 @@ namespace kda {
 constexpr int STEP_THREADS = 256;
 constexpr int STEP_MAX_L = 8;
 
-template <typename IO>
-__device__ __forceinline__ float ld_io(const IO *p) { return to_f(*p); }
-
 __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
+
+// a 4-byte global -> shared copy that holds no register (cp_async16 is its 16-byte form)
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(__cvta_generic_to_global(src))
+               : "memory");
+}
 
 // Shared memory of one CTA (static part; the column-sum partials are dynamic).
 struct StepSmem {
@@ -83,6 +86,30 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
   if (L == 0) return;   // padding only: no output, the state is unchanged
   float *red = step_red, *W = step_red + 8 * NV * D;
 
+  // The call's token rows go straight to shared memory first (q, k, v in the io type into the
+  // head of the partials area, free until sweep 1; g into G; beta), so that the state loads
+  // below are issued at once and the token work overlaps their arrival.
+  const IO *q = static_cast<const IO *>(p.q), *k = static_cast<const IO *>(p.k),
+           *v = static_cast<const IO *>(p.v);
+  IO *raw = reinterpret_cast<IO *>(step_red);   // [q, k, v][L][D]
+  {
+    constexpr int CPR = D * (int)sizeof(IO) / 16, CPG = D * (int)sizeof(float) / 16;   // 16-byte pieces per row
+    const int nio = 3 * L * CPR, ntask = nio + L * CPG;
+    for (int t = tid; t < ntask; t += STEP_THREADS) {
+      if (t < nio) {
+        const int a = t / (L * CPR), l = (t / CPR) % L, c = t % CPR;
+        const IO *src = (a == 0 ? q : a == 1 ? k : v) + (((size_t)seq * LS + F + l) * H + h) * D;
+        cp_async16(reinterpret_cast<char *>(raw + ((size_t)a * L + l) * D) + 16 * c,
+                   reinterpret_cast<const char *>(src) + 16 * c);
+      } else {
+        const int l = (t - nio) / CPG, c = (t - nio) % CPG;
+        cp_async16(reinterpret_cast<char *>(&sm.G[l][0]) + 16 * c,
+                   reinterpret_cast<const char *>(p.g + (((size_t)seq * LS + F + l) * H + h) * D) + 16 * c);
+      }
+    }
+    if (tid < L) cp_async4(&sm.beta[tid], p.beta + ((size_t)seq * LS + F + tid) * H + h);
+  }
+
   // state rows [16 warp, +16), columns [4 lane, +4) as two column pairs
   float *st = p.state + ((size_t)slot * H + h) * D * D;
   float2 S[16][2];
@@ -103,9 +130,7 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
         const int nslot = p.state_indices ? p.state_indices[nseq] : nseq;
         if (!p.state_indices || (nslot >= 0 && nslot < p.n_slots)) {
           const float *ns = p.state + ((size_t)nslot * H + nh) * D * D + (size_t)lane * (D * D / 4);
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(ns)),
-                       "r"(D * D * (int)sizeof(float) / 4)
-                       : "memory");
+          prefetch_l2(ns, D * D * (int)sizeof(float) / 4);
         }
       } else if (warp == 1 && lane < 4 * LS) {   // one row of q, k, v or g per lane, all LS slots
         const int arr = lane / LS, l = lane % LS;
@@ -113,35 +138,25 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
         const int esz = arr == 3 ? (int)sizeof(float) : (int)sizeof(IO);
         const void *base = arr == 0 ? p.q : arr == 1 ? p.k : arr == 2 ? p.v : static_cast<const void *>(p.g);
         const char *src = static_cast<const char *>(base) + row * D * esz;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(src)), "r"(D * esz)
-                     : "memory");
+        prefetch_l2(src, D * esz);
       }
     }
   }
 
-  // the call's tokens into shared memory
-  const IO *q = static_cast<const IO *>(p.q), *k = static_cast<const IO *>(p.k),
-           *v = static_cast<const IO *>(p.v);
-  for (int idx = tid; idx < L * D; idx += STEP_THREADS) {
-    const int l = idx / D, c = idx % D;
-    const size_t off = (((size_t)seq * LS + F + l) * H + h) * D + c;
-    sm.q[l][c] = ld_io(q + off);
-    sm.k[l][c] = ld_io(k + off);
-    sm.v[l][c] = ld_io(v + off);
-    sm.G[l][c] = p.g[off];
-  }
-  if (tid < L) sm.beta[tid] = p.beta[((size_t)seq * LS + F + tid) * H + h];
+  cp_async_wait_all();
   __syncthreads();
 
-  // L2 normalisation (one warp per token) and the running gate sums (one thread per channel)
+  // L2 normalisation (one warp per token), v to fp32, and the running gate sums (one thread
+  // per channel)
   if (warp < L) {
-    float sq = 0.f, sk = 0.f, qk = 0.f;
+    float x[4], y[4], sq = 0.f, sk = 0.f, qk = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float x = sm.q[warp][lane + 32 * j], y = sm.k[warp][lane + 32 * j];
-      sq = fmaf(x, x, sq);
-      sk = fmaf(y, y, sk);
-      qk = fmaf(x, y, qk);
+      x[j] = to_f(raw[(size_t)warp * D + lane + 32 * j]);
+      y[j] = to_f(raw[(size_t)(L + warp) * D + lane + 32 * j]);
+      sq = fmaf(x[j], x[j], sq);
+      sk = fmaf(y[j], y[j], sk);
+      qk = fmaf(x[j], y[j], qk);
     }
 #pragma unroll
     for (int m = 16; m; m >>= 1) {
@@ -152,11 +167,12 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
     const float rq = p.scale * rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      sm.q[warp][lane + 32 * j] *= rq;
-      sm.k[warp][lane + 32 * j] *= rk;
+      sm.q[warp][lane + 32 * j] = x[j] * rq;
+      sm.k[warp][lane + 32 * j] = y[j] * rk;
     }
     if (lane == 0) sm.b[warp][warp] = qk * rq * rk;
   }
+  for (int idx = tid; idx < L * D; idx += STEP_THREADS) sm.v[idx / D][idx % D] = to_f(raw[(size_t)2 * L * D + idx]);
   if (tid < D) {
     float run = 0.f;
     for (int l = 0; l < L; ++l) {

@@ -156,6 +156,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
+// The same box brought into L2 only (no shared memory, no barrier): a later load of it hits L2.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Pack 8 floats into one 16-byte chunk of bf16.
 __device__ __forceinline__ uint4 pack8(const float *x) {
   uint4 u;

@@ -555,58 +555,94 @@ __global__ void conv_dw_reduce_kernel(const float *partial, int groups, int C, i
   else if (db) db[c] = s;
 }
 
-template <typename IO, int W>
-__global__ void __launch_bounds__(CONV_THREADS, sizeof(IO) == 2 ? 4 : 3) conv_step_kernel(const ConvParams p) {
+// NS sequences per thread (the weights are loaded once for all of them); LM >= L token slots
+// held in registers (1, 2, 4 or 8: fewer registers, more warps per SM for short calls); VW:
+// weight and bias rows 16-byte aligned, loaded as float4 (the V x W weights of V consecutive
+// channels are contiguous). Every sequence's state rows and token rows are loaded before any
+// arithmetic.
+template <typename IO, int W, int NS, int LM, bool VW>
+__global__ void __launch_bounds__(CONV_THREADS, NS > 1                ? 2
+                                                : sizeof(IO) == 2      ? (LM <= 2 ? 6 : LM == 4 ? 5 : 4)
+                                                                       : (LM <= 4 ? 3 : 2))
+    conv_step_kernel(const ConvParams p) {
   constexpr int V = 4;   // 4 channels a thread: few registers, many warps for a latency-bound call
   constexpr int WP = W > 1 ? W - 1 : 1;
   constexpr bool FAST = sizeof(IO) == 2;
   using IOV = ConvIO<IO, V>;
   using Raw = typename IOV::Raw;
-  const int cg = blockIdx.x * CONV_THREADS + threadIdx.x, n = blockIdx.y;
+  const int cg = blockIdx.x * CONV_THREADS + threadIdx.x;
   if (cg >= p.C / V) return;
   const int c0 = cg * V, L = p.L;
-  const int slot = p.idx ? p.idx[n] : n;
-  if (slot < 0 || slot >= p.n_slots) {
-    if (cg == 0) report(p.status, KDA_ERR_INVALID_ARG_CODE);
-    return;
+  int F[NS], acc[NS];
+  bool live[NS];
+  IO *st[NS];
+  Raw win[NS][WP], xr[NS][LM];
+#pragma unroll
+  for (int u = 0; u < NS; ++u) {
+    const int n = blockIdx.y * NS + u;
+    live[u] = n < p.n_seqs;
+    const int slot = !live[u] ? 0 : (p.idx ? p.idx[n] : n);
+    if (live[u] && (slot < 0 || slot >= p.n_slots)) {
+      if (cg == 0) report(p.status, KDA_ERR_INVALID_ARG_CODE);
+      live[u] = false;
+    }
+    F[u] = live[u] && p.first ? min(max(p.first[n], 0), L) : 0;
+    acc[u] = live[u] && p.acc ? min(max(p.acc[n], 0), L) : L;
+    st[u] = static_cast<IO *>(p.st_out) + (size_t)slot * (W - 1) * p.C + c0;
+    if (live[u]) {
+#pragma unroll
+      for (int i = 0; i < W - 1; ++i) win[u][i] = IOV::ld(st[u] + (size_t)i * p.C);
+#pragma unroll
+      for (int l = 0; l < LM; ++l)
+        if (l >= F[u] && l < L) xr[u][l] = IOV::ld(static_cast<const IO *>(p.x) + ((size_t)n * L + l) * p.C + c0);
+    }
   }
-  const int F = p.first ? min(max(p.first[n], 0), L) : 0;
-  const int a = p.acc ? min(max(p.acc[n], 0), L) : L;
-  IO *st = static_cast<IO *>(p.st_out) + (size_t)slot * (W - 1) * p.C + c0;
   float w[W][V], b[V];
-  Raw win[WP], keep[WP];
+  if (VW) {
+    const float4 *w4 = reinterpret_cast<const float4 *>(p.w + (size_t)c0 * W);
 #pragma unroll
-  for (int e = 0; e < V; ++e) {
+    for (int i = 0; i < W; ++i) {   // V * W = 4 W floats
+      const float4 t = w4[i];
+      const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-    for (int j = 0; j < W; ++j) w[j][e] = p.w[(size_t)(c0 + e) * W + j];
-    b[e] = p.bias ? p.bias[c0 + e] : 0.f;
+      for (int k = 0; k < 4; ++k) w[(4 * i + k) % W][(4 * i + k) / W] = tv[k];
+    }
+    const float4 t = p.bias ? *reinterpret_cast<const float4 *>(p.bias + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    b[0] = t.x; b[1] = t.y; b[2] = t.z; b[3] = t.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) w[j][e] = p.w[(size_t)(c0 + e) * W + j];
+      b[e] = p.bias ? p.bias[c0 + e] : 0.f;
+    }
   }
 #pragma unroll
-  for (int i = 0; i < W - 1; ++i) win[i] = IOV::ld(st + (size_t)i * p.C);
-  Raw xr[8];   // at most 8 slots
+  for (int u = 0; u < NS; ++u) {
+    if (!live[u]) continue;
+    const int n = blockIdx.y * NS + u;
+    Raw keep[WP];
 #pragma unroll
-  for (int l = 0; l < 8; ++l)
-    if (l >= F && l < L) xr[l] = IOV::ld(static_cast<const IO *>(p.x) + ((size_t)n * L + l) * p.C + c0);
+    for (int l = 0; l < LM; ++l) {
+      if (l < F[u] || l >= L) continue;
+      float xv[V], z[V];
+      IOV::unpack(xr[u][l], xv);
+      conv_point<IO, V, W, WP>(w, b, win[u], xv, z);
+      if (p.act)
 #pragma unroll
-  for (int l = 0; l < 8; ++l) {
-    if (l < F || l >= L) continue;
-    float xv[V], z[V];
-    IOV::unpack(xr[l], xv);
-    conv_point<IO, V, W, WP>(w, b, win, xv, z);
-    if (p.act)
+        for (int e = 0; e < V; ++e) z[e] *= sigm<FAST>(z[e]);
+      IOV::store(static_cast<IO *>(p.y) + ((size_t)n * L + l) * p.C + c0, z);
 #pragma unroll
-      for (int e = 0; e < V; ++e) z[e] *= sigm<FAST>(z[e]);
-    IOV::store(static_cast<IO *>(p.y) + ((size_t)n * L + l) * p.C + c0, z);
+      for (int i = 0; i + 1 < W - 1; ++i) win[u][i] = win[u][i + 1];
+      if (W > 1) win[u][WP - 1] = xr[u][l];
+      if (l + 1 == acc[u])
 #pragma unroll
-    for (int i = 0; i + 1 < W - 1; ++i) win[i] = win[i + 1];
-    if (W > 1) win[WP - 1] = xr[l];
-    if (l + 1 == a)
+        for (int i = 0; i < W - 1; ++i) keep[i] = win[u][i];
+    }
+    if (acc[u] > F[u])
 #pragma unroll
-      for (int i = 0; i < W - 1; ++i) keep[i] = win[i];
+      for (int i = 0; i < W - 1; ++i) *reinterpret_cast<Raw *>(st[u] + (size_t)i * p.C) = keep[i];
   }
-  if (a > F)
-#pragma unroll
-    for (int i = 0; i < W - 1; ++i) *reinterpret_cast<Raw *>(st + (size_t)i * p.C) = keep[i];
 }
 
 namespace {
@@ -657,15 +693,32 @@ cudaError_t bwd_t(const ConvParams &p, cudaStream_t s) {
     default: return bwd_w<IO, 4>(p, s);
   }
 }
+constexpr int CONV_STEP_NS = 1;   // sequences per thread
+template <typename IO, int W, int LM>
+void step_l(const ConvParams &p, dim3 grid, cudaStream_t s) {
+  const bool vw = reinterpret_cast<uintptr_t>(p.w) % 16 == 0 && reinterpret_cast<uintptr_t>(p.bias) % 16 == 0;
+  if (vw)
+    conv_step_kernel<IO, W, CONV_STEP_NS, LM, true><<<grid, CONV_THREADS, 0, s>>>(p);
+  else
+    conv_step_kernel<IO, W, CONV_STEP_NS, LM, false><<<grid, CONV_THREADS, 0, s>>>(p);
+}
+template <typename IO, int W>
+void step_w(const ConvParams &p, dim3 grid, cudaStream_t s) {
+  if (p.L <= 1) step_l<IO, W, 1>(p, grid, s);
+  else if (p.L <= 2) step_l<IO, W, 2>(p, grid, s);
+  else if (p.L <= 4) step_l<IO, W, 4>(p, grid, s);
+  else step_l<IO, W, 8>(p, grid, s);
+}
 template <typename IO>
 cudaError_t step_t(const ConvParams &p, cudaStream_t s) {
   constexpr int V = 4;
-  const dim3 grid((unsigned)((p.C / V + CONV_THREADS - 1) / CONV_THREADS), (unsigned)p.n_seqs);
+  const dim3 grid((unsigned)((p.C / V + CONV_THREADS - 1) / CONV_THREADS),
+                  (unsigned)((p.n_seqs + CONV_STEP_NS - 1) / CONV_STEP_NS));
   switch (p.W) {
-    case 1: conv_step_kernel<IO, 1><<<grid, CONV_THREADS, 0, s>>>(p); break;
-    case 2: conv_step_kernel<IO, 2><<<grid, CONV_THREADS, 0, s>>>(p); break;
-    case 3: conv_step_kernel<IO, 3><<<grid, CONV_THREADS, 0, s>>>(p); break;
-    default: conv_step_kernel<IO, 4><<<grid, CONV_THREADS, 0, s>>>(p); break;
+    case 1: step_w<IO, 1>(p, grid, s); break;
+    case 2: step_w<IO, 2>(p, grid, s); break;
+    case 3: step_w<IO, 3>(p, grid, s); break;
+    default: step_w<IO, 4>(p, grid, s); break;
   }
   return cudaGetLastError();
 }

@@ -94,20 +94,22 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
   IO *raw = reinterpret_cast<IO *>(step_red);   // [q, k, v][L][D]
   {
     constexpr int CPR = D * (int)sizeof(IO) / 16, CPG = D * (int)sizeof(float) / 16;   // 16-byte pieces per row
-    const int nio = 3 * L * CPR, ntask = nio + L * CPG;
-    for (int t = tid; t < ntask; t += STEP_THREADS) {
-      if (t < nio) {
-        const int a = t / (L * CPR), l = (t / CPR) % L, c = t % CPR;
-        const IO *src = (a == 0 ? q : a == 1 ? k : v) + (((size_t)seq * LS + F + l) * H + h) * D;
+    const size_t row0 = ((size_t)seq * LS + F) * H + h;   // token slot F + l is row row0 + l * H
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      const IO *src = a == 0 ? q : a == 1 ? k : v;
+      for (int t = tid; t < L * CPR; t += STEP_THREADS) {
+        const int l = t / CPR, c = t % CPR;
         cp_async16(reinterpret_cast<char *>(raw + ((size_t)a * L + l) * D) + 16 * c,
-                   reinterpret_cast<const char *>(src) + 16 * c);
-      } else {
-        const int l = (t - nio) / CPG, c = (t - nio) % CPG;
-        cp_async16(reinterpret_cast<char *>(&sm.G[l][0]) + 16 * c,
-                   reinterpret_cast<const char *>(p.g + (((size_t)seq * LS + F + l) * H + h) * D) + 16 * c);
+                   reinterpret_cast<const char *>(src + (row0 + (size_t)l * H) * D) + 16 * c);
       }
     }
-    if (tid < L) cp_async4(&sm.beta[tid], p.beta + ((size_t)seq * LS + F + tid) * H + h);
+    for (int t = tid; t < L * CPG; t += STEP_THREADS) {
+      const int l = t / CPG, c = t % CPG;
+      cp_async16(reinterpret_cast<char *>(&sm.G[l][0]) + 16 * c,
+                 reinterpret_cast<const char *>(p.g + (row0 + (size_t)l * H) * D) + 16 * c);
+    }
+    if (tid < L) cp_async4(&sm.beta[tid], p.beta + row0 + (size_t)tid * H);
   }
 
   // state rows [16 warp, +16), columns [4 lane, +4) as two column pairs
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
   __syncthreads();
 
   // L2 normalisation (one warp per token), v to fp32, and the running gate sums (one thread
-  // per channel)
+  // per channel, on the last four warps: the first L warps normalise)
   if (warp < L) {
     float x[4], y[4], sq = 0.f, sk = 0.f, qk = 0.f;
 #pragma unroll
@@ -173,11 +175,12 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
     if (lane == 0) sm.b[warp][warp] = qk * rq * rk;
   }
   for (int idx = tid; idx < L * D; idx += STEP_THREADS) sm.v[idx / D][idx % D] = to_f(raw[(size_t)2 * L * D + idx]);
-  if (tid < D) {
+  if (tid >= STEP_THREADS - D) {
+    const int c = tid - (STEP_THREADS - D);
     float run = 0.f;
     for (int l = 0; l < L; ++l) {
-      run += sm.G[l][tid];
-      sm.G[l][tid] = run;
+      run += sm.G[l][c];
+      sm.G[l][c] = run;
     }
   }
   __syncthreads();

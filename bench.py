@@ -510,7 +510,8 @@ def bench_cp(args, dev, peaks, fwd_ms, P=4):
             "unsplit_fwd_ms": fwd_ms, "tokens_per_s": T / (ms * 1e-3), "gbs_algorithmic": gbs,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"]},
-            "note": "one GPU runs all P segments: 3 forward passes (segment maps, offsets, final) + the combine"}
+            "note": "one GPU runs all P segments: the chunk records, the segment maps and offsets (one paired scan "
+                    "launch), the combine, and the final forward pass"}
 
 
 def bench_decode(args, dev, lib, stream, peaks):

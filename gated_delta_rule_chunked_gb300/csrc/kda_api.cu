@@ -513,7 +513,11 @@ size_t kda_bwd_workspace_size(const kda_bwd_args *a) {
   return plan(&f, true).bytes;
 }
 
-kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
+namespace {
+// The forward; hT_ident (bf16 I/O, no `saved`) asks for the paired scan launch, which also runs
+// every sequence from the identity with zero values and writes those final states (the
+// sequence's state map) to hT_ident.
+kda_status fwd_impl(const kda_fwd_args *a, cudaStream_t stream, float *hT_ident) {
   kda_status st = check_fwd(a, "kda_fwd");
   if (st != KDA_OK) return st;
   const WsPlan w = plan(a, false);
@@ -568,7 +572,7 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
   mark(1, stream);
   kda::FwdScanParams sp{geo, a->v, rec, a->h0, a->o, a->hT, a->saved, a->dev_status, a->h0_identity != 0, {},
                         a->wait_limit_ns > 0 ? (unsigned long long)a->wait_limit_ns : 2000000000ull,
-                        a->debug_starve != 0};
+                        a->debug_starve != 0, f32 || a->saved ? nullptr : hT_ident};
   if (!f32 && a->v && !map_tokens(&sp.tm_v, a->v, false, a->total_tokens, a->heads, 64, true))
     return fail(KDA_ERR_CUDA, "%s: could not encode the TMA tensor maps", "kda_fwd");
   e = f32 ? kda::launch_fwd_scan(sp, true, pick_slice(a), stream) : kda::launch_fwd_scan_tc(sp, stream);
@@ -577,6 +581,9 @@ kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) {
   g_last_error.clear();
   return KDA_OK;
 }
+}  // namespace
+
+kda_status kda_fwd(const kda_fwd_args *a, cudaStream_t stream) { return fwd_impl(a, stream, nullptr); }
 
 namespace {
 // fp32 I/O: the prep runs again into the workspace (records, A, T), then the fp32 dS scan and
@@ -791,21 +798,31 @@ kda_status kda_fwd_cp(const kda_fwd_cp_args *c, cudaStream_t stream) {
   s.cu_seqlens = seg;
   s.workspace = ws + w.fws;
   s.workspace_bytes = w.fws_bytes;
-  // pass 1: chunk records and the segment maps M (identity start, zero values, no outputs)
-  kda_fwd_args p1 = s;
-  p1.v = nullptr;
-  p1.o = nullptr;
-  p1.h0 = nullptr;
-  p1.hT = M;
-  p1.h0_identity = 1;
-  if ((st = kda_fwd(&p1, stream)) != KDA_OK) return st;
-  // pass 2: the segment offsets b (zero start, same records)
-  kda_fwd_args p2 = s;
-  p2.o = nullptr;
-  p2.h0 = nullptr;
-  p2.hT = b;
-  p2.skip_prep = 1;
-  if ((st = kda_fwd(&p2, stream)) != KDA_OK) return st;
+  if (f.io_dtype != KDA_F32) {
+    // passes 1 and 2 in one launch: the chunk records, then paired scans per (segment, head), one
+    // for the segment maps M (identity start, zero values), one for the offsets b (zero start)
+    kda_fwd_args p12 = s;
+    p12.o = nullptr;
+    p12.h0 = nullptr;
+    p12.hT = b;
+    if ((st = fwd_impl(&p12, stream, M)) != KDA_OK) return st;
+  } else {
+    // pass 1: chunk records and the segment maps M (identity start, zero values, no outputs)
+    kda_fwd_args p1 = s;
+    p1.v = nullptr;
+    p1.o = nullptr;
+    p1.h0 = nullptr;
+    p1.hT = M;
+    p1.h0_identity = 1;
+    if ((st = kda_fwd(&p1, stream)) != KDA_OK) return st;
+    // pass 2: the segment offsets b (zero start, same records)
+    kda_fwd_args p2 = s;
+    p2.o = nullptr;
+    p2.h0 = nullptr;
+    p2.hT = b;
+    p2.skip_prep = 1;
+    if ((st = kda_fwd(&p2, stream)) != KDA_OK) return st;
+  }
   // combine: the state entering each segment
   if ((e = kda::launch_cp_combine(N, P, H, M, b, f.h0, s_in, stream)) != cudaSuccess)
     return cuda_fail(e, "kda_fwd_cp combine");

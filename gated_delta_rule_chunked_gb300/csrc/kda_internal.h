@@ -87,6 +87,9 @@ struct FwdScanParams {
   CUtensorMap tm_v;        // bf16 scan: v as boxes of 64 channels x 1 head x 64 tokens, 128-byte swizzle
   unsigned long long wait_ns;   // limit of every bounded wait of the tcgen05 scan
   int starve;              // testing aid: CTA 0 issues none of its first copies (its waits run out)
+  float *hT_ident;         // tcgen05 scan, paired launch (non-null): CTA 2u runs unit u from the identity
+                           // with zero values and no outputs (final states here), CTA 2u + 1 runs it as
+                           // given; the two read the same records at about the same time (L2)
 };
 
 struct BwdScanParams {

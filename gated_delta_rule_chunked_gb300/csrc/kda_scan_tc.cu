@@ -60,7 +60,11 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
   extern __shared__ __align__(1024) char smem_raw[];
   // operand tiles need 1024-byte alignment in the shared window
   char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int H = p.geo.heads, h = blockIdx.x % H, seq = blockIdx.x / H;
+  // paired launch: even CTAs run their unit from the identity with zero values (the state map of
+  // the unit), odd CTAs run it as given
+  const bool paired = p.hT_ident != nullptr, ident_cta = paired && (blockIdx.x & 1u) == 0;
+  const unsigned unit = paired ? blockIdx.x >> 1 : blockIdx.x;
+  const int H = p.geo.heads, h = (int)(unit % (unsigned)H), seq = (int)(unit / (unsigned)H);
   const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
   const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -68,8 +72,12 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
   const int row = tid & 127, qw = warp & 3;   // row = TMEM lane = value channel
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + S::TSLOT);
-  const bf16 *v = (const bf16 *)p.v;
-  bf16 *o = (bf16 *)p.o;
+  const bf16 *v = ident_cta ? nullptr : (const bf16 *)p.v;
+  bf16 *o = ident_cta ? nullptr : (bf16 *)p.o;
+  float *hT = ident_cta ? p.hT_ident : p.hT;
+  const bool h0_identity = ident_cta || p.h0_identity;
+  const float *h0 = ident_cta ? nullptr : p.h0;
+  bf16 *saved = ident_cta ? nullptr : (bf16 *)p.saved;
   const size_t sh = (size_t)seq * H + h;
 
   // bar[0..1]: record buffers; bar[2]: phase 1 done; bar[3]: phase 2 done (MMA commits);
@@ -104,8 +112,8 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
       for (int cb = 0; cb < 8; ++cb) {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          buf[i] = p.h0_identity ? (16 * cb + i == row ? 1.f : 0.f)
-                                 : (p.h0 ? p.h0[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f);
+          buf[i] = h0_identity ? (16 * cb + i == row ? 1.f : 0.f)
+                               : (h0 ? h0[(sh * 128 + 16 * cb + i) * 128 + row] : 0.f);
         tc::st16(tl + set_of(1) + 16 * cb, buf);
       }
       tc::wait_st();
@@ -132,7 +140,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
       char *rb = smem + (b ? S::REC1 : S::REC0);
       ok &= mbar_wait(&bar[b], (j >> 1) & 1, lim);
       if (j > 0) ok &= mbar_wait(&bar[3], (j - 1) & 1, lim);
-      if (tid == 32 && p.saved) bulk_wait_read();   // the previous saved-state copy has read the S^T tile
+      if (tid == 32 && saved) bulk_wait_read();   // the previous saved-state copy has read the S^T tile
       tc::fence_after();
       if (!named_sync_and(1, 128, ok)) break;
       // the other record buffer's last reader (phase 2 of the previous chunk) has finished:
@@ -199,8 +207,8 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
         // the next chunk's values first, then the chunk-start state, which leaves as one bulk
         // copy of the operand tile (it has until the next pass A to read the tile)
         if (v && j + 1 < nch) tc_issue_v(smem + S::AV, p, h, s0 + (long long)(j + 1) * CH, &bar[4]);
-        if (p.saved) {
-          bulk_s2g((bf16 *)p.saved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
+        if (saved) {
+          bulk_s2g(saved + ((size_t)(cbase + j) * H + h) * 128 * 128, smem + S::AS, 32768);
           bulk_commit();
         }
       }
@@ -242,20 +250,20 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
     if (ok && done > 0) ok = mbar_wait(&bar[3], (done - 1) & 1, lim);
     tc::fence_after();
     if (named_sync_and(1, 128, ok)) {
-      if (p.hT) {   // hT[dk][dv] = S^T[dv][dk], in the set of the last chunk
+      if (hT) {   // hT[dk][dv] = S^T[dv][dk], in the set of the last chunk
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
           uint32_t r[64];
           tc::ld64(tl + set_of(done + 1) + 64 * hb, r);
           tc::wait_ld();
 #pragma unroll
-          for (int i = 0; i < 64; ++i) p.hT[(sh * 128 + 64 * hb + i) * 128 + row] = __uint_as_float(r[i]);
+          for (int i = 0; i < 64; ++i) hT[(sh * 128 + 64 * hb + i) * 128 + row] = __uint_as_float(r[i]);
         }
       }
     } else {
       report(p.status, ERR_TIMEOUT);
     }
-    if (tid == 32 && p.saved) bulk_wait_all();   // saved states complete before the CTA leaves
+    if (tid == 32 && saved) bulk_wait_all();   // saved states complete before the CTA leaves
   } else {
     // ------------------------------------------------------------ io warps
     // O^T of chunk j (TMEM) -> o. Each warp transposes its 32 value channels through its
@@ -300,7 +308,9 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kda_fwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        TcScanSmem::BYTES);
   if (e != cudaSuccess) return e;
-  kda_fwd_scan_tc_kernel<<<(unsigned)units, 256, TcScanSmem::BYTES, s>>>(p);
+  const long long ctas = units * (p.hT_ident ? 2 : 1);
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kda_fwd_scan_tc_kernel<<<(unsigned)ctas, 256, TcScanSmem::BYTES, s>>>(p);
   return cudaGetLastError();
 }
 

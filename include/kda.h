@@ -230,7 +230,8 @@ kda_status kda_cp_combine(const kda_cp_args *args, cudaStream_t stream);
  * bullet: contiguous token ranges kept for KDA's recurrent state propagation):
  *   1. the chunk records of every segment (they depend on q, k, g, beta only);
  *   2. each segment's map M: final state from the identity with zero values;
- *   3. each segment's offset b: final state from zero;
+ *   3. each segment's offset b: final state from zero (with bf16 I/O, 2 and 3 run as one
+ *      launch, the two scans of a segment side by side);
  *   4. kda_cp_combine: the state entering each segment;
  *   5. a forward over every segment from its entering state, writing o, and the
  *      final state of each sequence's last segment to hT.

@@ -63,7 +63,7 @@ struct StepSmem {
 template <typename IO, bool PAD>
 __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p) {
   __shared__ __align__(16) StepSmem sm;
-  // partials [8 row groups][2L vectors][D], then the reduced sums [2L][D]
+  // partials [8 row groups][2L vectors][D]
   extern __shared__ __align__(16) float step_red[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
     return;
   }
   if (L == 0) return;   // padding only: no output, the state is unchanged
-  float *red = step_red, *W = step_red + 8 * NV * D;
+  float *red = step_red;
 
   // The call's token rows go straight to shared memory first (q, k, v in the io type into the
   // head of the partials area, free until sweep 1; g into G; beta), so that the state loads
@@ -256,28 +256,20 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
   }
   __syncthreads();
 
-  // reduce the 8 row-group partials: one (vector, column quad) per task, fixed order
-  for (int t = tid; t < NV * (D / 4); t += STEP_THREADS) {
-    const int vec = t / (D / 4), c4 = 4 * (t % (D / 4));
-    float2 s0 = make_float2(0.f, 0.f), s1 = s0;
-#pragma unroll
-    for (int g8 = 0; g8 < 8; ++g8) {
-      const float4 x = *reinterpret_cast<const float4 *>(&red[((size_t)g8 * NV + vec) * D + c4]);
-      s0 = __fadd2_rn(s0, make_float2(x.x, x.y));
-      s1 = __fadd2_rn(s1, make_float2(x.z, x.w));
-    }
-    *reinterpret_cast<float4 *>(&W[vec * D + c4]) = make_float4(s0.x, s0.y, s1.x, s1.y);
-  }
-  __syncthreads();
-
-  // the token-token solve, one value column per thread; outputs of all L tokens
+  // the token-token solve, one value column per thread: the 8 row-group partials of this column
+  // summed in a fixed order, then the outputs of all L tokens
   if (tid < D) {
     IO *o = static_cast<IO *>(p.o);
     float u[STEP_MAX_L];
 #pragma unroll
     for (int l = 0; l < STEP_MAX_L; ++l) {
       if (l < L) {
-        float w = W[(2 * l) * D + tid], ol = W[(2 * l + 1) * D + tid];
+        float w = 0.f, ol = 0.f;
+#pragma unroll
+        for (int g8 = 0; g8 < 8; ++g8) {
+          w += red[((size_t)g8 * NV + 2 * l) * D + tid];
+          ol += red[((size_t)g8 * NV + 2 * l + 1) * D + tid];
+        }
 #pragma unroll
         for (int m = 0; m < l; ++m) {
           w = fmaf(sm.a[l][m], u[m], w);
@@ -327,9 +319,9 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) kda_step_kernel(StepParams p)
 
 template <typename IO, bool PAD>
 static cudaError_t launch_step_t(const StepParams &p, unsigned grid, cudaStream_t s) {
-  // Dynamic shared memory: 8 row-group partials plus the reduced sums, 2L vectors each.
-  constexpr int max_smem = (8 + 1) * 2 * STEP_MAX_L * D * (int)sizeof(float);
-  const int smem = (8 + 1) * 2 * p.steps * D * (int)sizeof(float);
+  // Dynamic shared memory: 8 row-group partials, 2L vectors each.
+  constexpr int max_smem = 8 * 2 * STEP_MAX_L * D * (int)sizeof(float);
+  const int smem = 8 * 2 * p.steps * D * (int)sizeof(float);
   // static + dynamic exceeds the 48 KiB default: opt in (per device, idempotent)
   const cudaError_t e =
       cudaFuncSetAttribute(kda_step_kernel<IO, PAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);

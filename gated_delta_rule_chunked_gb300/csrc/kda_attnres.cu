@@ -124,6 +124,12 @@ __global__ void __cluster_dims__(AR_CL, 1, 1) __launch_bounds__(256) attnres_fwd
       for (int i = 0; i < S; ++i)
         bulk_g2s(xs + (size_t)i * per, static_cast<const IO *>(p.src[i]) + t * d + (size_t)cbeg * N, (uint32_t)(nown * 16),
                  &bar);
+  } else if ((int)threadIdx.x <= S && nown > 0 && p.prefetch_dist > 0 &&
+             (long long)blockIdx.x + p.prefetch_dist < (long long)gridDim.x) {
+    // the same quarter of a later token (the distance is a whole number of clusters) into L2,
+    // so that CTA's copies hit L2
+    const long long t2 = ((long long)blockIdx.x + p.prefetch_dist) / AR_CL;
+    prefetch_l2(static_cast<const IO *>(p.src[threadIdx.x - 1]) + t2 * d + (size_t)cbeg * N, (uint32_t)(nown * 16));
   }
   float acc[2 * AR_MAXS];
 #pragma unroll
@@ -386,7 +392,15 @@ cudaError_t launch_attnres_fwd(const AttnresParams &p, bool f32, cudaStream_t s)
   auto kern = f32 ? attnres_fwd_kernel<float> : attnres_fwd_kernel<bf16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, threads, smem, s>>>(p);
+  // prefetch distance: half the CTAs resident at once, in whole clusters (a quarter to three
+  // quarters of a wave measured the same; two waves slower)
+  AttnresParams q = p;
+  q.prefetch_dist = 0;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) == cudaSuccess)
+    q.prefetch_dist = (long long)sms * per_sm / 2 / AR_CL * AR_CL;
+  kern<<<grid, threads, smem, s>>>(q);
   return cudaGetLastError();
 }
 

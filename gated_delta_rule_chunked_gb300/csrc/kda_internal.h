@@ -169,6 +169,7 @@ struct AttnresParams {
   void *dsrc[9];
   float *dw;
   float *partial;                // [backward CTAs][dim]
+  long long prefetch_dist;       // forward: CTA b brings the source slices of CTA b + prefetch_dist into L2
 };
 
 cudaError_t launch_attnres_fwd(const AttnresParams &p, bool f32, cudaStream_t s);

@@ -254,6 +254,11 @@ __global__ void __cluster_dims__(AR_CL, 1, 1) __launch_bounds__(256) attnres_bwd
     if (tid == 0) {
       if (!dbl) issue(t, 0);
       else if (t + K < p.T) issue(t + K, b ^ 1);
+    } else if (tid <= S + 1 && nown > 0 && t + (dbl ? 2 : 1) * K < p.T) {
+      // the slices of the token after the one being copied, into L2: its copies then hit L2
+      const long long t2 = t + (dbl ? 2 : 1) * K;
+      const void *base = tid <= S ? p.src[tid - 1] : p.dout;
+      prefetch_l2(static_cast<const IO *>(base) + t2 * d + (size_t)cbeg * N, (uint32_t)(nown * 16));
     }
     if (tid < S) {
       st[0][tid] = p.alpha[t * S + tid];

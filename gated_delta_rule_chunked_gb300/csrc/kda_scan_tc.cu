@@ -414,6 +414,11 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_scan_tc_kernel(const __grid_co
       if (!named_sync_and(1, 128, ok)) break;
       if (tid == 32 && it >= 1 && it + 1 < nch)   // next record, a whole chunk step ahead
         issue(smem + ((it + 1) & 1 ? S::REC1 : S::REC0), rec_of(j - 1), &bar[(it + 1) & 1]);
+      if (tid == 64 && it + 2 < nch) {   // the chunk after that (record and dO) into L2
+        prefetch_l2(rec_of(j - 2), TcRec::BYTES);
+        tc::tma_prefetch_3d(&p.tm_do, 0, h, (int)(s0 + (long long)(j - 2) * CH));
+        tc::tma_prefetch_3d(&p.tm_do, 64, h, (int)(s0 + (long long)(j - 2) * CH));
+      }
       // pass A: dS^T -> operand tile, decayed dS^T back to TMEM
       {
         const float *gC = reinterpret_cast<const float *>(rb + TcRec::GC);

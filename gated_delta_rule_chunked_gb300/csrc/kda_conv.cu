@@ -571,6 +571,22 @@ __global__ void __launch_bounds__(CONV_THREADS, NS > 1                ? 2
   using IOV = ConvIO<IO, V>;
   using Raw = typename IOV::Raw;
   const int cg = blockIdx.x * CONV_THREADS + threadIdx.x;
+  if (p.prefetch_dist > 0 && (int)threadIdx.x < W - 1 + p.L) {
+    // the state rows (threads < W - 1) and token rows of the CTA about one wave later into L2
+    const long long lin = (long long)blockIdx.y * gridDim.x + blockIdx.x + p.prefetch_dist;
+    const int bx = (int)(lin % gridDim.x), n2 = (int)(lin / gridDim.x) * NS;
+    const int cb = bx * CONV_THREADS * V, nb = min(CONV_THREADS * V, p.C - cb) * (int)sizeof(IO) / 16 * 16;
+    if (lin < (long long)gridDim.x * gridDim.y && n2 < p.n_seqs && nb > 0) {
+      const int i = threadIdx.x;
+      if (i < W - 1) {
+        const int slot = p.idx ? p.idx[n2] : n2;
+        if (slot >= 0 && slot < p.n_slots)
+          prefetch_l2(static_cast<const IO *>(p.st_out) + ((size_t)slot * (W - 1) + i) * p.C + cb, (uint32_t)nb);
+      } else {
+        prefetch_l2(static_cast<const IO *>(p.x) + ((size_t)n2 * p.L + (i - (W - 1))) * p.C + cb, (uint32_t)nb);
+      }
+    }
+  }
   if (cg >= p.C / V) return;
   const int c0 = cg * V, L = p.L;
   int F[NS], acc[NS];
@@ -694,13 +710,27 @@ cudaError_t bwd_t(const ConvParams &p, cudaStream_t s) {
   }
 }
 constexpr int CONV_STEP_NS = 1;   // sequences per thread
+template <typename IO, int W, int LM, bool VW>
+void step_v(const ConvParams &p, dim3 grid, cudaStream_t s) {
+  auto kern = conv_step_kernel<IO, W, CONV_STEP_NS, LM, VW>;
+  // prefetch distance: the CTAs resident at once (one wave); rows must start on 16 bytes
+  ConvParams q = p;
+  q.prefetch_dist = 0;
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((size_t)p.C * sizeof(IO) % 16 == 0 && reinterpret_cast<uintptr_t>(p.x) % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(p.st_out) % 16 == 0 && cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CONV_THREADS, 0) == cudaSuccess)
+    q.prefetch_dist = (long long)sms * per_sm;
+  kern<<<grid, CONV_THREADS, 0, s>>>(q);
+}
 template <typename IO, int W, int LM>
 void step_l(const ConvParams &p, dim3 grid, cudaStream_t s) {
   const bool vw = reinterpret_cast<uintptr_t>(p.w) % 16 == 0 && reinterpret_cast<uintptr_t>(p.bias) % 16 == 0;
   if (vw)
-    conv_step_kernel<IO, W, CONV_STEP_NS, LM, true><<<grid, CONV_THREADS, 0, s>>>(p);
+    step_v<IO, W, LM, true>(p, grid, s);
   else
-    conv_step_kernel<IO, W, CONV_STEP_NS, LM, false><<<grid, CONV_THREADS, 0, s>>>(p);
+    step_v<IO, W, LM, false>(p, grid, s);
 }
 template <typename IO, int W>
 void step_w(const ConvParams &p, dim3 grid, cudaStream_t s) {

@@ -202,6 +202,7 @@ struct ConvParams {
   int L, n_slots;
   const int *idx, *acc, *first;
   int *status;
+  long long prefetch_dist;   // step: CTA b brings the state and token rows of CTA b + prefetch_dist into L2
 };
 cudaError_t launch_conv_fwd(const ConvParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_conv_bwd(const ConvParams &p, bool f32, cudaStream_t s);

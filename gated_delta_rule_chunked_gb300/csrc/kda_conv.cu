@@ -203,6 +203,17 @@ __device__ __forceinline__ void conv_issue(char *ring, uint64_t *full, long long
                src[i] + (size_t)(a + r) * pitch, rowbytes, &full[slot]);
 }
 
+// The rows of stage k into L2 only (a stage beyond the ring, so that its copies hit L2). The
+// forward uses it; in the backward (two staged tensors, fp32 dx stores) it measured slower.
+template <int ROWS>
+__device__ __forceinline__ void conv_prefetch(long long k, long long r0, long long rend, const char *const *src, int ntens,
+                                              size_t pitch, uint32_t rowbytes) {
+  const long long a = r0 + k * ROWS;
+  const int n = (int)min((long long)ROWS, rend - a);
+  for (int r = 0; r < n; ++r)
+    for (int i = 0; i < ntens; ++i) prefetch_l2(src[i] + (size_t)(a + r) * pitch, rowbytes);
+}
+
 // After a wait gave up at stage k: wait (bounded) for the copies of the stages still in flight,
 // so none lands after the CTA has left.
 __device__ __forceinline__ void conv_drain(uint64_t *full, long long k, long long nst) {
@@ -311,8 +322,10 @@ __global__ void __launch_bounds__(CONV_THREADS, 2) conv_fwd_kernel(const ConvPar
             *reinterpret_cast<Raw *>(static_cast<IO *>(p.st_out) + ((long long)s.n * (W - 1) + i) * p.C + c0) = win[i];
       }
     __syncthreads();   // every thread is done with this slot
-    if (tid == 0 && k + CONV_NST < nst)
+    if (tid == 0 && k + CONV_NST < nst) {
       conv_issue<ROWS>(ring, full, k + CONV_NST, T0, T1, src, 1, pitch, (uint32_t)(nch * sizeof(IO)));
+      if (k + CONV_NST + 1 < nst) conv_prefetch<ROWS>(k + CONV_NST + 1, T0, T1, src, 1, pitch, (uint32_t)(nch * sizeof(IO)));
+    }
   }
 }
 

@@ -95,6 +95,11 @@ __device__ __forceinline__ float ld_peer(const float *p, uint32_t rank) {
   return v;
 }
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
+// Arrival that publishes nothing (this CTA only signals that its reads of the peers' sums are
+// done; their values are already in registers and used), so it needs no release fence.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
 
 constexpr int AR_CL = 4;   // CTAs per token
@@ -179,7 +184,7 @@ __global__ void __cluster_dims__(AR_CL, 1, 1) __launch_bounds__(256) attnres_fwd
       }
     }
   }
-  cluster_arrive();   // done reading the peers' sums; the matching wait comes before exit
+  cluster_arrive_relaxed();   // done reading the peers' sums; the matching wait comes before exit
   __syncthreads();
   for (int c = threadIdx.x; c < nown; c += blockDim.x) {
     float o[N], x[N];
@@ -300,8 +305,8 @@ __global__ void __cluster_dims__(AR_CL, 1, 1) __launch_bounds__(256) attnres_bwd
       for (int o = 16; o; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
       if (tid < S) dl[tid] = a * (v - m);
     }
-    cluster_arrive();   // done reading the peers' sums
-    __syncthreads();    // dl
+    cluster_arrive_relaxed();   // done reading the peers' sums
+    __syncthreads();            // dl
     // pass 2: dx_i and the dw partials
 #pragma unroll
     for (int j = 0; j < J; ++j) {

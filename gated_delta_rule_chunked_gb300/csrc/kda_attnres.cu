@@ -60,17 +60,36 @@ template <> struct Vec<float> {
 };
 
 // Sum `n` per-thread values over the CTA (fixed order); results in out[0..n) for every thread.
+// Inside a warp the values are padded to NP (a power of two) and reduced by recursive halving:
+// at each of the first log2(NP) steps a lane sends half of its values to its partner and keeps
+// the other half, so after them lane l holds the warp's partial of value idx(l) (one shuffle
+// per value kept: NP - 1 in all, instead of 5 per value).
 template <int NMAX>
 __device__ __forceinline__ void block_sum(float (&v)[NMAX], int n, float *red, float *out) {
+  constexpr int NP = NMAX <= 8 ? 8 : (NMAX <= 16 ? 16 : 32);
+  constexpr int LG = NP == 8 ? 3 : (NP == 16 ? 4 : 5);   // halving steps
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float x[NP];
 #pragma unroll
-  for (int i = 0; i < NMAX; ++i)
-    if (i < n) {
-      float x = v[i];
+  for (int i = 0; i < NP; ++i) x[i] = i < NMAX && i < n ? v[i < NMAX ? i : 0] : 0.f;
+  int idx = 0;   // which value this lane ends up holding
 #pragma unroll
-      for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-      if (lane == 0) red[warp * NMAX + i] = x;
+  for (int st = 0; st < 5; ++st) {
+    const int o = 16 >> st;
+    if (st < LG) {
+      const int half = NP >> (st + 1);
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float send = up ? x[i] : x[i + half], keep = up ? x[i + half] : x[i];
+        x[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+      if (up) idx += half;
+    } else {
+      x[0] += __shfl_xor_sync(0xffffffffu, x[0], o);
     }
+  }
+  if (idx < n && (lane & ((1 << (5 - LG)) - 1)) == 0) red[warp * NMAX + idx] = x[0];
   __syncthreads();
   if ((int)threadIdx.x < n) {
     float s = 0.f;

@@ -144,6 +144,43 @@ def test_conv_step_paged_verify_and_padding(kda, io):
     np.testing.assert_array_equal(dpool.float().cpu().numpy(), pool_ref)
 
 
+@pytest.mark.parametrize("L,W,C,aligned", [(1, 4, 2056, True), (2, 2, 2056, False), (3, 4, 1032, True),
+                                             (5, 4, 1032, False), (7, 2, 3080, True)])
+def test_conv_step_slot_counts(kda, L, W, C, aligned):
+    """Every register specialisation of the step (slot counts up to 1, 2, 4 and 8) and both
+    weight paths (16-byte aligned weight rows read as float4, misaligned ones read per element),
+    channel counts that leave the last CTA partly empty, accept lengths 0..L and padding, against
+    the oracle."""
+    N, P = 9, 13
+    gen = torch.Generator().manual_seed(100 + 10 * L + W)
+    x = torch.randn(N, L, C, generator=gen).to(torch.bfloat16)
+    w = torch.randn(C, W, generator=gen)
+    b = torch.randn(C, generator=gen) * 0.1
+    pool = torch.randn(P, W - 1, C, generator=gen).to(torch.bfloat16)
+    idx = torch.randperm(P, generator=gen)[:N].to(torch.int32)
+    acc = torch.randint(0, L + 1, (N,), generator=gen, dtype=torch.int32)
+    first = torch.randint(0, L, (N,), generator=gen, dtype=torch.int32)
+    y_ref, pool_ref = oracle.conv_step(x, w, b, pool, idx, acc, first)
+    if aligned:
+        wd, bd = w.cuda(), b.cuda()
+    else:   # weight and bias 4 bytes past a 16-byte boundary
+        wbig = torch.zeros(C * W + 1, device="cuda")
+        bbig = torch.zeros(C + 1, device="cuda")
+        wbig[1:] = w.reshape(-1).cuda()
+        bbig[1:] = b.cuda()
+        wd, bd = wbig[1:].view(C, W), bbig[1:]
+        assert wd.data_ptr() % 16 != 0 and bd.data_ptr() % 16 != 0
+    dpool = pool.cuda()
+    y = torch.full((N, L, C), 7.0, dtype=torch.bfloat16, device="cuda")
+    kda.conv_step(x.cuda(), wd, bd, dpool, acc, state_indices=idx, first_slot=first, out=y)
+    torch.cuda.synchronize()
+    yc = y.float().cpu().numpy()
+    mask = ~np.isnan(y_ref)
+    assert rel(yc[mask], y_ref[mask]) <= TOL["bf16"]
+    assert (yc[~mask] == 7.0).all()
+    np.testing.assert_array_equal(dpool.float().cpu().numpy(), pool_ref)
+
+
 def test_conv_step_equals_forward(kda):
     W, C, L, N = 3, 512, 8, 5
     gen = torch.Generator().manual_seed(12)

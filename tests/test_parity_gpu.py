@@ -558,4 +558,5 @@ def test_fullsize_decode_sampled(kda):
     ro = np.stack([[res[(a, b_)][0] for b_ in range(len(heads))] for a in range(len(seqs))])
     gs = np.stack([[st[i, h].cpu().numpy() for h in heads] for i in seqs])
     rs = np.stack([[res[(a, b_)][1] for b_ in range(len(heads))] for a in range(len(seqs))])
+    print("decode-bf16-N256-L4-H96", f"o {rel(go, ro):.2e} state {rel(gs, rs):.2e}")
     assert rel(go, ro) <= TOL["bf16"] and rel(gs, rs) <= TOL["bf16"], (rel(go, ro), rel(gs, rs))

@@ -168,24 +168,74 @@ __device__ __forceinline__ void wgemm(float (&acc)[NT][4], TA A, int m0, TB B, i
   }
 }
 
-// fp32 tiles: same fragment positions, exact fp32 FMAs.
+// fp32 tiles: same fragment positions, exact fp32 FMAs, in k order. With B stored [k][n] a
+// lane's two columns 2q, 2q+1 sit in one 16-byte chunk of the row, so they come in one 8-byte
+// load; with A stored [m][k] the values at k and k + 1 (k even) do too, so A is read two k at a
+// time (k0 and k1 even).
 template <bool AK, bool BK, int NT, int LDA, int LDB>
 __device__ __forceinline__ void wgemm(float (&acc)[NT][4], Tile<float, LDA> A, int m0, Tile<float, LDB> B,
                                       int n0, int k0, int k1) {
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
-  for (int k = k0; k < k1; ++k) {
-    const float a0 = AK ? *A.at(m0 + g, k) : *A.at(k, m0 + g);
-    const float a1 = AK ? *A.at(m0 + g + 8, k) : *A.at(k, m0 + g + 8);
+  auto step = [&](int k, float a0, float a1) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int n = n0 + nt * 8 + 2 * q;
-      const float b0 = BK ? *B.at(n, k) : *B.at(k, n);
-      const float b1 = BK ? *B.at(n + 1, k) : *B.at(k, n + 1);
+      float b0, b1;
+      if constexpr (BK) {
+        b0 = *B.at(n, k);
+        b1 = *B.at(n + 1, k);
+      } else {
+        const float2 bb = *reinterpret_cast<const float2 *>(B.at(k, n));
+        b0 = bb.x;
+        b1 = bb.y;
+      }
       acc[nt][0] = fmaf(a0, b0, acc[nt][0]);
       acc[nt][1] = fmaf(a0, b1, acc[nt][1]);
       acc[nt][2] = fmaf(a1, b0, acc[nt][2]);
       acc[nt][3] = fmaf(a1, b1, acc[nt][3]);
+    }
+  };
+  if constexpr (AK) {
+    for (int k = k0; k < k1; k += 2) {
+      const float2 x0 = *reinterpret_cast<const float2 *>(A.at(m0 + g, k));
+      const float2 x1 = *reinterpret_cast<const float2 *>(A.at(m0 + g + 8, k));
+      step(k, x0.x, x1.x);
+      step(k + 1, x0.y, x1.y);
+    }
+  } else {
+    for (int k = k0; k < k1; ++k) step(k, *A.at(k, m0 + g), *A.at(k, m0 + g + 8));
+  }
+}
+
+// Two fp32 products with one B operand in one k loop (each accumulator in k order, as two
+// wgemm calls): acc1 += A1 B, acc2 += A2 B, A1 and A2 stored [m][k], B stored [k][n]; the B
+// values are loaded once for both. k0 and k1 even.
+template <int NT, int LDA, int LDB>
+__device__ __forceinline__ void wgemm2(float (&acc1)[NT][4], float (&acc2)[NT][4], Tile<float, LDA> A1,
+                                       Tile<float, LDA> A2, int m0, Tile<float, LDB> B, int n0, int k0, int k1) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  for (int k = k0; k < k1; k += 2) {
+    const float2 x0 = *reinterpret_cast<const float2 *>(A1.at(m0 + g, k));
+    const float2 x1 = *reinterpret_cast<const float2 *>(A1.at(m0 + g + 8, k));
+    const float2 y0 = *reinterpret_cast<const float2 *>(A2.at(m0 + g, k));
+    const float2 y1 = *reinterpret_cast<const float2 *>(A2.at(m0 + g + 8, k));
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const float a0 = kk ? x0.y : x0.x, a1 = kk ? x1.y : x1.x, c0 = kk ? y0.y : y0.x, c1 = kk ? y1.y : y1.x;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float2 bb = *reinterpret_cast<const float2 *>(B.at(k + kk, n0 + nt * 8 + 2 * q));
+        acc1[nt][0] = fmaf(a0, bb.x, acc1[nt][0]);
+        acc1[nt][1] = fmaf(a0, bb.y, acc1[nt][1]);
+        acc1[nt][2] = fmaf(a1, bb.x, acc1[nt][2]);
+        acc1[nt][3] = fmaf(a1, bb.y, acc1[nt][3]);
+        acc2[nt][0] = fmaf(c0, bb.x, acc2[nt][0]);
+        acc2[nt][1] = fmaf(c0, bb.y, acc2[nt][1]);
+        acc2[nt][2] = fmaf(c1, bb.x, acc2[nt][2]);
+        acc2[nt][3] = fmaf(c1, bb.y, acc2[nt][3]);
+      }
     }
   }
 }

@@ -147,8 +147,7 @@ __global__ void __launch_bounds__(128 * NG, 1) kda_fwd_scan_kernel(FwdScanParams
     float accV[NT][4], accO[NT][4];
     zero(accV);
     zero(accO);
-    wgemm<true, false, NT>(accV, Kt, 16 * warp, sS, 0, 0, 128);
-    wgemm<true, false, NT>(accO, Qt, 16 * warp, sS, 0, 0, 128);
+    wgemm2<NT>(accV, accO, Kt, Qt, 16 * warp, sS, 0, 0, 128);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

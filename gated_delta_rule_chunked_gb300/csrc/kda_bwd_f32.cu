@@ -245,32 +245,33 @@ __global__ void __launch_bounds__(128, 1) kda_bwd_scan_f32_kernel(const __grid_c
 
 // ------------------------------------------------------------------ 2. state side
 constexpr int BC_T = 256;   // threads of the chunk kernels
+constexpr int CTA_KB = 32;   // k-block of the staged block products (K is a multiple of it)
 constexpr int LDP = 129;    // padded fp32 row of the [64][128] tiles: row and column reads hit distinct banks
 
-// acc[i][j] += sum_k A(4 tr + i, k) B(k, tc + 16 j) over k < K (a multiple of 16), for the 64 x 16 NJ
-// product of the CTA (tr = tid / 16, tc = tid % 16). The operands are read through fa(r, k) and
-// fb(k, n) (shared or global memory) into a staging area, 16 values of k at a time.
+// acc[i][j] += sum_k A(4 tr + i, k) B(k, tc + 16 j) over k < K (a multiple of CTA_KB), for the
+// 64 x 16 NJ product of the CTA (tr = tid / 16, tc = tid % 16). The operands are read through
+// fa(r, k) and fb(k, n) (shared or global memory) into a staging area, CTA_KB values of k at a time.
 template <int NJ, class FA, class FB>
 __device__ __forceinline__ void cta_mm(float (&acc)[4][NJ], FA fa, FB fb, int K, float *st) {
   constexpr int N = 16 * NJ;
-  float *sa = st, *sbm = st + 64 * 17;
+  float *sa = st, *sbm = st + 64 * (CTA_KB + 1);
   const int tid = threadIdx.x, tr = tid >> 4, tc = tid & 15;
-  for (int k0 = 0; k0 < K; k0 += 16) {
+  for (int k0 = 0; k0 < K; k0 += CTA_KB) {
     __syncthreads();   // the staging area is free (and earlier shared-memory results are visible)
-    for (int idx = tid; idx < 64 * 16; idx += BC_T) {
-      const int r = idx >> 4, kk = idx & 15;
-      sa[r * 17 + kk] = fa(r, k0 + kk);
+    for (int idx = tid; idx < 64 * CTA_KB; idx += BC_T) {
+      const int r = idx / CTA_KB, kk = idx % CTA_KB;
+      sa[r * (CTA_KB + 1) + kk] = fa(r, k0 + kk);
     }
-    for (int idx = tid; idx < 16 * N; idx += BC_T) {
+    for (int idx = tid; idx < CTA_KB * N; idx += BC_T) {
       const int kk = idx / N, n = idx % N;
       sbm[kk * N + n] = fb(k0 + kk, n);
     }
     __syncthreads();
 #pragma unroll 4
-    for (int kk = 0; kk < 16; ++kk) {
+    for (int kk = 0; kk < CTA_KB; ++kk) {
       float av[4], bv[NJ];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = sa[(4 * tr + i) * 17 + kk];
+      for (int i = 0; i < 4; ++i) av[i] = sa[(4 * tr + i) * (CTA_KB + 1) + kk];
 #pragma unroll
       for (int j = 0; j < NJ; ++j) bv[j] = sbm[kk * N + tc + 16 * j];
 #pragma unroll
@@ -293,8 +294,8 @@ __device__ __forceinline__ void zero_acc(float (&acc)[4][NJ]) {
 struct BxSmem {
   static constexpr int TILE = 64 * LDP * 4;
   static constexpr int VP = 0, U = TILE, DU = 2 * TILE, DV = 3 * TILE;   // V', U, dU, dV' [64][LDP]
-  static constexpr int ST = 4 * TILE;                                    // staging: A [64][17], B [16][128]
-  static constexpr int SB = ST + (64 * 17 + 16 * 128) * 4;               // beta [64]
+  static constexpr int ST = 4 * TILE;                                    // staging: A [64][KB + 1], B [KB][128]
+  static constexpr int SB = ST + (64 * (CTA_KB + 1) + CTA_KB * 128) * 4; // beta [64]
   static constexpr int PART = SB + 256;                                  // dbeta partials [2][16][64]
   static constexpr int BYTES = PART + 2 * 16 * 64 * 4;
   // regions reused once their products are done

@@ -259,13 +259,17 @@ __global__ void __launch_bounds__(PT_THREADS, 2) kda_prep_tc_kernel(const __grid
       em[0] = 0.f;
 #pragma unroll
       for (int b = 0; b < NSUB; ++b) em[b + 1] = em[b] + tot[b][c];
+      float ema = em[0];   // em[a], picked by compile-time indices (a run-time index would put em in local memory)
+#pragma unroll
+      for (int b = 1; b < NSUB; ++b)
+        if (b == a) ema = em[b];
       if (a == 0) *reinterpret_cast<float *>(rec + TcRec::GC + 4 * c) = ex2(em[NSUB]);   // e^{G_last}
-      pam[a * 128 + c] = ex2(em[a]);
+      pam[a * 128 + c] = ex2(ema);
 #pragma unroll
       for (int ap = 1; ap < NSUB; ++ap)
-        if (ap > a) pfm[pair_idx(a, ap) * 128 + c] = ex2(em[ap] - em[a]);
+        if (ap > a) pfm[pair_idx(a, ap) * 128 + c] = ex2(em[ap] - ema);
       // Kh = k^ e^{G_last - G} into the record (B2 rows 0..127, transposed: row c, tokens 16a..)
-      const float ftail = em[NSUB] - em[a];
+      const float ftail = em[NSUB] - ema;
 #pragma unroll
       for (int i8 = 0; i8 < SUB; i8 += 8) {
         float khv[8];

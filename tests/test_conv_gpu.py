@@ -181,6 +181,40 @@ def test_conv_step_slot_counts(kda, L, W, C, aligned):
     np.testing.assert_array_equal(dpool.float().cpu().numpy(), pool_ref)
 
 
+def test_conv_step_more_than_a_wave(kda):
+    """The measured width (C = 3 x 96 x 128) with more CTAs than are resident at once (each
+    brings the state and token rows of the CTA one wave later into L2, looking its slot up in
+    the pool), one sequence's slot outside the pool: that sequence is reported and untouched,
+    the others match the oracle."""
+    W, C, L, N, P = 4, 3 * 96 * 128, 4, 24, 32
+    gen = torch.Generator().manual_seed(13)
+    x = torch.randn(N, L, C, generator=gen).to(torch.bfloat16)
+    w = torch.randn(C, W, generator=gen) / 2
+    b = torch.randn(C, generator=gen) * 0.1
+    pool = torch.randn(P, W - 1, C, generator=gen).to(torch.bfloat16)
+    idx = torch.randperm(P, generator=gen)[:N].to(torch.int32)
+    bad = 9
+    idx[bad] = P
+    acc = torch.randint(0, L + 1, (N,), generator=gen, dtype=torch.int32)
+    first = torch.randint(0, L, (N,), generator=gen, dtype=torch.int32)
+    good = [i for i in range(N) if i != bad]
+    y_ref, pool_ref = oracle.conv_step(x[good], w, b, pool, idx[good], acc[good], first[good])
+    dpool = pool.cuda()
+    y = torch.full((N, L, C), 7.0, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.conv_step(x.cuda(), w.cuda(), b.cuda(), dpool, acc, state_indices=idx, first_slot=first, out=y,
+                  dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    yc = y.float().cpu().numpy()
+    assert (yc[bad] == 7.0).all()
+    yg = yc[good]
+    mask = ~np.isnan(y_ref)
+    assert rel(yg[mask], y_ref[mask]) <= TOL["bf16"]
+    assert (yg[~mask] == 7.0).all()
+    np.testing.assert_array_equal(dpool.float().cpu().numpy(), pool_ref)
+
+
 def test_conv_step_equals_forward(kda):
     W, C, L, N = 3, 512, 8, 5
     gen = torch.Generator().manual_seed(12)

@@ -428,6 +428,45 @@ def test_step_bad_state_index_reports(kda):
     assert torch.all(o[1].float() == 7.0)               # that sequence is left untouched
 
 
+def test_step_paged_more_than_a_wave(kda):
+    """More CTAs than are resident at once (each brings the state of the CTA one wave later
+    into L2, looking its slot up in the pool), with one sequence's slot outside the pool: that
+    sequence is reported and left untouched, sampled (sequence, head) pairs of the others match
+    the oracle, and pool slots no sequence addresses are unchanged."""
+    N, L, H, P = 40, 4, 96, 64
+    d = make_decode_batch(N, L, H, "bf16", seed=61)
+    gen = torch.Generator().manual_seed(68)
+    pool = torch.randn(P, H, 128, 128, generator=gen) * 0.02
+    idx = torch.randperm(P, generator=gen)[:N].to(torch.int32)
+    bad = 17
+    idx[bad] = P + 3
+    first = torch.randint(0, L, (N,), generator=gen, dtype=torch.int32)
+    acc = torch.randint(1, L + 1, (N,), generator=gen, dtype=torch.int32)
+    st = pool.cuda()
+    o = torch.full(d.v.shape, 7.0, dtype=d.v.dtype, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_step(d.q.cuda(), d.k.cuda(), d.v.cuda(), d.beta.cuda(), d.g.cuda(), st, acc.cuda(), out=o,
+                 state_indices=idx.cuda(), first_slot=first.cuda(), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1                      # KDA_ERR_INVALID_ARG
+    assert torch.all(o[bad].float() == 7.0)
+    seqs, heads = [0, 5, 16, 18, 29, 39], [0, 47, 95]
+    sub = lambda t: t[seqs][:, :, heads]
+    res = oracle.step_paged(sub(d.q), sub(d.k), sub(d.v), sub(d.beta), sub(d.g), pool[:, heads],
+                            [int(idx[i]) for i in seqs], [int(first[i]) for i in seqs], [int(acc[i]) for i in seqs])
+    oc, stc = o.float().cpu(), st.cpu()
+    for a, i in enumerate(seqs):
+        f, slot = int(first[i]), int(idx[i])
+        for b, h in enumerate(heads):
+            o_ref, s_ref = res[(a, b)]
+            assert rel(oc[i, f:, h], o_ref) <= TOL["bf16"], (i, h)
+            assert rel(stc[slot, h], s_ref) <= TOL["bf16"], (i, h)
+    used = {int(x) for x in idx.tolist()}
+    for slot in range(P):
+        if slot not in used:
+            assert torch.equal(stc[slot], pool[slot]), slot
+
+
 # ---------------------------------------------------------------- context parallelism (emulated)
 
 def test_cp_combine_vs_fp64_chain(kda):

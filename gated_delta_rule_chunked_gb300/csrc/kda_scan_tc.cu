@@ -18,8 +18,11 @@
 // TMEM holds two sets of [S^T | O^T | U^T], alternating per chunk, so the previous
 // chunk's O^T is written out while this chunk's phase 1 runs.
 //
-// i.e. U = Tb (V - Kt S), O = Qt S + Bm U, S <- gC*S + Kh^T U. One thread issues
-// the MMAs; completion is signalled through mbarriers (tcgen05.commit). The next
+// i.e. U = Tb (V - Kt S), O = Qt S + Bm U, S <- gC*S + Kh^T U. A ninth warp issues
+// phase 1: V^T Tb^T as soon as the values land (it does not need the state), the K-block
+// of the state product that pass A has finished while pass A does the other, so only the
+// last four MMAs wait for the whole of pass A; thread 0 issues phase 2. Completion is
+// signalled through mbarriers (tcgen05.commit). The next
 // chunk's record arrives by TMA bulk copy into the second of two buffers, and
 // the next chunk's values arrive by TMA as soon as phase 1 has read this chunk's. Every wait
 // is bounded; on a timeout the kernel reports KDA_ERR_TIMEOUT, frees its tensor
@@ -55,7 +58,9 @@ __device__ __forceinline__ void tc_issue_v(char *dst, const FwdScanParams &p, in
   tc::tma_load_3d(dst + 8192, &p.tm_v, 64, h, (int)t0, bar);
 }
 
-__global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_constant__ FwdScanParams p) {
+constexpr int FS_THREADS = 288;   // 4 state warps, 4 io warps, 1 phase-1 issuer warp
+
+__global__ void __launch_bounds__(FS_THREADS, 1) kda_fwd_scan_tc_kernel(const __grid_constant__ FwdScanParams p) {
   using S = TcScanSmem;
   extern __shared__ __align__(1024) char smem_raw[];
   // operand tiles need 1024-byte alignment in the shared window
@@ -68,7 +73,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
   const long long s0 = p.geo.cu[seq], s1 = p.geo.cu[seq + 1];
   const int nch = (int)((s1 - s0 + CH - 1) / CH), cbase = p.geo.chunk_off[seq];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool io = warp >= 4;                  // warps 4..7: values in, outputs out
+  const bool io = warp >= 4 && warp < 8;      // warps 4..7: values in, outputs out; warp 8: phase-1 MMAs
   const int row = tid & 127, qw = warp & 3;   // row = TMEM lane = value channel
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::BAR);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + S::TSLOT);
@@ -81,10 +86,14 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
   const size_t sh = (size_t)seq * H + h;
 
   // bar[0..1]: record buffers; bar[2]: phase 1 done; bar[3]: phase 2 done (MMA commits);
-  // bar[4]: the V tile of a chunk landed (TMA); bar[5]: O^T of a chunk read out (128 io arrivals)
+  // bar[4]: the V tile of a chunk landed (TMA); bar[5]: O^T of a chunk read out (128 io arrivals);
+  // bar[6], bar[7]: pass A has written K-block 0, then all, of the S^T operand tile (128 state
+  // arrivals each, the second also after a short last chunk's value rows are zeroed)
   if (tid == 0) {
     for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
     mbar_init(&bar[5], 128);
+    mbar_init(&bar[6], 128);
+    mbar_init(&bar[7], 128);
     fence_mbar_init();
   }
   if (warp == 0) tc::alloc(tslot, 512);
@@ -103,7 +112,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
 
   const uint64_t lim = p.wait_ns;   // limit of every bounded wait below
   bool ok = true;
-  if (!io) {
+  if (warp < 4) {
     // ------------------------------------------------------------ state warps
     // initial state S^T[dv][dk] = h0[dk][dv], in the set chunk 0 reads from
     {
@@ -133,7 +142,6 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
         *reinterpret_cast<uint4 *>(smem + S::AV + 16 * idx) = make_uint4(0u, 0u, 0u, 0u);
       fence_proxy_async();
     }
-    const uint64_t idesc_v = tc::idesc_bf16_mn(128, 64, true, false);
     int done = 0;   // chunks whose phase 2 was issued
     for (int j = 0; j < nch; ++j) {
       const int b = j & 1;
@@ -167,6 +175,11 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
             for (int i = 0; i < 16; ++i) buf[i] *= gC[k0 + i];
             tc::st16(tl + set_of(j) + k0, buf);
           }
+          if (hb == 0) {   // K-block 0 of the operand tile is written: the issuer may start on it
+            fence_proxy_async();
+            tc::fence_before();
+            mbar_arrive(&bar[6]);
+          }
         }
         tc::wait_st();
       }
@@ -180,27 +193,11 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
                 make_uint4(0u, 0u, 0u, 0u);
           }
       }
+      // the whole operand tile (and a short chunk's zeroed value rows) is in place: the issuer
+      // finishes phase 1
       fence_proxy_async();
       tc::fence_before();
-      if (!named_sync_and(1, 128, ok)) break;
-      if (tid == 0) {
-        tc::fence_after();
-        {
-          const uint64_t d_rb = b ? d_rec1 : d_rec0, d_b1 = d_rb + (TcRec::B1 >> 4), d_tb = d_rb + (TcRec::TB >> 4);
-          const uint32_t dO = tmem + colO(j);
-#pragma unroll
-          for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint32_t off = (kb * 16384 + 32 * ks) >> 4;
-              tc::mma_bf16(dO, d_as + off, d_b1 + off, tc::idesc_bf16(128, 128), (kb | ks) != 0);
-            }
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(dO + 64, tc::desc_sw128_mn(smem_u32(smem + S::AV) + 2048u * ks, 8192), d_tb + 2 * ks, idesc_v, 1);
-          tc::commit(&bar[2]);
-        }
-      }
+      mbar_arrive(&bar[7]);
       ok &= mbar_wait(&bar[2], j & 1, lim);
       tc::fence_after();
       if (tid == 32) {
@@ -264,7 +261,7 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
       report(p.status, ERR_TIMEOUT);
     }
     if (tid == 32 && saved) bulk_wait_all();   // saved states complete before the CTA leaves
-  } else {
+  } else if (io) {
     // ------------------------------------------------------------ io warps
     // O^T of chunk j (TMEM) -> o. Each warp transposes its 32 value channels through its
     // own columns of the staging tile, then writes 64-byte row pieces with 16-byte stores.
@@ -296,6 +293,53 @@ __global__ void __launch_bounds__(256, 1) kda_fwd_scan_tc_kernel(const __grid_co
       tc::fence_before();
       mbar_arrive(&bar[5]);
     }
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ phase-1 issuer (warp 8)
+    // [O^T | U^T] = S^T [Qt; -W]^T + (0 | V^T Tb^T) of chunk j into its set. V^T Tb^T needs only
+    // the values and the record, so it goes first (full chunks; a sequence's short last chunk
+    // waits until the state warps have zeroed the rows past its end, bar[7]); K-block 0 of the
+    // state product follows once pass A has written it (bar[6]), K-block 1 at bar[7]. The first
+    // k-step is split into its O^T and U^T halves so that O^T is overwritten and U^T adds to
+    // the values' product. Every wait is bounded; a timeout ends the loop (the state warps'
+    // own bounded wait on bar[2] then reports it).
+    const uint64_t d_as = tc::desc_sw128(smem_u32(smem + S::AS));
+    const uint64_t d_rec0 = tc::desc_sw128(smem_u32(smem + S::REC0)), d_rec1 = tc::desc_sw128(smem_u32(smem + S::REC1));
+    const uint64_t idesc_v = tc::idesc_bf16_mn(128, 64, true, false);
+    auto v_products = [&](uint32_t dO, uint64_t d_tb, bool first) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc::mma_bf16(dO + 64, tc::desc_sw128_mn(smem_u32(smem + S::AV) + 2048u * ks, 8192), d_tb + 2 * ks, idesc_v,
+                     !(first && ks == 0));
+    };
+    for (int j = 0; j < nch; ++j) {
+      const int b = j & 1;
+      const long long t0 = s0 + (long long)j * CH;
+      const bool early_v = v && s1 - t0 >= CH;
+      const uint64_t d_rb = b ? d_rec1 : d_rec0, d_b1 = d_rb + (TcRec::B1 >> 4), d_tb = d_rb + (TcRec::TB >> 4);
+      const uint32_t dO = tmem + colO(j);
+      if (!mbar_wait(&bar[b], (j >> 1) & 1, lim)) break;
+      if (early_v) {
+        if (!mbar_wait(&bar[4], j & 1, lim)) break;
+        tc::fence_after();
+        v_products(dO, d_tb, true);
+      }
+      if (!mbar_wait(&bar[6], j & 1, lim)) break;
+      tc::fence_after();
+      tc::mma_bf16(dO, d_as, d_b1, tc::idesc_bf16(128, 64), 0);                              // O^T half
+      tc::mma_bf16(dO + 64, d_as, d_b1 + (8192 >> 4), tc::idesc_bf16(128, 64), early_v ? 1u : 0u);   // U^T half
+#pragma unroll
+      for (int ks = 1; ks < 4; ++ks)
+        tc::mma_bf16(dO, d_as + ((32 * ks) >> 4), d_b1 + ((32 * ks) >> 4), tc::idesc_bf16(128, 128), 1);
+      if (!mbar_wait(&bar[7], j & 1, lim)) break;
+      tc::fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint32_t off = (16384 + 32 * ks) >> 4;
+        tc::mma_bf16(dO, d_as + off, d_b1 + off, tc::idesc_bf16(128, 128), 1);
+      }
+      if (v && !early_v) v_products(dO, d_tb, false);
+      tc::commit(&bar[2]);
+    }
   }
   tc::fence_before();
   __syncthreads();
@@ -310,7 +354,7 @@ cudaError_t launch_fwd_scan_tc(const FwdScanParams &p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const long long ctas = units * (p.hT_ident ? 2 : 1);
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kda_fwd_scan_tc_kernel<<<(unsigned)ctas, 256, TcScanSmem::BYTES, s>>>(p);
+  kda_fwd_scan_tc_kernel<<<(unsigned)ctas, FS_THREADS, TcScanSmem::BYTES, s>>>(p);
   return cudaGetLastError();
 }
 

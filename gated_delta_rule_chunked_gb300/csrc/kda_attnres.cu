@@ -59,7 +59,9 @@ template <> struct Vec<float> {
   }
 };
 
-// Sum `n` per-thread values over the CTA (fixed order); results in out[0..n) for every thread.
+// Sum `n` per-thread values over the CTA (fixed order); results in out[0..n), written by threads
+// 0..n-1. There is no barrier after those writes: both callers follow with a cluster barrier
+// (release/acquire over every thread of the cluster), which orders them for every reader.
 // Inside a warp the values are padded to NP (a power of two) and reduced by recursive halving:
 // at each of the first log2(NP) steps a lane sends half of its values to its partner and keeps
 // the other half, so after them lane l holds the warp's partial of value idx(l) (one shuffle
@@ -96,7 +98,6 @@ __device__ __forceinline__ void block_sum(float (&v)[NMAX], int n, float *red, f
     for (int w = 0; w < nw; ++w) s += red[w * NMAX + threadIdx.x];
     out[threadIdx.x] = s;
   }
-  __syncthreads();
 }
 }  // namespace
 
